@@ -1,0 +1,125 @@
+"""Oracle policy loss and its gradient w.r.t. the logits (float64).
+
+Test infrastructure only; see ``oracle/__init__.py``.
+
+Sources, cited by page title and section:
+
+* "Sizing mini-batches and micro-batches" (cosmos posttrain batching how-to):
+  - *The problem*: the cost is the log-softmax over the vocabulary for every completion token.
+  - *The hard part: deferred normalization*: the loss is a token mean -- the per-token loss
+    summed over the whole optimizer step, divided once by N, the number of valid (masked-in)
+    completion positions; ``max(N, 1)`` guards an all-empty step; gradients are linear, so
+    the chunk sums over N equal the gradient of the un-chunked step.
+  - *pi_old must be frozen across the window*: the ratio is taken against pi_old, the clip
+    uses an epsilon, with pi_old = the current policy the ratio is exp(0) = 1.
+  - *Metric roll-up*: counts are summed; the loss is token-weighted.
+* "03 Data Protocol and Batch Lifecycle" (verl source reading), *response mask semantics*:
+  the policy loss accumulates only over response_mask = 1 tokens, and the advantage is
+  broadcast to tokens and multiplied by the mask.
+* "22-mini-batch-micro-batch-dynamic-batch-size的区别" (verl batching article), section 5:
+  token-mean normalisation by the step's global token count.
+
+The pages never print the surrogate. Reading (standard PPO clip, symmetric epsilon), for a
+token with logits z, target y, pi_old log-prob ``old``, advantage A and mask m:
+
+    LSE  = max(z) + log(sum(exp(z - max(z))))
+    logp = z[y] - LSE
+    r    = exp(logp - old)                       (r = 1 when there is no pi_old)
+    l    = -min(r*A, clip(r, 1-eps, 1+eps)*A)
+    loss_t = m * l
+    g    = 0 if (A > 0 and r > 1+eps) or (A < 0 and r < 1-eps) else 1
+    dloss_t/dz = m * A * r * g * (softmax(z) - onehot(y))
+
+and the step loss is sum(loss_t) / max(N, 1), with dlogits scaled by the same 1/max(N, 1)
+(``scale``). Masked tokens are not policy actions: their loss, log-prob output and dlogits
+are 0 and their logits are never read.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bfloat16 bit patterns (uint16) to float64."""
+    u32 = bits.astype(np.uint32) << np.uint32(16)
+    return u32.view(np.float32).astype(np.float64)
+
+
+def as_f64(logits: np.ndarray) -> np.ndarray:
+    """Logits given as float32/float64 values or as bfloat16 bit patterns (uint16)."""
+    if logits.dtype == np.uint16:
+        return bf16_bits_to_f64(logits)
+    return logits.astype(np.float64)
+
+
+def log_softmax_row(z: np.ndarray) -> np.ndarray:
+    m = np.max(z)
+    lse = m + math.log(float(np.sum(np.exp(z - m))))
+    return z - lse
+
+
+def token_objective(z, y, old, adv, mask, eps, scale=1.0, want_grad=True):
+    """One token row. Returns (loss_t, logp, r, clipped, dz or None)."""
+    V = z.shape[0]
+    if not mask:
+        return 0.0, 0.0, 1.0, False, (np.zeros(V) if want_grad else None)
+    z = np.asarray(z, dtype=np.float64)
+    lsm = log_softmax_row(z)
+    logp = float(lsm[y])
+    r = 1.0 if old is None else math.exp(logp - float(old))
+    A = float(adv)
+    eps = float(eps)
+    lo, hi = 1.0 - eps, 1.0 + eps
+    rc = min(max(r, lo), hi)
+    loss_t = -min(r * A, rc * A)
+    clipped = (A > 0 and r > hi) or (A < 0 and r < lo)
+    g = 0.0 if clipped else 1.0
+    dz = None
+    if want_grad:
+        coef = A * r * g * float(scale)
+        dz = coef * np.exp(lsm)
+        dz[y] -= coef
+    return loss_t, logp, r, clipped, dz
+
+
+def loss_fwd_bwd(logits, target, old_logp, adv_tok, mask, eps, scale=1.0, want_grad=True):
+    """All token rows of ``logits`` ([T, V], float or bf16 bits).
+
+    Returns dict with float64 ``loss_tok``, ``logp_tok``, ``ratio``, bool ``clipped`` and,
+    if ``want_grad``, float64 ``dlogits`` [T, V].
+    """
+    T = logits.shape[0]
+    V = logits.shape[1] if logits.ndim == 2 else 0
+    out = {
+        "loss_tok": np.zeros(T), "logp_tok": np.zeros(T), "ratio": np.ones(T),
+        "clipped": np.zeros(T, dtype=bool),
+    }
+    if want_grad:
+        out["dlogits"] = np.zeros((T, V))
+    for t in range(T):
+        old = None if old_logp is None else old_logp[t]
+        z = as_f64(logits[t]) if mask[t] else np.zeros(V)
+        lt, lp, r, cl, dz = token_objective(z, int(target[t]), old, adv_tok[t], int(mask[t]),
+                                            eps, scale, want_grad)
+        out["loss_tok"][t] = lt
+        out["logp_tok"][t] = lp
+        out["ratio"][t] = r
+        out["clipped"][t] = cl
+        if want_grad:
+            out["dlogits"][t] = dz
+    return out
+
+
+def finish_step(loss_tok, mask, clipped=None):
+    """Step metrics: loss = sum(loss_t) / max(N, 1), N = sum(mask); counts are sums."""
+    mask = np.asarray(mask)
+    n_valid = int(np.sum(mask != 0))
+    loss_sum = math.fsum(float(x) for x in np.asarray(loss_tok, dtype=np.float64))
+    res = {"loss_sum": loss_sum, "loss": loss_sum / max(n_valid, 1), "n_valid": n_valid}
+    if clipped is not None:
+        n_clip = int(np.sum(np.asarray(clipped) & (mask != 0)))
+        res["n_clipped"] = n_clip
+        res["clipfrac"] = n_clip / max(n_valid, 1)
+    return res
