@@ -1,0 +1,250 @@
+/*
+ * grpo.h -- C ABI of the GB300 (sm_103a) GRPO/PPO policy-loss hot path.
+ *
+ * One collected batch of rollouts is consumed as n_mini optimizer steps of n_micro
+ * forward/backward chunks each, and every step's token-mean loss is divided once by N, the
+ * number of valid (response_mask = 1) completion tokens of the whole step
+ * ("Sizing mini-batches and micro-batches", sections "The core idea" and
+ * "The hard part: deferred normalization").
+ *
+ * Typical step, all on one CUDA stream:
+ *   grpo_plan_microbatches     host: which rows form which chunk and optimizer step, N per step
+ *   grpo_group_advantage       device: group-normalised advantage per rollout, broadcast to tokens
+ *   grpo_logprob_loss_fwd_bwd  device: per chunk, log-softmax + clipped surrogate + dlogits
+ *   grpo_finish_step           device: the step's loss sum / max(N,1), metrics, deferred scaling
+ *
+ * Conventions shared by every entry point:
+ *   - Status: every function returns int: GRPO_OK (0), a positive step status, or a negative
+ *     GRPO_ERR_* code. No function aborts or prints.
+ *   - Ownership: every buffer belongs to the caller. The library allocates no device memory
+ *     and never frees caller memory. "device" pointers are CUDA device memory of the current
+ *     device; "host" pointers are ordinary host memory.
+ *   - Asynchrony: device work is enqueued on `stream` (cudaStream_t passed as void*; NULL is
+ *     the legacy default stream). Only grpo_finish_step with a non-NULL host result waits.
+ *   - Determinism: results depend only on the inputs, never on the chunking, the launch
+ *     shape or the scheduling (no order-dependent floating-point atomics).
+ */
+#ifndef GRPO_H_
+#define GRPO_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define GRPO_API __attribute__((visibility("default")))
+#else
+#define GRPO_API
+#endif
+
+/* ---- status codes ---------------------------------------------------------------------- */
+#define GRPO_OK                      0
+#define GRPO_STEP_SKIPPED_NONFINITE  1   /* a valid token's log-prob or loss was not finite */
+#define GRPO_ERR_INVALID            (-1) /* NULL pointer where one is required, bad size */
+#define GRPO_ERR_DIVISIBILITY       (-2) /* batch % group_size, batch % mini, mini % micro */
+#define GRPO_ERR_ROLLOUT_COUNT      (-3) /* the step does not hold exactly `batch` rollouts */
+#define GRPO_ERR_TOKEN_BUDGET       (-4) /* a row is longer than max_token_len */
+#define GRPO_ERR_INCOMPATIBLE       (-5) /* compaction with dynamic bins, packing, ... */
+#define GRPO_ERR_CAPACITY           (-6) /* output arrays too small; sizes written back */
+#define GRPO_ERR_CUDA               (-7) /* a CUDA runtime call failed */
+#define GRPO_ERR_N_MISMATCH         (-8) /* counted N differs from the planner's N */
+#define GRPO_ERR_KERNEL             (-9) /* a bounded wait inside a kernel gave up */
+#define GRPO_ERR_UNSUPPORTED       (-10) /* dtype or device the library was not built for */
+
+#define GRPO_DTYPE_F32   0
+#define GRPO_DTYPE_BF16  1
+
+#define GRPO_WORKLOAD_TOKENS     0  /* bin workload w = L       */
+#define GRPO_WORKLOAD_ATTENTION  1  /* bin workload w = L * L   */
+
+/* ---- planner ----------------------------------------------------------------------------- */
+
+/* Planner configuration. Field meanings follow
+ *  - "Sizing mini-batches and micro-batches", "The config surface": batch (trajectories per
+ *    replica, a positive multiple of group_size), mini (per optimizer step, 0 = whole batch),
+ *    micro (per forward/backward, 0 = one chunk); exact divisibility at every level;
+ *  - "22-mini-batch-micro-batch-dynamic-batch-size的区别", section 3: dynamic token-budget bins
+ *    (max_token_len, workload estimate, bins synced to a minimum count / rounded to a
+ *    multiple, small bins at both ends);
+ *  - "How a context-compaction step fits a variable number of rows into one batch":
+ *    compaction pads each group to a multiple of Q = n_gpus * lcm(micro, logprob_batch) and
+ *    rejects sequence packing, dynamic batching and the interleaved pipeline. */
+typedef struct grpo_plan_cfg {
+  int32_t batch;                 /* rollouts per replica per loop step (> 0) */
+  int32_t mini;                  /* rollouts per optimizer step; 0 = batch */
+  int32_t micro;                 /* rollouts (compaction: rows) per chunk; 0 = mini */
+  int32_t group_size;            /* rollouts per prompt group (> 0) */
+  int32_t dynamic;               /* 1 = token-budget bins inside each mini-batch */
+  int32_t workload;              /* GRPO_WORKLOAD_* */
+  int64_t max_token_len;         /* dynamic: token budget per bin (> 0) */
+  int32_t min_bins;              /* dynamic: lower bound on bins per mini-batch */
+  int32_t bin_multiple;          /* dynamic: bins per mini-batch rounded up to this (>= 1) */
+  int32_t balance_ends;          /* dynamic: 1 = smallest bins at both ends */
+  int32_t compaction;            /* 1 = context compaction */
+  int32_t n_gpus;                /* compaction: GPUs the group is split across */
+  int32_t logprob_batch;         /* compaction: log-prob micro batch */
+  int32_t sequence_packing;      /* only checked against compaction */
+  int32_t interleaved_pipeline;  /* only checked against compaction */
+  int32_t use_rollout_logprobs;  /* 1 = rollout log-probs serve as pi_old */
+} grpo_plan_cfg;
+
+/* Plan of one collected batch. "Exec rows" are the rows in execution order (compaction adds
+ * padding rows). Arrays are caller-owned HOST memory sized by the cap_* fields; on
+ * GRPO_ERR_CAPACITY the scalar fields hold the required sizes and no array is written. */
+typedef struct grpo_plan {
+  int32_t cap_rows, cap_chunks, cap_steps;       /* in: capacities of the arrays below */
+  int32_t n_rows;                /* out: exec rows */
+  int32_t n_chunks;              /* out: forward/backward calls */
+  int32_t n_steps;               /* out: optimizer steps (n_mini) */
+  int32_t n_micro;               /* out: chunks per step if constant, else 0 (dynamic) */
+  int32_t q;                     /* out: compaction multiple Q, else 0 */
+  int32_t n_pad_rows;            /* out: padding rows (compaction) */
+  int32_t needs_old_logp_cache;  /* out: n_steps > 1 and !use_rollout_logprobs */
+  int32_t* row_src;              /* [cap_rows] input row feeding each exec row */
+  int32_t* row_pad;              /* [cap_rows] 1 = padding row (mask 0, reward 0) */
+  int32_t* row_gpu;              /* [cap_rows] GPU slot (compaction), else 0 */
+  int32_t* row_rollout;          /* [cap_rows] rollout of the exec row, -1 for padding */
+  int32_t* inv_perm;             /* [n_rows_in] exec position of each input row, or NULL */
+  int32_t* chunk_row_off;        /* [cap_chunks + 1] exec-row offsets of the chunks */
+  int32_t* step_chunk_off;       /* [cap_steps + 1] chunk offsets of the optimizer steps */
+  int32_t* step_in_row_off;      /* [cap_steps + 1] input-row offsets of the steps */
+  int64_t* chunk_tokens;         /* [cap_chunks] logits rows per chunk */
+  int64_t* step_valid_tokens;    /* [cap_steps] N of each step */
+  int32_t* step_valid_rows;      /* [cap_steps] rows with >= 1 valid token */
+} grpo_plan;
+
+/* Plan the (mini, micro) loop of one collected batch (host only, integer only).
+ *  row_len[i]   logits rows (tokens) of input row i        host [n_rows_in]
+ *  row_valid[i] mask = 1 positions of input row i          host [n_rows_in], 0 <= valid <= len
+ *  seg_counts   rows produced by each rollout              host [n_rollouts], compaction only
+ * Fixed mode: chunks of `micro` consecutive rows. Dynamic: bins as defined in the design
+ * notes (longest-processing-time greedy under the token budget). Compaction: each group
+ * padded to a multiple of Q with copies of its first real row.
+ * Errors: GRPO_ERR_INVALID, _DIVISIBILITY, _ROLLOUT_COUNT, _TOKEN_BUDGET, _INCOMPATIBLE,
+ * _CAPACITY. */
+GRPO_API int grpo_plan_microbatches(const grpo_plan_cfg* cfg, int32_t n_rollouts,
+                                    int32_t n_rows_in, const int32_t* row_len,
+                                    const int32_t* row_valid, const int32_t* seg_counts,
+                                    grpo_plan* out);
+
+/* Expand a plan to one index per exec token (host only). For exec token t (exec rows in plan
+ * order, tokens of a row consecutive) tok_src[t] is the input-order token it reads, or
+ * -1 - that index for a padding row (masked: its logits row is still present, its loss is
+ * 0). row_tok_off is the host [n_rows_in + 1] prefix sum of row_len. cap = length of
+ * tok_src; the exec token count is written to *n_out (GRPO_ERR_CAPACITY if cap is short). */
+GRPO_API int grpo_plan_token_index(const grpo_plan* plan, int32_t n_rows_in,
+                                   const int64_t* row_tok_off, int64_t* tok_src, int64_t cap,
+                                   int64_t* n_out);
+
+/* ---- advantage --------------------------------------------------------------------------- */
+
+/* Group-normalised advantage ("03 Data Protocol and Batch Lifecycle", response mask
+ * semantics and reward/log-prob/advantage; "How a context-compaction step ...", why the row
+ * count does not change the math, item 2). The pages print no formula; reading:
+ *   A_r = (R_r - mean_g) / (std_g + eps), float64 inside, float32 out,
+ * std unbiased (n-1) when unbiased_std != 0, groups = consecutive runs of group_size
+ * rollouts, a single-rollout group (unbiased) or equal rewards give 0.
+ *  rewards     device float [n_rollouts]
+ *  adv_out     device float [n_rollouts]
+ * Optional token broadcast (skipped when adv_tok is NULL):
+ *  row_rollout device int32 [n_rows] rollout of each input row (-1 = padding -> 0), or NULL
+ *              for row i = rollout i
+ *  row_tok_off device int64 [n_rows + 1] token offsets of the rows
+ *  adv_tok     device float [row_tok_off[n_rows]] */
+GRPO_API int grpo_group_advantage(const float* rewards, int32_t n_rollouts, int32_t group_size,
+                                  float eps, int32_t unbiased_std, float* adv_out,
+                                  const int32_t* row_rollout, const int64_t* row_tok_off,
+                                  int32_t n_rows, float* adv_tok, void* stream);
+
+/* ---- loss forward + backward ------------------------------------------------------------- */
+
+/* Device-resident step accumulator (caller-allocated, 128 bytes, zeroed once before the first
+ * chunk). Loss calls add integer counts to it (order-independent); grpo_finish_step reads
+ * them, writes `result`, and zeroes the counters for the next step. */
+typedef struct grpo_step_result {
+  double  loss;        /* loss_sum / max(N, 1) */
+  double  loss_sum;    /* sum of loss_tok over the step, float64, fixed order */
+  double  clipfrac;    /* n_clipped / max(N, 1) */
+  int64_t n_valid;     /* N: mask = 1 tokens seen by the step's loss calls */
+  int64_t n_clipped;   /* valid tokens whose clip bound (gradient 0) */
+  int64_t n_nonfinite; /* valid tokens with a non-finite log-prob or loss */
+  int64_t n_tokens;    /* logits rows processed */
+  int32_t status;      /* GRPO_OK, GRPO_STEP_SKIPPED_NONFINITE, GRPO_ERR_N_MISMATCH, _KERNEL */
+  int32_t kernel_flags;/* internal error bits (0 when healthy) */
+} grpo_step_result;
+
+typedef struct grpo_step_acc {
+  uint64_t n_valid, n_clipped, n_nonfinite, n_tokens;
+  uint32_t flags, reserved0;
+  uint64_t reserved[3];
+  grpo_step_result result;
+} grpo_step_acc;
+
+/* One chunk of the step: per token row t of `logits`
+ * ("Sizing mini-batches and micro-batches", "The problem", "The hard part: deferred
+ * normalization", "pi_old must be frozen across the window"; clip reading as in the
+ * design notes):
+ *   LSE = log sum_v exp(z_v); logp = z_y - LSE; r = exp(logp - old) (1 if old_logp NULL)
+ *   loss_t = m * -min(r*A, clip(r, 1-eps, 1+eps)*A)
+ *   dlogits_t = grad_scale * m * A * r * g * (softmax(z) - onehot(y)),
+ *   g = 0 iff (A > 0 and r > 1+eps) or (A < 0 and r < 1-eps).
+ * grad_scale is 1/max(N,1) with N from the planner (then chunked == un-chunked bit for bit),
+ * or 1 with grpo_finish_step(deferred = 1) applying 1/max(N,1) once.
+ *  logits    device [T, ld] GRPO_DTYPE_F32 or _BF16, row-major, V <= ld
+ *  tok_src   device int64 [T] or NULL: side-input/output index of logits row t; negative
+ *            (-1 - i) marks a padding row (mask 0). NULL means row t <-> index t.
+ *  target    device int32, old_logp device float (or NULL), adv_tok device float,
+ *  mask      device uint8: all indexed through tok_src
+ *  dlogits   device [T, ld_out], same dtype as logits, or NULL (forward only: the pi_old
+ *            ahead pass); masked rows are written as zeros
+ *  loss_tok, logp_tok  device float, indexed through tok_src (logp_tok may be NULL); masked
+ *            tokens get 0 in both
+ *  acc       device grpo_step_acc
+ * A target outside [0, V) makes that token's log-prob NaN (counted as non-finite).
+ * Errors: GRPO_ERR_INVALID (NULL required pointer, T < 0, V < 1, ld < V),
+ * GRPO_ERR_UNSUPPORTED (dtype), GRPO_ERR_CUDA (launch failure). */
+GRPO_API int grpo_logprob_loss_fwd_bwd(const void* logits, int32_t dtype, int64_t T, int64_t V,
+                                       int64_t ld, const int64_t* tok_src,
+                                       const int32_t* target, const float* old_logp,
+                                       const float* adv_tok, const uint8_t* mask,
+                                       float clip_eps, float grad_scale, void* dlogits,
+                                       int64_t ld_out, float* loss_tok, float* logp_tok,
+                                       grpo_step_acc* acc, void* stream);
+
+/* ---- step finish ------------------------------------------------------------------------- */
+
+/* Close one optimizer step ("Sizing mini-batches and micro-batches", "The hard part:
+ * deferred normalization", "Metric roll-up", "The poisoned-window countdown"):
+ *   loss = sum(loss_tok[0..n_tok)) / max(N, 1) in float64 in a fixed order, N = counted
+ *   valid tokens; counts are sums; if any valid token was non-finite the step is skipped:
+ *   status GRPO_STEP_SKIPPED_NONFINITE and the registered gradient buffers are zeroed;
+ *   otherwise, when deferred != 0, each buffer is scaled once by 1/max(N, 1) (scale, then
+ *   the caller clips, then steps). expected_N >= 0 is checked against N
+ *   (GRPO_ERR_N_MISMATCH in result.status).
+ *  loss_tok    device float [n_tok]: the step's per-token losses (input order)
+ *  grad_bufs   host array of n_bufs device pointers; grad_numels host int64 [n_bufs];
+ *              grad_dtypes host int32 [n_bufs] (GRPO_DTYPE_*); may be NULL when n_bufs = 0
+ *  result_host host grpo_step_result or NULL. If non-NULL the call copies acc->result to it,
+ *              synchronises `stream` and returns result.status; if NULL it returns after
+ *              enqueueing and the result stays in acc->result on the device.
+ * Errors: GRPO_ERR_INVALID, GRPO_ERR_UNSUPPORTED, GRPO_ERR_CUDA. */
+GRPO_API int grpo_finish_step(grpo_step_acc* acc, const float* loss_tok, int64_t n_tok,
+                              int64_t expected_N, int32_t deferred, void* const* grad_bufs,
+                              const int64_t* grad_numels, const int32_t* grad_dtypes,
+                              int32_t n_bufs, grpo_step_result* result_host, void* stream);
+
+/* ---- misc -------------------------------------------------------------------------------- */
+
+/* Static string naming a status code. */
+GRPO_API const char* grpo_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+GRPO_API int grpo_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GRPO_H_ */

@@ -1,0 +1,290 @@
+"""ctypes binding of ``libgrpo.so`` (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does nothing but turn
+Python/torch arguments into pointers and sizes, call the library, and turn a negative status
+into ``GrpoError``. All computation happens in the library. If the library has not been
+built, every call raises instead of falling back to anything.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgrpo.so")
+
+OK = 0
+STEP_SKIPPED_NONFINITE = 1
+ERR_INVALID = -1
+ERR_DIVISIBILITY = -2
+ERR_ROLLOUT_COUNT = -3
+ERR_TOKEN_BUDGET = -4
+ERR_INCOMPATIBLE = -5
+ERR_CAPACITY = -6
+ERR_CUDA = -7
+ERR_N_MISMATCH = -8
+ERR_KERNEL = -9
+ERR_UNSUPPORTED = -10
+DTYPE_F32 = 0
+DTYPE_BF16 = 1
+ACC_BYTES = 128
+
+_i32p = C.POINTER(C.c_int32)
+_i64p = C.POINTER(C.c_int64)
+
+
+class GrpoError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        msg = _lib().grpo_status_string(code).decode() if _LIB is not None else str(code)
+        super().__init__(f"{where}: {msg} (status {code})")
+        self.code = code
+
+
+class grpo_plan_cfg(C.Structure):
+    _fields_ = [("batch", C.c_int32), ("mini", C.c_int32), ("micro", C.c_int32),
+                ("group_size", C.c_int32), ("dynamic", C.c_int32), ("workload", C.c_int32),
+                ("max_token_len", C.c_int64), ("min_bins", C.c_int32), ("bin_multiple", C.c_int32),
+                ("balance_ends", C.c_int32), ("compaction", C.c_int32), ("n_gpus", C.c_int32),
+                ("logprob_batch", C.c_int32), ("sequence_packing", C.c_int32),
+                ("interleaved_pipeline", C.c_int32), ("use_rollout_logprobs", C.c_int32)]
+
+
+class grpo_plan(C.Structure):
+    _fields_ = [("cap_rows", C.c_int32), ("cap_chunks", C.c_int32), ("cap_steps", C.c_int32),
+                ("n_rows", C.c_int32), ("n_chunks", C.c_int32), ("n_steps", C.c_int32),
+                ("n_micro", C.c_int32), ("q", C.c_int32), ("n_pad_rows", C.c_int32),
+                ("needs_old_logp_cache", C.c_int32),
+                ("row_src", _i32p), ("row_pad", _i32p), ("row_gpu", _i32p), ("row_rollout", _i32p),
+                ("inv_perm", _i32p), ("chunk_row_off", _i32p), ("step_chunk_off", _i32p),
+                ("step_in_row_off", _i32p), ("chunk_tokens", _i64p), ("step_valid_tokens", _i64p),
+                ("step_valid_rows", _i32p)]
+
+
+class grpo_step_result(C.Structure):
+    _fields_ = [("loss", C.c_double), ("loss_sum", C.c_double), ("clipfrac", C.c_double),
+                ("n_valid", C.c_int64), ("n_clipped", C.c_int64), ("n_nonfinite", C.c_int64),
+                ("n_tokens", C.c_int64), ("status", C.c_int32), ("kernel_flags", C.c_int32)]
+
+    def as_dict(self) -> dict:
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+_PLAN_CFG_FIELDS = [f for f, _ in grpo_plan_cfg._fields_]
+_LIB: Optional[C.CDLL] = None
+
+
+def _lib() -> C.CDLL:
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built; run `python -m rl_post_token_gb300.build` "
+                           "(the library has no fallback path)")
+    lib = C.CDLL(LIB_PATH)
+    vp = C.c_void_p
+    lib.grpo_plan_microbatches.argtypes = [C.POINTER(grpo_plan_cfg), C.c_int32, C.c_int32, _i32p,
+                                           _i32p, _i32p, C.POINTER(grpo_plan)]
+    lib.grpo_plan_token_index.argtypes = [C.POINTER(grpo_plan), C.c_int32, _i64p, _i64p, C.c_int64,
+                                          _i64p]
+    lib.grpo_group_advantage.argtypes = [vp, C.c_int32, C.c_int32, C.c_float, C.c_int32, vp, vp, vp,
+                                         C.c_int32, vp, vp]
+    lib.grpo_logprob_loss_fwd_bwd.argtypes = [vp, C.c_int32, C.c_int64, C.c_int64, C.c_int64, vp, vp,
+                                              vp, vp, vp, C.c_float, C.c_float, vp, C.c_int64, vp, vp,
+                                              vp, vp]
+    lib.grpo_finish_step.argtypes = [vp, vp, C.c_int64, C.c_int64, C.c_int32, C.POINTER(vp), _i64p,
+                                     _i32p, C.c_int32, C.POINTER(grpo_step_result), vp]
+    lib.grpo_status_string.argtypes = [C.c_int]
+    lib.grpo_status_string.restype = C.c_char_p
+    lib.grpo_version.argtypes = []
+    for f in ("grpo_plan_microbatches", "grpo_plan_token_index", "grpo_group_advantage",
+              "grpo_logprob_loss_fwd_bwd", "grpo_finish_step", "grpo_version"):
+        getattr(lib, f).restype = C.c_int
+    _LIB = lib
+    return lib
+
+
+def lib() -> C.CDLL:
+    """The loaded library (raises if it is not built)."""
+    return _lib()
+
+
+def _ptr(t) -> Optional[int]:
+    """Device/host address of a torch tensor (None -> NULL)."""
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _np_i32(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def _p32(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(_i32p)
+
+
+# ---- planner (host) ------------------------------------------------------------------------
+
+def grpo_plan_microbatches(cfg: dict, row_len, row_valid, seg_counts=None,
+                           n_rollouts: Optional[int] = None) -> dict:
+    """Plan one collected batch; returns the plan as a dict of scalars and numpy arrays."""
+    L = _lib()
+    c = grpo_plan_cfg()
+    for k, v in cfg.items():
+        if k not in _PLAN_CFG_FIELDS:
+            raise KeyError(f"unknown planner field {k}")
+        setattr(c, k, int(v))
+    if "bin_multiple" not in cfg:
+        c.bin_multiple = 1
+    if "n_gpus" not in cfg:
+        c.n_gpus = 1
+    if "logprob_batch" not in cfg:
+        c.logprob_batch = 1
+    rl = _np_i32(row_len)
+    rv = _np_i32(row_valid)
+    sc = None if seg_counts is None else _np_i32(seg_counts)
+    n_in = rl.shape[0]
+    if n_rollouts is None:
+        n_rollouts = sc.shape[0] if sc is not None else n_in
+    p = grpo_plan()
+    rc = L.grpo_plan_microbatches(C.byref(c), n_rollouts, n_in, _p32(rl), _p32(rv), _p32(sc), C.byref(p))
+    if rc not in (OK, ERR_CAPACITY):
+        raise GrpoError(rc, "grpo_plan_microbatches")
+    nr, nc, ns = max(p.n_rows, 1), max(p.n_chunks, 1), max(p.n_steps, 1)
+    arr = {
+        "row_src": np.zeros(nr, np.int32), "row_pad": np.zeros(nr, np.int32),
+        "row_gpu": np.zeros(nr, np.int32), "row_rollout": np.zeros(nr, np.int32),
+        "inv_perm": np.zeros(max(n_in, 1), np.int32), "chunk_row_off": np.zeros(nc + 1, np.int32),
+        "step_chunk_off": np.zeros(ns + 1, np.int32), "step_in_row_off": np.zeros(ns + 1, np.int32),
+        "chunk_tokens": np.zeros(nc, np.int64), "step_valid_tokens": np.zeros(ns, np.int64),
+        "step_valid_rows": np.zeros(ns, np.int32),
+    }
+    p = grpo_plan()
+    p.cap_rows, p.cap_chunks, p.cap_steps = nr, nc, ns
+    for k, a in arr.items():
+        setattr(p, k, a.ctypes.data_as(_i64p if a.dtype == np.int64 else _i32p))
+    rc = L.grpo_plan_microbatches(C.byref(c), n_rollouts, n_in, _p32(rl), _p32(rv), _p32(sc), C.byref(p))
+    if rc != OK:
+        raise GrpoError(rc, "grpo_plan_microbatches")
+    out = {k: getattr(p, k) for k in ("n_rows", "n_chunks", "n_steps", "n_micro", "q", "n_pad_rows",
+                                      "needs_old_logp_cache")}
+    lens = {"row_src": p.n_rows, "row_pad": p.n_rows, "row_gpu": p.n_rows, "row_rollout": p.n_rows,
+            "inv_perm": n_in, "chunk_row_off": p.n_chunks + 1, "step_chunk_off": p.n_steps + 1,
+            "step_in_row_off": p.n_steps + 1, "chunk_tokens": p.n_chunks,
+            "step_valid_tokens": p.n_steps, "step_valid_rows": p.n_steps}
+    for k, a in arr.items():
+        out[k] = a[:lens[k]].copy()
+    return out
+
+
+def grpo_plan_token_index(plan: dict, row_len) -> np.ndarray:
+    """Exec-order token -> input-order token index (negative -1-i for padding rows)."""
+    L = _lib()
+    rl = np.asarray(row_len, np.int64)
+    off = np.zeros(rl.shape[0] + 1, np.int64)
+    np.cumsum(rl, out=off[1:])
+    p = grpo_plan()
+    p.n_rows = int(plan["n_rows"])
+    rs = _np_i32(plan["row_src"])
+    rp = _np_i32(plan["row_pad"])
+    p.row_src, p.row_pad = _p32(rs), _p32(rp)
+    n = C.c_int64(0)
+    rc = L.grpo_plan_token_index(C.byref(p), rl.shape[0], off.ctypes.data_as(_i64p), None, 0, C.byref(n))
+    if rc not in (OK, ERR_CAPACITY):
+        raise GrpoError(rc, "grpo_plan_token_index")
+    out = np.zeros(max(n.value, 1), np.int64)
+    rc = L.grpo_plan_token_index(C.byref(p), rl.shape[0], off.ctypes.data_as(_i64p),
+                                 out.ctypes.data_as(_i64p), out.shape[0], C.byref(n))
+    if rc != OK:
+        raise GrpoError(rc, "grpo_plan_token_index")
+    return out[:n.value]
+
+
+# ---- device entry points ---------------------------------------------------------------------
+
+def grpo_group_advantage(rewards, group_size: int, eps: float, unbiased_std: bool, adv_out,
+                         row_rollout=None, row_tok_off=None, adv_tok=None, stream=None) -> None:
+    """rewards/adv_out float32 device tensors; optional token broadcast into adv_tok."""
+    n_rows = 0 if row_tok_off is None else row_tok_off.numel() - 1
+    rc = _lib().grpo_group_advantage(_ptr(rewards), rewards.numel(), int(group_size), float(eps),
+                                     int(bool(unbiased_std)), _ptr(adv_out), _ptr(row_rollout),
+                                     _ptr(row_tok_off), n_rows, _ptr(adv_tok), _stream(stream))
+    if rc != OK:
+        raise GrpoError(rc, "grpo_group_advantage")
+
+
+def grpo_logprob_loss_fwd_bwd(logits, target, old_logp, adv_tok, mask, clip_eps: float,
+                              grad_scale: float, dlogits, loss_tok, logp_tok, acc, tok_src=None,
+                              V: Optional[int] = None, stream=None) -> None:
+    """logits [T, ld] (float32 or bfloat16) on the device; see grpo.h for the rest."""
+    import torch
+
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be a 2-D tensor with unit inner stride")
+    dt = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16}[logits.dtype]
+    T, ld = logits.shape[0], logits.stride(0) if logits.shape[0] > 1 else logits.shape[1]
+    V = logits.shape[1] if V is None else V
+    ld_out = 0
+    if dlogits is not None:
+        if dlogits.dtype != logits.dtype or dlogits.dim() != 2 or dlogits.stride(1) != 1:
+            raise ValueError("dlogits must match logits' dtype, 2-D, unit inner stride")
+        if dlogits.shape[0] != T:
+            raise ValueError("dlogits must have the same row count as logits")
+        ld_out = dlogits.stride(0) if T > 1 else dlogits.shape[1]
+    rc = _lib().grpo_logprob_loss_fwd_bwd(_ptr(logits), dt, T, V, ld, _ptr(tok_src), _ptr(target),
+                                          _ptr(old_logp), _ptr(adv_tok), _ptr(mask), float(clip_eps),
+                                          float(grad_scale), _ptr(dlogits), ld_out, _ptr(loss_tok),
+                                          _ptr(logp_tok), _ptr(acc), _stream(stream))
+    if rc != OK:
+        raise GrpoError(rc, "grpo_logprob_loss_fwd_bwd")
+
+
+def grpo_finish_step(acc, loss_tok, n_tok: Optional[int] = None, expected_N: int = -1,
+                     deferred: bool = False, grad_bufs: Sequence = (), sync: bool = True,
+                     stream=None):
+    """Close the step. With sync=True returns the result dict (the call waits on the stream);
+    with sync=False returns None and the result stays on the device in acc."""
+    import torch
+
+    n_tok = loss_tok.numel() if n_tok is None else n_tok
+    nb = len(grad_bufs)
+    bufs = (C.c_void_p * max(nb, 1))(*[g.data_ptr() for g in grad_bufs])
+    numels = (C.c_int64 * max(nb, 1))(*[g.numel() for g in grad_bufs])
+    dts = (C.c_int32 * max(nb, 1))(*[{torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16}[g.dtype]
+                                      for g in grad_bufs])
+    res = grpo_step_result()
+    rc = _lib().grpo_finish_step(_ptr(acc), _ptr(loss_tok), int(n_tok), int(expected_N), int(bool(deferred)),
+                                 bufs, numels, dts, nb, C.byref(res) if sync else None, _stream(stream))
+    if rc < 0 and not sync:
+        raise GrpoError(rc, "grpo_finish_step")
+    if rc < 0 and rc not in (ERR_N_MISMATCH, ERR_KERNEL):
+        raise GrpoError(rc, "grpo_finish_step")
+    return res.as_dict() if sync else None
+
+
+def new_step_acc(device="cuda"):
+    """A zeroed device-resident grpo_step_acc (caller-owned, 128 bytes)."""
+    import torch
+    return torch.zeros(ACC_BYTES, dtype=torch.uint8, device=device)
+
+
+def read_step_result(acc) -> dict:
+    """Decode acc->result after an asynchronous grpo_finish_step (copies 64 bytes to host)."""
+    raw = acc[64:128].cpu().numpy().tobytes()
+    return grpo_step_result.from_buffer_copy(raw).as_dict()
+
+
+def grpo_version() -> int:
+    return _lib().grpo_version()

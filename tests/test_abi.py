@@ -1,0 +1,41 @@
+"""The C-ABI library loads without a GPU and exports every entry point the header declares."""
+import ctypes
+import os
+import re
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        names += re.findall(r"GRPO_API\s+[\w\s\*]*?\b(grpo_\w+)\s*\(", text)
+    return names
+
+
+def test_header_declares_entry_points():
+    names = _declared()
+    for n in ("grpo_plan_microbatches", "grpo_group_advantage", "grpo_logprob_loss_fwd_bwd",
+              "grpo_finish_step"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(grpo_lib):
+    missing = [n for n in _declared() if not hasattr(grpo_lib, n)]
+    assert missing == []
+
+
+def test_status_strings_and_version(grpo_lib):
+    grpo_lib.grpo_status_string.restype = ctypes.c_char_p
+    assert grpo_lib.grpo_status_string(0) == b"ok"
+    assert b"N" in grpo_lib.grpo_status_string(-8)
+    assert grpo_lib.grpo_version() >= 100
+
+
+def test_struct_sizes_match_header(grpo_lib):
+    from rl_post_token_gb300 import _lib
+    assert ctypes.sizeof(_lib.grpo_step_result) == 64
+    assert _lib.ACC_BYTES == 128
