@@ -1,0 +1,455 @@
+"""Benchmark: GRPO loss forward+backward, valid tokens/s at V = 151936 bf16, and the fraction of
+the HBM roofline.
+
+A "step" is one whole collected batch through the library: plan -> group advantage -> every
+(mini, micro) chunk's loss forward+backward -> every optimizer step's finish. The default
+workload is the Qwen3-VL-2B-shaped step (8 prompts x 4 rollouts, completion lengths uniform in
+[128, 2048], V = 151936 bf16 logits ~ N(0, 3), mini 16, micro 8), synthetic and seeded; its
+~10.6 GB of logits are larger than L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--workload qwen_step|dynamic|compaction|tiny]
+
+Under torchrun (N > 1) every rank runs its own batch (weak scaling, no collective on the
+data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GRPO loss fwd+bwd valid tokens/s at V=151936 bf16; % of HBM roofline"
+UNIT = "valid tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "rl_post_token_gb300", "csrc", "grpo_rowpass.cu")
+
+WORKLOAD_TEXT = {
+    "qwen_step": "Qwen3-VL-2B-shaped step: 8 prompts x 4 rollouts, completion lengths U[128,2048] "
+                 "packed, V=151936 bf16 logits ~N(0,3), mini 16, micro 8, rewards Bernoulli(0.3), eps 0.2",
+    "dynamic": "dynamic batching: 16 prompts x 8 rollouts, lognormal lengths (median 700, cap 2048), "
+               "V=151936 bf16, token-budget bins of 16384 by attention workload, one optimizer step",
+    "compaction": "context compaction: 3 prompts x 2 generations, segments {1,3},{2,5},{1,1}, 1024-token "
+                  "rows, Q=4 -> 16 rows incl. 3 pad rows, V=151936 bf16, one step",
+    "tiny": "tiny oracle check: 8 prompts x 4 rollouts, 64 positions, V=512 f32, mini 16, micro 8",
+}
+
+
+# ---- distributed helpers (also exercised by the CPU gloo test) ---------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_timing(elapsed_s: float, units: float, world: int, device=None):
+    """(max elapsed over ranks, sum of units over ranks)."""
+    if world <= 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---- peaks, clocks, profiles --------------------------------------------------------------------
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, path: str):
+        self.path = path
+        self.proc = None
+        try:
+            self.f = open(path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(gpu_index)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def profiled_traffic():
+    """Per-valid-token DRAM traffic of the row-pass kernel from the committed ncu summary, or
+    None when the summary is missing or was taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "rowpass_qwen_step_ncu.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m1 = re.search(r"traffic_per_valid_token_bytes:\s*([0-9.eE+]+)", text)
+    m2 = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    if not (m1 and m2):
+        return None
+    cur = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+    return float(m1.group(1)) if cur == m2.group(1) else None
+
+
+# ---- oracle timing (CPU baseline and reference arm) ----------------------------------------------
+
+def oracle_sample_rate(wl, n_tokens: int, budget_s: float):
+    """Time the float64 oracle on the first valid tokens of a host-generated sample of the
+    workload. Returns (valid tokens/s, tokens timed, seconds)."""
+    from oracle import loss as OL
+    from rl_post_token_gb300 import workloads as W
+
+    rows = min(wl.T, n_tokens)
+    rng = np.random.default_rng(wl.seed + 7)
+    x = rng.standard_normal((rows, wl.V), dtype=np.float32) * np.float32(wl.logit_std)
+    logits = W.bf16_round_bits(x) if wl.dtype == "bf16" else x
+    tgt, msk, adv = wl.target[:rows], wl.mask[:rows], np.where(np.arange(rows) % 2, 1.0, -1.0)
+    ref = np.array([OL.log_softmax_row(OL.as_f64(logits[t]))[tgt[t]] for t in range(rows)])
+    old = ref + wl.old_noise[:rows]
+    done, t0 = 0, time.perf_counter()
+    while True:
+        for t in range(rows):
+            OL.token_objective(OL.as_f64(logits[t]), int(tgt[t]), float(old[t]), float(adv[t]),
+                               int(msk[t]), wl.eps, 1.0, True)
+            done += int(msk[t])
+            if time.perf_counter() - t0 > budget_s:
+                break
+        if time.perf_counter() - t0 > budget_s or done == 0:
+            break
+    dt = time.perf_counter() - t0
+    return done / dt, done, dt
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from rl_post_token_gb300 import workloads as W
+    wl = W.make_workload(args.workload, seed=0)
+    per_step_s = 0.5
+    for _ in range(args.warmup):
+        oracle_sample_rate(wl, 16, per_step_s / 4)
+    done, dt = 0, 0.0
+    for _ in range(args.steps):
+        _, n, d = oracle_sample_rate(wl, 16, per_step_s)
+        done += n
+        dt += d
+    v = done / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / max(args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "parallelism": "rank 0 only"},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"float64 numpy oracle, first 16 tokens of a host-drawn batch of the "
+                                   f"workload, {per_step_s}s per step"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- the library arm ------------------------------------------------------------------------------
+
+class Batch:
+    """Device-resident inputs and outputs of one collected batch."""
+
+    def __init__(self, wl, device):
+        import torch
+        from rl_post_token_gb300 import _lib
+        from rl_post_token_gb300 import step as S
+        from rl_post_token_gb300 import workloads as W
+
+        self.wl = wl
+        self.dev = device
+        self.bp = S.plan_batch(wl.plan, wl.row_len, wl.row_valid, wl.seg_counts)
+        Te = self.bp.exec_tokens
+        T = wl.T
+        self.logits = W.make_logits(wl, device, rows=Te)       # exec order, as a model emits
+        self.dlogits = torch.empty_like(self.logits)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        self.target, self.mask, self.rewards = t(wl.target), t(wl.mask), t(wl.rewards)
+        self.row_tok_off = t(wl.tok_off)
+        self.row_rollout = t(wl.row_rollout)
+        self.tok_src = None if self.bp.tok_src is None else t(self.bp.tok_src)
+        self.tok_src_host = None
+        if self.tok_src is not None:  # pinned double buffer for the per-step plan upload
+            self.tok_src_host = [torch.empty(self.tok_src.numel(), dtype=torch.int64, pin_memory=True)
+                                 for _ in range(2)]
+            self.tok_src_free = [None, None]
+        self.adv_rollout = torch.empty_like(self.rewards)
+        self.adv_tok = torch.empty(T, dtype=torch.float32, device=device)
+        self.loss_tok = torch.empty(T, dtype=torch.float32, device=device)
+        self.logp_tok = torch.empty(T, dtype=torch.float32, device=device)
+        self.accs = torch.zeros(self.bp.n_steps * _lib.ACC_BYTES, dtype=torch.uint8, device=device)
+        # pi_old from the ahead pass (forward only, before any pi_old exists), plus seeded noise
+        self.old = None
+        self.run(with_grad=False)
+        self.old = self.logp_tok + t(wl.old_noise)
+        torch.cuda.synchronize(device)
+        self.n_step = 0
+
+    def replan(self, stream):
+        """The host planner runs every step; its token index goes up through pinned memory."""
+        import torch
+        from rl_post_token_gb300 import step as S
+        wl = self.wl
+        self.bp = S.plan_batch(wl.plan, wl.row_len, wl.row_valid, wl.seg_counts)
+        if self.tok_src is not None:
+            k = self.n_step % 2
+            if self.tok_src_free[k] is not None:
+                self.tok_src_free[k].synchronize()
+            self.tok_src_host[k].numpy()[:] = self.bp.tok_src
+            self.tok_src.copy_(self.tok_src_host[k], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            self.tok_src_free[k] = ev
+        self.n_step += 1
+
+    def run(self, with_grad=True, stream=None, chunk_ready=None, launch_events=None):
+        from rl_post_token_gb300 import step as S
+        return S.run_batch(self.bp, logits=self.logits, dlogits=self.dlogits if with_grad else None,
+                           target=self.target, old_logp=self.old, mask=self.mask, adv_tok=self.adv_tok,
+                           loss_tok=self.loss_tok, logp_tok=self.logp_tok, accs=self.accs,
+                           clip_eps=self.wl.eps, rewards=self.rewards, adv_rollout=self.adv_rollout,
+                           group_size=self.wl.group_size, row_tok_off=self.row_tok_off,
+                           row_rollout=self.row_rollout, tok_src=self.tok_src, V=self.wl.V,
+                           stream=stream, chunk_ready=chunk_ready, launch_events=launch_events)
+
+    def algorithmic_bytes(self):
+        """Bytes the method must move per batch in the row pass: a valid token reads its logits
+        row and writes its dlogits row plus its side inputs and outputs (target, pi_old,
+        advantage, mask, loss, log-prob, and the token index when the order is permuted); a
+        masked or padding token writes a zero row."""
+        wl = self.wl
+        rowb = wl.V * wl.elem_bytes
+        idx = 8 if self.tok_src is not None else 0
+        valid = wl.n_valid  # each valid input token runs exactly once; padding rows are masked
+        masked = self.bp.exec_tokens - valid
+        return valid * (2 * rowb + 4 + 4 + 4 + 1 + 4 + 4 + idx) + masked * (rowb + 1 + idx)
+
+
+def run_gb300(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    from rl_post_token_gb300 import build as B
+    if rank == 0:
+        B.build()
+    barrier(world, device)
+    from rl_post_token_gb300 import _lib
+    from rl_post_token_gb300 import step as S
+    from rl_post_token_gb300 import workloads as W
+
+    _lib.lib()
+    wl = W.make_workload(args.workload, seed=rank)
+    batch = Batch(wl, device)
+    stream = torch.cuda.current_stream(device)
+
+    for _ in range(max(args.warmup, 3)):
+        batch.replan(stream)
+        batch.run(stream=stream)
+    torch.cuda.synchronize(device)
+
+    out_dir = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp"
+    clocks = ClockSampler(_gpu_index(local), os.path.join(out_dir, f"clocks_rank{rank}.csv"))
+    time.sleep(0.5)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    evs = []
+    start.record(stream)
+    for _ in range(args.steps):
+        batch.replan(stream)
+        launches += batch.run(stream=stream, launch_events=evs)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world, device)
+    clk = clocks.stop()
+    elapsed = start.elapsed_time(end) / 1e3
+    results = S.read_results(batch.accs, batch.bp.n_steps)
+
+    # the dominant kernel: row-pass launches timed on their own stream inside the timed region
+    row_s = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+    per_launch_bytes = batch.algorithmic_bytes() / (len(evs) / args.steps)
+    achieved_gbs = per_launch_bytes / (row_s / len(evs)) / 1e9
+
+    units = wl.n_valid * args.steps
+    max_el, all_units = reduce_timing(elapsed, units, world, device)
+    value = all_units / max_el
+
+    e2e = run_e2e(batch, device, stream, steps=min(args.steps, args.e2e_steps))
+
+    peak, peak_kind = hbm_peak()
+    tpv = profiled_traffic()
+    launches_per_step = len(evs) / args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": 1e3 * max_el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "valid_tokens_per_step": wl.n_valid,
+                   "logits_rows_per_step": batch.bp.exec_tokens, "vocab": wl.V,
+                   "l2": "inputs larger than L2 (%.1f GB of logits per step), no flush"
+                         % (batch.bp.exec_tokens * wl.V * wl.elem_bytes / 1e9),
+                   "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": achieved_gbs / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": "row pass (grpo_logprob_loss_fwd_bwd)",
+                     "row_pass_share_of_step": row_s / elapsed,
+                     "traffic": None if tpv is None else tpv * wl.n_valid / launches_per_step},
+        "gpu_launches": launches,
+        "e2e": e2e,
+        "step_results": [{k: r[k] for k in ("loss", "n_valid", "clipfrac", "status")} for r in results],
+    }
+    if clk is not None:
+        line["clocks"] = clk
+    if rank == 0 and not args.no_cpu_baseline:
+        v, n, dt = oracle_sample_rate(wl, 16, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"float64 numpy oracle (one thread) on {n} valid tokens "
+                                          f"({dt:.1f} s) of a host-drawn sample of the workload"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def _gpu_index(local: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    parts = [p for p in vis.split(",") if p.strip()]
+    if parts and all(p.strip().isdigit() for p in parts) and local < len(parts):
+        return int(parts[local])
+    return local
+
+
+def run_e2e(batch, device, stream, steps: int):
+    """Same metric through the public API with HOST inputs: every step copies the logits
+    (pinned host -> device, per chunk on a copy stream, each chunk's row pass waiting only for
+    its own copy) and the side inputs, runs the batch, and reads the step results back."""
+    import torch
+
+    host_logits = torch.empty(batch.logits.shape, dtype=batch.logits.dtype, pin_memory=True)
+    host_logits.copy_(batch.logits)
+    side = {k: getattr(batch, k).cpu().pin_memory() for k in ("target", "mask", "rewards", "old")}
+    host_res = torch.empty(batch.accs.numel(), dtype=torch.uint8, pin_memory=True)
+    copy = torch.cuda.Stream(device)
+    torch.cuda.synchronize(device)
+
+    def one_step():
+        batch.replan(stream)
+        bp = batch.bp
+        with torch.cuda.stream(stream):
+            for k, v in side.items():
+                getattr(batch, k).copy_(v, non_blocking=True)
+        copy.wait_stream(stream)
+        ready = []
+        with torch.cuda.stream(copy):
+            for c in range(bp.plan["n_chunks"]):
+                a, b = int(bp.exec_tok_off[c]), int(bp.exec_tok_off[c + 1])
+                batch.logits[a:b].copy_(host_logits[a:b], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(copy)
+                ready.append(e)
+        batch.run(stream=stream, chunk_ready=ready)
+        with torch.cuda.stream(stream):
+            host_res.copy_(batch.accs, non_blocking=True)
+        stream.synchronize()
+
+    one_step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one_step()
+    dt = time.perf_counter() - t0
+    h2d = host_logits.numel() * host_logits.element_size() + sum(v.numel() * v.element_size() for v in side.values())
+    return {"value": batch.wl.n_valid * steps / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(host_res.numel()), "steps": steps,
+            "how": "pinned host logits copied per chunk on a side stream, overlapped with the row pass; "
+                   "side inputs copied and step results read back every step"}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="qwen_step", choices=list(WORKLOAD_TEXT))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,121 @@
+"""Driver loop of one collected batch over the C-ABI entry points.
+
+Host control flow only ("Sizing mini-batches and micro-batches", "The loop at a glance"):
+plan -> group advantage -> for each optimizer step, for each chunk, the loss forward+backward
+-> the step finish. Every piece of arithmetic runs in ``libgrpo.so``.
+
+Layouts:
+* per-token side inputs (target, mask, pi_old, advantage) and per-token outputs (loss_tok,
+  logp_tok) are in INPUT order (rows in the order collected, tokens of a row consecutive);
+* logits and dlogits are in EXEC order (the plan's rows, which is what a model produces
+  chunk by chunk); ``tok_src`` maps exec tokens to input tokens and is None when the two
+  orders coincide (fixed chunks).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import List, Optional
+
+import numpy as np
+
+from . import _lib
+
+
+@dataclass
+class BatchPlan:
+    plan: dict                      # grpo_plan_microbatches output
+    row_tok_off: np.ndarray         # int64 [rows + 1], input order
+    exec_tok_off: np.ndarray        # int64 [chunks + 1], exec order
+    tok_src: Optional[np.ndarray]   # int64 [exec tokens] or None (identity)
+    step_tok_range: List[tuple]     # input-order token range of each optimizer step
+    step_exec_range: List[tuple]    # exec-order token range of each optimizer step
+
+    @property
+    def n_steps(self) -> int:
+        return int(self.plan["n_steps"])
+
+    @property
+    def exec_tokens(self) -> int:
+        return int(self.exec_tok_off[-1])
+
+
+def plan_batch(cfg: dict, row_len, row_valid, seg_counts=None) -> BatchPlan:
+    p = _lib.grpo_plan_microbatches(cfg, row_len, row_valid, seg_counts)
+    rl = np.asarray(row_len, np.int64)
+    row_tok_off = np.zeros(rl.shape[0] + 1, np.int64)
+    np.cumsum(rl, out=row_tok_off[1:])
+    exec_tok_off = np.zeros(p["n_chunks"] + 1, np.int64)
+    np.cumsum(p["chunk_tokens"], out=exec_tok_off[1:])
+    identity = p["n_rows"] == rl.shape[0] and np.array_equal(p["row_src"], np.arange(rl.shape[0]))
+    tok_src = None if identity else _lib.grpo_plan_token_index(p, rl)
+    steps, execs = [], []
+    for s in range(p["n_steps"]):
+        r0, r1 = p["step_in_row_off"][s], p["step_in_row_off"][s + 1]
+        steps.append((int(row_tok_off[r0]), int(row_tok_off[r1])))
+        c0, c1 = p["step_chunk_off"][s], p["step_chunk_off"][s + 1]
+        execs.append((int(exec_tok_off[c0]), int(exec_tok_off[c1])))
+    return BatchPlan(p, row_tok_off, exec_tok_off, tok_src, steps, execs)
+
+
+def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok, loss_tok,
+              logp_tok, accs, clip_eps: float, rewards=None, adv_rollout=None, group_size: int = 1,
+              adv_eps: float = 1e-6, row_tok_off=None, row_rollout=None, tok_src=None,
+              deferred: bool = False, V: Optional[int] = None, stream=None,
+              chunk_ready=None, launch_events=None) -> int:
+    """Enqueue the whole batch; returns the number of library kernel launches.
+
+    ``accs`` is a uint8 device tensor of n_steps * 128 bytes (one accumulator per optimizer
+    step, results read later with ``read_results``). If ``rewards`` is given the advantage is
+    computed into ``adv_rollout``/``adv_tok`` first. ``chunk_ready[c]`` (optional CUDA event)
+    is waited on before chunk c is launched, e.g. the end of its host-to-device copy;
+    ``launch_events`` (optional list) receives a (start, end) event pair per row-pass launch."""
+    import torch
+
+    st = torch.cuda.current_stream() if stream is None else stream
+    launches = 0
+    if rewards is not None:
+        _lib.grpo_group_advantage(rewards, group_size, adv_eps, True, adv_rollout, row_rollout,
+                                  row_tok_off, adv_tok, stream=st)
+        launches += 2
+    p = bp.plan
+    for s in range(p["n_steps"]):
+        N = int(p["step_valid_tokens"][s])
+        scale = 1.0 if deferred else 1.0 / max(N, 1)
+        acc = accs[s * _lib.ACC_BYTES:(s + 1) * _lib.ACC_BYTES]
+        for c in range(p["step_chunk_off"][s], p["step_chunk_off"][s + 1]):
+            a, b = int(bp.exec_tok_off[c]), int(bp.exec_tok_off[c + 1])
+            if chunk_ready is not None:
+                st.wait_event(chunk_ready[c])
+            if b == a:
+                continue
+            if launch_events is not None:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+            if tok_src is None:
+                # exec order == input order: the chunk's side inputs are the same slice
+                side = (target[a:b], None if old_logp is None else old_logp[a:b], adv_tok[a:b],
+                        mask[a:b], loss_tok[a:b], None if logp_tok is None else logp_tok[a:b], None)
+            else:
+                # side arrays stay whole; the kernel reads them through the token index
+                side = (target, old_logp, adv_tok, mask, loss_tok, logp_tok, tok_src[a:b])
+            tg, od, ad, mk, lt, lp, ts = side
+            _lib.grpo_logprob_loss_fwd_bwd(
+                logits[a:b], tg, od, ad, mk, clip_eps, scale,
+                None if dlogits is None else dlogits[a:b], lt, lp, acc, tok_src=ts, V=V, stream=st)
+            if launch_events is not None:
+                e1 = torch.cuda.Event(enable_timing=True)
+                e1.record(st)
+                launch_events.append((e0, e1))
+            launches += 1
+        t0, t1 = bp.step_tok_range[s]
+        e0, e1 = bp.step_exec_range[s]
+        grads = [] if dlogits is None or e1 == e0 else [dlogits[e0:e1]]
+        _lib.grpo_finish_step(acc, loss_tok[t0:t1], expected_N=N, deferred=deferred,
+                              grad_bufs=grads, sync=False, stream=st)
+        launches += 1 + len(grads)
+    return launches
+
+
+def read_results(accs, n_steps: int) -> List[dict]:
+    raw = accs.view(n_steps, _lib.ACC_BYTES)[:, 64:].cpu().numpy()
+    return [_lib.grpo_step_result.from_buffer_copy(raw[s].tobytes()).as_dict() for s in range(n_steps)]

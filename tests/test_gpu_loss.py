@@ -1,0 +1,264 @@
+"""GPU parity: the library's loss forward/backward, advantage and step finish vs the oracle,
+through the C ABI, on seeded inputs that span several tiles and ragged tails."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import advantage as OA
+from oracle import loss as OL
+from rl_post_token_gb300 import _lib
+from rl_post_token_gb300 import step as S
+from rl_post_token_gb300 import workloads as W
+
+from tests import _gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(grpo_lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return grpo_lib
+
+
+def _run_direct(case, scale=1.0, want_grad=True, tok_src=None, old=True, logits=None):
+    """One library call over all rows of a case."""
+    T = case.logits.shape[0]
+    lg = case.logits if logits is None else logits
+    dl = torch.empty_like(lg) if want_grad else None
+    loss = torch.full((T,), -7.0, device=DEV)
+    logp = torch.full((T,), -7.0, device=DEV)
+    acc = _lib.new_step_acc(DEV)
+    _lib.grpo_logprob_loss_fwd_bwd(lg, case.d_target, case.d_old if old else None, case.d_adv,
+                                   case.d_mask, case.wl.eps, scale, dl, loss, logp, acc,
+                                   tok_src=tok_src)
+    torch.cuda.synchronize()
+    return dl, loss, logp, acc
+
+
+def _check_case(case, scale=1.0, old=True):
+    dl, loss, logp, _ = _run_direct(case, scale, old=old)
+    if not old:
+        case_old, case.old = case.old, None
+    ref = H.oracle_run(case, scale_per_token=np.full(case.logits.shape[0], scale))
+    if not old:
+        case.old = case_old
+    H.assert_tokens_close(H.to_f64(loss), H.to_f64(logp), ref, case.adv_tok, case.mask)
+    amb = H.ambiguous_clip(ref["ratio"], case.wl.eps)
+    alt = None
+    if amb.any():
+        alt = ref["dlogits"].copy()
+        for t in np.nonzero(amb)[0]:
+            z = OL.as_f64(case.logits_host[t])
+            # the other clip decision: gradient on if it was off, off if it was on
+            coef = 0.0 if not ref["clipped"][t] else case.adv_tok[t] * ref["ratio"][t] * scale
+            alt[t] = coef * np.exp(OL.log_softmax_row(z))
+            alt[t, case.target[t]] -= coef
+    H.assert_dlogits_close(H.to_f64(dl), ref["dlogits"], case.wl.dtype, amb, alt,
+                           target=ref["target"], coef=np.maximum(np.abs(ref["coef"]), np.abs(
+                               case.adv_tok * ref["ratio"] * scale) * case.mask))
+    return ref
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_tiny_workload_full(dtype):
+    wl = W.make_workload("tiny", dtype=dtype)
+    case = H.Case(wl)
+    _check_case(case, scale=1.0 / 700)
+
+
+@pytest.mark.parametrize("V", [1, 7, 1000, 4104, 8200, 65537])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ragged_vocab(V, dtype):
+    wl = W.make_workload("qwen_step", rows=4, len_lo=4, len_hi=7, V=V, dtype=dtype, seed=V)
+    _check_case(H.Case(wl), scale=0.25)
+
+
+def test_qwen_vocab_bf16():
+    wl = W.make_workload("qwen_step", rows=4, len_lo=20, len_hi=40, seed=3)
+    _check_case(H.Case(wl), scale=1.0 / 97)
+
+
+def test_qwen_vocab_f32():
+    wl = W.make_workload("qwen_step", rows=4, len_lo=3, len_hi=5, dtype="f32", seed=4)
+    _check_case(H.Case(wl), scale=1.0)
+
+
+def test_no_pi_old_ratio_one():
+    wl = W.make_workload("qwen_step", rows=4, len_lo=8, len_hi=12, V=4104, seed=5)
+    case = H.Case(wl)
+    ref = _check_case(case, scale=0.5, old=False)
+    assert np.all(ref["ratio"] == 1.0)
+
+
+def test_stress_clip_binds():
+    wl = W.make_workload("qwen_step", rows=4, len_lo=30, len_hi=60, V=8200, seed=6, old_sigma=0.5)
+    adv = np.random.default_rng(6).choice([-1.5, -0.5, 0.5, 1.5], wl.T)
+    case = H.Case(wl, adv_override=adv)
+    ref = _check_case(case, scale=0.125)
+    assert ref["clipped"].sum() > 10
+
+
+def test_masked_and_zero_advantage_rows():
+    wl = W.make_workload("tiny", rows=8, positions=40, valid_lo=0, V=2048, dtype="bf16", seed=8)
+    case = H.Case(wl)
+    case.adv_tok[:40] = 0.0  # a zero-variance group: the whole row has A = 0
+    case.d_adv = torch.from_numpy(case.adv_tok).to(DEV)
+    ref = _check_case(case, scale=0.01)
+    dl, loss, logp, _ = _run_direct(case, 0.01)
+    assert torch.all(dl[:40] == 0)
+    assert np.all(ref["loss_tok"][wl.mask == 0] == 0)
+
+
+def test_forward_only_matches_and_writes_no_grad():
+    wl = W.make_workload("qwen_step", rows=4, len_lo=10, len_hi=20, V=8200, seed=9)
+    case = H.Case(wl)
+    _, loss, logp, acc = _run_direct(case, 1.0, want_grad=False)
+    ref = H.oracle_run(case, want_grad=False)
+    H.assert_tokens_close(H.to_f64(loss), H.to_f64(logp), ref, case.adv_tok, case.mask)
+
+
+def test_tok_src_permutation_and_padding_rows():
+    wl = W.make_workload("qwen_step", rows=4, len_lo=4, len_hi=9, V=4104, seed=10)
+    case = H.Case(wl)
+    T = case.logits.shape[0]
+    rng = np.random.default_rng(0)
+    perm = rng.permutation(T)
+    pads = rng.choice(T, 3)
+    tok_src = np.concatenate([perm, -1 - pads]).astype(np.int64)
+    lg = torch.cat([case.logits[torch.from_numpy(perm).to(DEV)], case.logits[torch.from_numpy(pads).to(DEV)]])
+    dl, loss, logp, acc = _run_direct(case, 0.5, tok_src=torch.from_numpy(tok_src).to(DEV), logits=lg)
+    ref = H.oracle_run(case, scale_per_token=np.full(T, 0.5))
+    H.assert_tokens_close(H.to_f64(loss), H.to_f64(logp), ref, case.adv_tok, case.mask)
+    got = H.to_f64(dl)
+    H.assert_dlogits_close(got[:T], ref["dlogits"][perm], "bf16", target=ref["target"][perm],
+                           coef=ref["coef"][perm])
+    assert np.all(got[T:] == 0)
+    res = _lib.grpo_finish_step(acc, loss)
+    assert res["n_tokens"] == T + 3 and res["n_valid"] == int(wl.mask.sum())
+
+
+def test_empty_chunk_and_empty_step():
+    acc = _lib.new_step_acc(DEV)
+    e = torch.empty((0, 64), device=DEV)
+    z = torch.empty(0, device=DEV)
+    _lib.grpo_logprob_loss_fwd_bwd(e, torch.empty(0, dtype=torch.int32, device=DEV), None, z,
+                                   torch.empty(0, dtype=torch.uint8, device=DEV), 0.2, 1.0, None, z, None, acc)
+    res = _lib.grpo_finish_step(acc, z, expected_N=0)
+    assert res["status"] == 0 and res["loss"] == 0.0 and res["n_valid"] == 0
+
+
+def test_advantage_bit_exact_and_broadcast():
+    rng = np.random.default_rng(12)
+    for G, unbiased in [(4, True), (8, True), (2, False), (1, True)]:
+        r = (rng.random(G * 16) < 0.3).astype(np.float32)
+        r[:G] = 1.0  # an all-equal group
+        r[G:2 * G] = rng.normal(size=G).astype(np.float32)
+        d_r = torch.from_numpy(r).to(DEV)
+        out = torch.empty_like(d_r)
+        _lib.grpo_group_advantage(d_r, G, np.float32(1e-6), unbiased, out)
+        want = OA.group_advantage(r, G, np.float32(1e-6), unbiased)
+        assert np.array_equal(out.cpu().numpy(), want)
+    # broadcast with a padding row (rollout -1)
+    adv = torch.tensor([0.5, -1.0], device=DEV)
+    rr = torch.tensor([0, 1, -1, 1], dtype=torch.int32, device=DEV)
+    off = torch.tensor([0, 2, 3, 6, 8], dtype=torch.int64, device=DEV)
+    tok = torch.full((8,), 9.0, device=DEV)
+    rewards = torch.tensor([1.0, 0.0], device=DEV)
+    _lib.grpo_group_advantage(rewards, 2, 1e-6, True, adv, rr, off, tok)
+    a = adv.cpu().numpy()
+    assert tok.cpu().numpy().tolist() == OA.broadcast_to_tokens(a, [0, 1, -1, 1], [2, 1, 3, 2]).tolist()
+
+
+def test_chunked_equals_unchunked_bitwise():
+    wl = W.make_workload("qwen_step", rows=8, len_lo=16, len_hi=40, V=8200, seed=13,
+                         mini=4, micro=1)
+    case = H.Case(wl)
+    outs = []
+    for micro in (1, 2, 4):
+        cfg = dict(wl.plan, micro=micro)
+        bp = S.plan_batch(cfg, wl.row_len, wl.row_valid)
+        T = wl.T
+        dl = torch.empty_like(case.logits)
+        loss = torch.empty(T, device=DEV)
+        logp = torch.empty(T, device=DEV)
+        accs = torch.zeros(bp.n_steps * _lib.ACC_BYTES, dtype=torch.uint8, device=DEV)
+        S.run_batch(bp, logits=case.logits, dlogits=dl, target=case.d_target, old_logp=case.d_old,
+                    mask=case.d_mask, adv_tok=case.d_adv, loss_tok=loss, logp_tok=logp, accs=accs,
+                    clip_eps=wl.eps)
+        torch.cuda.synchronize()
+        outs.append((dl.clone(), loss.clone(), S.read_results(accs, bp.n_steps)))
+    for dl, loss, res in outs[1:]:
+        assert torch.equal(dl.view(torch.int16), outs[0][0].view(torch.int16))
+        assert torch.equal(loss, outs[0][1])
+        assert res == outs[0][2]
+    # the step losses match the oracle's token mean over each mini-batch
+    ref = H.oracle_run(case, want_grad=False)
+    bp = S.plan_batch(dict(wl.plan, micro=1), wl.row_len, wl.row_valid)
+    for s, (t0, t1) in enumerate(bp.step_tok_range):
+        fin = OL.finish_step(ref["loss_tok"][t0:t1], wl.mask[t0:t1], ref["clipped"][t0:t1])
+        got = outs[0][2][s]
+        scale = max(abs(fin["loss"]), np.sum(np.abs(ref["loss_tok"][t0:t1])) / max(fin["n_valid"], 1))
+        assert abs(got["loss"] - fin["loss"]) <= 1e-5 * scale
+        assert got["n_valid"] == fin["n_valid"] == bp.plan["step_valid_tokens"][s]
+        assert got["status"] == 0
+
+
+def test_deferred_scaling_matches_direct_scale():
+    wl = W.make_workload("qwen_step", rows=4, len_lo=10, len_hi=20, V=4104, seed=14)
+    case = H.Case(wl)
+    N = int(wl.mask.sum())
+    dl, loss, logp, acc = _run_direct(case, 1.0)
+    res = _lib.grpo_finish_step(acc, loss, expected_N=N, deferred=True, grad_bufs=[dl])
+    assert res["status"] == 0 and res["n_valid"] == N
+    ref = H.oracle_run(case, scale_per_token=np.full(wl.T, 1.0 / N))
+    # two bf16 roundings (before and after the scale): allow twice the bf16 bar
+    got = H.to_f64(dl)
+    rowmax = np.max(np.abs(ref["dlogits"]), axis=1, keepdims=True)
+    assert np.all(np.abs(got - ref["dlogits"]) <= 2e-2 * np.abs(ref["dlogits"]) + 1e-6 * rowmax)
+
+
+def test_nonfinite_chunk_skips_step_and_zeroes_grads():
+    wl = W.make_workload("qwen_step", rows=4, len_lo=6, len_hi=8, V=1000, seed=15)
+    case = H.Case(wl)
+    lg = case.logits.clone()
+    lg[2, 17] = float("nan")   # a poisoned token row, planted in the host-side input
+    dl, loss, logp, acc = _run_direct(case, 1.0, logits=lg)
+    res = _lib.grpo_finish_step(acc, loss, grad_bufs=[dl])
+    assert res["status"] == _lib.STEP_SKIPPED_NONFINITE and res["n_nonfinite"] >= 1
+    assert torch.all(dl == 0)
+    # the accumulator was reset: the next clean step is fine
+    dl, loss, logp, acc2 = _run_direct(case, 1.0)
+    assert _lib.grpo_finish_step(acc2, loss)["status"] == 0
+
+
+def test_bad_target_counts_as_nonfinite():
+    wl = W.make_workload("qwen_step", rows=4, len_lo=4, len_hi=5, V=1000, seed=16)
+    case = H.Case(wl)
+    case.d_target = case.d_target.clone()
+    case.d_target[1] = 1000
+    dl, loss, logp, acc = _run_direct(case, 1.0)
+    assert _lib.grpo_finish_step(acc, loss)["n_nonfinite"] == 1
+
+
+def test_expected_n_mismatch_reported():
+    wl = W.make_workload("qwen_step", rows=4, len_lo=4, len_hi=5, V=1000, seed=17)
+    case = H.Case(wl)
+    dl, loss, logp, acc = _run_direct(case, 1.0)
+    res = _lib.grpo_finish_step(acc, loss, expected_N=int(wl.mask.sum()) + 1, grad_bufs=[dl])
+    assert res["status"] == _lib.ERR_N_MISMATCH
+    assert torch.all(dl == 0)
+
+
+def test_invalid_arguments_rejected():
+    acc = _lib.new_step_acc(DEV)
+    x = torch.zeros((2, 8), device=DEV)
+    i = torch.zeros(2, dtype=torch.int32, device=DEV)
+    m = torch.ones(2, dtype=torch.uint8, device=DEV)
+    f = torch.zeros(2, device=DEV)
+    with pytest.raises(_lib.GrpoError):
+        _lib.grpo_logprob_loss_fwd_bwd(x, i, None, f, m, 0.2, 1.0, None, f, None, acc, V=9)
+    with pytest.raises(_lib.GrpoError):
+        _lib.grpo_logprob_loss_fwd_bwd(x, i, None, f, m, 0.2, 1.0, None, None, None, acc)
