@@ -306,7 +306,10 @@ def run_gb300(args):
     from rl_post_token_gb300 import workloads as W
 
     _lib.lib()
-    wl = W.make_workload(args.workload, seed=rank)
+    ov = {"rows": args.rows} if args.rows else {}
+    if args.rows and args.workload == "qwen_step":
+        ov.update(mini=args.rows, micro=args.rows)
+    wl = W.make_workload(args.workload, seed=rank, **ov)
     batch = Batch(wl, device)
     stream = torch.cuda.current_stream(device)
 
@@ -353,7 +356,8 @@ def run_gb300(args):
         "warmup": max(args.warmup, 3), "ms_per_step": 1e3 * max_el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "valid_tokens_per_step": wl.n_valid,
+        "config": {"workload": WORKLOAD_TEXT[args.workload] + (f" [rows overridden: {args.rows}]" if args.rows else ""),
+                   "valid_tokens_per_step": wl.n_valid,
                    "logits_rows_per_step": batch.bp.exec_tokens, "vocab": wl.V,
                    "l2": "inputs larger than L2 (%.1f GB of logits per step), no flush"
                          % (batch.bp.exec_tokens * wl.V * wl.elem_bytes / 1e9),
@@ -445,6 +449,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--rows", type=int, default=0,
+                    help="override the workload's row count (smaller cases for profiling)")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
