@@ -58,17 +58,51 @@ __device__ __forceinline__ MS warp_ms(MS v) {
   return v;
 }
 
+// The same pair with the maximum kept in log2 units (m2 = max * log2(e)): the exponent of
+// every element is then a single fma(x, log2e, -m2) and the shift cancels exactly in
+// lse2 = m2 + log2(s), whatever the rounding of m2.
+__device__ __forceinline__ MS ms2_combine(MS a, MS b) {
+  const float m = fmaxf(a.m, b.m);
+  if (m == -INFINITY) return {m, 0.f};
+  return {m, a.s * ex2(a.m - m) + b.s * ex2(b.m - m)};
+}
+
+__device__ __forceinline__ MS warp_ms2(MS v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    MS w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o)};
+    v = ms2_combine(v, w);
+  }
+  return v;
+}
+
+// Fold N more values into a log2-domain online pair (one rescale per call).
+// Branch-free: while every value so far is -inf the shift is 0 and the sum stays 0.
+template <int N>
+__device__ __forceinline__ void online2(MS& acc, const float (&x)[N]) {
+  float gm = x[0];
+#pragma unroll
+  for (int i = 1; i < N; ++i) gm = fmaxf(gm, x[i]);
+  const float nm = fmaxf(acc.m, gm * kLog2e);
+  const bool none = nm == -INFINITY;
+  acc.s *= none ? 1.f : ex2(acc.m - nm);  // ex2(-inf) = 0 on the first finite block
+  acc.m = nm;
+  const float sh = none ? 0.f : nm;
+#pragma unroll
+  for (int i = 0; i < N; ++i) acc.s += ex2(fmaf(x[i], kLog2e, -sh));
+}
+
 // Per-token scalar epilogue: log-prob, ratio, clipped surrogate, gradient coefficient.
 struct TokenOut {
   float logp, loss, coef;
   bool clipped, nonfinite;
 };
 
-__device__ __forceinline__ TokenOut token_epilogue(float zy, float lse, const float* old_logp,
-                                                  int64_t idx, float A, float eps, float scale) {
+__device__ __forceinline__ TokenOut token_epilogue(float zy, float lse, bool has_old, float old,
+                                                  float A, float eps, float scale) {
   TokenOut o;
   o.logp = zy - lse;
-  const float r = old_logp ? expf(o.logp - old_logp[idx]) : 1.f;
+  const float r = has_old ? expf(o.logp - old) : 1.f;
   const float lo = 1.f - eps, hi = 1.f + eps;
   const float rc = fminf(fmaxf(r, lo), hi);
   o.loss = -fminf(r * A, rc * A);
@@ -76,6 +110,101 @@ __device__ __forceinline__ TokenOut token_epilogue(float zy, float lse, const fl
   o.coef = o.clipped ? 0.f : A * r * scale;
   o.nonfinite = !isfinite(o.logp) || !isfinite(o.loss) || !isfinite(o.coef);
   return o;
+}
+
+// ---- shared-memory, mbarrier, bulk-copy and cluster primitives (inline PTX, sm_90+) ----------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+               ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on an mbarrier phase: gives up after ~1 s (or 2^24 polls), raises *abort and
+// returns false. Once *abort is set no later wait blocks, so a broken pipeline still lets
+// the kernel run to its end and report kFlagWaitTimeout instead of hanging.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (*abort) return false;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1; i < (1u << 24); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0 && global_timer_ns() - t0 > 1000000000ull) break;
+    if (*abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort);
+}
+
+// One contiguous global -> shared bulk copy completing on `bar` (16-byte aligned addresses,
+// size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA in the cluster; release/acquire orders shared-memory writes
+// before the barrier with reads from other CTAs after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 }  // namespace grpo

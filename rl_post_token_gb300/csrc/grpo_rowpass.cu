@@ -24,6 +24,8 @@
 #include <cooperative_groups.h>
 
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 
 #include "grpo_common.cuh"
 
@@ -85,18 +87,48 @@ struct Vec<float> {
 };
 
 // Side inputs of one token row, resolved through tok_src.
-struct TokMeta {
+struct RowMeta {
   int64_t idx;   // index into the per-token side arrays (-1 for padding rows)
   bool valid;    // mask = 1 and not a padding row
+  int32_t y;     // target token id
+  float A, old;  // advantage, pi_old log-prob
 };
 
-__device__ __forceinline__ TokMeta tok_meta(const RowArgs& a, int64_t row) {
-  const int64_t src = a.tok_src ? a.tok_src[row] : row;
-  TokMeta t;
-  t.idx = src < 0 ? -1 : src;
-  t.valid = src >= 0 && a.mask[src] != 0;
-  return t;
+__device__ __forceinline__ int64_t row_src(const RowArgs& a, int64_t row) {
+  return a.tok_src ? a.tok_src[row] : row;
 }
+
+__device__ __forceinline__ RowMeta row_meta(const RowArgs& a, int64_t src) {
+  RowMeta m{src < 0 ? -1 : src, false, 0, 0.f, 0.f};
+  if (src >= 0) {
+    m.valid = a.mask[src] != 0;
+    m.y = a.target[src];
+    m.A = a.adv[src];
+    m.old = a.old_logp ? a.old_logp[src] : 0.f;
+  }
+  return m;
+}
+
+// Row metadata fetched ahead of use: the token index two rows ahead and the side inputs one
+// row ahead are in flight while the current row is processed, so the dependent global-load
+// chain (index -> mask/target/advantage/pi_old) never sits on a row's critical path.
+struct MetaPipe {
+  const RowArgs& a;
+  int64_t stride;
+  RowMeta next;
+  int64_t src2;
+  __device__ MetaPipe(const RowArgs& args, int64_t first, int64_t step) : a(args), stride(step) {
+    next = first < a.T ? row_meta(a, row_src(a, first)) : RowMeta{-1, false, 0, 0.f, 0.f};
+    src2 = first + step < a.T ? row_src(a, first + step) : -1;
+  }
+  // metadata of `row`; starts the loads for the rows after it
+  __device__ RowMeta advance(int64_t row) {
+    const RowMeta m = next;
+    if (row + stride < a.T) next = row_meta(a, src2);
+    src2 = row + 2 * stride < a.T ? row_src(a, row + 2 * stride) : -1;
+    return m;
+  }
+};
 
 // Counters a CTA accumulates and flushes once (integer: order-independent).
 struct Counts {
@@ -125,8 +157,9 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
   const int64_t tail0 = nvec * VN;
   Counts cnt;
 
+  MetaPipe pipe(a, blockIdx.x, gridDim.x);
   for (int64_t row = blockIdx.x; row < a.T; row += gridDim.x) {
-    const TokMeta tm = tok_meta(a, row);
+    const RowMeta tm = pipe.advance(row);
     const T* z = static_cast<const T*>(a.logits) + row * a.ld;
     T* dz = a.dlogits ? static_cast<T*>(a.dlogits) + row * a.ld_out : nullptr;
     if (!tm.valid) {
@@ -145,7 +178,7 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
       }
       continue;
     }
-    const int32_t y = a.target[tm.idx];
+    const int32_t y = tm.y;
     const bool ybad = y < 0 || (int64_t)y >= V;
     float zy = 0.f;
     if (tid == 0 && !ybad) zy = Vec<T>::load1(z + y);
@@ -195,8 +228,8 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
       v = warp_ms(v);
       if (lane == 0) {
         const float lse = v.m + logf(v.s);
-        const TokenOut o = token_epilogue(ybad ? __int_as_float(0x7fc00000) : zy, lse, a.old_logp,
-                                          tm.idx, a.adv[tm.idx], a.eps, a.scale);
+        const TokenOut o = token_epilogue(ybad ? __int_as_float(0x7fc00000) : zy, lse,
+                                          a.old_logp != nullptr, tm.old, tm.A, a.eps, a.scale);
         a.loss_tok[tm.idx] = o.loss;
         if (a.logp_tok) a.logp_tok[tm.idx] = o.logp;
         cnt.tokens++;
@@ -241,6 +274,276 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
     __syncthreads();  // sh_* are rewritten by the next row
   }
   if (tid == 0) cnt.flush(a.acc);
+}
+
+__device__ __forceinline__ void unpack8_at(const uint4& a, float* x) {
+  x[0] = bf16_lo(a.x); x[1] = bf16_hi(a.x); x[2] = bf16_lo(a.y); x[3] = bf16_hi(a.y);
+  x[4] = bf16_lo(a.z); x[5] = bf16_hi(a.z); x[6] = bf16_lo(a.w); x[7] = bf16_hi(a.w);
+}
+
+
+// Eight dlogits of one 16-byte vector: sign * 2^(z log2e - cexp), rounded to bf16.
+__device__ __forceinline__ void dz_vec(const uint4& u, uint4* dst, float cexp, uint32_t sgn) {
+  float x[8];
+  Vec<__nv_bfloat16>::unpack(u, x);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = ex2(fmaf(x[i], kLog2e, -cexp));
+  __stcs(dst, make_uint4(pack_bf16x2(x[0], x[1]) ^ sgn, pack_bf16x2(x[2], x[3]) ^ sgn,
+                         pack_bf16x2(x[4], x[5]) ^ sgn, pack_bf16x2(x[6], x[7]) ^ sgn));
+}
+
+// ------------------------------------------------------------------------------------------
+// Cluster kernel: a row is split across the C CTAs of a cluster. CTA r owns the slice
+// [r*Vs, r*Vs + n_r) and keeps it in shared memory for both passes. Warp 0 is the producer:
+// one lane issues the slice as 16 KB bulk copies, each completing on its own "full"
+// mbarrier, and refills chunk k for the next row as soon as every consumer warp has released
+// it on its "empty" mbarrier. Warps 1..NCW consume: pass 1 (online max / sum-exp) from shared
+// memory, a fixed-order reduction, one cluster barrier per row to exchange (max, sum-exp) and
+// the target logit through distributed shared memory, then pass 2 (dlogits) from shared
+// memory with 16-byte streaming stores. HBM sees one read and one write of each row.
+// ------------------------------------------------------------------------------------------
+constexpr int kMaxChunks = 16;
+
+// Elements per bulk-copied chunk: every consumer thread owns VPT 16-byte vectors of a full
+// chunk (32 KB for the 2-CTA cluster, 16 KB for the 4-CTA one).
+__host__ __device__ constexpr int cluster_chunk_elems(int NCW, int VPT) { return VPT * NCW * 32 * 8; }
+
+__host__ __device__ constexpr int cluster_slice_elems(int64_t V, int C) {
+  return (int)((((V + C - 1) / C) + 7) / 8 * 8);
+}
+
+__host__ __device__ constexpr size_t cluster_smem_bytes(int Vs, int NCW) {
+  return ((size_t)Vs * 2 + 127) / 128 * 128 + 2 * kMaxChunks * sizeof(uint64_t) +
+         8 * sizeof(float) + 2 * NCW * sizeof(float) + 16;
+}
+
+// Bounded wait used only when draining after a timeout (ignores the abort flag).
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 0; i < (1u << 24); ++i) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((i & 255u) == 0 && global_timer_ns() - t0 > 1000000000ull) return;
+  }
+}
+
+template <int C, int NCW, int VPT>
+__global__ void __launch_bounds__((NCW + 1) * 32, C >= 4 ? 2 : 1) row_cluster_kernel(RowArgs a, int Vs) {
+  constexpr int NC = NCW * 32;
+  constexpr int kChunkElems = cluster_chunk_elems(NCW, VPT);
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int slice_bytes = (Vs * 2 + 127) / 128 * 128;
+  __nv_bfloat16* slice = reinterpret_cast<__nv_bfloat16*>(smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + slice_bytes);
+  uint64_t* empty = full + kMaxChunks;
+  float* xch = reinterpret_cast<float*>(empty + kMaxChunks);  // [2 rows][m, s, z_y, -]
+  float* wpart = xch + 8;                                      // [NCW][m, s]
+  volatile int* s_abort = reinterpret_cast<volatile int*>(wpart + 2 * NCW);
+
+  const uint32_t rank = cluster_ctarank();
+  const int64_t cid = blockIdx.x / C, ncl = gridDim.x / C;
+  const int64_t V = a.V;
+  const int64_t base = (int64_t)rank * Vs;
+  const int n_r = (int)max((int64_t)0, min((int64_t)Vs, V - base));
+  const int nch = (n_r + kChunkElems - 1) / kChunkElems;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int k = 0; k < kMaxChunks; ++k) {
+      mbar_init(&full[k], 1);
+      mbar_init(&empty[k], NCW);
+    }
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  cluster_sync_all();
+
+  const __nv_bfloat16* lg = static_cast<const __nv_bfloat16*>(a.logits);
+  __nv_bfloat16* dg = static_cast<__nv_bfloat16*>(a.dlogits);
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  Counts cnt;
+  uint32_t vi = 0;  // valid rows so far: phase index of every full/empty barrier
+
+  MetaPipe pipe(a, cid, ncl);
+  for (int64_t row = cid; row < a.T; row += ncl) {
+    const RowMeta tm = pipe.advance(row);
+    uint4* dz = dg ? reinterpret_cast<uint4*>(dg + row * a.ld_out + base) : nullptr;
+    if (!tm.valid) {
+      // masked or padding row: nothing read, nothing exchanged; zero dlogits slice
+      if (warp > 0 && dz)
+        for (int v = tid - 32; v < n_r / 8; v += NC) __stcs(dz + v, zero);
+      if (rank == 0 && tid == 32) {
+        cnt.tokens++;
+        if (tm.idx >= 0) {
+          a.loss_tok[tm.idx] = 0.f;
+          if (a.logp_tok) a.logp_tok[tm.idx] = 0.f;
+        }
+      }
+      continue;
+    }
+    const uint32_t par = vi & 1u;
+    float* xb = xch + 4 * (vi & 1u);
+
+    if (warp == 0) {
+      // ---- producer ----
+      if (lane == 0) {
+        const __nv_bfloat16* src = lg + row * a.ld + base;
+        for (int k = 0; k < nch; ++k) {
+          if (vi > 0) mbar_wait_bounded(&empty[k], par ^ 1u, s_abort);
+          const int n_k = min(kChunkElems, n_r - k * kChunkElems);
+          mbar_arrive_expect_tx(&full[k], (uint32_t)n_k * 2u);
+          bulk_g2s(slice + k * kChunkElems, src + k * kChunkElems, (uint32_t)n_k * 2u, &full[k]);
+        }
+      }
+      __syncwarp();
+      cluster_sync_all();
+    } else {
+      // ---- consumers ----
+      const int ct = tid - 32;
+      const int32_t y = tm.y;
+      const bool ybad = y < 0 || (int64_t)y >= V;
+
+      // pass 1: log2-domain online (max, sum) over the slice, chunk by chunk as it lands
+      MS acc{-INFINITY, 0.f};
+      for (int k = 0; k < nch; ++k) {
+        mbar_wait_bounded(&full[k], par, s_abort);
+        const int nv = min(kChunkElems, n_r - k * kChunkElems) / 8;
+        const uint4* sv = reinterpret_cast<const uint4*>(slice + k * kChunkElems);
+        if (nv == VPT * NC) {  // full chunk: exactly VPT 16-byte vectors per consumer thread
+          float x[VPT * 8];
+#pragma unroll
+          for (int j = 0; j < VPT; ++j) unpack8_at(sv[ct + j * NC], x + 8 * j);
+          online2<VPT * 8>(acc, x);
+        } else {
+          for (int v = ct; v < nv; v += NC) {
+            float x[8];
+            Vec<__nv_bfloat16>::unpack(sv[v], x);
+            online2<8>(acc, x);
+          }
+        }
+      }
+      const MS w = warp_ms2(acc);
+      if (lane == 0) {
+        wpart[2 * (warp - 1)] = w.m;
+        wpart[2 * (warp - 1) + 1] = w.s;
+      }
+      named_bar_sync(1, NC);
+      if (warp == 1 && lane == 0) {
+        MS t{-INFINITY, 0.f};
+        for (int i = 0; i < NCW; ++i) t = ms2_combine(t, MS{wpart[2 * i], wpart[2 * i + 1]});
+        xb[0] = t.m;
+        xb[1] = t.s;
+        if (!ybad && (int64_t)y >= base && (int64_t)y < base + n_r)
+          xb[2] = __bfloat162float(slice[y - base]);
+      }
+      cluster_sync_all();
+
+      // every consumer combines the C slices in rank order: identical LSE in every CTA
+      MS tot{-INFINITY, 0.f};
+      float zy = __int_as_float(0x7fc00000);
+      const uint32_t xaddr = smem_u32(xb);
+#pragma unroll
+      for (int r = 0; r < C; ++r) {
+        const uint32_t ra = mapa_u32(xaddr, (uint32_t)r);
+        tot = ms2_combine(tot, MS{ld_dsmem_f32(ra), ld_dsmem_f32(ra + 4)});
+        if (!ybad && (int64_t)y >= (int64_t)r * Vs && (int64_t)y < (int64_t)(r + 1) * Vs)
+          zy = ld_dsmem_f32(ra + 8);
+      }
+      const float lse2 = tot.m + log2f(tot.s);  // log2(sum_v 2^(z_v log2 e)) = LSE * log2(e)
+      const TokenOut o = token_epilogue(zy, lse2 * kLn2, a.old_logp != nullptr, tm.old, tm.A, a.eps,
+                                        a.scale);
+      if (rank == 0 && ct == 0) {
+        a.loss_tok[tm.idx] = o.loss;
+        if (a.logp_tok) a.logp_tok[tm.idx] = o.logp;
+        cnt.tokens++;
+        cnt.valid++;
+        cnt.clipped += o.clipped;
+        cnt.nonfinite += o.nonfinite;
+      }
+      const float coef = o.coef;
+      if (dz && coef != 0.f) {
+        // pass 2: |coef| * softmax = 2^(z log2e - (lse2 - log2|coef|)), sign applied to the
+        // packed bf16 pair; the target element coef * (p_y - 1) is computed on its own
+        const float cexp = lse2 - log2f(fabsf(coef));
+        const uint32_t sgn = coef < 0.f ? 0x80008000u : 0u;
+        for (int k = 0; k < nch; ++k) {
+          const int nv = min(kChunkElems, n_r - k * kChunkElems) / 8;
+          const uint4* sv = reinterpret_cast<const uint4*>(slice + k * kChunkElems);
+          uint4* dv = dz + k * (kChunkElems / 8);
+          if (nv == VPT * NC) {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) dz_vec(sv[ct + j * NC], dv + ct + j * NC, cexp, sgn);
+          } else {
+            for (int v = ct; v < nv; v += NC) dz_vec(sv[v], dv + v, cexp, sgn);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[k]);
+        }
+        // the target element, coef * (p_y - 1), overwrites the value the vector pass wrote
+        // (same thread, program order)
+        const int64_t yl = ybad ? -1 : (int64_t)y - base;
+        if (yl >= 0 && yl < n_r && ct == (int)(((yl / 8) % (kChunkElems / 8)) % NC)) {
+          const float dzy = coef * ex2(fmaf(zy, kLog2e, -lse2)) - coef;
+          reinterpret_cast<__nv_bfloat16*>(dz)[yl] = __float2bfloat16_rn(dzy);
+        }
+      } else {
+        if (dz)
+          for (int v = ct; v < n_r / 8; v += NC) __stcs(dz + v, zero);
+        __syncwarp();
+        if (lane == 0)
+          for (int k = 0; k < nch; ++k) mbar_arrive(&empty[k]);
+      }
+    }
+    ++vi;
+  }
+
+  if (*s_abort) {
+    // a wait gave up: let any copy still in flight land before the CTA's memory goes away
+    if (tid == 0 && vi > 0)
+      for (int k = 0; k < nch; ++k) mbar_drain(&full[k], (vi - 1) & 1u);
+    if (tid == 0) atomicOr(&a.acc->flags, kFlagWaitTimeout);
+  }
+  cluster_sync_all();  // no CTA leaves while a peer may still read its exchange slots
+  if (tid == 32 && rank == 0) cnt.flush(a.acc);
+}
+
+template <int C, int NCW, int VPT>
+int launch_cluster(const RowArgs& a, cudaStream_t st) {
+  const int Vs = cluster_slice_elems(a.V, C);
+  if ((Vs + cluster_chunk_elems(NCW, VPT) - 1) / cluster_chunk_elems(NCW, VPT) > kMaxChunks)
+    return GRPO_ERR_UNSUPPORTED;
+  const size_t smem = cluster_smem_bytes(Vs, NCW);
+  auto kern = row_cluster_kernel<C, NCW, VPT>;
+  static int cached_dev = -1;
+  static size_t cached_smem = 0;
+  static int cached_clusters = 0;
+  int dev = 0;
+  GRPO_CUDA_TRY(cudaGetDevice(&dev));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3((NCW + 1) * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (dev != cached_dev || smem != cached_smem) {
+    GRPO_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    cfg.gridDim = dim3(C * 1024, 1, 1);
+    int n = 0;
+    GRPO_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
+    if (n < 1) return GRPO_ERR_UNSUPPORTED;
+    cached_dev = dev;
+    cached_smem = smem;
+    cached_clusters = n;
+  }
+  const int64_t clusters = std::min<int64_t>(a.T, cached_clusters);
+  cfg.gridDim = dim3((unsigned)(clusters * C), 1, 1);
+  GRPO_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, a, Vs));
+  return GRPO_OK;
 }
 
 template <typename T, int NT, int U>
@@ -291,6 +594,19 @@ extern "C" GRPO_API int grpo_logprob_loss_fwd_bwd(const void* logits, int32_t dt
   const bool vec = al16(logits) && (ld * es) % 16 == 0 &&
                    (!dlogits || (al16(dlogits) && (ld_out * es) % 16 == 0));
   if (dtype == GRPO_DTYPE_BF16) {
+    // Large bf16 vocabularies: rows split across a CTA cluster and staged in shared memory.
+    // GRPO_ROWPASS=l2|c2|c4 pins a variant (for measurements); the default is c2.
+    const char* pin = getenv("GRPO_ROWPASS");
+    constexpr int ch2 = cluster_chunk_elems(16, 4), ch4 = cluster_chunk_elems(16, 2);
+    const bool cluster_ok = vec && V % 8 == 0 && V >= 16384 &&
+                            (cluster_slice_elems(V, 4) + ch4 - 1) / ch4 <= kMaxChunks &&
+                            cluster_smem_bytes(cluster_slice_elems(V, 4), 16) <= 227 * 1024;
+    if (cluster_ok && !(pin && strcmp(pin, "l2") == 0)) {
+      const bool fits2 = cluster_smem_bytes(cluster_slice_elems(V, 2), 16) <= 227 * 1024 &&
+                         (cluster_slice_elems(V, 2) + ch2 - 1) / ch2 <= kMaxChunks;
+      if (fits2 && !(pin && strcmp(pin, "c4") == 0)) return launch_cluster<2, 16, 4>(a, st);
+      return launch_cluster<4, 16, 2>(a, st);
+    }
     if (V >= 8192) return launch_l2<__nv_bfloat16, 1024, 2>(a, vec, 1, st);
     return launch_l2<__nv_bfloat16, 128, 2>(a, vec, 16, st);
   }

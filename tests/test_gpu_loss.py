@@ -262,3 +262,80 @@ def test_invalid_arguments_rejected():
         _lib.grpo_logprob_loss_fwd_bwd(x, i, None, f, m, 0.2, 1.0, None, f, None, acc, V=9)
     with pytest.raises(_lib.GrpoError):
         _lib.grpo_logprob_loss_fwd_bwd(x, i, None, f, m, 0.2, 1.0, None, None, None, acc)
+
+
+# ---- the shared-memory cluster kernel and its variants ---------------------------------------
+
+VARIANTS = ["c2", "c4", "l2"]
+
+
+@pytest.fixture
+def variant(request, monkeypatch):
+    monkeypatch.setenv("GRPO_ROWPASS", request.param)
+    return request.param
+
+
+@pytest.mark.parametrize("variant", VARIANTS, indirect=True)
+@pytest.mark.parametrize("V,rows,positions", [(16384, 64, 12), (32776, 40, 10), (151936, 24, 12),
+                                              (262144, 8, 10)])
+def test_cluster_variants_many_rows_with_masks(variant, V, rows, positions):
+    # many rows per cluster (refill pipeline, barrier phases), masked rows interleaved,
+    # vocabularies whose last 16 KB chunk is ragged (32776) or that need 4-CTA clusters (262144)
+    wl = W.make_workload("tiny", rows=rows, positions=positions, valid_lo=0, V=V, dtype="bf16",
+                         seed=V % 997, std=3.0)
+    _check_case(H.Case(wl), scale=1.0 / 333)
+
+
+@pytest.mark.parametrize("variant", ["c2", "c4"], indirect=True)
+def test_cluster_permutation_pad_rows_and_forward_only(variant):
+    wl = W.make_workload("qwen_step", rows=8, len_lo=20, len_hi=40, V=16384, seed=21)
+    case = H.Case(wl)
+    T = case.logits.shape[0]
+    rng = np.random.default_rng(1)
+    perm = rng.permutation(T)
+    pads = rng.choice(T, 5)
+    tok_src = torch.from_numpy(np.concatenate([perm, -1 - pads]).astype(np.int64)).to(DEV)
+    lg = torch.cat([case.logits[torch.from_numpy(perm).to(DEV)], case.logits[torch.from_numpy(pads).to(DEV)]])
+    dl, loss, logp, acc = _run_direct(case, 0.5, tok_src=tok_src, logits=lg)
+    ref = H.oracle_run(case, scale_per_token=np.full(T, 0.5))
+    H.assert_tokens_close(H.to_f64(loss), H.to_f64(logp), ref, case.adv_tok, case.mask)
+    got = H.to_f64(dl)
+    H.assert_dlogits_close(got[:T], ref["dlogits"][perm], "bf16", target=ref["target"][perm],
+                           coef=ref["coef"][perm])
+    assert np.all(got[T:] == 0)
+    _, loss2, logp2, _ = _run_direct(case, 0.5, want_grad=False, tok_src=tok_src, logits=lg)
+    assert torch.equal(loss2, loss) and torch.equal(logp2, logp)
+
+
+@pytest.mark.parametrize("variant", ["c2", "c4"], indirect=True)
+def test_cluster_nonfinite_row(variant):
+    wl = W.make_workload("qwen_step", rows=4, len_lo=30, len_hi=40, V=16384, seed=22)
+    case = H.Case(wl)
+    lg = case.logits.clone()
+    lg[7, 12000] = float("inf")
+    lg[19, 3] = float("nan")
+    dl, loss, logp, acc = _run_direct(case, 1.0, logits=lg)
+    res = _lib.grpo_finish_step(acc, loss, grad_bufs=[dl])
+    assert res["status"] == _lib.STEP_SKIPPED_NONFINITE and res["n_nonfinite"] == 2
+    assert res["kernel_flags"] == 0
+    assert torch.all(dl == 0)
+
+
+@pytest.mark.parametrize("variant", ["c2", "c4"], indirect=True)
+def test_cluster_chunked_equals_unchunked_bitwise(variant):
+    wl = W.make_workload("qwen_step", rows=8, len_lo=16, len_hi=40, V=32776, seed=23, mini=4, micro=1)
+    case = H.Case(wl)
+    outs = []
+    for micro in (1, 4):
+        bp = S.plan_batch(dict(wl.plan, micro=micro), wl.row_len, wl.row_valid)
+        dl = torch.empty_like(case.logits)
+        loss = torch.empty(wl.T, device=DEV)
+        logp = torch.empty(wl.T, device=DEV)
+        accs = torch.zeros(bp.n_steps * _lib.ACC_BYTES, dtype=torch.uint8, device=DEV)
+        S.run_batch(bp, logits=case.logits, dlogits=dl, target=case.d_target, old_logp=case.d_old,
+                    mask=case.d_mask, adv_tok=case.d_adv, loss_tok=loss, logp_tok=logp, accs=accs,
+                    clip_eps=wl.eps)
+        torch.cuda.synchronize()
+        outs.append((dl.view(torch.int16).clone(), loss.clone(), S.read_results(accs, bp.n_steps)))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    assert outs[0][2] == outs[1][2]
