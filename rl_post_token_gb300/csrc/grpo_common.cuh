@@ -77,19 +77,64 @@ __device__ __forceinline__ MS warp_ms2(MS v) {
 }
 
 // Fold N more values into a log2-domain online pair (one rescale per call).
-// Branch-free: while every value so far is -inf the shift is 0 and the sum stays 0.
+// Pairwise (tree) reductions of a register array: log2(N) dependent steps instead of N, so
+// a thread's block of exponentials never waits on one long add chain. The order is fixed.
 template <int N>
-__device__ __forceinline__ void online2(MS& acc, const float (&x)[N]) {
-  float gm = x[0];
+__device__ __forceinline__ float tree_max(const float (&x)[N]) {
+  static_assert((N & (N - 1)) == 0, "power of two");
+  float t[N];
 #pragma unroll
-  for (int i = 1; i < N; ++i) gm = fmaxf(gm, x[i]);
-  const float nm = fmaxf(acc.m, gm * kLog2e);
+  for (int i = 0; i < N; ++i) t[i] = x[i];
+#pragma unroll
+  for (int w = N / 2; w >= 1; w /= 2)
+#pragma unroll
+    for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
+  return t[0];
+}
+
+template <int N>
+__device__ __forceinline__ float tree_sum(float (&t)[N]) {
+  static_assert((N & (N - 1)) == 0, "power of two");
+#pragma unroll
+  for (int w = N / 2; w >= 1; w /= 2)
+#pragma unroll
+    for (int i = 0; i < w; ++i) t[i] = t[i] + t[i + w];
+  return t[0];
+}
+
+// Fold N more values into a log2-domain online pair: one rescale per call, the N
+// exponentials independent, summed by a fixed tree. Branch-free: while every value so far is
+// -inf the shift is 0 and the sum stays 0.
+template <int N>
+__device__ __forceinline__ void online2(MS& acc, float (&x)[N]) {
+  const float nm = fmaxf(acc.m, tree_max(x) * kLog2e);
   const bool none = nm == -INFINITY;
-  acc.s *= none ? 1.f : ex2(acc.m - nm);  // ex2(-inf) = 0 on the first finite block
-  acc.m = nm;
+  const float scale = none ? 1.f : ex2(acc.m - nm);  // ex2(-inf) = 0 on the first finite block
   const float sh = none ? 0.f : nm;
 #pragma unroll
-  for (int i = 0; i < N; ++i) acc.s += ex2(fmaf(x[i], kLog2e, -sh));
+  for (int i = 0; i < N; ++i) x[i] = ex2(fmaf(x[i], kLog2e, -sh));
+  acc.s = fmaf(acc.s, scale, tree_sum(x));
+  acc.m = nm;
+}
+
+// Lazy variant: exponentials are taken against the current shift, and the block's maximum
+// is only computed when the block sum leaves the safe range (> 2^64, inf or NaN), which for
+// real logits happens about once per thread and row (the first block, shift -inf). Exact in
+// the same sense as online2: the sum carries its scale, and lse2 = m + log2(s) either way.
+template <int N>
+__device__ __forceinline__ void lazy_online2(MS& acc, float (&x)[N]) {
+  // the first block takes its first value as the shift (the sum is still 0, so any shift is
+  // exact); a block rising more than 2^64 above it falls back to the max-based update
+  if (acc.m == -INFINITY) acc.m = x[0] * kLog2e;
+  float e[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) e[i] = ex2(fmaf(x[i], kLog2e, -acc.m));
+  const float bs = tree_sum(e);
+  if (bs <= 1.8446744e19f) {  // false for inf and NaN
+    acc.s += bs;
+    return;
+  }
+  online2<N>(acc, x);
 }
 
 // Per-token scalar epilogue: log-prob, ratio, clipped surrogate, gradient coefficient.
@@ -143,6 +188,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Acquire at cluster scope: pairs with a peer CTA's release-arrive on this barrier, so the
+// peer's shared::cluster stores made before its arrive are visible after the wait.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Arrive on an mbarrier that lives in a peer CTA's shared memory (address from mapa),
+// releasing this thread's earlier shared::cluster stores to that CTA.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -167,6 +236,25 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, abort);
+}
+
+static __device__ __noinline__ bool mbar_wait_cluster_slow(uint64_t* bar, uint32_t parity,
+                                                          volatile int* abort) {
+  if (*abort) return false;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1; i < (1u << 24); ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 255u) == 0 && global_timer_ns() - t0 > 1000000000ull) break;
+    if (*abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity,
+                                                          volatile int* abort) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  return mbar_wait_cluster_slow(bar, parity, abort);
 }
 
 // One contiguous global -> shared bulk copy completing on `bar` (16-byte aligned addresses,

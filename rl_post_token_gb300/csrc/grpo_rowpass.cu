@@ -276,36 +276,20 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
   if (tid == 0) cnt.flush(a.acc);
 }
 
-__device__ __forceinline__ void unpack8_at(const uint4& a, float* x) {
-  x[0] = bf16_lo(a.x); x[1] = bf16_hi(a.x); x[2] = bf16_lo(a.y); x[3] = bf16_hi(a.y);
-  x[4] = bf16_lo(a.z); x[5] = bf16_hi(a.z); x[6] = bf16_lo(a.w); x[7] = bf16_hi(a.w);
-}
-
-
-// Eight dlogits of one 16-byte vector: sign * 2^(z log2e - cexp), rounded to bf16.
-__device__ __forceinline__ void dz_vec(const uint4& u, uint4* dst, float cexp, uint32_t sgn) {
-  float x[8];
-  Vec<__nv_bfloat16>::unpack(u, x);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) x[i] = ex2(fmaf(x[i], kLog2e, -cexp));
-  __stcs(dst, make_uint4(pack_bf16x2(x[0], x[1]) ^ sgn, pack_bf16x2(x[2], x[3]) ^ sgn,
-                         pack_bf16x2(x[4], x[5]) ^ sgn, pack_bf16x2(x[6], x[7]) ^ sgn));
-}
-
 // ------------------------------------------------------------------------------------------
-// Cluster kernel: a row is split across the C CTAs of a cluster. CTA r owns the slice
+// Cluster kernel: a row is split across the C CTAs of a cluster; CTA r owns the slice
 // [r*Vs, r*Vs + n_r) and keeps it in shared memory for both passes. Warp 0 is the producer:
-// one lane issues the slice as 16 KB bulk copies, each completing on its own "full"
-// mbarrier, and refills chunk k for the next row as soon as every consumer warp has released
-// it on its "empty" mbarrier. Warps 1..NCW consume: pass 1 (online max / sum-exp) from shared
-// memory, a fixed-order reduction, one cluster barrier per row to exchange (max, sum-exp) and
-// the target logit through distributed shared memory, then pass 2 (dlogits) from shared
-// memory with 16-byte streaming stores. HBM sees one read and one write of each row.
+// one lane issues the slice as 32 KB bulk copies, each completing on its own "full"
+// mbarrier, and refills chunk k with the next row as soon as every consumer warp has released
+// it on its "empty" mbarrier (so the next row streams in during this row's pass 2). Warps
+// 1..NCW consume: pass 1 (online max / sum-exp) from shared memory, a fixed-order reduction,
+// one cluster barrier per row to exchange (max, sum-exp) and the target logit through
+// distributed shared memory, then pass 2 (dlogits) from shared memory with 16-byte streaming
+// stores. HBM sees one read and one write of each row.
 // ------------------------------------------------------------------------------------------
 constexpr int kMaxChunks = 16;
 
-// Elements per bulk-copied chunk: every consumer thread owns VPT 16-byte vectors of a full
-// chunk (32 KB for the 2-CTA cluster, 16 KB for the 4-CTA one).
+// Elements per bulk-copied chunk: every consumer thread owns VPT 16-byte vectors of it.
 __host__ __device__ constexpr int cluster_chunk_elems(int NCW, int VPT) { return VPT * NCW * 32 * 8; }
 
 __host__ __device__ constexpr int cluster_slice_elems(int64_t V, int C) {
@@ -326,10 +310,52 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <int C, int NCW, int VPT>
-__global__ void __launch_bounds__((NCW + 1) * 32, C >= 4 ? 2 : 1) row_cluster_kernel(RowArgs a, int Vs) {
+__device__ __forceinline__ void unpack8_at(const uint4& a, float* x) {
+  x[0] = bf16_lo(a.x); x[1] = bf16_hi(a.x); x[2] = bf16_lo(a.y); x[3] = bf16_hi(a.y);
+  x[4] = bf16_lo(a.z); x[5] = bf16_hi(a.z); x[6] = bf16_lo(a.w); x[7] = bf16_hi(a.w);
+}
+
+// Eight dlogits of one 16-byte vector: (-1)^NEG * 2^(z log2e - cexp), rounded to bf16.
+template <bool NEG>
+__device__ __forceinline__ void dz_vec(const uint4& u, uint4* dst, float cexp) {
+  float x[8];
+  Vec<__nv_bfloat16>::unpack(u, x);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = ex2(fmaf(x[i], kLog2e, -cexp));
+  uint4 r = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                       pack_bf16x2(x[6], x[7]));
+  if (NEG) {
+    r.x ^= 0x80008000u;
+    r.y ^= 0x80008000u;
+    r.z ^= 0x80008000u;
+    r.w ^= 0x80008000u;
+  }
+  __stcs(dst, r);
+}
+
+// Pass 2 over the CTA's slice; each warp releases chunk k once it is done with it.
+template <bool NEG, int NC, int VPT, int CH>
+__device__ __forceinline__ void pass2_slice(const __nv_bfloat16* slice, uint4* dz, int n_r, int nch,
+                                            int ct, int lane, float cexp, uint64_t* empty) {
+  for (int k = 0; k < nch; ++k) {
+    const int nv = min(CH, n_r - k * CH) / 8;
+    const uint4* sv = reinterpret_cast<const uint4*>(slice + k * CH);
+    uint4* dv = dz + k * (CH / 8);
+    if (nv == VPT * NC) {
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) dz_vec<NEG>(sv[ct + j * NC], dv + ct + j * NC, cexp);
+    } else {
+      for (int v = ct; v < nv; v += NC) dz_vec<NEG>(sv[v], dv + v, cexp);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[k]);
+  }
+}
+
+template <int C, int NCW, int VPT, int MINB>
+__global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowArgs a, int Vs) {
   constexpr int NC = NCW * 32;
-  constexpr int kChunkElems = cluster_chunk_elems(NCW, VPT);
+  constexpr int CH = cluster_chunk_elems(NCW, VPT);
   extern __shared__ __align__(128) uint8_t smem[];
   const int slice_bytes = (Vs * 2 + 127) / 128 * 128;
   __nv_bfloat16* slice = reinterpret_cast<__nv_bfloat16*>(smem);
@@ -344,7 +370,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, C >= 4 ? 2 : 1) row_cluster_ke
   const int64_t V = a.V;
   const int64_t base = (int64_t)rank * Vs;
   const int n_r = (int)max((int64_t)0, min((int64_t)Vs, V - base));
-  const int nch = (n_r + kChunkElems - 1) / kChunkElems;
+  const int nch = (n_r + CH - 1) / CH;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
@@ -390,9 +416,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, C >= 4 ? 2 : 1) row_cluster_ke
         const __nv_bfloat16* src = lg + row * a.ld + base;
         for (int k = 0; k < nch; ++k) {
           if (vi > 0) mbar_wait_bounded(&empty[k], par ^ 1u, s_abort);
-          const int n_k = min(kChunkElems, n_r - k * kChunkElems);
+          const int n_k = min(CH, n_r - k * CH);
           mbar_arrive_expect_tx(&full[k], (uint32_t)n_k * 2u);
-          bulk_g2s(slice + k * kChunkElems, src + k * kChunkElems, (uint32_t)n_k * 2u, &full[k]);
+          bulk_g2s(slice + k * CH, src + k * CH, (uint32_t)n_k * 2u, &full[k]);
         }
       }
       __syncwarp();
@@ -403,22 +429,22 @@ __global__ void __launch_bounds__((NCW + 1) * 32, C >= 4 ? 2 : 1) row_cluster_ke
       const int32_t y = tm.y;
       const bool ybad = y < 0 || (int64_t)y >= V;
 
-      // pass 1: log2-domain online (max, sum) over the slice, chunk by chunk as it lands
+      // pass 1: log2-domain (shift, sum) over the slice, chunk by chunk as it lands
       MS acc{-INFINITY, 0.f};
       for (int k = 0; k < nch; ++k) {
         mbar_wait_bounded(&full[k], par, s_abort);
-        const int nv = min(kChunkElems, n_r - k * kChunkElems) / 8;
-        const uint4* sv = reinterpret_cast<const uint4*>(slice + k * kChunkElems);
+        const int nv = min(CH, n_r - k * CH) / 8;
+        const uint4* sv = reinterpret_cast<const uint4*>(slice + k * CH);
         if (nv == VPT * NC) {  // full chunk: exactly VPT 16-byte vectors per consumer thread
           float x[VPT * 8];
 #pragma unroll
           for (int j = 0; j < VPT; ++j) unpack8_at(sv[ct + j * NC], x + 8 * j);
-          online2<VPT * 8>(acc, x);
+          lazy_online2<VPT * 8>(acc, x);
         } else {
           for (int v = ct; v < nv; v += NC) {
             float x[8];
             Vec<__nv_bfloat16>::unpack(sv[v], x);
-            online2<8>(acc, x);
+            lazy_online2<8>(acc, x);
           }
         }
       }
@@ -462,27 +488,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32, C >= 4 ? 2 : 1) row_cluster_ke
       }
       const float coef = o.coef;
       if (dz && coef != 0.f) {
-        // pass 2: |coef| * softmax = 2^(z log2e - (lse2 - log2|coef|)), sign applied to the
-        // packed bf16 pair; the target element coef * (p_y - 1) is computed on its own
+        // pass 2: |coef| * softmax = 2^(z log2e - (lse2 - log2|coef|)), the sign applied to
+        // the packed bf16 pairs; the target element coef * (p_y - 1) is written on its own
         const float cexp = lse2 - log2f(fabsf(coef));
-        const uint32_t sgn = coef < 0.f ? 0x80008000u : 0u;
-        for (int k = 0; k < nch; ++k) {
-          const int nv = min(kChunkElems, n_r - k * kChunkElems) / 8;
-          const uint4* sv = reinterpret_cast<const uint4*>(slice + k * kChunkElems);
-          uint4* dv = dz + k * (kChunkElems / 8);
-          if (nv == VPT * NC) {
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) dz_vec(sv[ct + j * NC], dv + ct + j * NC, cexp, sgn);
-          } else {
-            for (int v = ct; v < nv; v += NC) dz_vec(sv[v], dv + v, cexp, sgn);
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[k]);
-        }
-        // the target element, coef * (p_y - 1), overwrites the value the vector pass wrote
-        // (same thread, program order)
+        if (coef < 0.f)
+          pass2_slice<true, NC, VPT, CH>(slice, dz, n_r, nch, ct, lane, cexp, empty);
+        else
+          pass2_slice<false, NC, VPT, CH>(slice, dz, n_r, nch, ct, lane, cexp, empty);
+        // the target element overwrites what the vector pass wrote (same thread, program order)
         const int64_t yl = ybad ? -1 : (int64_t)y - base;
-        if (yl >= 0 && yl < n_r && ct == (int)(((yl / 8) % (kChunkElems / 8)) % NC)) {
+        if (yl >= 0 && yl < n_r && ct == (int)(((yl / 8) % (CH / 8)) % NC)) {
           const float dzy = coef * ex2(fmaf(zy, kLog2e, -lse2)) - coef;
           reinterpret_cast<__nv_bfloat16*>(dz)[yl] = __float2bfloat16_rn(dzy);
         }
@@ -507,13 +522,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, C >= 4 ? 2 : 1) row_cluster_ke
   if (tid == 32 && rank == 0) cnt.flush(a.acc);
 }
 
-template <int C, int NCW, int VPT>
+template <int C, int NCW, int VPT, int MINB>
 int launch_cluster(const RowArgs& a, cudaStream_t st) {
+  constexpr int CH = cluster_chunk_elems(NCW, VPT);
   const int Vs = cluster_slice_elems(a.V, C);
-  if ((Vs + cluster_chunk_elems(NCW, VPT) - 1) / cluster_chunk_elems(NCW, VPT) > kMaxChunks)
-    return GRPO_ERR_UNSUPPORTED;
+  if ((Vs + CH - 1) / CH > kMaxChunks) return GRPO_ERR_UNSUPPORTED;
   const size_t smem = cluster_smem_bytes(Vs, NCW);
-  auto kern = row_cluster_kernel<C, NCW, VPT>;
+  auto kern = row_cluster_kernel<C, NCW, VPT, MINB>;
   static int cached_dev = -1;
   static size_t cached_smem = 0;
   static int cached_clusters = 0;
@@ -594,18 +609,23 @@ extern "C" GRPO_API int grpo_logprob_loss_fwd_bwd(const void* logits, int32_t dt
   const bool vec = al16(logits) && (ld * es) % 16 == 0 &&
                    (!dlogits || (al16(dlogits) && (ld_out * es) % 16 == 0));
   if (dtype == GRPO_DTYPE_BF16) {
-    // Large bf16 vocabularies: rows split across a CTA cluster and staged in shared memory.
-    // GRPO_ROWPASS=l2|c2|c4 pins a variant (for measurements); the default is c2.
+    // Large bf16 vocabularies: rows split across a CTA cluster, slices staged in shared
+    // memory. Variants (cluster size, consumer warps, vectors per thread, CTAs per SM):
+    // c2 = (2, 16, 4, 1), c3 = (3, 8, 4, 2), c4 = (4, 8, 4, 2).
     const char* pin = getenv("GRPO_ROWPASS");
-    constexpr int ch2 = cluster_chunk_elems(16, 4), ch4 = cluster_chunk_elems(16, 2);
-    const bool cluster_ok = vec && V % 8 == 0 && V >= 16384 &&
-                            (cluster_slice_elems(V, 4) + ch4 - 1) / ch4 <= kMaxChunks &&
-                            cluster_smem_bytes(cluster_slice_elems(V, 4), 16) <= 227 * 1024;
+    const bool cluster_ok = vec && V % 8 == 0 && V >= 16384;
     if (cluster_ok && !(pin && strcmp(pin, "l2") == 0)) {
-      const bool fits2 = cluster_smem_bytes(cluster_slice_elems(V, 2), 16) <= 227 * 1024 &&
-                         (cluster_slice_elems(V, 2) + ch2 - 1) / ch2 <= kMaxChunks;
-      if (fits2 && !(pin && strcmp(pin, "c4") == 0)) return launch_cluster<2, 16, 4>(a, st);
-      return launch_cluster<4, 16, 2>(a, st);
+      const int64_t cap = 227 * 1024;
+      auto fits = [&](int C, int NCW, int minb) {
+        return (int64_t)cluster_smem_bytes(cluster_slice_elems(V, C), NCW) * minb <= cap &&
+               (cluster_slice_elems(V, C) + cluster_chunk_elems(NCW, 4) - 1) / cluster_chunk_elems(NCW, 4) <=
+                   kMaxChunks;
+      };
+      if (pin && strcmp(pin, "c3") == 0 && fits(3, 8, 2)) return launch_cluster<3, 8, 4, 2>(a, st);
+      if (pin && strcmp(pin, "c4") == 0 && fits(4, 8, 2)) return launch_cluster<4, 8, 4, 2>(a, st);
+      if (fits(2, 16, 1)) return launch_cluster<2, 16, 4, 1>(a, st);
+      if (fits(4, 8, 2)) return launch_cluster<4, 8, 4, 2>(a, st);
+      if (fits(4, 16, 1)) return launch_cluster<4, 16, 4, 1>(a, st);
     }
     if (V >= 8192) return launch_l2<__nv_bfloat16, 1024, 2>(a, vec, 1, st);
     return launch_l2<__nv_bfloat16, 128, 2>(a, vec, 16, st);

@@ -266,7 +266,7 @@ def test_invalid_arguments_rejected():
 
 # ---- the shared-memory cluster kernel and its variants ---------------------------------------
 
-VARIANTS = ["c2", "c4", "l2"]
+VARIANTS = ["c2", "c3", "c4", "l2"]
 
 
 @pytest.fixture
@@ -286,7 +286,7 @@ def test_cluster_variants_many_rows_with_masks(variant, V, rows, positions):
     _check_case(H.Case(wl), scale=1.0 / 333)
 
 
-@pytest.mark.parametrize("variant", ["c2", "c4"], indirect=True)
+@pytest.mark.parametrize("variant", ["c2", "c3", "c4"], indirect=True)
 def test_cluster_permutation_pad_rows_and_forward_only(variant):
     wl = W.make_workload("qwen_step", rows=8, len_lo=20, len_hi=40, V=16384, seed=21)
     case = H.Case(wl)
@@ -307,7 +307,7 @@ def test_cluster_permutation_pad_rows_and_forward_only(variant):
     assert torch.equal(loss2, loss) and torch.equal(logp2, logp)
 
 
-@pytest.mark.parametrize("variant", ["c2", "c4"], indirect=True)
+@pytest.mark.parametrize("variant", ["c2", "c3", "c4"], indirect=True)
 def test_cluster_nonfinite_row(variant):
     wl = W.make_workload("qwen_step", rows=4, len_lo=30, len_hi=40, V=16384, seed=22)
     case = H.Case(wl)
@@ -321,7 +321,7 @@ def test_cluster_nonfinite_row(variant):
     assert torch.all(dl == 0)
 
 
-@pytest.mark.parametrize("variant", ["c2", "c4"], indirect=True)
+@pytest.mark.parametrize("variant", ["c2", "c3", "c4"], indirect=True)
 def test_cluster_chunked_equals_unchunked_bitwise(variant):
     wl = W.make_workload("qwen_step", rows=8, len_lo=16, len_hi=40, V=32776, seed=23, mini=4, micro=1)
     case = H.Case(wl)
