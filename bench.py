@@ -346,6 +346,7 @@ def run_gb300(args):
     max_el, all_units = reduce_timing(elapsed, units, world, device)
     value = all_units / max_el
 
+    ahead = run_ahead(batch, stream, steps=min(args.steps, 30))
     e2e = run_e2e(batch, device, stream, steps=min(args.steps, args.e2e_steps))
 
     peak, peak_kind = hbm_peak()
@@ -369,6 +370,7 @@ def run_gb300(args):
                      "traffic": None if tpv is None else tpv * wl.n_valid / launches_per_step},
         "gpu_launches": launches,
         "e2e": e2e,
+        "ahead_pass": dict(ahead, frac=ahead["achieved_gbs"] / hbm_peak()[0]),
         "step_results": [{k: r[k] for k in ("loss", "n_valid", "clipfrac", "status")} for r in results],
     }
     if clk is not None:
@@ -384,6 +386,30 @@ def run_gb300(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def run_ahead(batch, stream, steps: int):
+    """The pi_old ahead pass: the same batch forward only (no dlogits), timed with CUDA events
+    around each row-pass launch. Algorithmic bytes: each valid token reads its logits row and
+    its side inputs and writes its log-prob and loss."""
+    import torch
+    evs = []
+    for _ in range(3):
+        batch.run(with_grad=False, stream=stream)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        batch.run(with_grad=False, stream=stream, launch_events=evs)
+    end.record(stream)
+    torch.cuda.synchronize()
+    wl = batch.wl
+    row_s = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+    idx = 8 if batch.tok_src is not None else 0
+    per_batch = wl.n_valid * (wl.V * wl.elem_bytes + 4 + 4 + 4 + 1 + 4 + 4 + idx)
+    return {"value": wl.n_valid * steps / (start.elapsed_time(end) / 1e3), "unit": UNIT,
+            "achieved_gbs": per_batch * steps / row_s / 1e9, "steps": steps,
+            "what": "forward-only row pass (pi_old ahead pass): log-prob and loss, no dlogits"}
 
 
 def _gpu_index(local: int) -> int:
