@@ -108,7 +108,7 @@ def test_compaction_worked_example():
     assert p.step_valid_tokens == [13 * 1024]
     # global_valid_seqs counts rows, so under compaction it exceeds the rollout count
     assert p.step_valid_rows == [13] and 13 > cfg.batch
-    # a pad row copies its group's first real row (reading: the page says "a real row")
+    # a pad row copies its group's first real row (reading: the page leaves open which one)
     off = 0
     for tot in ex["group_rows"]:
         for j in range(off, off + tot):
