@@ -27,6 +27,7 @@
 #ifndef GRPO_H_
 #define GRPO_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -119,9 +120,13 @@ typedef struct grpo_plan {
  *  row_len[i]   logits rows (tokens) of input row i        host [n_rows_in]
  *  row_valid[i] mask = 1 positions of input row i          host [n_rows_in], 0 <= valid <= len
  *  seg_counts   rows produced by each rollout              host [n_rollouts], compaction only
- * Fixed mode: chunks of `micro` consecutive rows. Dynamic: bins as defined in the design
- * notes (longest-processing-time greedy under the token budget). Compaction: each group
- * padded to a multiple of Q with copies of its first real row.
+ * Fixed mode: chunks of `micro` consecutive rows. Dynamic (inside each mini-batch):
+ * k = max(ceil(sum L / max_token_len), min_bins, 1) rounded up to bin_multiple, capped at the
+ * row count; rows visited by (workload desc, length desc, index asc) go to the feasible bin
+ * (tokens + L <= max_token_len) with the least (workload, tokens, index), k growing to the
+ * next multiple when none fits; rows by index inside a bin, bins by first row, or with
+ * balance_ends the ascending (workload, first row) order dealt to positions 0, k-1, 1, ...
+ * Compaction: each group padded to a multiple of Q with copies of its first real row.
  * Errors: GRPO_ERR_INVALID, _DIVISIBILITY, _ROLLOUT_COUNT, _TOKEN_BUDGET, _INCOMPATIBLE,
  * _CAPACITY. */
 GRPO_API int grpo_plan_microbatches(const grpo_plan_cfg* cfg, int32_t n_rollouts,
@@ -184,8 +189,8 @@ typedef struct grpo_step_acc {
 
 /* One chunk of the step: per token row t of `logits`
  * ("Sizing mini-batches and micro-batches", "The problem", "The hard part: deferred
- * normalization", "pi_old must be frozen across the window"; clip reading as in the
- * design notes):
+ * normalization", "pi_old must be frozen across the window"; the pages name an epsilon
+ * clip without printing it, read here as the standard symmetric PPO clip):
  *   LSE = log sum_v exp(z_v); logp = z_y - LSE; r = exp(logp - old) (1 if old_logp NULL)
  *   loss_t = m * -min(r*A, clip(r, 1-eps, 1+eps)*A)
  *   dlogits_t = grad_scale * m * A * r * g * (softmax(z) - onehot(y)),
@@ -234,6 +239,36 @@ GRPO_API int grpo_finish_step(grpo_step_acc* acc, const float* loss_tok, int64_t
                               int64_t expected_N, int32_t deferred, void* const* grad_bufs,
                               const int64_t* grad_numels, const int32_t* grad_dtypes,
                               int32_t n_bufs, grpo_step_result* result_host, void* stream);
+
+/* ---- fused LM-head variant ---------------------------------------------------------------- */
+
+/* Bytes of device workspace grpo_lmhead_loss_fwd_bwd needs for [T, H] hidden states and a
+ * [V, H] output embedding: per-(token, 256-wide vocabulary tile) softmax partials, per-token
+ * LSE and coefficients, and one bf16 dlogits chunk of 16384 vocabulary columns. 0 on bad sizes. */
+GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H);
+
+/* The same loss with the logits produced on the tensor cores: z = h W^T, computed tile by tile
+ * and consumed by the softmax in the GEMM epilogue, so the [T, V] logits are never stored
+ * ("Sizing mini-batches and micro-batches", "The problem"). Forward: LSE, log-prob, ratio,
+ * clipped surrogate, per-token loss (as grpo_logprob_loss_fwd_bwd, one token per row of h).
+ * Backward: the logits of each vocabulary chunk are recomputed, dlogits written to the
+ * workspace chunk, then d_h = dlogits W (accumulated over chunks) and dW = dlogits^T h.
+ *  h          device bf16 [T, H] row-major, 16-byte aligned; H a multiple of 64
+ *  W          device bf16 [V, H] row-major, 16-byte aligned
+ *  target, old_logp (or NULL), adv_tok, mask   device, indexed by token row
+ *  grad_scale 1/max(N,1) (or 1 with a deferred finish on d_h / dW)
+ *  d_h        device float [T, H] or NULL; dW device float [V, H] or NULL (both NULL: forward only)
+ *  loss_tok, logp_tok (or NULL)  device float [T]
+ *  acc        device grpo_step_acc (counts as in grpo_logprob_loss_fwd_bwd)
+ *  workspace  device, >= grpo_lmhead_workspace_size(T, V, H) bytes, caller-owned
+ * Errors: GRPO_ERR_INVALID (sizes, NULL, alignment), GRPO_ERR_CAPACITY (workspace too small),
+ * GRPO_ERR_UNSUPPORTED (tensor-map creation), GRPO_ERR_CUDA. */
+GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, int64_t T, int64_t V, int64_t H,
+                                      const int32_t* target, const float* old_logp,
+                                      const float* adv_tok, const uint8_t* mask, float clip_eps,
+                                      float grad_scale, float* d_h, float* dW, float* loss_tok,
+                                      float* logp_tok, grpo_step_acc* acc, void* workspace,
+                                      size_t workspace_bytes, void* stream);
 
 /* ---- misc -------------------------------------------------------------------------------- */
 

@@ -24,7 +24,7 @@ Sources, cited by page title and section:
   compaction rejects sequence packing, dynamic batching and the interleaved pipeline;
   one optimizer step per training step.
 
-Readings where the pages are silent (each also listed in the design notes):
+Readings where the pages are silent:
 
 * fixed chunks are contiguous and unshuffled, in input order;
 * a pad row copies the input of its group's FIRST real row;

@@ -10,6 +10,8 @@ from ._lib import (  # noqa: F401
     GrpoError,
     grpo_finish_step,
     grpo_group_advantage,
+    grpo_lmhead_loss_fwd_bwd,
+    grpo_lmhead_workspace_size,
     grpo_logprob_loss_fwd_bwd,
     grpo_plan_microbatches,
     grpo_plan_token_index,

@@ -96,6 +96,11 @@ def _lib() -> C.CDLL:
                                               vp, vp]
     lib.grpo_finish_step.argtypes = [vp, vp, C.c_int64, C.c_int64, C.c_int32, C.POINTER(vp), _i64p,
                                      _i32p, C.c_int32, C.POINTER(grpo_step_result), vp]
+    lib.grpo_lmhead_workspace_size.argtypes = [C.c_int64, C.c_int64, C.c_int64]
+    lib.grpo_lmhead_workspace_size.restype = C.c_size_t
+    lib.grpo_lmhead_loss_fwd_bwd.argtypes = [vp, vp, C.c_int64, C.c_int64, C.c_int64, vp, vp, vp, vp, C.c_float,
+                                             C.c_float, vp, vp, vp, vp, vp, vp, C.c_size_t, vp]
+    lib.grpo_lmhead_loss_fwd_bwd.restype = C.c_int
     lib.grpo_status_string.argtypes = [C.c_int]
     lib.grpo_status_string.restype = C.c_char_p
     lib.grpo_version.argtypes = []
@@ -272,6 +277,24 @@ def grpo_finish_step(acc, loss_tok, n_tok: Optional[int] = None, expected_N: int
     if rc < 0 and rc not in (ERR_N_MISMATCH, ERR_KERNEL):
         raise GrpoError(rc, "grpo_finish_step")
     return res.as_dict() if sync else None
+
+
+def grpo_lmhead_workspace_size(T: int, V: int, H: int) -> int:
+    return int(_lib().grpo_lmhead_workspace_size(T, V, H))
+
+
+def grpo_lmhead_loss_fwd_bwd(h, W, target, old_logp, adv_tok, mask, clip_eps: float, grad_scale: float,
+                             d_h, dW, loss_tok, logp_tok, acc, workspace, stream=None) -> None:
+    """h [T, H] and W [V, H] bf16 device tensors; d_h / dW float32 or None; see grpo.h."""
+    T, H = h.shape
+    V = W.shape[0]
+    rc = _lib().grpo_lmhead_loss_fwd_bwd(_ptr(h), _ptr(W), T, V, H, _ptr(target), _ptr(old_logp),
+                                         _ptr(adv_tok), _ptr(mask), float(clip_eps), float(grad_scale),
+                                         _ptr(d_h), _ptr(dW), _ptr(loss_tok), _ptr(logp_tok), _ptr(acc),
+                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _stream(stream))
+    if rc != OK:
+        raise GrpoError(rc, "grpo_lmhead_loss_fwd_bwd")
 
 
 def new_step_acc(device="cuda"):

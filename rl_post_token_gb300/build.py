@@ -21,7 +21,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgrpo.so")
 
-SOURCES = ["grpo_plan.cpp", "grpo_rowpass.cu", "grpo_step.cu"]
+SOURCES = ["grpo_plan.cpp", "grpo_rowpass.cu", "grpo_step.cu", "grpo_lmhead.cu"]
+# cuBLAS serves the two plain backward GEMMs of the LM-head variant; the rpath lets the
+# library load (for its host-only entry points) before any framework has loaded cuBLAS.
+LINK = ["-lcublas", "-Xlinker", "-rpath=/usr/local/cuda/lib64"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -73,7 +76,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
     tmp = LIB + ".tmp"
-    cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+    cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, *LINK]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"linking failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")

@@ -1,0 +1,528 @@
+// Fused LM-head variant of the loss: the logits z = h W^T are produced on the tensor cores
+// tile by tile and consumed by the softmax in the GEMM epilogue, so the [T, V] logits never
+// reach memory ("Sizing mini-batches and micro-batches", "The problem": the log-softmax over
+// the vocabulary of 2048-token completions is what runs out of memory).
+//
+//  pass A  tcgen05 GEMM over all (128-token x 256-vocab) tiles; the epilogue reduces each
+//          tile row to a log2-domain (max, sum-exp) partial and picks up the target logit.
+//  reduce  per token: combine the partials in vocabulary order -> LSE, log-prob, ratio,
+//          clipped surrogate, gradient coefficient (same token epilogue as the row pass).
+//  pass B  per vocabulary chunk: the same GEMM recomputes the chunk's logits and its epilogue
+//          writes dlogits (bf16) into a bounded chunk workspace; then d_h += dz_c W_c and
+//          dW_c = dz_c^T h (plain GEMMs, cuBLAS, float32 outputs).
+//
+// GEMM kernel: persistent, one CTA per SM, 6 warps. Warp 0 issues TMA loads (128-byte
+// swizzled 128x64 h tiles and 256x64 W tiles) into a 4-stage shared-memory ring; warp 1 issues
+// tcgen05.mma (M=128, N=256, K=16, bf16 -> f32) into a double-buffered TMEM accumulator
+// (2 x 256 columns); warps 2-5 read the accumulator with tcgen05.ld (one TMEM lane = one token
+// row per thread) and run the epilogue while the next tile's MMAs proceed. Every mbarrier wait
+// is bounded and raises a flag instead of hanging.
+#include <cublas_v2.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "grpo_common.cuh"
+
+namespace grpo {
+namespace lmhead {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NTHREADS = 192;
+constexpr int TMEM_COLS = 2 * BN;  // two accumulators
+constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + 256;
+
+// Instruction descriptor of tcgen05.mma kind::f16: D f32, A and B bf16, both K-major,
+// N = 256, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+// Shared-memory matrix descriptor, K-major operand with 128-byte swizzle: rows of 128 bytes,
+// 8-row swizzle atoms 1024 bytes apart (stride byte offset), version 1, layout SWIZZLE_128B.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;              // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
+  d |= (uint64_t)1 << 46;              // descriptor version
+  d |= (uint64_t)2 << 61;              // SWIZZLE_128B
+  return d;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, bool accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(kIdesc), "r"((uint32_t)accum)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+// 32 consecutive accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct GemmArgs {
+  int64_t T, V, H;
+  int n_row_tiles;
+  int col_tile0, n_col_tiles;  // tiles [col_tile0, col_tile0 + n_col_tiles) of 256 columns
+  int mode;                    // 0: softmax partials; 1: dlogits
+  const int32_t* target;
+  // mode 0
+  float* part_m;  // [n_col_tiles_total][T] log2-domain max
+  float* part_s;  // [n_col_tiles_total][T]
+  float* zy;      // [T] target logit
+  // mode 1
+  const float* lse2;  // [T] LSE * log2(e)
+  const float* coef;  // [T] gradient coefficient (already scaled)
+  __nv_bfloat16* dz;  // chunk workspace [T][ldz], column 0 = vocabulary column v0
+  int64_t ldz, v0;
+  grpo_step_acc* acc;
+};
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w, GemmArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
+  uint64_t* full = reinterpret_cast<uint64_t*>(sgen + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;   // [2]
+  uint64_t* tempty = tfull + 2;       // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int n_tiles = g.n_row_tiles * g.n_col_tiles;
+  const int KB = (int)(g.H / BK);
+
+  if (warp == 0) {
+    // ---- TMA producer ----
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        const int rt = t % g.n_row_tiles, ct = g.col_tile0 + t / g.n_row_tiles;
+        for (int kb = 0; kb < KB; ++kb) {
+          mbar_wait_bounded(&empty[stage], phase ^ 1u, s_abort);
+          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+          tma_load_2d(sa, &map_h, smem_u32(&full[stage]), kb * BK, rt * BM);
+          tma_load_2d(sa + A_BYTES, &map_w, smem_u32(&full[stage]), kb * BK, ct * BN);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer ----
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, ab = 0, aphase = 0;
+      for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        mbar_wait_bounded(&tempty[ab], aphase ^ 1u, s_abort);
+        fence_after();
+        const uint32_t d = tmem + ab * BN;
+        for (int kb = 0; kb < KB; ++kb) {
+          mbar_wait_bounded(&full[stage], phase, s_abort);
+          fence_after();
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+          const uint64_t da = sdesc_sw128(sa), db = sdesc_sw128(sa + A_BYTES);
+#pragma unroll
+          for (int j = 0; j < BK / 16; ++j)  // +32 bytes along K per 16-element step
+            mma_bf16(d, da + 2 * j, db + 2 * j, kb > 0 || j > 0);
+          mma_commit(smem_u32(&empty[stage]));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        mma_commit(smem_u32(&tfull[ab]));
+        if (++ab == 2) {
+          ab = 0;
+          aphase ^= 1u;
+        }
+      }
+    }
+  } else {
+    // ---- epilogue: warps 2..5, thread = TMEM lane = token row of the tile ----
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int trow = quarter * 32 + lane;
+    uint32_t ab = 0, aphase = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+      const int rt = t % g.n_row_tiles, ct = g.col_tile0 + t / g.n_row_tiles;
+      mbar_wait_bounded(&tfull[ab], aphase, s_abort);
+      fence_after();
+      const int64_t row = (int64_t)rt * BM + trow;
+      const int64_t c0 = (int64_t)ct * BN;
+      const bool rok = row < g.T;
+      const int32_t y = rok ? g.target[row] : -1;
+      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + ab * BN;
+      if (g.mode == 0) {
+        MS acc{-INFINITY, 0.f};
+        float zy = 0.f;
+        const bool own = y >= c0 && y < c0 + BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(taddr + c * 32, v);
+          const int64_t cb = c0 + c * 32;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (cb + i >= g.V) v[i] = -INFINITY;  // zero-filled columns past the vocabulary
+          if (own && y >= cb && y < cb + 32) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (cb + i == y) zy = v[i];
+          }
+          lazy_online2<32>(acc, v);
+        }
+        if (rok) {
+          g.part_m[(int64_t)ct * g.T + row] = acc.m;
+          g.part_s[(int64_t)ct * g.T + row] = acc.s;
+          if (own) g.zy[row] = zy;
+        }
+      } else {
+        const float cf = rok ? g.coef[row] : 0.f;
+        const float l2 = rok ? g.lse2[row] : 0.f;
+        const float cexp = l2 - log2f(fabsf(cf));
+        const uint32_t sgn = cf < 0.f ? 0x80008000u : 0u;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(taddr + c * 32, v);
+          const int64_t cb = c0 + c * 32;
+          if (!rok || cb >= g.V) continue;
+          uint32_t w[16];
+          if (cf != 0.f) {
+            float zyv = 0.f;
+            const bool hit = y >= cb && y < cb + 32;
+            if (hit) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (cb + i == y) zyv = v[i];
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = ex2(fmaf(v[i], kLog2e, -cexp));
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]) ^ sgn;
+            if (hit) {
+              const float dzy = cf * ex2(fmaf(zyv, kLog2e, -l2)) - cf;
+              const uint32_t hb = __bfloat16_as_ushort(__float2bfloat16_rn(dzy));
+              const int k = (int)(y - cb);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                if (k == 2 * i) w[i] = (w[i] & 0xFFFF0000u) | hb;
+                if (k == 2 * i + 1) w[i] = (w[i] & 0x0000FFFFu) | (hb << 16);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = 0u;
+          }
+          __nv_bfloat16* dst = g.dz + row * g.ldz + (cb - g.v0);
+          const int nvalid = (int)std::min<int64_t>(32, g.V - cb);
+          if (nvalid == 32) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          } else {
+            for (int i = 0; i < nvalid; ++i)
+              dst[i] = __ushort_as_bfloat16((unsigned short)((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu)));
+          }
+        }
+      }
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[ab]);
+      if (++ab == 2) {
+        ab = 0;
+        aphase ^= 1u;
+      }
+    }
+  }
+
+  fence_before();
+  __syncthreads();
+  if (*s_abort && threadIdx.x == 0) atomicOr(&g.acc->flags, kFlagWaitTimeout);
+  if (warp == 1) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+// Per token: combine the vocabulary-tile partials in order, then the token epilogue.
+__global__ void reduce_kernel(int64_t T, int n_col_tiles, const float* __restrict__ part_m,
+                              const float* __restrict__ part_s, const float* __restrict__ zy,
+                              const int32_t* __restrict__ target, int64_t V, const float* old_logp,
+                              const float* __restrict__ adv, const uint8_t* __restrict__ mask, float eps,
+                              float scale, float* __restrict__ lse2_out, float* __restrict__ coef_out,
+                              float* loss_tok, float* logp_tok, grpo_step_acc* acc) {
+  __shared__ unsigned long long sc[4];
+  if (threadIdx.x < 4) sc[threadIdx.x] = 0;
+  __syncthreads();
+  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  unsigned long long v_valid = 0, v_clip = 0, v_nf = 0, v_tok = 0;
+  if (row < T) {
+    v_tok = 1;
+    float coef = 0.f, l2 = 0.f;
+    if (mask[row]) {
+      MS t{-INFINITY, 0.f};
+      for (int c = 0; c < n_col_tiles; ++c) t = ms2_combine(t, MS{part_m[(int64_t)c * T + row], part_s[(int64_t)c * T + row]});
+      l2 = t.m + log2f(t.s);
+      const int32_t y = target[row];
+      const float z = (y >= 0 && (int64_t)y < V) ? zy[row] : __int_as_float(0x7fc00000);
+      const TokenOut o = token_epilogue(z, l2 * kLn2, old_logp != nullptr, old_logp ? old_logp[row] : 0.f,
+                                        adv[row], eps, scale);
+      loss_tok[row] = o.loss;
+      if (logp_tok) logp_tok[row] = o.logp;
+      coef = o.coef;
+      v_valid = 1;
+      v_clip = o.clipped;
+      v_nf = o.nonfinite;
+    } else {
+      loss_tok[row] = 0.f;
+      if (logp_tok) logp_tok[row] = 0.f;
+    }
+    lse2_out[row] = l2;
+    coef_out[row] = coef;
+  }
+  if (v_tok) atomicAdd(&sc[0], v_tok);
+  if (v_valid) atomicAdd(&sc[1], v_valid);
+  if (v_clip) atomicAdd(&sc[2], v_clip);
+  if (v_nf) atomicAdd(&sc[3], v_nf);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (sc[0]) atomicAdd(reinterpret_cast<unsigned long long*>(&acc->n_tokens), sc[0]);
+    if (sc[1]) atomicAdd(reinterpret_cast<unsigned long long*>(&acc->n_valid), sc[1]);
+    if (sc[2]) atomicAdd(reinterpret_cast<unsigned long long*>(&acc->n_clipped), sc[2]);
+    if (sc[3]) atomicAdd(reinterpret_cast<unsigned long long*>(&acc->n_nonfinite), sc[3]);
+  }
+}
+
+// ---- host -------------------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major [rows, cols] bf16 matrix, box [box_rows, 64] with 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cublasHandle_t blas_handle() {
+  static cublasHandle_t h[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!h[dev] && cublasCreate(&h[dev]) != CUBLAS_STATUS_SUCCESS) h[dev] = nullptr;
+  return h[dev];
+}
+
+}  // namespace lmhead
+}  // namespace grpo
+
+using namespace grpo;
+using namespace grpo::lmhead;
+
+namespace {
+
+struct WsLayout {
+  size_t part_m, part_s, zy, lse2, coef, dz, total;
+  int n_col_tiles;
+  int64_t vchunk;
+};
+
+WsLayout ws_layout(int64_t T, int64_t V, int64_t vchunk) {
+  WsLayout w{};
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  w.n_col_tiles = (int)((V + BN - 1) / BN);
+  w.vchunk = std::min<int64_t>(vchunk, (int64_t)w.n_col_tiles * BN);
+  size_t off = 0;
+  w.part_m = off; off += up((size_t)w.n_col_tiles * T * 4);
+  w.part_s = off; off += up((size_t)w.n_col_tiles * T * 4);
+  w.zy = off; off += up((size_t)T * 4);
+  w.lse2 = off; off += up((size_t)T * 4);
+  w.coef = off; off += up((size_t)T * 4);
+  w.dz = off; off += up((size_t)T * w.vchunk * 2);
+  w.total = off;
+  return w;
+}
+
+constexpr int64_t kDefaultVChunk = 16384;  // vocabulary columns per pass-B chunk (64 tiles)
+
+}  // namespace
+
+extern "C" GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H) {
+  if (T <= 0 || V <= 0 || H <= 0) return 0;
+  return ws_layout(T, V, kDefaultVChunk).total;
+}
+
+extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, int64_t T, int64_t V, int64_t H,
+                                                 const int32_t* target, const float* old_logp,
+                                                 const float* adv_tok, const uint8_t* mask, float clip_eps,
+                                                 float grad_scale, float* d_h, float* dW, float* loss_tok,
+                                                 float* logp_tok, grpo_step_acc* acc, void* workspace,
+                                                 size_t workspace_bytes, void* stream) {
+  if (T < 0 || V < 1 || H < BK || H % BK != 0 || !acc) return GRPO_ERR_INVALID;
+  if (T == 0) return GRPO_OK;
+  if (!h || !W || !target || !adv_tok || !mask || !loss_tok || !workspace) return GRPO_ERR_INVALID;
+  if (((uintptr_t)h | (uintptr_t)W) & 15u) return GRPO_ERR_INVALID;
+  if (T > INT32_MAX / 2 || V > INT32_MAX / 2) return GRPO_ERR_INVALID;
+  const WsLayout ws = ws_layout(T, V, kDefaultVChunk);
+  if (workspace_bytes < ws.total) return GRPO_ERR_CAPACITY;
+  const cudaStream_t st = as_stream(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  float* part_m = reinterpret_cast<float*>(wsb + ws.part_m);
+  float* part_s = reinterpret_cast<float*>(wsb + ws.part_s);
+  float* zy = reinterpret_cast<float*>(wsb + ws.zy);
+  float* lse2 = reinterpret_cast<float*>(wsb + ws.lse2);
+  float* coef = reinterpret_cast<float*>(wsb + ws.coef);
+  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(wsb + ws.dz);
+
+  CUtensorMap map_h, map_w;
+  if (!make_map(&map_h, h, (uint64_t)T, (uint64_t)H, BM) || !make_map(&map_w, W, (uint64_t)V, (uint64_t)H, BN))
+    return GRPO_ERR_UNSUPPORTED;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  GRPO_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    GRPO_CUDA_TRY(cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES));
+    attr_set[dev] = true;
+  }
+  const int n_row_tiles = (int)((T + BM - 1) / BM);
+
+  GemmArgs g{};
+  g.T = T;
+  g.V = V;
+  g.H = H;
+  g.n_row_tiles = n_row_tiles;
+  g.target = target;
+  g.part_m = part_m;
+  g.part_s = part_s;
+  g.zy = zy;
+  g.lse2 = lse2;
+  g.coef = coef;
+  g.dz = dz;
+  g.ldz = ws.vchunk;
+  g.acc = acc;
+
+  // pass A: softmax partials over every vocabulary tile
+  g.mode = 0;
+  g.col_tile0 = 0;
+  g.n_col_tiles = ws.n_col_tiles;
+  {
+    const int grid = (int)std::min<int64_t>((int64_t)n_row_tiles * ws.n_col_tiles, sm_count());
+    gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(map_h, map_w, g);
+    GRPO_CUDA_TRY(cudaGetLastError());
+  }
+  reduce_kernel<<<(unsigned)((T + 255) / 256), 256, 0, st>>>(T, ws.n_col_tiles, part_m, part_s, zy, target, V,
+                                                              old_logp, adv_tok, mask, clip_eps, grad_scale, lse2,
+                                                              coef, loss_tok, logp_tok, acc);
+  GRPO_CUDA_TRY(cudaGetLastError());
+  if (!d_h && !dW) return GRPO_OK;
+
+  // pass B: per vocabulary chunk, dlogits into the workspace, then the two backward GEMMs
+  cublasHandle_t bh = blas_handle();
+  if (!bh || cublasSetStream(bh, st) != CUBLAS_STATUS_SUCCESS) return GRPO_ERR_CUDA;
+  const int tiles_per_chunk = (int)(ws.vchunk / BN);
+  const float one = 1.f, zero = 0.f;
+  for (int ct0 = 0, c = 0; ct0 < ws.n_col_tiles; ct0 += tiles_per_chunk, ++c) {
+    const int nct = std::min(tiles_per_chunk, ws.n_col_tiles - ct0);
+    const int64_t v0 = (int64_t)ct0 * BN;
+    const int64_t vc = std::min<int64_t>((int64_t)nct * BN, V - v0);
+    g.mode = 1;
+    g.col_tile0 = ct0;
+    g.n_col_tiles = nct;
+    g.v0 = v0;
+    const int grid = (int)std::min<int64_t>((int64_t)n_row_tiles * nct, sm_count());
+    gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(map_h, map_w, g);
+    GRPO_CUDA_TRY(cudaGetLastError());
+    const __nv_bfloat16* Wc = static_cast<const __nv_bfloat16*>(W) + v0 * H;
+    // d_h[T,H] (+)= dz[T,vc] W_c[vc,H]   (column-major view: d_h^T = W_c^T dz^T)
+    if (d_h &&
+        cublasGemmEx(bh, CUBLAS_OP_N, CUBLAS_OP_N, (int)H, (int)T, (int)vc, &one, Wc, CUDA_R_16BF, (int)H, dz,
+                     CUDA_R_16BF, (int)ws.vchunk, c == 0 ? &zero : &one, d_h, CUDA_R_32F, (int)H,
+                     CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+      return GRPO_ERR_CUDA;
+    // dW_c[vc,H] = dz^T[vc,T] h[T,H]   (column-major view: dW_c^T = h^T dz)
+    if (dW && cublasGemmEx(bh, CUBLAS_OP_N, CUBLAS_OP_T, (int)H, (int)vc, (int)T, &one, h, CUDA_R_16BF, (int)H, dz,
+                           CUDA_R_16BF, (int)ws.vchunk, &zero, dW + v0 * H, CUDA_R_32F, (int)H, CUBLAS_COMPUTE_32F,
+                           CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+      return GRPO_ERR_CUDA;
+  }
+  return GRPO_OK;
+}

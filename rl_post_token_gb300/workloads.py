@@ -157,6 +157,9 @@ def make_workload(name: str, seed: int = 0, old_sigma: float = 0.05, **ov) -> Wo
         Lrow = ov.get("row_tokens", 2048)
         V = ov.get("V", V_QWEN)
         row_len = np.full(B, Lrow, np.int32)
+        if "tokens" in ov:  # T tokens over B rows, the last row taking the remainder
+            row_len[:] = ov["tokens"] // B
+            row_len[-1] = ov["tokens"] - (B - 1) * (ov["tokens"] // B)
         plan = dict(batch=B, mini=0, micro=0, group_size=4)
         wl = _finish(name, seed, rng, V, "bf16", 0.0, 4, plan, row_len, row_len, 0.3, B, old_sigma)
         wl.extra.update(H=ov.get("H", 2048), h_std=1.0, w_std=0.02)
@@ -208,3 +211,27 @@ def logits_to_host(t) -> np.ndarray:
     if t.dtype == torch.bfloat16:
         return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
     return t.contiguous().cpu().numpy()
+
+
+def make_lmhead_inputs(wl: Workload, device="cpu"):
+    """Hidden states h [T, H] ~ N(0, 1) and output embedding W [V, H] ~ N(0, 0.02), bf16, as
+    torch tensors on ``device`` (numpy when small, a seeded device generator when large)."""
+    import torch
+
+    T, V, H = wl.T, wl.V, wl.extra["H"]
+    out = []
+    for k, (rows, std) in enumerate([(T, wl.extra["h_std"]), (V, wl.extra["w_std"])]):
+        if rows * H <= HOST_LOGITS_MAX_ELEMS:
+            rng = np.random.default_rng(wl.seed + 11 + k)
+            bits = bf16_round_bits(rng.standard_normal((rows, H), dtype=np.float32) * np.float32(std))
+            out.append(torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(device))
+        else:
+            g = torch.Generator(device=device)
+            g.manual_seed(wl.seed + 11 + k)
+            t = torch.empty((rows, H), dtype=torch.bfloat16, device=device)
+            blk = max(1, (256 * 1024 * 1024) // (4 * H))
+            for a in range(0, rows, blk):
+                b = min(rows, a + blk)
+                t[a:b].copy_(torch.randn((b - a, H), generator=g, device=device) * std)
+            out.append(t)
+    return out[0], out[1]

@@ -1,6 +1,8 @@
 """Shared test-side helpers for the GPU parity tests (test infrastructure; imports the oracle).
 
-Tolerances (the loss and dlogits bars; derivation in the design notes):
+Tolerances (the loss and dlogits bars; ex2.approx is within 2^-22 relative, the exponent
+argument (z - LSE) log2(e) carries <= |z - LSE| 2^-24 log2(e), the float32 LSE ~1e-6, bf16
+rounding 2^-9):
 * log-prob:   |d| <= 1e-5 * max(1, |ref|)
 * token loss: |d| <= 1e-5 * |ref| + 1e-7 * |A|
 * step loss:  |d| <= 1e-5 * max(|L_ref|, sum|m * l| / N)

@@ -1,0 +1,114 @@
+"""GPU parity of the fused LM-head variant (tcgen05 GEMM + softmax epilogue) against the
+float64 oracle: per-token loss and log-prob, d_h and dW, on sizes with ragged token and
+vocabulary tiles, several vocabulary chunks, masked tokens and forward-only calls.
+
+d_h and dW tolerance: both products are formed from bf16 dlogits (rounded to nearest), so
+each element may move by up to ~2^-8 of the sum of the magnitudes of its terms; the bar is
+|d| <= 8e-3 * (|dz| |W|)_ij (resp. (|dz|^T |h|)_ij) + 1e-12."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import advantage as OA
+from oracle import loss as OL
+from rl_post_token_gb300 import _lib
+from rl_post_token_gb300 import workloads as W
+
+from tests import _gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(grpo_lib):
+    assert torch.cuda.is_available()
+    return grpo_lib
+
+
+def _case(T, V, Hd, seed, valid_lo=None, old=True, adv=None):
+    wl = W.make_workload("lmhead", seed=seed, rows=4, tokens=T, V=V, H=Hd)
+    assert wl.T == T, (wl.T, T)
+    h, Wt = W.make_lmhead_inputs(wl, DEV)
+    hb = h.view(torch.int16).cpu().numpy().view(np.uint16)
+    wb = Wt.view(torch.int16).cpu().numpy().view(np.uint16)
+    mask = wl.mask.copy()
+    if valid_lo is not None:
+        mask[np.random.default_rng(seed).random(T) < valid_lo] = 0
+    a_tok = OA.broadcast_to_tokens(OA.group_advantage(wl.rewards, wl.group_size, np.float32(1e-6)),
+                                   wl.row_rollout, wl.row_len) if adv is None else adv.astype(np.float32)
+    old_logp = None
+    if old:
+        z = OL.as_f64(hb) @ OL.as_f64(wb).T
+        ref = np.array([OL.log_softmax_row(z[t])[wl.target[t]] for t in range(T)])
+        old_logp = (ref + wl.old_noise).astype(np.float32)
+    return wl, h, Wt, hb, wb, mask, a_tok, old_logp
+
+
+def _run(h, Wt, wl, mask, a_tok, old_logp, scale, grads=True):
+    T, Hd = h.shape
+    V = Wt.shape[0]
+    d_h = torch.full((T, Hd), 7.0, device=DEV) if grads else None
+    dW = torch.full((V, Hd), 7.0, device=DEV) if grads else None
+    loss = torch.full((T,), -7.0, device=DEV)
+    logp = torch.full((T,), -7.0, device=DEV)
+    acc = _lib.new_step_acc(DEV)
+    ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=DEV)
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, t(wl.target), t(old_logp), t(a_tok), t(mask), wl.eps, scale,
+                                  d_h, dW, loss, logp, acc, ws)
+    torch.cuda.synchronize()
+    return d_h, dW, loss, logp, acc
+
+
+def _check(T, V, Hd, seed, valid_lo=None, old=True, adv=None, grads=True):
+    wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed, valid_lo, old, adv)
+    N = max(int(mask.sum()), 1)
+    d_h, dW, loss, logp, acc = _run(h, Wt, wl, mask, a_tok, old_logp, 1.0 / N, grads)
+    ref = OL.lmhead_fwd_bwd(hb, wb, wl.target, old_logp, a_tok, mask, wl.eps, scale=1.0 / N)
+    H.assert_tokens_close(H.to_f64(loss), H.to_f64(logp), ref, a_tok, mask)
+    res = _lib.grpo_finish_step(acc, loss, expected_N=int(mask.sum()))
+    assert res["status"] == 0 and res["kernel_flags"] == 0
+    if not grads:
+        return ref
+    # tolerance from the magnitudes of the terms of each product
+    hf, wf = OL.as_f64(hb), OL.as_f64(wb)
+    z = hf @ wf.T
+    dz_abs = np.zeros_like(z)
+    for t in range(T):
+        if mask[t]:
+            dz_abs[t] = np.abs(OL.token_objective(z[t], int(wl.target[t]), None if old_logp is None else old_logp[t],
+                                                  a_tok[t], 1, wl.eps, 1.0 / N)[4])
+    tol_h = 8e-3 * (dz_abs @ np.abs(wf)) + 1e-12
+    tol_w = 8e-3 * (dz_abs.T @ np.abs(hf)) + 1e-12
+    gh, gw = H.to_f64(d_h), H.to_f64(dW)
+    bad_h = np.abs(gh - ref["d_h"]) > tol_h
+    bad_w = np.abs(gw - ref["dW"]) > tol_w
+    assert not bad_h.any(), (np.argwhere(bad_h)[:3], gh[bad_h][:3], ref["d_h"][bad_h][:3])
+    assert not bad_w.any(), (np.argwhere(bad_w)[:3], gw[bad_w][:3], ref["dW"][bad_w][:3])
+    return ref
+
+
+def test_lmhead_exact_tiles():
+    _check(256, 1024, 128, seed=1)
+
+
+def test_lmhead_ragged_tokens_vocab_and_k():
+    # 300 tokens (ragged 128-row tile), V = 1000 (ragged 256-column tile and 32-column group),
+    # H = 192 (three 64-wide K blocks)
+    _check(300, 1000, 192, seed=2)
+
+
+def test_lmhead_several_vocab_chunks_masked_tokens():
+    # V > 16384: two dlogits chunks, the second ragged; a quarter of the tokens masked
+    _check(128, 20000, 64, seed=3, valid_lo=0.25)
+
+
+def test_lmhead_no_pi_old_and_clip_stress():
+    T = 256
+    adv = np.random.default_rng(4).choice([-2.0, -0.5, 0.5, 2.0], T)
+    _check(T, 2048, 128, seed=4, old=False, adv=adv)
+
+
+def test_lmhead_forward_only():
+    _check(256, 4096, 256, seed=5, grads=False)

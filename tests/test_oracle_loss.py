@@ -160,3 +160,41 @@ def test_deferred_normalisation_linearity():
 def test_all_empty_step_is_zero_not_nan():
     fin = L.finish_step(np.zeros(5), np.zeros(5, np.uint8))
     assert fin["loss"] == 0.0 and fin["n_valid"] == 0
+
+
+def test_lmhead_oracle_matches_chain_rule():
+    # d_h and dW follow from dlogits by the chain rule of z = h W^T; pinned by central
+    # differences of the step loss with respect to h and W on a tiny problem
+    rng = np.random.default_rng(31)
+    T, H, V = 5, 6, 7
+    h = rng.normal(0, 1, (T, H))
+    W = rng.normal(0, 0.5, (V, H))
+    y = rng.integers(0, V, T)
+    A = rng.choice([-1.0, 0.5, 2.0], T)
+    m = np.array([1, 1, 0, 1, 1], np.uint8)
+    z = h @ W.T
+    lsm = np.array([sps.log_softmax(z[t])[y[t]] for t in range(T)])
+    old = lsm - np.log(rng.choice([0.9, 1.05, 1.1], T))
+    N = int(m.sum())
+    out = L.lmhead_fwd_bwd(h, W, y, old, A, m, EPS, scale=1.0 / N)
+
+    def f(hh, WW):
+        zz = hh @ WW.T
+        return sum(L.token_objective(zz[t], int(y[t]), old[t], A[t], int(m[t]), EPS, want_grad=False)[0]
+                   for t in range(T)) / N
+
+    eps_fd = 1e-6
+    for (i, j) in [(0, 0), (1, 3), (4, 5), (3, 2)]:
+        hp, hm = h.copy(), h.copy()
+        hp[i, j] += eps_fd
+        hm[i, j] -= eps_fd
+        assert out["d_h"][i, j] == pytest.approx((f(hp, W) - f(hm, W)) / (2 * eps_fd), rel=1e-5, abs=1e-9)
+    for (i, j) in [(0, 0), (6, 5), (3, 1), (2, 4)]:
+        Wp, Wm = W.copy(), W.copy()
+        Wp[i, j] += eps_fd
+        Wm[i, j] -= eps_fd
+        assert out["dW"][i, j] == pytest.approx((f(h, Wp) - f(h, Wm)) / (2 * eps_fd), rel=1e-5, abs=1e-9)
+    # the vocabulary sum of dW vanishes (each dlogits row sums to zero)
+    assert np.allclose(out["dW"].sum(0), 0, atol=1e-12)
+    # the masked token's hidden row gets no gradient
+    assert np.all(out["d_h"][2] == 0)
