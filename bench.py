@@ -42,6 +42,8 @@ WORKLOAD_TEXT = {
     "compaction": "context compaction: 3 prompts x 2 generations, segments {1,3},{2,5},{1,1}, 1024-token "
                   "rows, Q=4 -> 16 rows incl. 3 pad rows, V=151936 bf16, one step",
     "tiny": "tiny oracle check: 8 prompts x 4 rollouts, 64 positions, V=512 f32, mini 16, micro 8",
+    "lmhead": "fused LM-head: hidden [16384, 2048] bf16 ~N(0,1) x W [151936, 2048] bf16 ~N(0,0.02), "
+              "tcgen05 GEMM chunked over V feeding the online softmax, d_hidden and dW outputs (f32)",
 }
 
 
@@ -75,6 +77,16 @@ def barrier(world: int, device=None):
 
 
 # ---- peaks, clocks, profiles --------------------------------------------------------------------
+
+def bf16_peak(sustained: bool = True):
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained" if sustained else "bf16_tflops"]), "measured"
+    except Exception:
+        return (1700.0 if sustained else 1900.0), "fallback"
+
 
 def hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -285,6 +297,90 @@ class Batch:
         return valid * (2 * rowb + 4 + 4 + 4 + 1 + 4 + 4 + idx) + masked * (rowb + 1 + idx)
 
 
+def run_lmhead(args):
+    """Fused LM-head step: advantage, one grpo_lmhead_loss_fwd_bwd call (forward, recompute,
+    dlogits chunks, d_h and dW), the finish. Roofline: tensor, 6*T*V*H algorithmic flops
+    (forward GEMM and the two backward GEMMs; the recompute is not credited)."""
+    import torch
+    from rl_post_token_gb300 import build as B
+    from rl_post_token_gb300 import _lib
+    from rl_post_token_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if rank == 0:
+        B.build()
+    _lib.lib()
+    wl = W.make_workload("lmhead", seed=rank)
+    T, V, Hd = wl.T, wl.V, wl.extra["H"]
+    h, Wt = W.make_lmhead_inputs(wl, device)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    target, mask, rewards = t(wl.target), t(wl.mask), t(wl.rewards)
+    adv_r = torch.empty_like(rewards)
+    adv = torch.empty(T, device=device)
+    row_tok_off, row_rollout = t(wl.tok_off), t(wl.row_rollout)
+    d_h = torch.empty((T, Hd), device=device)
+    dW = torch.empty((V, Hd), device=device)
+    loss = torch.empty(T, device=device)
+    logp = torch.empty(T, device=device)
+    acc = _lib.new_step_acc(device)
+    ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    N = wl.n_valid
+
+    def step(grads=True, old=None):
+        _lib.grpo_group_advantage(rewards, wl.group_size, 1e-6, True, adv_r, row_rollout, row_tok_off, adv)
+        _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, target, old, adv, mask, wl.eps, 1.0 / max(N, 1),
+                                      d_h if grads else None, dW if grads else None, loss, logp, acc, ws)
+        _lib.grpo_finish_step(acc, loss, expected_N=N, sync=False)
+
+    step(grads=False)  # pi_old by the ahead pass, then seeded noise
+    old = logp + t(wl.old_noise)
+    for _ in range(max(args.warmup, 3)):
+        step(old=old)
+    torch.cuda.synchronize(device)
+    out_dir = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp"
+    clocks = ClockSampler(_gpu_index(local), os.path.join(out_dir, f"clocks_lmhead_rank{rank}.csv"))
+    time.sleep(0.5)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(old=old)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    full_s = e0.elapsed_time(e1) / 1e3 / args.steps
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        step(grads=False, old=old)
+    f1.record(stream)
+    torch.cuda.synchronize(device)
+    fwd_s = f0.elapsed_time(f1) / 1e3 / args.steps
+    clk = clocks.stop()
+    res = _lib.read_step_result(acc)
+    flops = 6.0 * T * V * Hd
+    peak, kind = bf16_peak(sustained=True)
+    line = {
+        "metric": "GRPO loss fwd+bwd valid tokens/s, fused LM-head (V=151936, H=2048, bf16)",
+        "value": N / full_s, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": 1e3 * full_s, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT["lmhead"], "tokens": T, "vocab": V, "hidden": Hd,
+                   "l2": "weights 622 MB + hidden 64 MB read per step, larger than L2; no flush"},
+        "roofline": {"bound": "tensor", "achieved": flops / full_s / 1e12, "peak": peak, "unit": "TFLOP/s",
+                     "frac": flops / full_s / 1e12 / peak, "peak_source": f"{kind} bf16_tflops_sustained",
+                     "flops_per_step": flops, "traffic": None},
+        "forward_only": {"ms": 1e3 * fwd_s, "tflops": 2.0 * T * V * Hd / fwd_s / 1e12,
+                         "what": "softmax-partials GEMM pass + per-token reduce (2*T*V*H flops)"},
+        "step_result": {k: res[k] for k in ("loss", "n_valid", "clipfrac", "status")},
+    }
+    if clk is not None:
+        line["clocks"] = clk
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_gb300(args):
     import torch
 
@@ -480,6 +576,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "lmhead":
+        return run_lmhead(args)
     return run_gb300(args)
 
 
