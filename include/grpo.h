@@ -270,6 +270,35 @@ GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, int64_t T, i
                                       float* logp_tok, grpo_step_acc* acc, void* workspace,
                                       size_t workspace_bytes, void* stream);
 
+/* Allocation-free forward pass of the fused LM-head variant. The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory when they need the
+ * loss -- a serving or scoring process whose device memory is all handed to its own pool (a
+ * KV cache or caching allocator), where a new cudaMalloc would fail or force the pool to
+ * shrink, or a code path that must not risk the device synchronisation cudaMalloc/cudaFree
+ * can cause. It computes what grpo_lmhead_loss_fwd_bwd computes with d_h = dW = NULL
+ * (per-token loss and log-prob, counts in acc) and calls no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *  - Its scratch is a 16 MiB file-scope device array inside this library
+ *    (grpo_lmhead_forward_noalloc_max_scratch() bytes); every GPU that loads the library holds
+ *    it until the process exits.
+ *  - Limit: 4*T*(2*ceil(V/256) + 3) bytes (each part rounded up to 256) must fit the array,
+ *    e.g. about 3,500 tokens at V = 151936; larger calls return GRPO_ERR_CAPACITY and launch
+ *    nothing.
+ *  - The first call on each device looks up the array's device address and sets the GEMM
+ *    kernel's shared-memory limit; make that first call before any stream capture.
+ *  - Every call shares the one array and leaves its contents behind; no part of it needs to
+ *    start at zero (each location a call reads was written earlier in that call), but calls
+ *    that overlap on the GPU (several streams, several host threads) race: serialise them.
+ * Arguments, layouts and other errors as grpo_lmhead_loss_fwd_bwd. */
+GRPO_API int grpo_lmhead_forward_noalloc(const void* h, const void* W, int64_t T, int64_t V, int64_t H,
+                                         const int32_t* target, const float* old_logp,
+                                         const float* adv_tok, const uint8_t* mask, float clip_eps,
+                                         float grad_scale, float* loss_tok, float* logp_tok,
+                                         grpo_step_acc* acc, void* stream);
+
+/* Size in bytes of grpo_lmhead_forward_noalloc's scratch array. */
+GRPO_API size_t grpo_lmhead_forward_noalloc_max_scratch(void);
+
 /* ---- misc -------------------------------------------------------------------------------- */
 
 /* Static string naming a status code. */

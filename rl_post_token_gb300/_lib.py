@@ -101,6 +101,11 @@ def _lib() -> C.CDLL:
     lib.grpo_lmhead_loss_fwd_bwd.argtypes = [vp, vp, C.c_int64, C.c_int64, C.c_int64, vp, vp, vp, vp, C.c_float,
                                              C.c_float, vp, vp, vp, vp, vp, vp, C.c_size_t, vp]
     lib.grpo_lmhead_loss_fwd_bwd.restype = C.c_int
+    lib.grpo_lmhead_forward_noalloc.argtypes = [vp, vp, C.c_int64, C.c_int64, C.c_int64, vp, vp, vp, vp,
+                                                C.c_float, C.c_float, vp, vp, vp, vp]
+    lib.grpo_lmhead_forward_noalloc.restype = C.c_int
+    lib.grpo_lmhead_forward_noalloc_max_scratch.argtypes = []
+    lib.grpo_lmhead_forward_noalloc_max_scratch.restype = C.c_size_t
     lib.grpo_status_string.argtypes = [C.c_int]
     lib.grpo_status_string.restype = C.c_char_p
     lib.grpo_version.argtypes = []
@@ -295,6 +300,22 @@ def grpo_lmhead_loss_fwd_bwd(h, W, target, old_logp, adv_tok, mask, clip_eps: fl
                                          _stream(stream))
     if rc != OK:
         raise GrpoError(rc, "grpo_lmhead_loss_fwd_bwd")
+
+
+def grpo_lmhead_forward_noalloc(h, W, target, old_logp, adv_tok, mask, clip_eps: float,
+                                grad_scale: float, loss_tok, logp_tok, acc, stream=None) -> None:
+    """Forward-only LM-head loss with the library's own fixed scratch (no allocation)."""
+    T, H = h.shape
+    V = W.shape[0]
+    rc = _lib().grpo_lmhead_forward_noalloc(_ptr(h), _ptr(W), T, V, H, _ptr(target), _ptr(old_logp),
+                                            _ptr(adv_tok), _ptr(mask), float(clip_eps), float(grad_scale),
+                                            _ptr(loss_tok), _ptr(logp_tok), _ptr(acc), _stream(stream))
+    if rc != OK:
+        raise GrpoError(rc, "grpo_lmhead_forward_noalloc")
+
+
+def grpo_lmhead_forward_noalloc_max_scratch() -> int:
+    return int(_lib().grpo_lmhead_forward_noalloc_max_scratch())
 
 
 def new_step_acc(device="cuda"):

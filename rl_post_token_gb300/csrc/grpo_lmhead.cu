@@ -526,3 +526,107 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
   }
   return GRPO_OK;
 }
+
+// ---- allocation-free forward entry point -----------------------------------------------------
+//
+// For callers that cannot allocate device memory when they need the loss: a serving or
+// scoring process that has handed all device memory to its own pool (KV cache, a caching
+// allocator) so that a fresh cudaMalloc would fail or force the pool to shrink, or a code path
+// that must not risk the implicit device synchronisation that cudaMalloc / cudaFree can
+// cause. Such a caller still passes its inputs and outputs; the forward pass's scratch
+// (per-token vocabulary-tile softmax partials, target logits, LSE, coefficients) lives in the
+// file-scope array below instead of a caller workspace.
+//
+// The array is a device symbol: every GPU that loads this library holds its 16 MiB until the
+// process exits. In host code its name only stands in for the symbol; the device address is
+// looked up once per device (with that device current) by cudaGetSymbolAddress and passed to
+// the kernels.
+constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
+static __device__ __align__(256) unsigned char g_lmhead_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+// Device address of the scratch array on the current device; the first call on a device does
+// the lookup (and sets the GEMM kernel's shared-memory attribute) and caches both.
+int noalloc_setup(void** scratch) {
+  static void* addr[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return GRPO_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= 64) return GRPO_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_lmhead_noalloc_scratch) != cudaSuccess || !p) {
+      (void)cudaGetLastError();
+      return GRPO_ERR_CUDA;
+    }
+    if (cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) !=
+        cudaSuccess) {
+      (void)cudaGetLastError();
+      return GRPO_ERR_CUDA;
+    }
+    addr[dev] = p;
+  }
+  *scratch = addr[dev];
+  return GRPO_OK;
+}
+
+}  // namespace
+
+extern "C" GRPO_API size_t grpo_lmhead_forward_noalloc_max_scratch(void) { return kNoAllocScratchBytes; }
+
+extern "C" GRPO_API int grpo_lmhead_forward_noalloc(const void* h, const void* W, int64_t T, int64_t V,
+                                                    int64_t H, const int32_t* target, const float* old_logp,
+                                                    const float* adv_tok, const uint8_t* mask, float clip_eps,
+                                                    float grad_scale, float* loss_tok, float* logp_tok,
+                                                    grpo_step_acc* acc, void* stream) {
+  if (T < 0 || V < 1 || H < BK || H % BK != 0 || !acc) return GRPO_ERR_INVALID;
+  if (T == 0) return GRPO_OK;
+  if (!h || !W || !target || !adv_tok || !mask || !loss_tok) return GRPO_ERR_INVALID;
+  if (((uintptr_t)h | (uintptr_t)W) & 15u) return GRPO_ERR_INVALID;
+  if (T > INT32_MAX / 2 || V > INT32_MAX / 2) return GRPO_ERR_INVALID;
+  // the forward pass uses the workspace layout up to (not including) the dlogits chunk
+  const WsLayout ws = ws_layout(T, V, kDefaultVChunk);
+  if (ws.dz > kNoAllocScratchBytes) return GRPO_ERR_CAPACITY;
+  void* scratch = nullptr;
+  const int rc = noalloc_setup(&scratch);
+  if (rc != GRPO_OK) return rc;
+  uint8_t* wsb = static_cast<uint8_t*>(scratch);
+  float* part_m = reinterpret_cast<float*>(wsb + ws.part_m);
+  float* part_s = reinterpret_cast<float*>(wsb + ws.part_s);
+  float* zy = reinterpret_cast<float*>(wsb + ws.zy);
+  float* lse2 = reinterpret_cast<float*>(wsb + ws.lse2);
+  float* coef = reinterpret_cast<float*>(wsb + ws.coef);
+
+  CUtensorMap map_h, map_w;
+  if (!make_map(&map_h, h, (uint64_t)T, (uint64_t)H, BM) || !make_map(&map_w, W, (uint64_t)V, (uint64_t)H, BN))
+    return GRPO_ERR_UNSUPPORTED;
+  const cudaStream_t st = as_stream(stream);
+  GemmArgs g{};
+  g.T = T;
+  g.V = V;
+  g.H = H;
+  g.n_row_tiles = (int)((T + BM - 1) / BM);
+  g.target = target;
+  g.part_m = part_m;
+  g.part_s = part_s;
+  g.zy = zy;
+  g.lse2 = lse2;
+  g.coef = coef;
+  g.acc = acc;
+  g.mode = 0;
+  g.col_tile0 = 0;
+  g.n_col_tiles = ws.n_col_tiles;
+  const int grid = (int)std::min<int64_t>((int64_t)g.n_row_tiles * ws.n_col_tiles, sm_count());
+  gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(map_h, map_w, g);
+  GRPO_CUDA_TRY(cudaGetLastError());
+  reduce_kernel<<<(unsigned)((T + 255) / 256), 256, 0, st>>>(T, ws.n_col_tiles, part_m, part_s, zy, target, V,
+                                                              old_logp, adv_tok, mask, clip_eps, grad_scale, lse2,
+                                                              coef, loss_tok, logp_tok, acc);
+  GRPO_CUDA_TRY(cudaGetLastError());
+  return GRPO_OK;
+}
