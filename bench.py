@@ -312,7 +312,7 @@ def run_lmhead(args):
     if rank == 0:
         B.build()
     _lib.lib()
-    wl = W.make_workload("lmhead", seed=rank)
+    wl = W.make_workload("lmhead", seed=rank, **({"tokens": args.lm_tokens} if args.lm_tokens else {}))
     T, V, Hd = wl.T, wl.V, wl.extra["H"]
     h, Wt = W.make_lmhead_inputs(wl, device)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
@@ -571,6 +571,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--lm-tokens", type=int, default=0,
+                    help="override the fused LM-head token count (smaller cases for profiling)")
     ap.add_argument("--rows", type=int, default=0,
                     help="override the workload's row count (smaller cases for profiling)")
     args = ap.parse_args(argv)

@@ -1,0 +1,103 @@
+"""Full-size batches in the launch configuration the benchmark times (the same planner, chunk
+loop and kernels), checked against the oracle on sampled token rows and by properties over
+every row:
+* sampled rows: per-token loss and log-prob, and the whole dlogits row, against the float64
+  oracle with the per-token and dlogits bars of the smaller parity tests;
+* every row: finite dlogits; each valid row's dlogits sum to ~0 (softmax and one-hot both sum
+  to one); masked and padding rows exactly zero; per-step N equals the planner's N.
+
+pi_old here is target logit - 12 + N(0, 0.05): a plain input recipe (no log-softmax) that puts
+the ratio far below 1, so tokens with A < 0 take the clipped branch and tokens with A > 0 the
+unclipped one, both at full size."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import loss as OL
+from rl_post_token_gb300 import _lib
+from rl_post_token_gb300 import step as S
+from rl_post_token_gb300 import workloads as W
+
+from tests import _gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(grpo_lib):
+    assert torch.cuda.is_available()
+    return grpo_lib
+
+
+def _host_row(t):
+    return W.logits_to_host(t.unsqueeze(0))[0]
+
+
+@pytest.mark.parametrize("name", ["qwen_step", "dynamic", "compaction"])
+def test_full_size_batch(name):
+    wl = W.make_workload(name, seed=0)
+    bp = S.plan_batch(wl.plan, wl.row_len, wl.row_valid, wl.seg_counts)
+    Te, T = bp.exec_tokens, wl.T
+    logits = W.make_logits(wl, DEV, rows=Te)
+    tok_src = None if bp.tok_src is None else bp.tok_src
+    src = np.arange(Te) if tok_src is None else tok_src
+    # pi_old from the target logit of each exec row's input token (valid rows only matter)
+    tgt_exec = np.where(src >= 0, wl.target[np.where(src >= 0, src, -1 - src)], 0)
+    zy = logits[torch.arange(Te, device=DEV), torch.from_numpy(tgt_exec.astype(np.int64)).to(DEV)].float().cpu().numpy()
+    old = np.zeros(T, np.float32)
+    ok = src >= 0
+    old[src[ok]] = zy[ok] - 12.0 + wl.old_noise[src[ok]]
+    adv = np.random.default_rng(1).choice([-1.5, -0.3, 0.4, 1.2], T).astype(np.float32)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    dl = torch.empty_like(logits)
+    loss = torch.full((T,), -7.0, device=DEV)
+    logp = torch.full((T,), -7.0, device=DEV)
+    accs = torch.zeros(bp.n_steps * _lib.ACC_BYTES, dtype=torch.uint8, device=DEV)
+    S.run_batch(bp, logits=logits, dlogits=dl, target=t(wl.target), old_logp=t(old), mask=t(wl.mask),
+                adv_tok=t(adv), loss_tok=loss, logp_tok=logp, accs=accs, clip_eps=wl.eps,
+                tok_src=None if tok_src is None else t(tok_src), V=wl.V)
+    torch.cuda.synchronize()
+    res = S.read_results(accs, bp.n_steps)
+    for s, r in enumerate(res):
+        assert r["status"] == 0 and r["n_valid"] == bp.plan["step_valid_tokens"][s]
+
+    # sampled exec rows: the first and last of every chunk plus a seeded handful
+    rng = np.random.default_rng(2)
+    pick = set()
+    for c in range(bp.plan["n_chunks"]):
+        a, b = int(bp.exec_tok_off[c]), int(bp.exec_tok_off[c + 1])
+        if b > a:
+            pick.update([a, b - 1])
+    pick.update(rng.integers(0, Te, 12).tolist())
+    pick = sorted(pick)[:48]
+    step_of = np.zeros(Te, np.int64)
+    for s, (e0, e1) in enumerate(bp.step_exec_range):
+        step_of[e0:e1] = s
+    lg, lp = H.to_f64(loss), H.to_f64(logp)
+    for e in pick:
+        i = int(src[e])
+        scale = 1.0 / max(int(bp.plan["step_valid_tokens"][step_of[e]]), 1)
+        got = dl[e].float().cpu().numpy().astype(np.float64)
+        if i < 0:  # padding row
+            assert np.all(got == 0)
+            continue
+        z = OL.as_f64(_host_row(logits[e]))
+        lt, lpv, r, cl, dz = OL.token_objective(z, int(wl.target[i]), float(old[i]), float(adv[i]),
+                                                int(wl.mask[i]), wl.eps, scale)
+        ref = {"loss_tok": np.array([lt]), "logp_tok": np.array([lpv])}
+        H.assert_tokens_close(lg[[i]], lp[[i]], ref, adv[[i]], wl.mask[[i]])
+        coef = 0.0 if (cl or not wl.mask[i]) else float(adv[i]) * r * scale
+        H.assert_dlogits_close(got[None, :], dz[None, :], "bf16", target=np.array([wl.target[i]]),
+                               coef=np.array([coef]))
+
+    # properties over every row, in blocks
+    valid_exec = torch.from_numpy((src >= 0) & (wl.mask[np.where(src >= 0, src, 0)] != 0)).to(DEV)
+    for a in range(0, Te, 4096):
+        blk = dl[a:a + 4096].float()
+        assert torch.isfinite(blk).all()
+        rs = blk.sum(1).abs()
+        mag = blk.abs().sum(1)
+        v = valid_exec[a:a + 4096]
+        assert torch.all(rs[v] <= 2e-2 * mag[v] + 1e-12)
+        assert torch.all(mag[~v] == 0)
