@@ -240,6 +240,43 @@ GRPO_API int grpo_finish_step(grpo_step_acc* acc, const float* loss_tok, int64_t
                               const int64_t* grad_numels, const int32_t* grad_dtypes,
                               int32_t n_bufs, grpo_step_result* result_host, void* stream);
 
+/* ---- accumulation window (host) ----------------------------------------------------------- */
+
+/* The trainer's view of one optimizer step fed chunk by chunk ("Sizing mini-batches and
+ * micro-batches": "The hard part: deferred normalization", "The poisoned-window countdown",
+ * "Metric roll-up"). Actions for each chunk: */
+#define GRPO_WIN_ACCUMULATE 0  /* backprop the chunk and keep accumulating */
+#define GRPO_WIN_STEP       1  /* backprop, scale the gradient by step_scale, clip, step */
+#define GRPO_WIN_DISCARD    2  /* the chunk is non-finite: zero the gradients, window abandoned */
+#define GRPO_WIN_DROP       3  /* a remaining chunk of an abandoned window: do not backprop */
+
+typedef struct grpo_window {
+  int32_t n_micro;            /* chunks per optimizer step */
+  int32_t pos;                /* chunks of the current window seen */
+  int32_t remaining_drop;     /* calls still to drop from an abandoned window */
+  int32_t reserved0;
+  int64_t denom;              /* divisors accumulated in the current window */
+  double  loss_x_denom;       /* sum of chunk loss * chunk divisor in the current window */
+  int64_t steps, skipped_windows, dropped_chunks;
+  double  batch_loss_x_denom; /* roll-up over the trained windows */
+  int64_t batch_denom;
+} grpo_window;
+
+/* Start a collected batch with n_micro >= 1 chunks per optimizer step (host only). */
+GRPO_API int grpo_window_init(grpo_window* w, int32_t n_micro);
+
+/* Feed one chunk: finite = 0 if its loss was non-finite; loss = the chunk's loss normalised
+ * by its own divisor; denom = that divisor (valid tokens). Writes the action and, on
+ * GRPO_WIN_STEP, step_scale = 1 / max(sum of the window's divisors, 1) (else 0). A
+ * non-finite chunk discards its window and the window's remaining n_micro - pos chunks are
+ * dropped before a fresh window starts; the divisor resets with it. */
+GRPO_API int grpo_window_chunk(grpo_window* w, int32_t finite, double loss, int64_t denom,
+                               int32_t* action, double* step_scale);
+
+/* Token-weighted loss sum(loss_i * denom_i) / max(sum(denom_i), 1) over the trained windows,
+ * the summed divisor and the optimizer steps taken (any output may be NULL). */
+GRPO_API int grpo_window_rollup(const grpo_window* w, double* loss, int64_t* denom, int64_t* steps);
+
 /* ---- fused LM-head variant ---------------------------------------------------------------- */
 
 /* Bytes of device workspace grpo_lmhead_loss_fwd_bwd needs for [T, H] hidden states and a

@@ -63,6 +63,13 @@ class grpo_plan(C.Structure):
                 ("step_valid_rows", _i32p)]
 
 
+class grpo_window(C.Structure):
+    _fields_ = [("n_micro", C.c_int32), ("pos", C.c_int32), ("remaining_drop", C.c_int32),
+                ("reserved0", C.c_int32), ("denom", C.c_int64), ("loss_x_denom", C.c_double),
+                ("steps", C.c_int64), ("skipped_windows", C.c_int64), ("dropped_chunks", C.c_int64),
+                ("batch_loss_x_denom", C.c_double), ("batch_denom", C.c_int64)]
+
+
 class grpo_step_result(C.Structure):
     _fields_ = [("loss", C.c_double), ("loss_sum", C.c_double), ("clipfrac", C.c_double),
                 ("n_valid", C.c_int64), ("n_clipped", C.c_int64), ("n_nonfinite", C.c_int64),
@@ -106,6 +113,12 @@ def _lib() -> C.CDLL:
     lib.grpo_lmhead_forward_noalloc.restype = C.c_int
     lib.grpo_lmhead_forward_noalloc_max_scratch.argtypes = []
     lib.grpo_lmhead_forward_noalloc_max_scratch.restype = C.c_size_t
+    lib.grpo_window_init.argtypes = [C.POINTER(grpo_window), C.c_int32]
+    lib.grpo_window_chunk.argtypes = [C.POINTER(grpo_window), C.c_int32, C.c_double, C.c_int64,
+                                      C.POINTER(C.c_int32), C.POINTER(C.c_double)]
+    lib.grpo_window_rollup.argtypes = [C.POINTER(grpo_window), C.POINTER(C.c_double), _i64p, _i64p]
+    for f in ("grpo_window_init", "grpo_window_chunk", "grpo_window_rollup"):
+        getattr(lib, f).restype = C.c_int
     lib.grpo_status_string.argtypes = [C.c_int]
     lib.grpo_status_string.restype = C.c_char_p
     lib.grpo_version.argtypes = []
@@ -316,6 +329,35 @@ def grpo_lmhead_forward_noalloc(h, W, target, old_logp, adv_tok, mask, clip_eps:
 
 def grpo_lmhead_forward_noalloc_max_scratch() -> int:
     return int(_lib().grpo_lmhead_forward_noalloc_max_scratch())
+
+
+class Window:
+    """The host accumulation window (grpo_window_* entry points)."""
+
+    def __init__(self, n_micro: int):
+        self._w = grpo_window()
+        rc = _lib().grpo_window_init(C.byref(self._w), int(n_micro))
+        if rc != OK:
+            raise GrpoError(rc, "grpo_window_init")
+
+    def grpo_window_chunk(self, finite: bool, loss: float, denom: int):
+        act, scale = C.c_int32(0), C.c_double(0.0)
+        rc = _lib().grpo_window_chunk(C.byref(self._w), int(bool(finite)), float(loss), int(denom),
+                                      C.byref(act), C.byref(scale))
+        if rc != OK:
+            raise GrpoError(rc, "grpo_window_chunk")
+        return act.value, scale.value
+
+    def grpo_window_rollup(self):
+        loss, denom, steps = C.c_double(0.0), C.c_int64(0), C.c_int64(0)
+        rc = _lib().grpo_window_rollup(C.byref(self._w), C.byref(loss), C.byref(denom), C.byref(steps))
+        if rc != OK:
+            raise GrpoError(rc, "grpo_window_rollup")
+        return loss.value, denom.value, steps.value
+
+    @property
+    def state(self) -> dict:
+        return {k: getattr(self._w, k) for k, _ in grpo_window._fields_}
 
 
 def new_step_acc(device="cuda"):

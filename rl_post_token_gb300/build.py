@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgrpo.so")
 
-SOURCES = ["grpo_plan.cpp", "grpo_rowpass.cu", "grpo_step.cu", "grpo_lmhead.cu"]
+SOURCES = ["grpo_plan.cpp", "grpo_window.cpp", "grpo_rowpass.cu", "grpo_step.cu", "grpo_lmhead.cu"]
 # cuBLAS serves the two plain backward GEMMs of the LM-head variant; the rpath lets the
 # library load (for its host-only entry points) before any framework has loaded cuBLAS.
 LINK = ["-lcublas", "-Xlinker", "-rpath=/usr/local/cuda/lib64"]
