@@ -339,3 +339,32 @@ def test_cluster_chunked_equals_unchunked_bitwise(variant):
         outs.append((dl.view(torch.int16).clone(), loss.clone(), S.read_results(accs, bp.n_steps)))
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
     assert outs[0][2] == outs[1][2]
+
+
+@pytest.mark.parametrize("variant", ["c2", "l2"], indirect=True)
+def test_dynamic_bins_equal_fixed_chunks_bitwise(variant):
+    # one mini-batch planned as fixed chunks and as token-budget bins (rows reordered, chunk
+    # boundaries moved): every token's loss, log-prob and dlogits row is bit-identical, and so
+    # are the step results
+    wl = W.make_workload("qwen_step", rows=8, len_lo=8, len_hi=60, V=32776, seed=31, mini=8, micro=2)
+    case = H.Case(wl)
+    outs = []
+    for cfg in (dict(wl.plan), dict(wl.plan, dynamic=1, max_token_len=128, workload=1, balance_ends=1)):
+        bp = S.plan_batch(cfg, wl.row_len, wl.row_valid)
+        src = np.arange(wl.T) if bp.tok_src is None else bp.tok_src
+        lg = case.logits[torch.from_numpy(src).to(DEV)]  # exec order, as a model would emit it
+        dl = torch.empty_like(lg)
+        loss = torch.empty(wl.T, device=DEV)
+        logp = torch.empty(wl.T, device=DEV)
+        accs = torch.zeros(bp.n_steps * _lib.ACC_BYTES, dtype=torch.uint8, device=DEV)
+        S.run_batch(bp, logits=lg, dlogits=dl, target=case.d_target, old_logp=case.d_old, mask=case.d_mask,
+                    adv_tok=case.d_adv, loss_tok=loss, logp_tok=logp, accs=accs, clip_eps=wl.eps,
+                    tok_src=None if bp.tok_src is None else torch.from_numpy(bp.tok_src).to(DEV))
+        torch.cuda.synchronize()
+        back = torch.empty_like(dl)
+        back[torch.from_numpy(src).to(DEV)] = dl  # dlogits rows back to input order
+        outs.append((bp.plan["n_chunks"], back.view(torch.int16), loss, logp, S.read_results(accs, bp.n_steps)))
+    assert outs[0][0] != outs[1][0]  # the two schedules really differ
+    assert torch.equal(outs[0][1], outs[1][1])
+    assert torch.equal(outs[0][2], outs[1][2]) and torch.equal(outs[0][3], outs[1][3])
+    assert outs[0][4] == outs[1][4]
