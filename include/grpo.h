@@ -218,6 +218,39 @@ GRPO_API int grpo_logprob_loss_fwd_bwd(const void* logits, int32_t dtype, int64_
                                        int64_t ld_out, float* loss_tok, float* logp_tok,
                                        grpo_step_acc* acc, void* stream);
 
+/* Regularisers that go through the same token-mean aggregation as the surrogate
+ * ("22-mini-batch-micro-batch-dynamic-batch-size的区别", section 5: the entropy and KL losses
+ * take the same global token count; "03 Data Protocol and Batch Lifecycle": the reference
+ * policy's log-prob ref_log_prob). The pages give no formulas; the usual ones are used:
+ *   + kl_coef * k,  k1 = logp - ref,  k3 = exp(ref - logp) - (ref - logp) - 1
+ *   - ent_coef * H, H = -sum_v p_v log p_v  (an entropy bonus)
+ * with gradients dk/dz = (dk/dlogp)(onehot - p) and dH/dz_v = -p_v (z_v - sum_u p_u z_u). */
+#define GRPO_KL_NONE 0
+#define GRPO_KL_K1   1
+#define GRPO_KL_K3   2
+
+typedef struct grpo_loss_terms {
+  int32_t kl_kind;       /* GRPO_KL_* */
+  float   kl_coef;
+  const float* ref_logp; /* device float per token, indexed like old_logp; required for KL */
+  float   ent_coef;      /* entropy bonus coefficient, 0 = off */
+  float*  entropy_tok;   /* device float per token, indexed like loss_tok, or NULL; written
+                            whenever non-NULL, also with ent_coef = 0 (entropy as a metric) */
+} grpo_loss_terms;
+
+/* grpo_logprob_loss_fwd_bwd with the regularisers above added to every valid token's loss
+ * and gradient (terms NULL: identical to grpo_logprob_loss_fwd_bwd). Masked tokens get 0 in
+ * entropy_tok. Errors as grpo_logprob_loss_fwd_bwd, plus GRPO_ERR_INVALID for an unknown
+ * kl_kind or a KL without ref_logp. */
+GRPO_API int grpo_logprob_loss_fwd_bwd_ex(const void* logits, int32_t dtype, int64_t T, int64_t V,
+                                          int64_t ld, const int64_t* tok_src,
+                                          const int32_t* target, const float* old_logp,
+                                          const float* adv_tok, const uint8_t* mask,
+                                          float clip_eps, float grad_scale, void* dlogits,
+                                          int64_t ld_out, float* loss_tok, float* logp_tok,
+                                          const grpo_loss_terms* terms, grpo_step_acc* acc,
+                                          void* stream);
+
 /* ---- step finish ------------------------------------------------------------------------- */
 
 /* Close one optimizer step ("Sizing mini-batches and micro-batches", "The hard part:

@@ -60,10 +60,25 @@ def log_softmax_row(z: np.ndarray) -> np.ndarray:
     return z - lse
 
 
-def token_objective(z, y, old, adv, mask, eps, scale=1.0, want_grad=True):
-    """One token row. Returns (loss_t, logp, r, clipped, dz or None)."""
+KL_NONE, KL_K1, KL_K3 = 0, 1, 2
+
+
+def token_objective(z, y, old, adv, mask, eps, scale=1.0, want_grad=True, terms=None):
+    """One token row. Returns (loss_t, logp, r, clipped, dz or None).
+
+    ``terms`` (optional dict) adds the regularisers that the verl batching article (section 5)
+    sends through the same token-mean aggregation; the pages give no formula, so the reading is
+    the usual one:
+      kl_coef * k(logp, ref)  with k1 = logp - ref, or k3 = exp(ref - logp) - (ref - logp) - 1
+                              (kl_kind 1 or 2, ``ref`` the reference policy's log-prob);
+      - ent_coef * H          with H = -sum_v p_v log p_v (an entropy bonus).
+    Their gradients w.r.t. the logits: dk/dz = (dk/dlogp) (onehot - p) and
+    dH/dz_v = -p_v (z_v - sum_u p_u z_u). The entropy is returned as terms["entropy"].
+    """
     V = z.shape[0]
     if not mask:
+        if terms is not None:
+            terms["entropy"] = 0.0
         return 0.0, 0.0, 1.0, False, (np.zeros(V) if want_grad else None)
     z = np.asarray(z, dtype=np.float64)
     lsm = log_softmax_row(z)
@@ -76,19 +91,44 @@ def token_objective(z, y, old, adv, mask, eps, scale=1.0, want_grad=True):
     loss_t = -min(r * A, rc * A)
     clipped = (A > 0 and r > hi) or (A < 0 and r < lo)
     g = 0.0 if clipped else 1.0
+    c = A * r * g          # d(loss)/dz = c * (p - onehot) for the surrogate
+    ent_coef = 0.0
+    if terms is not None:
+        kind = int(terms.get("kl_kind", KL_NONE))
+        if kind != KL_NONE:
+            d = float(terms["ref"]) - logp
+            if kind == KL_K1:
+                k, dk = -d, 1.0
+            else:
+                k, dk = math.exp(d) - d - 1.0, 1.0 - math.exp(d)
+            beta = float(terms.get("kl_coef", 0.0))
+            loss_t += beta * k
+            c -= beta * dk
+        ent_coef = float(terms.get("ent_coef", 0.0))
+        p = np.exp(lsm)
+        # p log p -> 0 as p -> 0: elements without mass (-inf logits) add nothing
+        with np.errstate(invalid="ignore"):
+            H = -float(np.sum(np.where(p > 0, p * lsm, 0.0)))
+        terms["entropy"] = H
+        loss_t -= ent_coef * H
     dz = None
     if want_grad:
-        coef = A * r * g * float(scale)
-        dz = coef * np.exp(lsm)
-        dz[y] -= coef
+        p = np.exp(lsm)
+        dz = float(scale) * c * p
+        dz[y] -= float(scale) * c
+        if ent_coef != 0.0:
+            with np.errstate(invalid="ignore"):
+                ez = float(np.sum(np.where(p > 0, p * z, 0.0)))
+                dz += float(scale) * ent_coef * np.where(p > 0, p * (z - ez), 0.0)
     return loss_t, logp, r, clipped, dz
 
 
-def loss_fwd_bwd(logits, target, old_logp, adv_tok, mask, eps, scale=1.0, want_grad=True):
+def loss_fwd_bwd(logits, target, old_logp, adv_tok, mask, eps, scale=1.0, want_grad=True, terms=None):
     """All token rows of ``logits`` ([T, V], float or bf16 bits).
 
     Returns dict with float64 ``loss_tok``, ``logp_tok``, ``ratio``, bool ``clipped`` and,
-    if ``want_grad``, float64 ``dlogits`` [T, V].
+    if ``want_grad``, float64 ``dlogits`` [T, V]. ``terms`` = dict(kl_kind, kl_coef, ref (array
+    per token), ent_coef) adds the regularisers of ``token_objective`` (output ``entropy``).
     """
     T = logits.shape[0]
     V = logits.shape[1] if logits.ndim == 2 else 0
@@ -98,11 +138,20 @@ def loss_fwd_bwd(logits, target, old_logp, adv_tok, mask, eps, scale=1.0, want_g
     }
     if want_grad:
         out["dlogits"] = np.zeros((T, V))
+    if terms is not None:
+        out["entropy"] = np.zeros(T)
     for t in range(T):
         old = None if old_logp is None else old_logp[t]
         z = as_f64(logits[t]) if mask[t] else np.zeros(V)
+        tt = None
+        if terms is not None:
+            tt = dict(kl_kind=terms.get("kl_kind", 0), kl_coef=terms.get("kl_coef", 0.0),
+                      ent_coef=terms.get("ent_coef", 0.0),
+                      ref=None if terms.get("ref") is None else terms["ref"][t])
         lt, lp, r, cl, dz = token_objective(z, int(target[t]), old, adv_tok[t], int(mask[t]),
-                                            eps, scale, want_grad)
+                                            eps, scale, want_grad, tt)
+        if tt is not None:
+            out["entropy"][t] = tt["entropy"]
         out["loss_tok"][t] = lt
         out["logp_tok"][t] = lp
         out["ratio"][t] = r

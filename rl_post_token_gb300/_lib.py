@@ -70,6 +70,11 @@ class grpo_window(C.Structure):
                 ("batch_loss_x_denom", C.c_double), ("batch_denom", C.c_int64)]
 
 
+class grpo_loss_terms(C.Structure):
+    _fields_ = [("kl_kind", C.c_int32), ("kl_coef", C.c_float), ("ref_logp", C.c_void_p),
+                ("ent_coef", C.c_float), ("entropy_tok", C.c_void_p)]
+
+
 class grpo_step_result(C.Structure):
     _fields_ = [("loss", C.c_double), ("loss_sum", C.c_double), ("clipfrac", C.c_double),
                 ("n_valid", C.c_int64), ("n_clipped", C.c_int64), ("n_nonfinite", C.c_int64),
@@ -101,6 +106,10 @@ def _lib() -> C.CDLL:
     lib.grpo_logprob_loss_fwd_bwd.argtypes = [vp, C.c_int32, C.c_int64, C.c_int64, C.c_int64, vp, vp,
                                               vp, vp, vp, C.c_float, C.c_float, vp, C.c_int64, vp, vp,
                                               vp, vp]
+    lib.grpo_logprob_loss_fwd_bwd_ex.argtypes = [vp, C.c_int32, C.c_int64, C.c_int64, C.c_int64, vp, vp,
+                                                 vp, vp, vp, C.c_float, C.c_float, vp, C.c_int64, vp, vp,
+                                                 C.POINTER(grpo_loss_terms), vp, vp]
+    lib.grpo_logprob_loss_fwd_bwd_ex.restype = C.c_int
     lib.grpo_finish_step.argtypes = [vp, vp, C.c_int64, C.c_int64, C.c_int32, C.POINTER(vp), _i64p,
                                      _i32p, C.c_int32, C.POINTER(grpo_step_result), vp]
     lib.grpo_lmhead_workspace_size.argtypes = [C.c_int64, C.c_int64, C.c_int64]
@@ -250,8 +259,11 @@ def grpo_group_advantage(rewards, group_size: int, eps: float, unbiased_std: boo
 
 def grpo_logprob_loss_fwd_bwd(logits, target, old_logp, adv_tok, mask, clip_eps: float,
                               grad_scale: float, dlogits, loss_tok, logp_tok, acc, tok_src=None,
-                              V: Optional[int] = None, stream=None) -> None:
-    """logits [T, ld] (float32 or bfloat16) on the device; see grpo.h for the rest."""
+                              V: Optional[int] = None, stream=None, terms: Optional[dict] = None) -> None:
+    """logits [T, ld] (float32 or bfloat16) on the device; see grpo.h for the rest.
+
+    ``terms`` (optional) = dict(kl_kind=0|1|2, kl_coef=..., ref_logp=tensor, ent_coef=...,
+    entropy_tok=tensor) selects grpo_logprob_loss_fwd_bwd_ex."""
     import torch
 
     if logits.dim() != 2 or logits.stride(1) != 1:
@@ -266,10 +278,19 @@ def grpo_logprob_loss_fwd_bwd(logits, target, old_logp, adv_tok, mask, clip_eps:
         if dlogits.shape[0] != T:
             raise ValueError("dlogits must have the same row count as logits")
         ld_out = dlogits.stride(0) if T > 1 else dlogits.shape[1]
-    rc = _lib().grpo_logprob_loss_fwd_bwd(_ptr(logits), dt, T, V, ld, _ptr(tok_src), _ptr(target),
-                                          _ptr(old_logp), _ptr(adv_tok), _ptr(mask), float(clip_eps),
-                                          float(grad_scale), _ptr(dlogits), ld_out, _ptr(loss_tok),
-                                          _ptr(logp_tok), _ptr(acc), _stream(stream))
+    if terms is None:
+        rc = _lib().grpo_logprob_loss_fwd_bwd(_ptr(logits), dt, T, V, ld, _ptr(tok_src), _ptr(target),
+                                              _ptr(old_logp), _ptr(adv_tok), _ptr(mask), float(clip_eps),
+                                              float(grad_scale), _ptr(dlogits), ld_out, _ptr(loss_tok),
+                                              _ptr(logp_tok), _ptr(acc), _stream(stream))
+    else:
+        tm = grpo_loss_terms(int(terms.get("kl_kind", 0)), float(terms.get("kl_coef", 0.0)),
+                             _ptr(terms.get("ref_logp")), float(terms.get("ent_coef", 0.0)),
+                             _ptr(terms.get("entropy_tok")))
+        rc = _lib().grpo_logprob_loss_fwd_bwd_ex(_ptr(logits), dt, T, V, ld, _ptr(tok_src), _ptr(target),
+                                                 _ptr(old_logp), _ptr(adv_tok), _ptr(mask), float(clip_eps),
+                                                 float(grad_scale), _ptr(dlogits), ld_out, _ptr(loss_tok),
+                                                 _ptr(logp_tok), C.byref(tm), _ptr(acc), _stream(stream))
     if rc != OK:
         raise GrpoError(rc, "grpo_logprob_loss_fwd_bwd")
 

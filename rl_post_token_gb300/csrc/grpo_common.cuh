@@ -137,6 +137,74 @@ __device__ __forceinline__ void lazy_online2(MS& acc, float (&x)[N]) {
   online2<N>(acc, x);
 }
 
+// (max, sum e, sum e*x) triple for the entropy term: s2 / s = sum_v p_v z_v.
+struct MS3 {
+  float m, s, s2;
+};
+
+// natural-log units (max in logit units)
+__device__ __forceinline__ MS3 ms3_combine(MS3 a, MS3 b) {
+  const float m = fmaxf(a.m, b.m);
+  if (m == -INFINITY) return {m, 0.f, 0.f};
+  const float fa = ex2((a.m - m) * kLog2e), fb = ex2((b.m - m) * kLog2e);
+  return {m, a.s * fa + b.s * fb, a.s2 * fa + b.s2 * fb};
+}
+
+// log2 units (max kept as max * log2(e))
+__device__ __forceinline__ MS3 ms3_combine2(MS3 a, MS3 b) {
+  const float m = fmaxf(a.m, b.m);
+  if (m == -INFINITY) return {m, 0.f, 0.f};
+  const float fa = ex2(a.m - m), fb = ex2(b.m - m);
+  return {m, a.s * fa + b.s * fb, a.s2 * fa + b.s2 * fb};
+}
+
+template <bool LOG2>
+__device__ __forceinline__ MS3 warp_ms3(MS3 v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    MS3 w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o),
+          __shfl_xor_sync(0xffffffffu, v.s2, o)};
+    v = LOG2 ? ms3_combine2(v, w) : ms3_combine(v, w);
+  }
+  return v;
+}
+
+// lazy_online2 that also accumulates sum e*x (log2-domain shift, natural-unit x). Pairs are
+// combined as they are produced, so only half-width arrays of partial sums stay live.
+template <int N>
+__device__ __forceinline__ void e_pairs(const float (&x)[N], float sh, float (&pe)[N / 2], float (&px)[N / 2]) {
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    const float e0 = ex2(fmaf(x[2 * i], kLog2e, -sh)), e1 = ex2(fmaf(x[2 * i + 1], kLog2e, -sh));
+    pe[i] = e0 + e1;
+    // p log p -> 0 as p -> 0: an element with no mass (a -inf logit) adds nothing to sum p z
+    px[i] = (e0 != 0.f ? e0 * x[2 * i] : 0.f) + (e1 != 0.f ? e1 * x[2 * i + 1] : 0.f);
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void lazy_online3(MS3& acc, const float (&x)[N]) {
+  if (acc.m == -INFINITY) acc.m = x[0] * kLog2e;
+  float pe[N / 2], px[N / 2];
+  e_pairs<N>(x, acc.m, pe, px);
+  const float bs = tree_sum(pe);
+  if (bs <= 1.8446744e19f) {
+    acc.s += bs;
+    acc.s2 += tree_sum(px);
+    return;
+  }
+  float gm = x[0];
+#pragma unroll
+  for (int i = 1; i < N; ++i) gm = fmaxf(gm, x[i]);
+  const float nm = fmaxf(acc.m, gm * kLog2e);
+  const bool none = nm == -INFINITY;
+  const float scale = none ? 1.f : ex2(acc.m - nm);
+  e_pairs<N>(x, none ? 0.f : nm, pe, px);
+  acc.s = fmaf(acc.s, scale, tree_sum(pe));
+  acc.s2 = fmaf(acc.s2, scale, tree_sum(px));
+  acc.m = nm;
+}
+
 // Per-token scalar epilogue: log-prob, ratio, clipped surrogate, gradient coefficient.
 struct TokenOut {
   float logp, loss, coef;
@@ -155,6 +223,30 @@ __device__ __forceinline__ TokenOut token_epilogue(float zy, float lse, bool has
   o.coef = o.clipped ? 0.f : A * r * scale;
   o.nonfinite = !isfinite(o.logp) || !isfinite(o.loss) || !isfinite(o.coef);
   return o;
+}
+
+// Regularisers sent through the same aggregation: kl_coef * k(logp, ref) with
+// k1 = logp - ref or k3 = exp(ref - logp) - (ref - logp) - 1 (gradient folded into the
+// (softmax - onehot) coefficient), and an entropy bonus -ent_coef * H (its loss part here; its
+// gradient ent_coef * p (z - E_p z) is added by the vocabulary pass).
+__device__ __forceinline__ void apply_terms(TokenOut& o, float scale, int kl_kind, float kl_coef, float ref,
+                                            float ent_coef, float H) {
+  if (kl_kind == GRPO_KL_K1 || kl_kind == GRPO_KL_K3) {
+    const float d = ref - o.logp;
+    float k, dk;
+    if (kl_kind == GRPO_KL_K1) {
+      k = -d;
+      dk = 1.f;
+    } else {
+      const float ed = expf(d);
+      k = ed - d - 1.f;
+      dk = 1.f - ed;
+    }
+    o.loss += kl_coef * k;
+    o.coef -= kl_coef * dk * scale;
+  }
+  if (ent_coef != 0.f) o.loss -= ent_coef * H;
+  o.nonfinite = o.nonfinite || !isfinite(o.loss) || !isfinite(o.coef);
 }
 
 // ---- shared-memory, mbarrier, bulk-copy and cluster primitives (inline PTX, sm_90+) ----------

@@ -47,6 +47,12 @@ struct RowArgs {
   float* loss_tok;
   float* logp_tok;
   grpo_step_acc* acc;
+  // regularisers (kl_kind 0 and ent_coef 0: none)
+  int32_t kl_kind;
+  float kl_coef;
+  const float* ref_logp;
+  float ent_coef;
+  float* entropy_tok;
 };
 
 template <typename T>
@@ -92,19 +98,22 @@ struct RowMeta {
   bool valid;    // mask = 1 and not a padding row
   int32_t y;     // target token id
   float A, old;  // advantage, pi_old log-prob
+  float ref;     // reference-policy log-prob (KL term)
 };
 
 __device__ __forceinline__ int64_t row_src(const RowArgs& a, int64_t row) {
   return a.tok_src ? a.tok_src[row] : row;
 }
 
+template <bool REF>
 __device__ __forceinline__ RowMeta row_meta(const RowArgs& a, int64_t src) {
-  RowMeta m{src < 0 ? -1 : src, false, 0, 0.f, 0.f};
+  RowMeta m{src < 0 ? -1 : src, false, 0, 0.f, 0.f, 0.f};
   if (src >= 0) {
     m.valid = a.mask[src] != 0;
     m.y = a.target[src];
     m.A = a.adv[src];
     m.old = a.old_logp ? a.old_logp[src] : 0.f;
+    if (REF) m.ref = a.ref_logp ? a.ref_logp[src] : 0.f;
   }
   return m;
 }
@@ -112,23 +121,29 @@ __device__ __forceinline__ RowMeta row_meta(const RowArgs& a, int64_t src) {
 // Row metadata fetched ahead of use: the token index two rows ahead and the side inputs one
 // row ahead are in flight while the current row is processed, so the dependent global-load
 // chain (index -> mask/target/advantage/pi_old) never sits on a row's critical path.
+template <bool REF>
 struct MetaPipe {
   const RowArgs& a;
   int64_t stride;
   RowMeta next;
   int64_t src2;
   __device__ MetaPipe(const RowArgs& args, int64_t first, int64_t step) : a(args), stride(step) {
-    next = first < a.T ? row_meta(a, row_src(a, first)) : RowMeta{-1, false, 0, 0.f, 0.f};
+    next = first < a.T ? row_meta<REF>(a, row_src(a, first)) : RowMeta{-1, false, 0, 0.f, 0.f, 0.f};
     src2 = first + step < a.T ? row_src(a, first + step) : -1;
   }
   // metadata of `row`; starts the loads for the rows after it
   __device__ RowMeta advance(int64_t row) {
     const RowMeta m = next;
-    if (row + stride < a.T) next = row_meta(a, src2);
+    if (row + stride < a.T) next = row_meta<REF>(a, src2);
     src2 = row + 2 * stride < a.T ? row_src(a, row + 2 * stride) : -1;
     return m;
   }
 };
+
+// One dlogit with the entropy term, p (ea + eb z); an element with no mass stays 0.
+__device__ __forceinline__ float ent_dz(float p, float z, float ea, float eb) {
+  return p != 0.f ? p * fmaf(eb, z, ea) : 0.f;
+}
 
 // Counters a CTA accumulates and flushes once (integer: order-independent).
 struct Counts {
@@ -144,12 +159,12 @@ struct Counts {
 // ------------------------------------------------------------------------------------------
 // Generic kernel: one CTA per row at a time, persistent over rows.
 // ------------------------------------------------------------------------------------------
-template <typename T, int NT, int U, bool VEC>
+template <typename T, int NT, int U, bool VEC, bool ENT, bool TERMS>
 __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
   constexpr int VN = Vec<T>::N;
   constexpr int NW = NT / 32;
-  __shared__ float sh_m[NW], sh_s[NW];
-  __shared__ float sh_lse, sh_coef;
+  __shared__ float sh_m[NW], sh_s[NW], sh_s2[NW];
+  __shared__ float sh_lse, sh_coef, sh_ez;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t V = a.V;
@@ -157,7 +172,7 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
   const int64_t tail0 = nvec * VN;
   Counts cnt;
 
-  MetaPipe pipe(a, blockIdx.x, gridDim.x);
+  MetaPipe<TERMS> pipe(a, blockIdx.x, gridDim.x);
   for (int64_t row = blockIdx.x; row < a.T; row += gridDim.x) {
     const RowMeta tm = pipe.advance(row);
     const T* z = static_cast<const T*>(a.logits) + row * a.ld;
@@ -174,6 +189,7 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
         if (tm.idx >= 0) {
           a.loss_tok[tm.idx] = 0.f;
           if (a.logp_tok) a.logp_tok[tm.idx] = 0.f;
+          if (TERMS && a.entropy_tok) a.entropy_tok[tm.idx] = 0.f;
         }
       }
       continue;
@@ -183,8 +199,9 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
     float zy = 0.f;
     if (tid == 0 && !ybad) zy = Vec<T>::load1(z + y);
 
-    // pass 1: online max / sum of exp over the row
+    // pass 1: online max / sum of exp over the row (and sum of exp * z for the entropy)
     MS acc{-INFINITY, 0.f};
+    float acc_s2 = 0.f;
     const uint4* zv = reinterpret_cast<const uint4*>(z);
     for (int64_t j0 = tid; j0 < nvec; j0 += (int64_t)NT * U) {
       float x[U][VN];
@@ -204,49 +221,81 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
 #pragma unroll
         for (int i = 0; i < VN; ++i) gm = fmaxf(gm, x[u][i]);
       if (gm > acc.m) {
-        acc.s *= ex2((acc.m - gm) * kLog2e);
+        const float f = ex2((acc.m - gm) * kLog2e);
+        acc.s *= f;
+        if (ENT) acc_s2 *= f;
         acc.m = gm;
       }
       if (acc.m != -INFINITY) {
 #pragma unroll
         for (int u = 0; u < U; ++u)
 #pragma unroll
-          for (int i = 0; i < VN; ++i) acc.s += ex2((x[u][i] - acc.m) * kLog2e);
+          for (int i = 0; i < VN; ++i) {
+            const float e = ex2((x[u][i] - acc.m) * kLog2e);
+            acc.s += e;
+            if (ENT && e != 0.f) acc_s2 = fmaf(e, x[u][i], acc_s2);  // no-mass elements add nothing
+          }
       }
     }
     for (int64_t e = tail0 + tid; e < V; e += NT) {
       const float x = Vec<T>::load1(z + e);
-      acc = ms_combine(acc, MS{x, 1.f});
+      if (ENT) {
+        const MS3 r = ms3_combine(MS3{acc.m, acc.s, acc_s2}, MS3{x, 1.f, x == -INFINITY ? 0.f : x});
+        acc = MS{r.m, r.s};
+        acc_s2 = r.s2;
+      } else {
+        acc = ms_combine(acc, MS{x, 1.f});
+      }
     }
 
     // CTA reduction (fixed tree) and the per-token epilogue on thread 0
-    MS w = warp_ms(acc);
-    if (lane == 0) { sh_m[warp] = w.m; sh_s[warp] = w.s; }
+    if (ENT) {
+      const MS3 w = warp_ms3<false>(MS3{acc.m, acc.s, acc_s2});
+      if (lane == 0) { sh_m[warp] = w.m; sh_s[warp] = w.s; sh_s2[warp] = w.s2; }
+    } else {
+      MS w = warp_ms(acc);
+      if (lane == 0) { sh_m[warp] = w.m; sh_s[warp] = w.s; }
+    }
     __syncthreads();
     if (warp == 0) {
-      MS v = lane < NW ? MS{sh_m[lane], sh_s[lane]} : MS{-INFINITY, 0.f};
-      v = warp_ms(v);
+      MS v;
+      float ez = 0.f;
+      if (ENT) {
+        MS3 v3 = lane < NW ? MS3{sh_m[lane], sh_s[lane], sh_s2[lane]} : MS3{-INFINITY, 0.f, 0.f};
+        v3 = warp_ms3<false>(v3);
+        v = MS{v3.m, v3.s};
+        ez = v3.s2 / v3.s;
+      } else {
+        v = lane < NW ? MS{sh_m[lane], sh_s[lane]} : MS{-INFINITY, 0.f};
+        v = warp_ms(v);
+      }
       if (lane == 0) {
         const float lse = v.m + logf(v.s);
-        const TokenOut o = token_epilogue(ybad ? __int_as_float(0x7fc00000) : zy, lse,
-                                          a.old_logp != nullptr, tm.old, tm.A, a.eps, a.scale);
+        TokenOut o = token_epilogue(ybad ? __int_as_float(0x7fc00000) : zy, lse,
+                                    a.old_logp != nullptr, tm.old, tm.A, a.eps, a.scale);
+        if (TERMS) apply_terms(o, a.scale, a.kl_kind, a.kl_coef, tm.ref, a.ent_coef, lse - ez);
         a.loss_tok[tm.idx] = o.loss;
         if (a.logp_tok) a.logp_tok[tm.idx] = o.logp;
+        if (TERMS && a.entropy_tok) a.entropy_tok[tm.idx] = ENT ? lse - ez : 0.f;
         cnt.tokens++;
         cnt.valid++;
         cnt.clipped += o.clipped;
         cnt.nonfinite += o.nonfinite;
         sh_lse = lse;
         sh_coef = o.coef;
+        sh_ez = ez;
       }
     }
     __syncthreads();
     const float lse = sh_lse, coef = sh_coef;
+    // entropy gradient: dz_v = p_v (ea + eb z_v) - coef [v == y]
+    const float eb = ENT ? a.scale * a.ent_coef : 0.f;
+    const float ea = ENT ? coef - eb * sh_ez : coef;
 
     // pass 2: dlogits = coef * (softmax - onehot)
     if (dz) {
       uint4* dv = reinterpret_cast<uint4*>(dz);
-      if (coef == 0.f) {
+      if (coef == 0.f && eb == 0.f) {
         const uint4 zero = make_uint4(0, 0, 0, 0);
         for (int64_t j = tid; j < nvec; j += NT) __stcs(dv + j, zero);
         for (int64_t e = tail0 + tid; e < V; e += NT) Vec<T>::store1(dz + e, 0.f);
@@ -255,7 +304,8 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
           float x[VN];
           Vec<T>::unpack(__ldcs(zv + j), x);
 #pragma unroll
-          for (int i = 0; i < VN; ++i) x[i] = coef * ex2((x[i] - lse) * kLog2e);
+          for (int i = 0; i < VN; ++i)
+            x[i] = ENT ? ent_dz(ex2((x[i] - lse) * kLog2e), x[i], ea, eb) : coef * ex2((x[i] - lse) * kLog2e);
           const int64_t off = (int64_t)y - j * VN;
           if (off >= 0 && off < VN) {
 #pragma unroll
@@ -265,7 +315,8 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
           __stcs(dv + j, Vec<T>::pack(x));
         }
         for (int64_t e = tail0 + tid; e < V; e += NT) {
-          float p = coef * ex2((Vec<T>::load1(z + e) - lse) * kLog2e);
+          const float xv = Vec<T>::load1(z + e);
+          float p = ENT ? ent_dz(ex2((xv - lse) * kLog2e), xv, ea, eb) : coef * ex2((xv - lse) * kLog2e);
           if (e == y) p -= coef;
           Vec<T>::store1(dz + e, p);
         }
@@ -298,7 +349,7 @@ __host__ __device__ constexpr int cluster_slice_elems(int64_t V, int C) {
 
 __host__ __device__ constexpr size_t cluster_smem_bytes(int Vs, int NCW) {
   return ((size_t)Vs * 2 + 127) / 128 * 128 + 2 * kMaxChunks * sizeof(uint64_t) +
-         8 * sizeof(float) + 2 * NCW * sizeof(float) + 16;
+         8 * sizeof(float) + 3 * NCW * sizeof(float) + 16;
 }
 
 // Bounded wait used only when draining after a timeout (ignores the abort flag).
@@ -333,6 +384,34 @@ __device__ __forceinline__ void dz_vec(const uint4& u, uint4* dst, float cexp) {
   __stcs(dst, r);
 }
 
+// Eight dlogits with the entropy term: 2^(z log2e - lse2) * (ea + eb z), rounded to bf16.
+__device__ __forceinline__ void dz_vec_ent(const uint4& u, uint4* dst, float lse2, float ea, float eb) {
+  float x[8];
+  Vec<__nv_bfloat16>::unpack(u, x);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = ent_dz(ex2(fmaf(x[i], kLog2e, -lse2)), x[i], ea, eb);
+  __stcs(dst, make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                         pack_bf16x2(x[6], x[7])));
+}
+
+template <int NC, int VPT, int CH>
+__device__ __forceinline__ void pass2_slice_ent(const __nv_bfloat16* slice, uint4* dz, int n_r, int nch, int ct,
+                                                int lane, float lse2, float ea, float eb, uint64_t* empty) {
+  for (int k = 0; k < nch; ++k) {
+    const int nv = min(CH, n_r - k * CH) / 8;
+    const uint4* sv = reinterpret_cast<const uint4*>(slice + k * CH);
+    uint4* dv = dz + k * (CH / 8);
+    if (nv == VPT * NC) {
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) dz_vec_ent(sv[ct + j * NC], dv + ct + j * NC, lse2, ea, eb);
+    } else {
+      for (int v = ct; v < nv; v += NC) dz_vec_ent(sv[v], dv + v, lse2, ea, eb);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[k]);
+  }
+}
+
 // Pass 2 over the CTA's slice; each warp releases chunk k once it is done with it.
 template <bool NEG, int NC, int VPT, int CH>
 __device__ __forceinline__ void pass2_slice(const __nv_bfloat16* slice, uint4* dz, int n_r, int nch,
@@ -352,18 +431,19 @@ __device__ __forceinline__ void pass2_slice(const __nv_bfloat16* slice, uint4* d
   }
 }
 
-template <int C, int NCW, int VPT, int MINB>
+template <int C, int NCW, int VPT, int MINB, bool ENT, bool TERMS>
 __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowArgs a, int Vs) {
   constexpr int NC = NCW * 32;
+  constexpr int WS = ENT ? 3 : 2;  // floats per warp partial
   constexpr int CH = cluster_chunk_elems(NCW, VPT);
   extern __shared__ __align__(128) uint8_t smem[];
   const int slice_bytes = (Vs * 2 + 127) / 128 * 128;
   __nv_bfloat16* slice = reinterpret_cast<__nv_bfloat16*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + slice_bytes);
   uint64_t* empty = full + kMaxChunks;
-  float* xch = reinterpret_cast<float*>(empty + kMaxChunks);  // [2 rows][m, s, z_y, -]
-  float* wpart = xch + 8;                                      // [NCW][m, s]
-  volatile int* s_abort = reinterpret_cast<volatile int*>(wpart + 2 * NCW);
+  float* xch = reinterpret_cast<float*>(empty + kMaxChunks);  // [2 rows][m, s, z_y, s2]
+  float* wpart = xch + 8;                                      // [NCW][m, s, s2]
+  volatile int* s_abort = reinterpret_cast<volatile int*>(wpart + 3 * NCW);
 
   const uint32_t rank = cluster_ctarank();
   const int64_t cid = blockIdx.x / C, ncl = gridDim.x / C;
@@ -390,7 +470,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
   Counts cnt;
   uint32_t vi = 0;  // valid rows so far: phase index of every full/empty barrier
 
-  MetaPipe pipe(a, cid, ncl);
+  MetaPipe<TERMS> pipe(a, cid, ncl);
   for (int64_t row = cid; row < a.T; row += ncl) {
     const RowMeta tm = pipe.advance(row);
     uint4* dz = dg ? reinterpret_cast<uint4*>(dg + row * a.ld_out + base) : nullptr;
@@ -403,6 +483,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
         if (tm.idx >= 0) {
           a.loss_tok[tm.idx] = 0.f;
           if (a.logp_tok) a.logp_tok[tm.idx] = 0.f;
+          if (TERMS && a.entropy_tok) a.entropy_tok[tm.idx] = 0.f;
         }
       }
       continue;
@@ -431,6 +512,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
 
       // pass 1: log2-domain (shift, sum) over the slice, chunk by chunk as it lands
       MS acc{-INFINITY, 0.f};
+      MS3 acc3{-INFINITY, 0.f, 0.f};
       for (int k = 0; k < nch; ++k) {
         mbar_wait_bounded(&full[k], par, s_abort);
         const int nv = min(CH, n_r - k * CH) / 8;
@@ -439,26 +521,48 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
           float x[VPT * 8];
 #pragma unroll
           for (int j = 0; j < VPT; ++j) unpack8_at(sv[ct + j * NC], x + 8 * j);
-          lazy_online2<VPT * 8>(acc, x);
+          if (ENT)
+            lazy_online3<VPT * 8>(acc3, x);
+          else
+            lazy_online2<VPT * 8>(acc, x);
         } else {
           for (int v = ct; v < nv; v += NC) {
             float x[8];
             Vec<__nv_bfloat16>::unpack(sv[v], x);
-            lazy_online2<8>(acc, x);
+            if (ENT)
+              lazy_online3<8>(acc3, x);
+            else
+              lazy_online2<8>(acc, x);
           }
         }
       }
-      const MS w = warp_ms2(acc);
-      if (lane == 0) {
-        wpart[2 * (warp - 1)] = w.m;
-        wpart[2 * (warp - 1) + 1] = w.s;
+      if (ENT) {
+        const MS3 w = warp_ms3<true>(acc3);
+        if (lane == 0) {
+          wpart[WS * (warp - 1)] = w.m;
+          wpart[WS * (warp - 1) + 1] = w.s;
+          wpart[WS * (warp - 1) + 2] = w.s2;
+        }
+      } else {
+        const MS w = warp_ms2(acc);
+        if (lane == 0) {
+          wpart[WS * (warp - 1)] = w.m;
+          wpart[WS * (warp - 1) + 1] = w.s;
+        }
       }
       named_bar_sync(1, NC);
       if (warp == 1 && lane == 0) {
-        MS t{-INFINITY, 0.f};
-        for (int i = 0; i < NCW; ++i) t = ms2_combine(t, MS{wpart[2 * i], wpart[2 * i + 1]});
+        MS3 t{-INFINITY, 0.f, 0.f};
+        if (ENT) {
+          for (int i = 0; i < NCW; ++i) t = ms3_combine2(t, MS3{wpart[WS * i], wpart[WS * i + 1], wpart[WS * i + 2]});
+        } else {
+          MS t2{-INFINITY, 0.f};
+          for (int i = 0; i < NCW; ++i) t2 = ms2_combine(t2, MS{wpart[WS * i], wpart[WS * i + 1]});
+          t = MS3{t2.m, t2.s, 0.f};
+        }
         xb[0] = t.m;
         xb[1] = t.s;
+        if (ENT) xb[3] = t.s2;
         if (!ybad && (int64_t)y >= base && (int64_t)y < base + n_r)
           xb[2] = __bfloat162float(slice[y - base]);
       }
@@ -466,28 +570,45 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
 
       // every consumer combines the C slices in rank order: identical LSE in every CTA
       MS tot{-INFINITY, 0.f};
+      MS3 tot3{-INFINITY, 0.f, 0.f};
       float zy = __int_as_float(0x7fc00000);
       const uint32_t xaddr = smem_u32(xb);
 #pragma unroll
       for (int r = 0; r < C; ++r) {
         const uint32_t ra = mapa_u32(xaddr, (uint32_t)r);
-        tot = ms2_combine(tot, MS{ld_dsmem_f32(ra), ld_dsmem_f32(ra + 4)});
+        if (ENT)
+          tot3 = ms3_combine2(tot3, MS3{ld_dsmem_f32(ra), ld_dsmem_f32(ra + 4), ld_dsmem_f32(ra + 12)});
+        else
+          tot = ms2_combine(tot, MS{ld_dsmem_f32(ra), ld_dsmem_f32(ra + 4)});
         if (!ybad && (int64_t)y >= (int64_t)r * Vs && (int64_t)y < (int64_t)(r + 1) * Vs)
           zy = ld_dsmem_f32(ra + 8);
       }
+      if (ENT) tot = MS{tot3.m, tot3.s};
       const float lse2 = tot.m + log2f(tot.s);  // log2(sum_v 2^(z_v log2 e)) = LSE * log2(e)
-      const TokenOut o = token_epilogue(zy, lse2 * kLn2, a.old_logp != nullptr, tm.old, tm.A, a.eps,
-                                        a.scale);
+      const float ez = ENT ? tot3.s2 / tot3.s : 0.f;  // sum_v p_v z_v
+      TokenOut o = token_epilogue(zy, lse2 * kLn2, a.old_logp != nullptr, tm.old, tm.A, a.eps, a.scale);
+      if (TERMS) apply_terms(o, a.scale, a.kl_kind, a.kl_coef, tm.ref, a.ent_coef, lse2 * kLn2 - ez);
       if (rank == 0 && ct == 0) {
         a.loss_tok[tm.idx] = o.loss;
         if (a.logp_tok) a.logp_tok[tm.idx] = o.logp;
+        if (TERMS && a.entropy_tok) a.entropy_tok[tm.idx] = ENT ? lse2 * kLn2 - ez : 0.f;
         cnt.tokens++;
         cnt.valid++;
         cnt.clipped += o.clipped;
         cnt.nonfinite += o.nonfinite;
       }
       const float coef = o.coef;
-      if (dz && coef != 0.f) {
+      const float eb = ENT ? a.scale * a.ent_coef : 0.f;
+      if (ENT && dz && eb != 0.f) {
+        // with the entropy term: dz_v = p_v (ea + eb z_v) - coef [v == y]
+        const float ea = coef - eb * ez;
+        pass2_slice_ent<NC, VPT, CH>(slice, dz, n_r, nch, ct, lane, lse2, ea, eb, empty);
+        const int64_t yl = ybad ? -1 : (int64_t)y - base;
+        if (yl >= 0 && yl < n_r && ct == (int)(((yl / 8) % (CH / 8)) % NC)) {
+          const float dzy = ent_dz(ex2(fmaf(zy, kLog2e, -lse2)), zy, ea, eb) - coef;
+          reinterpret_cast<__nv_bfloat16*>(dz)[yl] = __float2bfloat16_rn(dzy);
+        }
+      } else if (dz && coef != 0.f) {
         // pass 2: |coef| * softmax = 2^(z log2e - (lse2 - log2|coef|)), the sign applied to
         // the packed bf16 pairs; the target element coef * (p_y - 1) is written on its own
         const float cexp = lse2 - log2f(fabsf(coef));
@@ -522,13 +643,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
   if (tid == 32 && rank == 0) cnt.flush(a.acc);
 }
 
-template <int C, int NCW, int VPT, int MINB>
+template <int C, int NCW, int VPT, int MINB, bool ENT, bool TERMS>
 int launch_cluster(const RowArgs& a, cudaStream_t st) {
   constexpr int CH = cluster_chunk_elems(NCW, VPT);
   const int Vs = cluster_slice_elems(a.V, C);
   if ((Vs + CH - 1) / CH > kMaxChunks) return GRPO_ERR_UNSUPPORTED;
   const size_t smem = cluster_smem_bytes(Vs, NCW);
-  auto kern = row_cluster_kernel<C, NCW, VPT, MINB>;
+  auto kern = row_cluster_kernel<C, NCW, VPT, MINB, ENT, TERMS>;
   static int cached_dev = -1;
   static size_t cached_smem = 0;
   static int cached_clusters = 0;
@@ -561,13 +682,13 @@ int launch_cluster(const RowArgs& a, cudaStream_t st) {
   return GRPO_OK;
 }
 
-template <typename T, int NT, int U>
+template <typename T, int NT, int U, bool ENT, bool TERMS>
 int launch_l2(const RowArgs& a, bool vec, int blocks_per_sm, cudaStream_t st) {
   const int64_t grid = std::min<int64_t>(a.T, (int64_t)sm_count() * blocks_per_sm);
   if (vec)
-    row_l2_kernel<T, NT, U, true><<<(unsigned)grid, NT, 0, st>>>(a);
+    row_l2_kernel<T, NT, U, true, ENT, TERMS><<<(unsigned)grid, NT, 0, st>>>(a);
   else
-    row_l2_kernel<T, NT, U, false><<<(unsigned)grid, NT, 0, st>>>(a);
+    row_l2_kernel<T, NT, U, false, ENT, TERMS><<<(unsigned)grid, NT, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? GRPO_OK : GRPO_ERR_CUDA;
 }
 
@@ -586,28 +707,11 @@ int sm_count() {
 
 using namespace grpo;
 
-extern "C" GRPO_API int grpo_logprob_loss_fwd_bwd(const void* logits, int32_t dtype, int64_t T,
-                                                  int64_t V, int64_t ld, const int64_t* tok_src,
-                                                  const int32_t* target, const float* old_logp,
-                                                  const float* adv_tok, const uint8_t* mask,
-                                                  float clip_eps, float grad_scale,
-                                                  void* dlogits, int64_t ld_out, float* loss_tok,
-                                                  float* logp_tok, grpo_step_acc* acc,
-                                                  void* stream) {
-  if (dtype != GRPO_DTYPE_F32 && dtype != GRPO_DTYPE_BF16) return GRPO_ERR_UNSUPPORTED;
-  if (T < 0 || V < 1 || ld < V || !acc) return GRPO_ERR_INVALID;
-  if (dlogits && ld_out < V) return GRPO_ERR_INVALID;
-  if (T == 0) return GRPO_OK;
-  if (!logits || !target || !adv_tok || !mask || !loss_tok) return GRPO_ERR_INVALID;
-  if (V > (int64_t)INT32_MAX) return GRPO_ERR_INVALID;
+namespace {
 
-  RowArgs a{logits, T, V, ld, tok_src, target, old_logp, adv_tok, mask, clip_eps, grad_scale,
-            dlogits, ld_out, loss_tok, logp_tok, acc};
-  const cudaStream_t st = as_stream(stream);
-  const size_t es = dtype == GRPO_DTYPE_F32 ? 4 : 2;
-  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  const bool vec = al16(logits) && (ld * es) % 16 == 0 &&
-                   (!dlogits || (al16(dlogits) && (ld_out * es) % 16 == 0));
+template <bool ENT, bool TERMS>
+int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
+  const int64_t V = a.V;
   if (dtype == GRPO_DTYPE_BF16) {
     // Large bf16 vocabularies: rows split across a CTA cluster, slices staged in shared
     // memory. Variants (cluster size, consumer warps, vectors per thread, CTAs per SM):
@@ -621,15 +725,65 @@ extern "C" GRPO_API int grpo_logprob_loss_fwd_bwd(const void* logits, int32_t dt
                (cluster_slice_elems(V, C) + cluster_chunk_elems(NCW, 4) - 1) / cluster_chunk_elems(NCW, 4) <=
                    kMaxChunks;
       };
-      if (pin && strcmp(pin, "c3") == 0 && fits(3, 8, 2)) return launch_cluster<3, 8, 4, 2>(a, st);
-      if (pin && strcmp(pin, "c4") == 0 && fits(4, 8, 2)) return launch_cluster<4, 8, 4, 2>(a, st);
-      if (fits(2, 16, 1)) return launch_cluster<2, 16, 4, 1>(a, st);
-      if (fits(4, 8, 2)) return launch_cluster<4, 8, 4, 2>(a, st);
-      if (fits(4, 16, 1)) return launch_cluster<4, 16, 4, 1>(a, st);
+      if (pin && strcmp(pin, "c3") == 0 && fits(3, 8, 2)) return launch_cluster<3, 8, 4, 2, ENT, TERMS>(a, st);
+      if (pin && strcmp(pin, "c4") == 0 && fits(4, 8, 2)) return launch_cluster<4, 8, 4, 2, ENT, TERMS>(a, st);
+      if (fits(2, 16, 1)) return launch_cluster<2, 16, 4, 1, ENT, TERMS>(a, st);
+      if (fits(4, 8, 2)) return launch_cluster<4, 8, 4, 2, ENT, TERMS>(a, st);
+      if (fits(4, 16, 1)) return launch_cluster<4, 16, 4, 1, ENT, TERMS>(a, st);
     }
-    if (V >= 8192) return launch_l2<__nv_bfloat16, 1024, 2>(a, vec, 1, st);
-    return launch_l2<__nv_bfloat16, 128, 2>(a, vec, 16, st);
+    if (V >= 8192) return launch_l2<__nv_bfloat16, 1024, 2, ENT, TERMS>(a, vec, 1, st);
+    return launch_l2<__nv_bfloat16, 128, 2, ENT, TERMS>(a, vec, 16, st);
   }
-  if (V >= 8192) return launch_l2<float, 1024, 2>(a, vec, 1, st);
-  return launch_l2<float, 128, 2>(a, vec, 16, st);
+  if (V >= 8192) return launch_l2<float, 1024, 2, ENT, TERMS>(a, vec, 1, st);
+  return launch_l2<float, 128, 2, ENT, TERMS>(a, vec, 16, st);
+}
+
+}  // namespace
+
+extern "C" GRPO_API int grpo_logprob_loss_fwd_bwd_ex(const void* logits, int32_t dtype, int64_t T, int64_t V,
+                                                     int64_t ld, const int64_t* tok_src, const int32_t* target,
+                                                     const float* old_logp, const float* adv_tok,
+                                                     const uint8_t* mask, float clip_eps, float grad_scale,
+                                                     void* dlogits, int64_t ld_out, float* loss_tok,
+                                                     float* logp_tok, const grpo_loss_terms* terms,
+                                                     grpo_step_acc* acc, void* stream) {
+  if (dtype != GRPO_DTYPE_F32 && dtype != GRPO_DTYPE_BF16) return GRPO_ERR_UNSUPPORTED;
+  if (T < 0 || V < 1 || ld < V || !acc) return GRPO_ERR_INVALID;
+  if (dlogits && ld_out < V) return GRPO_ERR_INVALID;
+  if (terms) {
+    if (terms->kl_kind != GRPO_KL_NONE && terms->kl_kind != GRPO_KL_K1 && terms->kl_kind != GRPO_KL_K3)
+      return GRPO_ERR_INVALID;
+    if (terms->kl_kind != GRPO_KL_NONE && !terms->ref_logp) return GRPO_ERR_INVALID;
+    if (!isfinite(terms->kl_coef) || !isfinite(terms->ent_coef)) return GRPO_ERR_INVALID;
+  }
+  if (T == 0) return GRPO_OK;
+  if (!logits || !target || !adv_tok || !mask || !loss_tok) return GRPO_ERR_INVALID;
+  if (V > (int64_t)INT32_MAX) return GRPO_ERR_INVALID;
+
+  RowArgs a{logits, T, V, ld, tok_src, target, old_logp, adv_tok, mask, clip_eps, grad_scale,
+            dlogits, ld_out, loss_tok, logp_tok, acc,
+            terms ? terms->kl_kind : 0, terms ? terms->kl_coef : 0.f,
+            terms && terms->kl_kind ? terms->ref_logp : nullptr, terms ? terms->ent_coef : 0.f,
+            terms ? terms->entropy_tok : nullptr};
+  const cudaStream_t st = as_stream(stream);
+  const size_t es = dtype == GRPO_DTYPE_F32 ? 4 : 2;
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  const bool vec = al16(logits) && (ld * es) % 16 == 0 &&
+                   (!dlogits || (al16(dlogits) && (ld_out * es) % 16 == 0));
+  // the entropy (as a loss term or as an output) needs sum_v p_v z_v, a third accumulator:
+  // a separate kernel instance
+  if (terms && (terms->ent_coef != 0.f || terms->entropy_tok)) return dispatch<true, true>(a, dtype, vec, st);
+  if (terms && terms->kl_kind != GRPO_KL_NONE) return dispatch<false, true>(a, dtype, vec, st);
+  return dispatch<false, false>(a, dtype, vec, st);
+}
+
+extern "C" GRPO_API int grpo_logprob_loss_fwd_bwd(const void* logits, int32_t dtype, int64_t T, int64_t V,
+                                                  int64_t ld, const int64_t* tok_src, const int32_t* target,
+                                                  const float* old_logp, const float* adv_tok,
+                                                  const uint8_t* mask, float clip_eps, float grad_scale,
+                                                  void* dlogits, int64_t ld_out, float* loss_tok,
+                                                  float* logp_tok, grpo_step_acc* acc, void* stream) {
+  return grpo_logprob_loss_fwd_bwd_ex(logits, dtype, T, V, ld, tok_src, target, old_logp, adv_tok, mask,
+                                      clip_eps, grad_scale, dlogits, ld_out, loss_tok, logp_tok, nullptr, acc,
+                                      stream);
 }

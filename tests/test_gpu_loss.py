@@ -368,3 +368,63 @@ def test_dynamic_bins_equal_fixed_chunks_bitwise(variant):
     assert torch.equal(outs[0][1], outs[1][1])
     assert torch.equal(outs[0][2], outs[1][2]) and torch.equal(outs[0][3], outs[1][3])
     assert outs[0][4] == outs[1][4]
+
+
+# ---- regularisers: KL to the reference policy and the entropy bonus ----------------------------
+
+@pytest.mark.parametrize("variant", ["c2", "c4", "l2"], indirect=True)
+@pytest.mark.parametrize("kl_kind,ent", [(1, 0.0), (2, 0.0), (0, 0.02), (2, 0.05)])
+def test_kl_and_entropy_terms(variant, kl_kind, ent):
+    wl = W.make_workload("tiny", rows=8, positions=24, valid_lo=0, V=32776, dtype="bf16", seed=50 + kl_kind,
+                         std=3.0)
+    case = H.Case(wl)
+    T = wl.T
+    ref = (case.old + np.random.default_rng(3).normal(0, 0.3, T)).astype(np.float32)
+    scale = 1.0 / 97
+    dl = torch.empty_like(case.logits)
+    loss = torch.full((T,), -7.0, device=DEV)
+    logp = torch.full((T,), -7.0, device=DEV)
+    ent_t = torch.full((T,), -7.0, device=DEV)
+    acc = _lib.new_step_acc(DEV)
+    terms = dict(kl_kind=kl_kind, kl_coef=0.1, ref_logp=torch.from_numpy(ref).to(DEV), ent_coef=ent,
+                 entropy_tok=ent_t)
+    _lib.grpo_logprob_loss_fwd_bwd(case.logits, case.d_target, case.d_old, case.d_adv, case.d_mask, wl.eps,
+                                   scale, dl, loss, logp, acc, terms=terms)
+    torch.cuda.synchronize()
+    oterms = dict(kl_kind=kl_kind, kl_coef=float(np.float32(0.1)), ref=ref.astype(np.float64),
+                  ent_coef=float(np.float32(ent)))
+    ref_out = OL.loss_fwd_bwd(case.logits_host, wl.target, case.old, case.adv_tok, wl.mask, wl.eps,
+                              scale, True, oterms)
+    m = wl.mask.astype(bool)
+    gl, gp, ge = H.to_f64(loss), H.to_f64(logp), H.to_f64(ent_t)
+    assert np.all(np.abs(gp[m] - ref_out["logp_tok"][m]) <= 1e-5 * np.maximum(1, np.abs(ref_out["logp_tok"][m])))
+    assert np.all(np.abs(ge[m] - ref_out["entropy"][m]) <= 1e-5 * np.maximum(1, ref_out["entropy"][m]))
+    assert np.all(ge[~m] == 0) and np.all(gl[~m] == 0)
+    assert np.all(np.abs(gl - ref_out["loss_tok"]) <= 1e-5 * np.abs(ref_out["loss_tok"]) + 1e-6)
+    # dlogits: relative bar, plus the ambiguous-clip rows of the smaller tests
+    amb = H.ambiguous_clip(ref_out["ratio"], wl.eps)
+    got = H.to_f64(dl)
+    refd = ref_out["dlogits"]
+    rowmax = np.max(np.abs(refd), axis=1, keepdims=True)
+    bad = np.abs(got - refd) > 1e-2 * np.abs(refd) + 1e-6 * rowmax + 1e-5 * rowmax * (ent > 0)
+    bad[amb] = False
+    # the target element carries coef * (p_y - 1): allow the coefficient-scaled term there
+    rows = np.arange(T)
+    coefs = np.abs(np.array([np.sum(np.abs(refd[t])) for t in range(T)]))
+    tgt_bad = np.abs(got[rows, wl.target] - refd[rows, wl.target]) > 1e-2 * np.abs(refd[rows, wl.target]) + 1e-5 * coefs
+    bad[rows, wl.target] = tgt_bad
+    assert not bad.any(), np.argwhere(bad)[:3]
+    res = _lib.grpo_finish_step(acc, loss)
+    assert res["status"] == 0 and res["n_valid"] == int(wl.mask.sum())
+
+
+def test_terms_reject_bad_arguments():
+    acc = _lib.new_step_acc(DEV)
+    x = torch.zeros((2, 8), device=DEV)
+    i = torch.zeros(2, dtype=torch.int32, device=DEV)
+    mk = torch.ones(2, dtype=torch.uint8, device=DEV)
+    f = torch.zeros(2, device=DEV)
+    with pytest.raises(_lib.GrpoError):
+        _lib.grpo_logprob_loss_fwd_bwd(x, i, None, f, mk, 0.2, 1.0, None, f, None, acc, terms=dict(kl_kind=7))
+    with pytest.raises(_lib.GrpoError):
+        _lib.grpo_logprob_loss_fwd_bwd(x, i, None, f, mk, 0.2, 1.0, None, f, None, acc, terms=dict(kl_kind=1))

@@ -198,3 +198,55 @@ def test_lmhead_oracle_matches_chain_rule():
     assert np.allclose(out["dW"].sum(0), 0, atol=1e-12)
     # the masked token's hidden row gets no gradient
     assert np.all(out["d_h"][2] == 0)
+
+
+@pytest.mark.parametrize("kind", [1, 2])
+@pytest.mark.parametrize("ent", [0.0, 0.03])
+def test_extra_terms_central_differences(kind, ent):
+    # KL to a reference policy (k1 or k3) and an entropy bonus: the analytic dlogits equal
+    # central differences of the per-token loss; the entropy equals scipy's
+    rng = np.random.default_rng(40 + kind)
+    V = 9
+    for _ in range(4):
+        z = rng.normal(0, 1.5, V)
+        y = int(rng.integers(0, V))
+        lsm = sps.log_softmax(z)
+        old = lsm[y] - math.log(rng.choice([0.9, 1.05]))
+        A = float(rng.choice([-1.0, 0.7]))
+        terms = dict(kl_kind=kind, kl_coef=0.1, ref=lsm[y] + rng.normal(0, 0.3), ent_coef=ent)
+        lt, lp, r, cl, dz = L.token_objective(z, y, old, A, 1, EPS, 1.0, True, dict(terms))
+        t2 = dict(terms)
+        L.token_objective(z, y, old, A, 1, EPS, 1.0, False, t2)
+        p = sps.softmax(z)
+        assert t2["entropy"] == pytest.approx(-float(np.sum(p * np.log(p))), rel=1e-12)
+        h = 1e-6
+        for v in range(V):
+            zp, zm = z.copy(), z.copy()
+            zp[v] += h
+            zm[v] -= h
+            fp = L.token_objective(zp, y, old, A, 1, EPS, 1.0, False, dict(terms))[0]
+            fm = L.token_objective(zm, y, old, A, 1, EPS, 1.0, False, dict(terms))[0]
+            assert dz[v] == pytest.approx((fp - fm) / (2 * h), rel=1e-5, abs=1e-9)
+
+
+def test_k3_is_zero_at_the_reference_and_nonnegative():
+    z = np.array([0.5, -1.0, 2.0])
+    lp = float(sps.log_softmax(z)[2])
+    t = dict(kl_kind=2, kl_coef=1.0, ref=lp)
+    base = L.token_objective(z, 2, lp, 0.0, 1, EPS)[0]
+    assert L.token_objective(z, 2, lp, 0.0, 1, EPS, terms=t)[0] == pytest.approx(base, abs=1e-15)
+    for ref in (lp - 1.0, lp + 0.5):
+        t = dict(kl_kind=2, kl_coef=1.0, ref=ref)
+        assert L.token_objective(z, 2, lp, 0.0, 1, EPS, terms=t)[0] >= base
+
+
+def test_entropy_ignores_masked_vocabulary_entries():
+    # a -inf logit has no mass: the entropy and its gradient equal those of the row without it
+    z = np.array([0.3, -np.inf, 1.2, -0.7])
+    zr = np.array([0.3, 1.2, -0.7])
+    t1, t2 = dict(ent_coef=0.1), dict(ent_coef=0.1)
+    l1, _, _, _, d1 = L.token_objective(z, 2, None, 0.5, 1, EPS, 1.0, True, t1)
+    l2, _, _, _, d2 = L.token_objective(zr, 1, None, 0.5, 1, EPS, 1.0, True, t2)
+    assert t1["entropy"] == pytest.approx(t2["entropy"], rel=1e-14)
+    assert l1 == pytest.approx(l2, rel=1e-14)
+    assert d1[1] == 0 and np.allclose(np.delete(d1, 1), d2, rtol=1e-13)
