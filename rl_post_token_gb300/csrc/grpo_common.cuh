@@ -182,15 +182,32 @@ __device__ __forceinline__ void e_pairs(const float (&x)[N], float sh, float (&p
   }
 }
 
+// e_pairs without the no-mass guard: e * z is NaN only where a logit is -inf (or the row is
+// not finite at all), which the caller detects on the block sum.
+template <int N>
+__device__ __forceinline__ void e_pairs_fast(const float (&x)[N], float sh, float (&pe)[N / 2], float (&px)[N / 2]) {
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    const float e0 = ex2(fmaf(x[2 * i], kLog2e, -sh)), e1 = ex2(fmaf(x[2 * i + 1], kLog2e, -sh));
+    pe[i] = e0 + e1;
+    px[i] = fmaf(e1, x[2 * i + 1], e0 * x[2 * i]);
+  }
+}
+
 template <int N>
 __device__ __forceinline__ void lazy_online3(MS3& acc, const float (&x)[N]) {
   if (acc.m == -INFINITY) acc.m = x[0] * kLog2e;
   float pe[N / 2], px[N / 2];
-  e_pairs<N>(x, acc.m, pe, px);
+  e_pairs_fast<N>(x, acc.m, pe, px);
   const float bs = tree_sum(pe);
   if (bs <= 1.8446744e19f) {
+    float bx = tree_sum(px);
+    if (bx != bx) {  // a -inf logit in the block: redo it with no-mass elements adding nothing
+      e_pairs<N>(x, acc.m, pe, px);
+      bx = tree_sum(px);
+    }
     acc.s += bs;
-    acc.s2 += tree_sum(px);
+    acc.s2 += bx;
     return;
   }
   float gm = x[0];

@@ -26,6 +26,7 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <type_traits>
 
 #include "grpo_common.cuh"
 
@@ -347,9 +348,13 @@ __host__ __device__ constexpr int cluster_slice_elems(int64_t V, int C) {
   return (int)((((V + C - 1) / C) + 7) / 8 * 8);
 }
 
+__host__ __device__ constexpr size_t cluster_tail_bytes(int NCW) {
+  return 2 * kMaxChunks * sizeof(uint64_t) + 8 * sizeof(float) + 3 * NCW * sizeof(float) + 16;
+}
+
+// Shared memory of the fixed staging buffer (the smallest ring) plus barriers and exchange.
 __host__ __device__ constexpr size_t cluster_smem_bytes(int Vs, int NCW) {
-  return ((size_t)Vs * 2 + 127) / 128 * 128 + 2 * kMaxChunks * sizeof(uint64_t) +
-         8 * sizeof(float) + 3 * NCW * sizeof(float) + 16;
+  return ((size_t)Vs * 2 + 127) / 128 * 128 + cluster_tail_bytes(NCW);
 }
 
 // Bounded wait used only when draining after a timeout (ignores the abort flag).
@@ -394,12 +399,37 @@ __device__ __forceinline__ void dz_vec_ent(const uint4& u, uint4* dst, float lse
                          pack_bf16x2(x[6], x[7])));
 }
 
+// The shared-memory ring: S slots of one chunk each. A CTA's chunks, in row order, take slots
+// 0, 1, ..., S-1, 0, ...; the slot's phase bit flips at every wrap. With S equal to the
+// chunks of a row every row starts at slot 0 (a fixed staging buffer); with S larger, the
+// producer fills the spare slots with the first chunks of the next row while this row is
+// still being reduced and exchanged.
+struct RingCursor {
+  int slot;
+  uint32_t ph;
+  __device__ __forceinline__ void step(int S) {
+    if (++slot == S) {
+      slot = 0;
+      ph ^= 1u;
+    }
+  }
+  __device__ __forceinline__ void skip(int n, int S) {
+    slot += n;
+    if (slot >= S) {
+      slot -= S;
+      ph ^= 1u;
+    }
+  }
+};
+
+// Pass 2 with the entropy term over the CTA's slice, chunk k read from its ring slot.
 template <int NC, int VPT, int CH>
-__device__ __forceinline__ void pass2_slice_ent(const __nv_bfloat16* slice, uint4* dz, int n_r, int nch, int ct,
-                                                int lane, float lse2, float ea, float eb, uint64_t* empty) {
+__device__ __forceinline__ void pass2_slice_ent(const __nv_bfloat16* ring, RingCursor c, int S, uint4* dz, int n_r,
+                                                int nch, int ct, int lane, float lse2, float ea, float eb,
+                                                uint64_t* empty) {
   for (int k = 0; k < nch; ++k) {
     const int nv = min(CH, n_r - k * CH) / 8;
-    const uint4* sv = reinterpret_cast<const uint4*>(slice + k * CH);
+    const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)c.slot * CH);
     uint4* dv = dz + k * (CH / 8);
     if (nv == VPT * NC) {
 #pragma unroll
@@ -408,17 +438,18 @@ __device__ __forceinline__ void pass2_slice_ent(const __nv_bfloat16* slice, uint
       for (int v = ct; v < nv; v += NC) dz_vec_ent(sv[v], dv + v, lse2, ea, eb);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[k]);
+    if (lane == 0) mbar_arrive(&empty[c.slot]);
+    c.step(S);
   }
 }
 
-// Pass 2 over the CTA's slice; each warp releases chunk k once it is done with it.
+// Pass 2 over the CTA's slice; each warp releases a chunk's slot once it is done with it.
 template <bool NEG, int NC, int VPT, int CH>
-__device__ __forceinline__ void pass2_slice(const __nv_bfloat16* slice, uint4* dz, int n_r, int nch,
-                                            int ct, int lane, float cexp, uint64_t* empty) {
+__device__ __forceinline__ void pass2_slice(const __nv_bfloat16* ring, RingCursor c, int S, uint4* dz, int n_r,
+                                            int nch, int ct, int lane, float cexp, uint64_t* empty) {
   for (int k = 0; k < nch; ++k) {
     const int nv = min(CH, n_r - k * CH) / 8;
-    const uint4* sv = reinterpret_cast<const uint4*>(slice + k * CH);
+    const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)c.slot * CH);
     uint4* dv = dz + k * (CH / 8);
     if (nv == VPT * NC) {
 #pragma unroll
@@ -427,19 +458,36 @@ __device__ __forceinline__ void pass2_slice(const __nv_bfloat16* slice, uint4* d
       for (int v = ct; v < nv; v += NC) dz_vec<NEG>(sv[v], dv + v, cexp);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[k]);
+    if (lane == 0) mbar_arrive(&empty[c.slot]);
+    c.step(S);
   }
 }
 
+// First row at or after `row` (stepping by `stride`) that is read: not padding and mask = 1.
+__device__ __forceinline__ int64_t next_read_row(const RowArgs& a, int64_t row, int64_t stride) {
+  for (; row < a.T; row += stride) {
+    const int64_t src = row_src(a, row);
+    if (src >= 0 && a.mask[src] != 0) return row;
+  }
+  return a.T;
+}
+
+// Bytes of the ring for a slice of Vs elements and S slots of CH elements (S no larger than
+// the slice's chunk count: the fixed staging buffer, whose last slot is only as long as the
+// slice's last chunk).
+__host__ __device__ constexpr size_t cluster_ring_bytes(int Vs, int CH, int S) {
+  return S > (Vs + CH - 1) / CH ? (size_t)S * CH * 2 : ((size_t)Vs * 2 + 127) / 128 * 128;
+}
+
 template <int C, int NCW, int VPT, int MINB, bool ENT, bool TERMS>
-__global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowArgs a, int Vs) {
+__global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowArgs a, int Vs, int S) {
   constexpr int NC = NCW * 32;
   constexpr int WS = ENT ? 3 : 2;  // floats per warp partial
   constexpr int CH = cluster_chunk_elems(NCW, VPT);
   extern __shared__ __align__(128) uint8_t smem[];
-  const int slice_bytes = (Vs * 2 + 127) / 128 * 128;
-  __nv_bfloat16* slice = reinterpret_cast<__nv_bfloat16*>(smem);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + slice_bytes);
+  const int ring_bytes = (int)cluster_ring_bytes(Vs, CH, S);
+  __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + ring_bytes);
   uint64_t* empty = full + kMaxChunks;
   float* xch = reinterpret_cast<float*>(empty + kMaxChunks);  // [2 rows][m, s, z_y, s2]
   float* wpart = xch + 8;                                      // [NCW][m, s, s2]
@@ -451,6 +499,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
   const int64_t base = (int64_t)rank * Vs;
   const int n_r = (int)max((int64_t)0, min((int64_t)Vs, V - base));
   const int nch = (n_r + CH - 1) / CH;
+  const bool ring_mode = S > (Vs + CH - 1) / CH;
+  const int SL = ring_mode ? S : max(nch, 1);      // slots this CTA cycles through
+  const int P = ring_mode ? min(S - nch, nch) : 0;  // next-row chunks issued before this row's exchange
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
@@ -468,55 +519,78 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
   __nv_bfloat16* dg = static_cast<__nv_bfloat16*>(a.dlogits);
   const uint4 zero = make_uint4(0, 0, 0, 0);
   Counts cnt;
-  uint32_t vi = 0;  // valid rows so far: phase index of every full/empty barrier
+  uint32_t issued = 0;  // producer: chunks issued so far (slot reuse starts at SL)
 
-  MetaPipe<TERMS> pipe(a, cid, ncl);
-  for (int64_t row = cid; row < a.T; row += ncl) {
-    const RowMeta tm = pipe.advance(row);
-    uint4* dz = dg ? reinterpret_cast<uint4*>(dg + row * a.ld_out + base) : nullptr;
-    if (!tm.valid) {
-      // masked or padding row: nothing read, nothing exchanged; zero dlogits slice
-      if (warp > 0 && dz)
-        for (int v = tid - 32; v < n_r / 8; v += NC) __stcs(dz + v, zero);
-      if (rank == 0 && tid == 32) {
-        cnt.tokens++;
-        if (tm.idx >= 0) {
-          a.loss_tok[tm.idx] = 0.f;
-          if (a.logp_tok) a.logp_tok[tm.idx] = 0.f;
-          if (TERMS && a.entropy_tok) a.entropy_tok[tm.idx] = 0.f;
-        }
+  if (warp == 0) {
+    // ---- producer: one lane issues the bulk copies; the warp joins one exchange per read row ----
+    RingCursor pc{0, 0u};
+    bool stop = false;  // a wait gave up: issue nothing more
+    auto issue = [&](int64_t row, int k) {
+      if (stop) return;
+      if (issued >= (uint32_t)SL && !mbar_wait_bounded(&empty[pc.slot], pc.ph ^ 1u, s_abort)) {
+        stop = true;
+        return;
       }
-      continue;
-    }
-    const uint32_t par = vi & 1u;
-    float* xb = xch + 4 * (vi & 1u);
-
-    if (warp == 0) {
-      // ---- producer ----
+      const int n_k = min(CH, n_r - k * CH);
+      mbar_arrive_expect_tx(&full[pc.slot], (uint32_t)n_k * 2u);
+      bulk_g2s(ring + (size_t)pc.slot * CH, lg + row * a.ld + base + (int64_t)k * CH, (uint32_t)n_k * 2u,
+               &full[pc.slot]);
+      ++issued;
+      pc.step(SL);
+    };
+    int64_t cur = lane == 0 ? next_read_row(a, cid, ncl) : 0;
+    cur = __shfl_sync(0xffffffffu, cur, 0);
+    int pre = 0;  // chunks of `cur` issued during the previous row
+    while (cur < a.T) {
+      int64_t nxt = 0;
       if (lane == 0) {
-        const __nv_bfloat16* src = lg + row * a.ld + base;
-        for (int k = 0; k < nch; ++k) {
-          if (vi > 0) mbar_wait_bounded(&empty[k], par ^ 1u, s_abort);
-          const int n_k = min(CH, n_r - k * CH);
-          mbar_arrive_expect_tx(&full[k], (uint32_t)n_k * 2u);
-          bulk_g2s(slice + k * CH, src + k * CH, (uint32_t)n_k * 2u, &full[k]);
-        }
+        for (int k = pre; k < nch; ++k) issue(cur, k);
+        nxt = next_read_row(a, cur + ncl, ncl);
+        // the spare slots were released by the previous row's pass 2, which the consumers
+        // finish before this row's exchange: these waits cannot hold up the exchange
+        if (nxt < a.T)
+          for (int k = 0; k < P; ++k) issue(nxt, k);
       }
-      __syncwarp();
-      cluster_sync_all();
-    } else {
-      // ---- consumers ----
-      const int ct = tid - 32;
+      nxt = __shfl_sync(0xffffffffu, nxt, 0);
+      cluster_sync_all();  // this row's exchange
+      pre = P;
+      cur = nxt;
+    }
+  } else {
+    // ---- consumers ----
+    const int ct = tid - 32;
+    RingCursor rc{0, 0u};  // slot of the current row's first chunk
+    uint32_t vi = 0;       // rows read so far: selects the exchange buffer
+    MetaPipe<TERMS> pipe(a, cid, ncl);
+    for (int64_t row = cid; row < a.T; row += ncl) {
+      const RowMeta tm = pipe.advance(row);
+      uint4* dz = dg ? reinterpret_cast<uint4*>(dg + row * a.ld_out + base) : nullptr;
+      if (!tm.valid) {
+        // masked or padding row: nothing read, nothing exchanged; zero dlogits slice
+        if (dz)
+          for (int v = ct; v < n_r / 8; v += NC) __stcs(dz + v, zero);
+        if (rank == 0 && ct == 0) {
+          cnt.tokens++;
+          if (tm.idx >= 0) {
+            a.loss_tok[tm.idx] = 0.f;
+            if (a.logp_tok) a.logp_tok[tm.idx] = 0.f;
+            if (TERMS && a.entropy_tok) a.entropy_tok[tm.idx] = 0.f;
+          }
+        }
+        continue;
+      }
+      float* xb = xch + 4 * (vi & 1u);
       const int32_t y = tm.y;
       const bool ybad = y < 0 || (int64_t)y >= V;
 
       // pass 1: log2-domain (shift, sum) over the slice, chunk by chunk as it lands
       MS acc{-INFINITY, 0.f};
       MS3 acc3{-INFINITY, 0.f, 0.f};
+      RingCursor c = rc;
       for (int k = 0; k < nch; ++k) {
-        mbar_wait_bounded(&full[k], par, s_abort);
+        mbar_wait_bounded(&full[c.slot], c.ph, s_abort);
         const int nv = min(CH, n_r - k * CH) / 8;
-        const uint4* sv = reinterpret_cast<const uint4*>(slice + k * CH);
+        const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)c.slot * CH);
         if (nv == VPT * NC) {  // full chunk: exactly VPT 16-byte vectors per consumer thread
           float x[VPT * 8];
 #pragma unroll
@@ -535,6 +609,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
               lazy_online2<8>(acc, x);
           }
         }
+        c.step(SL);
       }
       if (ENT) {
         const MS3 w = warp_ms3<true>(acc3);
@@ -563,8 +638,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
         xb[0] = t.m;
         xb[1] = t.s;
         if (ENT) xb[3] = t.s2;
-        if (!ybad && (int64_t)y >= base && (int64_t)y < base + n_r)
-          xb[2] = __bfloat162float(slice[y - base]);
+        if (!ybad && (int64_t)y >= base && (int64_t)y < base + n_r) {
+          const int off = (int)((int64_t)y - base), k = off / CH;
+          RingCursor cy = rc;
+          cy.skip(k, SL);
+          xb[2] = __bfloat162float(ring[(size_t)cy.slot * CH + (off - k * CH)]);
+        }
       }
       cluster_sync_all();
 
@@ -602,7 +681,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
       if (ENT && dz && eb != 0.f) {
         // with the entropy term: dz_v = p_v (ea + eb z_v) - coef [v == y]
         const float ea = coef - eb * ez;
-        pass2_slice_ent<NC, VPT, CH>(slice, dz, n_r, nch, ct, lane, lse2, ea, eb, empty);
+        pass2_slice_ent<NC, VPT, CH>(ring, rc, SL, dz, n_r, nch, ct, lane, lse2, ea, eb, empty);
         const int64_t yl = ybad ? -1 : (int64_t)y - base;
         if (yl >= 0 && yl < n_r && ct == (int)(((yl / 8) % (CH / 8)) % NC)) {
           const float dzy = ent_dz(ex2(fmaf(zy, kLog2e, -lse2)), zy, ea, eb) - coef;
@@ -613,9 +692,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
         // the packed bf16 pairs; the target element coef * (p_y - 1) is written on its own
         const float cexp = lse2 - log2f(fabsf(coef));
         if (coef < 0.f)
-          pass2_slice<true, NC, VPT, CH>(slice, dz, n_r, nch, ct, lane, cexp, empty);
+          pass2_slice<true, NC, VPT, CH>(ring, rc, SL, dz, n_r, nch, ct, lane, cexp, empty);
         else
-          pass2_slice<false, NC, VPT, CH>(slice, dz, n_r, nch, ct, lane, cexp, empty);
+          pass2_slice<false, NC, VPT, CH>(ring, rc, SL, dz, n_r, nch, ct, lane, cexp, empty);
         // the target element overwrites what the vector pass wrote (same thread, program order)
         const int64_t yl = ybad ? -1 : (int64_t)y - base;
         if (yl >= 0 && yl < n_r && ct == (int)(((yl / 8) % (CH / 8)) % NC)) {
@@ -626,29 +705,55 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
         if (dz)
           for (int v = ct; v < n_r / 8; v += NC) __stcs(dz + v, zero);
         __syncwarp();
-        if (lane == 0)
-          for (int k = 0; k < nch; ++k) mbar_arrive(&empty[k]);
+        if (lane == 0) {
+          RingCursor ce = rc;
+          for (int k = 0; k < nch; ++k) {
+            mbar_arrive(&empty[ce.slot]);
+            ce.step(SL);
+          }
+        }
       }
+      rc.skip(nch, SL);
+      ++vi;
     }
-    ++vi;
   }
 
+  __syncthreads();
   if (*s_abort) {
-    // a wait gave up: let any copy still in flight land before the CTA's memory goes away
-    if (tid == 0 && vi > 0)
-      for (int k = 0; k < nch; ++k) mbar_drain(&full[k], (vi - 1) & 1u);
+    // a wait gave up: let every copy still in flight land before the CTA's memory goes away
+    // (the last use of slot s is copy number issued-1-s counted back in steps of SL)
+    if (tid == 0)
+      for (int sl = 0; sl < SL && (uint32_t)sl < issued; ++sl)
+        mbar_drain(&full[sl], ((issued - 1u - (uint32_t)sl) / (uint32_t)SL) & 1u);
     if (tid == 0) atomicOr(&a.acc->flags, kFlagWaitTimeout);
   }
   cluster_sync_all();  // no CTA leaves while a peer may still read its exchange slots
   if (tid == 32 && rank == 0) cnt.flush(a.acc);
 }
 
+size_t max_smem_optin();
+
 template <int C, int NCW, int VPT, int MINB, bool ENT, bool TERMS>
 int launch_cluster(const RowArgs& a, cudaStream_t st) {
   constexpr int CH = cluster_chunk_elems(NCW, VPT);
   const int Vs = cluster_slice_elems(a.V, C);
-  if ((Vs + CH - 1) / CH > kMaxChunks) return GRPO_ERR_UNSUPPORTED;
-  const size_t smem = cluster_smem_bytes(Vs, NCW);
+  const int nchm = (Vs + CH - 1) / CH;
+  if (nchm > kMaxChunks) return GRPO_ERR_UNSUPPORTED;
+  // Ring slots: a CTA alone on its SM takes as many chunk slots as the opt-in shared memory
+  // holds (the spare ones carry the next row); CTAs that share an SM keep the fixed buffer.
+  int S = nchm;
+  int s_fit = 0;
+  const size_t optin = max_smem_optin();
+  if (MINB == 1 && optin > cluster_tail_bytes(NCW)) {
+    s_fit = (int)std::min<size_t>(kMaxChunks, (optin - cluster_tail_bytes(NCW)) / ((size_t)CH * 2));
+    if (s_fit > nchm) S = s_fit;
+  }
+  if (const char* ov = getenv("GRPO_ROWPASS_SLOTS")) {  // 0: fixed buffer; n: n slots if they fit
+    const int n = atoi(ov);
+    if (n == 0) S = nchm;
+    else if (n > nchm && n <= s_fit) S = n;
+  }
+  const size_t smem = cluster_ring_bytes(Vs, CH, S) + cluster_tail_bytes(NCW);
   auto kern = row_cluster_kernel<C, NCW, VPT, MINB, ENT, TERMS>;
   static int cached_dev = -1;
   static size_t cached_smem = 0;
@@ -678,7 +783,7 @@ int launch_cluster(const RowArgs& a, cudaStream_t st) {
   }
   const int64_t clusters = std::min<int64_t>(a.T, cached_clusters);
   cfg.gridDim = dim3((unsigned)(clusters * C), 1, 1);
-  GRPO_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, a, Vs));
+  GRPO_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, a, Vs, S));
   return GRPO_OK;
 }
 
@@ -690,6 +795,17 @@ int launch_l2(const RowArgs& a, bool vec, int blocks_per_sm, cudaStream_t st) {
   else
     row_l2_kernel<T, NT, U, false, ENT, TERMS><<<(unsigned)grid, NT, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? GRPO_OK : GRPO_ERR_CUDA;
+}
+
+size_t max_smem_optin() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return (size_t)cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess || n < 0) n = 0;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return (size_t)n;
 }
 
 int sm_count() {
@@ -715,21 +831,35 @@ int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
   if (dtype == GRPO_DTYPE_BF16) {
     // Large bf16 vocabularies: rows split across a CTA cluster, slices staged in shared
     // memory. Variants (cluster size, consumer warps, vectors per thread, CTAs per SM):
-    // c2 = (2, 16, 4, 1), c3 = (3, 8, 4, 2), c4 = (4, 8, 4, 2).
+    // c2 = (2, 16, 4, 1) with a ring of spare slots, c3 = (3, 8, 4, 2), c4 = (4, 8, 4, 2)
+    // with fixed staging buffers; the entropy instances take 2 vectors per thread.
     const char* pin = getenv("GRPO_ROWPASS");
     const bool cluster_ok = vec && V % 8 == 0 && V >= 16384;
     if (cluster_ok && !(pin && strcmp(pin, "l2") == 0)) {
       const int64_t cap = 227 * 1024;
-      auto fits = [&](int C, int NCW, int minb) {
+      auto fits = [&](int C, int NCW, int minb, int vpt) {
         return (int64_t)cluster_smem_bytes(cluster_slice_elems(V, C), NCW) * minb <= cap &&
-               (cluster_slice_elems(V, C) + cluster_chunk_elems(NCW, 4) - 1) / cluster_chunk_elems(NCW, 4) <=
+               (cluster_slice_elems(V, C) + cluster_chunk_elems(NCW, vpt) - 1) / cluster_chunk_elems(NCW, vpt) <=
                    kMaxChunks;
       };
-      if (pin && strcmp(pin, "c3") == 0 && fits(3, 8, 2)) return launch_cluster<3, 8, 4, 2, ENT, TERMS>(a, st);
-      if (pin && strcmp(pin, "c4") == 0 && fits(4, 8, 2)) return launch_cluster<4, 8, 4, 2, ENT, TERMS>(a, st);
-      if (fits(2, 16, 1)) return launch_cluster<2, 16, 4, 1, ENT, TERMS>(a, st);
-      if (fits(4, 8, 2)) return launch_cluster<4, 8, 4, 2, ENT, TERMS>(a, st);
-      if (fits(4, 16, 1)) return launch_cluster<4, 16, 4, 1, ENT, TERMS>(a, st);
+      // the entropy instances carry a third accumulator: half-size chunks keep them in registers
+      // where the chunk count allows
+      auto c34 = [&](auto c_tag) {
+        constexpr int C = decltype(c_tag)::value;
+        if constexpr (ENT)
+          if (fits(C, 8, 2, 2)) return launch_cluster<C, 8, 2, 2, ENT, TERMS>(a, st);
+        return launch_cluster<C, 8, 4, 2, ENT, TERMS>(a, st);
+      };
+      using C3 = std::integral_constant<int, 3>;
+      using C4 = std::integral_constant<int, 4>;
+      if (pin && strcmp(pin, "c3") == 0 && fits(3, 8, 2, 4)) return c34(C3{});
+      if (pin && strcmp(pin, "c4") == 0 && fits(4, 8, 2, 4)) return c34(C4{});
+      if (fits(2, 16, 1, 4)) {
+        if constexpr (ENT) return launch_cluster<2, 16, 2, 1, ENT, TERMS>(a, st);
+        else return launch_cluster<2, 16, 4, 1, ENT, TERMS>(a, st);
+      }
+      if (fits(4, 8, 2, 4)) return c34(C4{});
+      if (fits(4, 16, 1, 4)) return launch_cluster<4, 16, 4, 1, ENT, TERMS>(a, st);
     }
     if (V >= 8192) return launch_l2<__nv_bfloat16, 1024, 2, ENT, TERMS>(a, vec, 1, st);
     return launch_l2<__nv_bfloat16, 128, 2, ENT, TERMS>(a, vec, 16, st);

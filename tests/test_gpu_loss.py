@@ -341,6 +341,57 @@ def test_cluster_chunked_equals_unchunked_bitwise(variant):
     assert outs[0][2] == outs[1][2]
 
 
+@pytest.mark.parametrize("V", [16384, 32776, 151936])
+def test_ring_slots_equal_fixed_buffer_bitwise(V, monkeypatch):
+    # The shared-memory ring only changes where a chunk waits and when it is copied, never
+    # the arithmetic: the fixed staging buffer (0), a ring with one spare slot or less (6) and
+    # the default ring must give the same bits. 16384: a whole row per chunk; 32776: the two
+    # CTAs of a cluster hold different chunk counts; 151936: the product vocabulary.
+    monkeypatch.setenv("GRPO_ROWPASS", "c2")
+    wl = W.make_workload("tiny", rows=12, positions=20, valid_lo=0, V=V, dtype="bf16", seed=V % 389, std=2.0)
+    case = H.Case(wl)
+    T = case.logits.shape[0]
+    rng = np.random.default_rng(3)
+    perm = rng.permutation(T)
+    pads = rng.choice(T, 9)
+    src = np.concatenate([perm, -1 - pads]).astype(np.int64)
+    rng.shuffle(src)
+    tok_src = torch.from_numpy(src).to(DEV)
+    lg = case.logits[torch.from_numpy(np.where(src >= 0, src, -1 - src)).to(DEV)]
+    outs = {}
+    for slots in ("0", "6", None):
+        if slots is None:
+            monkeypatch.delenv("GRPO_ROWPASS_SLOTS", raising=False)
+        else:
+            monkeypatch.setenv("GRPO_ROWPASS_SLOTS", slots)
+        dl, loss, logp, acc = _run_direct(case, 1.0 / 97, tok_src=tok_src, logits=lg)
+        res = _lib.grpo_finish_step(acc, loss, expected_N=int(case.mask.sum()))
+        outs[slots] = (dl.view(torch.int16).clone(), loss.clone(), logp.clone(), res)
+    for k in ("6", None):
+        assert torch.equal(outs[k][0], outs["0"][0]), k
+        assert torch.equal(outs[k][1], outs["0"][1]) and torch.equal(outs[k][2], outs["0"][2]), k
+        assert outs[k][3] == outs["0"][3], k
+    assert outs[None][3]["status"] == 0
+
+
+def test_cluster_long_masked_runs(monkeypatch):
+    # Read rows only in three short windows, separated by masked runs several grid strides
+    # long: the producer's look-ahead skips many rows at a time and a third of the clusters
+    # read no row at all; every row still gets its loss and its (zero or full) dlogits row.
+    monkeypatch.setenv("GRPO_ROWPASS", "c2")
+    wl = W.make_workload("tiny", rows=20, positions=30, valid_lo=0, V=16384, dtype="bf16", seed=41, std=2.0)
+    case = H.Case(wl)
+    T = case.logits.shape[0]
+    assert T == 600
+    m = np.zeros(T, np.uint8)
+    m[0:5] = 1
+    m[310:330] = 1
+    m[590:600] = 1
+    case.mask = m
+    case.d_mask = torch.from_numpy(m).to(DEV)
+    _check_case(case, scale=1.0 / 35)
+
+
 @pytest.mark.parametrize("variant", ["c2", "l2"], indirect=True)
 def test_dynamic_bins_equal_fixed_chunks_bitwise(variant):
     # one mini-batch planned as fixed chunks and as token-budget bins (rows reordered, chunk
@@ -416,6 +467,47 @@ def test_kl_and_entropy_terms(variant, kl_kind, ent):
     assert not bad.any(), np.argwhere(bad)[:3]
     res = _lib.grpo_finish_step(acc, loss)
     assert res["status"] == 0 and res["n_valid"] == int(wl.mask.sum())
+
+
+@pytest.mark.parametrize("variant", ["c2", "c4", "l2"], indirect=True)
+def test_entropy_with_masked_vocabulary(variant):
+    # A tenth of every row's vocabulary is -inf (a masked vocabulary; never the target): those
+    # elements carry no mass, add nothing to sum p z (p log p -> 0), and get a zero gradient.
+    wl = W.make_workload("tiny", rows=8, positions=16, valid_lo=0, V=32776, dtype="bf16", seed=61, std=2.0)
+    case = H.Case(wl)
+    T, V = wl.T, wl.V
+    rng = np.random.default_rng(5)
+    off = rng.random((T, V)) < 0.1
+    off[np.arange(T), wl.target] = False
+    lg = case.logits.clone()
+    lg[torch.from_numpy(off).to(DEV)] = float("-inf")
+    host = W.logits_to_host(lg)
+    scale = 1.0 / 61
+    dl = torch.empty_like(lg)
+    loss = torch.full((T,), -7.0, device=DEV)
+    logp = torch.full((T,), -7.0, device=DEV)
+    ent_t = torch.full((T,), -7.0, device=DEV)
+    acc = _lib.new_step_acc(DEV)
+    _lib.grpo_logprob_loss_fwd_bwd(lg, case.d_target, case.d_old, case.d_adv, case.d_mask, wl.eps, scale, dl,
+                                   loss, logp, acc, terms=dict(ent_coef=0.03, entropy_tok=ent_t))
+    torch.cuda.synchronize()
+    ref_out = OL.loss_fwd_bwd(host, wl.target, case.old, case.adv_tok, wl.mask, wl.eps, scale, True,
+                              dict(kl_kind=0, kl_coef=0.0, ref=None, ent_coef=float(np.float32(0.03))))
+    m = wl.mask.astype(bool)
+    ge, gp = H.to_f64(ent_t), H.to_f64(logp)
+    assert np.all(np.isfinite(ge)) and np.all(np.isfinite(gp))
+    assert np.all(np.abs(ge[m] - ref_out["entropy"][m]) <= 1e-5 * np.maximum(1, ref_out["entropy"][m]))
+    assert np.all(np.abs(gp[m] - ref_out["logp_tok"][m]) <= 1e-5 * np.maximum(1, np.abs(ref_out["logp_tok"][m])))
+    got = H.to_f64(dl)
+    assert np.all(np.isfinite(got)) and np.all(got[off] == 0)
+    refd = ref_out["dlogits"]
+    rowmax = np.max(np.abs(refd), axis=1, keepdims=True)
+    amb = H.ambiguous_clip(ref_out["ratio"], wl.eps)
+    bad = np.abs(got - refd) > 1e-2 * np.abs(refd) + 1e-5 * rowmax
+    bad[amb] = False
+    assert not bad.any(), np.argwhere(bad)[:3]
+    res = _lib.grpo_finish_step(acc, loss)
+    assert res["status"] == 0 and res["n_nonfinite"] == 0
 
 
 def test_terms_reject_bad_arguments():
