@@ -32,7 +32,17 @@ sys.path.insert(0, ROOT)
 METRIC = "GRPO loss fwd+bwd valid tokens/s at V=151936 bf16; % of HBM roofline"
 UNIT = "valid tokens/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "rl_post_token_gb300", "csrc", "grpo_rowpass.cu")
+# sources the row-pass kernel is compiled from (the profile records their combined hash)
+KERNEL_SRC = tuple(os.path.join(ROOT, "rl_post_token_gb300", "csrc", f)
+                   for f in ("grpo_rowpass.cu", "grpo_common.cuh"))
+
+
+def kernel_source_sha256() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SRC:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
+
 
 WORKLOAD_TEXT = {
     "qwen_step": "Qwen3-VL-2B-shaped step: 8 prompts x 4 rollouts, completion lengths U[128,2048] "
@@ -154,8 +164,7 @@ def profiled_traffic():
     m2 = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
     if not (m1 and m2):
         return None
-    cur = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
-    return float(m1.group(1)) if cur == m2.group(1) else None
+    return float(m1.group(1)) if kernel_source_sha256() == m2.group(1) else None
 
 
 # ---- oracle timing (CPU baseline and reference arm) ----------------------------------------------
