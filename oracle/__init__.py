@@ -15,6 +15,8 @@ What it computes, each step written out plainly from the pages (see each module'
 * ``oracle.advantage`` -- the group-normalised scalar advantage per rollout (float64).
 * ``oracle.loss``      -- per-token log-softmax, ratio against the frozen pi_old, clipped
   surrogate, masking, the token-mean over the whole step and the analytic dlogits (float64).
+* ``oracle.aggregate`` -- the step loss under token-mean and the two sequence-level modes,
+  and the per-token gradient scale each implies (float64).
 
 Pinning status (what ties each function to something other than itself; see ``tests/``):
 
@@ -26,4 +28,7 @@ Pinning status (what ties each function to something other than itself; see ``te
 * advantage                 -- hand-worked cases and numpy's own mean/std.
 * loss / gradient           -- ratio == 1 closed form, scipy log_softmax, central finite
   differences on tiny vocabularies, row sums of dlogits, clip hand cases, padding rows.
+* aggregation modes         -- a hand-worked step, closed forms relating the modes (equal
+  full rows, a single row), linearity, central differences through the logits, row-order
+  invariance, the empty step.
 """

@@ -127,8 +127,10 @@ def loss_fwd_bwd(logits, target, old_logp, adv_tok, mask, eps, scale=1.0, want_g
     """All token rows of ``logits`` ([T, V], float or bf16 bits).
 
     Returns dict with float64 ``loss_tok``, ``logp_tok``, ``ratio``, bool ``clipped`` and,
-    if ``want_grad``, float64 ``dlogits`` [T, V]. ``terms`` = dict(kl_kind, kl_coef, ref (array
-    per token), ent_coef) adds the regularisers of ``token_objective`` (output ``entropy``).
+    if ``want_grad``, float64 ``dlogits`` [T, V]. ``scale`` is one gradient scale for every
+    token or an array of per-token scales (an aggregation mode's dL/dl_t). ``terms`` =
+    dict(kl_kind, kl_coef, ref (array per token), ent_coef) adds the regularisers of
+    ``token_objective`` (output ``entropy``).
     """
     T = logits.shape[0]
     V = logits.shape[1] if logits.ndim == 2 else 0
@@ -148,8 +150,9 @@ def loss_fwd_bwd(logits, target, old_logp, adv_tok, mask, eps, scale=1.0, want_g
             tt = dict(kl_kind=terms.get("kl_kind", 0), kl_coef=terms.get("kl_coef", 0.0),
                       ent_coef=terms.get("ent_coef", 0.0),
                       ref=None if terms.get("ref") is None else terms["ref"][t])
+        st = scale[t] if np.ndim(scale) else scale
         lt, lp, r, cl, dz = token_objective(z, int(target[t]), old, adv_tok[t], int(mask[t]),
-                                            eps, scale, want_grad, tt)
+                                            eps, st, want_grad, tt)
         if tt is not None:
             out["entropy"][t] = tt["entropy"]
         out["loss_tok"][t] = lt
