@@ -143,6 +143,34 @@ GRPO_API int grpo_plan_token_index(const grpo_plan* plan, int32_t n_rows_in,
                                    const int64_t* row_tok_off, int64_t* tok_src, int64_t cap,
                                    int64_t* n_out);
 
+/* Loss aggregation modes ("Sizing mini-batches and micro-batches", "The hard part: deferred
+ * normalization": token mean over the step; "22-mini-batch-micro-batch-dynamic-batch-size的区别",
+ * section 5: token-mean divides by the global token count, the sequence-level modes by the
+ * global number of sequences). The pages do not print the sequence-level modes; reading, for
+ * the input rows r of one step with n_r valid tokens, N = sum n_r and B = rows with n_r >= 1:
+ *   TOKEN_MEAN          L = sum_t l_t / max(N, 1)
+ *   SEQ_MEAN_TOKEN_SUM  L = sum_r (sum_{t in r} l_t) / max(B, 1)
+ *   SEQ_MEAN_TOKEN_MEAN L = sum_r (sum_{t in r} l_t / max(n_r, 1)) / max(B, 1)
+ * On one GPU the data-parallel compensation factor is 1. */
+#define GRPO_AGG_TOKEN_MEAN          0
+#define GRPO_AGG_SEQ_MEAN_TOKEN_SUM  1
+#define GRPO_AGG_SEQ_MEAN_TOKEN_MEAN 2
+
+/* Divisor and per-token weights of an aggregation mode for every optimizer step of a plan
+ * (host only): step_divisor[s] = N_s (TOKEN_MEAN) or B_s (sequence-level modes), and, when
+ * w_tok is non-NULL, w_tok[t] = 1/max(n_r, 1) rounded to float for every token t of input row r
+ * under SEQ_MEAN_TOKEN_MEAN, else 1. A step's loss is then sum_t w_t loss_t / max(D_s, 1) and
+ * each token's gradient scale grad_scale * w_t with grad_scale = 1/max(D_s, 1) (or 1, deferred).
+ *  plan         host, from grpo_plan_microbatches (step_in_row_off is read)
+ *  row_tok_off  host int64 [n_rows_in + 1] token offsets of the input rows
+ *  row_valid    host int32 [n_rows_in] mask = 1 positions per input row (as given to the planner)
+ *  step_divisor host int64 [plan->n_steps]
+ *  w_tok        host float [row_tok_off[n_rows_in]] or NULL
+ * Errors: GRPO_ERR_INVALID (NULL required pointer, unknown mode, inconsistent offsets). */
+GRPO_API int grpo_plan_token_weights(const grpo_plan* plan, int32_t n_rows_in,
+                                     const int64_t* row_tok_off, const int32_t* row_valid,
+                                     int32_t agg, int64_t* step_divisor, float* w_tok);
+
 /* ---- advantage --------------------------------------------------------------------------- */
 
 /* Group-normalised advantage ("03 Data Protocol and Batch Lifecycle", response mask
@@ -169,8 +197,10 @@ GRPO_API int grpo_group_advantage(const float* rewards, int32_t n_rollouts, int3
  * chunk). Loss calls add integer counts to it (order-independent); grpo_finish_step reads
  * them, writes `result`, and zeroes the counters for the next step. */
 typedef struct grpo_step_result {
-  double  loss;        /* loss_sum / max(N, 1) */
-  double  loss_sum;    /* sum of loss_tok over the step, float64, fixed order */
+  double  loss;        /* loss_sum / max(D, 1), D the step's divisor (N unless the finish was
+                          given another, see grpo_finish_step_ex) */
+  double  loss_sum;    /* sum of loss_tok (times w_tok when given) over the step, float64,
+                          fixed order */
   double  clipfrac;    /* n_clipped / max(N, 1) */
   int64_t n_valid;     /* N: mask = 1 tokens seen by the step's loss calls */
   int64_t n_clipped;   /* valid tokens whose clip bound (gradient 0) */
@@ -183,7 +213,8 @@ typedef struct grpo_step_result {
 typedef struct grpo_step_acc {
   uint64_t n_valid, n_clipped, n_nonfinite, n_tokens;
   uint32_t flags, reserved0;
-  uint64_t reserved[3];
+  int64_t  divisor;     /* written by the finish: the step's divisor D (read by its gradient scaling) */
+  uint64_t reserved[2];
   grpo_step_result result;
 } grpo_step_acc;
 
@@ -236,6 +267,10 @@ typedef struct grpo_loss_terms {
   float   ent_coef;      /* entropy bonus coefficient, 0 = off */
   float*  entropy_tok;   /* device float per token, indexed like loss_tok, or NULL; written
                             whenever non-NULL, also with ent_coef = 0 (entropy as a metric) */
+  const float* w_tok;    /* device float per token, indexed like adv_tok, or NULL: a weight
+                            multiplying grad_scale in that token's gradient (all terms), e.g.
+                            1/max(n_r, 1) of GRPO_AGG_SEQ_MEAN_TOKEN_MEAN (see
+                            grpo_plan_token_weights); loss_tok stays unweighted */
 } grpo_loss_terms;
 
 /* grpo_logprob_loss_fwd_bwd with the regularisers above added to every valid token's loss
@@ -272,6 +307,17 @@ GRPO_API int grpo_finish_step(grpo_step_acc* acc, const float* loss_tok, int64_t
                               int64_t expected_N, int32_t deferred, void* const* grad_bufs,
                               const int64_t* grad_numels, const int32_t* grad_dtypes,
                               int32_t n_bufs, grpo_step_result* result_host, void* stream);
+
+/* grpo_finish_step for any aggregation mode: loss_sum = sum_t w_tok[t] * loss_tok[t] (each
+ * product exact in float64; w_tok NULL = 1) in the same fixed order, loss = loss_sum /
+ * max(D, 1) and the deferred gradient scale 1/max(D, 1), where D = divisor if >= 0, else the
+ * counted N. grpo_finish_step is this call with w_tok NULL and divisor -1.
+ *  w_tok    device float [n_tok] or NULL (the step's slice of grpo_plan_token_weights' output) */
+GRPO_API int grpo_finish_step_ex(grpo_step_acc* acc, const float* loss_tok, int64_t n_tok,
+                                 const float* w_tok, int64_t divisor, int64_t expected_N,
+                                 int32_t deferred, void* const* grad_bufs,
+                                 const int64_t* grad_numels, const int32_t* grad_dtypes,
+                                 int32_t n_bufs, grpo_step_result* result_host, void* stream);
 
 /* ---- accumulation window (host) ----------------------------------------------------------- */
 

@@ -30,6 +30,9 @@ ERR_KERNEL = -9
 ERR_UNSUPPORTED = -10
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
+AGG_TOKEN_MEAN = 0
+AGG_SEQ_MEAN_TOKEN_SUM = 1
+AGG_SEQ_MEAN_TOKEN_MEAN = 2
 ACC_BYTES = 128
 
 _i32p = C.POINTER(C.c_int32)
@@ -72,7 +75,7 @@ class grpo_window(C.Structure):
 
 class grpo_loss_terms(C.Structure):
     _fields_ = [("kl_kind", C.c_int32), ("kl_coef", C.c_float), ("ref_logp", C.c_void_p),
-                ("ent_coef", C.c_float), ("entropy_tok", C.c_void_p)]
+                ("ent_coef", C.c_float), ("entropy_tok", C.c_void_p), ("w_tok", C.c_void_p)]
 
 
 class grpo_step_result(C.Structure):
@@ -112,6 +115,12 @@ def _lib() -> C.CDLL:
     lib.grpo_logprob_loss_fwd_bwd_ex.restype = C.c_int
     lib.grpo_finish_step.argtypes = [vp, vp, C.c_int64, C.c_int64, C.c_int32, C.POINTER(vp), _i64p,
                                      _i32p, C.c_int32, C.POINTER(grpo_step_result), vp]
+    lib.grpo_finish_step_ex.argtypes = [vp, vp, C.c_int64, vp, C.c_int64, C.c_int64, C.c_int32, C.POINTER(vp),
+                                        _i64p, _i32p, C.c_int32, C.POINTER(grpo_step_result), vp]
+    lib.grpo_finish_step_ex.restype = C.c_int
+    lib.grpo_plan_token_weights.argtypes = [C.POINTER(grpo_plan), C.c_int32, _i64p, _i32p, C.c_int32, _i64p,
+                                            C.POINTER(C.c_float)]
+    lib.grpo_plan_token_weights.restype = C.c_int
     lib.grpo_lmhead_workspace_size.argtypes = [C.c_int64, C.c_int64, C.c_int64]
     lib.grpo_lmhead_workspace_size.restype = C.c_size_t
     lib.grpo_lmhead_loss_fwd_bwd.argtypes = [vp, vp, C.c_int64, C.c_int64, C.c_int64, vp, vp, vp, vp, C.c_float,
@@ -244,6 +253,26 @@ def grpo_plan_token_index(plan: dict, row_len) -> np.ndarray:
     return out[:n.value]
 
 
+def grpo_plan_token_weights(plan: dict, row_len, row_valid, agg: int, want_w: bool = True):
+    """(step_divisor int64 [n_steps], w_tok float32 [tokens] or None) of an aggregation mode."""
+    rl = np.asarray(row_len, np.int64)
+    off = np.zeros(rl.shape[0] + 1, np.int64)
+    np.cumsum(rl, out=off[1:])
+    rv = _np_i32(row_valid)
+    p = grpo_plan()
+    p.n_steps = int(plan["n_steps"])
+    so = _np_i32(plan["step_in_row_off"])
+    p.step_in_row_off = _p32(so)
+    div = np.zeros(max(p.n_steps, 1), np.int64)
+    w = np.zeros(max(int(off[-1]), 1), np.float32) if want_w else None
+    rc = _lib().grpo_plan_token_weights(C.byref(p), rl.shape[0], off.ctypes.data_as(_i64p), _p32(rv), int(agg),
+                                        div.ctypes.data_as(_i64p),
+                                        None if w is None else w.ctypes.data_as(C.POINTER(C.c_float)))
+    if rc != OK:
+        raise GrpoError(rc, "grpo_plan_token_weights")
+    return div[:p.n_steps], None if w is None else w[:int(off[-1])]
+
+
 # ---- device entry points ---------------------------------------------------------------------
 
 def grpo_group_advantage(rewards, group_size: int, eps: float, unbiased_std: bool, adv_out,
@@ -263,7 +292,7 @@ def grpo_logprob_loss_fwd_bwd(logits, target, old_logp, adv_tok, mask, clip_eps:
     """logits [T, ld] (float32 or bfloat16) on the device; see grpo.h for the rest.
 
     ``terms`` (optional) = dict(kl_kind=0|1|2, kl_coef=..., ref_logp=tensor, ent_coef=...,
-    entropy_tok=tensor) selects grpo_logprob_loss_fwd_bwd_ex."""
+    entropy_tok=tensor, w_tok=tensor) selects grpo_logprob_loss_fwd_bwd_ex."""
     import torch
 
     if logits.dim() != 2 or logits.stride(1) != 1:
@@ -286,7 +315,7 @@ def grpo_logprob_loss_fwd_bwd(logits, target, old_logp, adv_tok, mask, clip_eps:
     else:
         tm = grpo_loss_terms(int(terms.get("kl_kind", 0)), float(terms.get("kl_coef", 0.0)),
                              _ptr(terms.get("ref_logp")), float(terms.get("ent_coef", 0.0)),
-                             _ptr(terms.get("entropy_tok")))
+                             _ptr(terms.get("entropy_tok")), _ptr(terms.get("w_tok")))
         rc = _lib().grpo_logprob_loss_fwd_bwd_ex(_ptr(logits), dt, T, V, ld, _ptr(tok_src), _ptr(target),
                                                  _ptr(old_logp), _ptr(adv_tok), _ptr(mask), float(clip_eps),
                                                  float(grad_scale), _ptr(dlogits), ld_out, _ptr(loss_tok),
@@ -295,27 +324,49 @@ def grpo_logprob_loss_fwd_bwd(logits, target, old_logp, adv_tok, mask, clip_eps:
         raise GrpoError(rc, "grpo_logprob_loss_fwd_bwd")
 
 
-def grpo_finish_step(acc, loss_tok, n_tok: Optional[int] = None, expected_N: int = -1,
-                     deferred: bool = False, grad_bufs: Sequence = (), sync: bool = True,
-                     stream=None):
-    """Close the step. With sync=True returns the result dict (the call waits on the stream);
-    with sync=False returns None and the result stays on the device in acc."""
+def _grad_arrays(grad_bufs):
     import torch
 
-    n_tok = loss_tok.numel() if n_tok is None else n_tok
     nb = len(grad_bufs)
     bufs = (C.c_void_p * max(nb, 1))(*[g.data_ptr() for g in grad_bufs])
     numels = (C.c_int64 * max(nb, 1))(*[g.numel() for g in grad_bufs])
     dts = (C.c_int32 * max(nb, 1))(*[{torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16}[g.dtype]
                                       for g in grad_bufs])
+    return nb, bufs, numels, dts
+
+
+def _finish_rc(rc: int, res, sync: bool, where: str):
+    if rc < 0 and not sync:
+        raise GrpoError(rc, where)
+    if rc < 0 and rc not in (ERR_N_MISMATCH, ERR_KERNEL):
+        raise GrpoError(rc, where)
+    return res.as_dict() if sync else None
+
+
+def grpo_finish_step(acc, loss_tok, n_tok: Optional[int] = None, expected_N: int = -1,
+                     deferred: bool = False, grad_bufs: Sequence = (), sync: bool = True,
+                     stream=None):
+    """Close the step. With sync=True returns the result dict (the call waits on the stream);
+    with sync=False returns None and the result stays on the device in acc."""
+    n_tok = loss_tok.numel() if n_tok is None else n_tok
+    nb, bufs, numels, dts = _grad_arrays(grad_bufs)
     res = grpo_step_result()
     rc = _lib().grpo_finish_step(_ptr(acc), _ptr(loss_tok), int(n_tok), int(expected_N), int(bool(deferred)),
                                  bufs, numels, dts, nb, C.byref(res) if sync else None, _stream(stream))
-    if rc < 0 and not sync:
-        raise GrpoError(rc, "grpo_finish_step")
-    if rc < 0 and rc not in (ERR_N_MISMATCH, ERR_KERNEL):
-        raise GrpoError(rc, "grpo_finish_step")
-    return res.as_dict() if sync else None
+    return _finish_rc(rc, res, sync, "grpo_finish_step")
+
+
+def grpo_finish_step_ex(acc, loss_tok, w_tok=None, divisor: int = -1, n_tok: Optional[int] = None,
+                        expected_N: int = -1, deferred: bool = False, grad_bufs: Sequence = (),
+                        sync: bool = True, stream=None):
+    """grpo_finish_step with per-token weights (device float, or None) and a divisor (-1 = N)."""
+    n_tok = loss_tok.numel() if n_tok is None else n_tok
+    nb, bufs, numels, dts = _grad_arrays(grad_bufs)
+    res = grpo_step_result()
+    rc = _lib().grpo_finish_step_ex(_ptr(acc), _ptr(loss_tok), int(n_tok), _ptr(w_tok), int(divisor),
+                                    int(expected_N), int(bool(deferred)), bufs, numels, dts, nb,
+                                    C.byref(res) if sync else None, _stream(stream))
+    return _finish_rc(rc, res, sync, "grpo_finish_step_ex")
 
 
 def grpo_lmhead_workspace_size(T: int, V: int, H: int) -> int:

@@ -277,3 +277,37 @@ extern "C" GRPO_API int grpo_plan_token_index(const grpo_plan* plan, int32_t n_r
   }
   return GRPO_OK;
 }
+
+extern "C" GRPO_API int grpo_plan_token_weights(const grpo_plan* plan, int32_t n_rows_in,
+                                                const int64_t* row_tok_off, const int32_t* row_valid,
+                                                int32_t agg, int64_t* step_divisor, float* w_tok) {
+  if (!plan || !row_tok_off || !row_valid || !step_divisor || n_rows_in < 0 || plan->n_steps < 0)
+    return GRPO_ERR_INVALID;
+  if (agg != GRPO_AGG_TOKEN_MEAN && agg != GRPO_AGG_SEQ_MEAN_TOKEN_SUM && agg != GRPO_AGG_SEQ_MEAN_TOKEN_MEAN)
+    return GRPO_ERR_INVALID;
+  if (row_tok_off[0] != 0) return GRPO_ERR_INVALID;
+  for (int32_t r = 0; r < n_rows_in; ++r) {
+    const int64_t len = row_tok_off[r + 1] - row_tok_off[r];
+    if (len < 0 || row_valid[r] < 0 || row_valid[r] > len) return GRPO_ERR_INVALID;
+  }
+  const int32_t* so = plan->step_in_row_off;
+  if (!so || so[0] != 0 || so[plan->n_steps] != n_rows_in) return GRPO_ERR_INVALID;
+  for (int32_t s = 0; s < plan->n_steps; ++s)
+    if (so[s + 1] < so[s]) return GRPO_ERR_INVALID;
+  for (int32_t s = 0; s < plan->n_steps; ++s) {
+    int64_t N = 0, B = 0;
+    for (int32_t r = so[s]; r < so[s + 1]; ++r) {
+      N += row_valid[r];
+      B += row_valid[r] >= 1;
+    }
+    step_divisor[s] = agg == GRPO_AGG_TOKEN_MEAN ? N : B;
+    if (!w_tok) continue;
+    for (int32_t r = so[s]; r < so[s + 1]; ++r) {
+      const float w = agg == GRPO_AGG_SEQ_MEAN_TOKEN_MEAN
+                          ? (float)(1.0 / (double)(row_valid[r] > 1 ? row_valid[r] : 1))
+                          : 1.f;
+      for (int64_t t = row_tok_off[r]; t < row_tok_off[r + 1]; ++t) w_tok[t] = w;
+    }
+  }
+  return GRPO_OK;
+}

@@ -54,6 +54,7 @@ struct RowArgs {
   const float* ref_logp;
   float ent_coef;
   float* entropy_tok;
+  const float* w_tok;  // per-token weight multiplying `scale` (an aggregation mode), or NULL
 };
 
 template <typename T>
@@ -100,6 +101,7 @@ struct RowMeta {
   int32_t y;     // target token id
   float A, old;  // advantage, pi_old log-prob
   float ref;     // reference-policy log-prob (KL term)
+  float w;       // per-token weight of the gradient scale (aggregation mode)
 };
 
 __device__ __forceinline__ int64_t row_src(const RowArgs& a, int64_t row) {
@@ -108,13 +110,14 @@ __device__ __forceinline__ int64_t row_src(const RowArgs& a, int64_t row) {
 
 template <bool REF>
 __device__ __forceinline__ RowMeta row_meta(const RowArgs& a, int64_t src) {
-  RowMeta m{src < 0 ? -1 : src, false, 0, 0.f, 0.f, 0.f};
+  RowMeta m{src < 0 ? -1 : src, false, 0, 0.f, 0.f, 0.f, 1.f};
   if (src >= 0) {
     m.valid = a.mask[src] != 0;
     m.y = a.target[src];
     m.A = a.adv[src];
     m.old = a.old_logp ? a.old_logp[src] : 0.f;
     if (REF) m.ref = a.ref_logp ? a.ref_logp[src] : 0.f;
+    if (REF) m.w = a.w_tok ? a.w_tok[src] : 1.f;
   }
   return m;
 }
@@ -129,7 +132,7 @@ struct MetaPipe {
   RowMeta next;
   int64_t src2;
   __device__ MetaPipe(const RowArgs& args, int64_t first, int64_t step) : a(args), stride(step) {
-    next = first < a.T ? row_meta<REF>(a, row_src(a, first)) : RowMeta{-1, false, 0, 0.f, 0.f, 0.f};
+    next = first < a.T ? row_meta<REF>(a, row_src(a, first)) : RowMeta{-1, false, 0, 0.f, 0.f, 0.f, 1.f};
     src2 = first + step < a.T ? row_src(a, first + step) : -1;
   }
   // metadata of `row`; starts the loads for the rows after it
@@ -272,9 +275,10 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
       }
       if (lane == 0) {
         const float lse = v.m + logf(v.s);
+        const float sc = TERMS ? a.scale * tm.w : a.scale;
         TokenOut o = token_epilogue(ybad ? __int_as_float(0x7fc00000) : zy, lse,
-                                    a.old_logp != nullptr, tm.old, tm.A, a.eps, a.scale);
-        if (TERMS) apply_terms(o, a.scale, a.kl_kind, a.kl_coef, tm.ref, a.ent_coef, lse - ez);
+                                    a.old_logp != nullptr, tm.old, tm.A, a.eps, sc);
+        if (TERMS) apply_terms(o, sc, a.kl_kind, a.kl_coef, tm.ref, a.ent_coef, lse - ez);
         a.loss_tok[tm.idx] = o.loss;
         if (a.logp_tok) a.logp_tok[tm.idx] = o.logp;
         if (TERMS && a.entropy_tok) a.entropy_tok[tm.idx] = ENT ? lse - ez : 0.f;
@@ -290,7 +294,7 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
     __syncthreads();
     const float lse = sh_lse, coef = sh_coef;
     // entropy gradient: dz_v = p_v (ea + eb z_v) - coef [v == y]
-    const float eb = ENT ? a.scale * a.ent_coef : 0.f;
+    const float eb = ENT ? a.scale * tm.w * a.ent_coef : 0.f;
     const float ea = ENT ? coef - eb * sh_ez : coef;
 
     // pass 2: dlogits = coef * (softmax - onehot)
@@ -665,8 +669,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
       if (ENT) tot = MS{tot3.m, tot3.s};
       const float lse2 = tot.m + log2f(tot.s);  // log2(sum_v 2^(z_v log2 e)) = LSE * log2(e)
       const float ez = ENT ? tot3.s2 / tot3.s : 0.f;  // sum_v p_v z_v
-      TokenOut o = token_epilogue(zy, lse2 * kLn2, a.old_logp != nullptr, tm.old, tm.A, a.eps, a.scale);
-      if (TERMS) apply_terms(o, a.scale, a.kl_kind, a.kl_coef, tm.ref, a.ent_coef, lse2 * kLn2 - ez);
+      const float sc = TERMS ? a.scale * tm.w : a.scale;
+      TokenOut o = token_epilogue(zy, lse2 * kLn2, a.old_logp != nullptr, tm.old, tm.A, a.eps, sc);
+      if (TERMS) apply_terms(o, sc, a.kl_kind, a.kl_coef, tm.ref, a.ent_coef, lse2 * kLn2 - ez);
       if (rank == 0 && ct == 0) {
         a.loss_tok[tm.idx] = o.loss;
         if (a.logp_tok) a.logp_tok[tm.idx] = o.logp;
@@ -677,7 +682,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
         cnt.nonfinite += o.nonfinite;
       }
       const float coef = o.coef;
-      const float eb = ENT ? a.scale * a.ent_coef : 0.f;
+      const float eb = ENT ? sc * a.ent_coef : 0.f;
       if (ENT && dz && eb != 0.f) {
         // with the entropy term: dz_v = p_v (ea + eb z_v) - coef [v == y]
         const float ea = coef - eb * ez;
@@ -894,7 +899,7 @@ extern "C" GRPO_API int grpo_logprob_loss_fwd_bwd_ex(const void* logits, int32_t
             dlogits, ld_out, loss_tok, logp_tok, acc,
             terms ? terms->kl_kind : 0, terms ? terms->kl_coef : 0.f,
             terms && terms->kl_kind ? terms->ref_logp : nullptr, terms ? terms->ent_coef : 0.f,
-            terms ? terms->entropy_tok : nullptr};
+            terms ? terms->entropy_tok : nullptr, terms ? terms->w_tok : nullptr};
   const cudaStream_t st = as_stream(stream);
   const size_t es = dtype == GRPO_DTYPE_F32 ? 4 : 2;
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
@@ -903,7 +908,7 @@ extern "C" GRPO_API int grpo_logprob_loss_fwd_bwd_ex(const void* logits, int32_t
   // the entropy (as a loss term or as an output) needs sum_v p_v z_v, a third accumulator:
   // a separate kernel instance
   if (terms && (terms->ent_coef != 0.f || terms->entropy_tok)) return dispatch<true, true>(a, dtype, vec, st);
-  if (terms && terms->kl_kind != GRPO_KL_NONE) return dispatch<false, true>(a, dtype, vec, st);
+  if (terms && (terms->kl_kind != GRPO_KL_NONE || terms->w_tok)) return dispatch<false, true>(a, dtype, vec, st);
   return dispatch<false, false>(a, dtype, vec, st);
 }
 

@@ -54,24 +54,35 @@ __global__ void adv_broadcast_kernel(const float* __restrict__ adv,
 
 constexpr int kFinishThreads = 1024;
 
-// One CTA: float64 sum of the step's per-token losses in a fixed order (thread-strided
-// partial sums, then a fixed tree), the metrics, the status, and the counter reset.
+// One term of the step sum: the token's loss, times its aggregation weight when there is one
+// (the product of two floats is exact in float64).
+template <bool W>
+__device__ __forceinline__ double weighted(const float* __restrict__ loss_tok, const float* __restrict__ w_tok,
+                                           int64_t i) {
+  return W ? (double)w_tok[i] * (double)loss_tok[i] : (double)loss_tok[i];
+}
+
+// One CTA: float64 sum of the step's (weighted) per-token losses in a fixed order
+// (thread-strided partial sums, then a fixed tree), the metrics, the status, the divisor, and
+// the counter reset.
+template <bool W>
 __global__ void __launch_bounds__(kFinishThreads)
-finish_kernel(grpo_step_acc* acc, const float* __restrict__ loss_tok, int64_t n,
-              int64_t expected_N) {
+finish_kernel(grpo_step_acc* acc, const float* __restrict__ loss_tok, const float* __restrict__ w_tok,
+              int64_t n, int64_t expected_N, int64_t divisor) {
   __shared__ double sh[kFinishThreads];
   const int tid = threadIdx.x;
   double s = 0.0;
   int64_t i = tid;
   for (; i + 3 * kFinishThreads < n; i += 4 * kFinishThreads) {
-    const float a0 = loss_tok[i], a1 = loss_tok[i + kFinishThreads];
-    const float a2 = loss_tok[i + 2 * kFinishThreads], a3 = loss_tok[i + 3 * kFinishThreads];
-    s += (double)a0;
-    s += (double)a1;
-    s += (double)a2;
-    s += (double)a3;
+    const double a0 = weighted<W>(loss_tok, w_tok, i), a1 = weighted<W>(loss_tok, w_tok, i + kFinishThreads);
+    const double a2 = weighted<W>(loss_tok, w_tok, i + 2 * kFinishThreads);
+    const double a3 = weighted<W>(loss_tok, w_tok, i + 3 * kFinishThreads);
+    s += a0;
+    s += a1;
+    s += a2;
+    s += a3;
   }
-  for (; i < n; i += kFinishThreads) s += (double)loss_tok[i];
+  for (; i < n; i += kFinishThreads) s += weighted<W>(loss_tok, w_tok, i);
   sh[tid] = s;
   __syncthreads();
   for (int w = kFinishThreads / 2; w > 0; w >>= 1) {
@@ -87,8 +98,10 @@ finish_kernel(grpo_step_acc* acc, const float* __restrict__ loss_tok, int64_t n,
     r.n_tokens = (int64_t)acc->n_tokens;
     r.kernel_flags = (int32_t)acc->flags;
     const double N = (double)(r.n_valid > 1 ? r.n_valid : 1);
-    r.loss = r.loss_sum / N;
+    const int64_t D = divisor >= 0 ? divisor : r.n_valid;
+    r.loss = r.loss_sum / (double)(D > 1 ? D : 1);
     r.clipfrac = (double)r.n_clipped / N;
+    acc->divisor = D;
     if (r.kernel_flags)
       r.status = GRPO_ERR_KERNEL;
     else if (expected_N >= 0 && expected_N != r.n_valid)
@@ -104,15 +117,15 @@ finish_kernel(grpo_step_acc* acc, const float* __restrict__ loss_tok, int64_t n,
 }
 
 // Registered gradient buffer: zeroed when the step is discarded, else (deferred mode) scaled
-// once by 1/max(N, 1); a kept step in non-deferred mode leaves it untouched.
+// once by 1/max(D, 1), D the step's divisor; a kept step in non-deferred mode leaves it untouched.
 template <typename T>
 __global__ void grad_finish_kernel(T* __restrict__ g, int64_t n, const grpo_step_acc* acc,
                                    int32_t deferred) {
   const int32_t status = acc->result.status;
   const bool discard = status != GRPO_OK;
   if (!discard && !deferred) return;
-  const int64_t N = acc->result.n_valid;
-  const float f = discard ? 0.f : (float)(1.0 / (double)(N > 1 ? N : 1));
+  const int64_t D = acc->divisor;
+  const float f = discard ? 0.f : (float)(1.0 / (double)(D > 1 ? D : 1));
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
     const float v = discard ? 0.f : (float)g[i] * f;
@@ -150,11 +163,11 @@ extern "C" GRPO_API int grpo_group_advantage(const float* rewards, int32_t n_rol
   return GRPO_OK;
 }
 
-extern "C" GRPO_API int grpo_finish_step(grpo_step_acc* acc, const float* loss_tok, int64_t n_tok,
-                                         int64_t expected_N, int32_t deferred,
-                                         void* const* grad_bufs, const int64_t* grad_numels,
-                                         const int32_t* grad_dtypes, int32_t n_bufs,
-                                         grpo_step_result* result_host, void* stream) {
+extern "C" GRPO_API int grpo_finish_step_ex(grpo_step_acc* acc, const float* loss_tok, int64_t n_tok,
+                                            const float* w_tok, int64_t divisor, int64_t expected_N,
+                                            int32_t deferred, void* const* grad_bufs,
+                                            const int64_t* grad_numels, const int32_t* grad_dtypes,
+                                            int32_t n_bufs, grpo_step_result* result_host, void* stream) {
   if (!acc || n_tok < 0 || n_bufs < 0) return GRPO_ERR_INVALID;
   if (n_tok > 0 && !loss_tok) return GRPO_ERR_INVALID;
   if (n_bufs > 0 && (!grad_bufs || !grad_numels || !grad_dtypes)) return GRPO_ERR_INVALID;
@@ -163,7 +176,10 @@ extern "C" GRPO_API int grpo_finish_step(grpo_step_acc* acc, const float* loss_t
     if (grad_numels[b] < 0 || (grad_numels[b] > 0 && !grad_bufs[b])) return GRPO_ERR_INVALID;
   }
   const cudaStream_t st = as_stream(stream);
-  finish_kernel<<<1, kFinishThreads, 0, st>>>(acc, loss_tok, n_tok, expected_N);
+  if (w_tok && n_tok > 0)
+    finish_kernel<true><<<1, kFinishThreads, 0, st>>>(acc, loss_tok, w_tok, n_tok, expected_N, divisor);
+  else
+    finish_kernel<false><<<1, kFinishThreads, 0, st>>>(acc, loss_tok, nullptr, n_tok, expected_N, divisor);
   GRPO_CUDA_TRY(cudaGetLastError());
   for (int32_t b = 0; b < n_bufs; ++b) {
     const int64_t n = grad_numels[b];
@@ -181,6 +197,15 @@ extern "C" GRPO_API int grpo_finish_step(grpo_step_acc* acc, const float* loss_t
                                 cudaMemcpyDeviceToHost, st));
   GRPO_CUDA_TRY(cudaStreamSynchronize(st));
   return result_host->status;
+}
+
+extern "C" GRPO_API int grpo_finish_step(grpo_step_acc* acc, const float* loss_tok, int64_t n_tok,
+                                         int64_t expected_N, int32_t deferred,
+                                         void* const* grad_bufs, const int64_t* grad_numels,
+                                         const int32_t* grad_dtypes, int32_t n_bufs,
+                                         grpo_step_result* result_host, void* stream) {
+  return grpo_finish_step_ex(acc, loss_tok, n_tok, nullptr, -1, expected_N, deferred, grad_bufs, grad_numels,
+                             grad_dtypes, n_bufs, result_host, stream);
 }
 
 extern "C" GRPO_API const char* grpo_status_string(int status) {
@@ -201,8 +226,9 @@ extern "C" GRPO_API const char* grpo_status_string(int status) {
   }
 }
 
-extern "C" GRPO_API int grpo_version(void) { return 100; }
+extern "C" GRPO_API int grpo_version(void) { return 101; }
 
 static_assert(sizeof(grpo_step_result) == 64, "grpo_step_result is 64 bytes");
 static_assert(sizeof(grpo_step_acc) == 128, "grpo_step_acc is 128 bytes");
 static_assert(offsetof(grpo_step_acc, result) == 64, "result sits in the second half");
+static_assert(offsetof(grpo_step_acc, divisor) == 40, "divisor follows the flags");

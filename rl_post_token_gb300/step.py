@@ -29,6 +29,13 @@ class BatchPlan:
     tok_src: Optional[np.ndarray]   # int64 [exec tokens] or None (identity)
     step_tok_range: List[tuple]     # input-order token range of each optimizer step
     step_exec_range: List[tuple]    # exec-order token range of each optimizer step
+    row_len: np.ndarray             # int64 [rows], input order
+    row_valid: np.ndarray           # int32 [rows], input order
+
+    def token_weights(self, agg: int, want_w: bool = True):
+        """(divisor per step, per-token weights float32 in input order or None) of a loss
+        aggregation mode (``_lib.AGG_*``), from grpo_plan_token_weights."""
+        return _lib.grpo_plan_token_weights(self.plan, self.row_len, self.row_valid, agg, want_w)
 
     @property
     def n_steps(self) -> int:
@@ -54,21 +61,25 @@ def plan_batch(cfg: dict, row_len, row_valid, seg_counts=None) -> BatchPlan:
         steps.append((int(row_tok_off[r0]), int(row_tok_off[r1])))
         c0, c1 = p["step_chunk_off"][s], p["step_chunk_off"][s + 1]
         execs.append((int(exec_tok_off[c0]), int(exec_tok_off[c1])))
-    return BatchPlan(p, row_tok_off, exec_tok_off, tok_src, steps, execs)
+    return BatchPlan(p, row_tok_off, exec_tok_off, tok_src, steps, execs, rl,
+                     np.asarray(row_valid, np.int32))
 
 
 def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok, loss_tok,
               logp_tok, accs, clip_eps: float, rewards=None, adv_rollout=None, group_size: int = 1,
               adv_eps: float = 1e-6, row_tok_off=None, row_rollout=None, tok_src=None,
               deferred: bool = False, V: Optional[int] = None, stream=None,
-              chunk_ready=None, launch_events=None) -> int:
+              chunk_ready=None, launch_events=None, agg: int = _lib.AGG_TOKEN_MEAN,
+              w_tok=None) -> int:
     """Enqueue the whole batch; returns the number of library kernel launches.
 
     ``accs`` is a uint8 device tensor of n_steps * 128 bytes (one accumulator per optimizer
     step, results read later with ``read_results``). If ``rewards`` is given the advantage is
     computed into ``adv_rollout``/``adv_tok`` first. ``chunk_ready[c]`` (optional CUDA event)
     is waited on before chunk c is launched, e.g. the end of its host-to-device copy;
-    ``launch_events`` (optional list) receives a (start, end) event pair per row-pass launch."""
+    ``launch_events`` (optional list) receives a (start, end) event pair per row-pass launch.
+    ``agg`` selects the loss aggregation mode; SEQ_MEAN_TOKEN_MEAN also needs ``w_tok``, the
+    device copy of ``bp.token_weights(agg)[1]`` (input order)."""
     import torch
 
     st = torch.cuda.current_stream() if stream is None else stream
@@ -78,9 +89,14 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
                                   row_tok_off, adv_tok, stream=st)
         launches += 2
     p = bp.plan
+    plain = agg == _lib.AGG_TOKEN_MEAN and w_tok is None
+    if agg == _lib.AGG_SEQ_MEAN_TOKEN_MEAN and w_tok is None:
+        raise ValueError("SEQ_MEAN_TOKEN_MEAN needs the per-token weights w_tok")
+    divisors = None if plain else bp.token_weights(agg, want_w=False)[0]
     for s in range(p["n_steps"]):
         N = int(p["step_valid_tokens"][s])
-        scale = 1.0 if deferred else 1.0 / max(N, 1)
+        D = N if plain else int(divisors[s])
+        scale = 1.0 if deferred else 1.0 / max(D, 1)
         acc = accs[s * _lib.ACC_BYTES:(s + 1) * _lib.ACC_BYTES]
         for c in range(p["step_chunk_off"][s], p["step_chunk_off"][s + 1]):
             a, b = int(bp.exec_tok_off[c]), int(bp.exec_tok_off[c + 1])
@@ -94,14 +110,16 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
             if tok_src is None:
                 # exec order == input order: the chunk's side inputs are the same slice
                 side = (target[a:b], None if old_logp is None else old_logp[a:b], adv_tok[a:b],
-                        mask[a:b], loss_tok[a:b], None if logp_tok is None else logp_tok[a:b], None)
+                        mask[a:b], loss_tok[a:b], None if logp_tok is None else logp_tok[a:b], None,
+                        None if w_tok is None else w_tok[a:b])
             else:
                 # side arrays stay whole; the kernel reads them through the token index
-                side = (target, old_logp, adv_tok, mask, loss_tok, logp_tok, tok_src[a:b])
-            tg, od, ad, mk, lt, lp, ts = side
+                side = (target, old_logp, adv_tok, mask, loss_tok, logp_tok, tok_src[a:b], w_tok)
+            tg, od, ad, mk, lt, lp, ts, wt = side
             _lib.grpo_logprob_loss_fwd_bwd(
                 logits[a:b], tg, od, ad, mk, clip_eps, scale,
-                None if dlogits is None else dlogits[a:b], lt, lp, acc, tok_src=ts, V=V, stream=st)
+                None if dlogits is None else dlogits[a:b], lt, lp, acc, tok_src=ts, V=V, stream=st,
+                terms=None if wt is None else dict(w_tok=wt))
             if launch_events is not None:
                 e1 = torch.cuda.Event(enable_timing=True)
                 e1.record(st)
@@ -110,8 +128,13 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
         t0, t1 = bp.step_tok_range[s]
         e0, e1 = bp.step_exec_range[s]
         grads = [] if dlogits is None or e1 == e0 else [dlogits[e0:e1]]
-        _lib.grpo_finish_step(acc, loss_tok[t0:t1], expected_N=N, deferred=deferred,
-                              grad_bufs=grads, sync=False, stream=st)
+        if plain:
+            _lib.grpo_finish_step(acc, loss_tok[t0:t1], expected_N=N, deferred=deferred,
+                                  grad_bufs=grads, sync=False, stream=st)
+        else:
+            _lib.grpo_finish_step_ex(acc, loss_tok[t0:t1], None if w_tok is None else w_tok[t0:t1],
+                                     divisor=D, expected_N=N, deferred=deferred, grad_bufs=grads,
+                                     sync=False, stream=st)
         launches += 1 + len(grads)
     return launches
 
