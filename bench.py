@@ -307,9 +307,11 @@ class Batch:
 
 
 def run_lmhead(args):
-    """Fused LM-head step: advantage, one grpo_lmhead_loss_fwd_bwd call (forward, recompute,
-    dlogits chunks, d_h and dW), the finish. Roofline: tensor, 6*T*V*H algorithmic flops
-    (forward GEMM and the two backward GEMMs; the recompute is not credited)."""
+    """Fused LM-head step: advantage, one grpo_lmhead_loss_fwd_bwd call (forward, dlogits, d_h
+    and dW), the finish. The headline uses the stored-exponent backward (the workspace that
+    selects it); the recompute backward (the minimum workspace) is timed beside it. Roofline:
+    tensor, 6*T*V*H algorithmic flops (forward GEMM and the two backward GEMMs; the recompute
+    path's extra 2*T*V*H is not credited)."""
     import torch
     from rl_post_token_gb300 import build as B
     from rl_post_token_gb300 import _lib
@@ -334,14 +336,15 @@ def run_lmhead(args):
     loss = torch.empty(T, device=device)
     logp = torch.empty(T, device=device)
     acc = _lib.new_step_acc(device)
-    ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=device)
+    ws = torch.empty(_lib.grpo_lmhead_workspace_size_stored(T, V, Hd), dtype=torch.uint8, device=device)
+    ws_small = ws[:_lib.grpo_lmhead_workspace_size(T, V, Hd)]
     stream = torch.cuda.current_stream(device)
     N = wl.n_valid
 
-    def step(grads=True, old=None):
+    def step(grads=True, old=None, w=ws):
         _lib.grpo_group_advantage(rewards, wl.group_size, 1e-6, True, adv_r, row_rollout, row_tok_off, adv)
         _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, target, old, adv, mask, wl.eps, 1.0 / max(N, 1),
-                                      d_h if grads else None, dW if grads else None, loss, logp, acc, ws)
+                                      d_h if grads else None, dW if grads else None, loss, logp, acc, w)
         _lib.grpo_finish_step(acc, loss, expected_N=N, sync=False)
 
     step(grads=False)  # pi_old by the ahead pass, then seeded noise
@@ -359,6 +362,14 @@ def run_lmhead(args):
     e1.record(stream)
     torch.cuda.synchronize(device)
     full_s = e0.elapsed_time(e1) / 1e3 / args.steps
+    step(old=old, w=ws_small)
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record(stream)
+    for _ in range(args.steps):
+        step(old=old, w=ws_small)
+    r1.record(stream)
+    torch.cuda.synchronize(device)
+    rec_s = r0.elapsed_time(r1) / 1e3 / args.steps
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
     for _ in range(args.steps):
@@ -376,10 +387,14 @@ def run_lmhead(args):
         "ms_per_step": 1e3 * full_s, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT["lmhead"], "tokens": T, "vocab": V, "hidden": Hd,
+                   "backward": "stored exponents (workspace %.2f GB)" % (ws.numel() / 1e9),
                    "l2": "weights 622 MB + hidden 64 MB read per step, larger than L2; no flush"},
         "roofline": {"bound": "tensor", "achieved": flops / full_s / 1e12, "peak": peak, "unit": "TFLOP/s",
                      "frac": flops / full_s / 1e12 / peak, "peak_source": f"{kind} bf16_tflops_sustained",
                      "flops_per_step": flops, "traffic": None},
+        "recompute_path": {"ms": 1e3 * rec_s, "tflops": flops / rec_s / 1e12,
+                           "workspace_gb": ws_small.numel() / 1e9,
+                           "what": "minimum workspace: logits recomputed per 16384-column chunk"},
         "forward_only": {"ms": 1e3 * fwd_s, "tflops": 2.0 * T * V * Hd / fwd_s / 1e12,
                          "what": "softmax-partials GEMM pass + per-token reduce (2*T*V*H flops)"},
         "step_result": {k: res[k] for k in ("loss", "n_valid", "clipfrac", "status")},

@@ -363,12 +363,23 @@ GRPO_API int grpo_window_rollup(const grpo_window* w, double* loss, int64_t* den
  * LSE and coefficients, and one bf16 dlogits chunk of 16384 vocabulary columns. 0 on bad sizes. */
 GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H);
 
+/* Bytes of workspace that select the stored path of grpo_lmhead_loss_fwd_bwd: the partials
+ * above plus a bf16 [T, 256 * ceil(V/256)] matrix (about 2*T*V bytes). 0 on bad sizes. */
+GRPO_API size_t grpo_lmhead_workspace_size_stored(int64_t T, int64_t V, int64_t H);
+
 /* The same loss with the logits produced on the tensor cores: z = h W^T, computed tile by tile
- * and consumed by the softmax in the GEMM epilogue, so the [T, V] logits are never stored
- * ("Sizing mini-batches and micro-batches", "The problem"). Forward: LSE, log-prob, ratio,
- * clipped surrogate, per-token loss (as grpo_logprob_loss_fwd_bwd, one token per row of h).
- * Backward: the logits of each vocabulary chunk are recomputed, dlogits written to the
- * workspace chunk, then d_h = dlogits W (accumulated over chunks) and dW = dlogits^T h.
+ * and consumed by the softmax in the GEMM epilogue, so neither the [T, V] float32 logits nor
+ * their softmax are ever stored ("Sizing mini-batches and micro-batches", "The problem").
+ * Forward: LSE, log-prob, ratio, clipped surrogate, per-token loss (as
+ * grpo_logprob_loss_fwd_bwd, one token per row of h). Backward, by workspace size:
+ *  - >= grpo_lmhead_workspace_size: the logits of each 16384-column vocabulary chunk are
+ *    recomputed, dlogits written to the workspace chunk, then d_h = dlogits W (accumulated
+ *    over chunks) and dW = dlogits^T h per chunk (8 T V H flops in all);
+ *  - >= grpo_lmhead_workspace_size_stored: the forward epilogue also stores, per 256-wide
+ *    tile, e = exp(z - tile max) as bf16 (relative error 2^-9 whatever the logits' size);
+ *    dlogits = coef * exp(tile max - LSE) * e replaces it in place, the target element from
+ *    the float32 logit; then one d_h and one dW GEMM over the whole vocabulary (6 T V H
+ *    flops, no recompute).
  *  h          device bf16 [T, H] row-major, 16-byte aligned; H a multiple of 64
  *  W          device bf16 [V, H] row-major, 16-byte aligned
  *  target, old_logp (or NULL), adv_tok, mask   device, indexed by token row

@@ -103,6 +103,10 @@ struct GemmArgs {
   float* part_m;  // [n_col_tiles_total][T] log2-domain max
   float* part_s;  // [n_col_tiles_total][T]
   float* zy;      // [T] target logit
+  // mode 0 with est != NULL: e = 2^((z - tile max) log2 e) stored as bf16 [T][lde] (the
+  // partials then use the exact tile maximum)
+  __nv_bfloat16* est;
+  int64_t lde;
   // mode 1
   const float* lse2;  // [T] LSE * log2(e)
   const float* coef;  // [T] gradient coefficient (already scaled)
@@ -110,6 +114,22 @@ struct GemmArgs {
   int64_t ldz, v0;
   grpo_step_acc* acc;
 };
+
+// Stored path: e = 2^(z log2 e - shift) of 32 columns (-inf past the vocabulary gives 0),
+// written as bf16 for row `row` (if it exists) and added to s.
+__device__ __forceinline__ void store_e_chunk(const GemmArgs& g, bool rok, int64_t row, int64_t cb, float (&v)[32],
+                                              float shift, float& s) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = ex2(fmaf(v[i], kLog2e, -shift));
+  if (rok) {
+    uint4* d4 = reinterpret_cast<uint4*>(g.est + row * g.lde + cb);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      d4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                         pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+  }
+  s += tree_sum(v);  // reduces v in place: after the store
+}
 
 __global__ void __launch_bounds__(NTHREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w, GemmArgs g) {
@@ -212,7 +232,63 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ C
       const bool rok = row < g.T;
       const int32_t y = rok ? g.target[row] : -1;
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + ab * BN;
-      if (g.mode == 0) {
+      if (g.mode == 0 && g.est) {
+        // one pass: e relative to a shift taken from the first 32 columns, stored and summed;
+        // if a later value sits more than 2^64 above that shift the warp redoes the tile
+        // with the exact tile maximum (e <= 2^64 keeps every stored value and the sum finite)
+        float shift = 0.f, s = 0.f, zy = 0.f;
+        bool redo = false;
+        const bool own = y >= c0 && y < c0 + BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(taddr + c * 32, v);
+          const int64_t cb = c0 + c * 32;
+          float cmax = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (cb + i >= g.V) v[i] = -INFINITY;
+            cmax = fmaxf(cmax, v[i]);
+          }
+          if (own && y >= cb && y < cb + 32) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (cb + i == y) zy = v[i];
+          }
+          if (c == 0) shift = cmax * kLog2e;  // the first 32 columns always hold vocabulary entries
+          redo |= !(cmax * kLog2e <= shift + 64.f);
+          store_e_chunk(g, rok, row, cb, v, shift, s);
+        }
+        if (__any_sync(0xffffffffu, redo)) {
+          float mx = -INFINITY;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_ld32(taddr + c * 32, v);
+            const int64_t cb = c0 + c * 32;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (cb + i < g.V) mx = fmaxf(mx, v[i]);
+          }
+          shift = mx * kLog2e;
+          s = 0.f;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_ld32(taddr + c * 32, v);
+            const int64_t cb = c0 + c * 32;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (cb + i >= g.V) v[i] = -INFINITY;
+            store_e_chunk(g, rok, row, cb, v, shift, s);
+          }
+        }
+        if (rok) {
+          g.part_m[(int64_t)ct * g.T + row] = shift;
+          g.part_s[(int64_t)ct * g.T + row] = s;
+          if (own) g.zy[row] = zy;
+        }
+      } else if (g.mode == 0) {
         MS acc{-INFINITY, 0.f};
         float zy = 0.f;
         const bool own = y >= c0 && y < c0 + BN;
@@ -354,6 +430,45 @@ __global__ void reduce_kernel(int64_t T, int n_col_tiles, const float* __restric
   }
 }
 
+// Stored path, backward: dz = coef * 2^(tile max - LSE) * e, in place over the stored e, one CTA
+// per token row at a time; the target element, coef * (p_y - 1), is taken from the float32
+// target logit and written by the thread that wrote its vector.
+__global__ void __launch_bounds__(256) dz_from_e_kernel(int64_t T, int64_t V, int n_col_tiles, int64_t lde,
+                                                        const float* __restrict__ part_m,
+                                                        const float* __restrict__ lse2,
+                                                        const float* __restrict__ coef,
+                                                        const float* __restrict__ zy,
+                                                        const int32_t* __restrict__ target,
+                                                        __nv_bfloat16* __restrict__ e) {
+  extern __shared__ float f[];  // [n_col_tiles] per-tile factor of the current row
+  const int tid = threadIdx.x;
+  const int64_t nv = lde / 8;
+  for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
+    const float c = coef[row], l2 = lse2[row];
+    __syncthreads();
+    for (int ct = tid; ct < n_col_tiles; ct += blockDim.x)
+      f[ct] = c == 0.f ? 0.f : c * ex2(part_m[(int64_t)ct * T + row] - l2);
+    __syncthreads();
+    uint4* p = reinterpret_cast<uint4*>(e + row * lde);
+    if (c == 0.f) {  // masked or clipped: a zero row, whatever e holds
+      for (int64_t v = tid; v < nv; v += blockDim.x) p[v] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    for (int64_t v = tid; v < nv; v += blockDim.x) {
+      const float fv = f[v / (BN / 8)];
+      uint4 u = p[v];
+      float x[8];
+      x[0] = bf16_lo(u.x) * fv; x[1] = bf16_hi(u.x) * fv; x[2] = bf16_lo(u.y) * fv; x[3] = bf16_hi(u.y) * fv;
+      x[4] = bf16_lo(u.z) * fv; x[5] = bf16_hi(u.z) * fv; x[6] = bf16_lo(u.w) * fv; x[7] = bf16_hi(u.w) * fv;
+      p[v] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                        pack_bf16x2(x[6], x[7]));
+    }
+    const int32_t y = target[row];
+    if (y >= 0 && (int64_t)y < V && tid == (int)((y / 8) % blockDim.x))
+      e[row * lde + y] = __float2bfloat16_rn(c * ex2(fmaf(zy[row], kLog2e, -l2)) - c);
+  }
+}
+
 // ---- host -------------------------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -403,14 +518,15 @@ namespace {
 struct WsLayout {
   size_t part_m, part_s, zy, lse2, coef, dz, total;
   int n_col_tiles;
-  int64_t vchunk;
+  int64_t vchunk;  // columns of the dz region: one recompute chunk, or (stored) every tile
 };
 
-WsLayout ws_layout(int64_t T, int64_t V, int64_t vchunk) {
+// stored = true: the dz region holds the whole [T, n_col_tiles * 256] exponent/dlogits matrix
+WsLayout ws_layout(int64_t T, int64_t V, int64_t vchunk, bool stored = false) {
   WsLayout w{};
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   w.n_col_tiles = (int)((V + BN - 1) / BN);
-  w.vchunk = std::min<int64_t>(vchunk, (int64_t)w.n_col_tiles * BN);
+  w.vchunk = stored ? (int64_t)w.n_col_tiles * BN : std::min<int64_t>(vchunk, (int64_t)w.n_col_tiles * BN);
   size_t off = 0;
   w.part_m = off; off += up((size_t)w.n_col_tiles * T * 4);
   w.part_s = off; off += up((size_t)w.n_col_tiles * T * 4);
@@ -431,6 +547,11 @@ extern "C" GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int6
   return ws_layout(T, V, kDefaultVChunk).total;
 }
 
+extern "C" GRPO_API size_t grpo_lmhead_workspace_size_stored(int64_t T, int64_t V, int64_t H) {
+  if (T <= 0 || V <= 0 || H <= 0) return 0;
+  return ws_layout(T, V, kDefaultVChunk, true).total;
+}
+
 extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, int64_t T, int64_t V, int64_t H,
                                                  const int32_t* target, const float* old_logp,
                                                  const float* adv_tok, const uint8_t* mask, float clip_eps,
@@ -442,7 +563,9 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
   if (!h || !W || !target || !adv_tok || !mask || !loss_tok || !workspace) return GRPO_ERR_INVALID;
   if (((uintptr_t)h | (uintptr_t)W) & 15u) return GRPO_ERR_INVALID;
   if (T > INT32_MAX / 2 || V > INT32_MAX / 2) return GRPO_ERR_INVALID;
-  const WsLayout ws = ws_layout(T, V, kDefaultVChunk);
+  // the stored path when there is a backward pass and room for the whole exponent matrix
+  const bool stored = (d_h || dW) && workspace_bytes >= ws_layout(T, V, kDefaultVChunk, true).total;
+  const WsLayout ws = ws_layout(T, V, kDefaultVChunk, stored);
   if (workspace_bytes < ws.total) return GRPO_ERR_CAPACITY;
   const cudaStream_t st = as_stream(stream);
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
@@ -479,6 +602,8 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
   g.dz = dz;
   g.ldz = ws.vchunk;
   g.acc = acc;
+  g.est = stored ? dz : nullptr;
+  g.lde = ws.vchunk;
 
   // pass A: softmax partials over every vocabulary tile
   g.mode = 0;
@@ -495,11 +620,31 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
   GRPO_CUDA_TRY(cudaGetLastError());
   if (!d_h && !dW) return GRPO_OK;
 
-  // pass B: per vocabulary chunk, dlogits into the workspace, then the two backward GEMMs
   cublasHandle_t bh = blas_handle();
   if (!bh || cublasSetStream(bh, st) != CUBLAS_STATUS_SUCCESS) return GRPO_ERR_CUDA;
-  const int tiles_per_chunk = (int)(ws.vchunk / BN);
   const float one = 1.f, zero = 0.f;
+  if (stored) {
+    // dlogits in place over the stored exponents, then each backward GEMM over the whole vocabulary
+    const int grid = (int)std::min<int64_t>(T, (int64_t)sm_count() * 8);
+    const size_t fsm = (size_t)ws.n_col_tiles * sizeof(float);
+    if (fsm > 48 * 1024) return GRPO_ERR_UNSUPPORTED;
+    dz_from_e_kernel<<<grid, 256, fsm, st>>>(T, V, ws.n_col_tiles, ws.vchunk, part_m, lse2, coef, zy, target, dz);
+    GRPO_CUDA_TRY(cudaGetLastError());
+    // d_h[T,H] = dz[T,V] W[V,H]   (column-major view: d_h^T = W^T dz^T)
+    if (d_h && cublasGemmEx(bh, CUBLAS_OP_N, CUBLAS_OP_N, (int)H, (int)T, (int)V, &one, W, CUDA_R_16BF, (int)H, dz,
+                            CUDA_R_16BF, (int)ws.vchunk, &zero, d_h, CUDA_R_32F, (int)H, CUBLAS_COMPUTE_32F,
+                            CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+      return GRPO_ERR_CUDA;
+    // dW[V,H] = dz^T[V,T] h[T,H]   (column-major view: dW^T = h^T dz)
+    if (dW && cublasGemmEx(bh, CUBLAS_OP_N, CUBLAS_OP_T, (int)H, (int)V, (int)T, &one, h, CUDA_R_16BF, (int)H, dz,
+                           CUDA_R_16BF, (int)ws.vchunk, &zero, dW, CUDA_R_32F, (int)H, CUBLAS_COMPUTE_32F,
+                           CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+      return GRPO_ERR_CUDA;
+    return GRPO_OK;
+  }
+
+  // recompute path: per vocabulary chunk, dlogits into the workspace, then the two backward GEMMs
+  const int tiles_per_chunk = (int)(ws.vchunk / BN);
   for (int ct0 = 0, c = 0; ct0 < ws.n_col_tiles; ct0 += tiles_per_chunk, ++c) {
     const int nct = std::min(tiles_per_chunk, ws.n_col_tiles - ct0);
     const int64_t v0 = (int64_t)ct0 * BN;

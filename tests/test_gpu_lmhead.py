@@ -1,6 +1,8 @@
 """GPU parity of the fused LM-head variant (tcgen05 GEMM + softmax epilogue) against the
 float64 oracle: per-token loss and log-prob, d_h and dW, on sizes with ragged token and
-vocabulary tiles, several vocabulary chunks, masked tokens and forward-only calls.
+vocabulary tiles, several vocabulary chunks, masked tokens and forward-only calls, through
+both backward paths (the recompute path and, with the larger workspace, the stored-exponent
+path).
 
 d_h and dW tolerance: both products are formed from bf16 dlogits (rounded to nearest), so
 each element may move by up to ~2^-8 of the sum of the magnitudes of its terms; the bar is
@@ -26,10 +28,13 @@ def _built(grpo_lib):
     return grpo_lib
 
 
-def _case(T, V, Hd, seed, valid_lo=None, old=True, adv=None):
+def _case(T, V, Hd, seed, valid_lo=None, old=True, adv=None, w_row_scale=None):
     wl = W.make_workload("lmhead", seed=seed, rows=4, tokens=T, V=V, H=Hd)
     assert wl.T == T, (wl.T, T)
     h, Wt = W.make_lmhead_inputs(wl, DEV)
+    if w_row_scale is not None:  # (rows, factor): a few vocabulary entries with much larger logits
+        rows, factor = w_row_scale
+        Wt[rows] = (Wt[rows].float() * factor).to(torch.bfloat16)
     hb = h.view(torch.int16).cpu().numpy().view(np.uint16)
     wb = Wt.view(torch.int16).cpu().numpy().view(np.uint16)
     mask = wl.mask.copy()
@@ -45,7 +50,7 @@ def _case(T, V, Hd, seed, valid_lo=None, old=True, adv=None):
     return wl, h, Wt, hb, wb, mask, a_tok, old_logp
 
 
-def _run(h, Wt, wl, mask, a_tok, old_logp, scale, grads=True):
+def _run(h, Wt, wl, mask, a_tok, old_logp, scale, grads=True, stored=False):
     T, Hd = h.shape
     V = Wt.shape[0]
     d_h = torch.full((T, Hd), 7.0, device=DEV) if grads else None
@@ -53,7 +58,8 @@ def _run(h, Wt, wl, mask, a_tok, old_logp, scale, grads=True):
     loss = torch.full((T,), -7.0, device=DEV)
     logp = torch.full((T,), -7.0, device=DEV)
     acc = _lib.new_step_acc(DEV)
-    ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=DEV)
+    size = (_lib.grpo_lmhead_workspace_size_stored if stored else _lib.grpo_lmhead_workspace_size)(T, V, Hd)
+    ws = torch.empty(size, dtype=torch.uint8, device=DEV)
     t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
     _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, t(wl.target), t(old_logp), t(a_tok), t(mask), wl.eps, scale,
                                   d_h, dW, loss, logp, acc, ws)
@@ -61,10 +67,10 @@ def _run(h, Wt, wl, mask, a_tok, old_logp, scale, grads=True):
     return d_h, dW, loss, logp, acc
 
 
-def _check(T, V, Hd, seed, valid_lo=None, old=True, adv=None, grads=True):
-    wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed, valid_lo, old, adv)
+def _check(T, V, Hd, seed, valid_lo=None, old=True, adv=None, grads=True, stored=False, w_row_scale=None):
+    wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed, valid_lo, old, adv, w_row_scale)
     N = max(int(mask.sum()), 1)
-    d_h, dW, loss, logp, acc = _run(h, Wt, wl, mask, a_tok, old_logp, 1.0 / N, grads)
+    d_h, dW, loss, logp, acc = _run(h, Wt, wl, mask, a_tok, old_logp, 1.0 / N, grads, stored)
     ref = OL.lmhead_fwd_bwd(hb, wb, wl.target, old_logp, a_tok, mask, wl.eps, scale=1.0 / N)
     H.assert_tokens_close(H.to_f64(loss), H.to_f64(logp), ref, a_tok, mask)
     res = _lib.grpo_finish_step(acc, loss, expected_N=int(mask.sum()))
@@ -89,32 +95,46 @@ def _check(T, V, Hd, seed, valid_lo=None, old=True, adv=None, grads=True):
     return ref
 
 
-def test_lmhead_exact_tiles():
-    _check(256, 1024, 128, seed=1)
+@pytest.mark.parametrize("stored", [False, True])
+def test_lmhead_exact_tiles(stored):
+    _check(256, 1024, 128, seed=1, stored=stored)
 
 
-def test_lmhead_ragged_tokens_vocab_and_k():
+@pytest.mark.parametrize("stored", [False, True])
+def test_lmhead_ragged_tokens_vocab_and_k(stored):
     # 300 tokens (ragged 128-row tile), V = 1000 (ragged 256-column tile and 32-column group),
     # H = 192 (three 64-wide K blocks)
-    _check(300, 1000, 192, seed=2)
+    _check(300, 1000, 192, seed=2, stored=stored)
 
 
-def test_lmhead_several_vocab_chunks_masked_tokens():
+@pytest.mark.parametrize("stored", [False, True])
+def test_lmhead_several_vocab_chunks_masked_tokens(stored):
     # V > 16384: two dlogits chunks, the second ragged; a quarter of the tokens masked
-    _check(128, 20000, 64, seed=3, valid_lo=0.25)
+    _check(128, 20000, 64, seed=3, valid_lo=0.25, stored=stored)
 
 
-def test_lmhead_no_pi_old_and_clip_stress():
+@pytest.mark.parametrize("stored", [False, True])
+def test_lmhead_no_pi_old_and_clip_stress(stored):
     T = 256
     adv = np.random.default_rng(4).choice([-2.0, -0.5, 0.5, 2.0], T)
-    _check(T, 2048, 128, seed=4, old=False, adv=adv)
+    _check(T, 2048, 128, seed=4, old=False, adv=adv, stored=stored)
 
 
-def test_lmhead_forward_only():
-    _check(256, 4096, 256, seed=5, grads=False)
+@pytest.mark.parametrize("stored", [False, True])
+def test_lmhead_wide_logit_spread(stored):
+    # columns 300..307 get logits ~300x larger than the rest (spread far beyond 2^64 in the
+    # exponent): the stored path's shift from a tile's first 32 columns is then exceeded and
+    # the tile is redone with its exact maximum
+    _check(256, 1024, 128, seed=6, stored=stored, w_row_scale=(slice(300, 308), 300.0))
 
 
-def test_lmhead_full_size_sampled_rows():
+@pytest.mark.parametrize("stored", [False, True])
+def test_lmhead_forward_only(stored):
+    _check(256, 4096, 256, seed=5, grads=False, stored=stored)
+
+
+@pytest.mark.parametrize("stored", [False, True])
+def test_lmhead_full_size_sampled_rows(stored):
     # the full fused LM-head shape (16384 tokens, H = 2048, V = 151936) in the bench's launch
     # configuration; per-token outputs and d_h checked on sampled rows (the oracle recomputes
     # those rows' logits one by one), dW checked by a property that holds at any size: every
@@ -124,7 +144,7 @@ def test_lmhead_full_size_sampled_rows():
     h, Wt = W.make_lmhead_inputs(wl, DEV)
     adv = np.random.default_rng(9).choice([-1.5, -0.3, 0.4, 1.2], T).astype(np.float32)
     N = int(wl.mask.sum())
-    d_h, dW, loss, logp, acc = _run(h, Wt, wl, wl.mask, adv, None, 1.0 / N)
+    d_h, dW, loss, logp, acc = _run(h, Wt, wl, wl.mask, adv, None, 1.0 / N, stored=stored)
     res = _lib.grpo_finish_step(acc, loss, expected_N=N)
     assert res["status"] == 0 and res["n_valid"] == N
     rows = np.array([0, 1, 127, 128, 5000, 9999, 16254, 16383])
