@@ -32,9 +32,9 @@ sys.path.insert(0, ROOT)
 METRIC = "GRPO loss fwd+bwd valid tokens/s at V=151936 bf16; % of HBM roofline"
 UNIT = "valid tokens/s"
 FALLBACK_HBM_GBS = 6800.0
-# sources the row-pass kernel is compiled from (the profile records their combined hash)
+# device code of the row-pass kernel (the profile records the combined hash of these files)
 KERNEL_SRC = tuple(os.path.join(ROOT, "rl_post_token_gb300", "csrc", f)
-                   for f in ("grpo_rowpass.cu", "grpo_common.cuh"))
+                   for f in ("grpo_rowpass_kernels.cuh", "grpo_common.cuh"))
 
 
 def kernel_source_sha256() -> str:

@@ -579,12 +579,16 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
   CUtensorMap map_h, map_w;
   if (!make_map(&map_h, h, (uint64_t)T, (uint64_t)H, BM) || !make_map(&map_w, W, (uint64_t)V, (uint64_t)H, BN))
     return GRPO_ERR_UNSUPPORTED;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  GRPO_CUDA_TRY(cudaGetDevice(&dev));
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    GRPO_CUDA_TRY(cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES));
-    attr_set[dev] = true;
+  {
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    GRPO_CUDA_TRY(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+      GRPO_CUDA_TRY(cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES));
+      if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
   }
   const int n_row_tiles = (int)((T + BM - 1) / BM);
 

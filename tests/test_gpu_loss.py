@@ -520,3 +520,49 @@ def test_terms_reject_bad_arguments():
         _lib.grpo_logprob_loss_fwd_bwd(x, i, None, f, mk, 0.2, 1.0, None, f, None, acc, terms=dict(kl_kind=7))
     with pytest.raises(_lib.GrpoError):
         _lib.grpo_logprob_loss_fwd_bwd(x, i, None, f, mk, 0.2, 1.0, None, f, None, acc, terms=dict(kl_kind=1))
+
+
+def test_concurrent_host_threads_bitwise():
+    # two host threads, two streams, two vocabularies (two shared-memory sizes of the cluster
+    # kernel), launching at once: every result equals the single-threaded one bit for bit
+    import threading
+
+    cases = []
+    for V, seed in ((16384, 91), (151936, 92)):
+        wl = W.make_workload("tiny", rows=4, positions=12, valid_lo=0, V=V, dtype="bf16", seed=seed, std=2.0)
+        cases.append(H.Case(wl))
+
+    def run(case, stream, n):
+        outs = []
+        with torch.cuda.stream(stream):
+            for _ in range(n):
+                T = case.logits.shape[0]
+                dl = torch.empty_like(case.logits)
+                loss = torch.empty(T, device=DEV)
+                acc = _lib.new_step_acc(DEV)
+                _lib.grpo_logprob_loss_fwd_bwd(case.logits, case.d_target, case.d_old, case.d_adv, case.d_mask,
+                                               case.wl.eps, 1.0 / 41, dl, loss, None, acc, stream=stream)
+                outs.append((dl, loss))
+        stream.synchronize()
+        return outs
+
+    ref = [run(c, torch.cuda.Stream(), 1)[0] for c in cases]
+    got = [None, None]
+    errs = []
+
+    def worker(i):
+        try:
+            got[i] = run(cases[i], torch.cuda.Stream(), 12)
+        except Exception as e:  # surfaced below
+            errs.append(e)
+
+    th = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    assert not errs, errs
+    for i in range(2):
+        for dl, loss in got[i]:
+            assert torch.equal(dl.view(torch.int16), ref[i][0].view(torch.int16))
+            assert torch.equal(loss, ref[i][1])
