@@ -74,6 +74,34 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
+// CTA-pair variants: the load lands at the same shared-memory offset in every CTA of `mask`
+// and completes bytes on the mbarrier at `bar`'s offset in each of them; the commit arrives on
+// the mbarrier at `bar`'s offset in every CTA of `mask`.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%3, %4}], [%2], %5;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+      ::"r"(bar), "h"(mask)
+      : "memory");
+}
+
+// Bounded wait that ignores the abort flag: the end-of-kernel drains after a timeout.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 0; i < (1u << 24); ++i) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((i & 255u) == 0 && global_timer_ns() - t0 > 1000000000ull) return;
+  }
+}
+
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
@@ -131,6 +159,31 @@ __device__ __forceinline__ void store_e_chunk(const GemmArgs& g, bool rok, int64
   s += tree_sum(v);  // reduces v in place: after the store
 }
 
+// Work units of a launch. One CTA: a unit is one 128 x 256 tile. CTA pair (a 2-CTA cluster): a
+// unit is two vertically adjacent tiles sharing one W tile; CTA r of the pair computes row tile
+// 2u + r (past the last row tile it computes zero-filled rows whose results are discarded).
+template <bool PAIR>
+struct Units {
+  int n_row_units, n, first, stride;
+  uint32_t rank;
+  __device__ Units(const GemmArgs& g, uint32_t r) : rank(r) {
+    n_row_units = PAIR ? (g.n_row_tiles + 1) / 2 : g.n_row_tiles;
+    n = n_row_units * g.n_col_tiles;
+    first = PAIR ? (int)(blockIdx.x / 2) : (int)blockIdx.x;
+    stride = PAIR ? (int)(gridDim.x / 2) : (int)gridDim.x;
+  }
+  __device__ void tile(const GemmArgs& g, int t, int& rt, int& ct) const {
+    const int ru = t % n_row_units;
+    ct = g.col_tile0 + t / n_row_units;
+    rt = PAIR ? 2 * ru + (int)rank : ru;
+  }
+};
+
+// PAIR = false: one CTA per SM loads its h tile and the whole W tile. PAIR = true: the two CTAs
+// of a cluster each load their own h tile and one 128-row half of the shared W tile, multicast
+// into both, so each CTA pulls 32 KB per K step from L2 instead of 48 KB. A stage is refilled
+// only after both CTAs' MMAs have released it (each commit arrives on both CTAs' barrier).
+template <bool PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w, GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
@@ -147,7 +200,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ C
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], PAIR ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -164,24 +217,44 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ C
   }
   fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync_all();  // the peer's barriers exist before anything targets them
   fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int n_tiles = g.n_row_tiles * g.n_col_tiles;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const Units<PAIR> units(g, rank);
   const int KB = (int)(g.H / BK);
+  uint32_t issued = 0;  // producer: stage loads issued
 
   if (warp == 0) {
     // ---- TMA producer ----
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
-      for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-        const int rt = t % g.n_row_tiles, ct = g.col_tile0 + t / g.n_row_tiles;
+      for (int t = units.first; t < units.n; t += units.stride) {
+        int rt, ct;
+        units.tile(g, t, rt, ct);
         for (int kb = 0; kb < KB; ++kb) {
           mbar_wait_bounded(&empty[stage], phase ^ 1u, s_abort);
           mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           tma_load_2d(sa, &map_h, smem_u32(&full[stage]), kb * BK, rt * BM);
-          tma_load_2d(sa + A_BYTES, &map_w, smem_u32(&full[stage]), kb * BK, ct * BN);
+          if (PAIR)
+            tma_load_2d_mc(sa + A_BYTES + rank * (B_BYTES / 2), &map_w, smem_u32(&full[stage]), kb * BK,
+                           ct * BN + (int)rank * (BN / 2), (uint16_t)0x3);
+          else
+            tma_load_2d(sa + A_BYTES, &map_w, smem_u32(&full[stage]), kb * BK, ct * BN);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (PAIR) {
+        // every stage's last release (this CTA's commit and the peer's) has arrived before
+        // this CTA may leave: the peer's commits target this CTA's barriers
+        for (int i = 0; i < STAGES; ++i) {  // a stage never used passes at once
+          mbar_wait_bounded(&empty[stage], phase ^ 1u, s_abort);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -193,7 +266,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ C
     // ---- MMA issuer ----
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, ab = 0, aphase = 0;
-      for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+      for (int t = units.first; t < units.n; t += units.stride) {
         mbar_wait_bounded(&tempty[ab], aphase ^ 1u, s_abort);
         fence_after();
         const uint32_t d = tmem + ab * BN;
@@ -205,7 +278,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ C
 #pragma unroll
           for (int j = 0; j < BK / 16; ++j)  // +32 bytes along K per 16-element step
             mma_bf16(d, da + 2 * j, db + 2 * j, kb > 0 || j > 0);
-          mma_commit(smem_u32(&empty[stage]));
+          if (PAIR)
+            mma_commit_mc(smem_u32(&empty[stage]), (uint16_t)0x3);
+          else
+            mma_commit(smem_u32(&empty[stage]));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -223,8 +299,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ C
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int trow = quarter * 32 + lane;
     uint32_t ab = 0, aphase = 0;
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-      const int rt = t % g.n_row_tiles, ct = g.col_tile0 + t / g.n_row_tiles;
+    for (int t = units.first; t < units.n; t += units.stride) {
+      int rt, ct;
+      units.tile(g, t, rt, ct);
       mbar_wait_bounded(&tfull[ab], aphase, s_abort);
       fence_after();
       const int64_t row = (int64_t)rt * BM + trow;
@@ -374,6 +451,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ C
 
   fence_before();
   __syncthreads();
+  if (PAIR) {
+    cluster_sync_all();  // neither CTA leaves while the other may still signal or copy into it
+    if (*s_abort && threadIdx.x == 0) {
+      // after a timeout, let this CTA's copies and the peer's arrivals settle (bounded)
+      for (int sidx = 0; sidx < STAGES && (uint32_t)sidx < issued; ++sidx) {
+        const uint32_t uses = (issued - 1u - (uint32_t)sidx) / STAGES;
+        drain_wait(&full[sidx], uses & 1u);
+        drain_wait(&empty[sidx], uses & 1u);
+      }
+    }
+  }
   if (*s_abort && threadIdx.x == 0) atomicOr(&g.acc->flags, kFlagWaitTimeout);
   if (warp == 1) {
     fence_after();
@@ -507,6 +595,67 @@ cublasHandle_t blas_handle() {
   return h[dev];
 }
 
+// GEMM variant: the CTA pair unless GRPO_LMHEAD_PAIR=0 selects the one-CTA kernel.
+bool use_pair() {
+  const char* e = getenv("GRPO_LMHEAD_PAIR");
+  return !(e && e[0] == '0');
+}
+
+// h and W tensor maps for a variant (the pair loads W in 128-row halves).
+bool make_maps(CUtensorMap* map_h, CUtensorMap* map_w, const void* h, const void* W, int64_t T, int64_t V, int64_t H,
+               bool pair) {
+  return make_map(map_h, h, (uint64_t)T, (uint64_t)H, BM) &&
+         make_map(map_w, W, (uint64_t)V, (uint64_t)H, pair ? BN / 2 : BN);
+}
+
+// Launch one GEMM pass over the tiles g describes. The first launch of a variant on a device
+// sets its shared-memory limit and caches how many CTAs (or CTA pairs) fit at once.
+template <bool PAIR>
+int launch_gemm_t(const CUtensorMap& map_h, const CUtensorMap& map_w, const GemmArgs& g, cudaStream_t st) {
+  auto kern = gemm_kernel<PAIR>;
+  int dev = 0;
+  GRPO_CUDA_TRY(cudaGetDevice(&dev));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = PAIR ? 1 : 0;
+  int max_units = 0;
+  {
+    static std::mutex mu;
+    static int cached[64] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64) max_units = cached[dev];
+    if (max_units == 0) {
+      GRPO_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES));
+      if (PAIR) {
+        cfg.gridDim = dim3(2 * 1024, 1, 1);
+        GRPO_CUDA_TRY(cudaOccupancyMaxActiveClusters(&max_units, kern, &cfg));
+      } else {
+        max_units = sm_count();
+      }
+      if (max_units < 1) return GRPO_ERR_UNSUPPORTED;
+      if (dev >= 0 && dev < 64) cached[dev] = max_units;
+    }
+  }
+  const int64_t row_units = PAIR ? (g.n_row_tiles + 1) / 2 : g.n_row_tiles;
+  const int64_t units = std::min<int64_t>(row_units * g.n_col_tiles, max_units);
+  if (units <= 0) return GRPO_OK;
+  cfg.gridDim = dim3((unsigned)(PAIR ? 2 * units : units), 1, 1);
+  GRPO_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, map_h, map_w, g));
+  return GRPO_OK;
+}
+
+int launch_gemm(bool pair, const CUtensorMap& map_h, const CUtensorMap& map_w, const GemmArgs& g, cudaStream_t st) {
+  return pair ? launch_gemm_t<true>(map_h, map_w, g, st) : launch_gemm_t<false>(map_h, map_w, g, st);
+}
+
 }  // namespace lmhead
 }  // namespace grpo
 
@@ -576,20 +725,9 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
   float* coef = reinterpret_cast<float*>(wsb + ws.coef);
   __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(wsb + ws.dz);
 
+  const bool pair = use_pair();
   CUtensorMap map_h, map_w;
-  if (!make_map(&map_h, h, (uint64_t)T, (uint64_t)H, BM) || !make_map(&map_w, W, (uint64_t)V, (uint64_t)H, BN))
-    return GRPO_ERR_UNSUPPORTED;
-  {
-    static std::mutex mu;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    GRPO_CUDA_TRY(cudaGetDevice(&dev));
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-      GRPO_CUDA_TRY(cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES));
-      if (dev >= 0 && dev < 64) attr_set[dev] = true;
-    }
-  }
+  if (!make_maps(&map_h, &map_w, h, W, T, V, H, pair)) return GRPO_ERR_UNSUPPORTED;
   const int n_row_tiles = (int)((T + BM - 1) / BM);
 
   GemmArgs g{};
@@ -614,9 +752,8 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
   g.col_tile0 = 0;
   g.n_col_tiles = ws.n_col_tiles;
   {
-    const int grid = (int)std::min<int64_t>((int64_t)n_row_tiles * ws.n_col_tiles, sm_count());
-    gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(map_h, map_w, g);
-    GRPO_CUDA_TRY(cudaGetLastError());
+    const int rc = launch_gemm(pair, map_h, map_w, g, st);
+    if (rc != GRPO_OK) return rc;
   }
   reduce_kernel<<<(unsigned)((T + 255) / 256), 256, 0, st>>>(T, ws.n_col_tiles, part_m, part_s, zy, target, V,
                                                               old_logp, adv_tok, mask, clip_eps, grad_scale, lse2,
@@ -657,9 +794,8 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
     g.col_tile0 = ct0;
     g.n_col_tiles = nct;
     g.v0 = v0;
-    const int grid = (int)std::min<int64_t>((int64_t)n_row_tiles * nct, sm_count());
-    gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(map_h, map_w, g);
-    GRPO_CUDA_TRY(cudaGetLastError());
+    const int rc = launch_gemm(pair, map_h, map_w, g, st);
+    if (rc != GRPO_OK) return rc;
     const __nv_bfloat16* Wc = static_cast<const __nv_bfloat16*>(W) + v0 * H;
     // d_h[T,H] (+)= dz[T,vc] W_c[vc,H]   (column-major view: d_h^T = W_c^T dz^T)
     if (d_h &&
@@ -696,7 +832,8 @@ static __device__ __align__(256) unsigned char g_lmhead_noalloc_scratch[kNoAlloc
 namespace {
 
 // Device address of the scratch array on the current device; the first call on a device does
-// the lookup (and sets the GEMM kernel's shared-memory attribute) and caches both.
+// the lookup and caches it (the GEMM launcher sets the kernel's shared-memory limit on its own
+// first launch on the device).
 int noalloc_setup(void** scratch) {
   static void* addr[64] = {};
   static std::mutex mu;
@@ -710,11 +847,6 @@ int noalloc_setup(void** scratch) {
   if (!addr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_lmhead_noalloc_scratch) != cudaSuccess || !p) {
-      (void)cudaGetLastError();
-      return GRPO_ERR_CUDA;
-    }
-    if (cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) !=
-        cudaSuccess) {
       (void)cudaGetLastError();
       return GRPO_ERR_CUDA;
     }
@@ -751,9 +883,9 @@ extern "C" GRPO_API int grpo_lmhead_forward_noalloc(const void* h, const void* W
   float* lse2 = reinterpret_cast<float*>(wsb + ws.lse2);
   float* coef = reinterpret_cast<float*>(wsb + ws.coef);
 
+  const bool pair = use_pair();
   CUtensorMap map_h, map_w;
-  if (!make_map(&map_h, h, (uint64_t)T, (uint64_t)H, BM) || !make_map(&map_w, W, (uint64_t)V, (uint64_t)H, BN))
-    return GRPO_ERR_UNSUPPORTED;
+  if (!make_maps(&map_h, &map_w, h, W, T, V, H, pair)) return GRPO_ERR_UNSUPPORTED;
   const cudaStream_t st = as_stream(stream);
   GemmArgs g{};
   g.T = T;
@@ -770,9 +902,8 @@ extern "C" GRPO_API int grpo_lmhead_forward_noalloc(const void* h, const void* W
   g.mode = 0;
   g.col_tile0 = 0;
   g.n_col_tiles = ws.n_col_tiles;
-  const int grid = (int)std::min<int64_t>((int64_t)g.n_row_tiles * ws.n_col_tiles, sm_count());
-  gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(map_h, map_w, g);
-  GRPO_CUDA_TRY(cudaGetLastError());
+  const int lrc = launch_gemm(pair, map_h, map_w, g, st);
+  if (lrc != GRPO_OK) return lrc;
   reduce_kernel<<<(unsigned)((T + 255) / 256), 256, 0, st>>>(T, ws.n_col_tiles, part_m, part_s, zy, target, V,
                                                               old_logp, adv_tok, mask, clip_eps, grad_scale, lse2,
                                                               coef, loss_tok, logp_tok, acc);
