@@ -1,22 +1,26 @@
 // Fused LM-head variant of the loss: the logits z = h W^T are produced on the tensor cores
-// tile by tile and consumed by the softmax in the GEMM epilogue, so the [T, V] logits never
-// reach memory ("Sizing mini-batches and micro-batches", "The problem": the log-softmax over
-// the vocabulary of 2048-token completions is what runs out of memory).
+// tile by tile and consumed by the softmax in the GEMM epilogue, so the [T, V] float32 logits
+// and their softmax never reach memory ("Sizing mini-batches and micro-batches", "The problem":
+// the log-softmax over the vocabulary of 2048-token completions is what runs out of memory).
 //
 //  pass A  tcgen05 GEMM over all (128-token x 256-vocab) tiles; the epilogue reduces each
-//          tile row to a log2-domain (max, sum-exp) partial and picks up the target logit.
+//          tile row to a log2-domain (shift, sum-exp) partial and picks up the target logit
+//          (stored path: it also writes e = 2^(z log2 e - shift) of the tile as bf16).
 //  reduce  per token: combine the partials in vocabulary order -> LSE, log-prob, ratio,
 //          clipped surrogate, gradient coefficient (same token epilogue as the row pass).
-//  pass B  per vocabulary chunk: the same GEMM recomputes the chunk's logits and its epilogue
-//          writes dlogits (bf16) into a bounded chunk workspace; then d_h += dz_c W_c and
-//          dW_c = dz_c^T h (plain GEMMs, cuBLAS, float32 outputs).
+//  backward, recompute path (minimum workspace): per vocabulary chunk the same GEMM recomputes
+//          the chunk's logits and its epilogue writes dlogits (bf16) into a bounded chunk
+//          workspace; then d_h += dz_c W_c and dW_c = dz_c^T h (cuBLAS, float32 outputs).
+//  backward, stored path (workspace for the whole [T, V] exponent matrix): dz_from_e_kernel
+//          turns the stored e into dlogits in place; then one d_h and one dW GEMM.
 //
-// GEMM kernel: persistent, one CTA per SM, 6 warps. Warp 0 issues TMA loads (128-byte
-// swizzled 128x64 h tiles and 256x64 W tiles) into a 4-stage shared-memory ring; warp 1 issues
-// tcgen05.mma (M=128, N=256, K=16, bf16 -> f32) into a double-buffered TMEM accumulator
-// (2 x 256 columns); warps 2-5 read the accumulator with tcgen05.ld (one TMEM lane = one token
-// row per thread) and run the epilogue while the next tile's MMAs proceed. Every mbarrier wait
-// is bounded and raises a flag instead of hanging.
+// GEMM kernel: persistent, one CTA per SM, 6 warps, launched as 2-CTA clusters (CTA pair) or
+// as single CTAs. Warp 0 issues TMA loads (128-byte swizzled 128x64 h tiles and 256x64 W tiles;
+// in a pair each CTA loads one 128-row half of W, multicast to both) into a 4-stage
+// shared-memory ring; warp 1 issues tcgen05.mma (M=128, N=256, K=16, bf16 -> f32) into a
+// double-buffered TMEM accumulator (2 x 256 columns); warps 2-5 read the accumulator with
+// tcgen05.ld (one TMEM lane = one token row per thread) and run the epilogue while the next
+// tile's MMAs proceed. Every mbarrier wait is bounded and raises a flag instead of hanging.
 #include <cublas_v2.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
