@@ -52,7 +52,8 @@ __global__ void adv_broadcast_kernel(const float* __restrict__ adv,
   }
 }
 
-constexpr int kFinishThreads = 1024;
+constexpr int kFinishCtas = 8;       // one cluster
+constexpr int kFinishThreads = 256;  // per CTA
 
 // One term of the step sum: the token's loss, times its aggregation weight when there is one
 // (the product of two floats is exact in float64).
@@ -62,18 +63,27 @@ __device__ __forceinline__ double weighted(const float* __restrict__ loss_tok, c
   return W ? (double)w_tok[i] * (double)loss_tok[i] : (double)loss_tok[i];
 }
 
-// One CTA: float64 sum of the step's (weighted) per-token losses in a fixed order
-// (thread-strided partial sums, then a fixed tree), the metrics, the status, the divisor, and
-// the counter reset.
+__device__ __forceinline__ double ld_dsmem_f64(uint32_t addr) {
+  double v;
+  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// One cluster of kFinishCtas CTAs: CTA r sums the r-th contiguous eighth of the step's
+// (weighted) per-token losses in float64 (thread-strided partial sums, then a fixed tree);
+// CTA 0 adds the eight partials in rank order through distributed shared memory. The order
+// depends only on n. Then the metrics, the status, the divisor, and the counter reset.
 template <bool W>
 __global__ void __launch_bounds__(kFinishThreads)
 finish_kernel(grpo_step_acc* acc, const float* __restrict__ loss_tok, const float* __restrict__ w_tok,
               int64_t n, int64_t expected_N, int64_t divisor) {
   __shared__ double sh[kFinishThreads];
   const int tid = threadIdx.x;
+  const uint32_t rank = cluster_ctarank();
+  const int64_t lo = n * (int64_t)rank / kFinishCtas, hi = n * (int64_t)(rank + 1) / kFinishCtas;
   double s = 0.0;
-  int64_t i = tid;
-  for (; i + 3 * kFinishThreads < n; i += 4 * kFinishThreads) {
+  int64_t i = lo + tid;
+  for (; i + 3 * kFinishThreads < hi; i += 4 * kFinishThreads) {
     const double a0 = weighted<W>(loss_tok, w_tok, i), a1 = weighted<W>(loss_tok, w_tok, i + kFinishThreads);
     const double a2 = weighted<W>(loss_tok, w_tok, i + 2 * kFinishThreads);
     const double a3 = weighted<W>(loss_tok, w_tok, i + 3 * kFinishThreads);
@@ -82,38 +92,61 @@ finish_kernel(grpo_step_acc* acc, const float* __restrict__ loss_tok, const floa
     s += a2;
     s += a3;
   }
-  for (; i < n; i += kFinishThreads) s += weighted<W>(loss_tok, w_tok, i);
+  for (; i < hi; i += kFinishThreads) s += weighted<W>(loss_tok, w_tok, i);
   sh[tid] = s;
   __syncthreads();
   for (int w = kFinishThreads / 2; w > 0; w >>= 1) {
     if (tid < w) sh[tid] += sh[tid + w];
     __syncthreads();
   }
-  if (tid == 0) {
-    grpo_step_result r;
-    r.loss_sum = sh[0];
-    r.n_valid = (int64_t)acc->n_valid;
-    r.n_clipped = (int64_t)acc->n_clipped;
-    r.n_nonfinite = (int64_t)acc->n_nonfinite;
-    r.n_tokens = (int64_t)acc->n_tokens;
-    r.kernel_flags = (int32_t)acc->flags;
-    const double N = (double)(r.n_valid > 1 ? r.n_valid : 1);
-    const int64_t D = divisor >= 0 ? divisor : r.n_valid;
-    r.loss = r.loss_sum / (double)(D > 1 ? D : 1);
-    r.clipfrac = (double)r.n_clipped / N;
+  cluster_sync_all();  // every CTA's partial is in its sh[0]
+  if (rank == 0 && tid == 0) {
+    double total = 0.0;
+    const uint32_t a0 = smem_u32(&sh[0]);
+    for (int r = 0; r < kFinishCtas; ++r) total += ld_dsmem_f64(mapa_u32(a0, (uint32_t)r));
+    grpo_step_result res;
+    res.loss_sum = total;
+    res.n_valid = (int64_t)acc->n_valid;
+    res.n_clipped = (int64_t)acc->n_clipped;
+    res.n_nonfinite = (int64_t)acc->n_nonfinite;
+    res.n_tokens = (int64_t)acc->n_tokens;
+    res.kernel_flags = (int32_t)acc->flags;
+    const double N = (double)(res.n_valid > 1 ? res.n_valid : 1);
+    const int64_t D = divisor >= 0 ? divisor : res.n_valid;
+    res.loss = res.loss_sum / (double)(D > 1 ? D : 1);
+    res.clipfrac = (double)res.n_clipped / N;
     acc->divisor = D;
-    if (r.kernel_flags)
-      r.status = GRPO_ERR_KERNEL;
-    else if (expected_N >= 0 && expected_N != r.n_valid)
-      r.status = GRPO_ERR_N_MISMATCH;
-    else if (r.n_nonfinite > 0)
-      r.status = GRPO_STEP_SKIPPED_NONFINITE;
+    if (res.kernel_flags)
+      res.status = GRPO_ERR_KERNEL;
+    else if (expected_N >= 0 && expected_N != res.n_valid)
+      res.status = GRPO_ERR_N_MISMATCH;
+    else if (res.n_nonfinite > 0)
+      res.status = GRPO_STEP_SKIPPED_NONFINITE;
     else
-      r.status = GRPO_OK;
-    acc->result = r;
+      res.status = GRPO_OK;
+    acc->result = res;
     acc->n_valid = acc->n_clipped = acc->n_nonfinite = acc->n_tokens = 0;
     acc->flags = 0;
   }
+  cluster_sync_all();  // no CTA leaves while CTA 0 may still read its partial
+}
+
+template <bool W>
+int launch_finish(grpo_step_acc* acc, const float* loss_tok, const float* w_tok, int64_t n, int64_t expected_N,
+                  int64_t divisor, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kFinishCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(kFinishCtas, 1, 1);
+  cfg.blockDim = dim3(kFinishThreads, 1, 1);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  GRPO_CUDA_TRY(cudaLaunchKernelEx(&cfg, finish_kernel<W>, acc, loss_tok, w_tok, n, expected_N, divisor));
+  return GRPO_OK;
 }
 
 // Registered gradient buffer: zeroed when the step is discarded, else (deferred mode) scaled
@@ -176,11 +209,11 @@ extern "C" GRPO_API int grpo_finish_step_ex(grpo_step_acc* acc, const float* los
     if (grad_numels[b] < 0 || (grad_numels[b] > 0 && !grad_bufs[b])) return GRPO_ERR_INVALID;
   }
   const cudaStream_t st = as_stream(stream);
-  if (w_tok && n_tok > 0)
-    finish_kernel<true><<<1, kFinishThreads, 0, st>>>(acc, loss_tok, w_tok, n_tok, expected_N, divisor);
-  else
-    finish_kernel<false><<<1, kFinishThreads, 0, st>>>(acc, loss_tok, nullptr, n_tok, expected_N, divisor);
-  GRPO_CUDA_TRY(cudaGetLastError());
+  {
+    const int rc = w_tok && n_tok > 0 ? launch_finish<true>(acc, loss_tok, w_tok, n_tok, expected_N, divisor, st)
+                                      : launch_finish<false>(acc, loss_tok, nullptr, n_tok, expected_N, divisor, st);
+    if (rc != GRPO_OK) return rc;
+  }
   for (int32_t b = 0; b < n_bufs; ++b) {
     const int64_t n = grad_numels[b];
     if (n == 0) continue;
