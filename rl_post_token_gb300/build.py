@@ -2,7 +2,9 @@
 
 Each translation unit compiles in its own process (in parallel), then nvcc links the shared
 library with the static CUDA runtime, so the library loads on a machine without a GPU and
-needs no libcudart at run time. Objects go to ``rl_post_token_gb300/_build/``.
+needs no libcudart at run time. Objects go to ``rl_post_token_gb300/_build/``, with each CUDA
+file's ptxas resource report (registers, spills per kernel) beside its object as
+``<source>.ptxas.txt``.
 
     python -m rl_post_token_gb300.build [--force] [--verbose]
 """
@@ -42,8 +44,15 @@ def _deps():
     return files
 
 
+def ptxas_report(src: str) -> str:
+    """Path of the ptxas resource report of a CUDA source from the last build."""
+    return os.path.join(BUILD, src + ".ptxas.txt")
+
+
 def _up_to_date() -> bool:
     if not os.path.exists(LIB):
+        return False
+    if not all(os.path.exists(ptxas_report(s)) for s in SOURCES if s.endswith(".cu")):
         return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(f) <= t for f in _deps())
@@ -55,14 +64,15 @@ def _compile(src: str, verbose: bool) -> str:
     path = os.path.join(CSRC, src)
     common = ["-O3", "-std=c++17", f"-I{INCLUDE}", f"-I{CSRC}", "-Xcompiler", "-fPIC,-fvisibility=hidden"]
     if src.endswith(".cu"):
-        cmd = [nvcc, *ARCH, "-lineinfo", "--expt-relaxed-constexpr", *common, "-c", path, "-o", obj]
-        if verbose:
-            cmd.insert(1, "-Xptxas=-v")
+        cmd = [nvcc, *ARCH, "-Xptxas=-v", "-lineinfo", "--expt-relaxed-constexpr", *common, "-c", path, "-o", obj]
     else:
         cmd = [nvcc, "-x", "c++", *common, "-c", path, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"compiling {src} failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
+    if src.endswith(".cu"):
+        with open(ptxas_report(src), "w") as f:
+            f.write(r.stdout + r.stderr)
     if verbose and (r.stdout or r.stderr):
         sys.stderr.write(r.stdout + r.stderr)
     return obj

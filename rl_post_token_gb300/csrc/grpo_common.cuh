@@ -194,8 +194,10 @@ __device__ __forceinline__ void e_pairs_fast(const float (&x)[N], float sh, floa
   }
 }
 
+// `guarded` is set when the block needed the no-mass guard (or the rescue path, which uses
+// it): only then can the block hold a -inf logit.
 template <int N>
-__device__ __forceinline__ void lazy_online3(MS3& acc, const float (&x)[N]) {
+__device__ __forceinline__ void lazy_online3(MS3& acc, const float (&x)[N], bool& guarded) {
   if (acc.m == -INFINITY) acc.m = x[0] * kLog2e;
   float pe[N / 2], px[N / 2];
   e_pairs_fast<N>(x, acc.m, pe, px);
@@ -205,11 +207,13 @@ __device__ __forceinline__ void lazy_online3(MS3& acc, const float (&x)[N]) {
     if (bx != bx) {  // a -inf logit in the block: redo it with no-mass elements adding nothing
       e_pairs<N>(x, acc.m, pe, px);
       bx = tree_sum(px);
+      guarded = true;
     }
     acc.s += bs;
     acc.s2 += bx;
     return;
   }
+  guarded = true;
   float gm = x[0];
 #pragma unroll
   for (int i = 1; i < N; ++i) gm = fmaxf(gm, x[i]);

@@ -13,7 +13,7 @@ namespace grpo {
 
 size_t max_smem_optin();
 
-template <int C, int NCW, int VPT, int MINB, bool ENT, bool TERMS>
+template <int C, int NCW, int VPT, int MINB, bool ENT, int TERMS>
 int launch_cluster(const RowArgs& a, cudaStream_t st) {
   constexpr int CH = cluster_chunk_elems(NCW, VPT);
   const int Vs = cluster_slice_elems(a.V, C);
@@ -84,7 +84,7 @@ int launch_cluster(const RowArgs& a, cudaStream_t st) {
   return GRPO_OK;
 }
 
-template <typename T, int NT, int U, bool ENT, bool TERMS>
+template <typename T, int NT, int U, bool ENT, int TERMS>
 int launch_l2(const RowArgs& a, bool vec, int blocks_per_sm, cudaStream_t st) {
   const int64_t grid = std::min<int64_t>(a.T, (int64_t)sm_count() * blocks_per_sm);
   if (vec)
@@ -122,14 +122,15 @@ using namespace grpo;
 
 namespace {
 
-template <bool ENT, bool TERMS>
+template <bool ENT, int TERMS>
 int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
   const int64_t V = a.V;
   if (dtype == GRPO_DTYPE_BF16) {
     // Large bf16 vocabularies: rows split across a CTA cluster, slices staged in shared
     // memory. Variants (cluster size, consumer warps, vectors per thread, CTAs per SM):
     // c2 = (2, 16, 4, 1) with a ring of spare slots, c3 = (3, 8, 4, 2), c4 = (4, 8, 4, 2)
-    // with fixed staging buffers; the entropy instances take 2 vectors per thread.
+    // with fixed staging buffers; the entropy and per-token-weight instances take 2 vectors
+    // per thread.
     const char* pin = getenv("GRPO_ROWPASS");
     const bool cluster_ok = vec && V % 8 == 0 && V >= 16384;
     if (cluster_ok && !(pin && strcmp(pin, "l2") == 0)) {
@@ -139,11 +140,11 @@ int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
                (cluster_slice_elems(V, C) + cluster_chunk_elems(NCW, vpt) - 1) / cluster_chunk_elems(NCW, vpt) <=
                    kMaxChunks;
       };
-      // the entropy instances carry a third accumulator: half-size chunks keep them in registers
-      // where the chunk count allows
+      // the entropy and per-token-weight instances carry more per-thread state: half-size
+      // chunks keep them in registers where the chunk count allows
       auto c34 = [&](auto c_tag) {
         constexpr int C = decltype(c_tag)::value;
-        if constexpr (ENT)
+        if constexpr (ENT || TERMS == 2)
           if (fits(C, 8, 2, 2)) return launch_cluster<C, 8, 2, 2, ENT, TERMS>(a, st);
         return launch_cluster<C, 8, 4, 2, ENT, TERMS>(a, st);
       };
@@ -152,7 +153,7 @@ int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
       if (pin && strcmp(pin, "c3") == 0 && fits(3, 8, 2, 4)) return c34(C3{});
       if (pin && strcmp(pin, "c4") == 0 && fits(4, 8, 2, 4)) return c34(C4{});
       if (fits(2, 16, 1, 4)) {
-        if constexpr (ENT) return launch_cluster<2, 16, 2, 1, ENT, TERMS>(a, st);
+        if constexpr (ENT || TERMS == 2) return launch_cluster<2, 16, 2, 1, ENT, TERMS>(a, st);
         else return launch_cluster<2, 16, 4, 1, ENT, TERMS>(a, st);
       }
       if (fits(4, 8, 2, 4)) return c34(C4{});
@@ -199,9 +200,14 @@ extern "C" GRPO_API int grpo_logprob_loss_fwd_bwd_ex(const void* logits, int32_t
                    (!dlogits || (al16(dlogits) && (ld_out * es) % 16 == 0));
   // the entropy (as a loss term or as an output) needs sum_v p_v z_v, a third accumulator:
   // a separate kernel instance
-  if (terms && (terms->ent_coef != 0.f || terms->entropy_tok)) return dispatch<true, true>(a, dtype, vec, st);
-  if (terms && (terms->kl_kind != GRPO_KL_NONE || terms->w_tok)) return dispatch<false, true>(a, dtype, vec, st);
-  return dispatch<false, false>(a, dtype, vec, st);
+  // (per-token weights get instances of their own: the extra per-row value would push the
+  // other instances past their register budget)
+  const bool wt = terms && terms->w_tok;
+  if (terms && (terms->ent_coef != 0.f || terms->entropy_tok))
+    return wt ? dispatch<true, 2>(a, dtype, vec, st) : dispatch<true, 1>(a, dtype, vec, st);
+  if (terms && (terms->kl_kind != GRPO_KL_NONE || wt))
+    return wt ? dispatch<false, 2>(a, dtype, vec, st) : dispatch<false, 1>(a, dtype, vec, st);
+  return dispatch<false, 0>(a, dtype, vec, st);
 }
 
 extern "C" GRPO_API int grpo_logprob_loss_fwd_bwd(const void* logits, int32_t dtype, int64_t T, int64_t V,

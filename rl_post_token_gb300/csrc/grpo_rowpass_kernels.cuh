@@ -102,7 +102,8 @@ __device__ __forceinline__ int64_t row_src(const RowArgs& a, int64_t row) {
   return a.tok_src ? a.tok_src[row] : row;
 }
 
-template <bool REF>
+// TERMS: 0 = no extra terms, 1 = KL/entropy terms, 2 = terms and per-token weights
+template <int TERMS>
 __device__ __forceinline__ RowMeta row_meta(const RowArgs& a, int64_t src) {
   RowMeta m{src < 0 ? -1 : src, false, 0, 0.f, 0.f, 0.f, 1.f};
   if (src >= 0) {
@@ -110,8 +111,8 @@ __device__ __forceinline__ RowMeta row_meta(const RowArgs& a, int64_t src) {
     m.y = a.target[src];
     m.A = a.adv[src];
     m.old = a.old_logp ? a.old_logp[src] : 0.f;
-    if (REF) m.ref = a.ref_logp ? a.ref_logp[src] : 0.f;
-    if (REF) m.w = a.w_tok ? a.w_tok[src] : 1.f;
+    if (TERMS) m.ref = a.ref_logp ? a.ref_logp[src] : 0.f;
+    if (TERMS == 2) m.w = a.w_tok[src];
   }
   return m;
 }
@@ -119,20 +120,20 @@ __device__ __forceinline__ RowMeta row_meta(const RowArgs& a, int64_t src) {
 // Row metadata fetched ahead of use: the token index two rows ahead and the side inputs one
 // row ahead are in flight while the current row is processed, so the dependent global-load
 // chain (index -> mask/target/advantage/pi_old) never sits on a row's critical path.
-template <bool REF>
+template <int TERMS>
 struct MetaPipe {
   const RowArgs& a;
   int64_t stride;
   RowMeta next;
   int64_t src2;
   __device__ MetaPipe(const RowArgs& args, int64_t first, int64_t step) : a(args), stride(step) {
-    next = first < a.T ? row_meta<REF>(a, row_src(a, first)) : RowMeta{-1, false, 0, 0.f, 0.f, 0.f, 1.f};
+    next = first < a.T ? row_meta<TERMS>(a, row_src(a, first)) : RowMeta{-1, false, 0, 0.f, 0.f, 0.f, 1.f};
     src2 = first + step < a.T ? row_src(a, first + step) : -1;
   }
   // metadata of `row`; starts the loads for the rows after it
   __device__ RowMeta advance(int64_t row) {
     const RowMeta m = next;
-    if (row + stride < a.T) next = row_meta<REF>(a, src2);
+    if (row + stride < a.T) next = row_meta<TERMS>(a, src2);
     src2 = row + 2 * stride < a.T ? row_src(a, row + 2 * stride) : -1;
     return m;
   }
@@ -157,7 +158,7 @@ struct Counts {
 // ------------------------------------------------------------------------------------------
 // Generic kernel: one CTA per row at a time, persistent over rows.
 // ------------------------------------------------------------------------------------------
-template <typename T, int NT, int U, bool VEC, bool ENT, bool TERMS>
+template <typename T, int NT, int U, bool VEC, bool ENT, int TERMS>
 __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
   constexpr int VN = Vec<T>::N;
   constexpr int NW = NT / 32;
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
       }
       if (lane == 0) {
         const float lse = v.m + logf(v.s);
-        const float sc = TERMS ? a.scale * tm.w : a.scale;
+        const float sc = TERMS == 2 ? a.scale * tm.w : a.scale;
         TokenOut o = token_epilogue(ybad ? __int_as_float(0x7fc00000) : zy, lse,
                                     a.old_logp != nullptr, tm.old, tm.A, a.eps, sc);
         if (TERMS) apply_terms(o, sc, a.kl_kind, a.kl_coef, tm.ref, a.ent_coef, lse - ez);
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
     __syncthreads();
     const float lse = sh_lse, coef = sh_coef;
     // entropy gradient: dz_v = p_v (ea + eb z_v) - coef [v == y]
-    const float eb = ENT ? a.scale * tm.w * a.ent_coef : 0.f;
+    const float eb = ENT ? (TERMS == 2 ? a.scale * tm.w : a.scale) * a.ent_coef : 0.f;
     const float ea = ENT ? coef - eb * sh_ez : coef;
 
     // pass 2: dlogits = coef * (softmax - onehot)
@@ -388,11 +389,17 @@ __device__ __forceinline__ void dz_vec(const uint4& u, uint4* dst, float cexp) {
 }
 
 // Eight dlogits with the entropy term: 2^(z log2e - lse2) * (ea + eb z), rounded to bf16.
+// GUARD: an element without mass (a -inf logit) gives 0 instead of 0 * inf; needed only where
+// pass 1 met such an element.
+template <bool GUARD>
 __device__ __forceinline__ void dz_vec_ent(const uint4& u, uint4* dst, float lse2, float ea, float eb) {
   float x[8];
   Vec<__nv_bfloat16>::unpack(u, x);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) x[i] = ent_dz(ex2(fmaf(x[i], kLog2e, -lse2)), x[i], ea, eb);
+  for (int i = 0; i < 8; ++i) {
+    const float p = ex2(fmaf(x[i], kLog2e, -lse2));
+    x[i] = GUARD ? ent_dz(p, x[i], ea, eb) : p * fmaf(eb, x[i], ea);
+  }
   __stcs(dst, make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
                          pack_bf16x2(x[6], x[7])));
 }
@@ -421,7 +428,7 @@ struct RingCursor {
 };
 
 // Pass 2 with the entropy term over the CTA's slice, chunk k read from its ring slot.
-template <int NC, int VPT, int CH>
+template <bool GUARD, int NC, int VPT, int CH>
 __device__ __forceinline__ void pass2_slice_ent(const __nv_bfloat16* ring, RingCursor c, int S, uint4* dz, int n_r,
                                                 int nch, int ct, int lane, float lse2, float ea, float eb,
                                                 uint64_t* empty) {
@@ -431,9 +438,9 @@ __device__ __forceinline__ void pass2_slice_ent(const __nv_bfloat16* ring, RingC
     uint4* dv = dz + k * (CH / 8);
     if (nv == VPT * NC) {
 #pragma unroll
-      for (int j = 0; j < VPT; ++j) dz_vec_ent(sv[ct + j * NC], dv + ct + j * NC, lse2, ea, eb);
+      for (int j = 0; j < VPT; ++j) dz_vec_ent<GUARD>(sv[ct + j * NC], dv + ct + j * NC, lse2, ea, eb);
     } else {
-      for (int v = ct; v < nv; v += NC) dz_vec_ent(sv[v], dv + v, lse2, ea, eb);
+      for (int v = ct; v < nv; v += NC) dz_vec_ent<GUARD>(sv[v], dv + v, lse2, ea, eb);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[c.slot]);
@@ -477,7 +484,7 @@ __host__ __device__ constexpr size_t cluster_ring_bytes(int Vs, int CH, int S) {
   return S > (Vs + CH - 1) / CH ? (size_t)S * CH * 2 : ((size_t)Vs * 2 + 127) / 128 * 128;
 }
 
-template <int C, int NCW, int VPT, int MINB, bool ENT, bool TERMS>
+template <int C, int NCW, int VPT, int MINB, bool ENT, int TERMS>
 __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowArgs a, int Vs, int S) {
   constexpr int NC = NCW * 32;
   constexpr int WS = ENT ? 3 : 2;  // floats per warp partial
@@ -584,6 +591,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
       // pass 1: log2-domain (shift, sum) over the slice, chunk by chunk as it lands
       MS acc{-INFINITY, 0.f};
       MS3 acc3{-INFINITY, 0.f, 0.f};
+      bool guarded = false;  // entropy: pass 1 met a -inf logit among this thread's elements
       RingCursor c = rc;
       for (int k = 0; k < nch; ++k) {
         mbar_wait_bounded(&full[c.slot], c.ph, s_abort);
@@ -594,7 +602,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
 #pragma unroll
           for (int j = 0; j < VPT; ++j) unpack8_at(sv[ct + j * NC], x + 8 * j);
           if (ENT)
-            lazy_online3<VPT * 8>(acc3, x);
+            lazy_online3<VPT * 8>(acc3, x, guarded);
           else
             lazy_online2<VPT * 8>(acc, x);
         } else {
@@ -602,7 +610,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
             float x[8];
             Vec<__nv_bfloat16>::unpack(sv[v], x);
             if (ENT)
-              lazy_online3<8>(acc3, x);
+              lazy_online3<8>(acc3, x, guarded);
             else
               lazy_online2<8>(acc, x);
           }
@@ -663,7 +671,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
       if (ENT) tot = MS{tot3.m, tot3.s};
       const float lse2 = tot.m + log2f(tot.s);  // log2(sum_v 2^(z_v log2 e)) = LSE * log2(e)
       const float ez = ENT ? tot3.s2 / tot3.s : 0.f;  // sum_v p_v z_v
-      const float sc = TERMS ? a.scale * tm.w : a.scale;
+      const float sc = TERMS == 2 ? a.scale * tm.w : a.scale;
       TokenOut o = token_epilogue(zy, lse2 * kLn2, a.old_logp != nullptr, tm.old, tm.A, a.eps, sc);
       if (TERMS) apply_terms(o, sc, a.kl_kind, a.kl_coef, tm.ref, a.ent_coef, lse2 * kLn2 - ez);
       if (rank == 0 && ct == 0) {
@@ -680,7 +688,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
       if (ENT && dz && eb != 0.f) {
         // with the entropy term: dz_v = p_v (ea + eb z_v) - coef [v == y]
         const float ea = coef - eb * ez;
-        pass2_slice_ent<NC, VPT, CH>(ring, rc, SL, dz, n_r, nch, ct, lane, lse2, ea, eb, empty);
+        // pass 2 visits this thread's pass-1 elements; the warp takes the guarded form if any
+        // of its threads met a -inf logit
+        if (__any_sync(0xffffffffu, guarded))
+          pass2_slice_ent<true, NC, VPT, CH>(ring, rc, SL, dz, n_r, nch, ct, lane, lse2, ea, eb, empty);
+        else
+          pass2_slice_ent<false, NC, VPT, CH>(ring, rc, SL, dz, n_r, nch, ct, lane, lse2, ea, eb, empty);
         const int64_t yl = ybad ? -1 : (int64_t)y - base;
         if (yl >= 0 && yl < n_r && ct == (int)(((yl / 8) % (CH / 8)) % NC)) {
           const float dzy = ent_dz(ex2(fmaf(zy, kLog2e, -lse2)), zy, ea, eb) - coef;

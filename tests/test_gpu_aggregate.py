@@ -91,8 +91,10 @@ def test_seq_aggregation_matches_oracle(kind, agg):
 
 
 def test_token_mean_through_the_weighted_path_equals_plain():
-    # TOKEN_MEAN through the weighted entry points (weights all 1, divisor N) gives the same
-    # bits as the plain path
+    # TOKEN_MEAN through the weighted entry points (weights all 1, divisor N) matches the plain
+    # path: the weighted kernel instance sums a row in 16-element blocks instead of 32, so the
+    # LSE may differ in its last bit; counts are identical, losses agree within the per-token
+    # parity bar and dlogits to one bf16 rounding step
     wl = _workload("fixed", 0)
     case = H.Case(wl)
     outs = []
@@ -106,9 +108,19 @@ def test_token_mean_through_the_weighted_path_equals_plain():
                     mask=case.d_mask, adv_tok=case.d_adv, loss_tok=loss, logp_tok=None, accs=accs,
                     clip_eps=wl.eps, agg=_lib.AGG_TOKEN_MEAN, w_tok=w_d)
         torch.cuda.synchronize()
-        outs.append((dl.view(torch.int16).clone(), loss.clone(), S.read_results(accs, bp.n_steps)))
-    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
-    assert outs[0][2] == outs[1][2]
+        outs.append((dl.float().clone(), loss.clone(), S.read_results(accs, bp.n_steps)))
+    (d0, l0, r0), (d1, l1, r1) = outs
+    # one bf16 step (2^-7 relative at most), plus a little at the target element, where
+    # coef * (p_y - 1) cancels
+    rowmax = d0.abs().amax(dim=1, keepdim=True)
+    assert torch.all((d1 - d0).abs() <= 2.0 ** -7 * d0.abs() + 1e-5 * rowmax + 1e-12)
+    # a last-bit LSE difference moves log p by ~1e-6 and the loss by as much relative: the
+    # per-token parity bar
+    assert torch.all((l1 - l0).abs() <= 1e-5 * l0.abs() + 1e-7)
+    for a, b in zip(r0, r1):
+        for k in ("n_valid", "n_clipped", "n_nonfinite", "n_tokens", "status", "kernel_flags"):
+            assert a[k] == b[k], k
+        assert abs(a["loss"] - b["loss"]) <= 1e-5 * max(abs(a["loss"]), 1e-6)
 
 
 @pytest.mark.parametrize("agg", [_lib.AGG_SEQ_MEAN_TOKEN_SUM, _lib.AGG_SEQ_MEAN_TOKEN_MEAN])

@@ -1,0 +1,59 @@
+"""Register and spill budget of the product kernels, from the ptxas report the build records
+(no GPU needed). The cluster row pass runs 17 warps per SM, so a thread has at most 96
+registers; a spill in one of the instances the dispatcher selects by default costs that
+instance a large share of its bandwidth, so none is allowed."""
+import os
+import re
+
+import pytest
+
+from rl_post_token_gb300 import build as B
+
+
+def _report(src):
+    path = B.ptxas_report(src)
+    if not os.path.exists(path):
+        pytest.skip("library not built here")
+    kernels = {}
+    name = None
+    for line in open(path):
+        m = re.search(r"Compiling entry function '(\S+)'", line)
+        if m:
+            name = m.group(1)
+            continue
+        m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
+        if m and name:
+            kernels.setdefault(name, {})["spill"] = int(m.group(1)) + int(m.group(2))
+        m = re.search(r"Used (\d+) registers", line)
+        if m and name:
+            kernels.setdefault(name, {})["regs"] = int(m.group(1))
+    return kernels
+
+
+def _cluster(C, NCW, VPT, MINB, ENT, TERMS):
+    return f"_ZN4grpo18row_cluster_kernelILi{C}ELi{NCW}ELi{VPT}ELi{MINB}ELb{ENT}ELi{TERMS}EEEvNS_7RowArgsEii"
+
+
+# (cluster, consumer warps, vectors per thread, CTAs per SM, entropy, terms) as dispatched for
+# bf16 vocabularies that fit the 2-CTA cluster
+DEFAULT_ROW_PASS = [(2, 16, 4, 1, 0, 0), (2, 16, 4, 1, 0, 1), (2, 16, 2, 1, 0, 2), (2, 16, 2, 1, 1, 1),
+                    (2, 16, 2, 1, 1, 2)]
+
+
+def test_row_pass_default_instances_do_not_spill(grpo_lib):
+    k = _report("grpo_rowpass.cu")
+    for inst in DEFAULT_ROW_PASS:
+        name = _cluster(*inst)
+        assert name in k, (inst, "not compiled")
+        assert k[name]["spill"] == 0, (inst, k[name])
+        assert k[name]["regs"] <= 96, (inst, k[name])
+
+
+def test_lmhead_and_step_kernels_do_not_spill(grpo_lib):
+    for src, pat in (("grpo_lmhead.cu", r"gemm_kernel|dz_from_e|reduce_kernel"),
+                     ("grpo_step.cu", r"finish_kernel|adv_")):
+        k = _report(src)
+        hits = [n for n in k if re.search(pat, n)]
+        assert hits, (src, "no kernel found")
+        for n in hits:
+            assert k[n]["spill"] == 0, (n, k[n])
