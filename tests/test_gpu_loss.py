@@ -367,6 +367,11 @@ def test_ring_slots_equal_fixed_buffer_bitwise(V, monkeypatch):
         dl, loss, logp, acc = _run_direct(case, 1.0 / 97, tok_src=tok_src, logits=lg)
         res = _lib.grpo_finish_step(acc, loss, expected_N=int(case.mask.sum()))
         outs[slots] = (dl.view(torch.int16).clone(), loss.clone(), logp.clone(), res)
+        # forward only (slots released as soon as pass 1 is done with them): same per-token bits
+        _, loss_f, logp_f, acc_f = _run_direct(case, 1.0 / 97, want_grad=False, tok_src=tok_src, logits=lg)
+        res_f = _lib.grpo_finish_step(acc_f, loss_f, expected_N=int(case.mask.sum()))
+        assert torch.equal(loss_f, loss) and torch.equal(logp_f, logp), slots
+        assert res_f == res, slots
     for k in ("6", None):
         assert torch.equal(outs[k][0], outs["0"][0]), k
         assert torch.equal(outs[k][1], outs["0"][1]) and torch.equal(outs[k][2], outs["0"][2]), k

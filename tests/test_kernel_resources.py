@@ -14,19 +14,26 @@ def _report(src):
     path = B.ptxas_report(src)
     if not os.path.exists(path):
         pytest.skip("library not built here")
+    # ptxas prints, per entry function, "Compiling entry function NAME", then "Function
+    # properties for F" blocks (for NAME and for any non-inlined callee F), each followed by
+    # its stack/spill line, then NAME's register count
     kernels = {}
-    name = None
+    entry = prop = None
     for line in open(path):
         m = re.search(r"Compiling entry function '(\S+)'", line)
         if m:
-            name = m.group(1)
+            entry = prop = m.group(1)
+            continue
+        m = re.search(r"Function properties for (\S+)", line)
+        if m:
+            prop = m.group(1)
             continue
         m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
-        if m and name:
-            kernels.setdefault(name, {})["spill"] = int(m.group(1)) + int(m.group(2))
+        if m and entry and prop == entry:
+            kernels.setdefault(entry, {})["spill"] = int(m.group(1)) + int(m.group(2))
         m = re.search(r"Used (\d+) registers", line)
-        if m and name:
-            kernels.setdefault(name, {})["regs"] = int(m.group(1))
+        if m and entry:
+            kernels.setdefault(entry, {})["regs"] = int(m.group(1))
     return kernels
 
 
