@@ -92,14 +92,35 @@ __device__ __forceinline__ float tree_max(const float (&x)[N]) {
   return t[0];
 }
 
-template <int N>
+// Fixed-shape pairwise sum (t[i] += t[i + w], w = N/2, ..., 1), in place. PK: the levels with
+// w >= 2 use packed two-lane adds (each lane adds the same two operands as the scalar tree, so
+// the result is the same bits); PK = false keeps every add scalar (fewer register pairs).
+template <int N, bool PK = true>
 __device__ __forceinline__ float tree_sum(float (&t)[N]) {
   static_assert((N & (N - 1)) == 0, "power of two");
+  if constexpr (PK) {
 #pragma unroll
-  for (int w = N / 2; w >= 1; w /= 2)
+    for (int w = N / 2; w >= 2; w /= 2)
 #pragma unroll
-    for (int i = 0; i < w; ++i) t[i] = t[i] + t[i + w];
+      for (int i = 0; i < w; i += 2) {
+        const float2 r = __fadd2_rn(make_float2(t[i], t[i + 1]), make_float2(t[i + w], t[i + w + 1]));
+        t[i] = r.x;
+        t[i + 1] = r.y;
+      }
+    if (N >= 2) t[0] = t[0] + t[1];
+  } else {
+#pragma unroll
+    for (int w = N / 2; w >= 1; w /= 2)
+#pragma unroll
+      for (int i = 0; i < w; ++i) t[i] = t[i] + t[i + w];
+  }
   return t[0];
+}
+
+// 2^(x log2 e - sh) for a pair, the argument by one packed fused multiply-add per pair.
+__device__ __forceinline__ float2 ex2_pair(float x0, float x1, float sh) {
+  const float2 t = __ffma2_rn(make_float2(x0, x1), make_float2(kLog2e, kLog2e), make_float2(-sh, -sh));
+  return make_float2(ex2(t.x), ex2(t.y));
 }
 
 // Fold N more values into a log2-domain online pair: one rescale per call, the N
@@ -121,15 +142,24 @@ __device__ __forceinline__ void online2(MS& acc, float (&x)[N]) {
 // is only computed when the block sum leaves the safe range (> 2^64, inf or NaN), which for
 // real logits happens about once per thread and row (the first block, shift -inf). Exact in
 // the same sense as online2: the sum carries its scale, and lse2 = m + log2(s) either way.
-template <int N>
+template <int N, bool PK = true>
 __device__ __forceinline__ void lazy_online2(MS& acc, float (&x)[N]) {
   // the first block takes its first value as the shift (the sum is still 0, so any shift is
   // exact); a block rising more than 2^64 above it falls back to the max-based update
   if (acc.m == -INFINITY) acc.m = x[0] * kLog2e;
   float e[N];
 #pragma unroll
-  for (int i = 0; i < N; ++i) e[i] = ex2(fmaf(x[i], kLog2e, -acc.m));
-  const float bs = tree_sum(e);
+  for (int i = 0; i < N; i += 2) {
+    if constexpr (PK) {
+      const float2 p = ex2_pair(x[i], x[i + 1], acc.m);
+      e[i] = p.x;
+      e[i + 1] = p.y;
+    } else {
+      e[i] = ex2(fmaf(x[i], kLog2e, -acc.m));
+      e[i + 1] = ex2(fmaf(x[i + 1], kLog2e, -acc.m));
+    }
+  }
+  const float bs = tree_sum<N, PK>(e);
   if (bs <= 1.8446744e19f) {  // false for inf and NaN
     acc.s += bs;
     return;

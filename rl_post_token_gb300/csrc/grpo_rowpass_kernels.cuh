@@ -370,13 +370,23 @@ __device__ __forceinline__ void unpack8_at(const uint4& a, float* x) {
   x[4] = bf16_lo(a.z); x[5] = bf16_hi(a.z); x[6] = bf16_lo(a.w); x[7] = bf16_hi(a.w);
 }
 
-// Eight dlogits of one 16-byte vector: (-1)^NEG * 2^(z log2e - cexp), rounded to bf16.
-template <bool NEG>
+// Eight dlogits of one 16-byte vector: (-1)^NEG * 2^(z log2e - cexp), rounded to bf16 (PK:
+// the exponent arguments by packed pairs).
+template <bool NEG, bool PK>
 __device__ __forceinline__ void dz_vec(const uint4& u, uint4* dst, float cexp) {
   float x[8];
   Vec<__nv_bfloat16>::unpack(u, x);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) x[i] = ex2(fmaf(x[i], kLog2e, -cexp));
+  for (int i = 0; i < 8; i += 2) {
+    if constexpr (PK) {
+      const float2 p = ex2_pair(x[i], x[i + 1], cexp);
+      x[i] = p.x;
+      x[i + 1] = p.y;
+    } else {
+      x[i] = ex2(fmaf(x[i], kLog2e, -cexp));
+      x[i + 1] = ex2(fmaf(x[i + 1], kLog2e, -cexp));
+    }
+  }
   uint4 r = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
                        pack_bf16x2(x[6], x[7]));
   if (NEG) {
@@ -449,7 +459,7 @@ __device__ __forceinline__ void pass2_slice_ent(const __nv_bfloat16* ring, RingC
 }
 
 // Pass 2 over the CTA's slice; each warp releases a chunk's slot once it is done with it.
-template <bool NEG, int NC, int VPT, int CH>
+template <bool NEG, int NC, int VPT, int CH, bool PK>
 __device__ __forceinline__ void pass2_slice(const __nv_bfloat16* ring, RingCursor c, int S, uint4* dz, int n_r,
                                             int nch, int ct, int lane, float cexp, uint64_t* empty) {
   for (int k = 0; k < nch; ++k) {
@@ -458,9 +468,9 @@ __device__ __forceinline__ void pass2_slice(const __nv_bfloat16* ring, RingCurso
     uint4* dv = dz + k * (CH / 8);
     if (nv == VPT * NC) {
 #pragma unroll
-      for (int j = 0; j < VPT; ++j) dz_vec<NEG>(sv[ct + j * NC], dv + ct + j * NC, cexp);
+      for (int j = 0; j < VPT; ++j) dz_vec<NEG, PK>(sv[ct + j * NC], dv + ct + j * NC, cexp);
     } else {
-      for (int v = ct; v < nv; v += NC) dz_vec<NEG>(sv[v], dv + v, cexp);
+      for (int v = ct; v < nv; v += NC) dz_vec<NEG, PK>(sv[v], dv + v, cexp);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[c.slot]);
@@ -488,6 +498,9 @@ template <int C, int NCW, int VPT, int MINB, bool ENT, int TERMS>
 __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowArgs a, int Vs, int S) {
   constexpr int NC = NCW * 32;
   constexpr int WS = ENT ? 3 : 2;  // floats per warp partial
+  // packed two-lane arithmetic, except in the KL instance, whose 32 KB chunks leave no
+  // registers for the aligned pairs it needs
+  constexpr bool PK = !(TERMS == 1 && !ENT);
   constexpr int CH = cluster_chunk_elems(NCW, VPT);
   extern __shared__ __align__(128) uint8_t smem[];
   const int ring_bytes = (int)cluster_ring_bytes(Vs, CH, S);
@@ -604,7 +617,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
           if (ENT)
             lazy_online3<VPT * 8>(acc3, x, guarded);
           else
-            lazy_online2<VPT * 8>(acc, x);
+            lazy_online2<VPT * 8, PK>(acc, x);
         } else {
           for (int v = ct; v < nv; v += NC) {
             float x[8];
@@ -612,7 +625,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
             if (ENT)
               lazy_online3<8>(acc3, x, guarded);
             else
-              lazy_online2<8>(acc, x);
+              lazy_online2<8, PK>(acc, x);
           }
         }
         c.step(SL);
@@ -704,9 +717,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
         // the packed bf16 pairs; the target element coef * (p_y - 1) is written on its own
         const float cexp = lse2 - log2f(fabsf(coef));
         if (coef < 0.f)
-          pass2_slice<true, NC, VPT, CH>(ring, rc, SL, dz, n_r, nch, ct, lane, cexp, empty);
+          pass2_slice<true, NC, VPT, CH, PK>(ring, rc, SL, dz, n_r, nch, ct, lane, cexp, empty);
         else
-          pass2_slice<false, NC, VPT, CH>(ring, rc, SL, dz, n_r, nch, ct, lane, cexp, empty);
+          pass2_slice<false, NC, VPT, CH, PK>(ring, rc, SL, dz, n_r, nch, ct, lane, cexp, empty);
         // the target element overwrites what the vector pass wrote (same thread, program order)
         const int64_t yl = ybad ? -1 : (int64_t)y - base;
         if (yl >= 0 && yl < n_r && ct == (int)(((yl / 8) % (CH / 8)) % NC)) {
