@@ -218,9 +218,9 @@ template <int N>
 __device__ __forceinline__ void e_pairs_fast(const float (&x)[N], float sh, float (&pe)[N / 2], float (&px)[N / 2]) {
 #pragma unroll
   for (int i = 0; i < N / 2; ++i) {
-    const float e0 = ex2(fmaf(x[2 * i], kLog2e, -sh)), e1 = ex2(fmaf(x[2 * i + 1], kLog2e, -sh));
-    pe[i] = e0 + e1;
-    px[i] = fmaf(e1, x[2 * i + 1], e0 * x[2 * i]);
+    const float2 e = ex2_pair(x[2 * i], x[2 * i + 1], sh);
+    pe[i] = e.x + e.y;
+    px[i] = fmaf(e.y, x[2 * i + 1], e.x * x[2 * i]);
   }
 }
 

@@ -406,9 +406,16 @@ __device__ __forceinline__ void dz_vec_ent(const uint4& u, uint4* dst, float lse
   float x[8];
   Vec<__nv_bfloat16>::unpack(u, x);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float p = ex2(fmaf(x[i], kLog2e, -lse2));
-    x[i] = GUARD ? ent_dz(p, x[i], ea, eb) : p * fmaf(eb, x[i], ea);
+  for (int i = 0; i < 8; i += 2) {
+    const float2 p = ex2_pair(x[i], x[i + 1], lse2);
+    if constexpr (GUARD) {
+      x[i] = ent_dz(p.x, x[i], ea, eb);
+      x[i + 1] = ent_dz(p.y, x[i + 1], ea, eb);
+    } else {
+      const float2 q = __fmul2_rn(p, __ffma2_rn(make_float2(x[i], x[i + 1]), make_float2(eb, eb), make_float2(ea, ea)));
+      x[i] = q.x;
+      x[i + 1] = q.y;
+    }
   }
   __stcs(dst, make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
                          pack_bf16x2(x[6], x[7])));
