@@ -467,7 +467,11 @@ def run_gb300(args):
     value = all_units / max_el
 
     ahead = run_ahead(batch, stream, steps=min(args.steps, 30))
+    barrier(world, device)
     e2e = run_e2e(batch, device, stream, steps=min(args.steps, args.e2e_steps))
+    # whole job: every rank's tokens over the slowest rank's time, as for `value`
+    e2e_el, e2e_units = reduce_timing(e2e.pop("elapsed_s"), e2e.pop("units"), world, device)
+    e2e["value"] = e2e_units / e2e_el
 
     peak, peak_kind = hbm_peak()
     tpv = profiled_traffic()
@@ -490,7 +494,7 @@ def run_gb300(args):
                      "traffic": None if tpv is None else tpv * wl.n_valid / launches_per_step},
         "gpu_launches": launches,
         "e2e": e2e,
-        "ahead_pass": dict(ahead, frac=ahead["achieved_gbs"] / hbm_peak()[0]),
+        "ahead_pass": dict(ahead, frac=ahead["achieved_gbs"] / hbm_peak()[0], per_gpu=True),
         "step_results": [{k: r[k] for k in ("loss", "n_valid", "clipfrac", "status")} for r in results],
     }
     if clk is not None:
@@ -579,7 +583,8 @@ def run_e2e(batch, device, stream, steps: int):
         one_step()
     dt = time.perf_counter() - t0
     h2d = host_logits.numel() * host_logits.element_size() + sum(v.numel() * v.element_size() for v in side.values())
-    return {"value": batch.wl.n_valid * steps / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+    return {"value": batch.wl.n_valid * steps / dt, "elapsed_s": dt, "units": batch.wl.n_valid * steps,
+            "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(host_res.numel()), "steps": steps,
             "how": "pinned host logits copied per chunk on a side stream, overlapped with the row pass; "
                    "side inputs copied and step results read back every step"}
