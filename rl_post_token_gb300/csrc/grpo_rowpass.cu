@@ -13,10 +13,10 @@ namespace grpo {
 
 size_t max_smem_optin();
 
-template <int C, int NCW, int VPT, int MINB, bool ENT, int TERMS>
+template <typename T, int C, int NCW, int VPT, int MINB, bool ENT, int TERMS>
 int launch_cluster(const RowArgs& a, cudaStream_t st) {
-  constexpr int CH = cluster_chunk_elems(NCW, VPT);
-  const int Vs = cluster_slice_elems(a.V, C);
+  constexpr int CH = cluster_chunk_elems<T>(NCW, VPT);
+  const int Vs = cluster_slice_elems<T>(a.V, C);
   const int nchm = (Vs + CH - 1) / CH;
   if (nchm > kMaxChunks) return GRPO_ERR_UNSUPPORTED;
   // Ring slots: a CTA alone on its SM takes as many chunk slots as the opt-in shared memory
@@ -25,7 +25,7 @@ int launch_cluster(const RowArgs& a, cudaStream_t st) {
   int s_fit = 0;
   const size_t optin = max_smem_optin();
   if (MINB == 1 && optin > cluster_tail_bytes(NCW)) {
-    s_fit = (int)std::min<size_t>(kMaxChunks, (optin - cluster_tail_bytes(NCW)) / ((size_t)CH * 2));
+    s_fit = (int)std::min<size_t>(kMaxChunks, (optin - cluster_tail_bytes(NCW)) / ((size_t)CH * sizeof(T)));
     if (s_fit > nchm) S = s_fit;
   }
   if (const char* ov = getenv("GRPO_ROWPASS_SLOTS")) {  // 0: fixed buffer; n: n slots if they fit
@@ -33,8 +33,8 @@ int launch_cluster(const RowArgs& a, cudaStream_t st) {
     if (n == 0) S = nchm;
     else if (n > nchm && n <= s_fit) S = n;
   }
-  const size_t smem = cluster_ring_bytes(Vs, CH, S) + cluster_tail_bytes(NCW);
-  auto kern = row_cluster_kernel<C, NCW, VPT, MINB, ENT, TERMS>;
+  const size_t smem = cluster_ring_bytes<T>(Vs, CH, S) + cluster_tail_bytes(NCW);
+  auto kern = row_cluster_kernel<T, C, NCW, VPT, MINB, ENT, TERMS>;
   int dev = 0;
   GRPO_CUDA_TRY(cudaGetDevice(&dev));
   cudaLaunchConfig_t cfg = {};
@@ -122,45 +122,56 @@ using namespace grpo;
 
 namespace {
 
+// Whether the cluster kernel fits: the fixed staging buffer of `minb` CTAs in the shared memory
+// of one SM, and the slice in at most kMaxChunks chunks.
+template <typename T>
+bool cluster_fits(int64_t V, int C, int NCW, int minb, int vpt) {
+  const int64_t cap = 227 * 1024;
+  const int Vs = cluster_slice_elems<T>(V, C);
+  return (int64_t)cluster_smem_bytes<T>(Vs, NCW) * minb <= cap &&
+         (Vs + cluster_chunk_elems<T>(NCW, vpt) - 1) / cluster_chunk_elems<T>(NCW, vpt) <= kMaxChunks;
+}
+
 template <bool ENT, int TERMS>
 int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
   const int64_t V = a.V;
+  const char* pin = getenv("GRPO_ROWPASS");
+  const bool pin_l2 = pin && strcmp(pin, "l2") == 0;
+  // the entropy and per-token-weight instances carry more per-thread state: half-size chunks
+  // keep them in registers where the chunk count allows
+  constexpr bool HALF = ENT || TERMS == 2;
   if (dtype == GRPO_DTYPE_BF16) {
     // Large bf16 vocabularies: rows split across a CTA cluster, slices staged in shared
     // memory. Variants (cluster size, consumer warps, vectors per thread, CTAs per SM):
     // c2 = (2, 16, 4, 1) with a ring of spare slots, c3 = (3, 8, 4, 2), c4 = (4, 8, 4, 2)
-    // with fixed staging buffers; the entropy and per-token-weight instances take 2 vectors
-    // per thread.
-    const char* pin = getenv("GRPO_ROWPASS");
-    const bool cluster_ok = vec && V % 8 == 0 && V >= 16384;
-    if (cluster_ok && !(pin && strcmp(pin, "l2") == 0)) {
-      const int64_t cap = 227 * 1024;
-      auto fits = [&](int C, int NCW, int minb, int vpt) {
-        return (int64_t)cluster_smem_bytes(cluster_slice_elems(V, C), NCW) * minb <= cap &&
-               (cluster_slice_elems(V, C) + cluster_chunk_elems(NCW, vpt) - 1) / cluster_chunk_elems(NCW, vpt) <=
-                   kMaxChunks;
-      };
-      // the entropy and per-token-weight instances carry more per-thread state: half-size
-      // chunks keep them in registers where the chunk count allows
+    // with fixed staging buffers.
+    using B16 = __nv_bfloat16;
+    if (vec && V % 8 == 0 && V >= 16384 && !pin_l2) {
       auto c34 = [&](auto c_tag) {
         constexpr int C = decltype(c_tag)::value;
-        if constexpr (ENT || TERMS == 2)
-          if (fits(C, 8, 2, 2)) return launch_cluster<C, 8, 2, 2, ENT, TERMS>(a, st);
-        return launch_cluster<C, 8, 4, 2, ENT, TERMS>(a, st);
+        if constexpr (HALF)
+          if (cluster_fits<B16>(V, C, 8, 2, 2)) return launch_cluster<B16, C, 8, 2, 2, ENT, TERMS>(a, st);
+        return launch_cluster<B16, C, 8, 4, 2, ENT, TERMS>(a, st);
       };
       using C3 = std::integral_constant<int, 3>;
       using C4 = std::integral_constant<int, 4>;
-      if (pin && strcmp(pin, "c3") == 0 && fits(3, 8, 2, 4)) return c34(C3{});
-      if (pin && strcmp(pin, "c4") == 0 && fits(4, 8, 2, 4)) return c34(C4{});
-      if (fits(2, 16, 1, 4)) {
-        if constexpr (ENT || TERMS == 2) return launch_cluster<2, 16, 2, 1, ENT, TERMS>(a, st);
-        else return launch_cluster<2, 16, 4, 1, ENT, TERMS>(a, st);
+      if (pin && strcmp(pin, "c3") == 0 && cluster_fits<B16>(V, 3, 8, 2, 4)) return c34(C3{});
+      if (pin && strcmp(pin, "c4") == 0 && cluster_fits<B16>(V, 4, 8, 2, 4)) return c34(C4{});
+      if (cluster_fits<B16>(V, 2, 16, 1, 4)) {
+        if constexpr (HALF) return launch_cluster<B16, 2, 16, 2, 1, ENT, TERMS>(a, st);
+        else return launch_cluster<B16, 2, 16, 4, 1, ENT, TERMS>(a, st);
       }
-      if (fits(4, 8, 2, 4)) return c34(C4{});
-      if (fits(4, 16, 1, 4)) return launch_cluster<4, 16, 4, 1, ENT, TERMS>(a, st);
+      if (cluster_fits<B16>(V, 4, 8, 2, 4)) return c34(C4{});
+      if (cluster_fits<B16>(V, 4, 16, 1, 4)) return launch_cluster<B16, 4, 16, 4, 1, ENT, TERMS>(a, st);
     }
-    if (V >= 8192) return launch_l2<__nv_bfloat16, 1024, 2, ENT, TERMS>(a, vec, 1, st);
-    return launch_l2<__nv_bfloat16, 128, 2, ENT, TERMS>(a, vec, 16, st);
+    if (V >= 8192) return launch_l2<B16, 1024, 2, ENT, TERMS>(a, vec, 1, st);
+    return launch_l2<B16, 128, 2, ENT, TERMS>(a, vec, 16, st);
+  }
+  // float32 vocabularies: a row is twice the bytes, so a 4-CTA cluster, one CTA per SM with
+  // the ring of spare slots, holds the same slice size as the bf16 2-CTA cluster
+  if (vec && V % 4 == 0 && V >= 16384 && !pin_l2 && cluster_fits<float>(V, 4, 16, 1, 4)) {
+    if constexpr (HALF) return launch_cluster<float, 4, 16, 2, 1, ENT, TERMS>(a, st);
+    else return launch_cluster<float, 4, 16, 4, 1, ENT, TERMS>(a, st);
   }
   if (V >= 8192) return launch_l2<float, 1024, 2, ENT, TERMS>(a, vec, 1, st);
   return launch_l2<float, 128, 2, ENT, TERMS>(a, vec, 16, st);

@@ -340,11 +340,18 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
 // ------------------------------------------------------------------------------------------
 constexpr int kMaxChunks = 16;
 
-// Elements per bulk-copied chunk: every consumer thread owns VPT 16-byte vectors of it.
-__host__ __device__ constexpr int cluster_chunk_elems(int NCW, int VPT) { return VPT * NCW * 32 * 8; }
+// Elements of T per 16-byte vector.
+template <typename T>
+__host__ __device__ constexpr int vec_elems() { return 16 / (int)sizeof(T); }
 
+// Elements per bulk-copied chunk: every consumer thread owns VPT 16-byte vectors of it.
+template <typename T>
+__host__ __device__ constexpr int cluster_chunk_elems(int NCW, int VPT) { return VPT * NCW * 32 * vec_elems<T>(); }
+
+// A CTA's share of a row, rounded up to whole 16-byte vectors.
+template <typename T>
 __host__ __device__ constexpr int cluster_slice_elems(int64_t V, int C) {
-  return (int)((((V + C - 1) / C) + 7) / 8 * 8);
+  return (int)((((V + C - 1) / C) + vec_elems<T>() - 1) / vec_elems<T>() * vec_elems<T>());
 }
 
 __host__ __device__ constexpr size_t cluster_tail_bytes(int NCW) {
@@ -352,8 +359,9 @@ __host__ __device__ constexpr size_t cluster_tail_bytes(int NCW) {
 }
 
 // Shared memory of the fixed staging buffer (the smallest ring) plus barriers and exchange.
+template <typename T>
 __host__ __device__ constexpr size_t cluster_smem_bytes(int Vs, int NCW) {
-  return ((size_t)Vs * 2 + 127) / 128 * 128 + cluster_tail_bytes(NCW);
+  return ((size_t)Vs * sizeof(T) + 127) / 128 * 128 + cluster_tail_bytes(NCW);
 }
 
 // Bounded wait used only when draining after a timeout (ignores the abort flag).
@@ -365,19 +373,48 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ void unpack8_at(const uint4& a, float* x) {
-  x[0] = bf16_lo(a.x); x[1] = bf16_hi(a.x); x[2] = bf16_lo(a.y); x[3] = bf16_hi(a.y);
-  x[4] = bf16_lo(a.z); x[5] = bf16_hi(a.z); x[6] = bf16_lo(a.w); x[7] = bf16_hi(a.w);
+// The elements of one 16-byte vector as floats, written to x[0 .. vec_elems<T>()).
+template <typename T>
+__device__ __forceinline__ void unpack_at(const uint4& a, float* x) {
+  if constexpr (sizeof(T) == 2) {
+    x[0] = bf16_lo(a.x); x[1] = bf16_hi(a.x); x[2] = bf16_lo(a.y); x[3] = bf16_hi(a.y);
+    x[4] = bf16_lo(a.z); x[5] = bf16_hi(a.z); x[6] = bf16_lo(a.w); x[7] = bf16_hi(a.w);
+  } else {
+    x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y); x[2] = __uint_as_float(a.z);
+    x[3] = __uint_as_float(a.w);
+  }
 }
 
-// Eight dlogits of one 16-byte vector: (-1)^NEG * 2^(z log2e - cexp), rounded to bf16 (PK:
-// the exponent arguments by packed pairs).
-template <bool NEG, bool PK>
+// One 16-byte vector of T from floats (round to nearest), the sign of every element flipped
+// when NEG.
+template <typename T, bool NEG>
+__device__ __forceinline__ uint4 pack_vec(const float* x) {
+  if constexpr (sizeof(T) == 2) {
+    uint4 r = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                         pack_bf16x2(x[6], x[7]));
+    if (NEG) {
+      r.x ^= 0x80008000u;
+      r.y ^= 0x80008000u;
+      r.z ^= 0x80008000u;
+      r.w ^= 0x80008000u;
+    }
+    return r;
+  } else {
+    const uint32_t sg = NEG ? 0x80000000u : 0u;
+    return make_uint4(__float_as_uint(x[0]) ^ sg, __float_as_uint(x[1]) ^ sg, __float_as_uint(x[2]) ^ sg,
+                      __float_as_uint(x[3]) ^ sg);
+  }
+}
+
+// The dlogits of one 16-byte vector: (-1)^NEG * 2^(z log2e - cexp), rounded to T (PK: the
+// exponent arguments by packed pairs).
+template <typename T, bool NEG, bool PK>
 __device__ __forceinline__ void dz_vec(const uint4& u, uint4* dst, float cexp) {
-  float x[8];
-  Vec<__nv_bfloat16>::unpack(u, x);
+  constexpr int E = vec_elems<T>();
+  float x[E];
+  unpack_at<T>(u, x);
 #pragma unroll
-  for (int i = 0; i < 8; i += 2) {
+  for (int i = 0; i < E; i += 2) {
     if constexpr (PK) {
       const float2 p = ex2_pair(x[i], x[i + 1], cexp);
       x[i] = p.x;
@@ -387,26 +424,19 @@ __device__ __forceinline__ void dz_vec(const uint4& u, uint4* dst, float cexp) {
       x[i + 1] = ex2(fmaf(x[i + 1], kLog2e, -cexp));
     }
   }
-  uint4 r = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                       pack_bf16x2(x[6], x[7]));
-  if (NEG) {
-    r.x ^= 0x80008000u;
-    r.y ^= 0x80008000u;
-    r.z ^= 0x80008000u;
-    r.w ^= 0x80008000u;
-  }
-  __stcs(dst, r);
+  __stcs(dst, pack_vec<T, NEG>(x));
 }
 
-// Eight dlogits with the entropy term: 2^(z log2e - lse2) * (ea + eb z), rounded to bf16.
-// GUARD: an element without mass (a -inf logit) gives 0 instead of 0 * inf; needed only where
-// pass 1 met such an element.
-template <bool GUARD>
+// The dlogits of one vector with the entropy term: 2^(z log2e - lse2) * (ea + eb z), rounded
+// to T. GUARD: an element without mass (a -inf logit) gives 0 instead of 0 * inf; needed only
+// where pass 1 met such an element.
+template <typename T, bool GUARD>
 __device__ __forceinline__ void dz_vec_ent(const uint4& u, uint4* dst, float lse2, float ea, float eb) {
-  float x[8];
-  Vec<__nv_bfloat16>::unpack(u, x);
+  constexpr int E = vec_elems<T>();
+  float x[E];
+  unpack_at<T>(u, x);
 #pragma unroll
-  for (int i = 0; i < 8; i += 2) {
+  for (int i = 0; i < E; i += 2) {
     const float2 p = ex2_pair(x[i], x[i + 1], lse2);
     if constexpr (GUARD) {
       x[i] = ent_dz(p.x, x[i], ea, eb);
@@ -417,8 +447,7 @@ __device__ __forceinline__ void dz_vec_ent(const uint4& u, uint4* dst, float lse
       x[i + 1] = q.y;
     }
   }
-  __stcs(dst, make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                         pack_bf16x2(x[6], x[7])));
+  __stcs(dst, pack_vec<T, false>(x));
 }
 
 // The shared-memory ring: S slots of one chunk each. A CTA's chunks, in row order, take slots
@@ -445,19 +474,20 @@ struct RingCursor {
 };
 
 // Pass 2 with the entropy term over the CTA's slice, chunk k read from its ring slot.
-template <bool GUARD, int NC, int VPT, int CH>
-__device__ __forceinline__ void pass2_slice_ent(const __nv_bfloat16* ring, RingCursor c, int S, uint4* dz, int n_r,
+template <typename T, bool GUARD, int NC, int VPT, int CH>
+__device__ __forceinline__ void pass2_slice_ent(const T* ring, RingCursor c, int S, uint4* dz, int n_r,
                                                 int nch, int ct, int lane, float lse2, float ea, float eb,
                                                 uint64_t* empty) {
   for (int k = 0; k < nch; ++k) {
-    const int nv = min(CH, n_r - k * CH) / 8;
+    constexpr int E = vec_elems<T>();
+    const int nv = min(CH, n_r - k * CH) / E;
     const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)c.slot * CH);
-    uint4* dv = dz + k * (CH / 8);
+    uint4* dv = dz + k * (CH / E);
     if (nv == VPT * NC) {
 #pragma unroll
-      for (int j = 0; j < VPT; ++j) dz_vec_ent<GUARD>(sv[ct + j * NC], dv + ct + j * NC, lse2, ea, eb);
+      for (int j = 0; j < VPT; ++j) dz_vec_ent<T, GUARD>(sv[ct + j * NC], dv + ct + j * NC, lse2, ea, eb);
     } else {
-      for (int v = ct; v < nv; v += NC) dz_vec_ent<GUARD>(sv[v], dv + v, lse2, ea, eb);
+      for (int v = ct; v < nv; v += NC) dz_vec_ent<T, GUARD>(sv[v], dv + v, lse2, ea, eb);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[c.slot]);
@@ -466,18 +496,19 @@ __device__ __forceinline__ void pass2_slice_ent(const __nv_bfloat16* ring, RingC
 }
 
 // Pass 2 over the CTA's slice; each warp releases a chunk's slot once it is done with it.
-template <bool NEG, int NC, int VPT, int CH, bool PK>
-__device__ __forceinline__ void pass2_slice(const __nv_bfloat16* ring, RingCursor c, int S, uint4* dz, int n_r,
+template <typename T, bool NEG, int NC, int VPT, int CH, bool PK>
+__device__ __forceinline__ void pass2_slice(const T* ring, RingCursor c, int S, uint4* dz, int n_r,
                                             int nch, int ct, int lane, float cexp, uint64_t* empty) {
   for (int k = 0; k < nch; ++k) {
-    const int nv = min(CH, n_r - k * CH) / 8;
+    constexpr int E = vec_elems<T>();
+    const int nv = min(CH, n_r - k * CH) / E;
     const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)c.slot * CH);
-    uint4* dv = dz + k * (CH / 8);
+    uint4* dv = dz + k * (CH / E);
     if (nv == VPT * NC) {
 #pragma unroll
-      for (int j = 0; j < VPT; ++j) dz_vec<NEG, PK>(sv[ct + j * NC], dv + ct + j * NC, cexp);
+      for (int j = 0; j < VPT; ++j) dz_vec<T, NEG, PK>(sv[ct + j * NC], dv + ct + j * NC, cexp);
     } else {
-      for (int v = ct; v < nv; v += NC) dz_vec<NEG, PK>(sv[v], dv + v, cexp);
+      for (int v = ct; v < nv; v += NC) dz_vec<T, NEG, PK>(sv[v], dv + v, cexp);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[c.slot]);
@@ -494,24 +525,26 @@ __device__ __forceinline__ int64_t next_read_row(const RowArgs& a, int64_t row, 
   return a.T;
 }
 
-// Bytes of the ring for a slice of Vs elements and S slots of CH elements (S no larger than
-// the slice's chunk count: the fixed staging buffer, whose last slot is only as long as the
-// slice's last chunk).
+// Bytes of the ring for a slice of Vs elements of T and S slots of CH elements (S no larger
+// than the slice's chunk count: the fixed staging buffer, whose last slot is only as long as
+// the slice's last chunk).
+template <typename T>
 __host__ __device__ constexpr size_t cluster_ring_bytes(int Vs, int CH, int S) {
-  return S > (Vs + CH - 1) / CH ? (size_t)S * CH * 2 : ((size_t)Vs * 2 + 127) / 128 * 128;
+  return S > (Vs + CH - 1) / CH ? (size_t)S * CH * sizeof(T) : ((size_t)Vs * sizeof(T) + 127) / 128 * 128;
 }
 
-template <int C, int NCW, int VPT, int MINB, bool ENT, int TERMS>
+template <typename T, int C, int NCW, int VPT, int MINB, bool ENT, int TERMS>
 __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowArgs a, int Vs, int S) {
   constexpr int NC = NCW * 32;
+  constexpr int E = vec_elems<T>();  // elements per 16-byte vector
   constexpr int WS = ENT ? 3 : 2;  // floats per warp partial
   // packed two-lane arithmetic, except in the KL instance, whose 32 KB chunks leave no
   // registers for the aligned pairs it needs
   constexpr bool PK = !(TERMS == 1 && !ENT);
-  constexpr int CH = cluster_chunk_elems(NCW, VPT);
+  constexpr int CH = cluster_chunk_elems<T>(NCW, VPT);
   extern __shared__ __align__(128) uint8_t smem[];
-  const int ring_bytes = (int)cluster_ring_bytes(Vs, CH, S);
-  __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
+  const int ring_bytes = (int)cluster_ring_bytes<T>(Vs, CH, S);
+  T* ring = reinterpret_cast<T*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + ring_bytes);
   uint64_t* empty = full + kMaxChunks;
   float* xch = reinterpret_cast<float*>(empty + kMaxChunks);  // [2 rows][m, s, z_y, s2]
@@ -540,8 +573,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
   __syncthreads();
   cluster_sync_all();
 
-  const __nv_bfloat16* lg = static_cast<const __nv_bfloat16*>(a.logits);
-  __nv_bfloat16* dg = static_cast<__nv_bfloat16*>(a.dlogits);
+  const T* lg = static_cast<const T*>(a.logits);
+  T* dg = static_cast<T*>(a.dlogits);
   const uint4 zero = make_uint4(0, 0, 0, 0);
   Counts cnt;
   uint32_t issued = 0;  // producer: chunks issued so far (slot reuse starts at SL)
@@ -557,8 +590,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
         return;
       }
       const int n_k = min(CH, n_r - k * CH);
-      mbar_arrive_expect_tx(&full[pc.slot], (uint32_t)n_k * 2u);
-      bulk_g2s(ring + (size_t)pc.slot * CH, lg + row * a.ld + base + (int64_t)k * CH, (uint32_t)n_k * 2u,
+      mbar_arrive_expect_tx(&full[pc.slot], (uint32_t)n_k * (uint32_t)sizeof(T));
+      bulk_g2s(ring + (size_t)pc.slot * CH, lg + row * a.ld + base + (int64_t)k * CH, (uint32_t)n_k * (uint32_t)sizeof(T),
                &full[pc.slot]);
       ++issued;
       pc.step(SL);
@@ -593,7 +626,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
       if (!tm.valid) {
         // masked or padding row: nothing read, nothing exchanged; zero dlogits slice
         if (dz)
-          for (int v = ct; v < n_r / 8; v += NC) __stcs(dz + v, zero);
+          for (int v = ct; v < n_r / E; v += NC) __stcs(dz + v, zero);
         if (rank == 0 && ct == 0) {
           cnt.tokens++;
           if (tm.idx >= 0) {
@@ -615,24 +648,24 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
       RingCursor c = rc;
       for (int k = 0; k < nch; ++k) {
         mbar_wait_bounded(&full[c.slot], c.ph, s_abort);
-        const int nv = min(CH, n_r - k * CH) / 8;
+        const int nv = min(CH, n_r - k * CH) / E;
         const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)c.slot * CH);
         if (nv == VPT * NC) {  // full chunk: exactly VPT 16-byte vectors per consumer thread
-          float x[VPT * 8];
+          float x[VPT * E];
 #pragma unroll
-          for (int j = 0; j < VPT; ++j) unpack8_at(sv[ct + j * NC], x + 8 * j);
+          for (int j = 0; j < VPT; ++j) unpack_at<T>(sv[ct + j * NC], x + E * j);
           if (ENT)
-            lazy_online3<VPT * 8>(acc3, x, guarded);
+            lazy_online3<VPT * E>(acc3, x, guarded);
           else
-            lazy_online2<VPT * 8, PK>(acc, x);
+            lazy_online2<VPT * E, PK>(acc, x);
         } else {
           for (int v = ct; v < nv; v += NC) {
-            float x[8];
-            Vec<__nv_bfloat16>::unpack(sv[v], x);
+            float x[E];
+            unpack_at<T>(sv[v], x);
             if (ENT)
-              lazy_online3<8>(acc3, x, guarded);
+              lazy_online3<E>(acc3, x, guarded);
             else
-              lazy_online2<8, PK>(acc, x);
+              lazy_online2<E, PK>(acc, x);
           }
         }
         c.step(SL);
@@ -668,7 +701,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
           const int off = (int)((int64_t)y - base), k = off / CH;
           RingCursor cy = rc;
           cy.skip(k, SL);
-          xb[2] = __bfloat162float(ring[(size_t)cy.slot * CH + (off - k * CH)]);
+          xb[2] = Vec<T>::load1(ring + (size_t)cy.slot * CH + (off - k * CH));
         }
       }
       cluster_sync_all();
@@ -711,31 +744,31 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
         // pass 2 visits this thread's pass-1 elements; the warp takes the guarded form if any
         // of its threads met a -inf logit
         if (__any_sync(0xffffffffu, guarded))
-          pass2_slice_ent<true, NC, VPT, CH>(ring, rc, SL, dz, n_r, nch, ct, lane, lse2, ea, eb, empty);
+          pass2_slice_ent<T, true, NC, VPT, CH>(ring, rc, SL, dz, n_r, nch, ct, lane, lse2, ea, eb, empty);
         else
-          pass2_slice_ent<false, NC, VPT, CH>(ring, rc, SL, dz, n_r, nch, ct, lane, lse2, ea, eb, empty);
+          pass2_slice_ent<T, false, NC, VPT, CH>(ring, rc, SL, dz, n_r, nch, ct, lane, lse2, ea, eb, empty);
         const int64_t yl = ybad ? -1 : (int64_t)y - base;
-        if (yl >= 0 && yl < n_r && ct == (int)(((yl / 8) % (CH / 8)) % NC)) {
+        if (yl >= 0 && yl < n_r && ct == (int)(((yl / E) % (CH / E)) % NC)) {
           const float dzy = ent_dz(ex2(fmaf(zy, kLog2e, -lse2)), zy, ea, eb) - coef;
-          reinterpret_cast<__nv_bfloat16*>(dz)[yl] = __float2bfloat16_rn(dzy);
+          Vec<T>::store1(reinterpret_cast<T*>(dz) + yl, dzy);
         }
       } else if (dz && coef != 0.f) {
         // pass 2: |coef| * softmax = 2^(z log2e - (lse2 - log2|coef|)), the sign applied to
         // the packed bf16 pairs; the target element coef * (p_y - 1) is written on its own
         const float cexp = lse2 - log2f(fabsf(coef));
         if (coef < 0.f)
-          pass2_slice<true, NC, VPT, CH, PK>(ring, rc, SL, dz, n_r, nch, ct, lane, cexp, empty);
+          pass2_slice<T, true, NC, VPT, CH, PK>(ring, rc, SL, dz, n_r, nch, ct, lane, cexp, empty);
         else
-          pass2_slice<false, NC, VPT, CH, PK>(ring, rc, SL, dz, n_r, nch, ct, lane, cexp, empty);
+          pass2_slice<T, false, NC, VPT, CH, PK>(ring, rc, SL, dz, n_r, nch, ct, lane, cexp, empty);
         // the target element overwrites what the vector pass wrote (same thread, program order)
         const int64_t yl = ybad ? -1 : (int64_t)y - base;
-        if (yl >= 0 && yl < n_r && ct == (int)(((yl / 8) % (CH / 8)) % NC)) {
+        if (yl >= 0 && yl < n_r && ct == (int)(((yl / E) % (CH / E)) % NC)) {
           const float dzy = coef * ex2(fmaf(zy, kLog2e, -lse2)) - coef;
-          reinterpret_cast<__nv_bfloat16*>(dz)[yl] = __float2bfloat16_rn(dzy);
+          Vec<T>::store1(reinterpret_cast<T*>(dz) + yl, dzy);
         }
       } else {
         if (dz)
-          for (int v = ct; v < n_r / 8; v += NC) __stcs(dz + v, zero);
+          for (int v = ct; v < n_r / E; v += NC) __stcs(dz + v, zero);
         __syncwarp();
         if (lane == 0) {
           RingCursor ce = rc;

@@ -379,6 +379,65 @@ def test_ring_slots_equal_fixed_buffer_bitwise(V, monkeypatch):
     assert outs[None][3]["status"] == 0
 
 
+@pytest.mark.parametrize("V", [16384, 32776, 151936])
+def test_f32_cluster_rows_against_oracle(V, monkeypatch):
+    # float32 logits through the 4-CTA cluster kernel: masked and padding rows, the four
+    # slices of unequal length at V = 32776, forward-only bits equal to the full pass, and the
+    # fixed staging buffer giving the same bits as the ring
+    wl = W.make_workload("tiny", rows=8, positions=10, valid_lo=0, V=V, dtype="f32", seed=V % 211, std=2.0)
+    case = H.Case(wl)
+    T = case.logits.shape[0]
+    rng = np.random.default_rng(4)
+    perm = rng.permutation(T)
+    pads = rng.choice(T, 4)
+    src = np.concatenate([perm, -1 - pads]).astype(np.int64)
+    tok_src = torch.from_numpy(src).to(DEV)
+    lg = case.logits[torch.from_numpy(np.where(src >= 0, src, -1 - src)).to(DEV)]
+    dl, loss, logp, acc = _run_direct(case, 1.0 / 53, tok_src=tok_src, logits=lg)
+    ref = H.oracle_run(case, scale_per_token=np.full(T, 1.0 / 53))
+    H.assert_tokens_close(H.to_f64(loss), H.to_f64(logp), ref, case.adv_tok, case.mask)
+    got = H.to_f64(dl)
+    H.assert_dlogits_close(got[:T], ref["dlogits"][perm], "f32", target=ref["target"][perm],
+                           coef=ref["coef"][perm])
+    assert np.all(got[T:] == 0)
+    _, loss_f, logp_f, _ = _run_direct(case, 1.0 / 53, want_grad=False, tok_src=tok_src, logits=lg)
+    assert torch.equal(loss_f, loss) and torch.equal(logp_f, logp)
+    monkeypatch.setenv("GRPO_ROWPASS_SLOTS", "0")
+    dl0, loss0, _, _ = _run_direct(case, 1.0 / 53, tok_src=tok_src, logits=lg)
+    assert torch.equal(dl0, dl) and torch.equal(loss0, loss)
+
+
+@pytest.mark.parametrize("kl_kind,ent", [(2, 0.0), (0, 0.02)])
+def test_f32_cluster_terms(kl_kind, ent):
+    wl = W.make_workload("tiny", rows=4, positions=12, valid_lo=0, V=32776, dtype="f32", seed=60 + kl_kind, std=2.0)
+    case = H.Case(wl)
+    T = wl.T
+    ref = (case.old + np.random.default_rng(3).normal(0, 0.3, T)).astype(np.float32)
+    scale = 1.0 / 41
+    dl = torch.empty_like(case.logits)
+    loss = torch.full((T,), -7.0, device=DEV)
+    logp = torch.full((T,), -7.0, device=DEV)
+    ent_t = torch.full((T,), -7.0, device=DEV)
+    acc = _lib.new_step_acc(DEV)
+    _lib.grpo_logprob_loss_fwd_bwd(case.logits, case.d_target, case.d_old, case.d_adv, case.d_mask, wl.eps,
+                                   scale, dl, loss, logp, acc,
+                                   terms=dict(kl_kind=kl_kind, kl_coef=0.1, ref_logp=torch.from_numpy(ref).to(DEV),
+                                              ent_coef=ent, entropy_tok=ent_t))
+    torch.cuda.synchronize()
+    out = OL.loss_fwd_bwd(case.logits_host, wl.target, case.old, case.adv_tok, wl.mask, wl.eps, scale, True,
+                          dict(kl_kind=kl_kind, kl_coef=float(np.float32(0.1)), ref=ref.astype(np.float64),
+                               ent_coef=float(np.float32(ent))))
+    m = wl.mask.astype(bool)
+    assert np.all(np.abs(H.to_f64(ent_t)[m] - out["entropy"][m]) <= 1e-5 * np.maximum(1, out["entropy"][m]))
+    assert np.all(np.abs(H.to_f64(loss) - out["loss_tok"]) <= 1e-5 * np.abs(out["loss_tok"]) + 1e-6)
+    got, refd = H.to_f64(dl), out["dlogits"]
+    rowmax = np.max(np.abs(refd), axis=1, keepdims=True)
+    amb = H.ambiguous_clip(out["ratio"], wl.eps)
+    bad = np.abs(got - refd) > 2e-5 * np.abs(refd) + 1e-5 * rowmax
+    bad[amb] = False
+    assert not bad.any(), np.argwhere(bad)[:3]
+
+
 def test_cluster_long_masked_runs(monkeypatch):
     # Read rows only in three short windows, separated by masked runs several grid strides
     # long: the producer's look-ahead skips many rows at a time and a third of the clusters

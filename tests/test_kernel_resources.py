@@ -37,14 +37,17 @@ def _report(src):
     return kernels
 
 
-def _cluster(C, NCW, VPT, MINB, ENT, TERMS):
-    return f"_ZN4grpo18row_cluster_kernelILi{C}ELi{NCW}ELi{VPT}ELi{MINB}ELb{ENT}ELi{TERMS}EEEvNS_7RowArgsEii"
+def _cluster(T, C, NCW, VPT, MINB, ENT, TERMS):
+    t = {"bf16": "13__nv_bfloat16", "f32": "f"}[T]
+    return f"_ZN4grpo18row_cluster_kernelI{t}Li{C}ELi{NCW}ELi{VPT}ELi{MINB}ELb{ENT}ELi{TERMS}EEEvNS_7RowArgsEii"
 
 
-# (cluster, consumer warps, vectors per thread, CTAs per SM, entropy, terms) as dispatched for
-# bf16 vocabularies that fit the 2-CTA cluster
-DEFAULT_ROW_PASS = [(2, 16, 4, 1, 0, 0), (2, 16, 4, 1, 0, 1), (2, 16, 2, 1, 0, 2), (2, 16, 2, 1, 1, 1),
-                    (2, 16, 2, 1, 1, 2)]
+# (dtype, cluster, consumer warps, vectors per thread, CTAs per SM, entropy, terms) as
+# dispatched for vocabularies that fit one CTA per SM (bf16: 2-CTA cluster; f32: 4-CTA)
+DEFAULT_ROW_PASS = [("bf16", 2, 16, 4, 1, 0, 0), ("bf16", 2, 16, 4, 1, 0, 1), ("bf16", 2, 16, 2, 1, 0, 2),
+                    ("bf16", 2, 16, 2, 1, 1, 1), ("bf16", 2, 16, 2, 1, 1, 2),
+                    ("f32", 4, 16, 4, 1, 0, 0), ("f32", 4, 16, 4, 1, 0, 1), ("f32", 4, 16, 2, 1, 0, 2),
+                    ("f32", 4, 16, 2, 1, 1, 1), ("f32", 4, 16, 2, 1, 1, 2)]
 
 
 def test_row_pass_default_instances_do_not_spill(grpo_lib):
