@@ -239,6 +239,8 @@ class Batch:
 
         self.wl = wl
         self.dev = device
+        # a step's chunks alternate between the caller's stream and this one (None: one stream)
+        self.side = None if os.environ.get("GRPO_ONE_STREAM") == "1" else torch.cuda.Stream(device)
         self.bp = S.plan_batch(wl.plan, wl.row_len, wl.row_valid, wl.seg_counts)
         Te = self.bp.exec_tokens
         T = wl.T
@@ -285,7 +287,8 @@ class Batch:
 
     def run(self, with_grad=True, stream=None, chunk_ready=None, launch_events=None):
         from rl_post_token_gb300 import step as S
-        return S.run_batch(self.bp, logits=self.logits, dlogits=self.dlogits if with_grad else None,
+        return S.run_batch(self.bp, side_stream=self.side, logits=self.logits,
+                           dlogits=self.dlogits if with_grad else None,
                            target=self.target, old_logp=self.old, mask=self.mask, adv_tok=self.adv_tok,
                            loss_tok=self.loss_tok, logp_tok=self.logp_tok, accs=self.accs,
                            clip_eps=self.wl.eps, rewards=self.rewards, adv_rollout=self.adv_rollout,
@@ -457,8 +460,9 @@ def run_gb300(args):
     elapsed = start.elapsed_time(end) / 1e3
     results = S.read_results(batch.accs, batch.bp.n_steps)
 
-    # the dominant kernel: row-pass launches timed on their own stream inside the timed region
-    row_s = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+    # the dominant kernel: row-pass launches timed on the streams they run on inside the timed
+    # region (the union of their intervals: a step's chunks alternate between two streams)
+    row_s = busy_seconds(start, evs)
     per_launch_bytes = batch.algorithmic_bytes() / (len(evs) / args.steps)
     achieved_gbs = per_launch_bytes / (row_s / len(evs)) / 1e9
 
@@ -512,6 +516,24 @@ def run_gb300(args):
     return 0
 
 
+def busy_seconds(ref, evs):
+    """Length of the union of the [start, end] intervals of event pairs (seconds), measured from
+    the reference event: the time some row-pass launch was running. With a step's chunks on
+    two streams the launches overlap at their ends, so their durations must not be summed."""
+    iv = sorted((ref.elapsed_time(a), ref.elapsed_time(b)) for a, b in evs)
+    total, cur_a, cur_b = 0.0, None, None
+    for a, b in iv:
+        if cur_b is None or a > cur_b:
+            if cur_b is not None:
+                total += cur_b - cur_a
+            cur_a, cur_b = a, b
+        else:
+            cur_b = max(cur_b, b)
+    if cur_b is not None:
+        total += cur_b - cur_a
+    return total / 1e3
+
+
 def run_ahead(batch, stream, steps: int):
     """The pi_old ahead pass: the same batch forward only (no dlogits), timed with CUDA events
     around each row-pass launch. Algorithmic bytes: each valid token reads its logits row and
@@ -528,7 +550,7 @@ def run_ahead(batch, stream, steps: int):
     end.record(stream)
     torch.cuda.synchronize()
     wl = batch.wl
-    row_s = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+    row_s = busy_seconds(start, evs)
     idx = 8 if batch.tok_src is not None else 0
     per_batch = wl.n_valid * (wl.V * wl.elem_bytes + 4 + 4 + 4 + 1 + 4 + 4 + idx)
     return {"value": wl.n_valid * steps / (start.elapsed_time(end) / 1e3), "unit": UNIT,

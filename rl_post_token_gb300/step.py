@@ -70,7 +70,7 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
               adv_eps: float = 1e-6, row_tok_off=None, row_rollout=None, tok_src=None,
               deferred: bool = False, V: Optional[int] = None, stream=None,
               chunk_ready=None, launch_events=None, agg: int = _lib.AGG_TOKEN_MEAN,
-              w_tok=None) -> int:
+              w_tok=None, side_stream=None) -> int:
     """Enqueue the whole batch; returns the number of library kernel launches.
 
     ``accs`` is a uint8 device tensor of n_steps * 128 bytes (one accumulator per optimizer
@@ -79,7 +79,12 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
     is waited on before chunk c is launched, e.g. the end of its host-to-device copy;
     ``launch_events`` (optional list) receives a (start, end) event pair per row-pass launch.
     ``agg`` selects the loss aggregation mode; SEQ_MEAN_TOKEN_MEAN also needs ``w_tok``, the
-    device copy of ``bp.token_weights(agg)[1]`` (input order)."""
+    device copy of ``bp.token_weights(agg)[1]`` (input order).
+
+    ``side_stream`` (optional): the chunks of a step alternate between ``stream`` and this
+    stream, so that the next chunk's blocks take the SMs the current chunk's last rows leave
+    idle. Chunks of a step write disjoint rows and only add to the step's integer counters, so
+    the results are the same bits; the step's finish waits for both streams."""
     import torch
 
     st = torch.cuda.current_stream() if stream is None else stream
@@ -98,15 +103,18 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
         D = N if plain else int(divisors[s])
         scale = 1.0 if deferred else 1.0 / max(D, 1)
         acc = accs[s * _lib.ACC_BYTES:(s + 1) * _lib.ACC_BYTES]
-        for c in range(p["step_chunk_off"][s], p["step_chunk_off"][s + 1]):
+        if side_stream is not None:
+            side_stream.wait_stream(st)  # the advantage and the previous step's finish
+        for i, c in enumerate(range(p["step_chunk_off"][s], p["step_chunk_off"][s + 1])):
             a, b = int(bp.exec_tok_off[c]), int(bp.exec_tok_off[c + 1])
+            cs = side_stream if side_stream is not None and i % 2 == 1 else st
             if chunk_ready is not None:
-                st.wait_event(chunk_ready[c])
+                cs.wait_event(chunk_ready[c])
             if b == a:
                 continue
             if launch_events is not None:
                 e0 = torch.cuda.Event(enable_timing=True)
-                e0.record(st)
+                e0.record(cs)
             if tok_src is None:
                 # exec order == input order: the chunk's side inputs are the same slice
                 side = (target[a:b], None if old_logp is None else old_logp[a:b], adv_tok[a:b],
@@ -118,13 +126,15 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
             tg, od, ad, mk, lt, lp, ts, wt = side
             _lib.grpo_logprob_loss_fwd_bwd(
                 logits[a:b], tg, od, ad, mk, clip_eps, scale,
-                None if dlogits is None else dlogits[a:b], lt, lp, acc, tok_src=ts, V=V, stream=st,
+                None if dlogits is None else dlogits[a:b], lt, lp, acc, tok_src=ts, V=V, stream=cs,
                 terms=None if wt is None else dict(w_tok=wt))
             if launch_events is not None:
                 e1 = torch.cuda.Event(enable_timing=True)
-                e1.record(st)
+                e1.record(cs)
                 launch_events.append((e0, e1))
             launches += 1
+        if side_stream is not None:
+            st.wait_stream(side_stream)
         t0, t1 = bp.step_tok_range[s]
         e0, e1 = bp.step_exec_range[s]
         grads = [] if dlogits is None or e1 == e0 else [dlogits[e0:e1]]
