@@ -351,6 +351,32 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
                : "memory");
 }
 
+// Relaxed arrive (no fence) on an mbarrier in a peer CTA's shared memory: for a signal that
+// publishes no data of this thread's.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Relaxed arrive that also raises the phase's expected transaction bytes (the data comes by
+// st.async, whose completion the phase tracks; this thread publishes nothing).
+__device__ __forceinline__ void mbar_arrive_expect_tx_relaxed(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Asynchronous stores into a peer CTA's shared memory (cluster addresses from mapa), each
+// completing its bytes on an mbarrier of that CTA: the reader sees the data once the phase
+// completes, and the writer waits for nothing.
+__device__ __forceinline__ void st_async_v2f32(uint32_t cluster_addr, float x, float y, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+               ::"r"(cluster_addr), "f"(x), "f"(y), "r"(cluster_bar) : "memory");
+}
+
+__device__ __forceinline__ void st_async_f32(uint32_t cluster_addr, float x, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];"
+               ::"r"(cluster_addr), "f"(x), "r"(cluster_bar) : "memory");
+}
+
 __device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }

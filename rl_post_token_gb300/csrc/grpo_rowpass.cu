@@ -13,6 +13,58 @@ namespace grpo {
 
 size_t max_smem_optin();
 
+// Launches a persistent cluster kernel with as many clusters as fit on the device at once
+// (no more than there are rows). Per device and kernel: the kernel's shared-memory limit only
+// ever rises (a concurrent launch with a larger slice never finds it lowered under it), and
+// the co-resident cluster count is cached per shared-memory size.
+template <auto KERN>
+int launch_clusters(const RowArgs& a, int C, int NCW, size_t smem, int Vs, int S, cudaStream_t st) {
+  int dev = 0;
+  GRPO_CUDA_TRY(cudaGetDevice(&dev));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3((NCW + 1) * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n_clusters = 0;
+  {
+    struct Entry { size_t smem; int clusters; };
+    static std::mutex mu;
+    static size_t limit[64] = {};
+    static Entry seen[64][4] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    const bool known_dev = dev >= 0 && dev < 64;
+    if (known_dev)
+      for (const Entry& e : seen[dev])
+        if (e.smem == smem) n_clusters = e.clusters;
+    if (n_clusters == 0) {
+      if (!known_dev || smem > limit[dev]) {
+        GRPO_CUDA_TRY(cudaFuncSetAttribute(KERN, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        if (known_dev) limit[dev] = smem;
+      }
+      cfg.gridDim = dim3(C * 1024, 1, 1);
+      GRPO_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n_clusters, KERN, &cfg));
+      if (n_clusters < 1) return GRPO_ERR_UNSUPPORTED;
+      if (known_dev) {
+        Entry* slot = &seen[dev][0];
+        for (Entry& e : seen[dev])
+          if (e.smem == 0) { slot = &e; break; }
+        *slot = Entry{smem, n_clusters};
+      }
+    }
+  }
+  const int64_t clusters = std::min<int64_t>(a.T, n_clusters);
+  cfg.gridDim = dim3((unsigned)(clusters * C), 1, 1);
+  GRPO_CUDA_TRY(cudaLaunchKernelEx(&cfg, KERN, a, Vs, S));
+  return GRPO_OK;
+}
+
 template <typename T, int C, int NCW, int VPT, int MINB, bool ENT, int TERMS>
 int launch_cluster(const RowArgs& a, cudaStream_t st) {
   constexpr int CH = cluster_chunk_elems<T>(NCW, VPT);
@@ -34,54 +86,27 @@ int launch_cluster(const RowArgs& a, cudaStream_t st) {
     else if (n > nchm && n <= s_fit) S = n;
   }
   const size_t smem = cluster_ring_bytes<T>(Vs, CH, S) + cluster_tail_bytes(NCW);
-  auto kern = row_cluster_kernel<T, C, NCW, VPT, MINB, ENT, TERMS>;
-  int dev = 0;
-  GRPO_CUDA_TRY(cudaGetDevice(&dev));
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3((NCW + 1) * 32, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // Per device: the kernel's shared-memory limit only ever rises (a concurrent launch with a
-  // larger slice can never find it lowered under it), and the co-resident cluster count is
-  // cached per shared-memory size.
-  int n_clusters = 0;
-  {
-    struct Entry { size_t smem; int clusters; };
-    static std::mutex mu;
-    static size_t limit[64] = {};
-    static Entry seen[64][4] = {};
-    std::lock_guard<std::mutex> lock(mu);
-    const bool known_dev = dev >= 0 && dev < 64;
-    if (known_dev)
-      for (const Entry& e : seen[dev])
-        if (e.smem == smem) n_clusters = e.clusters;
-    if (n_clusters == 0) {
-      if (!known_dev || smem > limit[dev]) {
-        GRPO_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        if (known_dev) limit[dev] = smem;
-      }
-      cfg.gridDim = dim3(C * 1024, 1, 1);
-      GRPO_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n_clusters, kern, &cfg));
-      if (n_clusters < 1) return GRPO_ERR_UNSUPPORTED;
-      if (known_dev) {
-        Entry* slot = &seen[dev][0];
-        for (Entry& e : seen[dev])
-          if (e.smem == 0) { slot = &e; break; }
-        *slot = Entry{smem, n_clusters};
-      }
-    }
+  return launch_clusters<row_cluster_kernel<T, C, NCW, VPT, MINB, ENT, TERMS>>(a, C, NCW, smem, Vs, S, st);
+}
+
+// The forward-only streaming kernel: as many ring slots as the opt-in shared memory holds (at
+// least 2; GRPO_ROWPASS_SLOTS=n takes n of them, 0 the minimum), whatever the row length.
+template <typename T, int C, int NCW, int VPT>
+int launch_fwd(const RowArgs& a, cudaStream_t st) {
+  constexpr int CH = cluster_chunk_elems<T>(NCW, VPT);
+  const int Vs = cluster_slice_elems<T>(a.V, C);
+  const size_t optin = max_smem_optin();
+  const size_t tail = fwd_tail_bytes(C, NCW);
+  if (optin <= tail) return GRPO_ERR_UNSUPPORTED;
+  const int s_fit = (int)std::min<size_t>(kMaxChunks, (optin - tail) / ((size_t)CH * sizeof(T)));
+  if (s_fit < 2) return GRPO_ERR_UNSUPPORTED;
+  int S = s_fit;
+  if (const char* ov = getenv("GRPO_ROWPASS_SLOTS")) {
+    const int n = atoi(ov);
+    S = n < 2 ? 2 : std::min(n, s_fit);
   }
-  const int64_t clusters = std::min<int64_t>(a.T, n_clusters);
-  cfg.gridDim = dim3((unsigned)(clusters * C), 1, 1);
-  GRPO_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, a, Vs, S));
-  return GRPO_OK;
+  const size_t smem = (size_t)S * CH * sizeof(T) + tail;
+  return launch_clusters<row_fwd_kernel<T, C, NCW, VPT>>(a, C, NCW, smem, Vs, S, st);
 }
 
 template <typename T, int NT, int U, bool ENT, int TERMS>
@@ -132,6 +157,13 @@ bool cluster_fits(int64_t V, int C, int NCW, int minb, int vpt) {
          (Vs + cluster_chunk_elems<T>(NCW, vpt) - 1) / cluster_chunk_elems<T>(NCW, vpt) <= kMaxChunks;
 }
 
+// Forward-only calls without extra terms take the streaming kernel unless GRPO_ROWPASS_FWD=0
+// (the general cluster kernel, which gives the same bits).
+bool fwd_kernel_on() {
+  const char* v = getenv("GRPO_ROWPASS_FWD");
+  return !(v && strcmp(v, "0") == 0);
+}
+
 template <bool ENT, int TERMS>
 int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
   const int64_t V = a.V;
@@ -158,6 +190,8 @@ int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
       if (pin && strcmp(pin, "c3") == 0 && cluster_fits<B16>(V, 3, 8, 2, 4)) return c34(C3{});
       if (pin && strcmp(pin, "c4") == 0 && cluster_fits<B16>(V, 4, 8, 2, 4)) return c34(C4{});
       if (cluster_fits<B16>(V, 2, 16, 1, 4)) {
+        if constexpr (!ENT && TERMS == 0)
+          if (!a.dlogits && fwd_kernel_on()) return launch_fwd<B16, 2, 16, 4>(a, st);
         if constexpr (HALF) return launch_cluster<B16, 2, 16, 2, 1, ENT, TERMS>(a, st);
         else return launch_cluster<B16, 2, 16, 4, 1, ENT, TERMS>(a, st);
       }
@@ -170,6 +204,8 @@ int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
   // float32 vocabularies: a row is twice the bytes, so a 4-CTA cluster, one CTA per SM with
   // the ring of spare slots, holds the same slice size as the bf16 2-CTA cluster
   if (vec && V % 4 == 0 && V >= 16384 && !pin_l2 && cluster_fits<float>(V, 4, 16, 1, 4)) {
+    if constexpr (!ENT && TERMS == 0)
+      if (!a.dlogits && fwd_kernel_on()) return launch_fwd<float, 4, 16, 4>(a, st);
     if constexpr (HALF) return launch_cluster<float, 4, 16, 2, 1, ENT, TERMS>(a, st);
     else return launch_cluster<float, 4, 16, 4, 1, ENT, TERMS>(a, st);
   }

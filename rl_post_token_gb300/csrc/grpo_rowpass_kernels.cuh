@@ -796,4 +796,240 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
   if (tid == 32 && rank == 0) cnt.flush(a.acc);
 }
 
+// ------------------------------------------------------------------------------------------
+// Forward-only cluster kernel (no dlogits, no extra terms): the pi_old ahead pass. It splits
+// rows, chunks them and assigns elements to threads exactly as row_cluster_kernel<T, C, NCW,
+// VPT> does, and combines the partial sums in the same order, so the log-prob, the loss and
+// the counts are the same bits. What differs is that no thread waits for a row's exchange:
+//  * each consumer warp releases a chunk's slot as soon as it has folded the chunk in, and the
+//    producer streams the cluster's rows through the ring with no per-row barrier;
+//  * each warp sends its (shift, sum) straight into CTA 0's exchange buffer with an
+//    asynchronous DSMEM store that completes on CTA 0's mbarrier, and goes on to the next row
+//    without a fence;
+//  * one warp of CTA 0, rotating with the row, combines a row's C * NCW partials one row later
+//    (warps in order within a CTA, then CTAs in rank order) and writes the token's outputs.
+// kFwdBufs exchange buffers, each handed back by its combiner through an mbarrier in every
+// CTA, bound how far a warp can run ahead of the combines.
+// ------------------------------------------------------------------------------------------
+constexpr int kFwdBufs = 4;
+
+__host__ __device__ constexpr size_t fwd_tail_bytes(int C, int NCW) {
+  return (2 * kMaxChunks + 2 * kFwdBufs) * sizeof(uint64_t) + (size_t)kFwdBufs * C * NCW * 2 * sizeof(float) +
+         kFwdBufs * sizeof(float) + 16;
+}
+
+// First row at or after `from` (stepping by `stride`) that is read, examining 32 rows at once;
+// every lane of the warp calls it and gets the same answer.
+__device__ __forceinline__ int64_t scan_read_row(const RowArgs& a, int64_t from, int64_t stride, int lane) {
+  for (; from < a.T; from += 32 * stride) {
+    const int64_t r = from + (int64_t)lane * stride;
+    bool ok = false;
+    if (r < a.T) {
+      const int64_t src = row_src(a, r);
+      ok = src >= 0 && a.mask[src] != 0;
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, ok);
+    if (bal) return from + (int64_t)(__ffs(bal) - 1) * stride;
+  }
+  return a.T;
+}
+
+template <typename T, int C, int NCW, int VPT>
+__global__ void __launch_bounds__((NCW + 1) * 32, 1) row_fwd_kernel(RowArgs a, int Vs, int S) {
+  constexpr int NC = NCW * 32;
+  constexpr int E = vec_elems<T>();
+  constexpr int CH = cluster_chunk_elems<T>(NCW, VPT);
+  constexpr int NP = C * NCW;  // partials per row
+  constexpr bool PK = true;
+  extern __shared__ __align__(128) uint8_t smem[];
+  T* ring = reinterpret_cast<T*>(smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * CH * sizeof(T));
+  uint64_t* empty = full + kMaxChunks;
+  uint64_t* xfull = empty + kMaxChunks;  // CTA 0: all partials of the buffer's row are in
+  uint64_t* xempty = xfull + kFwdBufs;   // every CTA: CTA 0 has read the buffer
+  float* part = reinterpret_cast<float*>(xempty + kFwdBufs);  // CTA 0: [buffer][C * NCW][m, s]
+  float* zyv = part + kFwdBufs * NP * 2;                      // CTA 0: [buffer] target logit
+  volatile int* s_abort = reinterpret_cast<volatile int*>(zyv + kFwdBufs);
+
+  const uint32_t rank = cluster_ctarank();
+  const int64_t cid = blockIdx.x / C, ncl = gridDim.x / C;
+  const int64_t V = a.V;
+  const int64_t base = (int64_t)rank * Vs;
+  const int n_r = (int)max((int64_t)0, min((int64_t)Vs, V - base));
+  const int nch = (n_r + CH - 1) / CH;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int k = 0; k < kMaxChunks; ++k) {
+      mbar_init(&full[k], 1);
+      mbar_init(&empty[k], NCW);
+    }
+    for (int b = 0; b < kFwdBufs; ++b) {
+      mbar_init(&xfull[b], 1);  // the combiner's arrive, plus the bytes of the row's stores
+      mbar_init(&xempty[b], 1);
+    }
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  cluster_sync_all();
+
+  const T* lg = static_cast<const T*>(a.logits);
+  Counts cnt;
+  uint32_t issued = 0;  // producer: chunks issued so far (slot reuse starts at S)
+
+  if (warp == 0) {
+    // ---- producer: lane 0 streams the read rows' chunks; the warp looks for the next row ----
+    RingCursor pc{0, 0u};
+    int64_t cur = scan_read_row(a, cid, ncl, lane);
+    while (cur < a.T) {
+      // the next 32 candidate rows: their index and mask loads are in flight while lane 0
+      // issues this row's copies
+      const int64_t cand = cur + (int64_t)(lane + 1) * ncl;
+      const int64_t csrc = cand < a.T ? row_src(a, cand) : -1;
+      bool stop = false;
+      if (lane == 0) {
+        for (int k = 0; k < nch; ++k) {
+          if (issued >= (uint32_t)S && !mbar_wait_bounded(&empty[pc.slot], pc.ph ^ 1u, s_abort)) {
+            stop = true;
+            break;
+          }
+          const int n_k = min(CH, n_r - k * CH);
+          mbar_arrive_expect_tx(&full[pc.slot], (uint32_t)n_k * (uint32_t)sizeof(T));
+          bulk_g2s(ring + (size_t)pc.slot * CH, lg + cur * a.ld + base + (int64_t)k * CH,
+                   (uint32_t)n_k * (uint32_t)sizeof(T), &full[pc.slot]);
+          ++issued;
+          pc.step(S);
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) break;  // a wait gave up: issue nothing more
+      const bool ok = csrc >= 0 && a.mask[csrc] != 0;
+      const unsigned bal = __ballot_sync(0xffffffffu, ok);
+      cur = bal ? cur + (int64_t)__ffs(bal) * ncl : scan_read_row(a, cur + 33 * ncl, ncl, lane);
+    }
+  } else {
+    // ---- consumers ----
+    const int ct = tid - 32, cw = warp - 1;
+    RingCursor rc{0, 0u};
+    uint32_t xi = 0;  // read rows so far: the exchange sequence number
+    RowMeta pend{};   // the previous read row, combined one row late
+    MetaPipe<0> pipe(a, cid, ncl);
+
+    // CTA 0, warp xi % NCW: the row's log-sum-exp from its partials, then the token's outputs
+    auto combine = [&](uint32_t i, const RowMeta& tm) {
+      const uint32_t b = i % kFwdBufs, u = i / kFwdBufs;
+      const bool ybad = tm.y < 0 || (int64_t)tm.y >= V;
+      // the phase completes once every warp's partial (and the target logit) has landed;
+      // phase u-1 is complete already: this warp's own store for row i waited for its reader
+      if (lane == 0) mbar_arrive_expect_tx_relaxed(&xfull[b], NP * 8u + (ybad ? 0u : 4u));
+      mbar_wait_cluster_bounded(&xfull[b], u & 1u, s_abort);
+      MS t{-INFINITY, 0.f};
+      if (lane < C)
+        for (int j = 0; j < NCW; ++j) {
+          const float* p = part + 2 * (b * NP + lane * NCW + j);
+          t = ms2_combine(t, MS{p[0], p[1]});
+        }
+      const float zy = ybad ? __int_as_float(0x7fc00000) : zyv[b];
+      MS tot{-INFINITY, 0.f};
+#pragma unroll
+      for (int r = 0; r < C; ++r)
+        tot = ms2_combine(tot, MS{__shfl_sync(0xffffffffu, t.m, r), __shfl_sync(0xffffffffu, t.s, r)});
+      __syncwarp();
+      if (lane == 0) {
+        const float lse2 = tot.m + log2f(tot.s);
+        const TokenOut o = token_epilogue(zy, lse2 * kLn2, a.old_logp != nullptr, tm.old, tm.A, a.eps, a.scale);
+        // the buffer is free again in every CTA: what was read from it has been consumed
+        // (by the shuffles and the epilogue), so the signal needs no fence
+        for (int r = 0; r < C; ++r) mbar_arrive_remote_relaxed(mapa_u32(smem_u32(&xempty[b]), (uint32_t)r));
+        a.loss_tok[tm.idx] = o.loss;
+        if (a.logp_tok) a.logp_tok[tm.idx] = o.logp;
+        cnt.tokens++;
+        cnt.valid++;
+        cnt.clipped += o.clipped;
+        cnt.nonfinite += o.nonfinite;
+      }
+    };
+
+    for (int64_t row = cid; row < a.T; row += ncl) {
+      // the row's metadata: lane 0 keeps the prefetch pipeline and broadcasts, so lane 31,
+      // which releases the ring slots, has no global load in flight for its release to wait on
+      RowMeta tm{};
+      if (lane == 0) tm = pipe.advance(row);
+      tm.idx = __shfl_sync(0xffffffffu, tm.idx, 0);
+      tm.valid = __shfl_sync(0xffffffffu, (int)tm.valid, 0) != 0;
+      tm.y = __shfl_sync(0xffffffffu, tm.y, 0);
+      tm.A = __shfl_sync(0xffffffffu, tm.A, 0);
+      tm.old = __shfl_sync(0xffffffffu, tm.old, 0);
+      if (!tm.valid) {
+        // masked or padding row: nothing read, nothing exchanged
+        if (rank == 0 && ct == 0) {
+          cnt.tokens++;
+          if (tm.idx >= 0) {
+            a.loss_tok[tm.idx] = 0.f;
+            if (a.logp_tok) a.logp_tok[tm.idx] = 0.f;
+          }
+        }
+        continue;
+      }
+      // where the target logit sits in this CTA's slice, and which thread reads it
+      const int64_t yo = (tm.y < 0 || (int64_t)tm.y >= V) ? -1 : (int64_t)tm.y - base;
+      const bool own = yo >= 0 && yo < n_r;
+      const int ky = own ? (int)(yo / CH) : -1;
+      const int oy = own ? (int)(yo - (int64_t)ky * CH) : 0;
+      const int cty = (oy / E) % NC;
+      float zyl = 0.f;
+
+      // pass 1, slot by slot as the chunks land; each slot is released once folded in
+      MS acc{-INFINITY, 0.f};
+      for (int k = 0; k < nch; ++k) {
+        mbar_wait_bounded(&full[rc.slot], rc.ph, s_abort);
+        const int nv = min(CH, n_r - k * CH) / E;
+        const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)rc.slot * CH);
+        if (nv == VPT * NC) {
+          float x[VPT * E];
+#pragma unroll
+          for (int j = 0; j < VPT; ++j) unpack_at<T>(sv[ct + j * NC], x + E * j);
+          lazy_online2<VPT * E, PK>(acc, x);
+        } else {
+          for (int v = ct; v < nv; v += NC) {
+            float x[E];
+            unpack_at<T>(sv[v], x);
+            lazy_online2<E, PK>(acc, x);
+          }
+        }
+        if (k == ky && ct == cty) zyl = Vec<T>::load1(ring + (size_t)rc.slot * CH + oy);
+        __syncwarp();
+        if (lane == 31) mbar_arrive(&empty[rc.slot]);
+        rc.step(S);
+      }
+
+      // the warp's partial (and the target logit, from the warp that read it) to CTA 0
+      const MS w = warp_ms2(acc);
+      const bool wown = own && cty / 32 == cw;
+      const float zy = wown ? __shfl_sync(0xffffffffu, zyl, cty & 31) : 0.f;
+      if (lane == 0) {
+        const uint32_t b = xi % kFwdBufs, u = xi / kFwdBufs;
+        if (u > 0) mbar_wait_cluster_bounded(&xempty[b], (u - 1u) & 1u, s_abort);
+        const uint32_t bar = mapa_u32(smem_u32(&xfull[b]), 0u);
+        st_async_v2f32(mapa_u32(smem_u32(part + 2 * (b * NP + rank * NCW + cw)), 0u), w.m, w.s, bar);
+        if (wown) st_async_f32(mapa_u32(smem_u32(zyv + b), 0u), zy, bar);
+      }
+      if (rank == 0 && xi > 0 && (xi - 1u) % NCW == (uint32_t)cw) combine(xi - 1u, pend);
+      pend = tm;
+      ++xi;
+    }
+    if (rank == 0 && xi > 0 && (xi - 1u) % NCW == (uint32_t)cw) combine(xi - 1u, pend);
+  }
+
+  __syncthreads();
+  if (*s_abort) {
+    if (tid == 0)
+      for (int sl = 0; sl < S && (uint32_t)sl < issued; ++sl)
+        mbar_drain(&full[sl], ((issued - 1u - (uint32_t)sl) / (uint32_t)S) & 1u);
+    if (tid == 0) atomicOr(&a.acc->flags, kFlagWaitTimeout);
+  }
+  cluster_sync_all();  // no CTA leaves while a peer may still store into or arrive on its memory
+  if (rank == 0 && warp > 0 && lane == 0) cnt.flush(a.acc);
+}
+
 }  // namespace grpo

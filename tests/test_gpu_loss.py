@@ -379,6 +379,65 @@ def test_ring_slots_equal_fixed_buffer_bitwise(V, monkeypatch):
     assert outs[None][3]["status"] == 0
 
 
+@pytest.mark.parametrize("dtype,V,rows", [("bf16", 151936, 16), ("bf16", 32776, 32), ("f32", 32776, 32)])
+def test_forward_only_streaming_kernel_equals_general_bitwise(dtype, V, rows, monkeypatch):
+    # Forward-only calls run the streaming kernel: slots released during pass 1, partials sent
+    # to CTA 0 and combined one row late by a rotating warp. It must give the bits of the
+    # general cluster kernel called forward only (GRPO_ROWPASS_FWD=0) at every ring size
+    # (0 = two slots, the fewest), with masked and padding rows in a shuffled order, pi_old
+    # given, more read rows per cluster than exchange buffers, and a valid token whose target
+    # is out of range (its loss is NaN and it counts as non-finite).
+    wl = W.make_workload("tiny", rows=rows, positions=64, valid_lo=0, V=V, dtype=dtype, seed=V % 541 + rows,
+                         std=2.0)
+    case = H.Case(wl)
+    T = case.logits.shape[0]
+    rng = np.random.default_rng(7)
+    perm = rng.permutation(T)
+    pads = rng.choice(T, 11)
+    src = np.concatenate([perm, -1 - pads]).astype(np.int64)
+    rng.shuffle(src)
+    tok_src = torch.from_numpy(src).to(DEV)
+    lg = case.logits[torch.from_numpy(np.where(src >= 0, src, -1 - src)).to(DEV)]
+    bad = int(np.nonzero(case.mask)[0][5])
+    tgt = case.d_target.clone()
+    tgt[bad] = V
+
+    def run():
+        loss = torch.full((T,), -7.0, device=DEV)
+        logp = torch.full((T,), -7.0, device=DEV)
+        acc = _lib.new_step_acc(DEV)
+        _lib.grpo_logprob_loss_fwd_bwd(lg, tgt, case.d_old, case.d_adv, case.d_mask, wl.eps, 1.0 / 89, None,
+                                       loss, logp, acc, tok_src=tok_src)
+        torch.cuda.synchronize()
+        return loss.view(torch.int32).clone(), logp.view(torch.int32).clone(), acc.clone()
+
+    monkeypatch.setenv("GRPO_ROWPASS_FWD", "0")
+    want = run()
+    monkeypatch.delenv("GRPO_ROWPASS_FWD")
+    for slots in ("0", "3", None):
+        if slots is None:
+            monkeypatch.delenv("GRPO_ROWPASS_SLOTS", raising=False)
+        else:
+            monkeypatch.setenv("GRPO_ROWPASS_SLOTS", slots)
+        got = run()
+        for g, w, what in zip(got, want, ("loss", "logp", "acc")):
+            assert torch.equal(g, w), (slots, what)
+    res = _lib.grpo_finish_step(want[2].clone(), want[0].view(torch.float32))
+    assert res["status"] == _lib.STEP_SKIPPED_NONFINITE
+    assert res["n_nonfinite"] == 1 and res["kernel_flags"] == 0
+    assert res["n_tokens"] == T + 11 and res["n_valid"] == int(case.mask.sum())
+    # and against the oracle (outputs are indexed by input token), every token but the one
+    # with the bad target
+    got_loss = want[0].view(torch.float32).cpu().numpy().astype(np.float64)
+    got_logp = want[1].view(torch.float32).cpu().numpy().astype(np.float64)
+    ref = H.oracle_run(case, want_grad=False)
+    m = case.mask.copy()
+    m[bad] = 0
+    got_loss[bad] = got_logp[bad] = 0.0
+    ref["loss_tok"][bad] = ref["logp_tok"][bad] = 0.0
+    H.assert_tokens_close(got_loss, got_logp, ref, case.adv_tok, m)
+
+
 @pytest.mark.parametrize("V", [16384, 32776, 151936])
 def test_f32_cluster_rows_against_oracle(V, monkeypatch):
     # float32 logits through the 4-CTA cluster kernel: masked and padding rows, the four

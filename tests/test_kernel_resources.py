@@ -59,6 +59,20 @@ def test_row_pass_default_instances_do_not_spill(grpo_lib):
         assert k[name]["regs"] <= 96, (inst, k[name])
 
 
+# the forward-only streaming instances (dtype, cluster, consumer warps, vectors per thread)
+FORWARD_ONLY = [("bf16", 2, 16, 4), ("f32", 4, 16, 4)]
+
+
+def test_forward_only_instances_do_not_spill(grpo_lib):
+    k = _report("grpo_rowpass.cu")
+    for T, C, NCW, VPT in FORWARD_ONLY:
+        t = {"bf16": "13__nv_bfloat16", "f32": "f"}[T]
+        name = f"_ZN4grpo14row_fwd_kernelI{t}Li{C}ELi{NCW}ELi{VPT}EEEvNS_7RowArgsEii"
+        assert name in k, (T, "not compiled")
+        assert k[name]["spill"] == 0, (T, k[name])
+        assert k[name]["regs"] <= 96, (T, k[name])
+
+
 def test_lmhead_and_step_kernels_do_not_spill(grpo_lib):
     for src, pat in (("grpo_lmhead.cu", r"gemm_kernel|dz_from_e|reduce_kernel"),
                      ("grpo_step.cu", r"finish_kernel|adv_")):
