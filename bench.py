@@ -231,7 +231,7 @@ def run_reference(args):
 class Batch:
     """Device-resident inputs and outputs of one collected batch."""
 
-    def __init__(self, wl, device):
+    def __init__(self, wl, device, kl_kind=0, kl_coef=0.0, ent_coef=0.0):
         import torch
         from rl_post_token_gb300 import _lib
         from rl_post_token_gb300 import step as S
@@ -265,6 +265,18 @@ class Batch:
         self.old = None
         self.run(with_grad=False)
         self.old = self.logp_tok + t(wl.old_noise)
+        # regularisers of the training step (not of the pi_old pass): a reference policy's
+        # log-probs drawn like pi_old's (the ahead pass's log-probs plus seeded noise), and the
+        # per-token entropy as an output
+        self.terms, self.ref = None, None
+        if kl_kind or ent_coef:
+            self.terms = {"kl_kind": kl_kind, "kl_coef": kl_coef, "ent_coef": ent_coef}
+            if kl_kind:
+                noise = np.random.default_rng(wl.seed + 1).normal(0.0, 0.1, T).astype(np.float32)
+                self.ref = self.old - t(wl.old_noise) + t(noise)
+                self.terms["ref_logp"] = self.ref
+            if ent_coef:
+                self.terms["entropy_tok"] = torch.empty(T, dtype=torch.float32, device=device)
         torch.cuda.synchronize(device)
         self.n_step = 0
 
@@ -294,7 +306,8 @@ class Batch:
                            clip_eps=self.wl.eps, rewards=self.rewards, adv_rollout=self.adv_rollout,
                            group_size=self.wl.group_size, row_tok_off=self.row_tok_off,
                            row_rollout=self.row_rollout, tok_src=self.tok_src, V=self.wl.V,
-                           stream=stream, chunk_ready=chunk_ready, launch_events=launch_events)
+                           stream=stream, chunk_ready=chunk_ready, launch_events=launch_events,
+                           terms=self.terms if with_grad else None)
 
     def algorithmic_bytes(self):
         """Bytes the method must move per batch in the row pass: a valid token reads its logits
@@ -304,9 +317,13 @@ class Batch:
         wl = self.wl
         rowb = wl.V * wl.elem_bytes
         idx = 8 if self.tok_src is not None else 0
+        extra = 0  # the terms' per-token input (reference log-prob) and output (entropy)
+        if self.terms is not None:
+            extra = (4 if self.terms.get("ref_logp") is not None else 0) + \
+                    (4 if self.terms.get("entropy_tok") is not None else 0)
         valid = wl.n_valid  # each valid input token runs exactly once; padding rows are masked
         masked = self.bp.exec_tokens - valid
-        return valid * (2 * rowb + 4 + 4 + 4 + 1 + 4 + 4 + idx) + masked * (rowb + 1 + idx)
+        return valid * (2 * rowb + 4 + 4 + 4 + 1 + 4 + 4 + idx + extra) + masked * (rowb + 1 + idx)
 
 
 def run_lmhead(args):
@@ -433,7 +450,13 @@ def run_gb300(args):
     if args.rows and args.workload == "qwen_step":
         ov.update(mini=args.rows, micro=args.rows)
     wl = W.make_workload(args.workload, seed=rank, **ov)
-    batch = Batch(wl, device)
+    kl_kind = {"none": 0, "k1": _lib.KL_K1, "k3": _lib.KL_K3}[args.kl]
+    batch = Batch(wl, device, kl_kind=kl_kind, kl_coef=args.kl_coef, ent_coef=args.ent_coef)
+    terms_text = ""
+    if batch.terms is not None:
+        terms_text = ", ".join(([f"KL {args.kl} coef {args.kl_coef}"] if kl_kind else []) +
+                               ([f"entropy bonus coef {args.ent_coef} (entropy written per token)"]
+                                if args.ent_coef else []))
     stream = torch.cuda.current_stream(device)
 
     for _ in range(max(args.warmup, 3)):
@@ -485,7 +508,8 @@ def run_gb300(args):
         "warmup": max(args.warmup, 3), "ms_per_step": 1e3 * max_el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload] + (f" [rows overridden: {args.rows}]" if args.rows else ""),
+        "config": {"workload": WORKLOAD_TEXT[args.workload] + (f" [rows overridden: {args.rows}]" if args.rows else "")
+                               + (f" [loss terms: {terms_text}]" if terms_text else ""),
                    "valid_tokens_per_step": wl.n_valid,
                    "logits_rows_per_step": batch.bp.exec_tokens, "vocab": wl.V,
                    "l2": "inputs larger than L2 (%.1f GB of logits per step), no flush"
@@ -493,9 +517,10 @@ def run_gb300(args):
                    "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                      "frac": achieved_gbs / peak, "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": "row pass (grpo_logprob_loss_fwd_bwd)",
+                     "kernel": "row pass (grpo_logprob_loss_fwd_bwd" + (f"_ex: {terms_text})" if terms_text else ")"),
                      "row_pass_share_of_step": row_s / elapsed,
-                     "traffic": None if tpv is None else tpv * wl.n_valid / launches_per_step},
+                     # the committed capture is of the instance without terms
+                     "traffic": None if tpv is None or terms_text else tpv * wl.n_valid / launches_per_step},
         "gpu_launches": launches,
         "e2e": e2e,
         "ahead_pass": dict(ahead, frac=ahead["achieved_gbs"] / hbm_peak()[0], per_gpu=True),
@@ -574,7 +599,8 @@ def run_e2e(batch, device, stream, steps: int):
 
     host_logits = torch.empty(batch.logits.shape, dtype=batch.logits.dtype, pin_memory=True)
     host_logits.copy_(batch.logits)
-    side = {k: getattr(batch, k).cpu().pin_memory() for k in ("target", "mask", "rewards", "old")}
+    side = {k: getattr(batch, k).cpu().pin_memory() for k in ("target", "mask", "rewards", "old")
+            + (("ref",) if batch.ref is not None else ())}
     host_res = torch.empty(batch.accs.numel(), dtype=torch.uint8, pin_memory=True)
     copy = torch.cuda.Stream(device)
     torch.cuda.synchronize(device)
@@ -626,6 +652,11 @@ def main(argv=None):
                     help="override the fused LM-head token count (smaller cases for profiling)")
     ap.add_argument("--rows", type=int, default=0,
                     help="override the workload's row count (smaller cases for profiling)")
+    ap.add_argument("--kl", default="none", choices=["none", "k1", "k3"],
+                    help="add a KL term to a reference policy to the training step's loss")
+    ap.add_argument("--kl-coef", type=float, default=0.05)
+    ap.add_argument("--ent-coef", type=float, default=0.0,
+                    help="add an entropy bonus (and the per-token entropy output) to the step's loss")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)

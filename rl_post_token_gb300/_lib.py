@@ -33,6 +33,10 @@ DTYPE_BF16 = 1
 AGG_TOKEN_MEAN = 0
 AGG_SEQ_MEAN_TOKEN_SUM = 1
 AGG_SEQ_MEAN_TOKEN_MEAN = 2
+# GRPO_KL_*: the KL estimator of the regulariser term
+KL_NONE = 0
+KL_K1 = 1
+KL_K3 = 2
 ACC_BYTES = 128
 
 _i32p = C.POINTER(C.c_int32)

@@ -70,7 +70,7 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
               adv_eps: float = 1e-6, row_tok_off=None, row_rollout=None, tok_src=None,
               deferred: bool = False, V: Optional[int] = None, stream=None,
               chunk_ready=None, launch_events=None, agg: int = _lib.AGG_TOKEN_MEAN,
-              w_tok=None, side_stream=None) -> int:
+              w_tok=None, side_stream=None, terms: Optional[dict] = None) -> int:
     """Enqueue the whole batch; returns the number of library kernel launches.
 
     ``accs`` is a uint8 device tensor of n_steps * 128 bytes (one accumulator per optimizer
@@ -80,6 +80,10 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
     ``launch_events`` (optional list) receives a (start, end) event pair per row-pass launch.
     ``agg`` selects the loss aggregation mode; SEQ_MEAN_TOKEN_MEAN also needs ``w_tok``, the
     device copy of ``bp.token_weights(agg)[1]`` (input order).
+
+    ``terms`` (optional): the regularisers every chunk's call adds, as for
+    ``_lib.grpo_logprob_loss_fwd_bwd``: ``kl_kind``, ``kl_coef``, ``ref_logp`` (input order, all
+    tokens), ``ent_coef`` and ``entropy_tok`` (input order, all tokens; written).
 
     ``side_stream`` (optional): the chunks of a step alternate between ``stream`` and this
     stream, so that the next chunk's blocks take the SMs the current chunk's last rows leave
@@ -124,10 +128,19 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
                 # side arrays stay whole; the kernel reads them through the token index
                 side = (target, old_logp, adv_tok, mask, loss_tok, logp_tok, tok_src[a:b], w_tok)
             tg, od, ad, mk, lt, lp, ts, wt = side
+            ct = None
+            if terms is not None or wt is not None:
+                ct = dict(terms or {})
+                if tok_src is None:  # the per-token arrays of the terms follow the chunk's slice
+                    for k in ("ref_logp", "entropy_tok"):
+                        if ct.get(k) is not None:
+                            ct[k] = ct[k][a:b]
+                if wt is not None:
+                    ct["w_tok"] = wt
             _lib.grpo_logprob_loss_fwd_bwd(
                 logits[a:b], tg, od, ad, mk, clip_eps, scale,
                 None if dlogits is None else dlogits[a:b], lt, lp, acc, tok_src=ts, V=V, stream=cs,
-                terms=None if wt is None else dict(w_tok=wt))
+                terms=ct)
             if launch_events is not None:
                 e1 = torch.cuda.Event(enable_timing=True)
                 e1.record(cs)

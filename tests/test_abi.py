@@ -39,3 +39,16 @@ def test_struct_sizes_match_header(grpo_lib):
     from rl_post_token_gb300 import _lib
     assert ctypes.sizeof(_lib.grpo_step_result) == 64
     assert _lib.ACC_BYTES == 128
+
+
+def test_binding_constants_match_header():
+    # every integer constant the binding names after a header #define has the header's value
+    from rl_post_token_gb300 import _lib
+    text = open(os.path.join(ROOT, "include", "grpo.h")).read()
+    defs = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define GRPO_(\w+)\s+\(?(-?\d+)\)?", text)}
+    named = [k for k in defs if isinstance(getattr(_lib, k, None), int)]
+    for k in named:
+        assert getattr(_lib, k) == defs[k], k
+    for k in ("OK", "STEP_SKIPPED_NONFINITE", "ERR_UNSUPPORTED", "DTYPE_BF16", "AGG_SEQ_MEAN_TOKEN_MEAN",
+              "KL_K1", "KL_K3"):
+        assert k in named, k

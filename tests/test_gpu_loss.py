@@ -592,6 +592,57 @@ def test_kl_and_entropy_terms(variant, kl_kind, ent):
     assert res["status"] == 0 and res["n_valid"] == int(wl.mask.sum())
 
 
+@pytest.mark.parametrize("kind", ["fixed", "dynamic"])
+def test_driver_loop_terms_equal_direct_calls_bitwise(kind):
+    # KL (k3) and the entropy bonus through the driver loop: a step's chunks alternate over two
+    # streams, and for token-budget bins the order is permuted (the terms' per-token arrays are
+    # then read through the token index). Every token's loss, log-prob, entropy and dlogits row
+    # equals one direct call per optimizer step over its tokens in input order, bit for bit.
+    if kind == "fixed":
+        wl = W.make_workload("tiny", rows=8, positions=24, valid_lo=0, V=32776, dtype="bf16", seed=93, std=2.0,
+                             mini=4, micro=2)
+    else:
+        wl = W.make_workload("dynamic", rows=16, len_hi=64, median=20, max_token_len=96, V=32776, seed=94)
+    case = H.Case(wl)
+    T = wl.T
+    ref = torch.from_numpy((case.old + np.random.default_rng(5).normal(0, 0.3, T)).astype(np.float32)).to(DEV)
+    bp = S.plan_batch(wl.plan, wl.row_len, wl.row_valid, wl.seg_counts)
+    assert bp.n_steps == (2 if kind == "fixed" else 1) and bp.plan["n_chunks"] >= 3
+    assert (bp.tok_src is None) == (kind == "fixed")
+    src = np.arange(bp.exec_tokens) if bp.tok_src is None else bp.tok_src
+    assert np.all(src >= 0)
+    lg = case.logits[torch.from_numpy(src).to(DEV)]  # exec order
+    dl = torch.empty_like(lg)
+    loss, logp, ent = (torch.full((T,), -7.0, device=DEV) for _ in range(3))
+    accs = torch.zeros(bp.n_steps * _lib.ACC_BYTES, dtype=torch.uint8, device=DEV)
+    terms = dict(kl_kind=_lib.KL_K3, kl_coef=0.1, ref_logp=ref, ent_coef=0.02, entropy_tok=ent)
+    S.run_batch(bp, logits=lg, dlogits=dl, target=case.d_target, old_logp=case.d_old, mask=case.d_mask,
+                adv_tok=case.d_adv, loss_tok=loss, logp_tok=logp, accs=accs, clip_eps=wl.eps,
+                tok_src=None if bp.tok_src is None else torch.from_numpy(bp.tok_src).to(DEV),
+                side_stream=torch.cuda.Stream(), terms=terms)
+    torch.cuda.synchronize()
+    res = S.read_results(accs, bp.n_steps)
+    back = torch.empty_like(dl)
+    back[torch.from_numpy(src).to(DEV)] = dl  # dlogits rows back to input order
+    for k in range(bp.n_steps):
+        t0, t1 = bp.step_tok_range[k]
+        N = int(bp.plan["step_valid_tokens"][k])
+        dl_k = torch.empty_like(case.logits[t0:t1])
+        loss_k, logp_k, ent_k = (torch.full((t1 - t0,), -7.0, device=DEV) for _ in range(3))
+        acc_k = _lib.new_step_acc(DEV)
+        _lib.grpo_logprob_loss_fwd_bwd(case.logits[t0:t1], case.d_target[t0:t1], case.d_old[t0:t1],
+                                       case.d_adv[t0:t1], case.d_mask[t0:t1], wl.eps, 1.0 / max(N, 1), dl_k,
+                                       loss_k, logp_k, acc_k,
+                                       terms=dict(terms, ref_logp=ref[t0:t1], entropy_tok=ent_k))
+        torch.cuda.synchronize()
+        for got, want in ((loss[t0:t1], loss_k), (logp[t0:t1], logp_k), (ent[t0:t1], ent_k)):
+            assert torch.equal(got.view(torch.int32), want.view(torch.int32)), k
+        assert torch.equal(back[t0:t1].view(torch.int16), dl_k.view(torch.int16)), k
+        direct = _lib.grpo_finish_step(acc_k, loss_k, expected_N=N)
+        for key in ("loss", "n_valid", "n_clipped", "n_nonfinite", "n_tokens", "status"):
+            assert res[k][key] == direct[key], (k, key)
+
+
 @pytest.mark.parametrize("variant", ["c2", "c4", "l2"], indirect=True)
 def test_entropy_with_masked_vocabulary(variant):
     # A tenth of every row's vocabulary is -inf (a masked vocabulary; never the target): those
