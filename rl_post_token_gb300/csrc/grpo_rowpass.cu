@@ -169,9 +169,10 @@ int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
   const int64_t V = a.V;
   const char* pin = getenv("GRPO_ROWPASS");
   const bool pin_l2 = pin && strcmp(pin, "l2") == 0;
-  // the entropy and per-token-weight instances carry more per-thread state: half-size chunks
-  // keep them in registers where the chunk count allows
-  constexpr bool HALF = ENT || TERMS == 2;
+  // the per-token-weight instances carry more per-thread state: half-size chunks keep them in
+  // registers where the chunk count allows (the entropy instances fold a chunk in 16-element
+  // blocks instead, and need half-size chunks only where two CTAs share an SM)
+  constexpr bool HALF = TERMS == 2;
   if (dtype == GRPO_DTYPE_BF16) {
     // Large bf16 vocabularies: rows split across a CTA cluster, slices staged in shared
     // memory. Variants (cluster size, consumer warps, vectors per thread, CTAs per SM):
@@ -181,7 +182,7 @@ int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
     if (vec && V % 8 == 0 && V >= 16384 && !pin_l2) {
       auto c34 = [&](auto c_tag) {
         constexpr int C = decltype(c_tag)::value;
-        if constexpr (HALF)
+        if constexpr (HALF || ENT)
           if (cluster_fits<B16>(V, C, 8, 2, 2)) return launch_cluster<B16, C, 8, 2, 2, ENT, TERMS>(a, st);
         return launch_cluster<B16, C, 8, 4, 2, ENT, TERMS>(a, st);
       };

@@ -654,9 +654,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
           float x[VPT * E];
 #pragma unroll
           for (int j = 0; j < VPT; ++j) unpack_at<T>(sv[ct + j * NC], x + E * j);
-          if (ENT)
-            lazy_online3<VPT * E>(acc3, x, guarded);
-          else
+          if (ENT) {
+            // blocks of at most 16: the pair sums of a whole 32-element chunk would not stay
+            // in registers
+            constexpr int EB = VPT * E < 16 ? VPT * E : 16;
+#pragma unroll
+            for (int h = 0; h < VPT * E / EB; ++h)
+              lazy_online3<EB>(acc3, *reinterpret_cast<const float(*)[EB]>(x + EB * h), guarded);
+          } else
             lazy_online2<VPT * E, PK>(acc, x);
         } else {
           for (int v = ct; v < nv; v += NC) {
