@@ -212,16 +212,31 @@ __device__ __forceinline__ void e_pairs(const float (&x)[N], float sh, float (&p
   }
 }
 
-// e_pairs without the no-mass guard: e * z is NaN only where a logit is -inf (or the row is
-// not finite at all), which the caller detects on the block sum.
+// Block sums (sum e, sum e*x) of N values without the no-mass guard, in packed two-lane
+// arithmetic: groups of four elements give lane j the elements 4g + j and 4g + 2 + j, the
+// groups are summed by a fixed pairwise tree, and the two lanes are added last. e * x is NaN
+// only where a logit is -inf (or the row is not finite at all), which the caller detects on
+// the block sum.
 template <int N>
-__device__ __forceinline__ void e_pairs_fast(const float (&x)[N], float sh, float (&pe)[N / 2], float (&px)[N / 2]) {
+__device__ __forceinline__ void e_sums_packed(const float (&x)[N], float sh, float& se, float& sx) {
+  static_assert(N % 4 == 0 && (((N / 4) & (N / 4 - 1)) == 0), "N / 4 a power of two");
+  float2 s[N / 4], p[N / 4];
 #pragma unroll
-  for (int i = 0; i < N / 2; ++i) {
-    const float2 e = ex2_pair(x[2 * i], x[2 * i + 1], sh);
-    pe[i] = e.x + e.y;
-    px[i] = fmaf(e.y, x[2 * i + 1], e.x * x[2 * i]);
+  for (int g = 0; g < N / 4; ++g) {
+    const float2 xa = make_float2(x[4 * g], x[4 * g + 1]), xb = make_float2(x[4 * g + 2], x[4 * g + 3]);
+    const float2 ea = ex2_pair(xa.x, xa.y, sh), eb = ex2_pair(xb.x, xb.y, sh);
+    s[g] = __fadd2_rn(ea, eb);
+    p[g] = __ffma2_rn(eb, xb, __fmul2_rn(ea, xa));
   }
+#pragma unroll
+  for (int w = N / 8; w >= 1; w /= 2)
+#pragma unroll
+    for (int g = 0; g < w; ++g) {
+      s[g] = __fadd2_rn(s[g], s[g + w]);
+      p[g] = __fadd2_rn(p[g], p[g + w]);
+    }
+  se = s[0].x + s[0].y;
+  sx = p[0].x + p[0].y;
 }
 
 // `guarded` is set when the block needed the no-mass guard (or the rescue path, which uses
@@ -230,10 +245,9 @@ template <int N>
 __device__ __forceinline__ void lazy_online3(MS3& acc, const float (&x)[N], bool& guarded) {
   if (acc.m == -INFINITY) acc.m = x[0] * kLog2e;
   float pe[N / 2], px[N / 2];
-  e_pairs_fast<N>(x, acc.m, pe, px);
-  const float bs = tree_sum(pe);
+  float bs, bx;
+  e_sums_packed<N>(x, acc.m, bs, bx);
   if (bs <= 1.8446744e19f) {
-    float bx = tree_sum(px);
     if (bx != bx) {  // a -inf logit in the block: redo it with no-mass elements adding nothing
       e_pairs<N>(x, acc.m, pe, px);
       bx = tree_sum(px);
