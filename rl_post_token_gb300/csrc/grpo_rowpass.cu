@@ -169,10 +169,11 @@ int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
   const int64_t V = a.V;
   const char* pin = getenv("GRPO_ROWPASS");
   const bool pin_l2 = pin && strcmp(pin, "l2") == 0;
-  // the per-token-weight instances carry more per-thread state: half-size chunks keep them in
-  // registers where the chunk count allows (the entropy instances fold a chunk in 16-element
-  // blocks instead, and need half-size chunks only where two CTAs share an SM)
-  constexpr bool HALF = TERMS == 2;
+  // the per-token-weight instance without the entropy carries more per-thread state than its
+  // 32 KB chunks leave registers for: half-size chunks where the chunk count allows (the
+  // entropy instances fold a chunk in 16-element blocks instead, and need half-size chunks only
+  // where two CTAs share an SM)
+  constexpr bool HALF = TERMS == 2 && !ENT;
   if (dtype == GRPO_DTYPE_BF16) {
     // Large bf16 vocabularies: rows split across a CTA cluster, slices staged in shared
     // memory. Variants (cluster size, consumer warps, vectors per thread, CTAs per SM):
