@@ -198,7 +198,11 @@ int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
         else return launch_cluster<B16, 2, 16, 4, 1, ENT, TERMS>(a, st);
       }
       if (cluster_fits<B16>(V, 4, 8, 2, 4)) return c34(C4{});
-      if (cluster_fits<B16>(V, 4, 16, 1, 4)) return launch_cluster<B16, 4, 16, 4, 1, ENT, TERMS>(a, st);
+      if (cluster_fits<B16>(V, 4, 16, 1, 4)) {
+        if constexpr (!ENT && TERMS == 0)
+          if (!a.dlogits && fwd_kernel_on()) return launch_fwd<B16, 4, 16, 4>(a, st);
+        return launch_cluster<B16, 4, 16, 4, 1, ENT, TERMS>(a, st);
+      }
     }
     if (V >= 8192) return launch_l2<B16, 1024, 2, ENT, TERMS>(a, vec, 1, st);
     return launch_l2<B16, 128, 2, ENT, TERMS>(a, vec, 16, st);

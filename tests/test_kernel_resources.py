@@ -60,7 +60,7 @@ def test_row_pass_default_instances_do_not_spill(grpo_lib):
 
 
 # the forward-only streaming instances (dtype, cluster, consumer warps, vectors per thread)
-FORWARD_ONLY = [("bf16", 2, 16, 4), ("f32", 4, 16, 4)]
+FORWARD_ONLY = [("bf16", 2, 16, 4), ("bf16", 4, 16, 4), ("f32", 4, 16, 4)]
 
 
 def test_forward_only_instances_do_not_spill(grpo_lib):
