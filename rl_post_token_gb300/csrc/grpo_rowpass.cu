@@ -169,11 +169,11 @@ int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
   const int64_t V = a.V;
   const char* pin = getenv("GRPO_ROWPASS");
   const bool pin_l2 = pin && strcmp(pin, "l2") == 0;
-  // the per-token-weight instance without the entropy carries more per-thread state than its
-  // 32 KB chunks leave registers for: half-size chunks where the chunk count allows (the
-  // entropy instances fold a chunk in 16-element blocks instead, and need half-size chunks only
-  // where two CTAs share an SM)
-  constexpr bool HALF = TERMS == 2 && !ENT;
+  // the instance with both the KL term and per-token weights (and no entropy) carries more
+  // per-thread state than its 32 KB chunks leave registers for: half-size chunks where the
+  // chunk count allows (the entropy instances fold a chunk in 16-element blocks instead, and
+  // need half-size chunks only where two CTAs share an SM)
+  constexpr bool HALF = TERMS == (kTermsReg | kTermsWeight) && !ENT;
   if (dtype == GRPO_DTYPE_BF16) {
     // Large bf16 vocabularies: rows split across a CTA cluster, slices staged in shared
     // memory. Variants (cluster size, consumer warps, vectors per thread, CTAs per SM):
@@ -201,6 +201,8 @@ int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
       if (cluster_fits<B16>(V, 4, 16, 1, 4)) {
         if constexpr (!ENT && TERMS == 0)
           if (!a.dlogits && fwd_kernel_on()) return launch_fwd<B16, 4, 16, 4>(a, st);
+        if constexpr (HALF)
+          if (cluster_fits<B16>(V, 4, 16, 1, 2)) return launch_cluster<B16, 4, 16, 2, 1, ENT, TERMS>(a, st);
         return launch_cluster<B16, 4, 16, 4, 1, ENT, TERMS>(a, st);
       }
     }
@@ -251,15 +253,17 @@ extern "C" GRPO_API int grpo_logprob_loss_fwd_bwd_ex(const void* logits, int32_t
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   const bool vec = al16(logits) && (ld * es) % 16 == 0 &&
                    (!dlogits || (al16(dlogits) && (ld_out * es) % 16 == 0));
-  // the entropy (as a loss term or as an output) needs sum_v p_v z_v, a third accumulator:
-  // a separate kernel instance
-  // (per-token weights get instances of their own: the extra per-row value would push the
-  // other instances past their register budget)
+  // Kernel instances by the work a call needs: the entropy (as a loss term or as an output)
+  // needs sum_v p_v z_v, a third accumulator; the KL term a reference log-prob per row; the
+  // aggregation weights a weight per row. Each instance carries only its own state, so none
+  // pays for the others' registers.
+  constexpr int R = kTermsReg, W = kTermsWeight;
   const bool wt = terms && terms->w_tok;
-  if (terms && (terms->ent_coef != 0.f || terms->entropy_tok))
-    return wt ? dispatch<true, 2>(a, dtype, vec, st) : dispatch<true, 1>(a, dtype, vec, st);
-  if (terms && (terms->kl_kind != GRPO_KL_NONE || wt))
-    return wt ? dispatch<false, 2>(a, dtype, vec, st) : dispatch<false, 1>(a, dtype, vec, st);
+  const bool ent = terms && (terms->ent_coef != 0.f || terms->entropy_tok);
+  const bool kl = terms && terms->kl_kind != GRPO_KL_NONE;
+  if (ent) return wt ? dispatch<true, R | W>(a, dtype, vec, st) : dispatch<true, R>(a, dtype, vec, st);
+  if (kl) return wt ? dispatch<false, R | W>(a, dtype, vec, st) : dispatch<false, R>(a, dtype, vec, st);
+  if (wt) return dispatch<false, W>(a, dtype, vec, st);
   return dispatch<false, 0>(a, dtype, vec, st);
 }
 

@@ -102,7 +102,10 @@ __device__ __forceinline__ int64_t row_src(const RowArgs& a, int64_t row) {
   return a.tok_src ? a.tok_src[row] : row;
 }
 
-// TERMS: 0 = no extra terms, 1 = KL/entropy terms, 2 = terms and per-token weights
+// TERMS is a set of kTerms* bits: the KL / entropy regularisers, the per-token weights.
+constexpr int kTermsReg = 1;
+constexpr int kTermsWeight = 2;
+
 template <int TERMS>
 __device__ __forceinline__ RowMeta row_meta(const RowArgs& a, int64_t src) {
   RowMeta m{src < 0 ? -1 : src, false, 0, 0.f, 0.f, 0.f, 1.f};
@@ -111,8 +114,8 @@ __device__ __forceinline__ RowMeta row_meta(const RowArgs& a, int64_t src) {
     m.y = a.target[src];
     m.A = a.adv[src];
     m.old = a.old_logp ? a.old_logp[src] : 0.f;
-    if (TERMS) m.ref = a.ref_logp ? a.ref_logp[src] : 0.f;
-    if (TERMS == 2) m.w = a.w_tok[src];
+    if (TERMS & kTermsReg) m.ref = a.ref_logp ? a.ref_logp[src] : 0.f;
+    if (TERMS & kTermsWeight) m.w = a.w_tok[src];
   }
   return m;
 }
@@ -188,7 +191,7 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
         if (tm.idx >= 0) {
           a.loss_tok[tm.idx] = 0.f;
           if (a.logp_tok) a.logp_tok[tm.idx] = 0.f;
-          if (TERMS && a.entropy_tok) a.entropy_tok[tm.idx] = 0.f;
+          if ((TERMS & kTermsReg) && a.entropy_tok) a.entropy_tok[tm.idx] = 0.f;
         }
       }
       continue;
@@ -270,13 +273,13 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
       }
       if (lane == 0) {
         const float lse = v.m + logf(v.s);
-        const float sc = TERMS == 2 ? a.scale * tm.w : a.scale;
+        const float sc = (TERMS & kTermsWeight) ? a.scale * tm.w : a.scale;
         TokenOut o = token_epilogue(ybad ? __int_as_float(0x7fc00000) : zy, lse,
                                     a.old_logp != nullptr, tm.old, tm.A, a.eps, sc);
-        if (TERMS) apply_terms(o, sc, a.kl_kind, a.kl_coef, tm.ref, a.ent_coef, lse - ez);
+        if (TERMS & kTermsReg) apply_terms(o, sc, a.kl_kind, a.kl_coef, tm.ref, a.ent_coef, lse - ez);
         a.loss_tok[tm.idx] = o.loss;
         if (a.logp_tok) a.logp_tok[tm.idx] = o.logp;
-        if (TERMS && a.entropy_tok) a.entropy_tok[tm.idx] = ENT ? lse - ez : 0.f;
+        if ((TERMS & kTermsReg) && a.entropy_tok) a.entropy_tok[tm.idx] = ENT ? lse - ez : 0.f;
         cnt.tokens++;
         cnt.valid++;
         cnt.clipped += o.clipped;
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
     __syncthreads();
     const float lse = sh_lse, coef = sh_coef;
     // entropy gradient: dz_v = p_v (ea + eb z_v) - coef [v == y]
-    const float eb = ENT ? (TERMS == 2 ? a.scale * tm.w : a.scale) * a.ent_coef : 0.f;
+    const float eb = ENT ? ((TERMS & kTermsWeight) ? a.scale * tm.w : a.scale) * a.ent_coef : 0.f;
     const float ea = ENT ? coef - eb * sh_ez : coef;
 
     // pass 2: dlogits = coef * (softmax - onehot)
@@ -538,9 +541,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
   constexpr int NC = NCW * 32;
   constexpr int E = vec_elems<T>();  // elements per 16-byte vector
   constexpr int WS = ENT ? 3 : 2;  // floats per warp partial
-  // packed two-lane arithmetic, except in the KL instance, whose 32 KB chunks leave no
-  // registers for the aligned pairs it needs
-  constexpr bool PK = !(TERMS == 1 && !ENT);
+  // packed two-lane arithmetic, except in the KL instances, whose 32 KB chunks leave no
+  // registers for the aligned pairs they need
+  constexpr bool PK = !((TERMS & kTermsReg) && !ENT);
   constexpr int CH = cluster_chunk_elems<T>(NCW, VPT);
   extern __shared__ __align__(128) uint8_t smem[];
   const int ring_bytes = (int)cluster_ring_bytes<T>(Vs, CH, S);
@@ -632,7 +635,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
           if (tm.idx >= 0) {
             a.loss_tok[tm.idx] = 0.f;
             if (a.logp_tok) a.logp_tok[tm.idx] = 0.f;
-            if (TERMS && a.entropy_tok) a.entropy_tok[tm.idx] = 0.f;
+            if ((TERMS & kTermsReg) && a.entropy_tok) a.entropy_tok[tm.idx] = 0.f;
           }
         }
         continue;
@@ -729,13 +732,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
       if (ENT) tot = MS{tot3.m, tot3.s};
       const float lse2 = tot.m + log2f(tot.s);  // log2(sum_v 2^(z_v log2 e)) = LSE * log2(e)
       const float ez = ENT ? tot3.s2 / tot3.s : 0.f;  // sum_v p_v z_v
-      const float sc = TERMS == 2 ? a.scale * tm.w : a.scale;
+      const float sc = (TERMS & kTermsWeight) ? a.scale * tm.w : a.scale;
       TokenOut o = token_epilogue(zy, lse2 * kLn2, a.old_logp != nullptr, tm.old, tm.A, a.eps, sc);
-      if (TERMS) apply_terms(o, sc, a.kl_kind, a.kl_coef, tm.ref, a.ent_coef, lse2 * kLn2 - ez);
+      if (TERMS & kTermsReg) apply_terms(o, sc, a.kl_kind, a.kl_coef, tm.ref, a.ent_coef, lse2 * kLn2 - ez);
       if (rank == 0 && ct == 0) {
         a.loss_tok[tm.idx] = o.loss;
         if (a.logp_tok) a.logp_tok[tm.idx] = o.logp;
-        if (TERMS && a.entropy_tok) a.entropy_tok[tm.idx] = ENT ? lse2 * kLn2 - ez : 0.f;
+        if ((TERMS & kTermsReg) && a.entropy_tok) a.entropy_tok[tm.idx] = ENT ? lse2 * kLn2 - ez : 0.f;
         cnt.tokens++;
         cnt.valid++;
         cnt.clipped += o.clipped;
