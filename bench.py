@@ -217,7 +217,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[args.workload], "parallelism": "rank 0 only"},
-        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "host_cpus": os.cpu_count(), "kind": "oracle",
                          "sample": f"float64 numpy oracle, first 16 tokens of a host-drawn batch of the "
                                    f"workload, {per_step_s}s per step"},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -530,7 +530,7 @@ def run_gb300(args):
         line["clocks"] = clk
     if rank == 0 and not args.no_cpu_baseline:
         v, n, dt = oracle_sample_rate(wl, 16, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "host_cpus": os.cpu_count(), "kind": "oracle",
                                 "sample": f"float64 numpy oracle (one thread) on {n} valid tokens "
                                           f"({dt:.1f} s) of a host-drawn sample of the workload"}
     if rank == 0:
