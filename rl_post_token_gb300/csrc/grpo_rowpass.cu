@@ -18,7 +18,7 @@ size_t max_smem_optin();
 // ever rises (a concurrent launch with a larger slice never finds it lowered under it), and
 // the co-resident cluster count is cached per shared-memory size.
 template <auto KERN>
-int launch_clusters(const RowArgs& a, int C, int NCW, size_t smem, int Vs, int S, cudaStream_t st) {
+int launch_clusters(const RowArgs& a, int C, int threads, size_t smem, int Vs, int S, cudaStream_t st) {
   int dev = 0;
   GRPO_CUDA_TRY(cudaGetDevice(&dev));
   cudaLaunchConfig_t cfg = {};
@@ -27,7 +27,7 @@ int launch_clusters(const RowArgs& a, int C, int NCW, size_t smem, int Vs, int S
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3((NCW + 1) * 32, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
@@ -86,7 +86,8 @@ int launch_cluster(const RowArgs& a, cudaStream_t st) {
     else if (n > nchm && n <= s_fit) S = n;
   }
   const size_t smem = cluster_ring_bytes<T>(Vs, CH, S) + cluster_tail_bytes(NCW);
-  return launch_clusters<row_cluster_kernel<T, C, NCW, VPT, MINB, ENT, TERMS>>(a, C, NCW, smem, Vs, S, st);
+  return launch_clusters<row_cluster_kernel<T, C, NCW, VPT, MINB, ENT, TERMS>>(a, C, (NCW + 1) * 32, smem, Vs, S,
+                                                                               st);
 }
 
 // The forward-only streaming kernel: as many ring slots as the opt-in shared memory holds (at
@@ -106,7 +107,7 @@ int launch_fwd(const RowArgs& a, cudaStream_t st) {
     S = n < 2 ? 2 : std::min(n, s_fit);
   }
   const size_t smem = (size_t)S * CH * sizeof(T) + tail;
-  return launch_clusters<row_fwd_kernel<T, C, NCW, VPT>>(a, C, NCW, smem, Vs, S, st);
+  return launch_clusters<row_fwd_kernel<T, C, NCW, VPT>>(a, C, fwd_block_threads(NCW), smem, Vs, S, st);
 }
 
 template <typename T, int NT, int U, bool ENT, int TERMS>

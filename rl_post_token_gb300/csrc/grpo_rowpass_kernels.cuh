@@ -808,16 +808,17 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
 // Forward-only cluster kernel (no dlogits, no extra terms): the pi_old ahead pass. It splits
 // rows, chunks them and assigns elements to threads exactly as row_cluster_kernel<T, C, NCW,
 // VPT> does, and combines the partial sums in the same order, so the log-prob, the loss and
-// the counts are the same bits. What differs is that no thread waits for a row's exchange:
+// the counts are the same bits. What differs is that no consumer waits for a row's exchange:
 //  * each consumer warp releases a chunk's slot as soon as it has folded the chunk in, and the
 //    producer streams the cluster's rows through the ring with no per-row barrier;
-//  * each warp sends its (shift, sum) straight into CTA 0's exchange buffer with an
+//  * each consumer warp sends its (shift, sum) straight into CTA 0's exchange buffer with an
 //    asynchronous DSMEM store that completes on CTA 0's mbarrier, and goes on to the next row
 //    without a fence;
-//  * one warp of CTA 0, rotating with the row, combines a row's C * NCW partials one row later
-//    (warps in order within a CTA, then CTAs in rank order) and writes the token's outputs.
-// kFwdBufs exchange buffers, each handed back by its combiner through an mbarrier in every
-// CTA, bound how far a warp can run ahead of the combines.
+//  * a combiner warp of CTA 0 (the block's last warp) takes the rows in order, combines each
+//    row's C * NCW partials (warps in order within a CTA, then CTAs in rank order) and writes
+//    the token's outputs; it also writes the outputs of masked and padding rows.
+// kFwdBufs exchange buffers, each handed back by the combiner through an mbarrier in every
+// CTA, bound how far a consumer can run ahead of the combines.
 // ------------------------------------------------------------------------------------------
 constexpr int kFwdBufs = 4;
 
@@ -825,6 +826,9 @@ __host__ __device__ constexpr size_t fwd_tail_bytes(int C, int NCW) {
   return (2 * kMaxChunks + 2 * kFwdBufs) * sizeof(uint64_t) + (size_t)kFwdBufs * C * NCW * 2 * sizeof(float) +
          kFwdBufs * sizeof(float) + 16;
 }
+
+// Threads per block of the forward-only kernel: producer, NCW consumers, combiner.
+__host__ __device__ constexpr int fwd_block_threads(int NCW) { return (NCW + 2) * 32; }
 
 // First row at or after `from` (stepping by `stride`) that is read, examining 32 rows at once;
 // every lane of the warp calls it and gets the same answer.
@@ -843,7 +847,7 @@ __device__ __forceinline__ int64_t scan_read_row(const RowArgs& a, int64_t from,
 }
 
 template <typename T, int C, int NCW, int VPT>
-__global__ void __launch_bounds__((NCW + 1) * 32, 1) row_fwd_kernel(RowArgs a, int Vs, int S) {
+__global__ void __launch_bounds__(fwd_block_threads(NCW), 1) row_fwd_kernel(RowArgs a, int Vs, int S) {
   constexpr int NC = NCW * 32;
   constexpr int E = vec_elems<T>();
   constexpr int CH = cluster_chunk_elems<T>(NCW, VPT);
@@ -915,70 +919,20 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) row_fwd_kernel(RowArgs a, i
       const unsigned bal = __ballot_sync(0xffffffffu, ok);
       cur = bal ? cur + (int64_t)__ffs(bal) * ncl : scan_read_row(a, cur + 33 * ncl, ncl, lane);
     }
-  } else {
+  } else if (warp <= NCW) {
     // ---- consumers ----
     const int ct = tid - 32, cw = warp - 1;
     RingCursor rc{0, 0u};
     uint32_t xi = 0;  // read rows so far: the exchange sequence number
-    RowMeta pend{};   // the previous read row, combined one row late
     MetaPipe<0> pipe(a, cid, ncl);
-
-    // CTA 0, warp xi % NCW: the row's log-sum-exp from its partials, then the token's outputs
-    auto combine = [&](uint32_t i, const RowMeta& tm) {
-      const uint32_t b = i % kFwdBufs, u = i / kFwdBufs;
-      const bool ybad = tm.y < 0 || (int64_t)tm.y >= V;
-      // the phase completes once every warp's partial (and the target logit) has landed;
-      // phase u-1 is complete already: this warp's own store for row i waited for its reader
-      if (lane == 0) mbar_arrive_expect_tx_relaxed(&xfull[b], NP * 8u + (ybad ? 0u : 4u));
-      mbar_wait_cluster_bounded(&xfull[b], u & 1u, s_abort);
-      MS t{-INFINITY, 0.f};
-      if (lane < C)
-        for (int j = 0; j < NCW; ++j) {
-          const float* p = part + 2 * (b * NP + lane * NCW + j);
-          t = ms2_combine(t, MS{p[0], p[1]});
-        }
-      const float zy = ybad ? __int_as_float(0x7fc00000) : zyv[b];
-      MS tot{-INFINITY, 0.f};
-#pragma unroll
-      for (int r = 0; r < C; ++r)
-        tot = ms2_combine(tot, MS{__shfl_sync(0xffffffffu, t.m, r), __shfl_sync(0xffffffffu, t.s, r)});
-      __syncwarp();
-      if (lane == 0) {
-        const float lse2 = tot.m + log2f(tot.s);
-        const TokenOut o = token_epilogue(zy, lse2 * kLn2, a.old_logp != nullptr, tm.old, tm.A, a.eps, a.scale);
-        // the buffer is free again in every CTA: what was read from it has been consumed
-        // (by the shuffles and the epilogue), so the signal needs no fence
-        for (int r = 0; r < C; ++r) mbar_arrive_remote_relaxed(mapa_u32(smem_u32(&xempty[b]), (uint32_t)r));
-        a.loss_tok[tm.idx] = o.loss;
-        if (a.logp_tok) a.logp_tok[tm.idx] = o.logp;
-        cnt.tokens++;
-        cnt.valid++;
-        cnt.clipped += o.clipped;
-        cnt.nonfinite += o.nonfinite;
-      }
-    };
-
     for (int64_t row = cid; row < a.T; row += ncl) {
       // the row's metadata: lane 0 keeps the prefetch pipeline and broadcasts, so lane 31,
       // which releases the ring slots, has no global load in flight for its release to wait on
       RowMeta tm{};
       if (lane == 0) tm = pipe.advance(row);
-      tm.idx = __shfl_sync(0xffffffffu, tm.idx, 0);
       tm.valid = __shfl_sync(0xffffffffu, (int)tm.valid, 0) != 0;
       tm.y = __shfl_sync(0xffffffffu, tm.y, 0);
-      tm.A = __shfl_sync(0xffffffffu, tm.A, 0);
-      tm.old = __shfl_sync(0xffffffffu, tm.old, 0);
-      if (!tm.valid) {
-        // masked or padding row: nothing read, nothing exchanged
-        if (rank == 0 && ct == 0) {
-          cnt.tokens++;
-          if (tm.idx >= 0) {
-            a.loss_tok[tm.idx] = 0.f;
-            if (a.logp_tok) a.logp_tok[tm.idx] = 0.f;
-          }
-        }
-        continue;
-      }
+      if (!tm.valid) continue;  // masked or padding row: nothing read, nothing exchanged
       // where the target logit sits in this CTA's slice, and which thread reads it
       const int64_t yo = (tm.y < 0 || (int64_t)tm.y >= V) ? -1 : (int64_t)tm.y - base;
       const bool own = yo >= 0 && yo < n_r;
@@ -1022,11 +976,59 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) row_fwd_kernel(RowArgs a, i
         st_async_v2f32(mapa_u32(smem_u32(part + 2 * (b * NP + rank * NCW + cw)), 0u), w.m, w.s, bar);
         if (wown) st_async_f32(mapa_u32(smem_u32(zyv + b), 0u), zy, bar);
       }
-      if (rank == 0 && xi > 0 && (xi - 1u) % NCW == (uint32_t)cw) combine(xi - 1u, pend);
-      pend = tm;
       ++xi;
     }
-    if (rank == 0 && xi > 0 && (xi - 1u) % NCW == (uint32_t)cw) combine(xi - 1u, pend);
+  } else if (rank == 0) {
+    // ---- combiner (CTA 0): every row of the cluster in order; the read rows' log-sum-exp
+    // from their partials, then the token's outputs ----
+    uint32_t xi = 0;
+    MetaPipe<0> pipe(a, cid, ncl);
+    for (int64_t row = cid; row < a.T; row += ncl) {
+      const RowMeta tm = pipe.advance(row);
+      if (!tm.valid) {
+        if (lane == 0) {
+          cnt.tokens++;
+          if (tm.idx >= 0) {
+            a.loss_tok[tm.idx] = 0.f;
+            if (a.logp_tok) a.logp_tok[tm.idx] = 0.f;
+          }
+        }
+        continue;
+      }
+      const uint32_t b = xi % kFwdBufs, u = xi / kFwdBufs;
+      const bool ybad = tm.y < 0 || (int64_t)tm.y >= V;
+      // the phase completes once every warp's partial (and the target logit) has landed.
+      // Phase u-1 is complete: this warp waited for it four read rows ago, and no store of
+      // this row is issued before the buffer's release that followed that wait.
+      if (lane == 0) mbar_arrive_expect_tx_relaxed(&xfull[b], NP * 8u + (ybad ? 0u : 4u));
+      mbar_wait_cluster_bounded(&xfull[b], u & 1u, s_abort);
+      MS t{-INFINITY, 0.f};
+      if (lane < C)
+        for (int j = 0; j < NCW; ++j) {
+          const float* p = part + 2 * (b * NP + lane * NCW + j);
+          t = ms2_combine(t, MS{p[0], p[1]});
+        }
+      const float zy = ybad ? __int_as_float(0x7fc00000) : zyv[b];
+      MS tot{-INFINITY, 0.f};
+#pragma unroll
+      for (int r = 0; r < C; ++r)
+        tot = ms2_combine(tot, MS{__shfl_sync(0xffffffffu, t.m, r), __shfl_sync(0xffffffffu, t.s, r)});
+      __syncwarp();
+      if (lane == 0) {
+        const float lse2 = tot.m + log2f(tot.s);
+        const TokenOut o = token_epilogue(zy, lse2 * kLn2, a.old_logp != nullptr, tm.old, tm.A, a.eps, a.scale);
+        // the buffer is free again in every CTA: what was read from it has been consumed
+        // (by the shuffles and the epilogue), so the signal needs no fence
+        for (int r = 0; r < C; ++r) mbar_arrive_remote_relaxed(mapa_u32(smem_u32(&xempty[b]), (uint32_t)r));
+        a.loss_tok[tm.idx] = o.loss;
+        if (a.logp_tok) a.logp_tok[tm.idx] = o.logp;
+        cnt.tokens++;
+        cnt.valid++;
+        cnt.clipped += o.clipped;
+        cnt.nonfinite += o.nonfinite;
+      }
+      ++xi;
+    }
   }
 
   __syncthreads();
@@ -1037,7 +1039,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) row_fwd_kernel(RowArgs a, i
     if (tid == 0) atomicOr(&a.acc->flags, kFlagWaitTimeout);
   }
   cluster_sync_all();  // no CTA leaves while a peer may still store into or arrive on its memory
-  if (rank == 0 && warp > 0 && lane == 0) cnt.flush(a.acc);
+  if (rank == 0 && warp == NCW + 1 && lane == 0) cnt.flush(a.acc);
 }
 
 }  // namespace grpo
