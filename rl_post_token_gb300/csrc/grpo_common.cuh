@@ -76,6 +76,18 @@ __device__ __forceinline__ MS warp_ms2(MS v) {
   return v;
 }
 
+// The partials of each W-lane group of the warp (W a power of two, at most 32) combined by a
+// fixed pairwise tree: lane g*W ends with group g's result, the same bits wherever the group
+// sits in the warp.
+template <int W>
+__device__ __forceinline__ MS group_tree_ms2(MS v) {
+  static_assert(W >= 1 && W <= 32 && (W & (W - 1)) == 0, "power of two");
+#pragma unroll
+  for (int o = W / 2; o > 0; o >>= 1)
+    v = ms2_combine(v, MS{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o)});
+  return v;
+}
+
 // Fold N more values into a log2-domain online pair (one rescale per call).
 // Pairwise (tree) reductions of a register array: log2(N) dependent steps instead of N, so
 // a thread's block of exponentials never waits on one long add chain. The order is fixed.
@@ -196,6 +208,16 @@ __device__ __forceinline__ MS3 warp_ms3(MS3 v) {
           __shfl_xor_sync(0xffffffffu, v.s2, o)};
     v = LOG2 ? ms3_combine2(v, w) : ms3_combine(v, w);
   }
+  return v;
+}
+
+template <int W>
+__device__ __forceinline__ MS3 group_tree_ms3(MS3 v) {
+  static_assert(W >= 1 && W <= 32 && (W & (W - 1)) == 0, "power of two");
+#pragma unroll
+  for (int o = W / 2; o > 0; o >>= 1)
+    v = ms3_combine2(v, MS3{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o),
+                            __shfl_xor_sync(0xffffffffu, v.s2, o)});
   return v;
 }
 

@@ -693,23 +693,27 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
         }
       }
       named_bar_sync(1, NC);
-      if (warp == 1 && lane == 0) {
+      if (warp == 1) {
+        // the CTA's NCW warp partials combined by a fixed pairwise tree across warp 1's lanes
         MS3 t{-INFINITY, 0.f, 0.f};
         if (ENT) {
-          for (int i = 0; i < NCW; ++i) t = ms3_combine2(t, MS3{wpart[WS * i], wpart[WS * i + 1], wpart[WS * i + 2]});
+          t = group_tree_ms3<NCW>(lane < NCW ? MS3{wpart[WS * lane], wpart[WS * lane + 1], wpart[WS * lane + 2]}
+                                             : MS3{-INFINITY, 0.f, 0.f});
         } else {
-          MS t2{-INFINITY, 0.f};
-          for (int i = 0; i < NCW; ++i) t2 = ms2_combine(t2, MS{wpart[WS * i], wpart[WS * i + 1]});
+          const MS t2 = group_tree_ms2<NCW>(lane < NCW ? MS{wpart[WS * lane], wpart[WS * lane + 1]}
+                                                       : MS{-INFINITY, 0.f});
           t = MS3{t2.m, t2.s, 0.f};
         }
-        xb[0] = t.m;
-        xb[1] = t.s;
-        if (ENT) xb[3] = t.s2;
-        if (!ybad && (int64_t)y >= base && (int64_t)y < base + n_r) {
-          const int off = (int)((int64_t)y - base), k = off / CH;
-          RingCursor cy = rc;
-          cy.skip(k, SL);
-          xb[2] = Vec<T>::load1(ring + (size_t)cy.slot * CH + (off - k * CH));
+        if (lane == 0) {
+          xb[0] = t.m;
+          xb[1] = t.s;
+          if (ENT) xb[3] = t.s2;
+          if (!ybad && (int64_t)y >= base && (int64_t)y < base + n_r) {
+            const int off = (int)((int64_t)y - base), k = off / CH;
+            RingCursor cy = rc;
+            cy.skip(k, SL);
+            xb[2] = Vec<T>::load1(ring + (size_t)cy.slot * CH + (off - k * CH));
+          }
         }
       }
       cluster_sync_all();
@@ -1002,17 +1006,25 @@ __global__ void __launch_bounds__(fwd_block_threads(NCW), 1) row_fwd_kernel(RowA
       // this row is issued before the buffer's release that followed that wait.
       if (lane == 0) mbar_arrive_expect_tx_relaxed(&xfull[b], NP * 8u + (ybad ? 0u : 4u));
       mbar_wait_cluster_bounded(&xfull[b], u & 1u, s_abort);
-      MS t{-INFINITY, 0.f};
-      if (lane < C)
-        for (int j = 0; j < NCW; ++j) {
-          const float* p = part + 2 * (b * NP + lane * NCW + j);
-          t = ms2_combine(t, MS{p[0], p[1]});
-        }
-      const float zy = ybad ? __int_as_float(0x7fc00000) : zyv[b];
+      // each CTA's NCW partials by the general kernel's pairwise tree (32 / NCW CTAs at a time,
+      // one per NCW-lane group), then the CTAs in rank order
+      constexpr int G = 32 / NCW;
       MS tot{-INFINITY, 0.f};
 #pragma unroll
-      for (int r = 0; r < C; ++r)
-        tot = ms2_combine(tot, MS{__shfl_sync(0xffffffffu, t.m, r), __shfl_sync(0xffffffffu, t.s, r)});
+      for (int r0 = 0; r0 < C; r0 += G) {
+        const int r = r0 + lane / NCW;
+        MS v{-INFINITY, 0.f};
+        if (r < C) {
+          const float* p = part + 2 * (b * NP + r * NCW + lane % NCW);
+          v = MS{p[0], p[1]};
+        }
+        v = group_tree_ms2<NCW>(v);
+#pragma unroll
+        for (int k = 0; k < G; ++k)
+          if (r0 + k < C)
+            tot = ms2_combine(tot, MS{__shfl_sync(0xffffffffu, v.m, k * NCW), __shfl_sync(0xffffffffu, v.s, k * NCW)});
+      }
+      const float zy = ybad ? __int_as_float(0x7fc00000) : zyv[b];
       __syncwarp();
       if (lane == 0) {
         const float lse2 = tot.m + log2f(tot.s);
