@@ -4,7 +4,9 @@ every row:
 * sampled rows: per-token loss and log-prob, and the whole dlogits row, against the float64
   oracle with the per-token and dlogits bars of the smaller parity tests;
 * every row: finite dlogits; each valid row's dlogits sum to ~0 (softmax and one-hot both sum
-  to one); masked and padding rows exactly zero; per-step N equals the planner's N.
+  to one); masked and padding rows exactly zero; per-step N equals the planner's N;
+* the forward-only pass over the same batch: every token's loss and log-prob the bits of the
+  full pass.
 
 pi_old here is target logit - 12 + N(0, 0.05): a plain input recipe (no log-softmax) that puts
 the ratio far below 1, so tokens with A < 0 take the clipped branch and tokens with A > 0 the
@@ -61,6 +63,22 @@ def test_full_size_batch(name):
     res = S.read_results(accs, bp.n_steps)
     for s, r in enumerate(res):
         assert r["status"] == 0 and r["n_valid"] == bp.plan["step_valid_tokens"][s]
+
+    # the same batch forward only (the pi_old ahead pass, on its own streaming kernel): every
+    # token's loss and log-prob, and every step's result, are the bits of the full pass
+    loss_f = torch.full((T,), -7.0, device=DEV)
+    logp_f = torch.full((T,), -7.0, device=DEV)
+    accs_f = torch.zeros_like(accs)
+    S.run_batch(bp, logits=logits, dlogits=None, target=t(wl.target), old_logp=t(old), mask=t(wl.mask),
+                adv_tok=t(adv), loss_tok=loss_f, logp_tok=logp_f, accs=accs_f, clip_eps=wl.eps,
+                tok_src=None if tok_src is None else t(tok_src), V=wl.V)
+    torch.cuda.synchronize()
+    assert torch.equal(loss_f.view(torch.int32), loss.view(torch.int32))
+    assert torch.equal(logp_f.view(torch.int32), logp.view(torch.int32))
+    res_f = S.read_results(accs_f, bp.n_steps)
+    for a, b in zip(res_f, res):
+        for k in ("loss", "n_valid", "n_clipped", "n_nonfinite", "n_tokens", "status"):
+            assert a[k] == b[k], k
 
     # sampled exec rows: the first and last of every chunk plus a seeded handful
     rng = np.random.default_rng(2)
