@@ -434,6 +434,16 @@ GRPO_API const char* grpo_status_string(int status);
 /* Library version, major * 10000 + minor * 100 + patch. */
 GRPO_API int grpo_version(void);
 
+/* Self-test of the bounded waits every pipelined kernel of this library relies on (no page
+ * defines it). Launches one CTA on `stream` that waits on an mbarrier nothing completes. The wait
+ * gives up after its limit, the same one the row-pass and LM-head kernels use: about one
+ * second, or 2^24 polls if those end sooner. The kernel then raises the wait-timeout bit of
+ * acc->flags, as a kernel whose pipeline broke would. The next grpo_finish_step on `acc`
+ * reports GRPO_ERR_KERNEL and zeroes the gradient buffers it is given.
+ * `acc`: device pointer to a caller-owned accumulator. Returns GRPO_ERR_INVALID for a NULL
+ * `acc`, GRPO_ERR_CUDA if the launch fails, else GRPO_OK (asynchronous). */
+GRPO_API int grpo_selftest_wait_timeout(grpo_step_acc* acc, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

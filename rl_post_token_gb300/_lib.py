@@ -146,8 +146,9 @@ def _lib() -> C.CDLL:
     lib.grpo_status_string.argtypes = [C.c_int]
     lib.grpo_status_string.restype = C.c_char_p
     lib.grpo_version.argtypes = []
+    lib.grpo_selftest_wait_timeout.argtypes = [vp, vp]
     for f in ("grpo_plan_microbatches", "grpo_plan_token_index", "grpo_group_advantage",
-              "grpo_logprob_loss_fwd_bwd", "grpo_finish_step", "grpo_version"):
+              "grpo_logprob_loss_fwd_bwd", "grpo_finish_step", "grpo_version", "grpo_selftest_wait_timeout"):
         getattr(lib, f).restype = C.c_int
     _LIB = lib
     return lib
@@ -456,3 +457,11 @@ def read_step_result(acc) -> dict:
 
 def grpo_version() -> int:
     return _lib().grpo_version()
+
+
+def grpo_selftest_wait_timeout(acc, stream=None) -> None:
+    """One bounded wait that nothing completes: sets acc's wait-timeout flag after about a
+    second (see grpo.h); the next grpo_finish_step on acc reports ERR_KERNEL."""
+    rc = _lib().grpo_selftest_wait_timeout(_ptr(acc), _stream(stream))
+    if rc != OK:
+        raise GrpoError(rc, "grpo_selftest_wait_timeout")

@@ -166,9 +166,30 @@ __global__ void grad_finish_kernel(T* __restrict__ g, int64_t n, const grpo_step
   }
 }
 
+// One bounded wait that nothing completes: the barrier's first phase never ends, so the wait
+// gives up at its limit and the kernel raises the wait-timeout flag, as a pipelined kernel
+// whose producer or peer stopped would.
+__global__ void wait_timeout_selftest_kernel(grpo_step_acc* acc) {
+  __shared__ uint64_t bar;
+  __shared__ int s_abort;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    s_abort = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait_bounded(&bar, 0u, &s_abort)) atomicOr(&acc->flags, kFlagWaitTimeout);
+}
+
 }  // namespace grpo
 
 using namespace grpo;
+
+extern "C" GRPO_API int grpo_selftest_wait_timeout(grpo_step_acc* acc, void* stream) {
+  if (!acc) return GRPO_ERR_INVALID;
+  wait_timeout_selftest_kernel<<<1, 32, 0, as_stream(stream)>>>(acc);
+  GRPO_CUDA_TRY(cudaGetLastError());
+  return GRPO_OK;
+}
 
 extern "C" GRPO_API int grpo_group_advantage(const float* rewards, int32_t n_rollouts,
                                              int32_t group_size, float eps,

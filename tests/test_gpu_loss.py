@@ -763,3 +763,25 @@ def test_two_stream_chunks_bitwise():
         outs.append((dl.view(torch.int16).clone(), loss.clone(), S.read_results(accs, bp.n_steps)))
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
     assert outs[0][2] == outs[1][2]
+
+
+def test_bounded_wait_gives_up_and_the_step_reports_it():
+    # The bounded waits every pipelined kernel relies on: a wait that nothing completes gives
+    # up at its limit (about a second) instead of hanging, raises the wait-timeout flag, the
+    # step finish reports ERR_KERNEL and zeroes the gradients, and the context stays usable.
+    import time
+    wl = W.make_workload("tiny", rows=4, positions=8, valid_lo=0, V=16384, dtype="bf16", seed=71, std=2.0)
+    case = H.Case(wl)
+    dl, loss, logp, acc = _run_direct(case, 0.5)
+    t0 = time.perf_counter()
+    _lib.grpo_selftest_wait_timeout(acc)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 10.0
+    res = _lib.grpo_finish_step(acc, loss, grad_bufs=[dl])
+    assert res["status"] == _lib.ERR_KERNEL and res["kernel_flags"] == 1
+    assert torch.all(dl == 0)
+    # the flag was consumed by the finish, and the device still runs the path normally
+    dl2, loss2, logp2, acc2 = _run_direct(case, 0.5)
+    res2 = _lib.grpo_finish_step(acc2, loss2, grad_bufs=[dl2])
+    assert res2["status"] == 0 and res2["kernel_flags"] == 0
+    assert torch.equal(loss2, loss) and torch.equal(logp2, logp)
