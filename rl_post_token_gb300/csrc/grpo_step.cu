@@ -280,7 +280,7 @@ extern "C" GRPO_API const char* grpo_status_string(int status) {
   }
 }
 
-extern "C" GRPO_API int grpo_version(void) { return 101; }
+extern "C" GRPO_API int grpo_version(void) { return 200; }
 
 static_assert(sizeof(grpo_step_result) == 64, "grpo_step_result is 64 bytes");
 static_assert(sizeof(grpo_step_acc) == 128, "grpo_step_acc is 128 bytes");
