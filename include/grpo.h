@@ -286,6 +286,36 @@ GRPO_API int grpo_logprob_loss_fwd_bwd_ex(const void* logits, int32_t dtype, int
                                           const grpo_loss_terms* terms, grpo_step_acc* acc,
                                           void* stream);
 
+/* grpo_logprob_loss_fwd_bwd_ex over logits that live in HOST memory (the page's problem: the
+ * [T, V] logits of a step are many gigabytes; this streams them through a small device
+ * buffer). Row t of the call is host row t (`ld` elements apart, `dtype` as above); every
+ * other argument (side arrays, dlogits, outputs, terms, acc) is as in
+ * grpo_logprob_loss_fwd_bwd_ex, on the device.
+ * The rows go up in blocks of `block_rows`:
+ *  - each block is copied into one half of `staging` on `copy_stream` (one cudaMemcpyAsync);
+ *  - its row pass runs on `stream` once that copy has landed;
+ *  - the next block's copy goes into the other half, so copy and row pass overlap.
+ * The results are the bits grpo_logprob_loss_fwd_bwd_ex gives on the same rows in device
+ * memory: a row's arithmetic does not depend on how the rows are split.
+ * `staging`: device, 16-byte aligned, at least 2 * block_rows * ld * element-size bytes,
+ * caller-owned. `logits_host`: pinned memory gives the link's full rate; pageable memory
+ * works at a lower one. `copy_stream` may equal `stream` (no overlap).
+ * Asynchronous: the first copy waits for the work already on `stream`, which may still read
+ * `staging`. When `stream` has finished, all of the call's copies have too, and the host rows
+ * may be reused.
+ * Errors: as grpo_logprob_loss_fwd_bwd_ex; GRPO_ERR_INVALID also for a NULL host or staging
+ * pointer, block_rows < 1 or misaligned staging; GRPO_ERR_CUDA for a failed copy or event call.
+ * On an error after some blocks were enqueued, those blocks' work stays enqueued. */
+GRPO_API int grpo_logprob_loss_fwd_bwd_host(const void* logits_host, int32_t dtype, int64_t T, int64_t V,
+                                            int64_t ld, const int64_t* tok_src,
+                                            const int32_t* target, const float* old_logp,
+                                            const float* adv_tok, const uint8_t* mask,
+                                            float clip_eps, float grad_scale, void* dlogits,
+                                            int64_t ld_out, float* loss_tok, float* logp_tok,
+                                            const grpo_loss_terms* terms, grpo_step_acc* acc,
+                                            void* staging, int64_t block_rows, void* stream,
+                                            void* copy_stream);
+
 /* ---- step finish ------------------------------------------------------------------------- */
 
 /* Close one optimizer step ("Sizing mini-batches and micro-batches", "The hard part:

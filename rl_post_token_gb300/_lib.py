@@ -117,6 +117,10 @@ def _lib() -> C.CDLL:
                                                  vp, vp, vp, C.c_float, C.c_float, vp, C.c_int64, vp, vp,
                                                  C.POINTER(grpo_loss_terms), vp, vp]
     lib.grpo_logprob_loss_fwd_bwd_ex.restype = C.c_int
+    lib.grpo_logprob_loss_fwd_bwd_host.argtypes = [vp, C.c_int32, C.c_int64, C.c_int64, C.c_int64, vp, vp,
+                                                   vp, vp, vp, C.c_float, C.c_float, vp, C.c_int64, vp, vp,
+                                                   C.POINTER(grpo_loss_terms), vp, vp, C.c_int64, vp, vp]
+    lib.grpo_logprob_loss_fwd_bwd_host.restype = C.c_int
     lib.grpo_finish_step.argtypes = [vp, vp, C.c_int64, C.c_int64, C.c_int32, C.POINTER(vp), _i64p,
                                      _i32p, C.c_int32, C.POINTER(grpo_step_result), vp]
     lib.grpo_finish_step_ex.argtypes = [vp, vp, C.c_int64, vp, C.c_int64, C.c_int64, C.c_int32, C.POINTER(vp),
@@ -329,6 +333,44 @@ def grpo_logprob_loss_fwd_bwd(logits, target, old_logp, adv_tok, mask, clip_eps:
                                                  _ptr(logp_tok), C.byref(tm), _ptr(acc), _stream(stream))
     if rc != OK:
         raise GrpoError(rc, "grpo_logprob_loss_fwd_bwd")
+
+
+def grpo_logprob_loss_fwd_bwd_host(logits_host, target, old_logp, adv_tok, mask, clip_eps: float,
+                                   grad_scale: float, dlogits, loss_tok, logp_tok, acc, staging,
+                                   block_rows: int, tok_src=None, V: Optional[int] = None, stream=None,
+                                   copy_stream=None, terms: Optional[dict] = None) -> None:
+    """logits_host [T, ld] (float32 or bfloat16) in host memory (pinned for the link's full
+    rate), streamed through ``staging`` (a device uint8 tensor of at least
+    2 * block_rows * ld * element-size bytes) in blocks of ``block_rows``; the rest as
+    grpo_logprob_loss_fwd_bwd. See grpo.h."""
+    import torch
+
+    if logits_host.device.type != "cpu" or logits_host.dim() != 2 or logits_host.stride(1) != 1:
+        raise ValueError("logits_host must be a 2-D host tensor with unit inner stride")
+    dt = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16}[logits_host.dtype]
+    T = logits_host.shape[0]
+    ld = logits_host.stride(0) if T > 1 else logits_host.shape[1]
+    V = logits_host.shape[1] if V is None else V
+    need = 2 * min(int(block_rows), max(T, 1)) * ld * logits_host.element_size()
+    if staging.device.type != "cuda" or staging.numel() * staging.element_size() < need:
+        raise ValueError(f"staging must be a device buffer of at least {need} bytes")
+    ld_out = 0
+    if dlogits is not None:
+        if dlogits.dtype != logits_host.dtype or dlogits.dim() != 2 or dlogits.stride(1) != 1 or dlogits.shape[0] != T:
+            raise ValueError("dlogits must match logits' dtype and rows, 2-D, unit inner stride")
+        ld_out = dlogits.stride(0) if T > 1 else dlogits.shape[1]
+    terms = terms or {}
+    tm = grpo_loss_terms(int(terms.get("kl_kind", 0)), float(terms.get("kl_coef", 0.0)),
+                         _ptr(terms.get("ref_logp")), float(terms.get("ent_coef", 0.0)),
+                         _ptr(terms.get("entropy_tok")), _ptr(terms.get("w_tok")))
+    st = _stream(stream)
+    rc = _lib().grpo_logprob_loss_fwd_bwd_host(logits_host.data_ptr(), dt, T, V, ld, _ptr(tok_src), _ptr(target),
+                                               _ptr(old_logp), _ptr(adv_tok), _ptr(mask), float(clip_eps),
+                                               float(grad_scale), _ptr(dlogits), ld_out, _ptr(loss_tok),
+                                               _ptr(logp_tok), C.byref(tm), _ptr(acc), _ptr(staging),
+                                               int(block_rows), st, st if copy_stream is None else _stream(copy_stream))
+    if rc != OK:
+        raise GrpoError(rc, "grpo_logprob_loss_fwd_bwd_host")
 
 
 def _grad_arrays(grad_bufs):

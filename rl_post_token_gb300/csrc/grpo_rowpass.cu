@@ -278,3 +278,82 @@ extern "C" GRPO_API int grpo_logprob_loss_fwd_bwd(const void* logits, int32_t dt
                                       clip_eps, grad_scale, dlogits, ld_out, loss_tok, logp_tok, nullptr, acc,
                                       stream);
 }
+
+namespace {
+
+// The events of one host-input call, destroyed when it returns (a pending event may be
+// destroyed: its resources go once it completes).
+struct CallEvents {
+  cudaEvent_t ev[5] = {};
+  int n = 0;
+  bool create() {
+    for (; n < 5; ++n)
+      if (cudaEventCreateWithFlags(&ev[n], cudaEventDisableTiming) != cudaSuccess) return false;
+    return true;
+  }
+  ~CallEvents() {
+    for (int i = 0; i < n; ++i) cudaEventDestroy(ev[i]);
+  }
+};
+
+}  // namespace
+
+extern "C" GRPO_API int grpo_logprob_loss_fwd_bwd_host(const void* logits_host, int32_t dtype, int64_t T, int64_t V,
+                                                       int64_t ld, const int64_t* tok_src, const int32_t* target,
+                                                       const float* old_logp, const float* adv_tok,
+                                                       const uint8_t* mask, float clip_eps, float grad_scale,
+                                                       void* dlogits, int64_t ld_out, float* loss_tok,
+                                                       float* logp_tok, const grpo_loss_terms* terms,
+                                                       grpo_step_acc* acc, void* staging, int64_t block_rows,
+                                                       void* stream, void* copy_stream) {
+  if (dtype != GRPO_DTYPE_F32 && dtype != GRPO_DTYPE_BF16) return GRPO_ERR_UNSUPPORTED;
+  if (T < 0 || V < 1 || ld < V || !acc || block_rows < 1) return GRPO_ERR_INVALID;
+  if (dlogits && ld_out < V) return GRPO_ERR_INVALID;
+  if (T == 0) return GRPO_OK;
+  if (!logits_host || !staging || (reinterpret_cast<uintptr_t>(staging) & 15u)) return GRPO_ERR_INVALID;
+  if (!target || !adv_tok || !mask || !loss_tok) return GRPO_ERR_INVALID;
+  const size_t es = dtype == GRPO_DTYPE_F32 ? 4 : 2;
+  const int64_t br = std::min(block_rows, T);
+  const size_t row_bytes = (size_t)ld * es;
+  const size_t half = (size_t)br * row_bytes;
+  const cudaStream_t st = as_stream(stream), cs = as_stream(copy_stream);
+  CallEvents e;  // ev[0..1]: block copied into half b; ev[2..3]: half b read; ev[4]: call start
+  if (!e.create()) return GRPO_ERR_CUDA;
+  // the first copies wait for what is already on `stream` (an earlier call may still read
+  // the staging buffer)
+  GRPO_CUDA_TRY(cudaEventRecord(e.ev[4], st));
+  GRPO_CUDA_TRY(cudaStreamWaitEvent(cs, e.ev[4], 0));
+  const bool perm = tok_src != nullptr;
+  const uint8_t* src = static_cast<const uint8_t*>(logits_host);
+  for (int64_t r0 = 0, k = 0; r0 < T; r0 += br, ++k) {
+    const int64_t n = std::min(br, T - r0);
+    const int b = (int)(k & 1);
+    uint8_t* dst = static_cast<uint8_t*>(staging) + (size_t)b * half;
+    if (k >= 2) GRPO_CUDA_TRY(cudaStreamWaitEvent(cs, e.ev[2 + b], 0));  // block k-2's row pass is done
+    GRPO_CUDA_TRY(cudaMemcpyAsync(dst, src + (size_t)r0 * row_bytes, (size_t)n * row_bytes,
+                                  cudaMemcpyHostToDevice, cs));
+    GRPO_CUDA_TRY(cudaEventRecord(e.ev[b], cs));
+    GRPO_CUDA_TRY(cudaStreamWaitEvent(st, e.ev[b], 0));
+    // the block's rows: side arrays and outputs follow the rows unless read through tok_src
+    grpo_loss_terms tb;
+    const grpo_loss_terms* tp = nullptr;
+    if (terms) {
+      tb = *terms;
+      if (!perm) {
+        if (tb.ref_logp) tb.ref_logp += r0;
+        if (tb.entropy_tok) tb.entropy_tok += r0;
+        if (tb.w_tok) tb.w_tok += r0;
+      }
+      tp = &tb;
+    }
+    const int64_t o = perm ? 0 : r0;
+    const int rc = grpo_logprob_loss_fwd_bwd_ex(
+        dst, dtype, n, V, ld, perm ? tok_src + r0 : nullptr, target + o, old_logp ? old_logp + o : nullptr,
+        adv_tok + o, mask + o, clip_eps, grad_scale,
+        dlogits ? static_cast<uint8_t*>(dlogits) + (size_t)r0 * (size_t)ld_out * es : nullptr, ld_out, loss_tok + o,
+        logp_tok ? logp_tok + o : nullptr, tp, acc, stream);
+    if (rc != GRPO_OK) return rc;
+    GRPO_CUDA_TRY(cudaEventRecord(e.ev[2 + b], st));
+  }
+  return GRPO_OK;
+}

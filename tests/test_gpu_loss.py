@@ -785,3 +785,51 @@ def test_bounded_wait_gives_up_and_the_step_reports_it():
     res2 = _lib.grpo_finish_step(acc2, loss2, grad_bufs=[dl2])
     assert res2["status"] == 0 and res2["kernel_flags"] == 0
     assert torch.equal(loss2, loss) and torch.equal(logp2, logp)
+
+
+@pytest.mark.parametrize("dtype,V,block,pinned,permuted,two_streams", [
+    ("bf16", 32776, 37, True, True, True), ("bf16", 151936, 64, True, False, True),
+    ("f32", 16384, 50, False, True, False), ("bf16", 32776, 1000, True, True, True)])
+def test_host_logits_streaming_equals_device_call(dtype, V, block, pinned, permuted, two_streams):
+    # Logits in host memory, streamed through a two-block device staging buffer (copies on a
+    # second stream, each block's row pass waiting only for its own copy): the bits of the
+    # device call on the same rows. Ragged blocks, a permuted order with padding rows or the
+    # identity order, pi_old, the KL and entropy terms; pageable host memory and a single
+    # stream too; a block larger than the call.
+    wl = W.make_workload("tiny", rows=12, positions=20, valid_lo=0, V=V, dtype=dtype, seed=V % 331 + block, std=2.0)
+    case = H.Case(wl)
+    T = case.logits.shape[0]
+    rng = np.random.default_rng(9)
+    tok_src, lg = None, case.logits
+    if permuted:
+        src = np.concatenate([rng.permutation(T), -1 - rng.choice(T, 5)]).astype(np.int64)
+        rng.shuffle(src)
+        tok_src = torch.from_numpy(src).to(DEV)
+        lg = case.logits[torch.from_numpy(np.where(src >= 0, src, -1 - src)).to(DEV)]
+    ref = torch.from_numpy((case.old + rng.normal(0, 0.3, T)).astype(np.float32)).to(DEV)
+
+    def run(host):
+        dl = torch.empty_like(lg)
+        loss, logp, ent = (torch.full((T,), -7.0, device=DEV) for _ in range(3))
+        acc = _lib.new_step_acc(DEV)
+        terms = dict(kl_kind=_lib.KL_K3, kl_coef=0.1, ref_logp=ref, ent_coef=0.02, entropy_tok=ent)
+        if host:
+            lh = lg.cpu()
+            lh = lh.pin_memory() if pinned else lh
+            staging = torch.empty(2 * block * lg.stride(0) * lg.element_size(), dtype=torch.uint8, device=DEV)
+            _lib.grpo_logprob_loss_fwd_bwd_host(lh, case.d_target, case.d_old, case.d_adv, case.d_mask, wl.eps,
+                                                1.0 / 97, dl, loss, logp, acc, staging, block, tok_src=tok_src,
+                                                copy_stream=torch.cuda.Stream() if two_streams else None,
+                                                terms=terms)
+        else:
+            _lib.grpo_logprob_loss_fwd_bwd(lg, case.d_target, case.d_old, case.d_adv, case.d_mask, wl.eps,
+                                           1.0 / 97, dl, loss, logp, acc, tok_src=tok_src, terms=terms)
+        torch.cuda.synchronize()
+        bits = torch.int16 if dtype == "bf16" else torch.int32
+        return (dl.view(bits), loss.view(torch.int32), logp.view(torch.int32), ent.view(torch.int32), acc)
+
+    want, got = run(False), run(True)
+    for g, w, what in zip(got, want, ("dlogits", "loss", "logp", "entropy", "acc")):
+        assert torch.equal(g, w), what
+    res = _lib.grpo_finish_step(got[4], got[1].view(torch.float32))
+    assert res["status"] == 0 and res["n_valid"] == int(case.mask.sum())
