@@ -297,9 +297,12 @@ class Batch:
             self.tok_src_free[k] = ev
         self.n_step += 1
 
-    def run(self, with_grad=True, stream=None, chunk_ready=None, launch_events=None):
+    def run(self, with_grad=True, stream=None, chunk_ready=None, launch_events=None, logits_host=None,
+            staging=None, copy_stream=None, block_rows=1024):
         from rl_post_token_gb300 import step as S
-        return S.run_batch(self.bp, side_stream=self.side, logits=self.logits,
+        host = logits_host is not None
+        return S.run_batch(self.bp, side_stream=None if host else self.side, logits=None if host else self.logits,
+                           logits_host=logits_host, staging=staging, copy_stream=copy_stream, block_rows=block_rows,
                            dlogits=self.dlogits if with_grad else None,
                            target=self.target, old_logp=self.old, mask=self.mask, adv_tok=self.adv_tok,
                            loss_tok=self.loss_tok, logp_tok=self.logp_tok, accs=self.accs,
@@ -592,9 +595,13 @@ def _gpu_index(local: int) -> int:
 
 
 def run_e2e(batch, device, stream, steps: int):
-    """Same metric through the public API with HOST inputs: every step copies the logits
-    (pinned host -> device, per chunk on a copy stream, each chunk's row pass waiting only for
-    its own copy) and the side inputs, runs the batch, and reads the step results back."""
+    """Same metric through the public API with HOST inputs. Every step:
+    - the logits stream from pinned host memory through the library's host entry point
+      (`grpo_logprob_loss_fwd_bwd_host`): 1024-row blocks into a two-block device staging
+      buffer, the copies on a copy stream, each block's row pass waiting only for its own copy;
+    - the side inputs are copied up;
+    - the batch runs;
+    - the step results are read back."""
     import torch
 
     host_logits = torch.empty(batch.logits.shape, dtype=batch.logits.dtype, pin_memory=True)
@@ -602,25 +609,18 @@ def run_e2e(batch, device, stream, steps: int):
     side = {k: getattr(batch, k).cpu().pin_memory() for k in ("target", "mask", "rewards", "old")
             + (("ref",) if batch.ref is not None else ())}
     host_res = torch.empty(batch.accs.numel(), dtype=torch.uint8, pin_memory=True)
+    block = 1024
+    staging = torch.empty(2 * block * host_logits.stride(0) * host_logits.element_size(), dtype=torch.uint8,
+                          device=device)
     copy = torch.cuda.Stream(device)
     torch.cuda.synchronize(device)
 
     def one_step():
         batch.replan(stream)
-        bp = batch.bp
         with torch.cuda.stream(stream):
             for k, v in side.items():
                 getattr(batch, k).copy_(v, non_blocking=True)
-        copy.wait_stream(stream)
-        ready = []
-        with torch.cuda.stream(copy):
-            for c in range(bp.plan["n_chunks"]):
-                a, b = int(bp.exec_tok_off[c]), int(bp.exec_tok_off[c + 1])
-                batch.logits[a:b].copy_(host_logits[a:b], non_blocking=True)
-                e = torch.cuda.Event()
-                e.record(copy)
-                ready.append(e)
-        batch.run(stream=stream, chunk_ready=ready)
+        batch.run(stream=stream, logits_host=host_logits, staging=staging, copy_stream=copy, block_rows=block)
         with torch.cuda.stream(stream):
             host_res.copy_(batch.accs, non_blocking=True)
         stream.synchronize()
@@ -634,8 +634,9 @@ def run_e2e(batch, device, stream, steps: int):
     return {"value": batch.wl.n_valid * steps / dt, "elapsed_s": dt, "units": batch.wl.n_valid * steps,
             "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(host_res.numel()), "steps": steps,
-            "how": "pinned host logits copied per chunk on a side stream, overlapped with the row pass; "
-                   "side inputs copied and step results read back every step"}
+            "how": "pinned host logits streamed by grpo_logprob_loss_fwd_bwd_host (1024-row blocks through a "
+                   "two-block device staging buffer, copies overlapped with the row pass); side inputs copied "
+                   "and step results read back every step"}
 
 
 def main(argv=None):

@@ -70,7 +70,8 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
               adv_eps: float = 1e-6, row_tok_off=None, row_rollout=None, tok_src=None,
               deferred: bool = False, V: Optional[int] = None, stream=None,
               chunk_ready=None, launch_events=None, agg: int = _lib.AGG_TOKEN_MEAN,
-              w_tok=None, side_stream=None, terms: Optional[dict] = None) -> int:
+              w_tok=None, side_stream=None, terms: Optional[dict] = None, logits_host=None,
+              staging=None, block_rows: int = 1024, copy_stream=None) -> int:
     """Enqueue the whole batch; returns the number of library kernel launches.
 
     ``accs`` is a uint8 device tensor of n_steps * 128 bytes (one accumulator per optimizer
@@ -84,6 +85,12 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
     ``terms`` (optional): the regularisers every chunk's call adds, as for
     ``_lib.grpo_logprob_loss_fwd_bwd``: ``kl_kind``, ``kl_coef``, ``ref_logp`` (input order, all
     tokens), ``ent_coef`` and ``entropy_tok`` (input order, all tokens; written).
+
+    ``logits_host`` (instead of ``logits``): the batch's logits in host memory, exec order. Each
+    optimizer step's rows are streamed in one ``grpo_logprob_loss_fwd_bwd_host`` call through
+    ``staging`` (device, 2 * block_rows rows), the copies on ``copy_stream``. The micro-batch
+    boundaries change no bit, so the step is one call; ``chunk_ready`` and ``side_stream`` do
+    not apply, and ``launch_events`` receives one pair per step.
 
     ``side_stream`` (optional): the chunks of a step alternate between ``stream`` and this
     stream, so that the next chunk's blocks take the SMs the current chunk's last rows leave
@@ -107,9 +114,14 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
         D = N if plain else int(divisors[s])
         scale = 1.0 if deferred else 1.0 / max(D, 1)
         acc = accs[s * _lib.ACC_BYTES:(s + 1) * _lib.ACC_BYTES]
-        if side_stream is not None:
+        if logits_host is not None:
+            launches += _host_step(bp, s, logits_host, staging, block_rows, copy_stream, st, dlogits, target,
+                                   old_logp, adv_tok, mask, loss_tok, logp_tok, acc, clip_eps, scale, tok_src,
+                                   w_tok, terms, V, launch_events)
+        elif side_stream is not None:
             side_stream.wait_stream(st)  # the advantage and the previous step's finish
-        for i, c in enumerate(range(p["step_chunk_off"][s], p["step_chunk_off"][s + 1])):
+        chunks = range(0) if logits_host is not None else range(p["step_chunk_off"][s], p["step_chunk_off"][s + 1])
+        for i, c in enumerate(chunks):
             a, b = int(bp.exec_tok_off[c]), int(bp.exec_tok_off[c + 1])
             cs = side_stream if side_stream is not None and i % 2 == 1 else st
             if chunk_ready is not None:
@@ -146,7 +158,7 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
                 e1.record(cs)
                 launch_events.append((e0, e1))
             launches += 1
-        if side_stream is not None:
+        if side_stream is not None and logits_host is None:
             st.wait_stream(side_stream)
         t0, t1 = bp.step_tok_range[s]
         e0, e1 = bp.step_exec_range[s]
@@ -160,6 +172,41 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
                                      sync=False, stream=st)
         launches += 1 + len(grads)
     return launches
+
+
+def _host_step(bp, s, logits_host, staging, block_rows, copy_stream, st, dlogits, target, old_logp, adv_tok,
+               mask, loss_tok, logp_tok, acc, clip_eps, scale, tok_src, w_tok, terms, V, launch_events) -> int:
+    """One optimizer step's rows streamed from host memory: returns the kernel launches."""
+    import torch
+
+    e0, e1 = bp.step_exec_range[s]
+    if e1 == e0:
+        return 0
+    ct = dict(terms or {})
+    if w_tok is not None:
+        ct["w_tok"] = w_tok
+    if tok_src is None:  # exec order == input order: the side arrays follow the rows
+        side = [None if a is None else a[e0:e1] for a in (target, old_logp, adv_tok, mask, loss_tok, logp_tok)]
+        for k in ("ref_logp", "entropy_tok", "w_tok"):
+            if ct.get(k) is not None:
+                ct[k] = ct[k][e0:e1]
+        ts = None
+    else:
+        side = [target, old_logp, adv_tok, mask, loss_tok, logp_tok]
+        ts = tok_src[e0:e1]
+    tg, od, ad, mk, lt, lp = side
+    if launch_events is not None:
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev0.record(st)
+    _lib.grpo_logprob_loss_fwd_bwd_host(logits_host[e0:e1], tg, od, ad, mk, clip_eps, scale,
+                                        None if dlogits is None else dlogits[e0:e1], lt, lp, acc, staging,
+                                        block_rows, tok_src=ts, V=V, stream=st, copy_stream=copy_stream,
+                                        terms=ct or None)
+    if launch_events is not None:
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev1.record(st)
+        launch_events.append((ev0, ev1))
+    return -(-(e1 - e0) // block_rows)
 
 
 def read_results(accs, n_steps: int) -> List[dict]:

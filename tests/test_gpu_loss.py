@@ -833,3 +833,42 @@ def test_host_logits_streaming_equals_device_call(dtype, V, block, pinned, permu
         assert torch.equal(g, w), what
     res = _lib.grpo_finish_step(got[4], got[1].view(torch.float32))
     assert res["status"] == 0 and res["n_valid"] == int(case.mask.sum())
+
+
+@pytest.mark.parametrize("kind", ["fixed", "dynamic"])
+def test_driver_loop_host_logits_equals_device_logits(kind):
+    # The driver loop over logits in host memory (each optimizer step streamed through a
+    # small staging buffer, copies on their own stream) gives the device loop's bits, with the
+    # KL and entropy terms, for fixed chunks and for permuted token-budget bins.
+    if kind == "fixed":
+        wl = W.make_workload("tiny", rows=8, positions=24, valid_lo=0, V=32776, dtype="bf16", seed=95, std=2.0,
+                             mini=4, micro=2)
+    else:
+        wl = W.make_workload("dynamic", rows=16, len_hi=64, median=20, max_token_len=96, V=32776, seed=96)
+    case = H.Case(wl)
+    T = wl.T
+    ref = torch.from_numpy((case.old + np.random.default_rng(6).normal(0, 0.3, T)).astype(np.float32)).to(DEV)
+    bp = S.plan_batch(wl.plan, wl.row_len, wl.row_valid, wl.seg_counts)
+    src = np.arange(bp.exec_tokens) if bp.tok_src is None else bp.tok_src
+    lg = case.logits[torch.from_numpy(src).to(DEV)]
+    ts = None if bp.tok_src is None else torch.from_numpy(bp.tok_src).to(DEV)
+    outs = []
+    for host in (False, True):
+        dl = torch.empty_like(lg)
+        loss, logp, ent = (torch.full((T,), -7.0, device=DEV) for _ in range(3))
+        accs = torch.zeros(bp.n_steps * _lib.ACC_BYTES, dtype=torch.uint8, device=DEV)
+        terms = dict(kl_kind=_lib.KL_K3, kl_coef=0.1, ref_logp=ref, ent_coef=0.02, entropy_tok=ent)
+        kw = dict(dlogits=dl, target=case.d_target, old_logp=case.d_old, mask=case.d_mask, adv_tok=case.d_adv,
+                  loss_tok=loss, logp_tok=logp, accs=accs, clip_eps=wl.eps, tok_src=ts, terms=terms)
+        if host:
+            block = 13
+            staging = torch.empty(2 * block * lg.stride(0) * lg.element_size(), dtype=torch.uint8, device=DEV)
+            S.run_batch(bp, logits=None, logits_host=lg.cpu().pin_memory(), staging=staging, block_rows=block,
+                        copy_stream=torch.cuda.Stream(), **kw)
+        else:
+            S.run_batch(bp, logits=lg, side_stream=torch.cuda.Stream(), **kw)
+        torch.cuda.synchronize()
+        outs.append((dl.view(torch.int16), loss.view(torch.int32), logp.view(torch.int32), ent.view(torch.int32),
+                     S.read_results(accs, bp.n_steps)))
+    for a, b, what in zip(outs[0], outs[1], ("dlogits", "loss", "logp", "entropy", "results")):
+        assert (a == b) if what == "results" else torch.equal(a, b), what
