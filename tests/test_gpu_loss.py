@@ -686,6 +686,43 @@ def test_entropy_with_masked_vocabulary(variant):
     assert res["status"] == 0 and res["n_nonfinite"] == 0
 
 
+@pytest.mark.parametrize("variant", ["c2", "c4", "l2"], indirect=True)
+def test_plain_and_forward_only_with_masked_vocabulary(variant):
+    # -inf logits in the plain instance and the forward-only pass: a tenth of every row at
+    # random, every row's first element (the lazy shift's starting point), and a run of 4096
+    # (whole per-thread blocks of -inf), never the target. They carry no mass, their dlogits
+    # are exactly 0, every output is finite, and the forward-only pass gives the full pass's bits.
+    wl = W.make_workload("tiny", rows=8, positions=16, valid_lo=0, V=32776, dtype="bf16", seed=62, std=2.0)
+    case = H.Case(wl)
+    T, V = wl.T, wl.V
+    rng = np.random.default_rng(6)
+    off = rng.random((T, V)) < 0.1
+    off[:, 0] = True
+    off[:, 8192:8192 + 4096] = True
+    off[np.arange(T), wl.target] = False
+    lg = case.logits.clone()
+    lg[torch.from_numpy(off).to(DEV)] = float("-inf")
+    host = W.logits_to_host(lg)
+    scale = 1.0 / 59
+    dl, loss, logp, acc = _run_direct(case, scale, logits=lg)
+    ref_out = OL.loss_fwd_bwd(host, wl.target, case.old, case.adv_tok, wl.mask, wl.eps, scale, True)
+    m = wl.mask.astype(bool)
+    gp, gl = H.to_f64(logp), H.to_f64(loss)
+    assert np.all(np.isfinite(gp)) and np.all(np.isfinite(gl))
+    assert np.all(np.abs(gp[m] - ref_out["logp_tok"][m]) <= 1e-5 * np.maximum(1, np.abs(ref_out["logp_tok"][m])))
+    got = H.to_f64(dl)
+    assert np.all(np.isfinite(got)) and np.all(got[off] == 0)
+    refd = ref_out["dlogits"]
+    rowmax = np.max(np.abs(refd), axis=1, keepdims=True)
+    bad = np.abs(got - refd) > 1e-2 * np.abs(refd) + 1e-5 * rowmax
+    bad[H.ambiguous_clip(ref_out["ratio"], wl.eps)] = False
+    assert not bad.any(), np.argwhere(bad)[:3]
+    res = _lib.grpo_finish_step(acc, loss)
+    assert res["status"] == 0 and res["n_nonfinite"] == 0
+    _, loss_f, logp_f, _ = _run_direct(case, scale, want_grad=False, logits=lg)
+    assert torch.equal(loss_f, loss) and torch.equal(logp_f, logp)
+
+
 def test_terms_reject_bad_arguments():
     acc = _lib.new_step_acc(DEV)
     x = torch.zeros((2, 8), device=DEV)
