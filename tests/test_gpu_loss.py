@@ -909,3 +909,57 @@ def test_driver_loop_host_logits_equals_device_logits(kind):
                      S.read_results(accs, bp.n_steps)))
     for a, b, what in zip(outs[0], outs[1], ("dlogits", "loss", "logp", "entropy", "results")):
         assert (a == b) if what == "results" else torch.equal(a, b), what
+
+
+def test_step_captured_in_a_cuda_graph_replays_bitwise():
+    # A whole batch (advantage, chunks alternating over two streams, the step finishes) captured
+    # once into a CUDA graph: a replay gives the eager run's bits, also after new inputs are
+    # written into the same buffers.
+    wl = W.make_workload("tiny", rows=8, positions=24, valid_lo=0, V=32776, dtype="bf16", seed=97, std=2.0,
+                         mini=4, micro=2)
+    case = H.Case(wl)
+    T = wl.T
+    bp = S.plan_batch(wl.plan, wl.row_len, wl.row_valid)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    rewards, row_tok_off, row_rollout = t(wl.rewards), t(wl.tok_off), t(wl.row_rollout)
+    adv_rollout = torch.empty_like(rewards)
+    adv_tok = torch.empty(T, device=DEV)
+    lg = case.logits.clone()
+    dl = torch.empty_like(lg)
+    loss, logp = torch.empty(T, device=DEV), torch.empty(T, device=DEV)
+    accs = torch.zeros(bp.n_steps * _lib.ACC_BYTES, dtype=torch.uint8, device=DEV)
+    side = torch.cuda.Stream()
+
+    def step():
+        S.run_batch(bp, logits=lg, dlogits=dl, target=case.d_target, old_logp=case.d_old, mask=case.d_mask,
+                    adv_tok=adv_tok, loss_tok=loss, logp_tok=logp, accs=accs, clip_eps=wl.eps, rewards=rewards,
+                    adv_rollout=adv_rollout, group_size=wl.group_size, row_tok_off=row_tok_off,
+                    row_rollout=row_rollout, side_stream=side)
+
+    def snapshot():
+        torch.cuda.synchronize()
+        return (dl.view(torch.int16).clone(), loss.clone(), logp.clone(), accs[:].view(-1, _lib.ACC_BYTES)[:, 64:].clone())
+
+    step()  # eager (the first calls also set the kernels' attributes)
+    eager = snapshot()
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(g, stream=cs):
+            step()
+    for _ in range(2):
+        dl.fill_(7.0)
+        loss.fill_(7.0)
+        g.replay()
+        got = snapshot()
+        for a, b in zip(got, eager):
+            assert torch.equal(a, b)
+    # new logits in the same buffer: the replay follows them exactly as an eager run does
+    lg.copy_(torch.flip(case.logits, dims=[1]))
+    g.replay()
+    replayed = snapshot()
+    step()
+    for a, b in zip(replayed, snapshot()):
+        assert torch.equal(a, b)
+    assert not torch.equal(replayed[1], eager[1])
