@@ -402,6 +402,28 @@ def run_lmhead(args):
     fwd_s = f0.elapsed_time(f1) / 1e3 / args.steps
     clk = clocks.stop()
     res = _lib.read_step_result(acc)
+
+    # e2e: the step's inputs start in pinned host memory (hidden states, weights, side arrays)
+    # and are copied up every step; the step result is read back
+    host = {"h": h.cpu().pin_memory(), "Wt": Wt.cpu().pin_memory(), "target": target.cpu().pin_memory(),
+            "mask": mask.cpu().pin_memory(), "rewards": rewards.cpu().pin_memory(), "old": old.cpu().pin_memory()}
+    dev_in = {"h": h, "Wt": Wt, "target": target, "mask": mask, "rewards": rewards, "old": old}
+    host_res = torch.empty(64, dtype=torch.uint8, pin_memory=True)
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+    def e2e_step():
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        step(old=old)
+        host_res.copy_(acc[64:128], non_blocking=True)
+        stream.synchronize()
+
+    e2e_step()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
     flops = 6.0 * T * V * Hd
     peak, kind = bf16_peak(sustained=True)
     line = {
@@ -421,6 +443,13 @@ def run_lmhead(args):
         "forward_only": {"ms": 1e3 * fwd_s, "tflops": 2.0 * T * V * Hd / fwd_s / 1e12,
                          "what": "softmax-partials GEMM pass + per-token reduce (2*T*V*H flops)"},
         "step_result": {k: res[k] for k in ("loss", "n_valid", "clipfrac", "status")},
+        "e2e": {"value": N / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(host_res.numel()), "steps": e2e_steps,
+                "how": "hidden states, weights and side inputs copied from pinned host memory every step, "
+                       "the step result read back"},
+        # per step: the advantage (2), pass A, the per-token reduce and dz-from-e (3; the two
+        # cuBLAS GEMMs are not counted), the finish (1)
+        "gpu_launches": 6 * args.steps,
     }
     if clk is not None:
         line["clocks"] = clk
