@@ -22,6 +22,7 @@ import os
 import re
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -375,8 +376,7 @@ def run_lmhead(args):
     for _ in range(max(args.warmup, 3)):
         step(old=old)
     torch.cuda.synchronize(device)
-    out_dir = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp"
-    clocks = ClockSampler(_gpu_index(local), os.path.join(out_dir, f"clocks_lmhead_rank{rank}.csv"))
+    clocks = ClockSampler(_gpu_index(local), os.path.join(args.clocks_dir, f"clocks_lmhead_rank{rank}.csv"))
     time.sleep(0.5)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -496,8 +496,7 @@ def run_gb300(args):
         batch.run(stream=stream)
     torch.cuda.synchronize(device)
 
-    out_dir = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp"
-    clocks = ClockSampler(_gpu_index(local), os.path.join(out_dir, f"clocks_rank{rank}.csv"))
+    clocks = ClockSampler(_gpu_index(local), os.path.join(args.clocks_dir, f"clocks_rank{rank}.csv"))
     time.sleep(0.5)
     barrier(world, device)
     torch.cuda.synchronize(device)
@@ -677,6 +676,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="qwen_step", choices=list(WORKLOAD_TEXT))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-dir", default=tempfile.gettempdir(),
+                    help="where the raw clock samples of the timed region are written (CSV)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--lm-tokens", type=int, default=0,
                     help="override the fused LM-head token count (smaller cases for profiling)")
