@@ -963,3 +963,41 @@ def test_step_captured_in_a_cuda_graph_replays_bitwise():
     for a, b in zip(replayed, snapshot()):
         assert torch.equal(a, b)
     assert not torch.equal(replayed[1], eager[1])
+
+
+def test_all_masked_batch_and_empty_calls_at_product_vocabulary():
+    # Degenerate inputs on the product kernels (V = 151936 bf16): a batch with every token
+    # masked (no row is read; the producer's scan finds nothing) through the full pass, the
+    # forward-only pass and the host-input path, and zero-row calls. Outputs are zeros, the
+    # step loss is 0 (not NaN) and N = 0.
+    wl = W.make_workload("tiny", rows=4, positions=8, valid_lo=0, V=151936, dtype="bf16", seed=98, std=2.0)
+    case = H.Case(wl)
+    T = wl.T
+    case.mask = np.zeros(T, np.uint8)
+    case.d_mask = torch.zeros(T, dtype=torch.uint8, device=DEV)
+    for want_grad in (True, False):
+        dl, loss, logp, acc = _run_direct(case, 1.0, want_grad=want_grad)
+        assert torch.all(loss == 0) and torch.all(logp == 0)
+        if want_grad:
+            assert torch.all(dl == 0)
+        res = _lib.grpo_finish_step(acc, loss, expected_N=0)
+        assert res["status"] == 0 and res["n_valid"] == 0 and res["loss"] == 0.0 and res["n_tokens"] == T
+    staging = torch.empty(2 * 8 * case.logits.stride(0) * 2, dtype=torch.uint8, device=DEV)
+    dl = torch.full_like(case.logits, 3.0)
+    loss = torch.full((T,), -7.0, device=DEV)
+    acc = _lib.new_step_acc(DEV)
+    _lib.grpo_logprob_loss_fwd_bwd_host(case.logits.cpu().pin_memory(), case.d_target, case.d_old, case.d_adv,
+                                        case.d_mask, 0.2, 1.0, dl, loss, None, acc, staging, 8)
+    torch.cuda.synchronize()
+    assert torch.all(dl == 0) and torch.all(loss == 0)
+    # zero rows: nothing launched, nothing counted
+    e = torch.empty((0, 151936), dtype=torch.bfloat16)
+    z = torch.empty(0, device=DEV)
+    acc = _lib.new_step_acc(DEV)
+    _lib.grpo_logprob_loss_fwd_bwd_host(e, torch.empty(0, dtype=torch.int32, device=DEV), None, z,
+                                        torch.empty(0, dtype=torch.uint8, device=DEV), 0.2, 1.0, None, z, None, acc,
+                                        staging, 8)
+    _lib.grpo_logprob_loss_fwd_bwd(e.to(DEV), torch.empty(0, dtype=torch.int32, device=DEV), None, z,
+                                   torch.empty(0, dtype=torch.uint8, device=DEV), 0.2, 1.0, None, z, None, acc)
+    res = _lib.grpo_finish_step(acc, z, expected_N=0)
+    assert res["status"] == 0 and res["n_tokens"] == 0 and res["loss"] == 0.0
