@@ -232,7 +232,7 @@ def run_reference(args):
 class Batch:
     """Device-resident inputs and outputs of one collected batch."""
 
-    def __init__(self, wl, device, kl_kind=0, kl_coef=0.0, ent_coef=0.0):
+    def __init__(self, wl, device, kl_kind=0, kl_coef=0.0, ent_coef=0.0, agg=0):
         import torch
         from rl_post_token_gb300 import _lib
         from rl_post_token_gb300 import step as S
@@ -278,6 +278,10 @@ class Batch:
                 self.terms["ref_logp"] = self.ref
             if ent_coef:
                 self.terms["entropy_tok"] = torch.empty(T, dtype=torch.float32, device=device)
+        # the loss aggregation mode; seq-mean-token-mean needs the planner's per-token weights
+        self.agg, self.w_tok = agg, None
+        if agg == _lib.AGG_SEQ_MEAN_TOKEN_MEAN:
+            self.w_tok = t(self.bp.token_weights(agg)[1])
         torch.cuda.synchronize(device)
         self.n_step = 0
 
@@ -300,6 +304,7 @@ class Batch:
 
     def run(self, with_grad=True, stream=None, chunk_ready=None, launch_events=None, logits_host=None,
             staging=None, copy_stream=None, block_rows=1024):
+        from rl_post_token_gb300 import _lib
         from rl_post_token_gb300 import step as S
         host = logits_host is not None
         return S.run_batch(self.bp, side_stream=None if host else self.side, logits=None if host else self.logits,
@@ -311,7 +316,9 @@ class Batch:
                            group_size=self.wl.group_size, row_tok_off=self.row_tok_off,
                            row_rollout=self.row_rollout, tok_src=self.tok_src, V=self.wl.V,
                            stream=stream, chunk_ready=chunk_ready, launch_events=launch_events,
-                           terms=self.terms if with_grad else None)
+                           terms=self.terms if with_grad else None,
+                           agg=self.agg if with_grad else _lib.AGG_TOKEN_MEAN,
+                           w_tok=self.w_tok if with_grad else None)
 
     def algorithmic_bytes(self):
         """Bytes the method must move per batch in the row pass: a valid token reads its logits
@@ -321,10 +328,12 @@ class Batch:
         wl = self.wl
         rowb = wl.V * wl.elem_bytes
         idx = 8 if self.tok_src is not None else 0
-        extra = 0  # the terms' per-token input (reference log-prob) and output (entropy)
+        extra = 0  # the terms' per-token inputs (reference log-prob, aggregation weight), output (entropy)
         if self.terms is not None:
             extra = (4 if self.terms.get("ref_logp") is not None else 0) + \
                     (4 if self.terms.get("entropy_tok") is not None else 0)
+        if self.w_tok is not None:
+            extra += 4
         valid = wl.n_valid  # each valid input token runs exactly once; padding rows are masked
         masked = self.bp.exec_tokens - valid
         return valid * (2 * rowb + 4 + 4 + 4 + 1 + 4 + 4 + idx + extra) + masked * (rowb + 1 + idx)
@@ -483,12 +492,13 @@ def run_gb300(args):
         ov.update(mini=args.rows, micro=args.rows)
     wl = W.make_workload(args.workload, seed=rank, **ov)
     kl_kind = {"none": 0, "k1": _lib.KL_K1, "k3": _lib.KL_K3}[args.kl]
-    batch = Batch(wl, device, kl_kind=kl_kind, kl_coef=args.kl_coef, ent_coef=args.ent_coef)
-    terms_text = ""
-    if batch.terms is not None:
-        terms_text = ", ".join(([f"KL {args.kl} coef {args.kl_coef}"] if kl_kind else []) +
-                               ([f"entropy bonus coef {args.ent_coef} (entropy written per token)"]
-                                if args.ent_coef else []))
+    agg = {"token-mean": _lib.AGG_TOKEN_MEAN, "seq-mean-token-sum": _lib.AGG_SEQ_MEAN_TOKEN_SUM,
+           "seq-mean-token-mean": _lib.AGG_SEQ_MEAN_TOKEN_MEAN}[args.agg]
+    batch = Batch(wl, device, kl_kind=kl_kind, kl_coef=args.kl_coef, ent_coef=args.ent_coef, agg=agg)
+    terms_text = ", ".join(([f"KL {args.kl} coef {args.kl_coef}"] if kl_kind else []) +
+                           ([f"entropy bonus coef {args.ent_coef} (entropy written per token)"]
+                            if args.ent_coef else []) +
+                           ([f"aggregation {args.agg}"] if agg != _lib.AGG_TOKEN_MEAN else []))
     stream = torch.cuda.current_stream(device)
 
     for _ in range(max(args.warmup, 3)):
@@ -635,7 +645,7 @@ def run_e2e(batch, device, stream, steps: int):
     host_logits = torch.empty(batch.logits.shape, dtype=batch.logits.dtype, pin_memory=True)
     host_logits.copy_(batch.logits)
     side = {k: getattr(batch, k).cpu().pin_memory() for k in ("target", "mask", "rewards", "old")
-            + (("ref",) if batch.ref is not None else ())}
+            + (("ref",) if batch.ref is not None else ()) + (("w_tok",) if batch.w_tok is not None else ())}
     host_res = torch.empty(batch.accs.numel(), dtype=torch.uint8, pin_memory=True)
     block = 1024
     staging = torch.empty(2 * block * host_logits.stride(0) * host_logits.element_size(), dtype=torch.uint8,
@@ -688,6 +698,8 @@ def main(argv=None):
     ap.add_argument("--kl-coef", type=float, default=0.05)
     ap.add_argument("--ent-coef", type=float, default=0.0,
                     help="add an entropy bonus (and the per-token entropy output) to the step's loss")
+    ap.add_argument("--agg", default="token-mean", choices=["token-mean", "seq-mean-token-sum", "seq-mean-token-mean"],
+                    help="the loss aggregation mode of the step")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
