@@ -239,8 +239,8 @@ typedef struct grpo_step_acc {
  *            tokens get 0 in both
  *  acc       device grpo_step_acc
  * A target outside [0, V) makes that token's log-prob NaN (counted as non-finite).
- * Errors: GRPO_ERR_INVALID (NULL required pointer, T < 0, V < 1, ld < V),
- * GRPO_ERR_UNSUPPORTED (dtype), GRPO_ERR_CUDA (launch failure). */
+ * Errors: GRPO_ERR_INVALID (NULL required pointer, T < 0, V < 1, ld < V, T or V above
+ * 2^31 - 1), GRPO_ERR_UNSUPPORTED (dtype), GRPO_ERR_CUDA (launch failure). */
 GRPO_API int grpo_logprob_loss_fwd_bwd(const void* logits, int32_t dtype, int64_t T, int64_t V,
                                        int64_t ld, const int64_t* tok_src,
                                        const int32_t* target, const float* old_logp,

@@ -170,11 +170,8 @@ int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
   const int64_t V = a.V;
   const char* pin = getenv("GRPO_ROWPASS");
   const bool pin_l2 = pin && strcmp(pin, "l2") == 0;
-  // the instance with both the KL term and per-token weights (and no entropy) carries more
-  // per-thread state than its 32 KB chunks leave registers for: half-size chunks where the
-  // chunk count allows (the entropy instances fold a chunk in 16-element blocks instead, and
-  // need half-size chunks only where two CTAs share an SM)
-  constexpr bool HALF = TERMS == (kTermsReg | kTermsWeight) && !ENT;
+  // every instance runs 32 KB chunks where one CTA has an SM to itself; where two CTAs share
+  // an SM (c3/c4) the entropy instances take half-size chunks to stay in registers
   if (dtype == GRPO_DTYPE_BF16) {
     // Large bf16 vocabularies: rows split across a CTA cluster, slices staged in shared
     // memory. Variants (cluster size, consumer warps, vectors per thread, CTAs per SM):
@@ -184,7 +181,7 @@ int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
     if (vec && V % 8 == 0 && V >= 16384 && !pin_l2) {
       auto c34 = [&](auto c_tag) {
         constexpr int C = decltype(c_tag)::value;
-        if constexpr (HALF || ENT)
+        if constexpr (ENT)
           if (cluster_fits<B16>(V, C, 8, 2, 2)) return launch_cluster<B16, C, 8, 2, 2, ENT, TERMS>(a, st);
         return launch_cluster<B16, C, 8, 4, 2, ENT, TERMS>(a, st);
       };
@@ -195,15 +192,12 @@ int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
       if (cluster_fits<B16>(V, 2, 16, 1, 4)) {
         if constexpr (!ENT && TERMS == 0)
           if (!a.dlogits && fwd_kernel_on()) return launch_fwd<B16, 2, 16, 4>(a, st);
-        if constexpr (HALF) return launch_cluster<B16, 2, 16, 2, 1, ENT, TERMS>(a, st);
-        else return launch_cluster<B16, 2, 16, 4, 1, ENT, TERMS>(a, st);
+        return launch_cluster<B16, 2, 16, 4, 1, ENT, TERMS>(a, st);
       }
       if (cluster_fits<B16>(V, 4, 8, 2, 4)) return c34(C4{});
       if (cluster_fits<B16>(V, 4, 16, 1, 4)) {
         if constexpr (!ENT && TERMS == 0)
           if (!a.dlogits && fwd_kernel_on()) return launch_fwd<B16, 4, 16, 4>(a, st);
-        if constexpr (HALF)
-          if (cluster_fits<B16>(V, 4, 16, 1, 2)) return launch_cluster<B16, 4, 16, 2, 1, ENT, TERMS>(a, st);
         return launch_cluster<B16, 4, 16, 4, 1, ENT, TERMS>(a, st);
       }
     }
@@ -215,8 +209,7 @@ int dispatch(const RowArgs& a, int32_t dtype, bool vec, cudaStream_t st) {
   if (vec && V % 4 == 0 && V >= 16384 && !pin_l2 && cluster_fits<float>(V, 4, 16, 1, 4)) {
     if constexpr (!ENT && TERMS == 0)
       if (!a.dlogits && fwd_kernel_on()) return launch_fwd<float, 4, 16, 4>(a, st);
-    if constexpr (HALF) return launch_cluster<float, 4, 16, 2, 1, ENT, TERMS>(a, st);
-    else return launch_cluster<float, 4, 16, 4, 1, ENT, TERMS>(a, st);
+    return launch_cluster<float, 4, 16, 4, 1, ENT, TERMS>(a, st);
   }
   if (V >= 8192) return launch_l2<float, 1024, 2, ENT, TERMS>(a, vec, 1, st);
   return launch_l2<float, 128, 2, ENT, TERMS>(a, vec, 16, st);
@@ -242,7 +235,7 @@ extern "C" GRPO_API int grpo_logprob_loss_fwd_bwd_ex(const void* logits, int32_t
   }
   if (T == 0) return GRPO_OK;
   if (!logits || !target || !adv_tok || !mask || !loss_tok) return GRPO_ERR_INVALID;
-  if (V > (int64_t)INT32_MAX) return GRPO_ERR_INVALID;
+  if (V > (int64_t)INT32_MAX || T > (int64_t)INT32_MAX) return GRPO_ERR_INVALID;
 
   RowArgs a{logits, T, V, ld, tok_src, target, old_logp, adv_tok, mask, clip_eps, grad_scale,
             dlogits, ld_out, loss_tok, logp_tok, acc,

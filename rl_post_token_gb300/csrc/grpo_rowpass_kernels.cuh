@@ -23,6 +23,7 @@
 // Each row's reduction order depends only on V and the kernel's fixed shape, never on T or on
 // how the step was chunked, so chunked and un-chunked calls agree bit for bit.
 #include <algorithm>
+#include <type_traits>
 
 #include "grpo_common.cuh"
 
@@ -88,9 +89,13 @@ struct Vec<float> {
   __device__ __forceinline__ static void store1(float* p, float v) { *p = v; }
 };
 
-// Side inputs of one token row, resolved through tok_src.
+// Side inputs of one token row, resolved through tok_src. The instances with extra terms
+// keep the token index in 32 bits (a call has fewer than 2^31 rows): the register it saves
+// is what lets them run full-size chunks without spilling. The plain instances keep 64 bits,
+// the layout their register allocation was tuned with.
+template <int TERMS>
 struct RowMeta {
-  int64_t idx;   // index into the per-token side arrays (-1 for padding rows)
+  std::conditional_t<TERMS == 0, int64_t, int32_t> idx;  // index into the per-token side arrays (-1: padding)
   bool valid;    // mask = 1 and not a padding row
   int32_t y;     // target token id
   float A, old;  // advantage, pi_old log-prob
@@ -107,8 +112,8 @@ constexpr int kTermsReg = 1;
 constexpr int kTermsWeight = 2;
 
 template <int TERMS>
-__device__ __forceinline__ RowMeta row_meta(const RowArgs& a, int64_t src) {
-  RowMeta m{src < 0 ? -1 : src, false, 0, 0.f, 0.f, 0.f, 1.f};
+__device__ __forceinline__ RowMeta<TERMS> row_meta(const RowArgs& a, int64_t src) {
+  RowMeta<TERMS> m{src < 0 ? -1 : (decltype(RowMeta<TERMS>::idx))src, false, 0, 0.f, 0.f, 0.f, 1.f};
   if (src >= 0) {
     m.valid = a.mask[src] != 0;
     m.y = a.target[src];
@@ -127,15 +132,15 @@ template <int TERMS>
 struct MetaPipe {
   const RowArgs& a;
   int64_t stride;
-  RowMeta next;
+  RowMeta<TERMS> next;
   int64_t src2;
   __device__ MetaPipe(const RowArgs& args, int64_t first, int64_t step) : a(args), stride(step) {
-    next = first < a.T ? row_meta<TERMS>(a, row_src(a, first)) : RowMeta{-1, false, 0, 0.f, 0.f, 0.f, 1.f};
+    next = first < a.T ? row_meta<TERMS>(a, row_src(a, first)) : RowMeta<TERMS>{-1, false, 0, 0.f, 0.f, 0.f, 1.f};
     src2 = first + step < a.T ? row_src(a, first + step) : -1;
   }
   // metadata of `row`; starts the loads for the rows after it
-  __device__ RowMeta advance(int64_t row) {
-    const RowMeta m = next;
+  __device__ RowMeta<TERMS> advance(int64_t row) {
+    const RowMeta<TERMS> m = next;
     if (row + stride < a.T) next = row_meta<TERMS>(a, src2);
     src2 = row + 2 * stride < a.T ? row_src(a, row + 2 * stride) : -1;
     return m;
@@ -176,7 +181,7 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
 
   MetaPipe<TERMS> pipe(a, blockIdx.x, gridDim.x);
   for (int64_t row = blockIdx.x; row < a.T; row += gridDim.x) {
-    const RowMeta tm = pipe.advance(row);
+    const auto tm = pipe.advance(row);
     const T* z = static_cast<const T*>(a.logits) + row * a.ld;
     T* dz = a.dlogits ? static_cast<T*>(a.dlogits) + row * a.ld_out : nullptr;
     if (!tm.valid) {
@@ -624,7 +629,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
     uint32_t vi = 0;       // rows read so far: selects the exchange buffer
     MetaPipe<TERMS> pipe(a, cid, ncl);
     for (int64_t row = cid; row < a.T; row += ncl) {
-      const RowMeta tm = pipe.advance(row);
+      const auto tm = pipe.advance(row);
       uint4* dz = dg ? reinterpret_cast<uint4*>(dg + row * a.ld_out + base) : nullptr;
       if (!tm.valid) {
         // masked or padding row: nothing read, nothing exchanged; zero dlogits slice
@@ -932,7 +937,7 @@ __global__ void __launch_bounds__(fwd_block_threads(NCW), 1) row_fwd_kernel(RowA
     for (int64_t row = cid; row < a.T; row += ncl) {
       // the row's metadata: lane 0 keeps the prefetch pipeline and broadcasts, so lane 31,
       // which releases the ring slots, has no global load in flight for its release to wait on
-      RowMeta tm{};
+      RowMeta<0> tm{};
       if (lane == 0) tm = pipe.advance(row);
       tm.valid = __shfl_sync(0xffffffffu, (int)tm.valid, 0) != 0;
       tm.y = __shfl_sync(0xffffffffu, tm.y, 0);
@@ -988,7 +993,7 @@ __global__ void __launch_bounds__(fwd_block_threads(NCW), 1) row_fwd_kernel(RowA
     uint32_t xi = 0;
     MetaPipe<0> pipe(a, cid, ncl);
     for (int64_t row = cid; row < a.T; row += ncl) {
-      const RowMeta tm = pipe.advance(row);
+      const auto tm = pipe.advance(row);
       if (!tm.valid) {
         if (lane == 0) {
           cnt.tokens++;

@@ -1001,3 +1001,20 @@ def test_all_masked_batch_and_empty_calls_at_product_vocabulary():
                                    torch.empty(0, dtype=torch.uint8, device=DEV), 0.2, 1.0, None, z, None, acc)
     res = _lib.grpo_finish_step(acc, z, expected_N=0)
     assert res["status"] == 0 and res["n_tokens"] == 0 and res["loss"] == 0.0
+
+
+def test_row_count_above_int32_is_rejected():
+    # a call's rows index the per-token arrays with 32-bit indices: more than 2^31 - 1 rows is
+    # an invalid call (checked before anything is read)
+    import ctypes
+    lib = _lib.lib()
+    acc = _lib.new_step_acc(DEV)
+    x = torch.zeros((1, 8), device=DEV)
+    i = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mk = torch.ones(1, dtype=torch.uint8, device=DEV)
+    f = torch.zeros(1, device=DEV)
+    rc = lib.grpo_logprob_loss_fwd_bwd(x.data_ptr(), _lib.DTYPE_F32, ctypes.c_int64(2 ** 31), 8, 8, None,
+                                       i.data_ptr(), None, f.data_ptr(), mk.data_ptr(), ctypes.c_float(0.2),
+                                       ctypes.c_float(1.0), None, 0, f.data_ptr(), None, acc.data_ptr(),
+                                       torch.cuda.current_stream().cuda_stream)
+    assert rc == _lib.ERR_INVALID

@@ -47,13 +47,13 @@ def _cluster(T, C, NCW, VPT, MINB, ENT, TERMS):
 DEFAULT_ROW_PASS = [
     # bf16, 2-CTA cluster: no terms, KL, weights, KL + weights, entropy, entropy + weights
     ("bf16", 2, 16, 4, 1, 0, 0), ("bf16", 2, 16, 4, 1, 0, 1), ("bf16", 2, 16, 4, 1, 0, 2),
-    ("bf16", 2, 16, 2, 1, 0, 3), ("bf16", 2, 16, 4, 1, 1, 1), ("bf16", 2, 16, 4, 1, 1, 3),
+    ("bf16", 2, 16, 4, 1, 0, 3), ("bf16", 2, 16, 4, 1, 1, 1), ("bf16", 2, 16, 4, 1, 1, 3),
     # bf16, 4-CTA cluster (rows too long for two CTAs)
     ("bf16", 4, 16, 4, 1, 0, 0), ("bf16", 4, 16, 4, 1, 0, 1), ("bf16", 4, 16, 4, 1, 0, 2),
-    ("bf16", 4, 16, 2, 1, 0, 3), ("bf16", 4, 16, 4, 1, 1, 1), ("bf16", 4, 16, 4, 1, 1, 3),
+    ("bf16", 4, 16, 4, 1, 0, 3), ("bf16", 4, 16, 4, 1, 1, 1), ("bf16", 4, 16, 4, 1, 1, 3),
     # float32, 4-CTA cluster
     ("f32", 4, 16, 4, 1, 0, 0), ("f32", 4, 16, 4, 1, 0, 1), ("f32", 4, 16, 4, 1, 0, 2),
-    ("f32", 4, 16, 2, 1, 0, 3), ("f32", 4, 16, 4, 1, 1, 1), ("f32", 4, 16, 4, 1, 1, 3)]
+    ("f32", 4, 16, 4, 1, 0, 3), ("f32", 4, 16, 4, 1, 1, 1), ("f32", 4, 16, 4, 1, 1, 3)]
 
 
 def test_row_pass_default_instances_do_not_spill(grpo_lib):
