@@ -16,11 +16,18 @@
  * Conventions shared by every entry point:
  *   - Status: every function returns int: GRPO_OK (0), a positive step status, or a negative
  *     GRPO_ERR_* code. No function aborts or prints.
- *   - Ownership: every buffer belongs to the caller. The library allocates no device memory
- *     and never frees caller memory. "device" pointers are CUDA device memory of the current
- *     device; "host" pointers are ordinary host memory.
+ *   - Ownership: every buffer belongs to the caller, and the library never frees caller
+ *     memory. The library allocates no device memory of its own with two exceptions:
+ *       - the LM-head backward's first call on a device creates a cuBLAS handle, with
+ *         cuBLAS's own workspace;
+ *       - the module's 16 MiB device array of grpo_lmhead_forward_noalloc is held by every
+ *         GPU that loads the library.
+ *     "device" pointers are CUDA device memory of the current device; "host" pointers are
+ *     ordinary host memory.
  *   - Asynchrony: device work is enqueued on `stream` (cudaStream_t passed as void*; NULL is
- *     the legacy default stream). Only grpo_finish_step with a non-NULL host result waits.
+ *     the legacy default stream). Only grpo_finish_step with a non-NULL host result waits, so
+ *     a whole step can be captured into a CUDA graph (after one call per kernel and
+ *     shared-memory size has set the kernels' attributes).
  *   - Determinism: results depend only on the inputs, never on the chunking, the launch
  *     shape or the scheduling (no order-dependent floating-point atomics).
  */
