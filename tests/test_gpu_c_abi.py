@@ -1,0 +1,84 @@
+"""The C ABI from a plain C program, with no Python or torch in its process.
+tests/c_abi/loss_step.c is compiled with gcc against include/grpo.h, libgrpo.so and the CUDA
+runtime, and run on seeded inputs. Its outputs (per-token loss and log-prob, dlogits, the
+step result) must equal the Python binding's on the same inputs, bit for bit."""
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+from rl_post_token_gb300 import _lib
+from rl_post_token_gb300 import workloads as W
+
+from tests import _gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _cuda_home():
+    for cand in (os.environ.get("CUDA_HOME"), "/usr/local/cuda"):
+        if cand and os.path.exists(os.path.join(cand, "include", "cuda_runtime_api.h")):
+            return cand
+    nvcc = shutil.which("nvcc")
+    if nvcc:
+        return os.path.dirname(os.path.dirname(os.path.realpath(nvcc)))
+    pytest.skip("CUDA toolkit headers not found")
+
+
+def _compile(out_dir):
+    gcc = shutil.which("gcc")
+    if not gcc:
+        pytest.skip("gcc not found")
+    cuda = _cuda_home()
+    pkg = os.path.join(ROOT, "rl_post_token_gb300")
+    exe = os.path.join(out_dir, "loss_step")
+    cmd = [gcc, "-std=c11", "-O2", "-Wall", f"-I{ROOT}/include", f"-I{cuda}/include",
+           os.path.join(ROOT, "tests", "c_abi", "loss_step.c"), "-o", exe, f"-L{pkg}", "-lgrpo",
+           f"-L{cuda}/lib64", "-lcudart", f"-Wl,-rpath,{pkg}", f"-Wl,-rpath,{cuda}/lib64"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    return exe
+
+
+def test_plain_c_client_matches_the_binding(grpo_lib, tmp_path):
+    assert torch.cuda.is_available()
+    exe = _compile(str(tmp_path))
+    wl = W.make_workload("tiny", rows=8, positions=16, valid_lo=0, V=32776, dtype="bf16", seed=99, std=2.0)
+    case = H.Case(wl)
+    T, V = case.logits.shape
+    scale = np.float32(1.0 / max(int(wl.mask.sum()), 1))
+    inp, outp = os.path.join(str(tmp_path), "in.bin"), os.path.join(str(tmp_path), "out.bin")
+    with open(inp, "wb") as f:
+        f.write(np.int64(T).tobytes() + np.int64(V).tobytes())
+        f.write(np.float32(wl.eps).tobytes() + scale.tobytes())
+        f.write(case.logits.view(torch.int16).cpu().numpy().astype(np.uint16).tobytes())
+        f.write(np.asarray(wl.target, np.int32).tobytes() + np.asarray(case.old, np.float32).tobytes())
+        f.write(np.asarray(case.adv_tok, np.float32).tobytes() + np.asarray(wl.mask, np.uint8).tobytes())
+    r = subprocess.run([exe, inp, outp], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    raw = open(outp, "rb").read()
+    o = 0
+    status = int(np.frombuffer(raw, np.int32, 1, o)[0]); o += 4
+    c_loss = np.frombuffer(raw, np.float32, T, o); o += 4 * T
+    c_logp = np.frombuffer(raw, np.float32, T, o); o += 4 * T
+    c_dz = np.frombuffer(raw, np.uint16, T * V, o); o += 2 * T * V
+    c_res_loss = float(np.frombuffer(raw, np.float64, 1, o)[0]); o += 8
+    c_n_valid, c_n_clipped = (int(x) for x in np.frombuffer(raw, np.int64, 2, o))
+
+    # the binding, same inputs
+    dl = torch.empty_like(case.logits)
+    loss, logp = torch.empty(T, device=DEV), torch.empty(T, device=DEV)
+    acc = _lib.new_step_acc(DEV)
+    _lib.grpo_logprob_loss_fwd_bwd(case.logits, case.d_target, case.d_old, case.d_adv, case.d_mask, wl.eps,
+                                   float(scale), dl, loss, logp, acc)
+    res = _lib.grpo_finish_step(acc, loss)
+    assert status == res["status"] == 0
+    assert np.array_equal(c_loss.view(np.uint32), loss.cpu().numpy().view(np.uint32))
+    assert np.array_equal(c_logp.view(np.uint32), logp.cpu().numpy().view(np.uint32))
+    assert np.array_equal(c_dz, dl.view(torch.int16).cpu().numpy().astype(np.uint16).ravel())
+    assert c_res_loss == res["loss"] and c_n_valid == res["n_valid"] and c_n_clipped == res["n_clipped"]
