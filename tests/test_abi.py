@@ -52,3 +52,22 @@ def test_binding_constants_match_header():
     for k in ("OK", "STEP_SKIPPED_NONFINITE", "ERR_UNSUPPORTED", "DTYPE_BF16", "AGG_SEQ_MEAN_TOKEN_MEAN",
               "KL_K1", "KL_K3"):
         assert k in named, k
+
+
+def test_header_is_plain_c_and_a_c_client_links(grpo_lib, tmp_path):
+    # the boundary is a C ABI: the plain-C client compiles as C11 against grpo.h (with warnings
+    # as errors) and links against the library; running it needs a GPU (its own GPU test)
+    import shutil
+    import subprocess
+    import pytest
+    gcc = shutil.which("gcc")
+    cuda = next((c for c in (os.environ.get("CUDA_HOME"), "/usr/local/cuda")
+                 if c and os.path.exists(os.path.join(c, "include", "cuda_runtime_api.h"))), None)
+    if not gcc or not cuda:
+        pytest.skip("gcc or the CUDA headers not found")
+    pkg = os.path.join(ROOT, "rl_post_token_gb300")
+    cmd = [gcc, "-std=c11", "-O1", "-Wall", "-Wextra", "-Werror", f"-I{ROOT}/include", f"-I{cuda}/include",
+           os.path.join(ROOT, "tests", "c_abi", "loss_step.c"), "-o", str(tmp_path / "loss_step"), f"-L{pkg}",
+           "-lgrpo", f"-L{cuda}/lib64", "-lcudart"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
