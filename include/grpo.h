@@ -246,6 +246,11 @@ typedef struct grpo_step_acc {
  *            tokens get 0 in both
  *  acc       device grpo_step_acc
  * A target outside [0, V) makes that token's log-prob NaN (counted as non-finite).
+ * Numerical range: the log-prob is formed as (z_y - shift) - log(sum), without cancellation.
+ * Results are vouched for while the row's |LSE| <= 4096 (natural units; trained models' logits
+ * are in the tens). A row beyond that reports a NaN log-prob and counts as non-finite, so the
+ * step is skipped, instead of returning dlogits or an entropy degraded by the rounding at
+ * that scale.
  * Errors: GRPO_ERR_INVALID (NULL required pointer, T < 0, V < 1, ld < V, T or V above
  * 2^31 - 1), GRPO_ERR_UNSUPPORTED (dtype), GRPO_ERR_CUDA (launch failure). */
 GRPO_API int grpo_logprob_loss_fwd_bwd(const void* logits, int32_t dtype, int64_t T, int64_t V,

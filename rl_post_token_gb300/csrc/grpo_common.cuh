@@ -298,10 +298,19 @@ struct TokenOut {
   bool clipped, nonfinite;
 };
 
-__device__ __forceinline__ TokenOut token_epilogue(float zy, float lse, bool has_old, float old,
+// Largest |LSE| (natural units) of a row whose results this library vouches for. The
+// log-prob itself is formed without cancellation at any magnitude (the callers compute it as
+// (z_y - shift) - log(sum) from their exact shift). Pass 2's exponent argument and the
+// entropy's LSE - E_p[z], though, round at the scale of the LSE: within 4096 that is below
+// 2.5e-4, beyond it the token is reported non-finite rather than returned degraded. Trained
+// models' logits are in the tens.
+constexpr float kLseMax = 4096.f;
+
+// logp: the target's log-prob; in_range: |LSE| <= kLseMax (else the token reports NaN)
+__device__ __forceinline__ TokenOut token_epilogue(float logp, bool in_range, bool has_old, float old,
                                                   float A, float eps, float scale) {
   TokenOut o;
-  o.logp = zy - lse;
+  o.logp = in_range ? logp : __int_as_float(0x7fc00000);
   const float r = has_old ? expf(o.logp - old) : 1.f;
   const float lo = 1.f - eps, hi = 1.f + eps;
   const float rc = fminf(fmaxf(r, lo), hi);

@@ -491,11 +491,13 @@ __global__ void reduce_kernel(int64_t T, int n_col_tiles, const float* __restric
     if (mask[row]) {
       MS t{-INFINITY, 0.f};
       for (int c = 0; c < n_col_tiles; ++c) t = ms2_combine(t, MS{part_m[(int64_t)c * T + row], part_s[(int64_t)c * T + row]});
-      l2 = t.m + log2f(t.s);
+      const float l2s = log2f(t.s);
+      l2 = t.m + l2s;
       const int32_t y = target[row];
       const float z = (y >= 0 && (int64_t)y < V) ? zy[row] : __int_as_float(0x7fc00000);
-      const TokenOut o = token_epilogue(z, l2 * kLn2, old_logp != nullptr, old_logp ? old_logp[row] : 0.f,
-                                        adv[row], eps, scale);
+      // log2 p_y = (z_y log2e - m) - log2(sum), without cancellation
+      const TokenOut o = token_epilogue((fmaf(z, kLog2e, -t.m) - l2s) * kLn2, fabsf(l2) <= kLseMax * kLog2e,
+                                        old_logp != nullptr, old_logp ? old_logp[row] : 0.f, adv[row], eps, scale);
       loss_tok[row] = o.loss;
       if (logp_tok) logp_tok[row] = o.logp;
       coef = o.coef;

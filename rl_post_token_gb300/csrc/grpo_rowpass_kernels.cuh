@@ -277,9 +277,12 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
         v = warp_ms(v);
       }
       if (lane == 0) {
-        const float lse = v.m + logf(v.s);
+        const float ls = logf(v.s);
+        const float lse = v.m + ls;
         const float sc = (TERMS & kTermsWeight) ? a.scale * tm.w : a.scale;
-        TokenOut o = token_epilogue(ybad ? __int_as_float(0x7fc00000) : zy, lse,
+        // log p_y = (z_y - max) - log(sum): the difference of two logits is exact, so there is no
+        // cancellation at any magnitude
+        TokenOut o = token_epilogue((ybad ? __int_as_float(0x7fc00000) : zy - v.m) - ls, fabsf(lse) <= kLseMax,
                                     a.old_logp != nullptr, tm.old, tm.A, a.eps, sc);
         if (TERMS & kTermsReg) apply_terms(o, sc, a.kl_kind, a.kl_coef, tm.ref, a.ent_coef, lse - ez);
         a.loss_tok[tm.idx] = o.loss;
@@ -739,10 +742,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
           zy = ld_dsmem_f32(ra + 8);
       }
       if (ENT) tot = MS{tot3.m, tot3.s};
-      const float lse2 = tot.m + log2f(tot.s);  // log2(sum_v 2^(z_v log2 e)) = LSE * log2(e)
+      const float l2s = log2f(tot.s);
+      const float lse2 = tot.m + l2s;  // log2(sum_v 2^(z_v log2 e)) = LSE * log2(e)
       const float ez = ENT ? tot3.s2 / tot3.s : 0.f;  // sum_v p_v z_v
       const float sc = (TERMS & kTermsWeight) ? a.scale * tm.w : a.scale;
-      TokenOut o = token_epilogue(zy, lse2 * kLn2, a.old_logp != nullptr, tm.old, tm.A, a.eps, sc);
+      // log2 p_y = (z_y log2e - m) - log2(sum): one rounding of z_y log2e - m, no cancellation
+      TokenOut o = token_epilogue((fmaf(zy, kLog2e, -tot.m) - l2s) * kLn2, fabsf(lse2) <= kLseMax * kLog2e,
+                                  a.old_logp != nullptr, tm.old, tm.A, a.eps, sc);
       if (TERMS & kTermsReg) apply_terms(o, sc, a.kl_kind, a.kl_coef, tm.ref, a.ent_coef, lse2 * kLn2 - ez);
       if (rank == 0 && ct == 0) {
         a.loss_tok[tm.idx] = o.loss;
@@ -1032,8 +1038,10 @@ __global__ void __launch_bounds__(fwd_block_threads(NCW), 1) row_fwd_kernel(RowA
       const float zy = ybad ? __int_as_float(0x7fc00000) : zyv[b];
       __syncwarp();
       if (lane == 0) {
-        const float lse2 = tot.m + log2f(tot.s);
-        const TokenOut o = token_epilogue(zy, lse2 * kLn2, a.old_logp != nullptr, tm.old, tm.A, a.eps, a.scale);
+        const float l2s = log2f(tot.s);
+        const float lse2 = tot.m + l2s;
+        const TokenOut o = token_epilogue((fmaf(zy, kLog2e, -tot.m) - l2s) * kLn2, fabsf(lse2) <= kLseMax * kLog2e,
+                                          a.old_logp != nullptr, tm.old, tm.A, a.eps, a.scale);
         // the buffer is free again in every CTA: what was read from it has been consumed
         // (by the shuffles and the epilogue), so the signal needs no fence
         for (int r = 0; r < C; ++r) mbar_arrive_remote_relaxed(mapa_u32(smem_u32(&xempty[b]), (uint32_t)r));

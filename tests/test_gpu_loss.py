@@ -1018,3 +1018,93 @@ def test_row_count_above_int32_is_rejected():
                                        ctypes.c_float(1.0), None, 0, f.data_ptr(), None, acc.data_ptr(),
                                        torch.cuda.current_stream().cuda_stream)
     assert rc == _lib.ERR_INVALID
+
+
+@pytest.mark.parametrize("variant", ["c2", "l2"], indirect=True)
+def test_extreme_logit_magnitudes(variant):
+    # Rows far from the usual scale take the lazy shift's fallback: a row scaled by 30 (a
+    # spread of hundreds), rows offset by +300 and by -300. Log-probs are formed without
+    # cancellation, so they meet the same bar as ordinary rows; losses and dlogits match the
+    # oracle, and the forward-only pass gives the full pass's bits.
+    wl = W.make_workload("tiny", rows=4, positions=8, valid_lo=8, V=32776, dtype="bf16", seed=63, std=2.0)
+    case = H.Case(wl)
+    lg = case.logits.float()
+    lg[3] *= 30.0
+    lg[9] += 300.0
+    lg[17] -= 300.0
+    lg = lg.to(torch.bfloat16)
+    host = W.logits_to_host(lg)
+    scale = 1.0 / 31
+    dl, loss, logp, acc = _run_direct(case, scale, logits=lg)
+    ref = OL.loss_fwd_bwd(host, wl.target, case.old, case.adv_tok, wl.mask, wl.eps, scale, True)
+    gp = H.to_f64(logp)
+    assert np.all(np.isfinite(gp))
+    assert np.all(np.abs(gp - ref["logp_tok"]) <= 1e-5 * np.maximum(1, np.abs(ref["logp_tok"])))
+    got, refd = H.to_f64(dl), ref["dlogits"]
+    rowmax = np.max(np.abs(refd), axis=1, keepdims=True)
+    bad = np.abs(got - refd) > 1e-2 * np.abs(refd) + 1e-5 * rowmax
+    bad[H.ambiguous_clip(ref["ratio"], wl.eps)] = False
+    assert not bad.any(), np.argwhere(bad)[:3]
+    res = _lib.grpo_finish_step(acc, loss)
+    assert res["status"] == 0 and res["n_nonfinite"] == 0
+    _, loss_f, logp_f, _ = _run_direct(case, scale, want_grad=False, logits=lg)
+    assert torch.equal(loss_f, loss) and torch.equal(logp_f, logp)
+
+
+@pytest.mark.parametrize("variant", ["c2", "l2"], indirect=True)
+def test_log_probs_are_shift_invariant(variant):
+    # log-softmax is invariant under adding a constant to a row. float32 logits on a 2^-8 grid
+    # plus integer shifts are exact, so every shifted row must give the unshifted row's
+    # log-probs (up to the arithmetic's own error) and the oracle's, up to the library's stated
+    # envelope |LSE| <= 4096; a row shifted past it is reported non-finite.
+    V = 32776
+    rng = np.random.default_rng(65)
+    base = np.round(rng.normal(0, 3.0, V) * 256) / 256
+    shifts = [0.0, 100.0, -100.0, 1000.0, -2000.0, 4000.0, 5000.0]
+    host = np.stack([base + c for c in shifts]).astype(np.float32)
+    assert np.array_equal(host - np.array(shifts, np.float32)[:, None], np.tile(base.astype(np.float32), (7, 1)))
+    T = len(shifts)
+    lg = torch.from_numpy(host).to(DEV)
+    tgt = torch.from_numpy(np.full(T, 123, np.int32)).to(DEV)
+    mask = torch.ones(T, dtype=torch.uint8, device=DEV)
+    adv = torch.ones(T, device=DEV)
+    loss, logp = torch.empty(T, device=DEV), torch.empty(T, device=DEV)
+    dl = torch.empty_like(lg)
+    acc = _lib.new_step_acc(DEV)
+    _lib.grpo_logprob_loss_fwd_bwd(lg, tgt, None, adv, mask, 0.2, 1.0, dl, loss, logp, acc)
+    gp = H.to_f64(logp)
+    ref = OL.log_softmax_row(base)[123]
+    assert np.all(np.abs(gp[:-1] - ref) <= 1e-5 * max(1.0, abs(ref))), (gp, ref)
+    assert np.all(np.abs(gp[1:-1] - gp[0]) <= 2e-6 * max(1.0, abs(ref))), gp
+    assert not np.isfinite(gp[-1])  # |LSE| above 4096: reported, not returned degraded
+    # dlogits (ratio 1, A = 1): p - onehot, the same for every in-range row
+    d = H.to_f64(dl)
+    p = np.exp(OL.log_softmax_row(base))
+    p[123] -= 1.0
+    for r in range(T - 1):
+        assert np.all(np.abs(d[r] - p) <= 2e-5 * np.abs(p) + 1e-6 * np.abs(p).max()), r
+
+
+@pytest.mark.parametrize("variant", ["c2", "l2"], indirect=True)
+def test_logits_beyond_the_shift_range_are_reported_not_wrong(variant):
+    # Rows offset by +-1e30 lie far beyond the envelope |LSE| <= 4096. Their tokens are reported
+    # non-finite and the step is skipped with its gradients zeroed: an answer the caller sees,
+    # never a silently wrong one. The other rows keep the oracle's log-probs.
+    wl = W.make_workload("tiny", rows=4, positions=8, valid_lo=8, V=32776, dtype="bf16", seed=64, std=2.0)
+    case = H.Case(wl)
+    lg = case.logits.float()
+    lg[9] += 1e30
+    lg[17] -= 1e30
+    lg = lg.to(torch.bfloat16)
+    host = W.logits_to_host(lg)
+    dl, loss, logp, acc = _run_direct(case, 1.0 / 31, logits=lg)
+    gp = H.to_f64(logp)
+    assert not np.isfinite(gp[9]) and not np.isfinite(gp[17])
+    ok = np.ones(wl.T, bool)
+    ok[[9, 17]] = False
+    ref = OL.loss_fwd_bwd(host[ok], wl.target[ok], case.old[ok], case.adv_tok[ok], wl.mask[ok], wl.eps,
+                          1.0 / 31, False)
+    assert np.all(np.abs(gp[ok] - ref["logp_tok"]) <= 1e-5 * np.maximum(1, np.abs(ref["logp_tok"])))
+    res = _lib.grpo_finish_step(acc, loss, grad_bufs=[dl])
+    assert res["status"] == _lib.STEP_SKIPPED_NONFINITE and res["n_nonfinite"] == 2
+    assert torch.all(dl == 0)
