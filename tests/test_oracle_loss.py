@@ -250,3 +250,21 @@ def test_entropy_ignores_masked_vocabulary_entries():
     assert t1["entropy"] == pytest.approx(t2["entropy"], rel=1e-14)
     assert l1 == pytest.approx(l2, rel=1e-14)
     assert d1[1] == 0 and np.allclose(np.delete(d1, 1), d2, rtol=1e-13)
+
+
+@pytest.mark.parametrize("c", [1e3, -4e3, 2.0 ** 40, -(2.0 ** 44)])
+def test_objective_is_shift_invariant(c):
+    # log-softmax, and so the whole token objective and its gradient, does not change when a
+    # constant is added to a row. With logits on a 2^-8 grid and shifts that keep them exact in
+    # float64 (up to 2^44), the oracle gives the same numbers at any offset: it subtracts the
+    # row maximum before exponentiating. The library's shift-invariance test compares with it.
+    rng = np.random.default_rng(11)
+    z = np.round(rng.normal(0, 3.0, 64) * 256) / 256
+    zc = z + c
+    assert np.array_equal(zc - c, z)
+    base = L.token_objective(z, 5, -2.0, 0.7, 1, 0.2, 1.0 / 7, True)
+    shifted = L.token_objective(zc, 5, -2.0, 0.7, 1, 0.2, 1.0 / 7, True)
+    for a, b in zip(base[:3], shifted[:3]):  # loss, log-prob, ratio
+        assert abs(a - b) <= 1e-12 * max(1.0, abs(a))
+    assert base[3] == shifted[3]  # the clip decision
+    assert np.allclose(base[4], shifted[4], rtol=1e-12, atol=1e-15)
