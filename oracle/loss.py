@@ -55,9 +55,11 @@ def as_f64(logits: np.ndarray) -> np.ndarray:
 
 
 def log_softmax_row(z: np.ndarray) -> np.ndarray:
+    # (z - max) - log sum exp(z - max): the definition z - log sum exp(z), written so that no
+    # large quantity is subtracted from another (exact under any shift that keeps z exact)
     m = np.max(z)
-    lse = m + math.log(float(np.sum(np.exp(z - m))))
-    return z - lse
+    d = z - m
+    return d - math.log(float(np.sum(np.exp(d))))
 
 
 KL_NONE, KL_K1, KL_K3 = 0, 1, 2
