@@ -38,10 +38,19 @@ KERNEL_SRC = tuple(os.path.join(ROOT, "rl_post_token_gb300", "csrc", f)
                    for f in ("grpo_rowpass_kernels.cuh", "grpo_common.cuh"))
 
 
+def _code_only(text: str) -> str:
+    """The source without comments, trailing spaces or blank lines: what the compiler sees."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_sha256() -> str:
+    """Hash of the row-pass kernels' device code (comments ignored), tying the committed ncu
+    traffic figure to the code it was measured on."""
     h = hashlib.sha256()
     for f in KERNEL_SRC:
-        h.update(open(f, "rb").read())
+        h.update(_code_only(open(f, encoding="utf-8").read()).encode())
     return h.hexdigest()
 
 

@@ -9,19 +9,24 @@
 // the window" (ratio against the frozen pi_old, epsilon clip). The surrogate's formula is the
 // standard PPO clip; the pages do not print it.
 //
-// Two kernels serve one entry point:
+// Three kernels serve one entry point:
 //  * row_l2_kernel      -- any dtype / V / alignment. A CTA owns a row: pass 1 streams the row
 //                          from HBM with 16-byte loads keeping an online (max, sum-exp);
 //                          pass 2 re-reads it (from L2 when the working set fits) and writes
 //                          dlogits with 16-byte streaming stores.
-//  * row_cluster_kernel -- bf16 rows with V % 8 == 0 and 16-byte aligned rows: a cluster of
-//                          C CTAs splits each row; every CTA bulk-copies its slice into shared
-//                          memory once (cp.async.bulk + mbarrier), both passes run from shared
-//                          memory, and the CTAs exchange their (max, sum-exp) pairs and the
-//                          target logit through distributed shared memory. HBM traffic is one
-//                          read and one write of the row.
+//  * row_cluster_kernel -- bf16 (V % 8 == 0) or float32 (V % 4 == 0) rows, 16-byte aligned: a
+//                          cluster of C CTAs splits each row; every CTA streams its slice
+//                          through a shared-memory ring (cp.async.bulk + mbarrier), both passes
+//                          run from shared memory, and the CTAs exchange their (shift, sum-exp)
+//                          pairs and the target logit through distributed shared memory. HBM
+//                          traffic is one read and one write of the row.
+//  * row_fwd_kernel     -- the same split for forward-only calls without extra terms (the
+//                          pi_old ahead pass): no per-row barrier, partials sent to CTA 0 and
+//                          combined there by a dedicated warp, the same bits.
 // Each row's reduction order depends only on V and the kernel's fixed shape, never on T or on
-// how the step was chunked, so chunked and un-chunked calls agree bit for bit.
+// how the step was chunked, so chunked and un-chunked calls agree bit for bit. The log-prob is
+// formed as (z_y - shift) - log(sum) from the shift every term used, without cancellation;
+// rows with |LSE| above kLseMax are reported non-finite.
 #include <algorithm>
 #include <type_traits>
 
@@ -341,11 +346,13 @@ __global__ void __launch_bounds__(NT) row_l2_kernel(RowArgs a) {
 // ------------------------------------------------------------------------------------------
 // Cluster kernel: a row is split across the C CTAs of a cluster; CTA r owns the slice
 // [r*Vs, r*Vs + n_r) and keeps it in shared memory for both passes. Warp 0 is the producer:
-// one lane issues the slice as 32 KB bulk copies, each completing on its own "full"
-// mbarrier, and refills chunk k with the next row as soon as every consumer warp has released
-// it on its "empty" mbarrier (so the next row streams in during this row's pass 2). Warps
-// 1..NCW consume: pass 1 (online max / sum-exp) from shared memory, a fixed-order reduction,
-// one cluster barrier per row to exchange (max, sum-exp) and the target logit through
+// one lane issues the slice as bulk copies of one chunk each (32 KB, or 16 KB for the
+// entropy instances where two CTAs share an SM) into a ring of slots, each completing on its
+// own "full" mbarrier, and refills a slot as soon as every consumer warp has released it on
+// its "empty" mbarrier. Slots beyond the row's chunks carry the next row's first chunks while
+// the current row is exchanged. Warps 1..NCW consume: pass 1 (a log2-domain sum against a lazy
+// shift) from shared memory, a fixed-order reduction (shuffle trees within and across warps),
+// one cluster barrier per row to exchange (shift, sum) and the target logit through
 // distributed shared memory, then pass 2 (dlogits) from shared memory with 16-byte streaming
 // stores. HBM sees one read and one write of each row.
 // ------------------------------------------------------------------------------------------
