@@ -67,13 +67,22 @@ __device__ __forceinline__ MS ms2_combine(MS a, MS b) {
   return {m, a.s * ex2(a.m - m) + b.s * ex2(b.m - m)};
 }
 
+// Warp maximum of a float in one reduction instruction (NaN inputs are ignored, as fmaxf does).
+__device__ __forceinline__ float warp_max_f32(float x) {
+  float r;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// The warp's log2-domain (shift, sum) pairs combined: the largest shift M by one reduction,
+// every lane's sum rescaled to it, the sums added by a fixed pairwise tree. Lane 0's result
+// is the warp's (its order of additions is fixed). A warp without mass gives (-inf, 0).
 __device__ __forceinline__ MS warp_ms2(MS v) {
+  const float M = warp_max_f32(v.m);
+  float s = M == -INFINITY ? 0.f : v.s * ex2(v.m - M);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    MS w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o)};
-    v = ms2_combine(v, w);
-  }
-  return v;
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return {M, s};
 }
 
 // The partials of each W-lane group of the warp (W a power of two, at most 32) combined by a
@@ -202,13 +211,26 @@ __device__ __forceinline__ MS3 ms3_combine2(MS3 a, MS3 b) {
 
 template <bool LOG2>
 __device__ __forceinline__ MS3 warp_ms3(MS3 v) {
+  if constexpr (LOG2) {
+    // as warp_ms2: one maximum, one rescale per lane, two fixed addition trees
+    const float M = warp_max_f32(v.m);
+    const float f = M == -INFINITY ? 0.f : ex2(v.m - M);
+    float s = v.s * f, s2 = v.s2 * f;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    MS3 w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o),
-          __shfl_xor_sync(0xffffffffu, v.s2, o)};
-    v = LOG2 ? ms3_combine2(v, w) : ms3_combine(v, w);
+    for (int o = 16; o > 0; o >>= 1) {
+      s += __shfl_xor_sync(0xffffffffu, s, o);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+    }
+    return {M, s, s2};
+  } else {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      MS3 w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o),
+            __shfl_xor_sync(0xffffffffu, v.s2, o)};
+      v = ms3_combine(v, w);
+    }
+    return v;
   }
-  return v;
 }
 
 template <int W>
