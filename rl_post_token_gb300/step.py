@@ -92,13 +92,17 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
     boundaries change no bit, so the step is one call; ``chunk_ready`` and ``side_stream`` do
     not apply, and ``launch_events`` receives one pair per step.
 
-    ``side_stream`` (optional): the chunks of a step alternate between ``stream`` and this
-    stream, so that the next chunk's blocks take the SMs the current chunk's last rows leave
-    idle. Chunks of a step write disjoint rows and only add to the step's integer counters, so
-    the results are the same bits; the step's finish waits for both streams."""
+    ``side_stream`` (optional, a stream or a list of streams): the chunks of a step rotate
+    between ``stream`` and these streams, so that the next chunk's blocks take the SMs the
+    current chunk's last rows leave idle. Chunks of a step write disjoint rows and only add to
+    the step's integer counters, so the results are the same bits; the step's finish waits for
+    every stream."""
     import torch
 
     st = torch.cuda.current_stream() if stream is None else stream
+    sides = [] if side_stream is None else (list(side_stream) if isinstance(side_stream, (list, tuple))
+                                            else [side_stream])
+    rotation = [st] + sides
     launches = 0
     if rewards is not None:
         _lib.grpo_group_advantage(rewards, group_size, adv_eps, True, adv_rollout, row_rollout,
@@ -118,12 +122,13 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
             launches += _host_step(bp, s, logits_host, staging, block_rows, copy_stream, st, dlogits, target,
                                    old_logp, adv_tok, mask, loss_tok, logp_tok, acc, clip_eps, scale, tok_src,
                                    w_tok, terms, V, launch_events)
-        elif side_stream is not None:
-            side_stream.wait_stream(st)  # the advantage and the previous step's finish
+        else:
+            for ss in sides:
+                ss.wait_stream(st)  # the advantage and the previous step's finish
         chunks = range(0) if logits_host is not None else range(p["step_chunk_off"][s], p["step_chunk_off"][s + 1])
         for i, c in enumerate(chunks):
             a, b = int(bp.exec_tok_off[c]), int(bp.exec_tok_off[c + 1])
-            cs = side_stream if side_stream is not None and i % 2 == 1 else st
+            cs = rotation[i % len(rotation)]
             if chunk_ready is not None:
                 cs.wait_event(chunk_ready[c])
             if b == a:
@@ -158,8 +163,9 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
                 e1.record(cs)
                 launch_events.append((e0, e1))
             launches += 1
-        if side_stream is not None and logits_host is None:
-            st.wait_stream(side_stream)
+        if logits_host is None:
+            for ss in sides:
+                st.wait_stream(ss)
         t0, t1 = bp.step_tok_range[s]
         e0, e1 = bp.step_exec_range[s]
         grads = [] if dlogits is None or e1 == e0 else [dlogits[e0:e1]]
