@@ -6,7 +6,9 @@ every row:
 * every row: finite dlogits; each valid row's dlogits sum to ~0 (softmax and one-hot both sum
   to one); masked and padding rows exactly zero; per-step N equals the planner's N;
 * the forward-only pass over the same batch: every token's loss and log-prob the bits of the
-  full pass.
+  full pass;
+* the headline batch streamed from pinned host memory (the host entry point): the device run's
+  bits.
 
 pi_old here is target logit - 12 + N(0, 0.05): a plain input recipe (no log-softmax) that puts
 the ratio far below 1, so tokens with A < 0 take the clipped branch and tokens with A > 0 the
@@ -79,6 +81,26 @@ def test_full_size_batch(name):
     for a, b in zip(res_f, res):
         for k in ("loss", "n_valid", "n_clipped", "n_nonfinite", "n_tokens", "status"):
             assert a[k] == b[k], k
+
+    if name == "qwen_step":
+        # the same batch streamed from pinned host memory through the host entry point (the
+        # bench's e2e path): the device run's bits, at full size
+        lh = logits.cpu().pin_memory()
+        staging = torch.empty(2 * 1024 * logits.stride(0) * logits.element_size(), dtype=torch.uint8, device=DEV)
+        dl_h = torch.empty_like(logits)
+        loss_h = torch.full((T,), -7.0, device=DEV)
+        logp_h = torch.full((T,), -7.0, device=DEV)
+        accs_h = torch.zeros_like(accs)
+        S.run_batch(bp, logits=None, logits_host=lh, staging=staging, block_rows=1024, copy_stream=torch.cuda.Stream(),
+                    dlogits=dl_h, target=t(wl.target), old_logp=t(old), mask=t(wl.mask), adv_tok=t(adv),
+                    loss_tok=loss_h, logp_tok=logp_h, accs=accs_h, clip_eps=wl.eps,
+                    tok_src=None if tok_src is None else t(tok_src), V=wl.V)
+        torch.cuda.synchronize()
+        assert torch.equal(dl_h.view(torch.int16), dl.view(torch.int16))
+        assert torch.equal(loss_h.view(torch.int32), loss.view(torch.int32))
+        assert torch.equal(logp_h.view(torch.int32), logp.view(torch.int32))
+        assert S.read_results(accs_h, bp.n_steps) == res
+        del lh, dl_h
 
     # sampled exec rows: the first and last of every chunk plus a seeded handful
     rng = np.random.default_rng(2)
