@@ -641,6 +641,26 @@ def _gpu_index(local: int) -> int:
     return local
 
 
+def _h2d_copy_gbs(host, dev, stream, reps: int = 8) -> float:
+    """GB/s of `reps` plain host->device copies from the start of the pinned tensor `host`
+    into `dev` (`dev`'s size, or all of `host` if smaller), timed with CUDA events on
+    `stream`: the host link's rate at that moment."""
+    import torch
+
+    src = host.reshape(-1).view(torch.uint8)
+    n = min(src.numel(), dev.numel())
+    src, dev = src[:n], dev[:n]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        dev.copy_(src, non_blocking=True)
+        e0.record(stream)
+        for _ in range(reps):
+            dev.copy_(src, non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    return reps * dev.numel() / (e0.elapsed_time(e1) / 1e3) / 1e9
+
+
 def run_e2e(batch, device, stream, steps: int):
     """Same metric through the public API with HOST inputs. Every step:
     - the logits stream from pinned host memory through the library's host entry point
@@ -673,14 +693,20 @@ def run_e2e(batch, device, stream, steps: int):
         stream.synchronize()
 
     one_step()
+    link_before = _h2d_copy_gbs(host_logits, staging, copy)
     t0 = time.perf_counter()
     for _ in range(steps):
         one_step()
     dt = time.perf_counter() - t0
+    link_after = _h2d_copy_gbs(host_logits, staging, copy)
     h2d = host_logits.numel() * host_logits.element_size() + sum(v.numel() * v.element_size() for v in side.values())
     return {"value": batch.wl.n_valid * steps / dt, "elapsed_s": dt, "units": batch.wl.n_valid * steps,
             "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(host_res.numel()), "steps": steps,
+            "h2d_gbs": h2d * steps / dt / 1e9,
+            "link_copy_gbs": {"before": link_before, "after": link_after,
+                              "what": "plain pinned host->device copies of the staging buffer's size, "
+                                      "on the copy stream, just before and just after the timed steps"},
             "how": "pinned host logits streamed by grpo_logprob_loss_fwd_bwd_host (1024-row blocks through a "
                    "two-block device staging buffer, copies overlapped with the row pass); side inputs copied "
                    "and step results read back every step"}
