@@ -32,7 +32,9 @@ Readings where the pages are silent:
   (contiguous blocks, which is also what the explainer's figure draws);
 * compaction runs one optimizer step, so ``mini`` must be 0 or ``batch``;
 * the dynamic binning rule (longest-processing-time greedy with a capacity check) is ours:
-  the pages name no partition algorithm.
+  the pages name no partition algorithm. Where the budget does not bind, the rule is plain
+  LPT list scheduling, and the tests pin it there to Graham's tight instance (heaviest bin
+  4k-1 against the optimum 3k) and to his 4/3 - 1/(3k) bound against brute force.
 """
 from __future__ import annotations
 

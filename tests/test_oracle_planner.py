@@ -227,6 +227,63 @@ def test_dynamic_bin_count_and_brute_force_tiny():
     assert k >= best == 3
 
 
+def _graham_rows(k):
+    """Graham's tight instance for longest-processing-time-first list scheduling on k
+    machines: two jobs each of lengths 2k-1 down to k+1, and three of length k."""
+    return [L for L in range(2 * k - 1, k, -1) for _ in range(2)] + [k] * 3
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_dynamic_lpt_graham_tight_instance(k):
+    # With the token budget out of the way (budget = total) and k bins forced by min_bins,
+    # the binning is plain LPT: the heaviest bin of Graham's instance carries exactly 4k-1
+    # tokens, while the best split carries 3k. A rule that fills the fullest bin, visits rows
+    # in ascending or input order, or finds the optimum instead, gives another figure.
+    row_len = _graham_rows(k)
+    n = len(row_len)
+    cfg = P.PlanConfig(batch=n, dynamic=1, max_token_len=sum(row_len), min_bins=k)
+    p = P.plan(cfg, row_len, row_len)
+    assert p.n_chunks == k
+    assert max(p.chunk_tokens) == 4 * k - 1
+    assert sum(p.chunk_tokens) == 3 * k * k
+    if k == 2:
+        # rows 0..4 = 3, 3, 2, 2, 2: 3 -> bin 0, 3 -> bin 1, then the ties go to the lower bin
+        assert [p.row_src[p.chunk_row_off[c]:p.chunk_row_off[c + 1]] for c in range(2)] == [[0, 2, 4], [1, 3]]
+
+
+def _best_makespan(row_len, k):
+    import itertools
+    w = np.asarray(row_len, np.int64)
+    best = None
+    for assign in itertools.product(range(k), repeat=len(row_len)):
+        if assign[0] != 0:  # bins are interchangeable: fix the first row's bin
+            continue
+        loads = np.bincount(np.asarray(assign), weights=w, minlength=k)
+        m = int(loads.max())
+        best = m if best is None else min(best, m)
+    return best
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_dynamic_lpt_bound_against_brute_force(seed):
+    # Graham's bound for LPT on k machines: makespan <= (4/3 - 1/(3k)) * optimum, with the
+    # optimum found by brute force over every assignment of up to 8 rows to k <= 3 bins.
+    rng = np.random.default_rng(7000 + seed)
+    n = int(rng.integers(4, 9))
+    k = int(rng.integers(2, 4))
+    row_len = [int(x) for x in rng.integers(1, 60, n)]
+    cfg = P.PlanConfig(batch=n, dynamic=1, max_token_len=sum(row_len), min_bins=k)
+    p = P.plan(cfg, row_len, row_len)
+    assert p.n_chunks == k
+    opt = _best_makespan(row_len, k)
+    assert 3 * k * max(p.chunk_tokens) <= (4 * k - 1) * opt
+    # list scheduling: the heaviest bin's last row arrived when that bin was the lightest
+    heavy = int(np.argmax(p.chunk_tokens))
+    members = p.row_src[p.chunk_row_off[heavy]:p.chunk_row_off[heavy + 1]]
+    last = min(members, key=lambda r: (row_len[r], -r))  # visited last: smallest length, then largest index
+    assert k * (max(p.chunk_tokens) - row_len[last]) <= sum(row_len) - row_len[last]
+
+
 def test_restore_roundtrip():
     row_len = [100, 900, 50, 700, 300, 20, 1500, 10]
     cfg = P.PlanConfig(batch=8, dynamic=1, max_token_len=2048, workload=1, balance_ends=1)

@@ -117,3 +117,17 @@ def test_token_index(grpo_lib):
         toks = list(range(off[r], off[r + 1]))
         want += [-1 - t for t in toks] if p["row_pad"][j] else toks
     assert idx.tolist() == want
+
+
+@pytest.mark.parametrize("k", [2, 3, 4, 6])
+@pytest.mark.parametrize("workload", [0, 1])
+def test_dynamic_graham_instances(grpo_lib, k, workload):
+    # Graham's tight LPT instance (two rows each of 2k-1 .. k+1 tokens, three of k) with the
+    # token budget out of the way and k bins forced; both workload estimates
+    row_len = [L for L in range(2 * k - 1, k, -1) for _ in range(2)] + [k] * 3
+    n = len(row_len)
+    cfg = dict(batch=n, group_size=1, dynamic=1, max_token_len=sum(row_len), min_bins=k, workload=workload)
+    c = _assert_same(cfg, row_len, row_len)
+    assert c["n_chunks"] == k
+    if workload == 0:
+        assert int(c["chunk_tokens"].max()) == 4 * k - 1
