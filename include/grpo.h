@@ -18,8 +18,8 @@
  *     GRPO_ERR_* code. No function aborts or prints.
  *   - Ownership: every buffer belongs to the caller, and the library never frees caller
  *     memory. The library allocates no device memory of its own with two exceptions:
- *       - the LM-head backward's first call on a device creates a cuBLAS handle, with
- *         cuBLAS's own workspace;
+ *       - the LM-head backward's first call on a device creates a cuBLAS handle (its GEMMs
+ *         run in a region of the caller's workspace);
  *       - the module's 16 MiB device array of grpo_lmhead_forward_noalloc is held by every
  *         GPU that loads the library.
  *     "device" pointers are CUDA device memory of the current device; "host" pointers are
@@ -402,11 +402,13 @@ GRPO_API int grpo_window_rollup(const grpo_window* w, double* loss, int64_t* den
 
 /* Bytes of device workspace grpo_lmhead_loss_fwd_bwd needs for [T, H] hidden states and a
  * [V, H] output embedding: per-(token, 256-wide vocabulary tile) softmax partials, per-token
- * LSE and coefficients, and one bf16 dlogits chunk of 16384 vocabulary columns. 0 on bad sizes. */
+ * LSE and coefficients, one bf16 dlogits chunk of 16384 vocabulary columns, and 32 MiB of
+ * scratch for the backward's cuBLAS GEMMs. 0 on bad sizes. */
 GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H);
 
 /* Bytes of workspace that select the stored path of grpo_lmhead_loss_fwd_bwd: the partials
- * above plus a bf16 [T, 256 * ceil(V/256)] matrix (about 2*T*V bytes). 0 on bad sizes. */
+ * above plus a bf16 [T, 256 * ceil(V/256)] matrix (about 2*T*V bytes) and the same 32 MiB of
+ * GEMM scratch. 0 on bad sizes. */
 GRPO_API size_t grpo_lmhead_workspace_size_stored(int64_t T, int64_t V, int64_t H);
 
 /* The same loss with the logits produced on the tensor cores: z = h W^T, computed tile by tile
@@ -429,7 +431,10 @@ GRPO_API size_t grpo_lmhead_workspace_size_stored(int64_t T, int64_t V, int64_t 
  *  d_h        device float [T, H] or NULL; dW device float [V, H] or NULL (both NULL: forward only)
  *  loss_tok, logp_tok (or NULL)  device float [T]
  *  acc        device grpo_step_acc (counts as in grpo_logprob_loss_fwd_bwd)
- *  workspace  device, >= grpo_lmhead_workspace_size(T, V, H) bytes, caller-owned
+ *  workspace  device, 256-byte aligned, >= grpo_lmhead_workspace_size(T, V, H) bytes,
+ *             caller-owned; it holds all of the call's scratch, the GEMMs' included, so calls
+ *             may overlap (several streams, several host threads) as long as each has its own
+ *             workspace and outputs
  * Errors: GRPO_ERR_INVALID (sizes, NULL, alignment), GRPO_ERR_CAPACITY (workspace too small),
  * GRPO_ERR_UNSUPPORTED (tensor-map creation), GRPO_ERR_CUDA. */
 GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, int64_t T, int64_t V, int64_t H,

@@ -591,12 +591,16 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cublasHandle_t blas_handle() {
+// The current device's cuBLAS handle, created on first use. A handle's stream and workspace
+// are settings of the handle, so the caller holds `lock` (taken here) from setting them until
+// its last GEMM is enqueued: calls from several host threads then never enqueue on one
+// another's stream or scratch.
+cublasHandle_t blas_handle(std::unique_lock<std::mutex>& lock) {
   static cublasHandle_t h[64] = {};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
+  lock = std::unique_lock<std::mutex>(mu);
   if (!h[dev] && cublasCreate(&h[dev]) != CUBLAS_STATUS_SUCCESS) h[dev] = nullptr;
   return h[dev];
 }
@@ -670,8 +674,12 @@ using namespace grpo::lmhead;
 
 namespace {
 
+// Scratch of the backward GEMMs, a region of the caller's workspace: each call brings its own,
+// so GEMMs of calls that overlap on several streams share none.
+constexpr size_t kBlasWorkspaceBytes = (size_t)32 << 20;
+
 struct WsLayout {
-  size_t part_m, part_s, zy, lse2, coef, dz, total;
+  size_t part_m, part_s, zy, lse2, coef, dz, blas, total;
   int n_col_tiles;
   int64_t vchunk;  // columns of the dz region: one recompute chunk, or (stored) every tile
 };
@@ -689,6 +697,7 @@ WsLayout ws_layout(int64_t T, int64_t V, int64_t vchunk, bool stored = false) {
   w.lse2 = off; off += up((size_t)T * 4);
   w.coef = off; off += up((size_t)T * 4);
   w.dz = off; off += up((size_t)T * w.vchunk * 2);
+  w.blas = off; off += kBlasWorkspaceBytes;
   w.total = off;
   return w;
 }
@@ -717,6 +726,7 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
   if (T == 0) return GRPO_OK;
   if (!h || !W || !target || !adv_tok || !mask || !loss_tok || !workspace) return GRPO_ERR_INVALID;
   if (((uintptr_t)h | (uintptr_t)W) & 15u) return GRPO_ERR_INVALID;
+  if ((uintptr_t)workspace & 255u) return GRPO_ERR_INVALID;
   if (T > INT32_MAX / 2 || V > INT32_MAX / 2) return GRPO_ERR_INVALID;
   // the stored path when there is a backward pass and room for the whole exponent matrix
   const bool stored = (d_h || dW) && workspace_bytes >= ws_layout(T, V, kDefaultVChunk, true).total;
@@ -767,8 +777,11 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
   GRPO_CUDA_TRY(cudaGetLastError());
   if (!d_h && !dW) return GRPO_OK;
 
-  cublasHandle_t bh = blas_handle();
-  if (!bh || cublasSetStream(bh, st) != CUBLAS_STATUS_SUCCESS) return GRPO_ERR_CUDA;
+  std::unique_lock<std::mutex> blas_lock;
+  cublasHandle_t bh = blas_handle(blas_lock);
+  if (!bh || cublasSetStream(bh, st) != CUBLAS_STATUS_SUCCESS ||
+      cublasSetWorkspace(bh, wsb + ws.blas, kBlasWorkspaceBytes) != CUBLAS_STATUS_SUCCESS)
+    return GRPO_ERR_CUDA;
   const float one = 1.f, zero = 0.f;
   if (stored) {
     // dlogits in place over the stored exponents, then each backward GEMM over the whole vocabulary
