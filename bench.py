@@ -403,6 +403,7 @@ def run_lmhead(args):
     e1.record(stream)
     torch.cuda.synchronize(device)
     full_s = e0.elapsed_time(e1) / 1e3 / args.steps
+    res = _lib.read_step_result(acc)  # the headline step's result (the stored-exponent path)
     step(old=old, w=ws_small)
     r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     r0.record(stream)
@@ -419,28 +420,55 @@ def run_lmhead(args):
     torch.cuda.synchronize(device)
     fwd_s = f0.elapsed_time(f1) / 1e3 / args.steps
     clk = clocks.stop()
-    res = _lib.read_step_result(acc)
 
-    # e2e: the step's inputs start in pinned host memory (hidden states, weights, side arrays)
-    # and are copied up every step; the step result is read back
+    # e2e: every step's inputs (hidden states, weights, side arrays) start in pinned host memory
+    # and are copied up on a copy stream into one of two device input sets, the next step's
+    # copy overlapping this step's compute (the first step's copy does not overlap); the step
+    # result is read back every step
     host = {"h": h.cpu().pin_memory(), "Wt": Wt.cpu().pin_memory(), "target": target.cpu().pin_memory(),
             "mask": mask.cpu().pin_memory(), "rewards": rewards.cpu().pin_memory(), "old": old.cpu().pin_memory()}
     dev_in = {"h": h, "Wt": Wt, "target": target, "mask": mask, "rewards": rewards, "old": old}
+    sets = [dev_in, {k: torch.empty_like(v) for k, v in dev_in.items()}]
     host_res = torch.empty(64, dtype=torch.uint8, pin_memory=True)
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    copy = torch.cuda.Stream(device)
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    used = [torch.cuda.Event(), torch.cuda.Event()]
+    for e in used:
+        e.record(stream)
 
-    def e2e_step():
-        for k, v in host.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        step(old=old)
+    def upload(k):
+        s = sets[k % 2]
+        copy.wait_event(used[k % 2])  # the step that last read this set is done
+        with torch.cuda.stream(copy):
+            for name, v in host.items():
+                s[name].copy_(v, non_blocking=True)
+        copied[k % 2].record(copy)
+
+    def e2e_step(k, n):
+        if k == 0:
+            upload(0)
+        if k + 1 < n:
+            upload(k + 1)
+        s = sets[k % 2]
+        stream.wait_event(copied[k % 2])
+        _lib.grpo_group_advantage(s["rewards"], wl.group_size, 1e-6, True, adv_r, row_rollout, row_tok_off, adv)
+        _lib.grpo_lmhead_loss_fwd_bwd(s["h"], s["Wt"], s["target"], s["old"], adv, s["mask"], wl.eps,
+                                      1.0 / max(N, 1), d_h, dW, loss, logp, acc, ws)
+        _lib.grpo_finish_step(acc, loss, expected_N=N, sync=False)
+        used[k % 2].record(stream)
         host_res.copy_(acc[64:128], non_blocking=True)
         stream.synchronize()
 
-    e2e_step()
+    for k in range(2):
+        e2e_step(k, 2)
+    torch.cuda.synchronize(device)
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
+    for k in range(e2e_steps):
+        e2e_step(k, e2e_steps)
     e2e_s = (time.perf_counter() - t0) / e2e_steps
+    copy.synchronize()
+    e2e_res = _lib.read_step_result(acc)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     flops = 6.0 * T * V * Hd
     peak, kind = bf16_peak(sustained=True)
@@ -463,8 +491,10 @@ def run_lmhead(args):
         "step_result": {k: res[k] for k in ("loss", "n_valid", "clipfrac", "status")},
         "e2e": {"value": N / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(host_res.numel()), "steps": e2e_steps,
-                "how": "hidden states, weights and side inputs copied from pinned host memory every step, "
-                       "the step result read back"},
+                "how": "hidden states, weights and side inputs copied from pinned host memory every step on a "
+                       "copy stream into one of two device input sets (the next step's copy overlaps this step's "
+                       "compute, the first step's does not), the step result read back every step",
+                "step_result_matches": all(e2e_res[k] == res[k] for k in ("loss", "n_valid", "clipfrac", "status"))},
         # per step: the advantage (2), pass A, the per-token reduce and dz-from-e (3; the two
         # cuBLAS GEMMs are not counted), the finish (1)
         "gpu_launches": 6 * args.steps,
@@ -545,7 +575,7 @@ def run_gb300(args):
 
     ahead = run_ahead(batch, stream, steps=min(args.steps, 30))
     barrier(world, device)
-    e2e = run_e2e(batch, device, stream, steps=min(args.steps, args.e2e_steps))
+    e2e = run_e2e(batch, device, stream, steps=min(args.steps, args.e2e_steps), ref_results=results)
     # whole job: every rank's tokens over the slowest rank's time, as for `value`
     e2e_el, e2e_units = reduce_timing(e2e.pop("elapsed_s"), e2e.pop("units"), world, device)
     e2e["value"] = e2e_units / e2e_el
@@ -661,7 +691,7 @@ def _h2d_copy_gbs(host, dev, stream, reps: int = 8) -> float:
     return reps * dev.numel() / (e0.elapsed_time(e1) / 1e3) / 1e9
 
 
-def run_e2e(batch, device, stream, steps: int):
+def run_e2e(batch, device, stream, steps: int, ref_results=None):
     """Same metric through the public API with HOST inputs. Every step:
     - the logits stream from pinned host memory through the library's host entry point
       (`grpo_logprob_loss_fwd_bwd_host`): 1024-row blocks into a two-block device staging
@@ -694,16 +724,26 @@ def run_e2e(batch, device, stream, steps: int):
 
     one_step()
     link_before = _h2d_copy_gbs(host_logits, staging, copy)
+    step_s = []
     t0 = time.perf_counter()
     for _ in range(steps):
+        ts = time.perf_counter()
         one_step()
+        step_s.append(time.perf_counter() - ts)
     dt = time.perf_counter() - t0
     link_after = _h2d_copy_gbs(host_logits, staging, copy)
+    from rl_post_token_gb300 import step as S
+    keys = ("loss", "n_valid", "clipfrac", "status")
+    got = [{k: r[k] for k in keys} for r in S.read_results(host_res, batch.bp.n_steps)]
+    match = None if ref_results is None else got == [{k: r[k] for k in keys} for r in ref_results]
     h2d = host_logits.numel() * host_logits.element_size() + sum(v.numel() * v.element_size() for v in side.values())
     return {"value": batch.wl.n_valid * steps / dt, "elapsed_s": dt, "units": batch.wl.n_valid * steps,
             "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(host_res.numel()), "steps": steps,
             "h2d_gbs": h2d * steps / dt / 1e9,
+            "step_ms": [round(1e3 * x, 2) for x in step_s],
+            "value_at_median_step": batch.wl.n_valid / float(np.median(step_s)),
+            "step_results_match": match,
             "link_copy_gbs": {"before": link_before, "after": link_after,
                               "what": "plain pinned host->device copies of the staging buffer's size, "
                                       "on the copy stream, just before and just after the timed steps"},
