@@ -206,6 +206,37 @@ def oracle_sample_rate(wl, n_tokens: int, budget_s: float):
     return done / dt, done, dt
 
 
+def oracle_lmhead_rate(wl, n_tokens: int, budget_s: float):
+    """Time the float64 LM-head oracle (z = h W^T, the objective, d_h and dW) on `n_tokens`
+    hidden states of a host-drawn sample at the workload's V and H, repeating the call until
+    `budget_s` has passed (at least once). Returns (valid tokens/s, tokens timed, seconds)."""
+    from oracle import loss as OL
+    from rl_post_token_gb300 import workloads as W
+
+    H = wl.extra["H"]
+    n = min(wl.T, n_tokens)
+    rng = np.random.default_rng(wl.seed + 7)
+    h = W.bf16_round_bits(rng.standard_normal((n, H), dtype=np.float32) * np.float32(wl.extra["h_std"]))
+    w = W.bf16_round_bits(rng.standard_normal((wl.V, H), dtype=np.float32) * np.float32(wl.extra["w_std"]))
+    tgt, msk, adv = wl.target[:n], wl.mask[:n], np.where(np.arange(n) % 2, 1.0, -1.0)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        OL.lmhead_fwd_bwd(h, w, tgt, None, adv, msk, wl.eps, 1.0)
+        done += int(msk.sum())
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done / dt, done, dt
+
+
+def _blas_threads() -> int:
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(k, "")
+        if v.isdigit() and int(v) > 0:
+            return int(v)
+    return os.cpu_count() or 1
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -213,11 +244,21 @@ def run_reference(args):
     from rl_post_token_gb300 import workloads as W
     wl = W.make_workload(args.workload, seed=0)
     per_step_s = 0.5
+    if args.workload == "lmhead":
+        # one call of the LM-head oracle on 4 tokens per step (its products use every BLAS thread)
+        rate = lambda budget: oracle_lmhead_rate(wl, 4, budget)
+        cores = _blas_threads()
+        sample = "float64 numpy LM-head oracle (z = h W^T, objective, d_h, dW), 4 host-drawn tokens per step"
+    else:
+        rate = lambda budget: oracle_sample_rate(wl, 16, budget)
+        cores = 1
+        sample = (f"float64 numpy oracle, first 16 tokens of a host-drawn batch of the workload, "
+                  f"{per_step_s}s per step")
     for _ in range(args.warmup):
-        oracle_sample_rate(wl, 16, per_step_s / 4)
+        rate(per_step_s / 4)
     done, dt = 0, 0.0
     for _ in range(args.steps):
-        _, n, d = oracle_sample_rate(wl, 16, per_step_s)
+        _, n, d = rate(per_step_s)
         done += n
         dt += d
     v = done / dt
@@ -227,9 +268,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[args.workload], "parallelism": "rank 0 only"},
-        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "host_cpus": os.cpu_count(), "kind": "oracle",
-                         "sample": f"float64 numpy oracle, first 16 tokens of a host-drawn batch of the "
-                                   f"workload, {per_step_s}s per step"},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "host_cpus": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -501,7 +541,15 @@ def run_lmhead(args):
     }
     if clk is not None:
         line["clocks"] = clk
-    print(json.dumps(line), flush=True)
+    if rank == 0 and not args.no_cpu_baseline:
+        v, n, dt = oracle_lmhead_rate(wl, 16, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": _blas_threads(), "host_cpus": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": f"float64 numpy LM-head oracle (z = h W^T, objective, d_h, dW; its "
+                                          f"products on every BLAS thread), 16 host-drawn tokens per call, "
+                                          f"{n} valid tokens in {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
     return 0
 
 
