@@ -3,8 +3,10 @@ the repository root, so that the library's per-kernel launch caches start empty)
 
 Several host threads, each on its own CUDA stream with its own outputs, call the library at
 the same time: every row-pass instance (plain, forward-only, with KL / entropy / weights, the
-L2 kernel for short rows, both logit types) and both LM-head backward paths. Each result must
-equal, bit for bit, the same call made alone afterwards. Prints ``THREADS_OK <n>`` (n
+L2 kernel for short rows, both logit types), the row pass over pinned host logits, and both
+LM-head backward paths, each call followed by its step finish. Each result (per-token outputs,
+gradients, the finished step's result) must equal, bit for bit, the same call made alone
+afterwards. Prints ``THREADS_OK <n>`` (n
 compared buffers) and exits 0, or prints the first mismatch and exits 1."""
 import sys
 import threading
@@ -71,6 +73,30 @@ class RowCase:
         _lib.grpo_logprob_loss_fwd_bwd(self.logits, self.target, self.old, self.adv, self.mask, 0.2,
                                        1.0 / 700, o.get("dl"), o["loss"], o["logp"], o["acc"],
                                        stream=stream, terms=terms)
+        _lib.grpo_finish_step(o["acc"], o["loss"], sync=False, stream=stream)
+
+
+class HostCase(RowCase):
+    """The row pass over pinned host logits: each caller has its own staging buffer and copy
+    stream (32-row blocks, so a call runs several blocks through the two halves)."""
+
+    BLOCK = 32
+
+    def __init__(self, k):
+        super().__init__(k, W.V_QWEN, "bf16", True, None)
+        self.host = self.logits.cpu().pin_memory()
+
+    def outputs(self):
+        o = super().outputs()
+        o["_staging"] = torch.empty(2 * self.BLOCK * self.host.stride(0) * 2, dtype=torch.uint8, device=DEV)
+        o["_copy"] = torch.cuda.Stream(DEV)
+        return o
+
+    def call(self, o, stream):
+        _lib.grpo_logprob_loss_fwd_bwd_host(self.host, self.target, self.old, self.adv, self.mask, 0.2, 1.0 / 700,
+                                            o["dl"], o["loss"], o["logp"], o["acc"], o["_staging"], self.BLOCK,
+                                            stream=stream, copy_stream=o["_copy"])
+        _lib.grpo_finish_step(o["acc"], o["loss"], sync=False, stream=stream)
 
 
 class LmCase:
@@ -96,6 +122,7 @@ class LmCase:
         _lib.grpo_lmhead_loss_fwd_bwd(self.h, self.W, self.target, None, self.adv, self.mask, 0.2, 1.0 / 300,
                                       o["d_h"], o["dW"], o["loss"], o["logp"], o["acc"], o["_ws"],
                                       stream=stream)
+        _lib.grpo_finish_step(o["acc"], o["loss"], sync=False, stream=stream)
 
 
 def main():
@@ -114,6 +141,7 @@ def main():
         RowCase(8, 4104, "f32", True, dict(ent_coef=0.01)),
         LmCase(9, stored=False),
         LmCase(10, stored=True),
+        HostCase(11),  # logits in pinned host memory, streamed through a staging buffer
     ]
     streams = [torch.cuda.Stream(DEV) for _ in range(N_THREADS)]
     # per thread, case and repetition its own outputs (accumulators zeroed here, before any
@@ -157,9 +185,7 @@ def main():
                 for key, want in ref.items():
                     if key.startswith("_"):
                         continue
-                    a, b = _bits(got[key]), _bits(want)
-                    if key == "acc":
-                        a, b = a[:64], b[:64]  # the counters; the rest is the finish's
+                    a, b = _bits(got[key]), _bits(want)  # acc: the finish's result and divisor too
                     if not torch.equal(a, b):
                         print(f"MISMATCH case {j} thread {i} rep {r} output {key}")
                         return 1

@@ -1,6 +1,7 @@
 """Concurrent callers: several host threads, each on its own stream with its own outputs,
-call every row-pass instance and both LM-head backward paths at once, starting from empty
-launch caches (a fresh process). Each result equals the same call made alone, bit for bit."""
+call every row-pass instance, the row pass over host logits and both LM-head backward paths
+at once, each followed by its step finish, starting from empty launch caches (a fresh
+process). Each result equals the same call made alone, bit for bit."""
 import os
 import subprocess
 import sys
