@@ -218,3 +218,62 @@ def _host_step(bp, s, logits_host, staging, block_rows, copy_stream, st, dlogits
 def read_results(accs, n_steps: int) -> List[dict]:
     raw = accs.view(n_steps, _lib.ACC_BYTES)[:, 64:].cpu().numpy()
     return [_lib.grpo_step_result.from_buffer_copy(raw[s].tobytes()).as_dict() for s in range(n_steps)]
+
+
+# ---- data parallelism over one optimizer step's rows ------------------------------------------
+#
+# Every rank plans the whole batch (the planner is host-only and cheap), so each rank knows
+# every step's N without communication. Rank r runs the rows `dp_row_block` gives it, with
+# grad_scale = 1/max(N, 1) and a finish whose divisor is N (grpo_finish_step_ex); its dlogits
+# rows are then those of a single-GPU run. The step's one exchange is the ranks' float64 loss
+# sums and integer counts (`dp_allreduce_step_result`).
+
+_RESULT_FIELDS = ("loss_sum", "n_valid", "n_clipped", "n_nonfinite", "n_tokens", "status", "kernel_flags")
+
+
+def dp_row_block(n_rows: int, rank: int, world: int) -> tuple:
+    """The contiguous rows [lo, hi) of an optimizer step's `n_rows` that data-parallel rank
+    `rank` of `world` runs: equal counts, the first n_rows % world ranks one row more."""
+    if world < 1 or not 0 <= rank < world or n_rows < 0:
+        raise ValueError("need 0 <= rank < world and n_rows >= 0")
+    q, r = divmod(n_rows, world)
+    lo = rank * q + min(rank, r)
+    return lo, lo + q + (1 if rank < r else 0)
+
+
+def combine_step_results(results: List[dict], divisor: int) -> dict:
+    """One step's result from the per-rank results of its row blocks (each finished with the
+    step's divisor): sums of the float64 loss sums (in rank order) and of the counts; the loss
+    is the summed loss sum over max(divisor, 1). Status: the first error a rank reports, else
+    skipped if any rank skipped, else OK; kernel flags are OR-ed."""
+    loss_sum = 0.0
+    counts = {k: 0 for k in ("n_valid", "n_clipped", "n_nonfinite", "n_tokens")}
+    status, flags = _lib.OK, 0
+    for res in results:
+        loss_sum += float(res["loss_sum"])
+        for k in counts:
+            counts[k] += int(res[k])
+        st = int(res["status"])
+        if st < 0 and status >= 0:
+            status = st
+        elif st == _lib.STEP_SKIPPED_NONFINITE and status == _lib.OK:
+            status = st
+        flags |= int(res["kernel_flags"])
+    out = dict(counts, loss_sum=loss_sum, loss=loss_sum / max(int(divisor), 1),
+               clipfrac=counts["n_clipped"] / max(counts["n_valid"], 1), status=status, kernel_flags=flags)
+    return out
+
+
+def dp_allreduce_step_result(res: dict, divisor: int, group=None) -> dict:
+    """Every rank's step result -> the whole step's, identical on all ranks: one all-gather of
+    seven numbers per rank (float64; the counts are exact below 2^53), then
+    `combine_step_results` in rank order. CPU tensors under gloo, device tensors under nccl."""
+    import torch
+    import torch.distributed as dist
+
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend(group) == "nccl" else "cpu"
+    mine = torch.tensor([float(res[k]) for k in _RESULT_FIELDS], dtype=torch.float64, device=dev)
+    allv = [torch.empty_like(mine) for _ in range(dist.get_world_size(group))]
+    dist.all_gather(allv, mine, group=group)
+    rows = [dict(zip(_RESULT_FIELDS, v.cpu().tolist())) for v in allv]
+    return combine_step_results(rows, divisor)

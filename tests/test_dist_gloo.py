@@ -1,5 +1,7 @@
-"""The multi-rank timing path of bench.py (max elapsed over ranks, sum of units) on CPU with
-two gloo ranks."""
+"""Multi-rank paths on CPU with gloo ranks: bench.py's timing reduction (max elapsed over
+ranks, sum of units), and data parallelism over one optimizer step's rows (each rank's row
+block scaled by the step's global N, the step result reduced across ranks) against the
+unsharded step."""
 import os
 import socket
 
@@ -44,3 +46,92 @@ def test_reduce_timing_two_ranks():
 def test_single_rank_is_identity():
     import bench
     assert bench.reduce_timing(3.5, 42.0, 1) == (3.5, 42.0)
+
+
+def _dp_worker(rank, world, port, q):
+    # each rank plans the whole batch, runs (with the oracle, on the CPU) the row block of
+    # every optimizer step that dp_row_block gives it, scaled by the step's global N, and
+    # reduces the step result; the reduced result must be the unsharded step's
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import math
+    import numpy as np
+    from oracle import advantage as OA
+    from oracle import loss as OL
+    from rl_post_token_gb300 import step as S
+    from rl_post_token_gb300 import workloads as W
+
+    wl = W.make_workload("tiny", rows=24, seed=5, mini=12, micro=4)
+    z = W.logits_to_host(W.make_logits(wl, "cpu"))
+    adv = OA.broadcast_to_tokens(OA.group_advantage(wl.rewards, wl.group_size, np.float32(1e-6), True),
+                                 wl.row_rollout, wl.row_len)
+    logp = OL.loss_fwd_bwd(z, wl.target, None, adv, wl.mask, wl.eps, want_grad=False)["logp_tok"]
+    old = logp + wl.old_noise
+    bp = S.plan_batch(wl.plan, wl.row_len, wl.row_valid)
+    out = []
+    for s in range(bp.n_steps):
+        N = int(bp.plan["step_valid_tokens"][s])
+        r0, r1 = int(bp.plan["step_in_row_off"][s]), int(bp.plan["step_in_row_off"][s + 1])
+        lo, hi = S.dp_row_block(r1 - r0, rank, world)
+        t0, t1 = int(bp.row_tok_off[r0 + lo]), int(bp.row_tok_off[r0 + hi])
+        mine = OL.loss_fwd_bwd(z[t0:t1], wl.target[t0:t1], old[t0:t1], adv[t0:t1], wl.mask[t0:t1], wl.eps,
+                               1.0 / max(N, 1))
+        m = wl.mask[t0:t1] != 0
+        res = dict(loss_sum=math.fsum(mine["loss_tok"]), n_valid=int(m.sum()),
+                   n_clipped=int((mine["clipped"] & m).sum()), n_nonfinite=0, n_tokens=t1 - t0,
+                   status=0, kernel_flags=0)
+        got = S.dp_allreduce_step_result(res, N)
+        # the unsharded step, for comparison
+        a, b = int(bp.row_tok_off[r0]), int(bp.row_tok_off[r1])
+        full = OL.loss_fwd_bwd(z[a:b], wl.target[a:b], old[a:b], adv[a:b], wl.mask[a:b], wl.eps, 1.0 / max(N, 1))
+        want = OL.finish_step(full["loss_tok"], wl.mask[a:b], full["clipped"])
+        out.append((got, want, N, b - a))
+    q.put((rank, out))
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_data_parallel_step_reduces_to_the_unsharded_step(world):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_dp_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=180) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert sorted(res) == list(range(world))
+    for r in range(world):
+        assert len(res[r]) == 2  # two optimizer steps
+        for k, (got, want, N, T) in enumerate(res[r]):
+            assert got == res[0][k][0]  # identical on every rank
+            assert got["n_valid"] == want["n_valid"] == N
+            assert got["n_clipped"] == want["n_clipped"] and got["n_tokens"] == T
+            assert got["clipfrac"] == want["clipfrac"]
+            assert abs(got["loss"] - want["loss"]) <= 1e-12 * max(abs(want["loss_sum"]) / max(N, 1), 1e-300)
+            assert got["status"] == 0 and got["kernel_flags"] == 0
+
+
+def test_dp_row_blocks_and_combine():
+    from rl_post_token_gb300 import _lib
+    from rl_post_token_gb300 import step as S
+    for n in range(0, 12):
+        for world in range(1, 5):
+            blocks = [S.dp_row_block(n, r, world) for r in range(world)]
+            assert blocks[0][0] == 0 and blocks[-1][1] == n
+            assert all(blocks[i][1] == blocks[i + 1][0] for i in range(world - 1))
+            sizes = [b - a for a, b in blocks]
+            assert max(sizes) - min(sizes) <= 1 and sizes == sorted(sizes, reverse=True)
+    with pytest.raises(ValueError):
+        S.dp_row_block(4, 2, 2)
+    base = dict(loss_sum=1.5, n_valid=3, n_clipped=1, n_nonfinite=0, n_tokens=4, status=0, kernel_flags=0)
+    r = S.combine_step_results([base, dict(base, loss_sum=-0.5, n_valid=2)], divisor=5)
+    assert r["loss"] == 1.0 / 5 and r["n_valid"] == 5 and r["clipfrac"] == 2 / 5 and r["status"] == 0
+    skip = dict(base, status=_lib.STEP_SKIPPED_NONFINITE, n_nonfinite=1, kernel_flags=2)
+    err = dict(base, status=_lib.ERR_N_MISMATCH, kernel_flags=4)
+    assert S.combine_step_results([base, skip], 6)["status"] == _lib.STEP_SKIPPED_NONFINITE
+    both = S.combine_step_results([skip, err, dict(base, status=_lib.ERR_KERNEL)], 6)
+    assert both["status"] == _lib.ERR_N_MISMATCH and both["kernel_flags"] == 6 and both["n_nonfinite"] == 1
+    assert S.combine_step_results([], 0)["loss"] == 0.0

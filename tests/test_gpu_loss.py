@@ -1110,3 +1110,41 @@ def test_logits_beyond_the_shift_range_are_reported_not_wrong(variant):
     res = _lib.grpo_finish_step(acc, loss, grad_bufs=[dl])
     assert res["status"] == _lib.STEP_SKIPPED_NONFINITE and res["n_nonfinite"] == 2
     assert torch.all(dl == 0)
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_data_parallel_row_blocks_match_the_whole_step(world):
+    # The row blocks data-parallel ranks would run, run one after another on this GPU: each
+    # with the step's global scale 1/N and a finish whose divisor is N. Per-token outputs and
+    # dlogits are the whole step's bits; the combined step result is the whole step's (the
+    # float64 loss sum up to the order of its additions).
+    wl = W.make_workload("qwen_step", rows=8, len_lo=20, len_hi=40, seed=77, mini=8, micro=8)
+    case = H.Case(wl)
+    T = case.logits.shape[0]
+    N = int(wl.mask.sum())
+    dl, loss, logp, acc = _run_direct(case, 1.0 / N)
+    whole = _lib.grpo_finish_step(acc, loss, expected_N=N)
+    dl_s = torch.full_like(case.logits, 7.0)
+    loss_s = torch.full((T,), -7.0, device=DEV)
+    logp_s = torch.full((T,), -7.0, device=DEV)
+    parts = []
+    for r in range(world):
+        lo, hi = S.dp_row_block(8, r, world)
+        t0, t1 = int(wl.tok_off[lo]), int(wl.tok_off[hi])
+        a = _lib.new_step_acc(DEV)
+        _lib.grpo_logprob_loss_fwd_bwd(case.logits[t0:t1], case.d_target[t0:t1], case.d_old[t0:t1],
+                                       case.d_adv[t0:t1], case.d_mask[t0:t1], wl.eps, 1.0 / N, dl_s[t0:t1],
+                                       loss_s[t0:t1], logp_s[t0:t1], a)
+        parts.append(_lib.grpo_finish_step_ex(a, loss_s[t0:t1], divisor=N,
+                                              expected_N=int(wl.mask[t0:t1].sum())))
+    torch.cuda.synchronize()
+    assert torch.equal(dl_s.view(torch.int16), dl.view(torch.int16))
+    assert torch.equal(loss_s.view(torch.int32), loss.view(torch.int32))
+    assert torch.equal(logp_s.view(torch.int32), logp.view(torch.int32))
+    got = S.combine_step_results(parts, N)
+    for k in ("n_valid", "n_clipped", "n_nonfinite", "n_tokens", "status", "kernel_flags"):
+        assert got[k] == whole[k], k
+    assert got["clipfrac"] == whole["clipfrac"]
+    bound = 1e-12 * float(torch.abs(loss.double()).sum()) / N
+    assert abs(got["loss"] - whole["loss"]) <= bound
+    assert all(p["loss"] == p["loss_sum"] / N for p in parts)
