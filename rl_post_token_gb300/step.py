@@ -241,6 +241,40 @@ def dp_row_block(n_rows: int, rank: int, world: int) -> tuple:
     return lo, lo + q + (1 if rank < r else 0)
 
 
+def dp_exec_ranges(bp: BatchPlan, s: int, rank: int, world: int) -> List[tuple]:
+    """The exec-order token ranges [t0, t1) of optimizer step `s` that data-parallel rank
+    `rank` of `world` runs.
+
+    A compaction plan assigns rows to GPUs itself: each padded group is split evenly across
+    the GPUs ("How a context-compaction step fits a variable number of rows into one batch",
+    the figure), in the plan's ``row_gpu``. The plan must then have been made for `world`
+    GPUs. Any other plan splits the step's rows, in execution order, into `dp_row_block`'s
+    contiguous blocks."""
+    p = bp.plan
+    c0, c1 = int(p["step_chunk_off"][s]), int(p["step_chunk_off"][s + 1])
+    j0, j1 = int(p["chunk_row_off"][c0]), int(p["chunk_row_off"][c1])
+    lens = bp.row_len[np.asarray(p["row_src"][j0:j1], np.int64)]
+    off = int(bp.exec_tok_off[c0]) + np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    if int(p["q"]) > 0:
+        gpu = np.asarray(p["row_gpu"][j0:j1])
+        n_gpus = int(np.asarray(p["row_gpu"][:int(p["n_rows"])]).max()) + 1
+        if n_gpus != world:
+            raise ValueError(f"the compaction plan was made for {n_gpus} GPUs, not {world}")
+        ranges, j = [], 0
+        while j < j1 - j0:
+            if gpu[j] != rank:
+                j += 1
+                continue
+            k = j
+            while k < j1 - j0 and gpu[k] == rank:
+                k += 1
+            ranges.append((int(off[j]), int(off[k])))
+            j = k
+        return ranges
+    lo, hi = dp_row_block(j1 - j0, rank, world)
+    return [(int(off[lo]), int(off[hi]))] if hi > lo else []
+
+
 def combine_step_results(results: List[dict], divisor: int) -> dict:
     """One step's result from the per-rank results of its row blocks (each finished with the
     step's divisor): sums of the float64 loss sums (in rank order) and of the counts; the loss

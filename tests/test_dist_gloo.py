@@ -135,3 +135,50 @@ def test_dp_row_blocks_and_combine():
     both = S.combine_step_results([skip, err, dict(base, status=_lib.ERR_KERNEL)], 6)
     assert both["status"] == _lib.ERR_N_MISMATCH and both["kernel_flags"] == 6 and both["n_nonfinite"] == 1
     assert S.combine_step_results([], 0)["loss"] == 0.0
+
+
+@pytest.mark.parametrize("name, world", [("tiny", 2), ("qwen_step", 3), ("dynamic", 4), ("compaction", 4),
+                                         ("compaction", 2)])
+def test_dp_exec_ranges_partition_every_step(name, world):
+    # the ranks' ranges cover each optimizer step's exec tokens exactly once; a compaction plan
+    # gives each rank the rows its row_gpu slots name (each padded group split evenly)
+    import numpy as np
+    from rl_post_token_gb300 import step as S
+    from rl_post_token_gb300 import workloads as W
+    ov = {"n_gpus": world, "micro": 1} if name == "compaction" else {}
+    wl = W.make_workload(name)
+    plan = dict(wl.plan, **ov)
+    bp = S.plan_batch(plan, wl.row_len, wl.row_valid, wl.seg_counts)
+    p = bp.plan
+    for s in range(bp.n_steps):
+        c0, c1 = int(p["step_chunk_off"][s]), int(p["step_chunk_off"][s + 1])
+        t_lo, t_hi = int(bp.exec_tok_off[c0]), int(bp.exec_tok_off[c1])
+        covered = np.zeros(t_hi - t_lo, np.int32)
+        per_rank_rows = []
+        for r in range(world):
+            rows = 0
+            for a, b in S.dp_exec_ranges(bp, s, r, world):
+                assert t_lo <= a < b <= t_hi
+                covered[a - t_lo:b - t_lo] += 1
+                rows += b - a
+            per_rank_rows.append(rows)
+        assert (covered == 1).all()
+        if name == "compaction":
+            # every row has the same length here, so equal token counts mean equal row counts
+            assert len(set(per_rank_rows)) == 1
+            gpu = np.asarray(p["row_gpu"][:int(p["n_rows"])])
+            off = np.concatenate([[0], np.cumsum(bp.row_len[np.asarray(p["row_src"][:int(p["n_rows"])])])])
+            for r in range(world):
+                want = [(int(off[j]), int(off[j + 1])) for j in np.nonzero(gpu == r)[0]]
+                got = [(x, y) for a, b in S.dp_exec_ranges(bp, s, r, world) for x, y in
+                       zip(range(a, b, 1024), range(a + 1024, b + 1, 1024))]
+                assert got == want
+
+
+def test_dp_exec_ranges_compaction_needs_its_gpu_count():
+    from rl_post_token_gb300 import step as S
+    from rl_post_token_gb300 import workloads as W
+    wl = W.make_workload("compaction")  # planned for 4 GPUs
+    bp = S.plan_batch(wl.plan, wl.row_len, wl.row_valid, wl.seg_counts)
+    with pytest.raises(ValueError):
+        S.dp_exec_ranges(bp, 0, 0, 2)
