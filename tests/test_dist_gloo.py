@@ -48,9 +48,9 @@ def test_single_rank_is_identity():
     assert bench.reduce_timing(3.5, 42.0, 1) == (3.5, 42.0)
 
 
-def _dp_worker(rank, world, port, q):
-    # each rank plans the whole batch, runs (with the oracle, on the CPU) the row block of
-    # every optimizer step that dp_row_block gives it, scaled by the step's global N, and
+def _dp_worker(rank, world, port, q, name="tiny"):
+    # each rank plans the whole batch, runs (with the oracle, on the CPU) its exec-order token
+    # ranges of every optimizer step (dp_exec_ranges), scaled by the step's global N, and
     # reduces the step result; the reduced result must be the unsharded step's
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
@@ -61,41 +61,52 @@ def _dp_worker(rank, world, port, q):
     from rl_post_token_gb300 import step as S
     from rl_post_token_gb300 import workloads as W
 
-    wl = W.make_workload("tiny", rows=24, seed=5, mini=12, micro=4)
+    if name == "compaction":  # 4/8/4 rows padded for `world` GPUs, short rows, small V
+        wl = W.make_workload("compaction", V=512, row_tokens=16, seed=5)
+        wl.plan = dict(wl.plan, n_gpus=world, micro=1)
+    else:
+        wl = W.make_workload("tiny", rows=24, seed=5, mini=12, micro=4)
     z = W.logits_to_host(W.make_logits(wl, "cpu"))
     adv = OA.broadcast_to_tokens(OA.group_advantage(wl.rewards, wl.group_size, np.float32(1e-6), True),
                                  wl.row_rollout, wl.row_len)
     logp = OL.loss_fwd_bwd(z, wl.target, None, adv, wl.mask, wl.eps, want_grad=False)["logp_tok"]
     old = logp + wl.old_noise
-    bp = S.plan_batch(wl.plan, wl.row_len, wl.row_valid)
+    bp = S.plan_batch(wl.plan, wl.row_len, wl.row_valid, wl.seg_counts)
+    # exec-order inputs: a padding row reads its source row's inputs with the mask off
+    if bp.tok_src is None:
+        src = np.arange(z.shape[0])
+        real = np.ones(z.shape[0], bool)
+    else:
+        ts = np.asarray(bp.tok_src)
+        real = ts >= 0
+        src = np.where(real, ts, -1 - ts)
+    zx, yx, ox, ax = z[src], wl.target[src], old[src], adv[src]
+    mx = (wl.mask[src] != 0) & real
     out = []
     for s in range(bp.n_steps):
-        N = int(bp.plan["step_valid_tokens"][s])
-        r0, r1 = int(bp.plan["step_in_row_off"][s]), int(bp.plan["step_in_row_off"][s + 1])
-        lo, hi = S.dp_row_block(r1 - r0, rank, world)
-        t0, t1 = int(bp.row_tok_off[r0 + lo]), int(bp.row_tok_off[r0 + hi])
-        mine = OL.loss_fwd_bwd(z[t0:t1], wl.target[t0:t1], old[t0:t1], adv[t0:t1], wl.mask[t0:t1], wl.eps,
-                               1.0 / max(N, 1))
-        m = wl.mask[t0:t1] != 0
-        res = dict(loss_sum=math.fsum(mine["loss_tok"]), n_valid=int(m.sum()),
-                   n_clipped=int((mine["clipped"] & m).sum()), n_nonfinite=0, n_tokens=t1 - t0,
+        c0, c1 = int(bp.plan["step_chunk_off"][s]), int(bp.plan["step_chunk_off"][s + 1])
+        a, b = int(bp.exec_tok_off[c0]), int(bp.exec_tok_off[c1])
+        N = int(mx[a:b].sum())
+        idx = np.concatenate([np.arange(t0, t1) for t0, t1 in S.dp_exec_ranges(bp, s, rank, world)] or
+                             [np.zeros(0, np.int64)]).astype(np.int64)
+        mine = OL.loss_fwd_bwd(zx[idx], yx[idx], ox[idx], ax[idx], mx[idx], wl.eps, 1.0 / max(N, 1))
+        res = dict(loss_sum=math.fsum(mine["loss_tok"]), n_valid=int(mx[idx].sum()),
+                   n_clipped=int((mine["clipped"] & mx[idx]).sum()), n_nonfinite=0, n_tokens=int(idx.size),
                    status=0, kernel_flags=0)
         got = S.dp_allreduce_step_result(res, N)
-        # the unsharded step, for comparison
-        a, b = int(bp.row_tok_off[r0]), int(bp.row_tok_off[r1])
-        full = OL.loss_fwd_bwd(z[a:b], wl.target[a:b], old[a:b], adv[a:b], wl.mask[a:b], wl.eps, 1.0 / max(N, 1))
-        want = OL.finish_step(full["loss_tok"], wl.mask[a:b], full["clipped"])
+        full = OL.loss_fwd_bwd(zx[a:b], yx[a:b], ox[a:b], ax[a:b], mx[a:b], wl.eps, 1.0 / max(N, 1))
+        want = OL.finish_step(full["loss_tok"], mx[a:b], full["clipped"])
         out.append((got, want, N, b - a))
     q.put((rank, out))
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world", [2, 3])
-def test_data_parallel_step_reduces_to_the_unsharded_step(world):
+@pytest.mark.parametrize("name, world", [("tiny", 2), ("tiny", 3), ("compaction", 2)])
+def test_data_parallel_step_reduces_to_the_unsharded_step(name, world):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_dp_worker, args=(r, world, port, q)) for r in range(world)]
+    procs = [ctx.Process(target=_dp_worker, args=(r, world, port, q, name)) for r in range(world)]
     for p in procs:
         p.start()
     res = dict(q.get(timeout=180) for _ in procs)
@@ -104,7 +115,7 @@ def test_data_parallel_step_reduces_to_the_unsharded_step(world):
         assert p.exitcode == 0
     assert sorted(res) == list(range(world))
     for r in range(world):
-        assert len(res[r]) == 2  # two optimizer steps
+        assert len(res[r]) == (2 if name == "tiny" else 1)  # optimizer steps
         for k, (got, want, N, T) in enumerate(res[r]):
             assert got == res[0][k][0]  # identical on every rank
             assert got["n_valid"] == want["n_valid"] == N
