@@ -1,6 +1,6 @@
-"""Randomised search (hypothesis) for any plan on which the library's host planner and the
-oracle planner disagree: every field and every error code, over fixed, dynamic and
-compaction configurations. Host code only."""
+"""Randomised search (hypothesis) for any input on which the library's host code and the
+oracle disagree: the planner (every field and every error code, over fixed, dynamic and
+compaction configurations) and the accumulation window. Host code only."""
 import numpy as np
 import pytest
 
@@ -56,3 +56,34 @@ def test_fixed_and_dynamic_plans_agree(grpo_lib, case):
 def test_compaction_plans_agree(grpo_lib, case):
     cfg, row_len, seg = case
     _assert_same(cfg, np.asarray(row_len), np.asarray(row_len), seg)
+
+
+@st.composite
+def window_runs(draw):
+    n_micro = draw(st.integers(1, 8))
+    chunks = draw(st.lists(st.tuples(st.booleans(), st.floats(-1e6, 1e6, allow_nan=False, width=64),
+                                     st.integers(0, 5000)), min_size=0, max_size=60))
+    return n_micro, chunks
+
+
+@settings(**SETTINGS)
+@given(window_runs())
+def test_window_runs_agree(grpo_lib, run):
+    # the host accumulation window: every chunk's action and scale, the counters and the
+    # roll-up, for any sequence of finite and non-finite chunks
+    import math
+
+    from oracle import window as OW
+    from rl_post_token_gb300 import _lib
+    n_micro, chunks = run
+    o, c = OW.Window(n_micro), _lib.Window(n_micro)
+    for finite, loss, denom in chunks:
+        x = loss if finite else math.nan
+        assert o.chunk(finite, x, denom) == c.grpo_window_chunk(finite, x, denom)
+    st_ = c.state
+    assert (st_["steps"], st_["skipped_windows"], st_["dropped_chunks"]) == (o.steps, o.skipped_windows,
+                                                                             o.dropped_chunks)
+    lo, do, so = o.rollup()
+    lc, dc, sc = c.grpo_window_rollup()
+    assert (do, so) == (dc, sc)
+    assert lc == lo or abs(lc - lo) <= 1e-15 * max(abs(lo), 1e-300)
