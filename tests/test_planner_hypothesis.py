@@ -1,6 +1,7 @@
 """Randomised search (hypothesis) for any input on which the library's host code and the
 oracle disagree: the planner (every field and every error code, over fixed, dynamic and
-compaction configurations) and the accumulation window. Host code only."""
+compaction configurations), the aggregation weights and the accumulation window. Host code
+only."""
 import numpy as np
 import pytest
 
@@ -87,3 +88,30 @@ def test_window_runs_agree(grpo_lib, run):
     lc, dc, sc = c.grpo_window_rollup()
     assert (do, so) == (dc, sc)
     assert lc == lo or abs(lc - lo) <= 1e-15 * max(abs(lo), 1e-300)
+
+
+@st.composite
+def weight_plans(draw):
+    G = draw(st.sampled_from([1, 2, 4]))
+    B = G * draw(st.integers(1, 10))
+    row_len = draw(st.lists(st.integers(0, 60), min_size=B, max_size=B))
+    row_valid = [draw(st.integers(0, L)) for L in row_len]
+    mini = draw(st.sampled_from([d for d in range(1, B + 1) if B % d == 0]))
+    cfg = dict(batch=B, group_size=G, mini=mini, micro=draw(st.sampled_from([d for d in range(1, mini + 1)
+                                                                              if mini % d == 0])))
+    if draw(st.booleans()):
+        cfg.update(dynamic=1, max_token_len=max(row_len + [1]) + draw(st.integers(0, 200)),
+                   workload=draw(st.integers(0, 1)), balance_ends=draw(st.integers(0, 1)))
+    return cfg, row_len, row_valid
+
+
+@settings(**SETTINGS)
+@given(weight_plans(), st.sampled_from([0, 1, 2]))
+def test_aggregation_weights_agree(grpo_lib, case, agg):
+    # grpo_plan_token_weights: every step's divisor and every token's weight, against the
+    # oracle's definition of the mode
+    from rl_post_token_gb300 import _lib
+    from tests.test_aggregate_weights import _check
+    cfg, row_len, row_valid = case
+    plan = _lib.grpo_plan_microbatches(cfg, np.asarray(row_len), np.asarray(row_valid))
+    _check(plan, np.asarray(row_len, np.int64), np.asarray(row_valid, np.int64), agg)
