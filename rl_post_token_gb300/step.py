@@ -99,6 +99,13 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
     every stream."""
     import torch
 
+    # checks that need no device, made before anything is enqueued
+    p = bp.plan
+    need = int(p["n_steps"]) * _lib.ACC_BYTES
+    if accs.numel() * accs.element_size() < need:
+        raise ValueError(f"accs must hold {need} bytes (one accumulator per optimizer step)")
+    if agg == _lib.AGG_SEQ_MEAN_TOKEN_MEAN and w_tok is None:
+        raise ValueError("SEQ_MEAN_TOKEN_MEAN needs the per-token weights w_tok")
     st = torch.cuda.current_stream() if stream is None else stream
     sides = [] if side_stream is None else (list(side_stream) if isinstance(side_stream, (list, tuple))
                                             else [side_stream])
@@ -108,10 +115,7 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
         _lib.grpo_group_advantage(rewards, group_size, adv_eps, True, adv_rollout, row_rollout,
                                   row_tok_off, adv_tok, stream=st)
         launches += 2
-    p = bp.plan
     plain = agg == _lib.AGG_TOKEN_MEAN and w_tok is None
-    if agg == _lib.AGG_SEQ_MEAN_TOKEN_MEAN and w_tok is None:
-        raise ValueError("SEQ_MEAN_TOKEN_MEAN needs the per-token weights w_tok")
     divisors = None if plain else bp.token_weights(agg, want_w=False)[0]
     for s in range(p["n_steps"]):
         N = int(p["step_valid_tokens"][s])

@@ -48,3 +48,20 @@ def test_status_error_carries_code_and_name():
     e = _lib.GrpoError(_lib.ERR_CAPACITY, "grpo_lmhead_loss_fwd_bwd")
     assert e.code == _lib.ERR_CAPACITY
     assert "grpo_lmhead_loss_fwd_bwd" in str(e)
+
+
+def test_driver_refuses_short_accumulators_before_launching():
+    # run_batch writes one 128-byte accumulator per optimizer step: a shorter buffer, or a
+    # sequence-level mode without its weights, is refused before anything is enqueued
+    from rl_post_token_gb300 import step as S
+    from rl_post_token_gb300 import workloads as W
+    wl = W.make_workload("tiny")
+    bp = S.plan_batch(wl.plan, wl.row_len, wl.row_valid)
+    assert bp.n_steps == 2
+    kw = dict(logits=None, dlogits=None, target=None, old_logp=None, mask=None, adv_tok=None, loss_tok=None,
+              logp_tok=None, clip_eps=0.2)
+    with pytest.raises(ValueError, match="accs"):
+        S.run_batch(bp, accs=torch.zeros(_lib.ACC_BYTES, dtype=torch.uint8), **kw)
+    with pytest.raises(ValueError, match="w_tok"):
+        S.run_batch(bp, accs=torch.zeros(2 * _lib.ACC_BYTES, dtype=torch.uint8),
+                    agg=_lib.AGG_SEQ_MEAN_TOKEN_MEAN, **kw)
