@@ -354,7 +354,12 @@ GRPO_API int grpo_finish_step(grpo_step_acc* acc, const float* loss_tok, int64_t
  * product exact in float64; w_tok NULL = 1) in the same fixed order, loss = loss_sum /
  * max(D, 1) and the deferred gradient scale 1/max(D, 1), where D = divisor if >= 0, else the
  * counted N. grpo_finish_step is this call with w_tok NULL and divisor -1.
- *  w_tok    device float [n_tok] or NULL (the step's slice of grpo_plan_token_weights' output) */
+ *  w_tok    device float [n_tok] or NULL (the step's slice of grpo_plan_token_weights' output)
+ * Data parallelism: when an optimizer step's rows are split across ranks, each rank runs its
+ * rows with grad_scale = 1/max(D, 1) for the whole step's D (every rank can plan the whole
+ * batch, so D needs no exchange) and finishes with divisor = D. The step's result is then the
+ * sum over ranks of loss_sum and of the counts, with loss = that sum / max(D, 1); status is
+ * the first error a rank reports, else skipped if any rank skipped. */
 GRPO_API int grpo_finish_step_ex(grpo_step_acc* acc, const float* loss_tok, int64_t n_tok,
                                  const float* w_tok, int64_t divisor, int64_t expected_N,
                                  int32_t deferred, void* const* grad_bufs,
