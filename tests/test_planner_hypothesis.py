@@ -1,6 +1,7 @@
 """Randomised search (hypothesis) for any input on which the library's host code and the
 oracle disagree: the planner (every field and every error code, over fixed, dynamic and
-compaction configurations), the aggregation weights and the accumulation window. Host code
+compaction configurations), the token index, the aggregation weights and the accumulation
+window. Host code
 only."""
 import numpy as np
 import pytest
@@ -115,3 +116,27 @@ def test_aggregation_weights_agree(grpo_lib, case, agg):
     cfg, row_len, row_valid = case
     plan = _lib.grpo_plan_microbatches(cfg, np.asarray(row_len), np.asarray(row_valid))
     _check(plan, np.asarray(row_len, np.int64), np.asarray(row_valid, np.int64), agg)
+
+
+@settings(**SETTINGS)
+@given(st.one_of(fixed_or_dynamic(), compaction()))
+def test_token_index_follows_its_definition(grpo_lib, case):
+    # grpo_plan_token_index: exec token k of exec row j is token k of input row row_src[j],
+    # stored as -1 - i for a padding row; checked on every plan the planner accepts
+    from rl_post_token_gb300 import _lib
+    cfg, row_len, third = case
+    seg = third if cfg.get("compaction") else None
+    valid = np.asarray(row_len) if seg is not None else np.asarray(third)
+    try:
+        p = _lib.grpo_plan_microbatches(cfg, np.asarray(row_len), valid, seg_counts=seg)
+    except _lib.GrpoError:
+        return
+    rl = np.asarray(row_len, np.int64)
+    off = np.concatenate([[0], np.cumsum(rl)])
+    want = []
+    for j in range(int(p["n_rows"])):
+        r = int(p["row_src"][j])
+        toks = list(range(int(off[r]), int(off[r + 1])))
+        want += [-1 - t for t in toks] if p["row_pad"][j] else toks
+    got = _lib.grpo_plan_token_index(p, rl)
+    assert got.tolist() == want
