@@ -1,8 +1,7 @@
 """Randomised search (hypothesis) for any input on which the library's host code and the
 oracle disagree: the planner (every field and every error code, over fixed, dynamic and
 compaction configurations), the token index, the aggregation weights and the accumulation
-window. Host code
-only."""
+window. Host code only."""
 import numpy as np
 import pytest
 
