@@ -388,22 +388,28 @@ class Batch:
         return valid * (2 * rowb + 4 + 4 + 4 + 1 + 4 + 4 + idx + extra) + masked * (rowb + 1 + idx)
 
 
+def lmhead_chunks(V):
+    """Vocabulary chunks of the LM-head backward: ceil(V/256) tiles in chunks of at most 66."""
+    tiles = -(-V // 256)
+    return -(-tiles // 66)
+
+
 def run_lmhead(args):
     """Fused LM-head step: advantage, one grpo_lmhead_loss_fwd_bwd call (forward, dlogits, d_h
-    and dW), the finish. The headline uses the stored-exponent backward (the workspace that
-    selects it); the recompute backward (the minimum workspace) is timed beside it. Roofline:
-    tensor, 6*T*V*H algorithmic flops (forward GEMM and the two backward GEMMs; the recompute
-    path's extra 2*T*V*H is not credited)."""
+    and dW, no [T, V] matrix stored: the backward recomputes each vocabulary chunk's logits),
+    the finish. Roofline: tensor, 6*T*V*H algorithmic flops (forward GEMM and the two backward
+    GEMMs; the recompute's extra 2*T*V*H is not credited). One GPU only."""
     import torch
     from rl_post_token_gb300 import build as B
     from rl_post_token_gb300 import _lib
     from rl_post_token_gb300 import workloads as W
 
     rank, world, local = dist_env()
+    if world > 1:
+        raise SystemExit("--workload lmhead runs on one GPU only")
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    if rank == 0:
-        B.build()
+    B.build()
     _lib.lib()
     wl = W.make_workload("lmhead", seed=rank, **({"tokens": args.lm_tokens} if args.lm_tokens else {}))
     T, V, Hd = wl.T, wl.V, wl.extra["H"]
@@ -418,8 +424,7 @@ def run_lmhead(args):
     loss = torch.empty(T, device=device)
     logp = torch.empty(T, device=device)
     acc = _lib.new_step_acc(device)
-    ws = torch.empty(_lib.grpo_lmhead_workspace_size_stored(T, V, Hd), dtype=torch.uint8, device=device)
-    ws_small = ws[:_lib.grpo_lmhead_workspace_size(T, V, Hd)]
+    ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
     N = wl.n_valid
 
@@ -443,15 +448,7 @@ def run_lmhead(args):
     e1.record(stream)
     torch.cuda.synchronize(device)
     full_s = e0.elapsed_time(e1) / 1e3 / args.steps
-    res = _lib.read_step_result(acc)  # the headline step's result (the stored-exponent path)
-    step(old=old, w=ws_small)
-    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    r0.record(stream)
-    for _ in range(args.steps):
-        step(old=old, w=ws_small)
-    r1.record(stream)
-    torch.cuda.synchronize(device)
-    rec_s = r0.elapsed_time(r1) / 1e3 / args.steps
+    res = _lib.read_step_result(acc)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
     for _ in range(args.steps):
@@ -518,14 +515,12 @@ def run_lmhead(args):
         "ms_per_step": 1e3 * full_s, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT["lmhead"], "tokens": T, "vocab": V, "hidden": Hd,
-                   "backward": "stored exponents (workspace %.2f GB)" % (ws.numel() / 1e9),
+                   "backward": "logits recomputed per vocabulary chunk, no [T, V] matrix stored "
+                               "(workspace %.2f GB)" % (ws.numel() / 1e9),
                    "l2": "weights 622 MB + hidden 64 MB read per step, larger than L2; no flush"},
         "roofline": {"bound": "tensor", "achieved": flops / full_s / 1e12, "peak": peak, "unit": "TFLOP/s",
                      "frac": flops / full_s / 1e12 / peak, "peak_source": f"{kind} bf16_tflops_sustained",
                      "flops_per_step": flops, "traffic": None},
-        "recompute_path": {"ms": 1e3 * rec_s, "tflops": flops / rec_s / 1e12,
-                           "workspace_gb": ws_small.numel() / 1e9,
-                           "what": "minimum workspace: logits recomputed per 16384-column chunk"},
         "forward_only": {"ms": 1e3 * fwd_s, "tflops": 2.0 * T * V * Hd / fwd_s / 1e12,
                          "what": "softmax-partials GEMM pass + per-token reduce (2*T*V*H flops)"},
         "step_result": {k: res[k] for k in ("loss", "n_valid", "clipfrac", "status")},
@@ -535,9 +530,9 @@ def run_lmhead(args):
                        "copy stream into one of two device input sets (the next step's copy overlaps this step's "
                        "compute, the first step's does not), the step result read back every step",
                 "step_result_matches": all(e2e_res[k] == res[k] for k in ("loss", "n_valid", "clipfrac", "status"))},
-        # per step: the advantage (2), pass A, the per-token reduce and dz-from-e (3; the two
-        # cuBLAS GEMMs are not counted), the finish (1)
-        "gpu_launches": 6 * args.steps,
+        # per step: the advantage (2), pass A and the per-token reduce (2), per vocabulary chunk
+        # the dlogits recompute, the d_h and the dW GEMM (3), the finish (1)
+        "gpu_launches": (5 + 3 * lmhead_chunks(V)) * args.steps,
     }
     if clk is not None:
         line["clocks"] = clk

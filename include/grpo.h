@@ -17,11 +17,9 @@
  *   - Status: every function returns int: GRPO_OK (0), a positive step status, or a negative
  *     GRPO_ERR_* code. No function aborts or prints.
  *   - Ownership: every buffer belongs to the caller, and the library never frees caller
- *     memory. The library allocates no device memory of its own with two exceptions:
- *       - the LM-head backward's first call on a device creates a cuBLAS handle (its GEMMs
- *         run in a region of the caller's workspace);
- *       - the module's 16 MiB device array of grpo_lmhead_forward_noalloc is held by every
- *         GPU that loads the library.
+ *     memory. The library allocates no device memory of its own with one exception: the
+ *     module's 16 MiB device array of grpo_lmhead_forward_noalloc, held by every GPU that
+ *     loads the library.
  *     "device" pointers are CUDA device memory of the current device; "host" pointers are
  *     ordinary host memory.
  *   - Asynchrony: device work is enqueued on `stream` (cudaStream_t passed as void*; NULL is
@@ -406,29 +404,26 @@ GRPO_API int grpo_window_rollup(const grpo_window* w, double* loss, int64_t* den
 /* ---- fused LM-head variant ---------------------------------------------------------------- */
 
 /* Bytes of device workspace grpo_lmhead_loss_fwd_bwd needs for [T, H] hidden states and a
- * [V, H] output embedding: per-(token, 256-wide vocabulary tile) softmax partials, per-token
- * LSE and coefficients, one bf16 dlogits chunk of 16384 vocabulary columns, and 32 MiB of
- * scratch for the backward's cuBLAS GEMMs. 0 on bad sizes. */
+ * [V, H] output embedding: per-(token, 256-wide vocabulary tile) softmax partials (float32
+ * shift and sum), per-token target logit, LSE and coefficient, and one bf16 dlogits chunk
+ * buffer [T, 256 * chunk_tiles], where the ceil(V/256) vocabulary tiles are split into
+ * ceil(tiles/66) chunks of equal width (V = 151936: 9 chunks of 66 tiles, 16896 columns).
+ * Each part is rounded up to 256 bytes. 0 on bad sizes. */
 GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H);
 
-/* Bytes of workspace that select the stored path of grpo_lmhead_loss_fwd_bwd: the partials
- * above plus a bf16 [T, 256 * ceil(V/256)] matrix (about 2*T*V bytes) and the same 32 MiB of
- * GEMM scratch. 0 on bad sizes. */
-GRPO_API size_t grpo_lmhead_workspace_size_stored(int64_t T, int64_t V, int64_t H);
-
 /* The same loss with the logits produced on the tensor cores: z = h W^T, computed tile by tile
- * and consumed by the softmax in the GEMM epilogue, so neither the [T, V] float32 logits nor
- * their softmax are ever stored ("Sizing mini-batches and micro-batches", "The problem").
- * Forward: LSE, log-prob, ratio, clipped surrogate, per-token loss (as
- * grpo_logprob_loss_fwd_bwd, one token per row of h). Backward, by workspace size:
- *  - >= grpo_lmhead_workspace_size: the logits of each 16384-column vocabulary chunk are
- *    recomputed, dlogits written to the workspace chunk, then d_h = dlogits W (accumulated
- *    over chunks) and dW = dlogits^T h per chunk (8 T V H flops in all);
- *  - >= grpo_lmhead_workspace_size_stored: the forward epilogue also stores, per 256-wide
- *    tile, e = exp(z - tile max) as bf16 (relative error 2^-9 whatever the logits' size);
- *    dlogits = coef * exp(tile max - LSE) * e replaces it in place, the target element from
- *    the float32 logit; then one d_h and one dW GEMM over the whole vocabulary (6 T V H
- *    flops, no recompute).
+ * and consumed by the softmax in the GEMM epilogue; no [T, V] matrix (logits, softmax,
+ * exponentials or dlogits) is ever stored ("Sizing mini-batches and micro-batches", "The
+ * problem"). All contractions are the library's own tcgen05 kernels (2-CTA clusters with
+ * paired MMAs, 256 x 256 tiles, bf16 operands, float32 accumulation).
+ *  - Forward: LSE, log-prob, ratio, clipped surrogate, per-token loss (as
+ *    grpo_logprob_loss_fwd_bwd, one token per row of h).
+ *  - Backward (d_h or dW non-NULL): per vocabulary chunk, the chunk's logits are recomputed
+ *    and its bf16 dlogits written to the workspace chunk buffer; then d_h (+)= dlogits W_c,
+ *    accumulated over the chunks in chunk order, and dW_c = dlogits^T h. The recompute makes
+ *    the step 8 T V H flops (6 T V H without it).
+ *  - Determinism: d_h and the per-token outputs of a token do not depend on which other
+ *    tokens share the call; dW sums over the call's tokens in a fixed order.
  *  h          device bf16 [T, H] row-major, 16-byte aligned; H a multiple of 64
  *  W          device bf16 [V, H] row-major, 16-byte aligned
  *  target, old_logp (or NULL), adv_tok, mask   device, indexed by token row
@@ -437,9 +432,10 @@ GRPO_API size_t grpo_lmhead_workspace_size_stored(int64_t T, int64_t V, int64_t 
  *  loss_tok, logp_tok (or NULL)  device float [T]
  *  acc        device grpo_step_acc (counts as in grpo_logprob_loss_fwd_bwd)
  *  workspace  device, 256-byte aligned, >= grpo_lmhead_workspace_size(T, V, H) bytes,
- *             caller-owned; it holds all of the call's scratch, the GEMMs' included, so calls
- *             may overlap (several streams, several host threads) as long as each has its own
- *             workspace and outputs
+ *             caller-owned; it holds all of the call's scratch, so calls may overlap (several
+ *             streams, several host threads) as long as each has its own workspace and outputs
+ * Environment: GRPO_LMHEAD_CTA_GROUP=1 selects one-CTA 128 x 256 tiles instead of the paired
+ * 256 x 256 tiles (same results; kept for comparison).
  * Errors: GRPO_ERR_INVALID (sizes, NULL, alignment), GRPO_ERR_CAPACITY (workspace too small),
  * GRPO_ERR_UNSUPPORTED (tensor-map creation), GRPO_ERR_CUDA. */
 GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, int64_t T, int64_t V, int64_t H,
@@ -463,8 +459,11 @@ GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, int64_t T, i
  *  - Limit: 4*T*(2*ceil(V/256) + 3) bytes (each part rounded up to 256) must fit the array,
  *    e.g. about 3,500 tokens at V = 151936; larger calls return GRPO_ERR_CAPACITY and launch
  *    nothing.
- *  - The first call on each device looks up the array's device address and sets the GEMM
- *    kernel's shared-memory limit; make that first call before any stream capture.
+ *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ *    with that device current) and sets the GEMM kernel's shared-memory limit; make that first
+ *    call before any stream capture. The address is kept with the id of the device's context:
+ *    if that context is destroyed and re-created (cudaDeviceReset), the next call looks the
+ *    address up again, so the same rule applies to it.
  *  - Every call shares the one array and leaves its contents behind; no part of it needs to
  *    start at zero (each location a call reads was written earlier in that call), but calls
  *    that overlap on the GPU (several streams, several host threads) race: serialise them.

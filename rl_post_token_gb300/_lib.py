@@ -131,8 +131,6 @@ def _lib() -> C.CDLL:
     lib.grpo_plan_token_weights.restype = C.c_int
     lib.grpo_lmhead_workspace_size.argtypes = [C.c_int64, C.c_int64, C.c_int64]
     lib.grpo_lmhead_workspace_size.restype = C.c_size_t
-    lib.grpo_lmhead_workspace_size_stored.argtypes = [C.c_int64, C.c_int64, C.c_int64]
-    lib.grpo_lmhead_workspace_size_stored.restype = C.c_size_t
     lib.grpo_lmhead_loss_fwd_bwd.argtypes = [vp, vp, C.c_int64, C.c_int64, C.c_int64, vp, vp, vp, vp, C.c_float,
                                              C.c_float, vp, vp, vp, vp, vp, vp, C.c_size_t, vp]
     lib.grpo_lmhead_loss_fwd_bwd.restype = C.c_int
@@ -420,10 +418,6 @@ def grpo_finish_step_ex(acc, loss_tok, w_tok=None, divisor: int = -1, n_tok: Opt
 
 def grpo_lmhead_workspace_size(T: int, V: int, H: int) -> int:
     return int(_lib().grpo_lmhead_workspace_size(T, V, H))
-
-
-def grpo_lmhead_workspace_size_stored(T: int, V: int, H: int) -> int:
-    return int(_lib().grpo_lmhead_workspace_size_stored(int(T), int(V), int(H)))
 
 
 def grpo_lmhead_loss_fwd_bwd(h, W, target, old_logp, adv_tok, mask, clip_eps: float, grad_scale: float,

@@ -24,9 +24,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgrpo.so")
 
 SOURCES = ["grpo_plan.cpp", "grpo_window.cpp", "grpo_rowpass.cu", "grpo_step.cu", "grpo_lmhead.cu"]
-# cuBLAS serves the two plain backward GEMMs of the LM-head variant; the rpath lets the
-# library load (for its host-only entry points) before any framework has loaded cuBLAS.
-LINK = ["-lcublas", "-Xlinker", "-rpath=/usr/local/cuda/lib64"]
+LINK: list = []  # every kernel is the library's own: no CUDA library beyond the static runtime
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,477 +1,34 @@
 // Fused LM-head variant of the loss: the logits z = h W^T are produced on the tensor cores
-// tile by tile and consumed by the softmax in the GEMM epilogue, so the [T, V] float32 logits
-// and their softmax never reach memory ("Sizing mini-batches and micro-batches", "The problem":
-// the log-softmax over the vocabulary of 2048-token completions is what runs out of memory).
+// tile by tile and consumed by the softmax in the GEMM epilogue; neither the [T, V] logits nor
+// their softmax nor any [T, V] matrix derived from them is ever held in memory ("Sizing
+// mini-batches and micro-batches", "The problem": the log-softmax over the vocabulary of
+// 2048-token completions is what runs out of memory).
 //
-//  pass A  tcgen05 GEMM over all (128-token x 256-vocab) tiles; the epilogue reduces each
-//          tile row to a log2-domain (shift, sum-exp) partial and picks up the target logit
-//          (stored path: it also writes e = 2^(z log2 e - shift) of the tile as bf16).
-//  reduce  per token: combine the partials in vocabulary order -> LSE, log-prob, ratio,
-//          clipped surrogate, gradient coefficient (same token epilogue as the row pass).
-//  backward, recompute path (minimum workspace): per vocabulary chunk the same GEMM recomputes
-//          the chunk's logits and its epilogue writes dlogits (bf16) into a bounded chunk
-//          workspace; then d_h += dz_c W_c and dW_c = dz_c^T h (cuBLAS, float32 outputs).
-//  backward, stored path (workspace for the whole [T, V] exponent matrix): dz_from_e_kernel
-//          turns the stored e into dlogits in place; then one d_h and one dW GEMM.
+//  pass A     tcgen05 GEMM over every (256-token x 256-vocabulary) tile; the epilogue reduces
+//             each token's tile to a log2-domain (shift, sum-exp) partial and picks up the
+//             target logit.
+//  reduce     per token: combine the partials in vocabulary order -> LSE, log-prob, ratio,
+//             clipped surrogate, gradient coefficient (the row pass's token epilogue).
+//  backward   per vocabulary chunk c (at most 66 tiles, 16896 columns): the same GEMM recomputes
+//             the chunk's logits and its epilogue writes the chunk's bf16 dlogits dz_c into a
+//             bounded [T, chunk] buffer; then d_h (+)= dz_c W_c and dW_c = dz_c^T h, both on the
+//             same tcgen05 kernel with float32 outputs. d_h is accumulated over the chunks in
+//             chunk order (a fixed order: the result does not depend on how the tokens are
+//             split into calls).
 //
-// GEMM kernel: persistent, one CTA per SM, 6 warps, launched as 2-CTA clusters (CTA pair) or
-// as single CTAs. Warp 0 issues TMA loads (128-byte swizzled 128x64 h tiles and 256x64 W tiles;
-// in a pair each CTA loads one 128-row half of W, multicast to both) into a 4-stage
-// shared-memory ring; warp 1 issues tcgen05.mma (M=128, N=256, K=16, bf16 -> f32) into a
-// double-buffered TMEM accumulator (2 x 256 columns); warps 2-5 read the accumulator with
-// tcgen05.ld (one TMEM lane = one token row per thread) and run the epilogue while the next
-// tile's MMAs proceed. Every mbarrier wait is bounded and raises a flag instead of hanging.
-#include <cublas_v2.h>
+// All four contractions run on grpo::lmhead::gemm_kernel (grpo_lmhead_gemm.cuh): 2-CTA
+// clusters with paired tcgen05.mma (cta_group::2, 256 x 256 tiles), plain TMA tile loads.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
-#include "grpo_common.cuh"
+#include "grpo_lmhead_gemm.cuh"
 
 namespace grpo {
 namespace lmhead {
-
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NTHREADS = 192;
-constexpr int TMEM_COLS = 2 * BN;  // two accumulators
-constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + 256;
-
-// Instruction descriptor of tcgen05.mma kind::f16: D f32, A and B bf16, both K-major,
-// N = 256, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
-
-// Shared-memory matrix descriptor, K-major operand with 128-byte swizzle: rows of 128 bytes,
-// 8-row swizzle atoms 1024 bytes apart (stride byte offset), version 1, layout SWIZZLE_128B.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;              // leading byte offset (unused for swizzled K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
-  d |= (uint64_t)1 << 46;              // descriptor version
-  d |= (uint64_t)2 << 61;              // SWIZZLE_128B
-  return d;
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, bool accum) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a), "l"(b), "r"(kIdesc), "r"((uint32_t)accum)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-
-// CTA-pair variants: the load lands at the same shared-memory offset in every CTA of `mask`
-// and completes bytes on the mbarrier at `bar`'s offset in each of them; the commit arrives on
-// the mbarrier at `bar`'s offset in every CTA of `mask`.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-      ::"r"(bar), "h"(mask)
-      : "memory");
-}
-
-// Bounded wait that ignores the abort flag: the end-of-kernel drains after a timeout.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t i = 0; i < (1u << 24); ++i) {
-    if (mbar_try_wait(bar, parity)) return;
-    if ((i & 255u) == 0 && global_timer_ns() - t0 > 1000000000ull) return;
-  }
-}
-
-__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-
-// 32 consecutive accumulator columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-struct GemmArgs {
-  int64_t T, V, H;
-  int n_row_tiles;
-  int col_tile0, n_col_tiles;  // tiles [col_tile0, col_tile0 + n_col_tiles) of 256 columns
-  int mode;                    // 0: softmax partials; 1: dlogits
-  const int32_t* target;
-  // mode 0
-  float* part_m;  // [n_col_tiles_total][T] log2-domain max
-  float* part_s;  // [n_col_tiles_total][T]
-  float* zy;      // [T] target logit
-  // mode 0 with est != NULL: e = 2^((z - tile max) log2 e) stored as bf16 [T][lde] (the
-  // partials then use the exact tile maximum)
-  __nv_bfloat16* est;
-  int64_t lde;
-  // mode 1
-  const float* lse2;  // [T] LSE * log2(e)
-  const float* coef;  // [T] gradient coefficient (already scaled)
-  __nv_bfloat16* dz;  // chunk workspace [T][ldz], column 0 = vocabulary column v0
-  int64_t ldz, v0;
-  grpo_step_acc* acc;
-};
-
-// Stored path: e = 2^(z log2 e - shift) of 32 columns (-inf past the vocabulary gives 0),
-// written as bf16 for row `row` (if it exists) and added to s.
-__device__ __forceinline__ void store_e_chunk(const GemmArgs& g, bool rok, int64_t row, int64_t cb, float (&v)[32],
-                                              float shift, float& s) {
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = ex2(fmaf(v[i], kLog2e, -shift));
-  if (rok) {
-    uint4* d4 = reinterpret_cast<uint4*>(g.est + row * g.lde + cb);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      d4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                         pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-  }
-  s += tree_sum(v);  // reduces v in place: after the store
-}
-
-// Work units of a launch. One CTA: a unit is one 128 x 256 tile. CTA pair (a 2-CTA cluster): a
-// unit is two vertically adjacent tiles sharing one W tile; CTA r of the pair computes row tile
-// 2u + r (past the last row tile it computes zero-filled rows whose results are discarded).
-template <bool PAIR>
-struct Units {
-  int n_row_units, n, first, stride;
-  uint32_t rank;
-  __device__ Units(const GemmArgs& g, uint32_t r) : rank(r) {
-    n_row_units = PAIR ? (g.n_row_tiles + 1) / 2 : g.n_row_tiles;
-    n = n_row_units * g.n_col_tiles;
-    first = PAIR ? (int)(blockIdx.x / 2) : (int)blockIdx.x;
-    stride = PAIR ? (int)(gridDim.x / 2) : (int)gridDim.x;
-  }
-  __device__ void tile(const GemmArgs& g, int t, int& rt, int& ct) const {
-    const int ru = t % n_row_units;
-    ct = g.col_tile0 + t / n_row_units;
-    rt = PAIR ? 2 * ru + (int)rank : ru;
-  }
-};
-
-// PAIR = false: one CTA per SM loads its h tile and the whole W tile. PAIR = true: the two CTAs
-// of a cluster each load their own h tile and one 128-row half of the shared W tile, multicast
-// into both, so each CTA pulls 32 KB per K step from L2 instead of 48 KB. A stage is refilled
-// only after both CTAs' MMAs have released it (each commit arrives on both CTAs' barrier).
-template <bool PAIR>
-__global__ void __launch_bounds__(NTHREADS, 1)
-gemm_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w, GemmArgs g) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
-  uint64_t* full = reinterpret_cast<uint64_t*>(sgen + STAGES * STAGE_BYTES);
-  uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;   // [2]
-  uint64_t* tempty = tfull + 2;       // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], PAIR ? 2 : 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
-    }
-    *s_abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  fence_before();
-  __syncthreads();
-  if (PAIR) cluster_sync_all();  // the peer's barriers exist before anything targets them
-  fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-  const Units<PAIR> units(g, rank);
-  const int KB = (int)(g.H / BK);
-  uint32_t issued = 0;  // producer: stage loads issued
-
-  if (warp == 0) {
-    // ---- TMA producer ----
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
-      for (int t = units.first; t < units.n; t += units.stride) {
-        int rt, ct;
-        units.tile(g, t, rt, ct);
-        for (int kb = 0; kb < KB; ++kb) {
-          mbar_wait_bounded(&empty[stage], phase ^ 1u, s_abort);
-          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-          const uint32_t sa = sbase + stage * STAGE_BYTES;
-          tma_load_2d(sa, &map_h, smem_u32(&full[stage]), kb * BK, rt * BM);
-          if (PAIR)
-            tma_load_2d_mc(sa + A_BYTES + rank * (B_BYTES / 2), &map_w, smem_u32(&full[stage]), kb * BK,
-                           ct * BN + (int)rank * (BN / 2), (uint16_t)0x3);
-          else
-            tma_load_2d(sa + A_BYTES, &map_w, smem_u32(&full[stage]), kb * BK, ct * BN);
-          ++issued;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (PAIR) {
-        // every stage's last release (this CTA's commit and the peer's) has arrived before
-        // this CTA may leave: the peer's commits target this CTA's barriers
-        for (int i = 0; i < STAGES; ++i) {  // a stage never used passes at once
-          mbar_wait_bounded(&empty[stage], phase ^ 1u, s_abort);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ---- MMA issuer ----
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0, ab = 0, aphase = 0;
-      for (int t = units.first; t < units.n; t += units.stride) {
-        mbar_wait_bounded(&tempty[ab], aphase ^ 1u, s_abort);
-        fence_after();
-        const uint32_t d = tmem + ab * BN;
-        for (int kb = 0; kb < KB; ++kb) {
-          mbar_wait_bounded(&full[stage], phase, s_abort);
-          fence_after();
-          const uint32_t sa = sbase + stage * STAGE_BYTES;
-          const uint64_t da = sdesc_sw128(sa), db = sdesc_sw128(sa + A_BYTES);
-#pragma unroll
-          for (int j = 0; j < BK / 16; ++j)  // +32 bytes along K per 16-element step
-            mma_bf16(d, da + 2 * j, db + 2 * j, kb > 0 || j > 0);
-          if (PAIR)
-            mma_commit_mc(smem_u32(&empty[stage]), (uint16_t)0x3);
-          else
-            mma_commit(smem_u32(&empty[stage]));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        mma_commit(smem_u32(&tfull[ab]));
-        if (++ab == 2) {
-          ab = 0;
-          aphase ^= 1u;
-        }
-      }
-    }
-  } else {
-    // ---- epilogue: warps 2..5, thread = TMEM lane = token row of the tile ----
-    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
-    const int trow = quarter * 32 + lane;
-    uint32_t ab = 0, aphase = 0;
-    for (int t = units.first; t < units.n; t += units.stride) {
-      int rt, ct;
-      units.tile(g, t, rt, ct);
-      mbar_wait_bounded(&tfull[ab], aphase, s_abort);
-      fence_after();
-      const int64_t row = (int64_t)rt * BM + trow;
-      const int64_t c0 = (int64_t)ct * BN;
-      const bool rok = row < g.T;
-      const int32_t y = rok ? g.target[row] : -1;
-      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + ab * BN;
-      if (g.mode == 0 && g.est) {
-        // one pass: e relative to a shift taken from the first 32 columns, stored and summed;
-        // if a later value sits more than 2^64 above that shift the warp redoes the tile
-        // with the exact tile maximum (e <= 2^64 keeps every stored value and the sum finite)
-        float shift = 0.f, s = 0.f, zy = 0.f;
-        bool redo = false;
-        const bool own = y >= c0 && y < c0 + BN;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld32(taddr + c * 32, v);
-          const int64_t cb = c0 + c * 32;
-          float cmax = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (cb + i >= g.V) v[i] = -INFINITY;
-            cmax = fmaxf(cmax, v[i]);
-          }
-          if (own && y >= cb && y < cb + 32) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (cb + i == y) zy = v[i];
-          }
-          if (c == 0) shift = cmax * kLog2e;  // the first 32 columns always hold vocabulary entries
-          redo |= !(cmax * kLog2e <= shift + 64.f);
-          store_e_chunk(g, rok, row, cb, v, shift, s);
-        }
-        if (__any_sync(0xffffffffu, redo)) {
-          float mx = -INFINITY;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            tmem_ld32(taddr + c * 32, v);
-            const int64_t cb = c0 + c * 32;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (cb + i < g.V) mx = fmaxf(mx, v[i]);
-          }
-          shift = mx * kLog2e;
-          s = 0.f;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            tmem_ld32(taddr + c * 32, v);
-            const int64_t cb = c0 + c * 32;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (cb + i >= g.V) v[i] = -INFINITY;
-            store_e_chunk(g, rok, row, cb, v, shift, s);
-          }
-        }
-        if (rok) {
-          g.part_m[(int64_t)ct * g.T + row] = shift;
-          g.part_s[(int64_t)ct * g.T + row] = s;
-          if (own) g.zy[row] = zy;
-        }
-      } else if (g.mode == 0) {
-        MS acc{-INFINITY, 0.f};
-        float zy = 0.f;
-        const bool own = y >= c0 && y < c0 + BN;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld32(taddr + c * 32, v);
-          const int64_t cb = c0 + c * 32;
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (cb + i >= g.V) v[i] = -INFINITY;  // zero-filled columns past the vocabulary
-          if (own && y >= cb && y < cb + 32) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (cb + i == y) zy = v[i];
-          }
-          lazy_online2<32>(acc, v);
-        }
-        if (rok) {
-          g.part_m[(int64_t)ct * g.T + row] = acc.m;
-          g.part_s[(int64_t)ct * g.T + row] = acc.s;
-          if (own) g.zy[row] = zy;
-        }
-      } else {
-        const float cf = rok ? g.coef[row] : 0.f;
-        const float l2 = rok ? g.lse2[row] : 0.f;
-        const float cexp = l2 - log2f(fabsf(cf));
-        const uint32_t sgn = cf < 0.f ? 0x80008000u : 0u;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld32(taddr + c * 32, v);
-          const int64_t cb = c0 + c * 32;
-          if (!rok || cb >= g.V) continue;
-          uint32_t w[16];
-          if (cf != 0.f) {
-            float zyv = 0.f;
-            const bool hit = y >= cb && y < cb + 32;
-            if (hit) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (cb + i == y) zyv = v[i];
-            }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = ex2(fmaf(v[i], kLog2e, -cexp));
-#pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]) ^ sgn;
-            if (hit) {
-              const float dzy = cf * ex2(fmaf(zyv, kLog2e, -l2)) - cf;
-              const uint32_t hb = __bfloat16_as_ushort(__float2bfloat16_rn(dzy));
-              const int k = (int)(y - cb);
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                if (k == 2 * i) w[i] = (w[i] & 0xFFFF0000u) | hb;
-                if (k == 2 * i + 1) w[i] = (w[i] & 0x0000FFFFu) | (hb << 16);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = 0u;
-          }
-          __nv_bfloat16* dst = g.dz + row * g.ldz + (cb - g.v0);
-          const int nvalid = (int)std::min<int64_t>(32, g.V - cb);
-          if (nvalid == 32) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-          } else {
-            for (int i = 0; i < nvalid; ++i)
-              dst[i] = __ushort_as_bfloat16((unsigned short)((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu)));
-          }
-        }
-      }
-      fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[ab]);
-      if (++ab == 2) {
-        ab = 0;
-        aphase ^= 1u;
-      }
-    }
-  }
-
-  fence_before();
-  __syncthreads();
-  if (PAIR) {
-    cluster_sync_all();  // neither CTA leaves while the other may still signal or copy into it
-    if (*s_abort && threadIdx.x == 0) {
-      // after a timeout, let this CTA's copies and the peer's arrivals settle (bounded)
-      for (int sidx = 0; sidx < STAGES && (uint32_t)sidx < issued; ++sidx) {
-        const uint32_t uses = (issued - 1u - (uint32_t)sidx) / STAGES;
-        drain_wait(&full[sidx], uses & 1u);
-        drain_wait(&empty[sidx], uses & 1u);
-      }
-    }
-  }
-  if (*s_abort && threadIdx.x == 0) atomicOr(&g.acc->flags, kFlagWaitTimeout);
-  if (warp == 1) {
-    fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
-  }
-}
 
 // Per token: combine the vocabulary-tile partials in order, then the token epilogue.
 __global__ void reduce_kernel(int64_t T, int n_col_tiles, const float* __restrict__ part_m,
@@ -524,45 +81,6 @@ __global__ void reduce_kernel(int64_t T, int n_col_tiles, const float* __restric
   }
 }
 
-// Stored path, backward: dz = coef * 2^(tile max - LSE) * e, in place over the stored e, one CTA
-// per token row at a time; the target element, coef * (p_y - 1), is taken from the float32
-// target logit and written by the thread that wrote its vector.
-__global__ void __launch_bounds__(256) dz_from_e_kernel(int64_t T, int64_t V, int n_col_tiles, int64_t lde,
-                                                        const float* __restrict__ part_m,
-                                                        const float* __restrict__ lse2,
-                                                        const float* __restrict__ coef,
-                                                        const float* __restrict__ zy,
-                                                        const int32_t* __restrict__ target,
-                                                        __nv_bfloat16* __restrict__ e) {
-  extern __shared__ float f[];  // [n_col_tiles] per-tile factor of the current row
-  const int tid = threadIdx.x;
-  const int64_t nv = lde / 8;
-  for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
-    const float c = coef[row], l2 = lse2[row];
-    __syncthreads();
-    for (int ct = tid; ct < n_col_tiles; ct += blockDim.x)
-      f[ct] = c == 0.f ? 0.f : c * ex2(part_m[(int64_t)ct * T + row] - l2);
-    __syncthreads();
-    uint4* p = reinterpret_cast<uint4*>(e + row * lde);
-    if (c == 0.f) {  // masked or clipped: a zero row, whatever e holds
-      for (int64_t v = tid; v < nv; v += blockDim.x) p[v] = make_uint4(0, 0, 0, 0);
-      continue;
-    }
-    for (int64_t v = tid; v < nv; v += blockDim.x) {
-      const float fv = f[v / (BN / 8)];
-      uint4 u = p[v];
-      float x[8];
-      x[0] = bf16_lo(u.x) * fv; x[1] = bf16_hi(u.x) * fv; x[2] = bf16_lo(u.y) * fv; x[3] = bf16_hi(u.y) * fv;
-      x[4] = bf16_lo(u.z) * fv; x[5] = bf16_hi(u.z) * fv; x[6] = bf16_lo(u.w) * fv; x[7] = bf16_hi(u.w) * fv;
-      p[v] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                        pack_bf16x2(x[6], x[7]));
-    }
-    const int32_t y = target[row];
-    if (y >= 0 && (int64_t)y < V && tid == (int)((y / 8) % blockDim.x))
-      e[row * lde + y] = __float2bfloat16_rn(c * ex2(fmaf(zy[row], kLog2e, -l2)) - c);
-  }
-}
-
 // ---- host -------------------------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -578,64 +96,54 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Row-major [rows, cols] bf16 matrix, box [box_rows, 64] with 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// bf16 matrix [outer][ld] of which [outer][inner] is addressed, box {64, box_outer}, 128-byte
+// swizzle; reads past either extent return zeros.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_outer) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, box_outer};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The current device's cuBLAS handle, created on first use. A handle's stream and workspace
-// are settings of the handle, so the caller holds `lock` (taken here) from setting them until
-// its last GEMM is enqueued: calls from several host threads then never enqueue on one
-// another's stream or scratch.
-cublasHandle_t blas_handle(std::unique_lock<std::mutex>& lock) {
-  static cublasHandle_t h[64] = {};
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  lock = std::unique_lock<std::mutex>(mu);
-  if (!h[dev] && cublasCreate(&h[dev]) != CUBLAS_STATUS_SUCCESS) h[dev] = nullptr;
-  return h[dev];
+// Operand maps. K-major [rows][K]: box {64 K, box_rows rows}. MN-major [K][MN]: box {64 MN, 64 K}.
+bool map_k(CUtensorMap* m, const void* base, int64_t rows, int64_t k, int64_t ld, int box_rows) {
+  return make_map(m, base, (uint64_t)k, (uint64_t)rows, (uint64_t)ld, (uint32_t)box_rows);
+}
+bool map_mn(CUtensorMap* m, const void* base, int64_t k, int64_t mn, int64_t ld) {
+  return make_map(m, base, (uint64_t)mn, (uint64_t)k, (uint64_t)ld, 64u);
 }
 
-// GEMM variant: the CTA pair unless GRPO_LMHEAD_PAIR=0 selects the one-CTA kernel.
-bool use_pair() {
-  const char* e = getenv("GRPO_LMHEAD_PAIR");
-  return !(e && e[0] == '0');
+// CTAs per tile: 2 (paired MMA, the default) or 1 (GRPO_LMHEAD_CTA_GROUP=1, kept for comparison).
+int cta_group() {
+  const char* e = getenv("GRPO_LMHEAD_CTA_GROUP");
+  return (e && e[0] == '1') ? 1 : 2;
 }
 
-// h and W tensor maps for a variant (the pair loads W in 128-row halves).
-bool make_maps(CUtensorMap* map_h, CUtensorMap* map_w, const void* h, const void* W, int64_t T, int64_t V, int64_t H,
-               bool pair) {
-  return make_map(map_h, h, (uint64_t)T, (uint64_t)H, BM) &&
-         make_map(map_w, W, (uint64_t)V, (uint64_t)H, pair ? BN / 2 : BN);
-}
-
-// Launch one GEMM pass over the tiles g describes. The first launch of a variant on a device
-// sets its shared-memory limit and caches how many CTAs (or CTA pairs) fit at once.
-template <bool PAIR>
-int launch_gemm_t(const CUtensorMap& map_h, const CUtensorMap& map_w, const GemmArgs& g, cudaStream_t st) {
-  auto kern = gemm_kernel<PAIR>;
+// One persistent launch over g's units. The first launch of an instance on a device sets its
+// shared-memory limit and caches how many CTAs (or CTA pairs) fit at once.
+template <int CG, int EPI, bool AMN, bool BMN>
+int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs g, cudaStream_t st) {
+  using S = Shape<CG>;
+  auto kern = gemm_kernel<CG, EPI, AMN, BMN>;
+  g.n_m = (int)((g.M + BM * CG - 1) / (BM * CG));
   int dev = 0;
   GRPO_CUDA_TRY(cudaGetDevice(&dev));
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = CG;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(NTHREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = S::SMEM;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = PAIR ? 1 : 0;
+  cfg.numAttrs = CG == 2 ? 1 : 0;
   int max_units = 0;
   {
     static std::mutex mu;
@@ -643,8 +151,8 @@ int launch_gemm_t(const CUtensorMap& map_h, const CUtensorMap& map_w, const Gemm
     std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 64) max_units = cached[dev];
     if (max_units == 0) {
-      GRPO_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES));
-      if (PAIR) {
+      GRPO_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM));
+      if (CG == 2) {
         cfg.gridDim = dim3(2 * 1024, 1, 1);
         GRPO_CUDA_TRY(cudaOccupancyMaxActiveClusters(&max_units, kern, &cfg));
       } else {
@@ -654,16 +162,30 @@ int launch_gemm_t(const CUtensorMap& map_h, const CUtensorMap& map_w, const Gemm
       if (dev >= 0 && dev < 64) cached[dev] = max_units;
     }
   }
-  const int64_t row_units = PAIR ? (g.n_row_tiles + 1) / 2 : g.n_row_tiles;
-  const int64_t units = std::min<int64_t>(row_units * g.n_col_tiles, max_units);
+  const int64_t units = std::min<int64_t>((int64_t)g.n_m * g.n_n, max_units);
   if (units <= 0) return GRPO_OK;
-  cfg.gridDim = dim3((unsigned)(PAIR ? 2 * units : units), 1, 1);
-  GRPO_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, map_h, map_w, g));
+  cfg.gridDim = dim3((unsigned)(CG * units), 1, 1);
+  GRPO_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, ma, mb, g));
   return GRPO_OK;
 }
 
-int launch_gemm(bool pair, const CUtensorMap& map_h, const CUtensorMap& map_w, const GemmArgs& g, cudaStream_t st) {
-  return pair ? launch_gemm_t<true>(map_h, map_w, g, st) : launch_gemm_t<false>(map_h, map_w, g, st);
+template <int EPI, bool AMN, bool BMN>
+int launch(int cg, const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& g, cudaStream_t st) {
+  return cg == 2 ? launch_t<2, EPI, AMN, BMN>(ma, mb, g, st) : launch_t<1, EPI, AMN, BMN>(ma, mb, g, st);
+}
+
+// Logits GEMM over vocabulary tiles [col_tile0, col_tile0 + g.n_n): A = h [T, H], B = W [V, H],
+// both K-major; the epilogue is EPI.
+template <int EPI>
+int logits_gemm(int cg, const void* h, const void* W, int64_t T, int64_t V, int64_t H, GemmArgs g,
+                cudaStream_t st) {
+  CUtensorMap ma, mb;
+  if (!map_k(&ma, h, T, H, H, BM) || !map_k(&mb, W, V, H, H, BN / cg)) return GRPO_ERR_UNSUPPORTED;
+  g.M = T;
+  g.K = H;
+  g.V = V;
+  g.m_fast = 1;  // consecutive units share the W tile
+  return launch<EPI, false, false>(cg, ma, mb, g, st);
 }
 
 }  // namespace lmhead
@@ -674,22 +196,23 @@ using namespace grpo::lmhead;
 
 namespace {
 
-// Scratch of the backward GEMMs, a region of the caller's workspace: each call brings its own,
-// so GEMMs of calls that overlap on several streams share none.
-constexpr size_t kBlasWorkspaceBytes = (size_t)32 << 20;
+// Vocabulary tiles per backward chunk: at most 66 (16896 columns), the chunks of equal width
+// (V = 151936 -> 594 tiles -> 9 chunks of 66).
+constexpr int kMaxChunkTiles = 66;
 
 struct WsLayout {
-  size_t part_m, part_s, zy, lse2, coef, dz, blas, total;
-  int n_col_tiles;
-  int64_t vchunk;  // columns of the dz region: one recompute chunk, or (stored) every tile
+  size_t part_m, part_s, zy, lse2, coef, dz, total;
+  int n_col_tiles, chunk_tiles;
+  int64_t vchunk;  // columns of the dlogits chunk buffer
 };
 
-// stored = true: the dz region holds the whole [T, n_col_tiles * 256] exponent/dlogits matrix
-WsLayout ws_layout(int64_t T, int64_t V, int64_t vchunk, bool stored = false) {
+WsLayout ws_layout(int64_t T, int64_t V) {
   WsLayout w{};
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   w.n_col_tiles = (int)((V + BN - 1) / BN);
-  w.vchunk = stored ? (int64_t)w.n_col_tiles * BN : std::min<int64_t>(vchunk, (int64_t)w.n_col_tiles * BN);
+  const int n_chunks = (w.n_col_tiles + kMaxChunkTiles - 1) / kMaxChunkTiles;
+  w.chunk_tiles = (w.n_col_tiles + n_chunks - 1) / n_chunks;
+  w.vchunk = (int64_t)w.chunk_tiles * BN;
   size_t off = 0;
   w.part_m = off; off += up((size_t)w.n_col_tiles * T * 4);
   w.part_s = off; off += up((size_t)w.n_col_tiles * T * 4);
@@ -697,23 +220,60 @@ WsLayout ws_layout(int64_t T, int64_t V, int64_t vchunk, bool stored = false) {
   w.lse2 = off; off += up((size_t)T * 4);
   w.coef = off; off += up((size_t)T * 4);
   w.dz = off; off += up((size_t)T * w.vchunk * 2);
-  w.blas = off; off += kBlasWorkspaceBytes;
   w.total = off;
   return w;
 }
 
-constexpr int64_t kDefaultVChunk = 16384;  // vocabulary columns per pass-B chunk (64 tiles)
+struct Scratch {
+  float *part_m, *part_s, *zy, *lse2, *coef;
+  __nv_bfloat16* dz;
+};
+
+Scratch carve(void* base, const WsLayout& ws) {
+  uint8_t* b = static_cast<uint8_t*>(base);
+  return {reinterpret_cast<float*>(b + ws.part_m), reinterpret_cast<float*>(b + ws.part_s),
+          reinterpret_cast<float*>(b + ws.zy),     reinterpret_cast<float*>(b + ws.lse2),
+          reinterpret_cast<float*>(b + ws.coef),   reinterpret_cast<__nv_bfloat16*>(b + ws.dz)};
+}
+
+int check_args(const void* h, const void* W, int64_t T, int64_t V, int64_t H, const int32_t* target,
+               const float* adv_tok, const uint8_t* mask, const float* loss_tok, const grpo_step_acc* acc) {
+  if (T < 0 || V < 1 || H < BK || H % BK != 0 || !acc) return GRPO_ERR_INVALID;
+  if (T == 0) return GRPO_OK;
+  if (!h || !W || !target || !adv_tok || !mask || !loss_tok) return GRPO_ERR_INVALID;
+  if (((uintptr_t)h | (uintptr_t)W) & 15u) return GRPO_ERR_INVALID;
+  if (T > INT32_MAX / 2 || V > INT32_MAX / 2) return GRPO_ERR_INVALID;
+  return GRPO_OK;
+}
+
+// Pass A and the per-token reduce: loss_tok, logp_tok, the step counters, and each token's
+// LSE and gradient coefficient in the scratch.
+int forward(int cg, const void* h, const void* W, int64_t T, int64_t V, int64_t H, const int32_t* target,
+            const float* old_logp, const float* adv_tok, const uint8_t* mask, float clip_eps, float grad_scale,
+            float* loss_tok, float* logp_tok, grpo_step_acc* acc, const WsLayout& ws, const Scratch& sc,
+            cudaStream_t st) {
+  GemmArgs g{};
+  g.target = target;
+  g.part_m = sc.part_m;
+  g.part_s = sc.part_s;
+  g.zy = sc.zy;
+  g.acc = acc;
+  g.col_tile0 = 0;
+  g.n_n = ws.n_col_tiles;
+  const int rc = logits_gemm<EPI_PARTIALS>(cg, h, W, T, V, H, g, st);
+  if (rc != GRPO_OK) return rc;
+  reduce_kernel<<<(unsigned)((T + 255) / 256), 256, 0, st>>>(T, ws.n_col_tiles, sc.part_m, sc.part_s, sc.zy,
+                                                              target, V, old_logp, adv_tok, mask, clip_eps,
+                                                              grad_scale, sc.lse2, sc.coef, loss_tok, logp_tok, acc);
+  GRPO_CUDA_TRY(cudaGetLastError());
+  return GRPO_OK;
+}
 
 }  // namespace
 
 extern "C" GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H) {
   if (T <= 0 || V <= 0 || H <= 0) return 0;
-  return ws_layout(T, V, kDefaultVChunk).total;
-}
-
-extern "C" GRPO_API size_t grpo_lmhead_workspace_size_stored(int64_t T, int64_t V, int64_t H) {
-  if (T <= 0 || V <= 0 || H <= 0) return 0;
-  return ws_layout(T, V, kDefaultVChunk, true).total;
+  return ws_layout(T, V).total;
 }
 
 extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, int64_t T, int64_t V, int64_t H,
@@ -722,111 +282,70 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
                                                  float grad_scale, float* d_h, float* dW, float* loss_tok,
                                                  float* logp_tok, grpo_step_acc* acc, void* workspace,
                                                  size_t workspace_bytes, void* stream) {
-  if (T < 0 || V < 1 || H < BK || H % BK != 0 || !acc) return GRPO_ERR_INVALID;
-  if (T == 0) return GRPO_OK;
-  if (!h || !W || !target || !adv_tok || !mask || !loss_tok || !workspace) return GRPO_ERR_INVALID;
-  if (((uintptr_t)h | (uintptr_t)W) & 15u) return GRPO_ERR_INVALID;
-  if ((uintptr_t)workspace & 255u) return GRPO_ERR_INVALID;
-  if (T > INT32_MAX / 2 || V > INT32_MAX / 2) return GRPO_ERR_INVALID;
-  // the stored path when there is a backward pass and room for the whole exponent matrix
-  const bool stored = (d_h || dW) && workspace_bytes >= ws_layout(T, V, kDefaultVChunk, true).total;
-  const WsLayout ws = ws_layout(T, V, kDefaultVChunk, stored);
+  const int arc = check_args(h, W, T, V, H, target, adv_tok, mask, loss_tok, acc);
+  if (arc != GRPO_OK || T == 0) return arc;
+  if (!workspace || ((uintptr_t)workspace & 255u)) return GRPO_ERR_INVALID;
+  const WsLayout ws = ws_layout(T, V);
   if (workspace_bytes < ws.total) return GRPO_ERR_CAPACITY;
   const cudaStream_t st = as_stream(stream);
-  uint8_t* wsb = static_cast<uint8_t*>(workspace);
-  float* part_m = reinterpret_cast<float*>(wsb + ws.part_m);
-  float* part_s = reinterpret_cast<float*>(wsb + ws.part_s);
-  float* zy = reinterpret_cast<float*>(wsb + ws.zy);
-  float* lse2 = reinterpret_cast<float*>(wsb + ws.lse2);
-  float* coef = reinterpret_cast<float*>(wsb + ws.coef);
-  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(wsb + ws.dz);
+  const Scratch sc = carve(workspace, ws);
+  const int cg = cta_group();
+  int rc = forward(cg, h, W, T, V, H, target, old_logp, adv_tok, mask, clip_eps, grad_scale, loss_tok, logp_tok,
+                   acc, ws, sc, st);
+  if (rc != GRPO_OK || (!d_h && !dW)) return rc;
 
-  const bool pair = use_pair();
-  CUtensorMap map_h, map_w;
-  if (!make_maps(&map_h, &map_w, h, W, T, V, H, pair)) return GRPO_ERR_UNSUPPORTED;
-  const int n_row_tiles = (int)((T + BM - 1) / BM);
-
-  GemmArgs g{};
-  g.T = T;
-  g.V = V;
-  g.H = H;
-  g.n_row_tiles = n_row_tiles;
-  g.target = target;
-  g.part_m = part_m;
-  g.part_s = part_s;
-  g.zy = zy;
-  g.lse2 = lse2;
-  g.coef = coef;
-  g.dz = dz;
-  g.ldz = ws.vchunk;
-  g.acc = acc;
-  g.est = stored ? dz : nullptr;
-  g.lde = ws.vchunk;
-
-  // pass A: softmax partials over every vocabulary tile
-  g.mode = 0;
-  g.col_tile0 = 0;
-  g.n_col_tiles = ws.n_col_tiles;
-  {
-    const int rc = launch_gemm(pair, map_h, map_w, g, st);
-    if (rc != GRPO_OK) return rc;
-  }
-  reduce_kernel<<<(unsigned)((T + 255) / 256), 256, 0, st>>>(T, ws.n_col_tiles, part_m, part_s, zy, target, V,
-                                                              old_logp, adv_tok, mask, clip_eps, grad_scale, lse2,
-                                                              coef, loss_tok, logp_tok, acc);
-  GRPO_CUDA_TRY(cudaGetLastError());
-  if (!d_h && !dW) return GRPO_OK;
-
-  std::unique_lock<std::mutex> blas_lock;
-  cublasHandle_t bh = blas_handle(blas_lock);
-  if (!bh || cublasSetStream(bh, st) != CUBLAS_STATUS_SUCCESS ||
-      cublasSetWorkspace(bh, wsb + ws.blas, kBlasWorkspaceBytes) != CUBLAS_STATUS_SUCCESS)
-    return GRPO_ERR_CUDA;
-  const float one = 1.f, zero = 0.f;
-  if (stored) {
-    // dlogits in place over the stored exponents, then each backward GEMM over the whole vocabulary
-    const int grid = (int)std::min<int64_t>(T, (int64_t)sm_count() * 8);
-    const size_t fsm = (size_t)ws.n_col_tiles * sizeof(float);
-    if (fsm > 48 * 1024) return GRPO_ERR_UNSUPPORTED;
-    dz_from_e_kernel<<<grid, 256, fsm, st>>>(T, V, ws.n_col_tiles, ws.vchunk, part_m, lse2, coef, zy, target, dz);
-    GRPO_CUDA_TRY(cudaGetLastError());
-    // d_h[T,H] = dz[T,V] W[V,H]   (column-major view: d_h^T = W^T dz^T)
-    if (d_h && cublasGemmEx(bh, CUBLAS_OP_N, CUBLAS_OP_N, (int)H, (int)T, (int)V, &one, W, CUDA_R_16BF, (int)H, dz,
-                            CUDA_R_16BF, (int)ws.vchunk, &zero, d_h, CUDA_R_32F, (int)H, CUBLAS_COMPUTE_32F,
-                            CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-      return GRPO_ERR_CUDA;
-    // dW[V,H] = dz^T[V,T] h[T,H]   (column-major view: dW^T = h^T dz)
-    if (dW && cublasGemmEx(bh, CUBLAS_OP_N, CUBLAS_OP_T, (int)H, (int)V, (int)T, &one, h, CUDA_R_16BF, (int)H, dz,
-                           CUDA_R_16BF, (int)ws.vchunk, &zero, dW, CUDA_R_32F, (int)H, CUBLAS_COMPUTE_32F,
-                           CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-      return GRPO_ERR_CUDA;
-    return GRPO_OK;
-  }
-
-  // recompute path: per vocabulary chunk, dlogits into the workspace, then the two backward GEMMs
-  const int tiles_per_chunk = (int)(ws.vchunk / BN);
-  for (int ct0 = 0, c = 0; ct0 < ws.n_col_tiles; ct0 += tiles_per_chunk, ++c) {
-    const int nct = std::min(tiles_per_chunk, ws.n_col_tiles - ct0);
+  const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
+  for (int ct0 = 0, c = 0; ct0 < ws.n_col_tiles; ct0 += ws.chunk_tiles, ++c) {
+    const int nct = std::min(ws.chunk_tiles, ws.n_col_tiles - ct0);
     const int64_t v0 = (int64_t)ct0 * BN;
     const int64_t vc = std::min<int64_t>((int64_t)nct * BN, V - v0);
-    g.mode = 1;
-    g.col_tile0 = ct0;
-    g.n_col_tiles = nct;
+    // the chunk's dlogits, recomputed from its logits
+    GemmArgs g{};
+    g.target = target;
+    g.lse2 = sc.lse2;
+    g.coef = sc.coef;
+    g.dz = sc.dz;
+    g.ldz = ws.vchunk;
     g.v0 = v0;
-    const int rc = launch_gemm(pair, map_h, map_w, g, st);
+    g.acc = acc;
+    g.col_tile0 = ct0;
+    g.n_n = nct;
+    rc = logits_gemm<EPI_DLOGITS>(cg, h, W, T, V, H, g, st);
     if (rc != GRPO_OK) return rc;
-    const __nv_bfloat16* Wc = static_cast<const __nv_bfloat16*>(W) + v0 * H;
-    // d_h[T,H] (+)= dz[T,vc] W_c[vc,H]   (column-major view: d_h^T = W_c^T dz^T)
-    if (d_h &&
-        cublasGemmEx(bh, CUBLAS_OP_N, CUBLAS_OP_N, (int)H, (int)T, (int)vc, &one, Wc, CUDA_R_16BF, (int)H, dz,
-                     CUDA_R_16BF, (int)ws.vchunk, c == 0 ? &zero : &one, d_h, CUDA_R_32F, (int)H,
-                     CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-      return GRPO_ERR_CUDA;
-    // dW_c[vc,H] = dz^T[vc,T] h[T,H]   (column-major view: dW_c^T = h^T dz)
-    if (dW && cublasGemmEx(bh, CUBLAS_OP_N, CUBLAS_OP_T, (int)H, (int)vc, (int)T, &one, h, CUDA_R_16BF, (int)H, dz,
-                           CUDA_R_16BF, (int)ws.vchunk, &zero, dW + v0 * H, CUDA_R_32F, (int)H, CUBLAS_COMPUTE_32F,
-                           CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-      return GRPO_ERR_CUDA;
+    CUtensorMap ma, mb;
+    if (d_h) {
+      // d_h[T, H] (+)= dz_c[T, vc] W_c[vc, H]
+      if (!map_k(&ma, sc.dz, T, vc, ws.vchunk, BM) || !map_mn(&mb, Wb + v0 * H, vc, H, H))
+        return GRPO_ERR_UNSUPPORTED;
+      GemmArgs b{};
+      b.M = T;
+      b.N = H;
+      b.K = vc;
+      b.n_n = (int)((H + BN - 1) / BN);
+      b.m_fast = 0;  // consecutive units share the dz rows
+      b.C = d_h;
+      b.ldc = H;
+      b.accumulate = c > 0;
+      b.acc = acc;
+      rc = launch<EPI_STORE_F32, false, true>(cg, ma, mb, b, st);
+      if (rc != GRPO_OK) return rc;
+    }
+    if (dW) {
+      // dW_c[vc, H] = dz_c^T[vc, T] h[T, H]
+      if (!map_mn(&ma, sc.dz, T, vc, ws.vchunk) || !map_mn(&mb, h, T, H, H)) return GRPO_ERR_UNSUPPORTED;
+      GemmArgs b{};
+      b.M = vc;
+      b.N = H;
+      b.K = T;
+      b.n_n = (int)((H + BN - 1) / BN);
+      b.m_fast = 0;  // consecutive units share the dz columns
+      b.C = dW + v0 * H;
+      b.ldc = H;
+      b.accumulate = 0;
+      b.acc = acc;
+      rc = launch<EPI_STORE_F32, true, true>(cg, ma, mb, b, st);
+      if (rc != GRPO_OK) return rc;
+    }
   }
   return GRPO_OK;
 }
@@ -842,19 +361,45 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
 // file-scope array below instead of a caller workspace.
 //
 // The array is a device symbol: every GPU that loads this library holds its 16 MiB until the
-// process exits. In host code its name only stands in for the symbol; the device address is
-// looked up once per device (with that device current) by cudaGetSymbolAddress and passed to
-// the kernels.
+// process exits. In host code its name only stands in for the symbol; its device address is
+// looked up by cudaGetSymbolAddress (with the device current) and passed to the kernels.
 constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
 static __device__ __align__(256) unsigned char g_lmhead_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
 
-// Device address of the scratch array on the current device; the first call on a device does
-// the lookup and caches it (the GEMM launcher sets the kernel's shared-memory limit on its own
-// first launch on the device).
+// Unique id of the calling thread's current context (cuCtxGetId), or 0 if unavailable.
+unsigned long long current_ctx_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the scratch array in the current device's context. The first call on a
+// device (and the first after that device's primary context was destroyed and re-created, e.g.
+// by cudaDeviceReset: the context id changes) looks it up and records it with the context id;
+// later calls in the same context reuse it without any CUDA call but the id query.
 int noalloc_setup(void** scratch) {
   static void* addr[64] = {};
+  static unsigned long long ctx_of[64] = {};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -863,13 +408,15 @@ int noalloc_setup(void** scratch) {
   }
   if (dev < 0 || dev >= 64) return GRPO_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  const unsigned long long id = addr[dev] ? current_ctx_id() : 0;
+  if (!addr[dev] || id == 0 || id != ctx_of[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_lmhead_noalloc_scratch) != cudaSuccess || !p) {
       (void)cudaGetLastError();
       return GRPO_ERR_CUDA;
     }
     addr[dev] = p;
+    ctx_of[dev] = current_ctx_id();
   }
   *scratch = addr[dev];
   return GRPO_OK;
@@ -884,48 +431,14 @@ extern "C" GRPO_API int grpo_lmhead_forward_noalloc(const void* h, const void* W
                                                     const float* adv_tok, const uint8_t* mask, float clip_eps,
                                                     float grad_scale, float* loss_tok, float* logp_tok,
                                                     grpo_step_acc* acc, void* stream) {
-  if (T < 0 || V < 1 || H < BK || H % BK != 0 || !acc) return GRPO_ERR_INVALID;
-  if (T == 0) return GRPO_OK;
-  if (!h || !W || !target || !adv_tok || !mask || !loss_tok) return GRPO_ERR_INVALID;
-  if (((uintptr_t)h | (uintptr_t)W) & 15u) return GRPO_ERR_INVALID;
-  if (T > INT32_MAX / 2 || V > INT32_MAX / 2) return GRPO_ERR_INVALID;
+  const int arc = check_args(h, W, T, V, H, target, adv_tok, mask, loss_tok, acc);
+  if (arc != GRPO_OK || T == 0) return arc;
   // the forward pass uses the workspace layout up to (not including) the dlogits chunk
-  const WsLayout ws = ws_layout(T, V, kDefaultVChunk);
+  const WsLayout ws = ws_layout(T, V);
   if (ws.dz > kNoAllocScratchBytes) return GRPO_ERR_CAPACITY;
   void* scratch = nullptr;
   const int rc = noalloc_setup(&scratch);
   if (rc != GRPO_OK) return rc;
-  uint8_t* wsb = static_cast<uint8_t*>(scratch);
-  float* part_m = reinterpret_cast<float*>(wsb + ws.part_m);
-  float* part_s = reinterpret_cast<float*>(wsb + ws.part_s);
-  float* zy = reinterpret_cast<float*>(wsb + ws.zy);
-  float* lse2 = reinterpret_cast<float*>(wsb + ws.lse2);
-  float* coef = reinterpret_cast<float*>(wsb + ws.coef);
-
-  const bool pair = use_pair();
-  CUtensorMap map_h, map_w;
-  if (!make_maps(&map_h, &map_w, h, W, T, V, H, pair)) return GRPO_ERR_UNSUPPORTED;
-  const cudaStream_t st = as_stream(stream);
-  GemmArgs g{};
-  g.T = T;
-  g.V = V;
-  g.H = H;
-  g.n_row_tiles = (int)((T + BM - 1) / BM);
-  g.target = target;
-  g.part_m = part_m;
-  g.part_s = part_s;
-  g.zy = zy;
-  g.lse2 = lse2;
-  g.coef = coef;
-  g.acc = acc;
-  g.mode = 0;
-  g.col_tile0 = 0;
-  g.n_col_tiles = ws.n_col_tiles;
-  const int lrc = launch_gemm(pair, map_h, map_w, g, st);
-  if (lrc != GRPO_OK) return lrc;
-  reduce_kernel<<<(unsigned)((T + 255) / 256), 256, 0, st>>>(T, ws.n_col_tiles, part_m, part_s, zy, target, V,
-                                                              old_logp, adv_tok, mask, clip_eps, grad_scale, lse2,
-                                                              coef, loss_tok, logp_tok, acc);
-  GRPO_CUDA_TRY(cudaGetLastError());
-  return GRPO_OK;
+  return forward(cta_group(), h, W, T, V, H, target, old_logp, adv_tok, mask, clip_eps, grad_scale, loss_tok,
+                 logp_tok, acc, ws, carve(scratch, ws), as_stream(stream));
 }

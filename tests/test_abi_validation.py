@@ -109,25 +109,23 @@ def test_lmhead_argument_checks(kw, code):
 
 
 def test_lmhead_workspace_too_small_is_capacity():
-    # one byte short of the recompute path's workspace: no path fits
+    # one byte short of the documented workspace
     need = _lib.grpo_lmhead_workspace_size(256, 1024, 128)
     assert _lm(ws_bytes=need - 1) == _lib.ERR_CAPACITY
 
 
 def test_lmhead_workspace_sizes():
     up = lambda x: (x + 255) // 256 * 256
-    blas = 32 << 20
-    for T, V, H in [(1, 1, 64), (256, 1024, 128), (300, 40000, 512), (16384, 151936, 2048)]:
+    for T, V, H, chunk_tiles in [(1, 1, 64, 1), (256, 1024, 128, 4), (300, 40000, 512, 53),
+                                 (16384, 151936, 2048, 66), (8, 256 * 66, 64, 66), (8, 256 * 67, 64, 34)]:
         plain = _lib.grpo_lmhead_workspace_size(T, V, H)
-        stored = _lib.grpo_lmhead_workspace_size_stored(T, V, H)
         nct = (V + 255) // 256
-        # partials (two float arrays per tile and token), three per-token floats, a bf16
-        # dlogits region, then the GEMM scratch
+        # partials (two float arrays per tile and token), three per-token floats, then the bf16
+        # dlogits chunk buffer: the tiles split into ceil(tiles / 66) chunks of equal width
+        n_chunks = -(-nct // 66)
+        assert -(-nct // n_chunks) == chunk_tiles
         base = 2 * up(4 * nct * T) + 3 * up(4 * T)
-        assert plain == base + up(2 * T * min(16384, 256 * nct)) + blas
-        assert stored == base + up(2 * T * 256 * nct) + blas
-        assert stored >= plain
+        assert plain == base + up(2 * T * 256 * chunk_tiles)
     for bad in [(0, 8, 64), (8, 0, 64), (8, 8, 0), (-1, 8, 64)]:
         assert _lib.grpo_lmhead_workspace_size(*bad) == 0
-        assert _lib.grpo_lmhead_workspace_size_stored(*bad) == 0
     assert _lib.lib().grpo_lmhead_forward_noalloc_max_scratch() == 16 << 20

@@ -1,8 +1,7 @@
-"""GPU parity of the fused LM-head variant (tcgen05 GEMM + softmax epilogue) against the
-float64 oracle: per-token loss and log-prob, d_h and dW, on sizes with ragged token and
-vocabulary tiles, several vocabulary chunks, masked tokens and forward-only calls, through
-both backward paths (the recompute path and, with the larger workspace, the stored-exponent
-path).
+"""GPU parity of the fused LM-head variant (tcgen05 GEMMs + softmax epilogue) against the
+float64 oracle: per-token loss and log-prob, d_h and dW, on sizes with ragged token, vocabulary
+and K tiles, several vocabulary chunks, masked tokens and forward-only calls, for both tile
+shapes (the paired 2-CTA MMA of the product path and the one-CTA instance).
 
 d_h and dW tolerance: both products are formed from bf16 dlogits (rounded to nearest), so
 each element may move by up to ~2^-8 of the sum of the magnitudes of its terms; the bar is
@@ -28,6 +27,13 @@ def _built(grpo_lib):
     return grpo_lib
 
 
+@pytest.fixture(params=[2, 1], ids=["pair", "one_cta"])
+def cta_group(request, monkeypatch):
+    """Tile shape of the LM-head GEMMs (read by the library on every call)."""
+    monkeypatch.setenv("GRPO_LMHEAD_CTA_GROUP", str(request.param))
+    return request.param
+
+
 def _case(T, V, Hd, seed, valid_lo=None, old=True, adv=None, w_row_scale=None):
     wl = W.make_workload("lmhead", seed=seed, rows=4, tokens=T, V=V, H=Hd)
     assert wl.T == T, (wl.T, T)
@@ -50,7 +56,7 @@ def _case(T, V, Hd, seed, valid_lo=None, old=True, adv=None, w_row_scale=None):
     return wl, h, Wt, hb, wb, mask, a_tok, old_logp
 
 
-def _run(h, Wt, wl, mask, a_tok, old_logp, scale, grads=True, stored=False):
+def _run(h, Wt, wl, mask, a_tok, old_logp, scale, grads=True):
     T, Hd = h.shape
     V = Wt.shape[0]
     d_h = torch.full((T, Hd), 7.0, device=DEV) if grads else None
@@ -58,8 +64,7 @@ def _run(h, Wt, wl, mask, a_tok, old_logp, scale, grads=True, stored=False):
     loss = torch.full((T,), -7.0, device=DEV)
     logp = torch.full((T,), -7.0, device=DEV)
     acc = _lib.new_step_acc(DEV)
-    size = (_lib.grpo_lmhead_workspace_size_stored if stored else _lib.grpo_lmhead_workspace_size)(T, V, Hd)
-    ws = torch.empty(size, dtype=torch.uint8, device=DEV)
+    ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=DEV)
     t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
     _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, t(wl.target), t(old_logp), t(a_tok), t(mask), wl.eps, scale,
                                   d_h, dW, loss, logp, acc, ws)
@@ -67,10 +72,10 @@ def _run(h, Wt, wl, mask, a_tok, old_logp, scale, grads=True, stored=False):
     return d_h, dW, loss, logp, acc
 
 
-def _check(T, V, Hd, seed, valid_lo=None, old=True, adv=None, grads=True, stored=False, w_row_scale=None):
+def _check(T, V, Hd, seed, valid_lo=None, old=True, adv=None, grads=True, w_row_scale=None):
     wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed, valid_lo, old, adv, w_row_scale)
     N = max(int(mask.sum()), 1)
-    d_h, dW, loss, logp, acc = _run(h, Wt, wl, mask, a_tok, old_logp, 1.0 / N, grads, stored)
+    d_h, dW, loss, logp, acc = _run(h, Wt, wl, mask, a_tok, old_logp, 1.0 / N, grads)
     ref = OL.lmhead_fwd_bwd(hb, wb, wl.target, old_logp, a_tok, mask, wl.eps, scale=1.0 / N)
     H.assert_tokens_close(H.to_f64(loss), H.to_f64(logp), ref, a_tok, mask)
     res = _lib.grpo_finish_step(acc, loss, expected_N=int(mask.sum()))
@@ -95,46 +100,72 @@ def _check(T, V, Hd, seed, valid_lo=None, old=True, adv=None, grads=True, stored
     return ref
 
 
-@pytest.mark.parametrize("stored", [False, True])
-def test_lmhead_exact_tiles(stored):
-    _check(256, 1024, 128, seed=1, stored=stored)
+def test_lmhead_exact_tiles(cta_group):
+    _check(256, 1024, 128, seed=1)
 
 
-@pytest.mark.parametrize("stored", [False, True])
-def test_lmhead_ragged_tokens_vocab_and_k(stored):
-    # 300 tokens (ragged 128-row tile), V = 1000 (ragged 256-column tile and 32-column group),
-    # H = 192 (three 64-wide K blocks)
-    _check(300, 1000, 192, seed=2, stored=stored)
+def test_lmhead_ragged_tokens_vocab_and_k(cta_group):
+    # 300 tokens (ragged 128-row and 256-row tiles), V = 1000 (ragged 256-column tile and
+    # 32-column group), H = 192 (three 64-wide K blocks; a d_h / dW column tile of 192 of 256)
+    _check(300, 1000, 192, seed=2)
 
 
-@pytest.mark.parametrize("stored", [False, True])
-def test_lmhead_several_vocab_chunks_masked_tokens(stored):
-    # V > 16384: two dlogits chunks, the second ragged; a quarter of the tokens masked
-    _check(128, 20000, 64, seed=3, valid_lo=0.25, stored=stored)
+def test_lmhead_several_vocab_chunks_masked_tokens(cta_group):
+    # V = 40000: 157 vocabulary tiles in three chunks of 53 (the last ragged), so d_h is
+    # accumulated over three chunk products; a quarter of the tokens masked
+    _check(128, 40000, 64, seed=3, valid_lo=0.25)
 
 
-@pytest.mark.parametrize("stored", [False, True])
-def test_lmhead_no_pi_old_and_clip_stress(stored):
+def test_lmhead_no_pi_old_and_clip_stress(cta_group):
     T = 256
     adv = np.random.default_rng(4).choice([-2.0, -0.5, 0.5, 2.0], T)
-    _check(T, 2048, 128, seed=4, old=False, adv=adv, stored=stored)
+    _check(T, 2048, 128, seed=4, old=False, adv=adv)
 
 
-@pytest.mark.parametrize("stored", [False, True])
-def test_lmhead_wide_logit_spread(stored):
-    # columns 300..307 get logits ~300x larger than the rest (spread far beyond 2^64 in the
-    # exponent): the stored path's shift from a tile's first 32 columns is then exceeded and
-    # the tile is redone with its exact maximum
-    _check(256, 1024, 128, seed=6, stored=stored, w_row_scale=(slice(300, 308), 300.0))
+def test_lmhead_wide_logit_spread(cta_group):
+    # columns 300..307 get logits ~300x larger than the rest (a spread far beyond 2^64 in the
+    # exponent): the partials' lazy shift must rescale instead of overflowing
+    _check(256, 1024, 128, seed=6, w_row_scale=(slice(300, 308), 300.0))
 
 
-@pytest.mark.parametrize("stored", [False, True])
-def test_lmhead_forward_only(stored):
-    _check(256, 4096, 256, seed=5, grads=False, stored=stored)
+def test_lmhead_forward_only(cta_group):
+    _check(256, 4096, 256, seed=5, grads=False)
 
 
-@pytest.mark.parametrize("stored", [False, True])
-def test_lmhead_full_size_sampled_rows(stored):
+def test_lmhead_product_vocabulary_full_oracle(cta_group):
+    # the product vocabulary and hidden size (V = 151936, H = 2048) at 512 tokens, where the
+    # float64 oracle forms every logit: per-token outputs on every token, d_h on every row and
+    # dW on 300 sampled vocabulary rows plus every row some token targets, elementwise
+    T, V, Hd = 512, 151936, 2048
+    wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed=11, valid_lo=0.1)
+    N = max(int(mask.sum()), 1)
+    d_h, dW, loss, logp, acc = _run(h, Wt, wl, mask, a_tok, old_logp, 1.0 / N)
+    res = _lib.grpo_finish_step(acc, loss, expected_N=int(mask.sum()))
+    assert res["status"] == 0 and res["kernel_flags"] == 0
+    hf, wf = OL.as_f64(hb), OL.as_f64(wb)
+    ref = OL.lmhead_fwd_bwd(hb, wb, wl.target, old_logp, a_tok, mask, wl.eps, scale=1.0 / N, want_dw=False)
+    H.assert_tokens_close(H.to_f64(loss), H.to_f64(logp), ref, a_tok, mask)
+    z = hf @ wf.T
+    dz = np.zeros_like(z)
+    for t in range(T):
+        if mask[t]:
+            dz[t] = OL.token_objective(z[t], int(wl.target[t]), old_logp[t], a_tok[t], 1, wl.eps, 1.0 / N)[4]
+    del z
+    dz_abs = np.abs(dz)
+    tol_h = 8e-3 * (dz_abs @ np.abs(wf)) + 1e-12
+    gh = H.to_f64(d_h)
+    bad = np.abs(gh - ref["d_h"]) > tol_h
+    assert not bad.any(), (np.argwhere(bad)[:3], gh[bad][:3], ref["d_h"][bad][:3])
+    rows = np.unique(np.concatenate([np.random.default_rng(12).choice(V, 300, replace=False),
+                                     wl.target[mask.astype(bool)], [0, V - 1]]))
+    want = dz[:, rows].T @ hf
+    tol_w = 8e-3 * (dz_abs[:, rows].T @ np.abs(hf)) + 1e-12
+    gw = dW[torch.from_numpy(rows).to(DEV)].double().cpu().numpy()
+    bad = np.abs(gw - want) > tol_w
+    assert not bad.any(), (rows[np.argwhere(bad)[:3, 0]], gw[bad][:3], want[bad][:3])
+
+
+def test_lmhead_full_size_sampled_rows():
     # the full fused LM-head shape (16384 tokens, H = 2048, V = 151936) in the bench's launch
     # configuration; per-token outputs and d_h checked on sampled rows (the oracle recomputes
     # those rows' logits one by one), dW checked by a property that holds at any size: every
@@ -144,10 +175,10 @@ def test_lmhead_full_size_sampled_rows(stored):
     h, Wt = W.make_lmhead_inputs(wl, DEV)
     adv = np.random.default_rng(9).choice([-1.5, -0.3, 0.4, 1.2], T).astype(np.float32)
     N = int(wl.mask.sum())
-    d_h, dW, loss, logp, acc = _run(h, Wt, wl, wl.mask, adv, None, 1.0 / N, stored=stored)
+    d_h, dW, loss, logp, acc = _run(h, Wt, wl, wl.mask, adv, None, 1.0 / N)
     res = _lib.grpo_finish_step(acc, loss, expected_N=N)
-    assert res["status"] == 0 and res["n_valid"] == N
-    rows = np.array([0, 1, 127, 128, 5000, 9999, 16254, 16383])
+    assert res["status"] == 0 and res["n_valid"] == N and res["kernel_flags"] == 0
+    rows = np.array([0, 1, 127, 128, 255, 256, 5000, 9999, 16254, 16383])
     hb = h[torch.from_numpy(rows).to(DEV)].view(torch.int16).cpu().numpy().view(np.uint16)
     wb = Wt.view(torch.int16).cpu().numpy().view(np.uint16)
     ref = OL.lmhead_fwd_bwd(hb, wb, wl.target[rows], None, adv[rows], wl.mask[rows], wl.eps,
@@ -164,3 +195,20 @@ def test_lmhead_full_size_sampled_rows(stored):
     mag = dW.double().abs().sum(0)
     assert torch.all(col.abs() <= 2e-2 * mag + 1e-9)
     assert torch.isfinite(dW).all() and torch.isfinite(d_h).all()
+
+
+def test_lmhead_tile_shapes_agree():
+    # the paired 256 x 256 tiles and the one-CTA 128 x 256 tiles sum every product in the same
+    # K order: identical bits for every output
+    T, V, Hd = 300, 5000, 192
+    wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed=21, valid_lo=0.2)
+    outs = []
+    for cg in (2, 1):
+        import os
+        os.environ["GRPO_LMHEAD_CTA_GROUP"] = str(cg)
+        try:
+            outs.append(_run(h, Wt, wl, mask, a_tok, old_logp, 1.0 / max(int(mask.sum()), 1)))
+        finally:
+            del os.environ["GRPO_LMHEAD_CTA_GROUP"]
+    for a, b in zip(outs[0][:4], outs[1][:4]):
+        assert torch.equal(a, b)

@@ -8,13 +8,15 @@ library keeps the forward pass's scratch in a fixed device array of its own.
 
 This test calls that entry point through the C ABI twice in a row, with different shapes and
 inputs (so the second call runs over whatever the first left in the shared array), and checks
-each result against the workspace entry point's forward pass within the per-token tolerances
-the other parity tests use. The file is named to be collected last.
+each result against the workspace entry point's forward pass and against the float64 oracle,
+within the per-token tolerances the other parity tests use. The file is named to be collected
+last.
 """
 import numpy as np
 import pytest
 import torch
 
+from oracle import loss as OL
 from rl_post_token_gb300 import _lib
 from rl_post_token_gb300 import workloads as W
 
@@ -37,7 +39,7 @@ def _inputs(T, V, Hd, seed, with_old):
     adv = rng.choice([-1.5, -0.4, 0.6, 1.8], T).astype(np.float32)
     old = (rng.normal(-12.0, 1.0, T)).astype(np.float32) if with_old else None
     t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
-    return wl, h, Wt, t(wl.target), t(old), t(adv), t(mask), adv, mask
+    return wl, h, Wt, t(wl.target), t(old), t(adv), t(mask), adv, mask, old
 
 
 def _outputs(T):
@@ -47,7 +49,7 @@ def _outputs(T):
 def test_noalloc_forward_matches_workspace_entry_point():
     cases = [(512, 8192, 128, 1, False), (300, 151936, 256, 2, True)]
     for T, V, Hd, seed, with_old in cases:
-        wl, h, Wt, tgt, old, adv_d, mask_d, adv, mask = _inputs(T, V, Hd, seed, with_old)
+        wl, h, Wt, tgt, old, adv_d, mask_d, adv, mask, old_h = _inputs(T, V, Hd, seed, with_old)
         N = max(int(mask.sum()), 1)
 
         loss_r, logp_r, acc_r = _outputs(T)
@@ -68,6 +70,14 @@ def test_noalloc_forward_matches_workspace_entry_point():
             assert res_n[k] == res_r[k], k
         assert res_n["status"] == 0
         assert abs(res_n["loss"] - res_r["loss"]) <= 1e-5 * max(abs(res_r["loss"]), float(np.mean(np.abs(lr))))
+        # and against the float64 oracle, token by token
+        hb = h.view(torch.int16).cpu().numpy().view(np.uint16)
+        wb = Wt.view(torch.int16).cpu().numpy().view(np.uint16)
+        ref = OL.lmhead_fwd_bwd(hb, wb, wl.target, old_h, adv, mask, wl.eps, scale=1.0 / N, want_dw=False)
+        m = mask.astype(bool)
+        assert np.all(np.abs(pn[m] - ref["logp_tok"][m]) <= 1e-5 * np.maximum(1.0, np.abs(ref["logp_tok"][m])))
+        assert np.all(np.abs(ln - ref["loss_tok"]) <= 1e-5 * np.abs(ref["loss_tok"]) + 1e-7 * np.abs(adv))
+        assert np.all(pn[~m] == 0) and np.all(ln[~m] == 0)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
