@@ -161,20 +161,24 @@ GRPO_API int grpo_plan_token_index(const grpo_plan* plan, int32_t n_rows_in,
 #define GRPO_AGG_SEQ_MEAN_TOKEN_SUM  1
 #define GRPO_AGG_SEQ_MEAN_TOKEN_MEAN 2
 
-/* Divisor and per-token weights of an aggregation mode for every optimizer step of a plan
- * (host only): step_divisor[s] = N_s (TOKEN_MEAN) or B_s (sequence-level modes), and, when
- * w_tok is non-NULL, w_tok[t] = 1/max(n_r, 1) rounded to float for every token t of input row r
- * under SEQ_MEAN_TOKEN_MEAN, else 1. A step's loss is then sum_t w_t loss_t / max(D_s, 1) and
- * each token's gradient scale grad_scale * w_t with grad_scale = 1/max(D_s, 1) (or 1, deferred).
- *  plan         host, from grpo_plan_microbatches (step_in_row_off is read)
- *  row_tok_off  host int64 [n_rows_in + 1] token offsets of the input rows
- *  row_valid    host int32 [n_rows_in] mask = 1 positions per input row (as given to the planner)
- *  step_divisor host int64 [plan->n_steps]
- *  w_tok        host float [row_tok_off[n_rows_in]] or NULL
+/* Divisor, gradient scale and per-token weights of an aggregation mode for every optimizer step
+ * of a plan (host only): step_divisor[s] = N_s (TOKEN_MEAN) or B_s (sequence-level modes);
+ * when step_grad_scale is non-NULL, step_grad_scale[s] = 1/max(D_s, 1) (float64 division
+ * rounded once to float: the grad_scale of the step's loss calls unless a deferred finish
+ * applies it); when w_tok is non-NULL, w_tok[t] = 1/max(n_r, 1) rounded to float for every
+ * token t of input row r under SEQ_MEAN_TOKEN_MEAN, else 1. A step's loss is then
+ * sum_t w_t loss_t / max(D_s, 1) and each token's gradient scale grad_scale * w_t.
+ *  plan            host, from grpo_plan_microbatches (step_in_row_off is read)
+ *  row_tok_off     host int64 [n_rows_in + 1] token offsets of the input rows
+ *  row_valid       host int32 [n_rows_in] mask = 1 positions per input row (as given to the planner)
+ *  step_divisor    host int64 [plan->n_steps]
+ *  w_tok           host float [row_tok_off[n_rows_in]] or NULL
+ *  step_grad_scale host float [plan->n_steps] or NULL
  * Errors: GRPO_ERR_INVALID (NULL required pointer, unknown mode, inconsistent offsets). */
 GRPO_API int grpo_plan_token_weights(const grpo_plan* plan, int32_t n_rows_in,
                                      const int64_t* row_tok_off, const int32_t* row_valid,
-                                     int32_t agg, int64_t* step_divisor, float* w_tok);
+                                     int32_t agg, int64_t* step_divisor, float* w_tok,
+                                     float* step_grad_scale);
 
 /* ---- advantage --------------------------------------------------------------------------- */
 
@@ -396,6 +400,22 @@ GRPO_API int grpo_window_init(grpo_window* w, int32_t n_micro);
  * dropped before a fresh window starts; the divisor resets with it. */
 GRPO_API int grpo_window_chunk(grpo_window* w, int32_t finite, double loss, int64_t denom,
                                int32_t* action, double* step_scale);
+
+/* One optimizer step's result from the results of the n data-parallel ranks that ran its rows,
+ * each rank's finish given the whole step's divisor (grpo_finish_step_ex) so that its gradients
+ * already carry the step's one 1/max(D, 1) ("Sizing mini-batches and micro-batches", "The hard
+ * part: deferred normalization"; "How a context-compaction step fits ...": the valid tokens are
+ * summed over every GPU). Host only. The float64 loss sums and the counts are added in rank
+ * order (index 0 first); loss = that sum / max(divisor, 1); clipfrac = n_clipped / max(n_valid,
+ * 1); status = the first negative status in rank order, else GRPO_STEP_SKIPPED_NONFINITE if
+ * any rank skipped, else GRPO_OK; kernel_flags are OR-ed.
+ *  per_rank  host grpo_step_result [n] (the rank order is the summation order); n = 0 (per_rank
+ *            may then be NULL) gives the empty step: every count and the loss 0, status OK
+ *  divisor   the step's divisor D >= 0 (N for TOKEN_MEAN)
+ *  out       host grpo_step_result (may alias none of per_rank)
+ * Errors: GRPO_ERR_INVALID (NULL pointer, n < 0, divisor < 0). */
+GRPO_API int grpo_combine_step_results(const grpo_step_result* per_rank, int32_t n, int64_t divisor,
+                                       grpo_step_result* out);
 
 /* Token-weighted loss sum(loss_i * denom_i) / max(sum(denom_i), 1) over the trained windows,
  * the summed divisor and the optimizer steps taken (any output may be NULL). */

@@ -127,8 +127,11 @@ def _lib() -> C.CDLL:
                                         _i64p, _i32p, C.c_int32, C.POINTER(grpo_step_result), vp]
     lib.grpo_finish_step_ex.restype = C.c_int
     lib.grpo_plan_token_weights.argtypes = [C.POINTER(grpo_plan), C.c_int32, _i64p, _i32p, C.c_int32, _i64p,
-                                            C.POINTER(C.c_float)]
+                                            C.POINTER(C.c_float), C.POINTER(C.c_float)]
     lib.grpo_plan_token_weights.restype = C.c_int
+    lib.grpo_combine_step_results.argtypes = [C.POINTER(grpo_step_result), C.c_int32, C.c_int64,
+                                              C.POINTER(grpo_step_result)]
+    lib.grpo_combine_step_results.restype = C.c_int
     lib.grpo_lmhead_workspace_size.argtypes = [C.c_int64, C.c_int64, C.c_int64]
     lib.grpo_lmhead_workspace_size.restype = C.c_size_t
     lib.grpo_lmhead_loss_fwd_bwd.argtypes = [vp, vp, C.c_int64, C.c_int64, C.c_int64, vp, vp, vp, vp, C.c_float,
@@ -262,8 +265,10 @@ def grpo_plan_token_index(plan: dict, row_len) -> np.ndarray:
     return out[:n.value]
 
 
-def grpo_plan_token_weights(plan: dict, row_len, row_valid, agg: int, want_w: bool = True):
-    """(step_divisor int64 [n_steps], w_tok float32 [tokens] or None) of an aggregation mode."""
+def grpo_plan_token_weights(plan: dict, row_len, row_valid, agg: int, want_w: bool = True,
+                            want_scale: bool = False):
+    """(step_divisor int64 [n_steps], w_tok float32 [tokens] or None) of an aggregation mode;
+    with want_scale a third item, step_grad_scale float32 [n_steps] (1/max(D_s, 1))."""
     rl = np.asarray(row_len, np.int64)
     off = np.zeros(rl.shape[0] + 1, np.int64)
     np.cumsum(rl, out=off[1:])
@@ -274,12 +279,31 @@ def grpo_plan_token_weights(plan: dict, row_len, row_valid, agg: int, want_w: bo
     p.step_in_row_off = _p32(so)
     div = np.zeros(max(p.n_steps, 1), np.int64)
     w = np.zeros(max(int(off[-1]), 1), np.float32) if want_w else None
+    sc = np.zeros(max(p.n_steps, 1), np.float32) if want_scale else None
+    fp = C.POINTER(C.c_float)
     rc = _lib().grpo_plan_token_weights(C.byref(p), rl.shape[0], off.ctypes.data_as(_i64p), _p32(rv), int(agg),
-                                        div.ctypes.data_as(_i64p),
-                                        None if w is None else w.ctypes.data_as(C.POINTER(C.c_float)))
+                                        div.ctypes.data_as(_i64p), None if w is None else w.ctypes.data_as(fp),
+                                        None if sc is None else sc.ctypes.data_as(fp))
     if rc != OK:
         raise GrpoError(rc, "grpo_plan_token_weights")
-    return div[:p.n_steps], None if w is None else w[:int(off[-1])]
+    out = (div[:p.n_steps], None if w is None else w[:int(off[-1])])
+    return out + (sc[:p.n_steps],) if want_scale else out
+
+
+def grpo_combine_step_results(per_rank, divisor: int) -> dict:
+    """One step's result (dict) from the per-rank results (dicts with the grpo_step_result
+    fields; the list order is the rank order and the summation order)."""
+    n = len(per_rank)
+    arr = (grpo_step_result * max(n, 1))()
+    for k, r in enumerate(per_rank):
+        for name, ctype in grpo_step_result._fields_:
+            v = r.get(name, 0)
+            setattr(arr[k], name, float(v) if ctype is C.c_double else int(v))
+    out = grpo_step_result()
+    rc = _lib().grpo_combine_step_results(arr, n, int(divisor), C.byref(out))
+    if rc != OK:
+        raise GrpoError(rc, "grpo_combine_step_results")
+    return out.as_dict()
 
 
 # ---- device entry points ---------------------------------------------------------------------

@@ -280,7 +280,8 @@ extern "C" GRPO_API int grpo_plan_token_index(const grpo_plan* plan, int32_t n_r
 
 extern "C" GRPO_API int grpo_plan_token_weights(const grpo_plan* plan, int32_t n_rows_in,
                                                 const int64_t* row_tok_off, const int32_t* row_valid,
-                                                int32_t agg, int64_t* step_divisor, float* w_tok) {
+                                                int32_t agg, int64_t* step_divisor, float* w_tok,
+                                                float* step_grad_scale) {
   if (!plan || !row_tok_off || !row_valid || !step_divisor || n_rows_in < 0 || plan->n_steps < 0)
     return GRPO_ERR_INVALID;
   if (agg != GRPO_AGG_TOKEN_MEAN && agg != GRPO_AGG_SEQ_MEAN_TOKEN_SUM && agg != GRPO_AGG_SEQ_MEAN_TOKEN_MEAN)
@@ -301,6 +302,8 @@ extern "C" GRPO_API int grpo_plan_token_weights(const grpo_plan* plan, int32_t n
       B += row_valid[r] >= 1;
     }
     step_divisor[s] = agg == GRPO_AGG_TOKEN_MEAN ? N : B;
+    // the one division of the step, rounded once from float64 to float
+    if (step_grad_scale) step_grad_scale[s] = (float)(1.0 / (double)(step_divisor[s] > 1 ? step_divisor[s] : 1));
     if (!w_tok) continue;
     for (int32_t r = so[s]; r < so[s + 1]; ++r) {
       const float w = agg == GRPO_AGG_SEQ_MEAN_TOKEN_MEAN

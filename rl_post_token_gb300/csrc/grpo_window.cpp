@@ -60,3 +60,32 @@ extern "C" GRPO_API int grpo_window_rollup(const grpo_window* w, double* loss, i
   if (steps) *steps = w->steps;
   return GRPO_OK;
 }
+
+// One optimizer step's result from the results of the data-parallel ranks that ran its rows,
+// each finished with the step's divisor D ("Sizing mini-batches and micro-batches", "The hard
+// part: deferred normalization": the step's loss is divided once by the count of the whole
+// step; "How a context-compaction step fits ...": the valid tokens are summed over every GPU).
+// The float64 loss sums and the counts are added in rank order; loss = sum / max(D, 1).
+extern "C" GRPO_API int grpo_combine_step_results(const grpo_step_result* per_rank, int32_t n, int64_t divisor,
+                                                  grpo_step_result* out) {
+  if ((!per_rank && n > 0) || !out || n < 0 || divisor < 0) return GRPO_ERR_INVALID;
+  grpo_step_result r{};
+  r.status = GRPO_OK;
+  for (int32_t k = 0; k < n; ++k) {
+    const grpo_step_result& x = per_rank[k];
+    r.loss_sum += x.loss_sum;
+    r.n_valid += x.n_valid;
+    r.n_clipped += x.n_clipped;
+    r.n_nonfinite += x.n_nonfinite;
+    r.n_tokens += x.n_tokens;
+    if (x.status < 0 && r.status >= 0)
+      r.status = x.status;  // the first error, in rank order
+    else if (x.status == GRPO_STEP_SKIPPED_NONFINITE && r.status == GRPO_OK)
+      r.status = x.status;
+    r.kernel_flags |= x.kernel_flags;
+  }
+  r.loss = r.loss_sum / (double)(divisor > 1 ? divisor : 1);
+  r.clipfrac = (double)r.n_clipped / (double)(r.n_valid > 1 ? r.n_valid : 1);
+  *out = r;
+  return GRPO_OK;
+}

@@ -116,11 +116,13 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
                                   row_tok_off, adv_tok, stream=st)
         launches += 2
     plain = agg == _lib.AGG_TOKEN_MEAN and w_tok is None
-    divisors = None if plain else bp.token_weights(agg, want_w=False)[0]
+    # each step's divisor D and its grad scale 1/max(D, 1), both from the library
+    divisors, _, scales = _lib.grpo_plan_token_weights(p, bp.row_len, bp.row_valid, agg, want_w=False,
+                                                       want_scale=True)
     for s in range(p["n_steps"]):
         N = int(p["step_valid_tokens"][s])
-        D = N if plain else int(divisors[s])
-        scale = 1.0 if deferred else 1.0 / max(D, 1)
+        D = int(divisors[s])
+        scale = 1.0 if deferred else float(scales[s])
         acc = accs[s * _lib.ACC_BYTES:(s + 1) * _lib.ACC_BYTES]
         if logits_host is not None:
             launches += _host_step(bp, s, logits_host, staging, block_rows, copy_stream, st, dlogits, target,
@@ -281,25 +283,9 @@ def dp_exec_ranges(bp: BatchPlan, s: int, rank: int, world: int) -> List[tuple]:
 
 def combine_step_results(results: List[dict], divisor: int) -> dict:
     """One step's result from the per-rank results of its row blocks (each finished with the
-    step's divisor): sums of the float64 loss sums (in rank order) and of the counts; the loss
-    is the summed loss sum over max(divisor, 1). Status: the first error a rank reports, else
-    skipped if any rank skipped, else OK; kernel flags are OR-ed."""
-    loss_sum = 0.0
-    counts = {k: 0 for k in ("n_valid", "n_clipped", "n_nonfinite", "n_tokens")}
-    status, flags = _lib.OK, 0
-    for res in results:
-        loss_sum += float(res["loss_sum"])
-        for k in counts:
-            counts[k] += int(res[k])
-        st = int(res["status"])
-        if st < 0 and status >= 0:
-            status = st
-        elif st == _lib.STEP_SKIPPED_NONFINITE and status == _lib.OK:
-            status = st
-        flags |= int(res["kernel_flags"])
-    out = dict(counts, loss_sum=loss_sum, loss=loss_sum / max(int(divisor), 1),
-               clipfrac=counts["n_clipped"] / max(counts["n_valid"], 1), status=status, kernel_flags=flags)
-    return out
+    step's divisor), by grpo_combine_step_results: float64 loss sums and counts added in rank
+    order, loss = sum / max(divisor, 1), the first error status, OR-ed kernel flags."""
+    return _lib.grpo_combine_step_results(results, divisor)
 
 
 def dp_allreduce_step_result(res: dict, divisor: int, group=None) -> dict:

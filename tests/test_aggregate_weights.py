@@ -15,6 +15,8 @@ def _prefix_mask(row_len, row_valid):
 def _check(plan, row_len, row_valid, agg):
     from rl_post_token_gb300 import _lib
     div, w = _lib.grpo_plan_token_weights(plan, row_len, row_valid, agg)
+    div2, none, scale = _lib.grpo_plan_token_weights(plan, row_len, row_valid, agg, want_w=False, want_scale=True)
+    assert none is None and np.array_equal(div2, div)
     off = np.concatenate([[0], np.cumsum(np.asarray(row_len, np.int64))])
     mask = _prefix_mask(row_len, row_valid)
     for s in range(plan["n_steps"]):
@@ -22,6 +24,8 @@ def _check(plan, row_len, row_valid, agg):
         soff = off[r0:r1 + 1] - off[r0]
         m = mask[off[r0]:off[r1]]
         assert div[s] == AG.divisor(soff, m, agg)
+        # the step's gradient scale: the oracle's 1/max(D, 1), rounded once to float32
+        assert scale[s] == np.float32(1.0 / max(AG.divisor(soff, m, agg), 1))
         # the weight is the oracle's per-token scale without the step's 1/max(D, 1)
         want = AG.token_scale(soff, m, agg) * max(AG.divisor(soff, m, agg), 1)
         np.testing.assert_allclose(w[off[r0]:off[r1]], want, rtol=1e-7, atol=0)
