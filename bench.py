@@ -163,18 +163,17 @@ class ClockSampler:
 
 
 def profiled_traffic():
-    """Per-valid-token DRAM traffic of the row-pass kernel from the committed ncu summary, or
-    None when the summary is missing or was taken on a different kernel source."""
-    path = os.path.join(ROOT, "profiles", "rowpass_qwen_step_ncu.md")
+    """Per-valid-token DRAM traffic of the row-pass kernel from the committed ncu figure
+    (profiles/rowpass_qwen_step_traffic.json), or None when it is missing or was taken on a
+    different kernel source."""
+    path = os.path.join(ROOT, "profiles", "rowpass_qwen_step_traffic.json")
     try:
-        text = open(path).read()
-    except OSError:
+        with open(path) as f:
+            d = json.load(f)
+        tpv, sha = float(d["traffic_per_valid_token_bytes"]), str(d["kernel_source_sha256"])
+    except (OSError, ValueError, KeyError):
         return None
-    m1 = re.search(r"traffic_per_valid_token_bytes:\s*([0-9.eE+]+)", text)
-    m2 = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
-    if not (m1 and m2):
-        return None
-    return float(m1.group(1)) if kernel_source_sha256() == m2.group(1) else None
+    return tpv if kernel_source_sha256() == sha else None
 
 
 # ---- oracle timing (CPU baseline and reference arm) ----------------------------------------------
@@ -395,21 +394,33 @@ def lmhead_chunks(V):
 
 
 def run_lmhead(args):
-    """Fused LM-head step: advantage, one grpo_lmhead_loss_fwd_bwd call (forward, dlogits, d_h
-    and dW, no [T, V] matrix stored: the backward recomputes each vocabulary chunk's logits),
-    the finish. Roofline: tensor, 6*T*V*H algorithmic flops (forward GEMM and the two backward
-    GEMMs; the recompute's extra 2*T*V*H is not credited). One GPU only."""
+    """The fused LM-head workload as the line's headline (one GPU only)."""
     import torch
-    from rl_post_token_gb300 import build as B
-    from rl_post_token_gb300 import _lib
-    from rl_post_token_gb300 import workloads as W
 
     rank, world, local = dist_env()
     if world > 1:
         raise SystemExit("--workload lmhead runs on one GPU only")
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    from rl_post_token_gb300 import build as B
     B.build()
+    line = measure_lmhead(args, device, rank, local)
+    line.update({"n_gpus": 1, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                 "data": "synthetic"})
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def measure_lmhead(args, device, rank=0, local=0, with_e2e=True, with_cpu=True):
+    """Fused LM-head step: advantage, one grpo_lmhead_loss_fwd_bwd call (forward, dlogits, d_h
+    and dW, no [T, V] matrix stored: the backward recomputes each vocabulary chunk's logits),
+    the finish. Roofline: tensor, 6*T*V*H algorithmic flops (forward GEMM and the two backward
+    GEMMs; the recompute's extra 2*T*V*H is not credited) over the LM-head call's time, timed
+    with CUDA events around each call on its stream."""
+    import torch
+    from rl_post_token_gb300 import _lib
+    from rl_post_token_gb300 import workloads as W
+
     _lib.lib()
     wl = W.make_workload("lmhead", seed=rank, **({"tokens": args.lm_tokens} if args.lm_tokens else {}))
     T, V, Hd = wl.T, wl.V, wl.extra["H"]
@@ -427,11 +438,17 @@ def run_lmhead(args):
     ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
     N = wl.n_valid
+    call_evs = []
 
-    def step(grads=True, old=None, w=ws):
+    def step(grads=True, old=None, w=ws, evs=None):
         _lib.grpo_group_advantage(rewards, wl.group_size, 1e-6, True, adv_r, row_rollout, row_tok_off, adv)
+        if evs is not None:
+            evs.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+            evs[-1][0].record(stream)
         _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, target, old, adv, mask, wl.eps, 1.0 / max(N, 1),
                                       d_h if grads else None, dW if grads else None, loss, logp, acc, w)
+        if evs is not None:
+            evs[-1][1].record(stream)
         _lib.grpo_finish_step(acc, loss, expected_N=N, sync=False)
 
     step(grads=False)  # pi_old by the ahead pass, then seeded noise
@@ -444,10 +461,11 @@ def run_lmhead(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        step(old=old)
+        step(old=old, evs=call_evs)
     e1.record(stream)
     torch.cuda.synchronize(device)
     full_s = e0.elapsed_time(e1) / 1e3 / args.steps
+    call_s = sum(a.elapsed_time(b) for a, b in call_evs) / 1e3 / len(call_evs)
     res = _lib.read_step_result(acc)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
@@ -458,10 +476,56 @@ def run_lmhead(args):
     fwd_s = f0.elapsed_time(f1) / 1e3 / args.steps
     clk = clocks.stop()
 
-    # e2e: every step's inputs (hidden states, weights, side arrays) start in pinned host memory
-    # and are copied up on a copy stream into one of two device input sets, the next step's
-    # copy overlapping this step's compute (the first step's copy does not overlap); the step
-    # result is read back every step
+    e2e = measure_lmhead_e2e(args, wl, device, stream, h, Wt, target, mask, rewards, old, adv_r, adv, row_rollout,
+                             row_tok_off, d_h, dW, loss, logp, acc, ws, res) if with_e2e else None
+    flops = 6.0 * T * V * Hd
+    peak, kind = bf16_peak(sustained=True)
+    line = {
+        "metric": "GRPO loss fwd+bwd valid tokens/s, fused LM-head (V=151936, H=2048, bf16)",
+        "value": N / full_s, "unit": UNIT, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": 1e3 * full_s, "dtype": "bf16",
+        "config": {"workload": WORKLOAD_TEXT["lmhead"], "tokens": T, "vocab": V, "hidden": Hd,
+                   "backward": "logits recomputed per vocabulary chunk (%d chunks), no [T, V] matrix stored "
+                               "(workspace %.2f GB)" % (lmhead_chunks(V), ws.numel() / 1e9),
+                   "l2": "weights 622 MB + hidden 64 MB read per step, larger than L2; no flush"},
+        "roofline": {"bound": "tensor", "achieved": flops / call_s / 1e12, "peak": peak, "unit": "TFLOP/s",
+                     "frac": flops / call_s / 1e12 / peak, "peak_source": f"{kind} bf16_tflops_sustained",
+                     "kernel": "grpo_lmhead_loss_fwd_bwd (its GEMM launches and the per-token reduce), CUDA events "
+                               "around each call",
+                     "ms_per_call": 1e3 * call_s, "flops_per_call": flops,
+                     "executed_flops_per_call": 8.0 * T * V * Hd,
+                     "executed_tflops": 8.0 * T * V * Hd / call_s / 1e12, "traffic": None},
+        "forward_only": {"ms": 1e3 * fwd_s, "tflops": 2.0 * T * V * Hd / fwd_s / 1e12,
+                         "what": "softmax-partials GEMM pass + per-token reduce (2*T*V*H flops)"},
+        "step_result": {k: res[k] for k in ("loss", "n_valid", "clipfrac", "status")},
+        # per step: the advantage (2), pass A and the per-token reduce (2), per vocabulary chunk
+        # the dlogits recompute, the d_h and the dW GEMM (3), the finish (1)
+        "gpu_launches": (5 + 3 * lmhead_chunks(V)) * args.steps,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if clk is not None:
+        line["clocks"] = clk
+    if with_cpu and rank == 0 and not args.no_cpu_baseline:
+        v, n, dt = oracle_lmhead_rate(wl, 16, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": _blas_threads(), "host_cpus": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": f"float64 numpy LM-head oracle (z = h W^T, objective, d_h, dW; its "
+                                          f"products on every BLAS thread), 16 host-drawn tokens per call, "
+                                          f"{n} valid tokens in {dt:.1f} s"}
+    return line
+
+
+def measure_lmhead_e2e(args, wl, device, stream, h, Wt, target, mask, rewards, old, adv_r, adv, row_rollout,
+                       row_tok_off, d_h, dW, loss, logp, acc, ws, ref_res):
+    """The LM-head step through the public API with every step's inputs (hidden states, weights,
+    side arrays) starting in pinned host memory: copied up on a copy stream into one of two
+    device input sets, the next step's copy overlapping this step's compute (the first step's
+    copy does not overlap); the step result is read back every step."""
+    import torch
+    from rl_post_token_gb300 import _lib
+
+    N = wl.n_valid
     host = {"h": h.cpu().pin_memory(), "Wt": Wt.cpu().pin_memory(), "target": target.cpu().pin_memory(),
             "mask": mask.cpu().pin_memory(), "rewards": rewards.cpu().pin_memory(), "old": old.cpu().pin_memory()}
     dev_in = {"h": h, "Wt": Wt, "target": target, "mask": mask, "rewards": rewards, "old": old}
@@ -507,45 +571,80 @@ def run_lmhead(args):
     copy.synchronize()
     e2e_res = _lib.read_step_result(acc)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    flops = 6.0 * T * V * Hd
-    peak, kind = bf16_peak(sustained=True)
-    line = {
-        "metric": "GRPO loss fwd+bwd valid tokens/s, fused LM-head (V=151936, H=2048, bf16)",
-        "value": N / full_s, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
-        "ms_per_step": 1e3 * full_s, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT["lmhead"], "tokens": T, "vocab": V, "hidden": Hd,
-                   "backward": "logits recomputed per vocabulary chunk, no [T, V] matrix stored "
-                               "(workspace %.2f GB)" % (ws.numel() / 1e9),
-                   "l2": "weights 622 MB + hidden 64 MB read per step, larger than L2; no flush"},
-        "roofline": {"bound": "tensor", "achieved": flops / full_s / 1e12, "peak": peak, "unit": "TFLOP/s",
-                     "frac": flops / full_s / 1e12 / peak, "peak_source": f"{kind} bf16_tflops_sustained",
-                     "flops_per_step": flops, "traffic": None},
-        "forward_only": {"ms": 1e3 * fwd_s, "tflops": 2.0 * T * V * Hd / fwd_s / 1e12,
-                         "what": "softmax-partials GEMM pass + per-token reduce (2*T*V*H flops)"},
-        "step_result": {k: res[k] for k in ("loss", "n_valid", "clipfrac", "status")},
-        "e2e": {"value": N / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(host_res.numel()), "steps": e2e_steps,
-                "how": "hidden states, weights and side inputs copied from pinned host memory every step on a "
-                       "copy stream into one of two device input sets (the next step's copy overlaps this step's "
-                       "compute, the first step's does not), the step result read back every step",
-                "step_result_matches": all(e2e_res[k] == res[k] for k in ("loss", "n_valid", "clipfrac", "status"))},
-        # per step: the advantage (2), pass A and the per-token reduce (2), per vocabulary chunk
-        # the dlogits recompute, the d_h and the dW GEMM (3), the finish (1)
-        "gpu_launches": (5 + 3 * lmhead_chunks(V)) * args.steps,
+    keys = ("loss", "n_valid", "clipfrac", "status")
+    return {"value": N / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(host_res.numel()), "steps": e2e_steps,
+            "how": "hidden states, weights and side inputs copied from pinned host memory every step on a "
+                   "copy stream into one of two device input sets (the next step's copy overlaps this step's "
+                   "compute, the first step's does not), the step result read back every step",
+            "step_result_matches": all(e2e_res[k] == ref_res[k] for k in keys)}
+
+
+def time_rowpass(args, batch, device, stream, world, local, clocks_name):
+    """Warm up, then time `args.steps` whole batches between a barrier and a synchronize on
+    both sides, sampling the clocks during the timed region. Returns the timing record."""
+    import torch
+    from rl_post_token_gb300 import step as S
+
+    for _ in range(max(args.warmup, 3)):
+        batch.replan(stream)
+        batch.run(stream=stream)
+    torch.cuda.synchronize(device)
+    clocks = ClockSampler(_gpu_index(local), os.path.join(args.clocks_dir, clocks_name))
+    time.sleep(0.5)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    evs = []
+    start.record(stream)
+    for _ in range(args.steps):
+        batch.replan(stream)
+        launches += batch.run(stream=stream, launch_events=evs)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world, device)
+    clk = clocks.stop()
+    elapsed = start.elapsed_time(end) / 1e3
+    # the dominant kernel: row-pass launches timed on the streams they run on inside the timed
+    # region (the union of their intervals: a step's chunks alternate between two streams)
+    row_s = busy_seconds(start, evs)
+    per_launch_bytes = batch.algorithmic_bytes() / (len(evs) / args.steps)
+    return {"elapsed": elapsed, "launches": launches, "n_launches": len(evs), "row_s": row_s, "clocks": clk,
+            "achieved_gbs": per_launch_bytes / (row_s / len(evs)) / 1e9,
+            "results": S.read_results(batch.accs, batch.bp.n_steps)}
+
+
+def rowpass_entry(args, wl, batch, tm, world, device, workload, traffic_per_valid=None, terms_text=""):
+    """The JSON record of one row-pass workload: whole-job valid tokens/s, the row pass's
+    roofline (algorithmic bytes per launch over its average launch time), clocks, results."""
+    units = wl.n_valid * args.steps
+    max_el, all_units = reduce_timing(tm["elapsed"], units, world, device)
+    peak, peak_kind = hbm_peak()
+    launches_per_step = tm["n_launches"] / args.steps
+    entry = {
+        "metric": METRIC, "value": all_units / max_el, "unit": UNIT, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": 1e3 * max_el / args.steps,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "config": {"workload": WORKLOAD_TEXT[workload] + (f" [rows overridden: {args.rows}]" if args.rows else "")
+                               + (f" [loss terms: {terms_text}]" if terms_text else ""),
+                   "valid_tokens_per_step": wl.n_valid,
+                   "logits_rows_per_step": batch.bp.exec_tokens, "vocab": wl.V,
+                   "l2": "inputs larger than L2 (%.1f GB of logits per step), no flush"
+                         % (batch.bp.exec_tokens * wl.V * wl.elem_bytes / 1e9),
+                   "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "achieved": tm["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": tm["achieved_gbs"] / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                     "frac_of_8tbs": tm["achieved_gbs"] / 8000.0,
+                     "kernel": "row pass (grpo_logprob_loss_fwd_bwd" + (f"_ex: {terms_text})" if terms_text else ")"),
+                     "row_pass_share_of_step": tm["row_s"] / tm["elapsed"],
+                     "traffic": None if traffic_per_valid is None else traffic_per_valid * wl.n_valid / launches_per_step},
+        "gpu_launches": tm["launches"],
+        "step_results": [{k: r[k] for k in ("loss", "n_valid", "clipfrac", "status")} for r in tm["results"]],
     }
-    if clk is not None:
-        line["clocks"] = clk
-    if rank == 0 and not args.no_cpu_baseline:
-        v, n, dt = oracle_lmhead_rate(wl, 16, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": _blas_threads(), "host_cpus": os.cpu_count(),
-                                "kind": "oracle",
-                                "sample": f"float64 numpy LM-head oracle (z = h W^T, objective, d_h, dW; its "
-                                          f"products on every BLAS thread), 16 host-drawn tokens per call, "
-                                          f"{n} valid tokens in {dt:.1f} s"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    return 0
+    if tm["clocks"] is not None:
+        entry["clocks"] = tm["clocks"]
+    return entry
 
 
 def run_gb300(args):
@@ -565,7 +664,6 @@ def run_gb300(args):
         B.build()
     barrier(world, device)
     from rl_post_token_gb300 import _lib
-    from rl_post_token_gb300 import step as S
     from rl_post_token_gb300 import workloads as W
 
     _lib.lib()
@@ -582,80 +680,43 @@ def run_gb300(args):
                             if args.ent_coef else []) +
                            ([f"aggregation {args.agg}"] if agg != _lib.AGG_TOKEN_MEAN else []))
     stream = torch.cuda.current_stream(device)
-
-    for _ in range(max(args.warmup, 3)):
-        batch.replan(stream)
-        batch.run(stream=stream)
-    torch.cuda.synchronize(device)
-
-    clocks = ClockSampler(_gpu_index(local), os.path.join(args.clocks_dir, f"clocks_rank{rank}.csv"))
-    time.sleep(0.5)
-    barrier(world, device)
-    torch.cuda.synchronize(device)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches = 0
-    evs = []
-    start.record(stream)
-    for _ in range(args.steps):
-        batch.replan(stream)
-        launches += batch.run(stream=stream, launch_events=evs)
-    end.record(stream)
-    torch.cuda.synchronize(device)
-    barrier(world, device)
-    clk = clocks.stop()
-    elapsed = start.elapsed_time(end) / 1e3
-    results = S.read_results(batch.accs, batch.bp.n_steps)
-
-    # the dominant kernel: row-pass launches timed on the streams they run on inside the timed
-    # region (the union of their intervals: a step's chunks alternate between two streams)
-    row_s = busy_seconds(start, evs)
-    per_launch_bytes = batch.algorithmic_bytes() / (len(evs) / args.steps)
-    achieved_gbs = per_launch_bytes / (row_s / len(evs)) / 1e9
-
-    units = wl.n_valid * args.steps
-    max_el, all_units = reduce_timing(elapsed, units, world, device)
-    value = all_units / max_el
+    tm = time_rowpass(args, batch, device, stream, world, local, f"clocks_rank{rank}.csv")
+    # the committed capture is of the default workload's instance without terms
+    tpv = profiled_traffic() if args.workload == "qwen_step" and not terms_text and not args.rows else None
+    line = rowpass_entry(args, wl, batch, tm, world, device, args.workload, tpv, terms_text)
+    line.update({"n_gpus": world, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                 "data": "synthetic"})
 
     ahead = run_ahead(batch, stream, steps=min(args.steps, 30))
     barrier(world, device)
-    e2e = run_e2e(batch, device, stream, steps=min(args.steps, args.e2e_steps), ref_results=results)
+    e2e = run_e2e(batch, device, stream, steps=min(args.steps, args.e2e_steps), ref_results=tm["results"])
     # whole job: every rank's tokens over the slowest rank's time, as for `value`
     e2e_el, e2e_units = reduce_timing(e2e.pop("elapsed_s"), e2e.pop("units"), world, device)
     e2e["value"] = e2e_units / e2e_el
-
-    peak, peak_kind = hbm_peak()
-    tpv = profiled_traffic()
-    launches_per_step = len(evs) / args.steps
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": max(args.warmup, 3), "ms_per_step": 1e3 * max_el / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload] + (f" [rows overridden: {args.rows}]" if args.rows else "")
-                               + (f" [loss terms: {terms_text}]" if terms_text else ""),
-                   "valid_tokens_per_step": wl.n_valid,
-                   "logits_rows_per_step": batch.bp.exec_tokens, "vocab": wl.V,
-                   "l2": "inputs larger than L2 (%.1f GB of logits per step), no flush"
-                         % (batch.bp.exec_tokens * wl.V * wl.elem_bytes / 1e9),
-                   "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
-        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
-                     "frac": achieved_gbs / peak, "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": "row pass (grpo_logprob_loss_fwd_bwd" + (f"_ex: {terms_text})" if terms_text else ")"),
-                     "row_pass_share_of_step": row_s / elapsed,
-                     # the committed capture is of the instance without terms
-                     "traffic": None if tpv is None or terms_text else tpv * wl.n_valid / launches_per_step},
-        "gpu_launches": launches,
-        "e2e": e2e,
-        "ahead_pass": dict(ahead, frac=ahead["achieved_gbs"] / hbm_peak()[0], per_gpu=True),
-        "step_results": [{k: r[k] for k in ("loss", "n_valid", "clipfrac", "status")} for r in results],
-    }
-    if clk is not None:
-        line["clocks"] = clk
+    line["e2e"] = e2e
+    line["ahead_pass"] = dict(ahead, frac=ahead["achieved_gbs"] / hbm_peak()[0], per_gpu=True)
     if rank == 0 and not args.no_cpu_baseline:
         v, n, dt = oracle_sample_rate(wl, 16, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "host_cpus": os.cpu_count(), "kind": "oracle",
                                 "sample": f"float64 numpy oracle (one thread) on {n} valid tokens "
                                           f"({dt:.1f} s) of a host-drawn sample of the workload"}
+    del batch
+
+    # the other workloads of the method, timed the same way on the same GPU (one GPU only)
+    if world == 1 and args.workload == "qwen_step" and not args.no_extra_workloads and not args.rows \
+            and not terms_text:
+        extra = {}
+        for name in ("dynamic", "compaction"):
+            torch.cuda.empty_cache()
+            wx = W.make_workload(name, seed=rank)
+            bx = Batch(wx, device)
+            tmx = time_rowpass(args, bx, device, stream, world, local, f"clocks_{name}_rank{rank}.csv")
+            extra[name] = rowpass_entry(args, wx, bx, tmx, world, device, name)
+            del bx
+        torch.cuda.empty_cache()
+        extra["lmhead"] = measure_lmhead(args, device, rank, local, with_e2e=False, with_cpu=False)
+        line["workloads"] = extra
+        line["gpu_launches"] += sum(e["gpu_launches"] for e in extra.values())
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -714,6 +775,104 @@ def _gpu_index(local: int) -> int:
     return local
 
 
+# ---- host memory placement (NUMA) -----------------------------------------------------------------
+
+def gpu_numa_node(local: int):
+    """NUMA node the GPU's PCI function reports (sysfs numa_node), or None if unknown."""
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=pci.bus_id", "--format=csv,noheader",
+                              "-i", str(_gpu_index(local))], capture_output=True, text=True, timeout=20).stdout
+        bus = out.strip().splitlines()[0].strip().lower()
+        dom, rest = bus.split(":", 1)
+        path = f"/sys/bus/pci/devices/{int(dom, 16):04x}:{rest}/numa_node"
+        node = int(open(path).read().strip())
+        return node if node >= 0 else None
+    except Exception:
+        return None
+
+
+def node_cpus(node: int):
+    """CPUs of a NUMA node (sysfs cpulist), or an empty set."""
+    cpus = set()
+    try:
+        for part in open(f"/sys/devices/system/node/node{node}/cpulist").read().strip().split(","):
+            if "-" in part:
+                a, b = part.split("-")
+                cpus.update(range(int(a), int(b) + 1))
+            elif part:
+                cpus.add(int(part))
+    except OSError:
+        pass
+    return cpus
+
+
+def page_nodes(t, samples: int = 16):
+    """NUMA nodes of `samples` pages spread over a host tensor (move_pages with no target
+    nodes only reports where each page is), as {node: pages}; None if the query fails."""
+    import ctypes
+    import platform
+
+    nr = {"aarch64": 239, "x86_64": 279}.get(platform.machine())
+    if nr is None or t.numel() == 0:
+        return None
+    base, nbytes = t.data_ptr(), t.numel() * t.element_size()
+    page = os.sysconf("SC_PAGE_SIZE")
+    addrs = sorted({(base + k * nbytes // samples) // page * page for k in range(samples)})
+    n = len(addrs)
+    pages = (ctypes.c_void_p * n)(*addrs)
+    status = (ctypes.c_int * n)()
+    libc = ctypes.CDLL(None, use_errno=True)
+    libc.syscall.restype = ctypes.c_long
+    rc = libc.syscall(ctypes.c_long(nr), ctypes.c_int(0), ctypes.c_ulong(n), pages, None, status, ctypes.c_int(0))
+    if rc != 0:
+        return None
+    out = {}
+    for v in status:
+        out[int(v)] = out.get(int(v), 0) + 1
+    return out
+
+
+def pinned_like(t, local: int):
+    """A pinned host copy of device tensor `t`, allocated (and first touched) by this thread
+    while it is bound to the CPUs of the GPU's NUMA node, so that its pages sit on that node.
+    Returns (tensor, placement record)."""
+    import torch
+
+    node = gpu_numa_node(local)
+    cpus = node_cpus(node) if node is not None else set()
+    old = os.sched_getaffinity(0)
+    bound = False
+    if cpus and (cpus & old):
+        os.sched_setaffinity(0, cpus & old)
+        bound = True
+    try:
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.view(torch.uint8).zero_()  # first touch on the bound CPUs
+    finally:
+        if bound:
+            os.sched_setaffinity(0, old)
+    h.copy_(t)
+    return h, {"gpu_numa_node": node, "bound_to_gpu_node": bound, "host_pages_by_node": page_nodes(h)}
+
+
+def _d2h_copy_gbs(host, dev, stream, reps: int = 8) -> float:
+    """GB/s of `reps` plain device->host copies into the start of the pinned tensor `host`."""
+    import torch
+
+    dst = host.reshape(-1).view(torch.uint8)
+    n = min(dst.numel(), dev.numel())
+    dst, dev = dst[:n], dev[:n]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        dst.copy_(dev, non_blocking=True)
+        e0.record(stream)
+        for _ in range(reps):
+            dst.copy_(dev, non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    return reps * n / (e0.elapsed_time(e1) / 1e3) / 1e9
+
+
 def _h2d_copy_gbs(host, dev, stream, reps: int = 8) -> float:
     """GB/s of `reps` plain host->device copies from the start of the pinned tensor `host`
     into `dev` (`dev`'s size, or all of `host` if smaller), timed with CUDA events on
@@ -744,8 +903,7 @@ def run_e2e(batch, device, stream, steps: int, ref_results=None):
     - the step results are read back."""
     import torch
 
-    host_logits = torch.empty(batch.logits.shape, dtype=batch.logits.dtype, pin_memory=True)
-    host_logits.copy_(batch.logits)
+    host_logits, placement = pinned_like(batch.logits, device.index)
     side = {k: getattr(batch, k).cpu().pin_memory() for k in ("target", "mask", "rewards", "old")
             + (("ref",) if batch.ref is not None else ()) + (("w_tok",) if batch.w_tok is not None else ())}
     host_res = torch.empty(batch.accs.numel(), dtype=torch.uint8, pin_memory=True)
@@ -775,6 +933,7 @@ def run_e2e(batch, device, stream, steps: int, ref_results=None):
         step_s.append(time.perf_counter() - ts)
     dt = time.perf_counter() - t0
     link_after = _h2d_copy_gbs(host_logits, staging, copy)
+    d2h_link = _d2h_copy_gbs(host_logits, staging, copy)
     from rl_post_token_gb300 import step as S
     keys = ("loss", "n_valid", "clipfrac", "status")
     got = [{k: r[k] for k in keys} for r in S.read_results(host_res, batch.bp.n_steps)]
@@ -787,9 +946,11 @@ def run_e2e(batch, device, stream, steps: int, ref_results=None):
             "step_ms": [round(1e3 * x, 2) for x in step_s],
             "value_at_median_step": batch.wl.n_valid / float(np.median(step_s)),
             "step_results_match": match,
-            "link_copy_gbs": {"before": link_before, "after": link_after,
+            "link_copy_gbs": {"before": link_before, "after": link_after, "d2h": d2h_link,
                               "what": "plain pinned host->device copies of the staging buffer's size, "
-                                      "on the copy stream, just before and just after the timed steps"},
+                                      "on the copy stream, just before and just after the timed steps; "
+                                      "d2h: device->host copies of the same size after them"},
+            "host_placement": placement,
             "how": "pinned host logits streamed by grpo_logprob_loss_fwd_bwd_host (1024-row blocks through a "
                    "two-block device staging buffer, copies overlapped with the row pass); side inputs copied "
                    "and step results read back every step"}
@@ -807,6 +968,9 @@ def main(argv=None):
     ap.add_argument("--clocks-dir", default=tempfile.gettempdir(),
                     help="where the raw clock samples of the timed region are written (CSV)")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="time only the chosen workload (the default line also times the dynamic, compaction "
+                         "and fused LM-head workloads)")
     ap.add_argument("--lm-tokens", type=int, default=0,
                     help="override the fused LM-head token count (smaller cases for profiling)")
     ap.add_argument("--rows", type=int, default=0,

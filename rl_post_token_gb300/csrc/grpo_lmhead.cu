@@ -110,6 +110,20 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The dlogits chunk buffer [T][ld] as a TMA store target: the chunk's vc columns, box 32 x 32,
+// 64-byte swizzle (the epilogue's staging layout).
+bool map_dz_store(CUtensorMap* m, const void* base, int64_t T, int64_t vc, int64_t ld) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)vc, (cuuint64_t)T};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)EPI_BOX, (cuuint32_t)EPI_BOX};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Operand maps. K-major [rows][K]: box {64 K, box_rows rows}. MN-major [K][MN]: box {64 MN, 64 K}.
 bool map_k(CUtensorMap* m, const void* base, int64_t rows, int64_t k, int64_t ld, int box_rows) {
   return make_map(m, base, (uint64_t)k, (uint64_t)rows, (uint64_t)ld, (uint32_t)box_rows);
@@ -127,8 +141,8 @@ int cta_group() {
 // One persistent launch over g's units. The first launch of an instance on a device sets its
 // shared-memory limit and caches how many CTAs (or CTA pairs) fit at once.
 template <int CG, int EPI, bool AMN, bool BMN>
-int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs g, cudaStream_t st) {
-  using S = Shape<CG>;
+int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, GemmArgs g, cudaStream_t st) {
+  using S = Shape<CG, EPI>;
   auto kern = gemm_kernel<CG, EPI, AMN, BMN>;
   g.n_m = (int)((g.M + BM * CG - 1) / (BM * CG));
   int dev = 0;
@@ -165,27 +179,30 @@ int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs g, cudaStrea
   const int64_t units = std::min<int64_t>((int64_t)g.n_m * g.n_n, max_units);
   if (units <= 0) return GRPO_OK;
   cfg.gridDim = dim3((unsigned)(CG * units), 1, 1);
-  GRPO_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, ma, mb, g));
+  GRPO_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, g));
   return GRPO_OK;
 }
 
+// mc: the TMA store target of the dlogits epilogue (unused by the other epilogues)
 template <int EPI, bool AMN, bool BMN>
-int launch(int cg, const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& g, cudaStream_t st) {
-  return cg == 2 ? launch_t<2, EPI, AMN, BMN>(ma, mb, g, st) : launch_t<1, EPI, AMN, BMN>(ma, mb, g, st);
+int launch(int cg, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const GemmArgs& g,
+           cudaStream_t st) {
+  return cg == 2 ? launch_t<2, EPI, AMN, BMN>(ma, mb, mc, g, st) : launch_t<1, EPI, AMN, BMN>(ma, mb, mc, g, st);
 }
 
 // Logits GEMM over vocabulary tiles [col_tile0, col_tile0 + g.n_n): A = h [T, H], B = W [V, H],
 // both K-major; the epilogue is EPI.
 template <int EPI>
 int logits_gemm(int cg, const void* h, const void* W, int64_t T, int64_t V, int64_t H, GemmArgs g,
-                cudaStream_t st) {
-  CUtensorMap ma, mb;
+                cudaStream_t st, int64_t vc = 0) {
+  CUtensorMap ma, mb, mc = {};
   if (!map_k(&ma, h, T, H, H, BM) || !map_k(&mb, W, V, H, H, BN / cg)) return GRPO_ERR_UNSUPPORTED;
+  if (EPI == EPI_DLOGITS && !map_dz_store(&mc, g.dz, T, vc, g.ldz)) return GRPO_ERR_UNSUPPORTED;
   g.M = T;
   g.K = H;
   g.V = V;
   g.m_fast = 1;  // consecutive units share the W tile
-  return launch<EPI, false, false>(cg, ma, mb, g, st);
+  return launch<EPI, false, false>(cg, ma, mb, mc, g, st);
 }
 
 }  // namespace lmhead
@@ -310,7 +327,7 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
     g.acc = acc;
     g.col_tile0 = ct0;
     g.n_n = nct;
-    rc = logits_gemm<EPI_DLOGITS>(cg, h, W, T, V, H, g, st);
+    rc = logits_gemm<EPI_DLOGITS>(cg, h, W, T, V, H, g, st, vc);
     if (rc != GRPO_OK) return rc;
     CUtensorMap ma, mb;
     if (d_h) {
@@ -327,7 +344,7 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
       b.ldc = H;
       b.accumulate = c > 0;
       b.acc = acc;
-      rc = launch<EPI_STORE_F32, false, true>(cg, ma, mb, b, st);
+      rc = launch<EPI_STORE_F32, false, true>(cg, ma, mb, ma, b, st);
       if (rc != GRPO_OK) return rc;
     }
     if (dW) {
@@ -343,7 +360,7 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
       b.ldc = H;
       b.accumulate = 0;
       b.acc = acc;
-      rc = launch<EPI_STORE_F32, true, true>(cg, ma, mb, b, st);
+      rc = launch<EPI_STORE_F32, true, true>(cg, ma, mb, ma, b, st);
       if (rc != GRPO_OK) return rc;
     }
   }

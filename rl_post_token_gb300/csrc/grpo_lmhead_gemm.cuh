@@ -38,14 +38,23 @@ constexpr int TMEM_COLS = 2 * BN;
 
 enum Epi : int { EPI_PARTIALS = 0, EPI_DLOGITS = 1, EPI_STORE_F32 = 2 };
 
-template <int CG>
+// Dlogits epilogue staging: each epilogue warp writes its 32 rows x 32 columns of bf16 (2 KB,
+// 64-byte rows in the 64-byte swizzle a TMA store expects) into one of two buffers, and one lane
+// stores the box with a TMA tile store (full 64-byte row segments instead of 32 scattered
+// 16-byte pieces per store instruction).
+constexpr int EPI_BOX = 32;                          // rows and columns of a staged box
+constexpr int EPI_BUF_BYTES = EPI_BOX * EPI_BOX * 2;  // 2 KB
+constexpr int EPI_WARPS = 4;
+
+template <int CG, int EPI = EPI_PARTIALS>
 struct Shape {
   static constexpr int A_BYTES = BM * BK * 2;            // 16 KB
   static constexpr int B_ROWS = BN / CG;                 // rows of B this CTA stages
   static constexpr int B_BYTES = B_ROWS * BK * 2;        // 16 KB (CG = 2) or 32 KB
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // bytes this CTA receives per stage
   static constexpr int STAGES = CG == 2 ? 6 : 4;
-  static constexpr size_t SMEM = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_BYTES + 256;
+  static constexpr int EPI_BYTES = EPI == EPI_DLOGITS ? EPI_WARPS * 2 * EPI_BUF_BYTES : 0;
+  static constexpr size_t SMEM = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_BYTES + EPI_BYTES + 256;
 };
 
 // Instruction descriptor of tcgen05.mma kind::f16: D f32, A and B bf16, the major-ness of each
@@ -109,6 +118,25 @@ __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* ma
   } else {
     tma2d<CG>(dst, map, bar, k0, mn0);
   }
+}
+
+// 2-D TMA tile store from this CTA's shared memory (bulk-group completion); the parts of the
+// box outside the tensor map's extents are not written.
+__device__ __forceinline__ void tma_store2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most N of this thread's committed bulk groups may still be reading shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// this thread's generic-proxy shared-memory writes become visible to the async proxy (TMA)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 template <int CG>
@@ -256,20 +284,27 @@ __device__ __forceinline__ void epi_partials(const GemmArgs& g, uint32_t taddr, 
 
 // dlogits of one tile: dz = coef * 2^(z log2 e - LSE2) - coef [v == y], rounded to bf16 (|coef|
 // is folded into the exponent, its sign applied to the packed pair). Masked and clipped tokens
-// (coef = 0) give zero rows. Columns past the vocabulary are not written.
-__device__ __forceinline__ void epi_dlogits(const GemmArgs& g, uint32_t taddr, int64_t row, bool rok, int ct) {
+// (coef = 0) give zero rows. Each 32-column group of the warp's 32 rows is staged in shared
+// memory (64-byte swizzle: chunk q of row r at q ^ ((r >> 1) & 3), conflict-free for the
+// warp's 16-byte writes) and written by one TMA store through map_c, whose extents (the chunk's
+// vocabulary columns, T rows) clip the vocabulary tail and the rows past T.
+__device__ __forceinline__ void epi_dlogits(const GemmArgs& g, const CUtensorMap* map_c, uint32_t taddr,
+                                            int64_t row, bool rok, int ct, int64_t warp_row0, uint32_t stage_buf,
+                                            int lane) {
   const int64_t c0 = (int64_t)ct * BN;
   const int32_t y = rok ? g.target[row] : -1;
   const float cf = rok ? g.coef[row] : 0.f;
   const float l2 = rok ? g.lse2[row] : 0.f;
   const float cexp = l2 - log2f(fabsf(cf));
   const uint32_t sgn = cf < 0.f ? 0x80008000u : 0u;
+  const uint32_t sw = (uint32_t)((lane >> 1) & 3);
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     float v[32];
     tmem_ld32(taddr + c * 32, v);
     const int64_t cb = c0 + c * 32;
-    if (!rok || cb >= g.V) continue;
+    // warp-uniform: the rest of the tile lies past the vocabulary, or all 32 rows past T
+    if (cb >= g.V || warp_row0 >= g.M) continue;
     uint32_t w[16];
     if (cf != 0.f) {
       float zyv = 0.f;
@@ -298,15 +333,20 @@ __device__ __forceinline__ void epi_dlogits(const GemmArgs& g, uint32_t taddr, i
 #pragma unroll
       for (int i = 0; i < 16; ++i) w[i] = 0u;
     }
-    __nv_bfloat16* dst = g.dz + row * g.ldz + (cb - g.v0);
-    const int nvalid = (int)(g.V - cb < 32 ? g.V - cb : 32);
-    if (nvalid == 32) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst);
+    const uint32_t buf = stage_buf + (uint32_t)(c & 1) * EPI_BUF_BYTES;
+    if (lane == 0) bulk_wait_read<1>();  // the store issued from this buffer two groups ago has read it
+    __syncwarp();
+    const uint32_t rb = buf + (uint32_t)lane * 64u;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-    } else {
-      for (int i = 0; i < nvalid; ++i)
-        dst[i] = __ushort_as_bfloat16((unsigned short)((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu)));
+    for (int q = 0; q < 4; ++q)
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rb + (((uint32_t)q ^ sw) << 4)),
+                   "r"(w[4 * q]), "r"(w[4 * q + 1]), "r"(w[4 * q + 2]), "r"(w[4 * q + 3])
+                   : "memory");
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store2d(map_c, buf, (int)(cb - g.v0), (int)warp_row0);
+      bulk_commit();
     }
   }
 }
@@ -341,13 +381,15 @@ __device__ __forceinline__ void epi_store_f32(const GemmArgs& g, uint32_t taddr,
 
 template <int CG, int EPI, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(NTHREADS, 1)
-gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, GemmArgs g) {
-  using S = Shape<CG>;
+gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+            const __grid_constant__ CUtensorMap map_c, GemmArgs g) {
+  using S = Shape<CG, EPI>;
   constexpr uint32_t ID = idesc<CG, A_MN, B_MN>();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
-  uint64_t* full = reinterpret_cast<uint64_t*>(sgen + S::STAGES * S::STAGE_BYTES);
+  const uint32_t epi_base = sbase + S::STAGES * S::STAGE_BYTES;  // dlogits staging (1024-aligned)
+  uint64_t* full = reinterpret_cast<uint64_t*>(sgen + S::STAGES * S::STAGE_BYTES + S::EPI_BYTES);
   uint64_t* empty = full + S::STAGES;
   uint64_t* tfull = empty + S::STAGES;  // [2]
   uint64_t* tempty = tfull + 2;         // [2]
@@ -472,7 +514,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
       if constexpr (EPI == EPI_PARTIALS)
         epi_partials(g, taddr, row, rok, g.col_tile0 + nu);
       else if constexpr (EPI == EPI_DLOGITS)
-        epi_dlogits(g, taddr, row, rok, g.col_tile0 + nu);
+        epi_dlogits(g, &map_c, taddr, row, rok, g.col_tile0 + nu, row - lane,
+                    epi_base + (uint32_t)quarter * 2u * EPI_BUF_BYTES, lane);
       else
         epi_store_f32(g, taddr, row, rok, (int64_t)nu * BN);
       fence_before();
@@ -488,6 +531,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         aphase ^= 1u;
       }
     }
+    if (EPI == EPI_DLOGITS && lane == 0) bulk_wait_all();  // this warp's stores are complete
   }
 
   fence_before();

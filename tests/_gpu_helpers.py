@@ -6,10 +6,18 @@ rounding 2^-9):
 * log-prob:   |d| <= 1e-5 * max(1, |ref|)
 * token loss: |d| <= 1e-5 * |ref| + 1e-7 * |A|
 * step loss:  |d| <= 1e-5 * max(|L_ref|, sum|m * l| / N)
-* dlogits, bf16 output:  |d| <= 1e-2 * |ref| + 1e-6 * max|ref row|
-* dlogits, f32 output:   |d| <= 2e-5 * |ref| + 1e-30
-  and at the target element, where coef * (p_y - 1) cancels when p_y is near 1, a further
+* dlogits, every element, relative to its own value:
+      bf16 output:  |d| <= 1e-2 * |ref| + 2^-120
+      f32 output:   |d| <= 2e-5 * |ref| + 2^-120
+  The 2^-120 floor only admits results that underflow: the kernels' ex2.approx.ftz returns 0
+  below the smallest normal float (2^-126, which bf16 shares), so an element whose exact value
+  is below 2^-126 |coef| may come back as 0; 2^-120 covers |coef| <= 64 and is far below any
+  element that does not underflow.
+  At the target element, where coef * (p_y - 1) cancels when p_y is near 1, a further
   1e-5 * |coef| (coef = m * A * r * g * scale: float32 rounding of p_y is relative to 1).
+  With the entropy bonus, element v also carries ent * scale * p_v (z_v - E_p z), whose float32
+  difference is exact only to ~2^-23 |z|: a further 1e-5 * p_v * sum_u |dz_u| (relative to the
+  element's own probability, so a wrong small element still fails).
 Tokens whose float64 ratio lies within 1e-4 (relative) of a clip bound are ambiguous (float32
 and float64 may take the clip decision differently); their dlogits row must equal the
 oracle's row for one of the two decisions.
@@ -23,8 +31,10 @@ from oracle import advantage as OA
 from oracle import loss as OL
 from oracle import planner as OP
 
-DLOGIT_TOL = {"bf16": (1e-2, 1e-6), "f32": (2e-5, 0.0)}
+DLOGIT_REL = {"bf16": 1e-2, "f32": 2e-5}
+UNDERFLOW_FLOOR = 2.0 ** -120
 TARGET_COEF_TOL = 1e-5
+ENTROPY_MASS_TOL = 1e-5
 
 
 def oracle_logp(logits_host: np.ndarray, target: np.ndarray, mask: np.ndarray) -> np.ndarray:
@@ -104,14 +114,27 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def _bad(got, ref, dtype, target, coef):
-    rt, at = DLOGIT_TOL[dtype]
-    rowmax = np.max(np.abs(ref), axis=1, keepdims=True)
-    tol = rt * np.abs(ref) + at * rowmax + 1e-30
-    if target is not None:
+def row_probs(logits_host: np.ndarray) -> np.ndarray:
+    """Softmax of every row (float64), from the oracle's log-softmax."""
+    return np.stack([np.exp(OL.log_softmax_row(OL.as_f64(r))) for r in logits_host])
+
+
+def dlogits_tol(ref, dtype, target=None, coef=None, probs=None, rel=None):
+    """Elementwise dlogits bar (see the module docstring): `rel` (default by output dtype)
+    times each element's own magnitude, the underflow floor, the target-element term when
+    `target` and `coef` are given, and the entropy term when `probs` (row softmax) is given."""
+    r = DLOGIT_REL[dtype] if rel is None else rel
+    tol = r * np.abs(ref) + UNDERFLOW_FLOOR
+    if target is not None and coef is not None:
         rows = np.arange(ref.shape[0])
         tol[rows, target] += TARGET_COEF_TOL * np.abs(coef)
-    return np.abs(got - ref) > tol
+    if probs is not None:
+        tol += ENTROPY_MASS_TOL * probs * np.sum(np.abs(ref), axis=1, keepdims=True)
+    return tol
+
+
+def _bad(got, ref, dtype, target, coef):
+    return np.abs(got - ref) > dlogits_tol(ref, dtype, target, coef)
 
 
 def assert_dlogits_close(got: np.ndarray, ref: np.ndarray, dtype: str, ok_rows=None, alt=None,

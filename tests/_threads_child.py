@@ -100,7 +100,7 @@ class HostCase(RowCase):
 
 
 class LmCase:
-    def __init__(self, k, stored):
+    def __init__(self, k):
         T, V, H = 384, 40000, 512
         wl = W.make_workload("lmhead", seed=950 + k, rows=4, tokens=T, V=V, H=H)
         self.h, self.W = W.make_lmhead_inputs(wl, DEV)
@@ -109,8 +109,7 @@ class LmCase:
         self.target, self.mask = t(wl.target), t(wl.mask)
         self.adv = t(rng.normal(0.0, 1.0, T).astype(np.float32))
         self.T, self.V, self.H = T, V, H
-        size = (_lib.grpo_lmhead_workspace_size_stored if stored else _lib.grpo_lmhead_workspace_size)(T, V, H)
-        self.ws_bytes = size
+        self.ws_bytes = _lib.grpo_lmhead_workspace_size(T, V, H)
 
     def outputs(self):
         T, V, H = self.T, self.V, self.H
@@ -139,8 +138,8 @@ def main():
         RowCase(6, big, "f32", True, dict(kl_kind=_lib.KL_K1, kl_coef=0.05, ent_coef=0.01, w_tok=True)),
         RowCase(7, 1000, "bf16", True, None),  # short rows: the L2 kernel
         RowCase(8, 4104, "f32", True, dict(ent_coef=0.01)),
-        LmCase(9, stored=False),
-        LmCase(10, stored=True),
+        LmCase(9),
+        LmCase(10),
         HostCase(11),  # logits in pinned host memory, streamed through a staging buffer
     ]
     streams = [torch.cuda.Stream(DEV) for _ in range(N_THREADS)]
