@@ -28,6 +28,17 @@
  *     shared-memory size has set the kernels' attributes).
  *   - Determinism: results depend only on the inputs, never on the chunking, the launch
  *     shape or the scheduling (no order-dependent floating-point atomics).
+ *   - Environment switches (read on every call; for A/B comparison and tests; none changes a
+ *     result bit, each only selects another instance of the same computation):
+ *       GRPO_ROWPASS=c3|c4|l2     row pass: pin the 3- or 4-CTA cluster instance (bf16, where it
+ *                                 fits) or the L2-streaming instance instead of the default
+ *                                 2-CTA cluster;
+ *       GRPO_ROWPASS_SLOTS=n      row pass: n shared-memory slices per CTA (0 = one fixed buffer
+ *                                 per slice) where they fit, instead of as many as fit;
+ *       GRPO_ROWPASS_FWD=0        forward-only calls take the general cluster kernel instead of
+ *                                 the streaming forward kernel;
+ *       GRPO_LMHEAD_CTA_GROUP=1   fused LM-head: one-CTA 128 x 256 tiles instead of paired
+ *                                 2-CTA 256 x 256 tiles.
  */
 #ifndef GRPO_H_
 #define GRPO_H_
