@@ -460,6 +460,13 @@ GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H);
  *  target, old_logp (or NULL), adv_tok, mask   device, indexed by token row
  *  grad_scale 1/max(N,1) (or 1 with a deferred finish on d_h / dW)
  *  d_h        device float [T, H] or NULL; dW device float [V, H] or NULL (both NULL: forward only)
+ *  flags      0: dW = dlogits^T h of this call's tokens; GRPO_LMHEAD_DW_ACCUMULATE: dW += it, so
+ *             the micro-batches of one optimizer step (one call each, grad_scale the step's
+ *             1/max(N,1), or 1 with a deferred finish over d_h and dW) sum into one dW, each
+ *             call's float32 product added in call order ("Sizing mini-batches and
+ *             micro-batches", "The hard part: deferred normalization": the chunks' gradients
+ *             sum to the un-chunked step's). d_h rows and per-token outputs never accumulate.
+ *             Other bits: GRPO_ERR_INVALID.
  *  loss_tok, logp_tok (or NULL)  device float [T]
  *  acc        device grpo_step_acc (counts as in grpo_logprob_loss_fwd_bwd)
  *  workspace  device, 256-byte aligned, >= grpo_lmhead_workspace_size(T, V, H) bytes,
@@ -469,12 +476,14 @@ GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H);
  * 256 x 256 tiles (same results; kept for comparison).
  * Errors: GRPO_ERR_INVALID (sizes, NULL, alignment), GRPO_ERR_CAPACITY (workspace too small),
  * GRPO_ERR_UNSUPPORTED (tensor-map creation), GRPO_ERR_CUDA. */
+#define GRPO_LMHEAD_DW_ACCUMULATE 1u /* flags: dW += dlogits^T h (the call's tokens added to dW) */
+
 GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, int64_t T, int64_t V, int64_t H,
                                       const int32_t* target, const float* old_logp,
                                       const float* adv_tok, const uint8_t* mask, float clip_eps,
-                                      float grad_scale, float* d_h, float* dW, float* loss_tok,
-                                      float* logp_tok, grpo_step_acc* acc, void* workspace,
-                                      size_t workspace_bytes, void* stream);
+                                      float grad_scale, float* d_h, float* dW, uint32_t flags,
+                                      float* loss_tok, float* logp_tok, grpo_step_acc* acc,
+                                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* Allocation-free forward pass of the fused LM-head variant. The pages have no counterpart:
  * this entry point exists for callers that cannot allocate device memory when they need the

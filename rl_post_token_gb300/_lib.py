@@ -135,7 +135,7 @@ def _lib() -> C.CDLL:
     lib.grpo_lmhead_workspace_size.argtypes = [C.c_int64, C.c_int64, C.c_int64]
     lib.grpo_lmhead_workspace_size.restype = C.c_size_t
     lib.grpo_lmhead_loss_fwd_bwd.argtypes = [vp, vp, C.c_int64, C.c_int64, C.c_int64, vp, vp, vp, vp, C.c_float,
-                                             C.c_float, vp, vp, vp, vp, vp, vp, C.c_size_t, vp]
+                                             C.c_float, vp, vp, C.c_uint32, vp, vp, vp, vp, C.c_size_t, vp]
     lib.grpo_lmhead_loss_fwd_bwd.restype = C.c_int
     lib.grpo_lmhead_forward_noalloc.argtypes = [vp, vp, C.c_int64, C.c_int64, C.c_int64, vp, vp, vp, vp,
                                                 C.c_float, C.c_float, vp, vp, vp, vp]
@@ -444,14 +444,20 @@ def grpo_lmhead_workspace_size(T: int, V: int, H: int) -> int:
     return int(_lib().grpo_lmhead_workspace_size(T, V, H))
 
 
+LMHEAD_DW_ACCUMULATE = 1
+
+
 def grpo_lmhead_loss_fwd_bwd(h, W, target, old_logp, adv_tok, mask, clip_eps: float, grad_scale: float,
-                             d_h, dW, loss_tok, logp_tok, acc, workspace, stream=None) -> None:
-    """h [T, H] and W [V, H] bf16 device tensors; d_h / dW float32 or None; see grpo.h."""
+                             d_h, dW, loss_tok, logp_tok, acc, workspace, stream=None,
+                             dw_accumulate: bool = False) -> None:
+    """h [T, H] and W [V, H] bf16 device tensors; d_h / dW float32 or None; dw_accumulate adds
+    this call's dW to the buffer instead of overwriting it; see grpo.h."""
     T, H = h.shape
     V = W.shape[0]
     rc = _lib().grpo_lmhead_loss_fwd_bwd(_ptr(h), _ptr(W), T, V, H, _ptr(target), _ptr(old_logp),
                                          _ptr(adv_tok), _ptr(mask), float(clip_eps), float(grad_scale),
-                                         _ptr(d_h), _ptr(dW), _ptr(loss_tok), _ptr(logp_tok), _ptr(acc),
+                                         _ptr(d_h), _ptr(dW), LMHEAD_DW_ACCUMULATE if dw_accumulate else 0,
+                                         _ptr(loss_tok), _ptr(logp_tok), _ptr(acc),
                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
                                          _stream(stream))
     if rc != OK:

@@ -296,11 +296,12 @@ extern "C" GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int6
 extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, int64_t T, int64_t V, int64_t H,
                                                  const int32_t* target, const float* old_logp,
                                                  const float* adv_tok, const uint8_t* mask, float clip_eps,
-                                                 float grad_scale, float* d_h, float* dW, float* loss_tok,
-                                                 float* logp_tok, grpo_step_acc* acc, void* workspace,
-                                                 size_t workspace_bytes, void* stream) {
+                                                 float grad_scale, float* d_h, float* dW, uint32_t flags,
+                                                 float* loss_tok, float* logp_tok, grpo_step_acc* acc,
+                                                 void* workspace, size_t workspace_bytes, void* stream) {
   const int arc = check_args(h, W, T, V, H, target, adv_tok, mask, loss_tok, acc);
   if (arc != GRPO_OK || T == 0) return arc;
+  if (flags & ~(uint32_t)GRPO_LMHEAD_DW_ACCUMULATE) return GRPO_ERR_INVALID;
   if (!workspace || ((uintptr_t)workspace & 255u)) return GRPO_ERR_INVALID;
   const WsLayout ws = ws_layout(T, V);
   if (workspace_bytes < ws.total) return GRPO_ERR_CAPACITY;
@@ -358,7 +359,7 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
       b.m_fast = 0;  // consecutive units share the dz columns
       b.C = dW + v0 * H;
       b.ldc = H;
-      b.accumulate = 0;
+      b.accumulate = (flags & GRPO_LMHEAD_DW_ACCUMULATE) ? 1 : 0;
       b.acc = acc;
       rc = launch<EPI_STORE_F32, true, true>(cg, ma, mb, ma, b, st);
       if (rc != GRPO_OK) return rc;

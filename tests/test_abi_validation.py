@@ -85,13 +85,14 @@ def test_host_entry_argument_checks(kw, code):
     assert _host(**kw) == code
 
 
-def _lm(T=256, V=1024, H=128, h=P, W=P, ws=P, ws_bytes=1 << 30, acc=P, target=P):
+def _lm(T=256, V=1024, H=128, h=P, W=P, ws=P, ws_bytes=1 << 30, acc=P, target=P, flags=0):
     return _lib.lib().grpo_lmhead_loss_fwd_bwd(h, W, T, V, H, target, None, P, P, C.c_float(0.2),
-                                               C.c_float(1.0), P, P, P, None, acc, ws, ws_bytes, None)
+                                               C.c_float(1.0), P, P, flags, P, None, acc, ws, ws_bytes, None)
 
 
 @pytest.mark.parametrize("kw, code", [
     (dict(H=100), _lib.ERR_INVALID),  # H a multiple of 64
+    (dict(flags=2), _lib.ERR_INVALID),  # unknown flag bits
     (dict(H=32), _lib.ERR_INVALID),
     (dict(V=0), _lib.ERR_INVALID),
     (dict(T=-1), _lib.ERR_INVALID),

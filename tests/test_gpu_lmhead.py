@@ -212,3 +212,58 @@ def test_lmhead_tile_shapes_agree():
             del os.environ["GRPO_LMHEAD_CTA_GROUP"]
     for a, b in zip(outs[0][:4], outs[1][:4]):
         assert torch.equal(a, b)
+
+
+def _oracle_grad_tol(hb, wb, wl, mask, a_tok, old_logp, N):
+    """The oracle's d_h and dW for a case, and the elementwise bars of the module docstring."""
+    ref = OL.lmhead_fwd_bwd(hb, wb, wl.target, old_logp, a_tok, mask, wl.eps, scale=1.0 / N)
+    hf, wf = OL.as_f64(hb), OL.as_f64(wb)
+    z = hf @ wf.T
+    dz_abs = np.zeros_like(z)
+    for t in range(z.shape[0]):
+        if mask[t]:
+            dz_abs[t] = np.abs(OL.token_objective(z[t], int(wl.target[t]), None if old_logp is None else old_logp[t],
+                                                  a_tok[t], 1, wl.eps, 1.0 / N)[4])
+    return ref, 8e-3 * (dz_abs @ np.abs(wf)) + 1e-12, 8e-3 * (dz_abs.T @ np.abs(hf)) + 1e-12
+
+
+@pytest.mark.parametrize("deferred", [False, True])
+def test_lmhead_micro_batches_accumulate_dw(cta_group, deferred):
+    # one optimizer step as three micro-batches (token blocks of 128, 200 and 172: ragged tiles),
+    # one call each with dW accumulated ("Sizing mini-batches and micro-batches", "The hard part:
+    # deferred normalization"), at the step's grad scale 1/N or, deferred, at 1 with the finish
+    # scaling d_h and dW once. Per-token outputs and the step loss equal the one-call step's;
+    # d_h and dW (the sum of three float32 products) meet the oracle's bar.
+    T, V, Hd = 500, 3000, 128
+    wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed=31, valid_lo=0.1)
+    N = max(int(mask.sum()), 1)
+    one = _run(h, Wt, wl, mask, a_tok, old_logp, 1.0 / N)
+    res_one = _lib.grpo_finish_step(one[4], one[2], expected_N=int(mask.sum()))
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    d_h = torch.full((T, Hd), 7.0, device=DEV)
+    dW = torch.full((V, Hd), 7.0, device=DEV)
+    loss = torch.full((T,), -7.0, device=DEV)
+    logp = torch.full((T,), -7.0, device=DEV)
+    acc = _lib.new_step_acc(DEV)
+    bounds = [0, 128, 328, 500]
+    for k in range(3):
+        a, b = bounds[k], bounds[k + 1]
+        ws = torch.empty(_lib.grpo_lmhead_workspace_size(b - a, V, Hd), dtype=torch.uint8, device=DEV)
+        _lib.grpo_lmhead_loss_fwd_bwd(h[a:b], Wt, t(wl.target[a:b]), t(old_logp[a:b]), t(a_tok[a:b]), t(mask[a:b]),
+                                      wl.eps, 1.0 if deferred else 1.0 / N, d_h[a:b], dW, loss[a:b], logp[a:b],
+                                      acc, ws, dw_accumulate=k > 0)
+    res = _lib.grpo_finish_step(acc, loss, expected_N=int(mask.sum()), deferred=deferred, grad_bufs=[d_h, dW])
+    torch.cuda.synchronize()
+    assert res["status"] == 0 and res["kernel_flags"] == 0
+    for key in ("loss", "n_valid", "n_clipped", "n_tokens"):
+        assert res[key] == res_one[key], key
+    assert torch.equal(loss, one[2]) and torch.equal(logp, one[3])
+    if not deferred:
+        # a token's d_h row depends on that token alone: the same bits in any micro-batch
+        assert torch.equal(d_h, one[0])
+    ref, tol_h, tol_w = _oracle_grad_tol(hb, wb, wl, mask, a_tok, old_logp, N)
+    gh, gw = H.to_f64(d_h), H.to_f64(dW)
+    bad = np.abs(gh - ref["d_h"]) > tol_h
+    assert not bad.any(), (np.argwhere(bad)[:3], gh[bad][:3], ref["d_h"][bad][:3])
+    bad = np.abs(gw - ref["dW"]) > tol_w
+    assert not bad.any(), (np.argwhere(bad)[:3], gw[bad][:3], ref["dW"][bad][:3])
