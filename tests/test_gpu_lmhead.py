@@ -267,3 +267,57 @@ def test_lmhead_micro_batches_accumulate_dw(cta_group, deferred):
     assert not bad.any(), (np.argwhere(bad)[:3], gh[bad][:3], ref["d_h"][bad][:3])
     bad = np.abs(gw - ref["dW"]) > tol_w
     assert not bad.any(), (np.argwhere(bad)[:3], gw[bad][:3], ref["dW"][bad][:3])
+
+
+@pytest.mark.parametrize("T, V, Hd", [(1, 1, 64), (3, 300, 64), (129, 257, 64), (2, 40000, 64)])
+def test_lmhead_degenerate_sizes(cta_group, T, V, Hd):
+    # one token, a one-entry vocabulary (log p = 0, every dlogit 0), tiles that are one row or
+    # one column past a multiple of the tile, and a few tokens over several vocabulary chunks
+    _check(T, V, Hd, seed=40 + T)
+
+
+def test_lmhead_step_captured_in_a_cuda_graph_replays_bitwise():
+    # the LM-head step (one call with d_h and dW, then the finish) captured once into a CUDA
+    # graph: a replay gives the eager call's bits, and after new hidden states are written into
+    # the same buffer the replay gives what an eager call on them gives
+    T, V, Hd = 300, 5000, 128
+    wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed=51)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    tgt, old, adv, msk = t(wl.target), t(old_logp), t(a_tok), t(mask)
+    d_h = torch.empty((T, Hd), device=DEV)
+    dW = torch.empty((V, Hd), device=DEV)
+    loss, logp = torch.empty(T, device=DEV), torch.empty(T, device=DEV)
+    acc = _lib.new_step_acc(DEV)
+    ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=DEV)
+    N = int(mask.sum())
+
+    def step():
+        _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, tgt, old, adv, msk, wl.eps, 1.0 / max(N, 1), d_h, dW, loss, logp,
+                                      acc, ws)
+        _lib.grpo_finish_step(acc, loss, expected_N=N, sync=False)
+
+    def snapshot():
+        torch.cuda.synchronize()
+        return d_h.clone(), dW.clone(), loss.clone(), logp.clone(), acc[64:128].clone()
+
+    step()  # eager (sets the kernels' attributes before the capture)
+    eager = snapshot()
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(g, stream=cs):
+            step()
+    for _ in range(2):
+        d_h.fill_(7.0)
+        dW.fill_(7.0)
+        g.replay()
+        for a, b in zip(snapshot(), eager):
+            assert torch.equal(a, b)
+    h.copy_(torch.flip(h, dims=[0]))
+    g.replay()
+    replayed = snapshot()
+    step()
+    for a, b in zip(replayed, snapshot()):
+        assert torch.equal(a, b)
+    assert not torch.equal(replayed[0], eager[0])
