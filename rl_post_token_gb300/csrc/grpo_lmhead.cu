@@ -7,7 +7,7 @@
 //  pass A     tcgen05 GEMM over every (256-token x 256-vocabulary) tile; the epilogue reduces
 //             each token's tile to a log2-domain (shift, sum-exp) partial and picks up the
 //             target logit.
-//  reduce     per token: combine the partials in vocabulary order -> LSE, log-prob, ratio,
+//  reduce     per token: combine the partials in a fixed order -> LSE, log-prob, ratio,
 //             clipped surrogate, gradient coefficient (the row pass's token epilogue).
 //  backward   per vocabulary chunk c (at most 66 tiles, 16896 columns): the same GEMM recomputes
 //             the chunk's logits and its epilogue writes the chunk's bf16 dlogits dz_c into a
@@ -30,30 +30,47 @@
 namespace grpo {
 namespace lmhead {
 
-// Per token: combine the vocabulary-tile partials in order, then the token epilogue.
-__global__ void reduce_kernel(int64_t T, int n_col_tiles, const float* __restrict__ part_m,
-                              const float* __restrict__ part_s, const float* __restrict__ zy,
-                              const int32_t* __restrict__ target, int64_t V, const float* old_logp,
-                              const float* __restrict__ adv, const uint8_t* __restrict__ mask, float eps,
-                              float scale, float* __restrict__ lse2_out, float* __restrict__ coef_out,
-                              float* loss_tok, float* logp_tok, grpo_step_acc* acc) {
+// Per token: combine the vocabulary-tile partials, then the token epilogue. A block takes 32
+// tokens (lane = token, so every partial load is one coalesced 128-byte line) and its 8 warps
+// split the tiles: warp w folds tiles w, w + 8, ... in order; warp 0 then folds the 8 warp
+// partials in warp order. The order depends only on the tile count.
+constexpr int kReduceWarps = 8;
+
+__global__ void __launch_bounds__(kReduceWarps * 32)
+reduce_kernel(int64_t T, int n_col_tiles, const float* __restrict__ part_m, const float* __restrict__ part_s,
+              const float* __restrict__ zy, const int32_t* __restrict__ target, int64_t V, const float* old_logp,
+              const float* __restrict__ adv, const uint8_t* __restrict__ mask, float eps, float scale,
+              float* __restrict__ lse2_out, float* __restrict__ coef_out, float* loss_tok, float* logp_tok,
+              grpo_step_acc* acc) {
+  __shared__ float wm[kReduceWarps][32], ws[kReduceWarps][32];
   __shared__ unsigned long long sc[4];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   if (threadIdx.x < 4) sc[threadIdx.x] = 0;
+  const int64_t row = (int64_t)blockIdx.x * 32 + lane;
+  const bool live = row < T && mask[row] != 0;
+  MS t{-INFINITY, 0.f};
+  if (live) {
+#pragma unroll 4
+    for (int c = w; c < n_col_tiles; c += kReduceWarps)
+      t = ms2_combine(t, MS{part_m[(int64_t)c * T + row], part_s[(int64_t)c * T + row]});
+  }
+  wm[w][lane] = t.m;
+  ws[w][lane] = t.s;
   __syncthreads();
-  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   unsigned long long v_valid = 0, v_clip = 0, v_nf = 0, v_tok = 0;
-  if (row < T) {
+  if (w == 0 && row < T) {
     v_tok = 1;
     float coef = 0.f, l2 = 0.f;
-    if (mask[row]) {
-      MS t{-INFINITY, 0.f};
-      for (int c = 0; c < n_col_tiles; ++c) t = ms2_combine(t, MS{part_m[(int64_t)c * T + row], part_s[(int64_t)c * T + row]});
-      const float l2s = log2f(t.s);
-      l2 = t.m + l2s;
+    if (live) {
+      MS tot{wm[0][lane], ws[0][lane]};
+#pragma unroll
+      for (int k = 1; k < kReduceWarps; ++k) tot = ms2_combine(tot, MS{wm[k][lane], ws[k][lane]});
+      const float l2s = log2f(tot.s);
+      l2 = tot.m + l2s;
       const int32_t y = target[row];
       const float z = (y >= 0 && (int64_t)y < V) ? zy[row] : __int_as_float(0x7fc00000);
       // log2 p_y = (z_y log2e - m) - log2(sum), without cancellation
-      const TokenOut o = token_epilogue((fmaf(z, kLog2e, -t.m) - l2s) * kLn2, fabsf(l2) <= kLseMax * kLog2e,
+      const TokenOut o = token_epilogue((fmaf(z, kLog2e, -tot.m) - l2s) * kLn2, fabsf(l2) <= kLseMax * kLog2e,
                                         old_logp != nullptr, old_logp ? old_logp[row] : 0.f, adv[row], eps, scale);
       loss_tok[row] = o.loss;
       if (logp_tok) logp_tok[row] = o.logp;
@@ -279,9 +296,9 @@ int forward(int cg, const void* h, const void* W, int64_t T, int64_t V, int64_t 
   g.n_n = ws.n_col_tiles;
   const int rc = logits_gemm<EPI_PARTIALS>(cg, h, W, T, V, H, g, st);
   if (rc != GRPO_OK) return rc;
-  reduce_kernel<<<(unsigned)((T + 255) / 256), 256, 0, st>>>(T, ws.n_col_tiles, sc.part_m, sc.part_s, sc.zy,
-                                                              target, V, old_logp, adv_tok, mask, clip_eps,
-                                                              grad_scale, sc.lse2, sc.coef, loss_tok, logp_tok, acc);
+  reduce_kernel<<<(unsigned)((T + 31) / 32), kReduceWarps * 32, 0, st>>>(
+      T, ws.n_col_tiles, sc.part_m, sc.part_s, sc.zy, target, V, old_logp, adv_tok, mask, clip_eps, grad_scale,
+      sc.lse2, sc.coef, loss_tok, logp_tok, acc);
   GRPO_CUDA_TRY(cudaGetLastError());
   return GRPO_OK;
 }
