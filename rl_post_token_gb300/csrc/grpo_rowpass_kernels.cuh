@@ -993,7 +993,10 @@ __global__ void __launch_bounds__(fwd_block_threads(NCW), 1) row_fwd_kernel(RowA
       const float zy = wown ? __shfl_sync(0xffffffffu, zyl, cty & 31) : 0.f;
       if (lane == 0) {
         const uint32_t b = xi % kFwdBufs, u = xi / kFwdBufs;
-        if (u > 0) mbar_wait_cluster_bounded(&xempty[b], (u - 1u) & 1u, s_abort);
+        // the buffer is free once the combiner's arrive completed this phase. The signal
+        // publishes no data (the combiner had consumed what it read from the buffer before
+        // arriving), so the wait needs no cluster-scope acquire; one cost the ahead pass 5%.
+        if (u > 0) mbar_wait_bounded(&xempty[b], (u - 1u) & 1u, s_abort);
         const uint32_t bar = mapa_u32(smem_u32(&xfull[b]), 0u);
         st_async_v2f32(mapa_u32(smem_u32(part + 2 * (b * NP + rank * NCW + cw)), 0u), w.m, w.s, bar);
         if (wown) st_async_f32(mapa_u32(smem_u32(zyv + b), 0u), zy, bar);
@@ -1021,9 +1024,12 @@ __global__ void __launch_bounds__(fwd_block_threads(NCW), 1) row_fwd_kernel(RowA
       const bool ybad = tm.y < 0 || (int64_t)tm.y >= V;
       // the phase completes once every warp's partial (and the target logit) has landed.
       // Phase u-1 is complete: this warp waited for it four read rows ago, and no store of
-      // this row is issued before the buffer's release that followed that wait.
+      // this row is issued before the buffer's release that followed that wait. The partials
+      // come by st.async, whose bytes the phase's transaction count tracks: observing the
+      // phase complete makes them visible, as for a bulk copy into this CTA, so the wait is
+      // the CTA-scope one (a cluster-scope acquire here cost the ahead pass another 4%).
       if (lane == 0) mbar_arrive_expect_tx_relaxed(&xfull[b], NP * 8u + (ybad ? 0u : 4u));
-      mbar_wait_cluster_bounded(&xfull[b], u & 1u, s_abort);
+      mbar_wait_bounded(&xfull[b], u & 1u, s_abort);
       // each CTA's NCW partials by the general kernel's pairwise tree (32 / NCW CTAs at a time,
       // one per NCW-lane group), then the CTAs in rank order
       constexpr int G = 32 / NCW;
