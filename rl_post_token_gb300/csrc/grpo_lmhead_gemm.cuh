@@ -421,7 +421,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
   const int first = CG == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int stride = CG == 2 ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   const int KB = (int)((g.K + BK - 1) / BK);
-  uint32_t issued = 0;  // producer: stage loads issued by this CTA
 
   if (warp == 0) {
     // ---- TMA producer: this CTA's A rows and B rows of every stage ----
@@ -433,20 +432,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
         unit_coords(g, t, mu, nu);
         const int a_row = mu * BM * CG + (int)rank * BM;
         const int b_row = (g.col_tile0 + nu) * BN + (int)rank * S::B_ROWS;
-        if (*s_abort) break;  // a wait gave up: issue nothing more
         for (int kb = 0; kb < KB; ++kb) {
-          mbar_wait_bounded(&empty[stage], phase ^ 1u, s_abort);
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, s_abort)) break;
           if (rank == 0) mbar_arrive_expect_tx(&full[stage], CG * S::STAGE_BYTES);
           const uint32_t sa = sbase + stage * S::STAGE_BYTES;
           const uint32_t bar = full0 + stage * 8u;
           load_operand<CG, A_MN, BM>(sa, &map_a, bar, kb * BK, a_row);
           load_operand<CG, B_MN, S::B_ROWS>(sa + S::A_BYTES, &map_b, bar, kb * BK, b_row);
-          ++issued;
           if (++stage == S::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
+        if (*s_abort) break;  // a wait gave up: issue nothing more
       }
       // every stage's last release has arrived before this CTA may leave: the MMAs that read
       // this CTA's shared memory are complete and no commit still targets its barriers
@@ -466,15 +464,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
     if (lane == 0 && rank == 0) {
       uint32_t stage = 0, phase = 0, ab = 0, aphase = 0;
       for (int t = first; t < n_units; t += stride) {
-        if (*s_abort) break;
-        if (CG == 2)
-          mbar_wait_cluster_bounded(&tempty[ab], aphase ^ 1u, s_abort);
-        else
-          mbar_wait_bounded(&tempty[ab], aphase ^ 1u, s_abort);
+        // the even CTA waits for both CTAs' epilogues to have read the accumulator (their
+        // arrives release the TMEM reads at cluster scope)
+        const bool free_acc = CG == 2 ? mbar_wait_cluster_bounded(&tempty[ab], aphase ^ 1u, s_abort)
+                                      : mbar_wait_bounded(&tempty[ab], aphase ^ 1u, s_abort);
+        if (!free_acc) break;
         fence_after();
         const uint32_t d = tmem + ab * BN;
         for (int kb = 0; kb < KB; ++kb) {
-          mbar_wait_bounded(&full[stage], phase, s_abort);
+          if (!mbar_wait_bounded(&full[stage], phase, s_abort)) break;
           fence_after();
           const uint32_t sa = sbase + stage * S::STAGE_BYTES;
           const uint64_t da = sdesc<A_MN>(sa), db = sdesc<B_MN>(sa + S::A_BYTES);
@@ -489,6 +487,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             phase ^= 1u;
           }
         }
+        if (*s_abort) break;  // the epilogues' waits give up on their own
         const uint32_t fb = smem_u32(&tfull[ab]);
         mma_commit<CG>(fb);
         if (CG == 2) mma_commit<CG>(mapa_u32(fb, 1));
