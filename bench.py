@@ -31,6 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GRPO loss fwd+bwd valid tokens/s at V=151936 bf16; % of HBM roofline"
+LMHEAD_METRIC = "GRPO loss fwd+bwd valid tokens/s, fused LM-head (V=151936, H=2048, bf16)"
 UNIT = "valid tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 # device code of the row-pass kernel (the profile records the combined hash of these files)
@@ -236,12 +237,34 @@ def _blas_threads() -> int:
     return os.cpu_count() or 1
 
 
+def lmhead_config(wl) -> dict:
+    """The `config` of an LM-head line: the same dict in the library arm and the reference arm."""
+    T, V, Hd = wl.T, wl.V, wl.extra["H"]
+    return {"workload": WORKLOAD_TEXT["lmhead"], "tokens": int(T), "vocab": int(V), "hidden": int(Hd),
+            "backward": "logits recomputed per vocabulary chunk (%d chunks), no [T, V] matrix stored"
+                        % lmhead_chunks(V),
+            "l2": "weights 622 MB + hidden 64 MB read per step, larger than L2; no flush"}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
+    from oracle import planner as OP
     from rl_post_token_gb300 import workloads as W
-    wl = W.make_workload(args.workload, seed=0)
+    ov = {"rows": args.rows} if args.rows else {}
+    if args.rows and args.workload == "qwen_step":
+        ov.update(mini=args.rows, micro=args.rows)
+    if args.workload == "lmhead" and args.lm_tokens:
+        ov = {"tokens": args.lm_tokens}
+    wl = W.make_workload(args.workload, seed=0, **ov)
+    if args.workload == "lmhead":
+        config = lmhead_config(wl)
+    else:
+        # the same config as the library arm's line; the exec rows from the oracle's planner
+        pl = OP.plan(OP.PlanConfig(**wl.plan), wl.row_len, wl.row_valid, seg_counts=wl.seg_counts)
+        exec_tokens = int(sum(int(wl.row_len[j]) for j in pl.row_src))
+        config = workload_config(args, wl, exec_tokens, world, args.workload)
     per_step_s = 0.5
     if args.workload == "lmhead":
         # one call of the LM-head oracle on 4 tokens per step (its products use every BLAS thread)
@@ -262,13 +285,13 @@ def run_reference(args):
         dt += d
     v = done / dt
     line = {
-        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": LMHEAD_METRIC if args.workload == "lmhead" else METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / max(args.steps, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "parallelism": "rank 0 only"},
+        "config": config,
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "host_cpus": os.cpu_count(), "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample + (" (rank 0 only)" if world > 1 else "")},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -481,13 +504,11 @@ def measure_lmhead(args, device, rank=0, local=0, with_e2e=True, with_cpu=True):
     flops = 6.0 * T * V * Hd
     peak, kind = bf16_peak(sustained=True)
     line = {
-        "metric": "GRPO loss fwd+bwd valid tokens/s, fused LM-head (V=151936, H=2048, bf16)",
+        "metric": LMHEAD_METRIC,
         "value": N / full_s, "unit": UNIT, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": 1e3 * full_s, "dtype": "bf16",
-        "config": {"workload": WORKLOAD_TEXT["lmhead"], "tokens": T, "vocab": V, "hidden": Hd,
-                   "backward": "logits recomputed per vocabulary chunk (%d chunks), no [T, V] matrix stored "
-                               "(workspace %.2f GB)" % (lmhead_chunks(V), ws.numel() / 1e9),
-                   "l2": "weights 622 MB + hidden 64 MB read per step, larger than L2; no flush"},
+        "config": lmhead_config(wl),
+        "workspace_gb": ws.numel() / 1e9,
         "roofline": {"bound": "tensor", "achieved": flops / call_s / 1e12, "peak": peak, "unit": "TFLOP/s",
                      "frac": flops / call_s / 1e12 / peak, "peak_source": f"{kind} bf16_tflops_sustained",
                      "kernel": "grpo_lmhead_loss_fwd_bwd (its GEMM launches and the per-token reduce), CUDA events "
@@ -615,6 +636,17 @@ def time_rowpass(args, batch, device, stream, world, local, clocks_name):
             "results": S.read_results(batch.accs, batch.bp.n_steps)}
 
 
+def workload_config(args, wl, exec_tokens: int, world: int, workload: str, terms_text: str = "") -> dict:
+    """The `config` of a row-pass line: the same dict in the library arm and the reference arm."""
+    return {"workload": WORKLOAD_TEXT[workload] + (f" [rows overridden: {args.rows}]" if args.rows else "")
+                        + (f" [loss terms: {terms_text}]" if terms_text else ""),
+            "valid_tokens_per_step": int(wl.n_valid),
+            "logits_rows_per_step": int(exec_tokens), "vocab": int(wl.V),
+            "l2": "inputs larger than L2 (%.1f GB of logits per step), no flush"
+                  % (exec_tokens * wl.V * wl.elem_bytes / 1e9),
+            "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"}
+
+
 def rowpass_entry(args, wl, batch, tm, world, device, workload, traffic_per_valid=None, terms_text=""):
     """The JSON record of one row-pass workload: whole-job valid tokens/s, the row pass's
     roofline (algorithmic bytes per launch over its average launch time), clocks, results."""
@@ -626,13 +658,7 @@ def rowpass_entry(args, wl, batch, tm, world, device, workload, traffic_per_vali
         "metric": METRIC, "value": all_units / max_el, "unit": UNIT, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": 1e3 * max_el / args.steps,
         "dtype": "bf16" if wl.dtype == "bf16" else "f32",
-        "config": {"workload": WORKLOAD_TEXT[workload] + (f" [rows overridden: {args.rows}]" if args.rows else "")
-                               + (f" [loss terms: {terms_text}]" if terms_text else ""),
-                   "valid_tokens_per_step": wl.n_valid,
-                   "logits_rows_per_step": batch.bp.exec_tokens, "vocab": wl.V,
-                   "l2": "inputs larger than L2 (%.1f GB of logits per step), no flush"
-                         % (batch.bp.exec_tokens * wl.V * wl.elem_bytes / 1e9),
-                   "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
+        "config": workload_config(args, wl, batch.bp.exec_tokens, world, workload, terms_text),
         "roofline": {"bound": "hbm", "achieved": tm["achieved_gbs"], "peak": peak, "unit": "GB/s",
                      "frac": tm["achieved_gbs"] / peak, "peak_source": f"{peak_kind} hbm_gbs",
                      "frac_of_8tbs": tm["achieved_gbs"] / 8000.0,
