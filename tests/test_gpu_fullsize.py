@@ -141,3 +141,35 @@ def test_full_size_batch(name):
         v = valid_exec[a:a + 4096]
         assert torch.all(rs[v] <= 2e-2 * mag[v] + 1e-12)
         assert torch.all(mag[~v] == 0)
+
+
+@pytest.mark.parametrize("dtype, V", [("bf16", 151936), ("f32", 151936)])
+def test_forward_only_repeated_calls_give_the_training_pass_bits(dtype, V):
+    # The forward-only kernel's cross-CTA exchange (partials sent by asynchronous DSMEM stores,
+    # combined by one warp of the cluster's first CTA) against the training pass, 40 calls in a
+    # row at the product vocabulary: every call's loss and log-prob must be the training pass's
+    # bits, so a partial read before it landed, or a buffer reused while still being read,
+    # would show as a mismatch.
+    T = 1024 if dtype == "bf16" else 512
+    wl = W.make_workload("tiny", rows=8, positions=T // 8, valid_lo=0, V=V, dtype=dtype, seed=77, std=3.0)
+    case = H.Case(wl, old_mode="none")
+    lg = case.logits
+    adv = torch.from_numpy(np.random.default_rng(5).normal(0, 1, wl.T).astype(np.float32)).to(DEV)
+    old = torch.from_numpy(np.random.default_rng(6).normal(-12, 1, wl.T).astype(np.float32)).to(DEV)
+    dl = torch.empty_like(lg)
+    loss_t, logp_t = torch.empty(wl.T, device=DEV), torch.empty(wl.T, device=DEV)
+    _lib.grpo_logprob_loss_fwd_bwd(lg, case.d_target, old, adv, case.d_mask, wl.eps, 1.0, dl, loss_t, logp_t,
+                                   _lib.new_step_acc(DEV))
+    torch.cuda.synchronize()
+    loss_f, logp_f = torch.empty(wl.T, device=DEV), torch.empty(wl.T, device=DEV)
+    for k in range(40):
+        loss_f.fill_(7.0)
+        logp_f.fill_(7.0)
+        acc = _lib.new_step_acc(DEV)
+        _lib.grpo_logprob_loss_fwd_bwd(lg, case.d_target, old, adv, case.d_mask, wl.eps, 1.0, None, loss_f, logp_f,
+                                       acc)
+        torch.cuda.synchronize()
+        assert torch.equal(loss_f.view(torch.int32), loss_t.view(torch.int32)), k
+        assert torch.equal(logp_f.view(torch.int32), logp_t.view(torch.int32)), k
+        res = _lib.grpo_finish_step(acc, loss_f)
+        assert res["kernel_flags"] == 0 and res["n_valid"] == int(wl.mask.sum()), k
