@@ -313,6 +313,8 @@ class Batch:
         self.dev = device
         # a step's chunks alternate between the caller's stream and this one (None: one stream)
         self.side = None if os.environ.get("GRPO_ONE_STREAM") == "1" else torch.cuda.Stream(device)
+        # each optimizer step's finish on its own stream, beside the next step's chunks
+        self.fin = None if self.side is None else torch.cuda.Stream(device)
         self.bp = S.plan_batch(wl.plan, wl.row_len, wl.row_valid, wl.seg_counts)
         Te = self.bp.exec_tokens
         T = wl.T
@@ -379,6 +381,7 @@ class Batch:
         from rl_post_token_gb300 import step as S
         host = logits_host is not None
         return S.run_batch(self.bp, side_stream=None if host else self.side, logits=None if host else self.logits,
+                           finish_stream=None if host else self.fin,
                            logits_host=logits_host, staging=staging, copy_stream=copy_stream, block_rows=block_rows,
                            dlogits=self.dlogits if with_grad else None,
                            target=self.target, old_logp=self.old, mask=self.mask, adv_tok=self.adv_tok,

@@ -71,7 +71,7 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
               deferred: bool = False, V: Optional[int] = None, stream=None,
               chunk_ready=None, launch_events=None, agg: int = _lib.AGG_TOKEN_MEAN,
               w_tok=None, side_stream=None, terms: Optional[dict] = None, logits_host=None,
-              staging=None, block_rows: int = 1024, copy_stream=None) -> int:
+              staging=None, block_rows: int = 1024, copy_stream=None, finish_stream=None) -> int:
     """Enqueue the whole batch; returns the number of library kernel launches.
 
     ``accs`` is a uint8 device tensor of n_steps * 128 bytes (one accumulator per optimizer
@@ -96,7 +96,13 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
     between ``stream`` and these streams, so that the next chunk's blocks take the SMs the
     current chunk's last rows leave idle. Chunks of a step write disjoint rows and only add to
     the step's integer counters, so the results are the same bits; the step's finish waits for
-    every stream."""
+    every stream.
+
+    ``finish_stream`` (optional, with device logits): each optimizer step's finish runs on this
+    stream, after that step's chunks on every stream, while the next step's chunks go on; the
+    caller's stream waits for the last finish at the end. A finish reads only its own step's
+    per-token losses and accumulator (and, deferred, scales its own step's dlogits rows), so
+    the results are the same bits."""
     import torch
 
     # checks that need no device, made before anything is enqueued
@@ -109,6 +115,7 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
     st = torch.cuda.current_stream() if stream is None else stream
     sides = [] if side_stream is None else (list(side_stream) if isinstance(side_stream, (list, tuple))
                                             else [side_stream])
+    fs = finish_stream if logits_host is None else None
     rotation = [st] + sides
     launches = 0
     if rewards is not None:
@@ -128,9 +135,9 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
             launches += _host_step(bp, s, logits_host, staging, block_rows, copy_stream, st, dlogits, target,
                                    old_logp, adv_tok, mask, loss_tok, logp_tok, acc, clip_eps, scale, tok_src,
                                    w_tok, terms, V, launch_events)
-        else:
+        elif s == 0 or fs is None:
             for ss in sides:
-                ss.wait_stream(st)  # the advantage and the previous step's finish
+                ss.wait_stream(st)  # the advantage (and, without a finish stream, the previous finish)
         chunks = range(0) if logits_host is not None else range(p["step_chunk_off"][s], p["step_chunk_off"][s + 1])
         for i, c in enumerate(chunks):
             a, b = int(bp.exec_tok_off[c]), int(bp.exec_tok_off[c + 1])
@@ -169,7 +176,13 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
                 e1.record(cs)
                 launch_events.append((e0, e1))
             launches += 1
-        if logits_host is None:
+        fin = st
+        if fs is not None:
+            fs.wait_stream(st)  # this step's chunks on every stream
+            for ss in sides:
+                fs.wait_stream(ss)
+            fin = fs
+        elif logits_host is None:
             for ss in sides:
                 st.wait_stream(ss)
         t0, t1 = bp.step_tok_range[s]
@@ -177,12 +190,16 @@ def run_batch(bp: BatchPlan, *, logits, dlogits, target, old_logp, mask, adv_tok
         grads = [] if dlogits is None or e1 == e0 else [dlogits[e0:e1]]
         if plain:
             _lib.grpo_finish_step(acc, loss_tok[t0:t1], expected_N=N, deferred=deferred,
-                                  grad_bufs=grads, sync=False, stream=st)
+                                  grad_bufs=grads, sync=False, stream=fin)
         else:
             _lib.grpo_finish_step_ex(acc, loss_tok[t0:t1], None if w_tok is None else w_tok[t0:t1],
                                      divisor=D, expected_N=N, deferred=deferred, grad_bufs=grads,
-                                     sync=False, stream=st)
+                                     sync=False, stream=fin)
         launches += 1 + len(grads)
+    if fs is not None:
+        st.wait_stream(fs)
+        for ss in sides:
+            st.wait_stream(ss)
     return launches
 
 

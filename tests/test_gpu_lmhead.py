@@ -321,3 +321,30 @@ def test_lmhead_step_captured_in_a_cuda_graph_replays_bitwise():
     for a, b in zip(replayed, snapshot()):
         assert torch.equal(a, b)
     assert not torch.equal(replayed[0], eager[0])
+
+
+@pytest.mark.parametrize("deferred", [False, True])
+def test_lmhead_nonfinite_hidden_state_skips_the_step(deferred):
+    # a NaN planted in one token's hidden state (host-side fault injection): that token's
+    # logits, log-prob and loss are not finite, the finish reports the step skipped and zeroes
+    # the gradient buffers it is given (d_h and dW), and every other token's outputs still match
+    # the oracle
+    T, V, Hd = 200, 3000, 128
+    wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed=71)
+    bad = 37
+    mask[bad] = 1
+    h[bad, 5] = float("nan")
+    N = int(mask.sum())
+    d_h, dW, loss, logp, acc = _run(h, Wt, wl, mask, a_tok, old_logp, 1.0 if deferred else 1.0 / N)
+    res = _lib.grpo_finish_step(acc, loss, expected_N=N, deferred=deferred, grad_bufs=[d_h, dW])
+    assert res["status"] == _lib.STEP_SKIPPED_NONFINITE and res["n_nonfinite"] == 1
+    assert res["kernel_flags"] == 0 and res["n_valid"] == N
+    assert torch.count_nonzero(d_h) == 0 and torch.count_nonzero(dW) == 0
+    gl, gp = H.to_f64(loss), H.to_f64(logp)
+    assert not np.isfinite(gp[bad])
+    keep = np.ones(T, bool)
+    keep[bad] = False
+    hb2 = h.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = OL.lmhead_fwd_bwd(hb2[keep], wb, wl.target[keep], old_logp[keep], a_tok[keep], mask[keep], wl.eps,
+                            scale=1.0 / N, want_dw=False)
+    H.assert_tokens_close(gl[keep], gp[keep], ref, a_tok[keep], mask[keep])

@@ -776,21 +776,24 @@ def test_concurrent_host_threads_bitwise():
             assert torch.equal(loss, ref[i][1])
 
 
-def test_two_stream_chunks_bitwise():
-    # a step's chunks rotating over two or three streams (overlapping at their ends) give the
-    # same bits as one stream: dlogits, per-token losses and the step results
+@pytest.mark.parametrize("deferred", [False, True])
+def test_two_stream_chunks_bitwise(deferred):
+    # a step's chunks rotating over two or three streams (overlapping at their ends), and each
+    # step's finish on a stream of its own while the next step's chunks run, give the same bits
+    # as one stream: dlogits (in deferred mode scaled by the finish), per-token losses and the
+    # step results
     wl = W.make_workload("qwen_step", rows=8, len_lo=16, len_hi=40, V=32776, seed=27, mini=4, micro=1)
     case = H.Case(wl)
-    side = torch.cuda.Stream()
+    side, fin = torch.cuda.Stream(), torch.cuda.Stream()
     outs = []
-    for ss in (None, side, [side, torch.cuda.Stream()]):
+    for ss, fs in ((None, None), (side, None), ([side, torch.cuda.Stream()], None), (side, fin), (None, fin)):
         bp = S.plan_batch(wl.plan, wl.row_len, wl.row_valid)
         dl = torch.empty_like(case.logits)
         loss = torch.empty(wl.T, device=DEV)
         accs = torch.zeros(bp.n_steps * _lib.ACC_BYTES, dtype=torch.uint8, device=DEV)
         S.run_batch(bp, logits=case.logits, dlogits=dl, target=case.d_target, old_logp=case.d_old,
                     mask=case.d_mask, adv_tok=case.d_adv, loss_tok=loss, logp_tok=None, accs=accs,
-                    clip_eps=wl.eps, side_stream=ss)
+                    clip_eps=wl.eps, side_stream=ss, finish_stream=fs, deferred=deferred)
         torch.cuda.synchronize()
         outs.append((dl.view(torch.int16).clone(), loss.clone(), S.read_results(accs, bp.n_steps)))
     for o in outs[1:]:
