@@ -87,3 +87,18 @@ def test_lmhead_and_step_kernels_do_not_spill(grpo_lib):
         assert hits, (src, "no kernel found")
         for n in hits:
             assert k[n]["spill"] == 0, (n, k[n])
+
+
+def test_lmhead_gemm_instances_do_not_spill(grpo_lib):
+    # every instance of the LM-head GEMM template (CTA group 1 and 2; partials, dlogits and
+    # float32 epilogues with their operand layouts) and the per-token reduce: no spill and no
+    # stack frame (a local array indexed at run time would live in local memory)
+    k = _report("grpo_lmhead.cu")
+    gemm = [n for n in k if "lmhead11gemm_kernel" in n]
+    assert len(gemm) == 8, sorted(gemm)
+    for name in gemm + [n for n in k if "lmhead13reduce_kernel" in n]:
+        assert k[name]["spill"] == 0, (name, k[name])
+        assert k[name]["regs"] <= 255, (name, k[name])
+    stack = re.findall(r"Compiling entry function '(\S*gemm_kernel\S*)'.*?\n\s+(\d+) bytes stack frame",
+                       open(B.ptxas_report("grpo_lmhead.cu")).read(), flags=re.S)
+    assert stack and all(int(b) == 0 for _, b in stack), stack
