@@ -19,7 +19,8 @@
  *   - Ownership: every buffer belongs to the caller, and the library never frees caller
  *     memory. The library allocates no device memory of its own with one exception: the
  *     module's 16 MiB device array of grpo_lmhead_forward_noalloc, held by every GPU that
- *     loads the library.
+ *     loads the library. The LM-head backward keeps one stream and four events per device
+ *     (created on first use, kept until exit).
  *     "device" pointers are CUDA device memory of the current device; "host" pointers are
  *     ordinary host memory.
  *   - Asynchrony: device work is enqueued on `stream` (cudaStream_t passed as void*; NULL is
@@ -38,7 +39,9 @@
  *       GRPO_ROWPASS_FWD=0        forward-only calls take the general cluster kernel instead of
  *                                 the streaming forward kernel;
  *       GRPO_LMHEAD_CTA_GROUP=1   fused LM-head: one-CTA 128 x 256 tiles instead of paired
- *                                 2-CTA 256 x 256 tiles.
+ *                                 2-CTA 256 x 256 tiles;
+ *       GRPO_LMHEAD_OVERLAP=0     fused LM-head: the backward's launches all on the caller's
+ *                                 stream instead of two streams.
  */
 #ifndef GRPO_H_
 #define GRPO_H_
@@ -436,8 +439,8 @@ GRPO_API int grpo_window_rollup(const grpo_window* w, double* loss, int64_t* den
 
 /* Bytes of device workspace grpo_lmhead_loss_fwd_bwd needs for [T, H] hidden states and a
  * [V, H] output embedding: per-(token, 256-wide vocabulary tile) softmax partials (float32
- * shift and sum), per-token target logit, LSE and coefficient, and one bf16 dlogits chunk
- * buffer [T, 256 * chunk_tiles], where the ceil(V/256) vocabulary tiles are split into
+ * shift and sum), per-token target logit, LSE and coefficient, and two bf16 dlogits chunk
+ * buffers [T, 256 * chunk_tiles], where the ceil(V/256) vocabulary tiles are split into
  * ceil(tiles/66) chunks of equal width (V = 151936: 9 chunks of 66 tiles, 16896 columns).
  * Each part is rounded up to 256 bytes. 0 on bad sizes. */
 GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H);
@@ -450,9 +453,12 @@ GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H);
  *  - Forward: LSE, log-prob, ratio, clipped surrogate, per-token loss (as
  *    grpo_logprob_loss_fwd_bwd, one token per row of h).
  *  - Backward (d_h or dW non-NULL): per vocabulary chunk, the chunk's logits are recomputed
- *    and its bf16 dlogits written to the workspace chunk buffer; then d_h (+)= dlogits W_c,
- *    accumulated over the chunks in chunk order, and dW_c = dlogits^T h. The recompute makes
- *    the step 8 T V H flops (6 T V H without it).
+ *    and its bf16 dlogits written to one of the two workspace chunk buffers; then d_h (+)=
+ *    dlogits W_c, accumulated over the chunks in chunk order, and dW_c = dlogits^T h. The
+ *    recompute makes the step 8 T V H flops (6 T V H without it). d_h and dW run on a second
+ *    stream of the library's (one per device, created by the first call that needs it, which
+ *    should come before any stream capture), so the next chunk's recompute runs beside them;
+ *    the call's work on both streams is done when `stream` reaches the call's end.
  *  - Determinism: d_h and the per-token outputs of a token do not depend on which other
  *    tokens share the call; dW sums over the call's tokens in a fixed order.
  *  h          device bf16 [T, H] row-major, 16-byte aligned; H a multiple of 64
@@ -473,7 +479,7 @@ GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H);
  *             caller-owned; it holds all of the call's scratch, so calls may overlap (several
  *             streams, several host threads) as long as each has its own workspace and outputs
  * Environment: GRPO_LMHEAD_CTA_GROUP=1 selects one-CTA 128 x 256 tiles instead of the paired
- * 256 x 256 tiles (same results; kept for comparison).
+ * 256 x 256 tiles; GRPO_LMHEAD_OVERLAP=0 keeps every launch on `stream` (same results).
  * Errors: GRPO_ERR_INVALID (sizes, NULL, alignment), GRPO_ERR_CAPACITY (workspace too small),
  * GRPO_ERR_UNSUPPORTED (tensor-map creation), GRPO_ERR_CUDA. */
 #define GRPO_LMHEAD_DW_ACCUMULATE 1u /* flags: dW += dlogits^T h (the call's tokens added to dW) */

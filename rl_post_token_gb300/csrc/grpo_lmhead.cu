@@ -235,7 +235,7 @@ namespace {
 constexpr int kMaxChunkTiles = 66;
 
 struct WsLayout {
-  size_t part_m, part_s, zy, lse2, coef, dz, total;
+  size_t part_m, part_s, zy, lse2, coef, dz, dz2, total;  // dz, dz2: the two dlogits chunk buffers
   int n_col_tiles, chunk_tiles;
   int64_t vchunk;  // columns of the dlogits chunk buffer
 };
@@ -254,20 +254,22 @@ WsLayout ws_layout(int64_t T, int64_t V) {
   w.lse2 = off; off += up((size_t)T * 4);
   w.coef = off; off += up((size_t)T * 4);
   w.dz = off; off += up((size_t)T * w.vchunk * 2);
+  w.dz2 = off; off += up((size_t)T * w.vchunk * 2);
   w.total = off;
   return w;
 }
 
 struct Scratch {
   float *part_m, *part_s, *zy, *lse2, *coef;
-  __nv_bfloat16* dz;
+  __nv_bfloat16* dz[2];
 };
 
 Scratch carve(void* base, const WsLayout& ws) {
   uint8_t* b = static_cast<uint8_t*>(base);
   return {reinterpret_cast<float*>(b + ws.part_m), reinterpret_cast<float*>(b + ws.part_s),
           reinterpret_cast<float*>(b + ws.zy),     reinterpret_cast<float*>(b + ws.lse2),
-          reinterpret_cast<float*>(b + ws.coef),   reinterpret_cast<__nv_bfloat16*>(b + ws.dz)};
+          reinterpret_cast<float*>(b + ws.coef),
+          {reinterpret_cast<__nv_bfloat16*>(b + ws.dz), reinterpret_cast<__nv_bfloat16*>(b + ws.dz2)}};
 }
 
 int check_args(const void* h, const void* W, int64_t T, int64_t V, int64_t H, const int32_t* target,
@@ -303,6 +305,48 @@ int forward(int cg, const void* h, const void* W, int64_t T, int64_t V, int64_t 
   return GRPO_OK;
 }
 
+// The backward's second stream and its events, one set per device, created by the first call
+// that needs them (with the device current) and kept for the process lifetime. A call holds
+// `lock` while it enqueues its backward, so calls from several host threads never interleave
+// their records of these events; their work on the shared stream runs in enqueue order.
+struct Overlap {
+  cudaStream_t aux = nullptr;
+  cudaEvent_t dz_ready = nullptr, joined = nullptr, buf_free[2] = {nullptr, nullptr};
+};
+
+// Whether the next chunk's recompute may run beside this chunk's d_h and dW
+// (GRPO_LMHEAD_OVERLAP=0 keeps every launch on the caller's stream).
+bool overlap_on() {
+  const char* e = getenv("GRPO_LMHEAD_OVERLAP");
+  return !(e && e[0] == '0');
+}
+
+Overlap* overlap_state(std::unique_lock<std::mutex>& lock) {
+  static Overlap per_dev[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  lock = std::unique_lock<std::mutex>(mu);
+  Overlap& o = per_dev[dev];
+  if (!o.aux) {
+    Overlap n;
+    const unsigned ef = cudaEventDisableTiming;
+    if (cudaStreamCreateWithFlags(&n.aux, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&n.dz_ready, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&n.joined, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&n.buf_free[0], ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&n.buf_free[1], ef) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return nullptr;  // (what was created is kept until exit; the call falls back to one stream)
+    }
+    o = n;
+  }
+  return &o;
+}
+
 }  // namespace
 
 extern "C" GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H) {
@@ -329,17 +373,28 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
                    acc, ws, sc, st);
   if (rc != GRPO_OK || (!d_h && !dW)) return rc;
 
+  // Per vocabulary chunk c: the recompute writes the chunk's dlogits into buffer c % 2 on the
+  // caller's stream; d_h and dW read it on the second stream, so the next chunk's recompute
+  // runs beside them. d_h's launches stay in chunk order on one stream (its accumulation
+  // order), and a buffer is rewritten only after the launches reading it two chunks before.
+  const int n_chunks = (ws.n_col_tiles + ws.chunk_tiles - 1) / ws.chunk_tiles;
+  std::unique_lock<std::mutex> ov_lock;
+  Overlap* ov = (overlap_on() && n_chunks > 1) ? overlap_state(ov_lock) : nullptr;
+  const cudaStream_t bst = ov ? ov->aux : st;  // the stream of d_h and dW
   const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
+  auto backward = [&]() -> int {
   for (int ct0 = 0, c = 0; ct0 < ws.n_col_tiles; ct0 += ws.chunk_tiles, ++c) {
     const int nct = std::min(ws.chunk_tiles, ws.n_col_tiles - ct0);
     const int64_t v0 = (int64_t)ct0 * BN;
     const int64_t vc = std::min<int64_t>((int64_t)nct * BN, V - v0);
+    __nv_bfloat16* dzb = sc.dz[ov ? (c & 1) : 0];
+    if (ov && c >= 2) GRPO_CUDA_TRY(cudaStreamWaitEvent(st, ov->buf_free[c & 1], 0));
     // the chunk's dlogits, recomputed from its logits
     GemmArgs g{};
     g.target = target;
     g.lse2 = sc.lse2;
     g.coef = sc.coef;
-    g.dz = sc.dz;
+    g.dz = dzb;
     g.ldz = ws.vchunk;
     g.v0 = v0;
     g.acc = acc;
@@ -347,10 +402,14 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
     g.n_n = nct;
     rc = logits_gemm<EPI_DLOGITS>(cg, h, W, T, V, H, g, st, vc);
     if (rc != GRPO_OK) return rc;
+    if (ov) {
+      GRPO_CUDA_TRY(cudaEventRecord(ov->dz_ready, st));
+      GRPO_CUDA_TRY(cudaStreamWaitEvent(bst, ov->dz_ready, 0));
+    }
     CUtensorMap ma, mb;
     if (d_h) {
       // d_h[T, H] (+)= dz_c[T, vc] W_c[vc, H]
-      if (!map_k(&ma, sc.dz, T, vc, ws.vchunk, BM) || !map_mn(&mb, Wb + v0 * H, vc, H, H))
+      if (!map_k(&ma, dzb, T, vc, ws.vchunk, BM) || !map_mn(&mb, Wb + v0 * H, vc, H, H))
         return GRPO_ERR_UNSUPPORTED;
       GemmArgs b{};
       b.M = T;
@@ -362,12 +421,12 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
       b.ldc = H;
       b.accumulate = c > 0;
       b.acc = acc;
-      rc = launch<EPI_STORE_F32, false, true>(cg, ma, mb, ma, b, st);
+      rc = launch<EPI_STORE_F32, false, true>(cg, ma, mb, ma, b, bst);
       if (rc != GRPO_OK) return rc;
     }
     if (dW) {
       // dW_c[vc, H] = dz_c^T[vc, T] h[T, H]
-      if (!map_mn(&ma, sc.dz, T, vc, ws.vchunk) || !map_mn(&mb, h, T, H, H)) return GRPO_ERR_UNSUPPORTED;
+      if (!map_mn(&ma, dzb, T, vc, ws.vchunk) || !map_mn(&mb, h, T, H, H)) return GRPO_ERR_UNSUPPORTED;
       GemmArgs b{};
       b.M = vc;
       b.N = H;
@@ -378,11 +437,23 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
       b.ldc = H;
       b.accumulate = (flags & GRPO_LMHEAD_DW_ACCUMULATE) ? 1 : 0;
       b.acc = acc;
-      rc = launch<EPI_STORE_F32, true, true>(cg, ma, mb, ma, b, st);
+      rc = launch<EPI_STORE_F32, true, true>(cg, ma, mb, ma, b, bst);
       if (rc != GRPO_OK) return rc;
     }
+    if (ov) GRPO_CUDA_TRY(cudaEventRecord(ov->buf_free[c & 1], bst));
   }
   return GRPO_OK;
+  };
+  rc = backward();
+  if (ov) {  // the caller's stream continues after every launch of the call (also after an error)
+    const bool joined = cudaEventRecord(ov->joined, bst) == cudaSuccess &&
+                        cudaStreamWaitEvent(st, ov->joined, 0) == cudaSuccess;
+    if (!joined) {
+      (void)cudaGetLastError();
+      if (rc == GRPO_OK) rc = GRPO_ERR_CUDA;
+    }
+  }
+  return rc;
 }
 
 // ---- allocation-free forward entry point -----------------------------------------------------

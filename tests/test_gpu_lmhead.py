@@ -348,3 +348,23 @@ def test_lmhead_nonfinite_hidden_state_skips_the_step(deferred):
     ref = OL.lmhead_fwd_bwd(hb2[keep], wb, wl.target[keep], old_logp[keep], a_tok[keep], mask[keep], wl.eps,
                             scale=1.0 / N, want_dw=False)
     H.assert_tokens_close(gl[keep], gp[keep], ref, a_tok[keep], mask[keep])
+
+
+def test_lmhead_backward_overlap_gives_the_same_bits(monkeypatch):
+    # the backward's d_h and dW on the library's second stream beside the next chunk's
+    # recompute (two chunk buffers) against every launch on the caller's stream: the same bits
+    # for every output, over four vocabulary chunks, with dW accumulated into a second call's
+    T, V, Hd = 300, 60000, 128
+    wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed=81, valid_lo=0.2)
+    outs = []
+    for ov in ("0", "1"):
+        monkeypatch.setenv("GRPO_LMHEAD_OVERLAP", ov)
+        d_h, dW, loss, logp, acc = _run(h, Wt, wl, mask, a_tok, old_logp, 1.0 / max(int(mask.sum()), 1))
+        ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=DEV)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+        _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, t(wl.target), t(old_logp), t(a_tok), t(mask), wl.eps, 0.5, d_h, dW,
+                                      loss, logp, _lib.new_step_acc(DEV), ws, dw_accumulate=True)
+        torch.cuda.synchronize()
+        outs.append((d_h, dW, loss, logp))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
