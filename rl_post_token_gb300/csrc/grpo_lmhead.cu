@@ -11,10 +11,11 @@
 //             clipped surrogate, gradient coefficient (the row pass's token epilogue).
 //  backward   per vocabulary chunk c (at most 66 tiles, 16896 columns): the same GEMM recomputes
 //             the chunk's logits and its epilogue writes the chunk's bf16 dlogits dz_c into a
-//             bounded [T, chunk] buffer; then d_h (+)= dz_c W_c and dW_c = dz_c^T h, both on the
-//             same tcgen05 kernel with float32 outputs. d_h is accumulated over the chunks in
-//             chunk order (a fixed order: the result does not depend on how the tokens are
-//             split into calls).
+//             bounded [T, chunk] buffer (two buffers, used in turn); then d_h (+)= dz_c W_c and
+//             dW_c = dz_c^T h, both on the same tcgen05 kernel with float32 outputs, on a second
+//             stream so that the next chunk's recompute runs beside them. d_h is accumulated
+//             over the chunks in chunk order (a fixed order: the result does not depend on how
+//             the tokens are split into calls).
 //
 // All four contractions run on grpo::lmhead::gemm_kernel (grpo_lmhead_gemm.cuh): 2-CTA
 // clusters with paired tcgen05.mma (cta_group::2, 256 x 256 tiles), plain TMA tile loads.
