@@ -442,7 +442,7 @@ __device__ __forceinline__ void dz_vec(const uint4& u, uint4* dst, float cexp) {
       x[i + 1] = ex2(fmaf(x[i + 1], kLog2e, -cexp));
     }
   }
-  __stcs(dst, pack_vec<T, NEG>(x));
+  *dst = pack_vec<T, NEG>(x);  // a plain store: on this GPU faster than an evict-first one here
 }
 
 // The dlogits of one vector with the entropy term: 2^(z log2e - lse2) * (ea + eb z), rounded
@@ -465,7 +465,7 @@ __device__ __forceinline__ void dz_vec_ent(const uint4& u, uint4* dst, float lse
       x[i + 1] = q.y;
     }
   }
-  __stcs(dst, pack_vec<T, false>(x));
+  *dst = pack_vec<T, false>(x);
 }
 
 // The shared-memory ring: S slots of one chunk each. A CTA's chunks, in row order, take slots
@@ -644,7 +644,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
       if (!tm.valid) {
         // masked or padding row: nothing read, nothing exchanged; zero dlogits slice
         if (dz)
-          for (int v = ct; v < n_r / E; v += NC) __stcs(dz + v, zero);
+          for (int v = ct; v < n_r / E; v += NC) dz[v] = zero;
         if (rank == 0 && ct == 0) {
           cnt.tokens++;
           if (tm.idx >= 0) {
@@ -798,7 +798,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB) row_cluster_kernel(RowAr
         }
       } else {
         if (dz)
-          for (int v = ct; v < n_r / E; v += NC) __stcs(dz + v, zero);
+          for (int v = ct; v < n_r / E; v += NC) dz[v] = zero;
         __syncwarp();
         if (lane == 0) {
           RingCursor ce = rc;
