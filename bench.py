@@ -479,11 +479,14 @@ def measure_lmhead(args, device, rank=0, local=0, with_e2e=True, with_cpu=True):
 
     step(grads=False)  # pi_old by the ahead pass, then seeded noise
     old = logp + t(wl.old_noise)
+    torch.cuda.synchronize(device)
+    # the clock sampler first, then the warm-up steps right before the timed ones (no idle gap
+    # in which the power-capped GPU could recover before the timed region)
+    clocks = ClockSampler(_gpu_index(local), os.path.join(args.clocks_dir, f"clocks_lmhead_rank{rank}.csv"))
+    time.sleep(0.5)
     for _ in range(max(args.warmup, 3)):
         step(old=old)
     torch.cuda.synchronize(device)
-    clocks = ClockSampler(_gpu_index(local), os.path.join(args.clocks_dir, f"clocks_lmhead_rank{rank}.csv"))
-    time.sleep(0.5)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
@@ -610,12 +613,13 @@ def time_rowpass(args, batch, device, stream, world, local, clocks_name):
     import torch
     from rl_post_token_gb300 import step as S
 
+    # the clock sampler starts first (it takes a moment to come up), then the warm-up steps run
+    # right before the timed ones, so the GPU does not idle between the two
+    clocks = ClockSampler(_gpu_index(local), os.path.join(args.clocks_dir, clocks_name))
+    time.sleep(0.5)
     for _ in range(max(args.warmup, 3)):
         batch.replan(stream)
         batch.run(stream=stream)
-    torch.cuda.synchronize(device)
-    clocks = ClockSampler(_gpu_index(local), os.path.join(args.clocks_dir, clocks_name))
-    time.sleep(0.5)
     barrier(world, device)
     torch.cuda.synchronize(device)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
