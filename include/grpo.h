@@ -439,10 +439,12 @@ GRPO_API int grpo_window_rollup(const grpo_window* w, double* loss, int64_t* den
 
 /* Bytes of device workspace grpo_lmhead_loss_fwd_bwd needs for [T, H] hidden states and a
  * [V, H] output embedding: per-(token, 256-wide vocabulary tile) softmax partials (float32
- * shift and sum), per-token target logit, LSE and coefficient, and two bf16 dlogits chunk
+ * shift and sum), per-token target logit, LSE and coefficient, two bf16 dlogits chunk
  * buffers [T, 256 * chunk_tiles], where the ceil(V/256) vocabulary tiles are split into
- * ceil(tiles/66) chunks of equal width (V = 151936: 9 chunks of 66 tiles, 16896 columns).
- * Each part is rounded up to 256 bytes. 0 on bad sizes. */
+ * ceil(tiles/66) chunks of equal width (V = 151936: 9 chunks of 66 tiles, 16896 columns), and,
+ * for the entropy bonus of grpo_lmhead_loss_fwd_bwd_ex, a third float32 partial per tile and
+ * token and two float32 coefficients per token. Each part is rounded up to 256 bytes. 0 on bad
+ * sizes. */
 GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H);
 
 /* The same loss with the logits produced on the tensor cores: z = h W^T, computed tile by tile
@@ -490,6 +492,25 @@ GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, int64_t T, i
                                       float grad_scale, float* d_h, float* dW, uint32_t flags,
                                       float* loss_tok, float* logp_tok, grpo_step_acc* acc,
                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* grpo_lmhead_loss_fwd_bwd with the regularisers of grpo_loss_terms added to every valid
+ * token's loss and gradient, as grpo_logprob_loss_fwd_bwd_ex adds them to the row pass (terms
+ * NULL: identical to grpo_lmhead_loss_fwd_bwd). KL to the reference policy (k1 or k3) and the
+ * per-token weight w_tok act on each token's gradient coefficient. The entropy bonus (ent_coef,
+ * or an entropy_tok output) makes pass A carry sum e z per vocabulary tile as well, and, with
+ * ent_coef != 0, the backward's dlogits take the form p_v (a + b z_v) - coef [v == y]
+ * (b = ent_coef * grad_scale * w, a = coef - b E_p[z]), so the bonus's gradient reaches d_h and
+ * dW. loss_tok stays unweighted; entropy_tok (natural units) is written for every token,
+ * 0 for masked ones. Indices: ref_logp and w_tok as adv_tok, entropy_tok as loss_tok.
+ * Errors: those of grpo_lmhead_loss_fwd_bwd, and GRPO_ERR_INVALID for an unknown kl_kind, a KL
+ * term without ref_logp, or a non-finite coefficient. */
+GRPO_API int grpo_lmhead_loss_fwd_bwd_ex(const void* h, const void* W, int64_t T, int64_t V, int64_t H,
+                                         const int32_t* target, const float* old_logp,
+                                         const float* adv_tok, const uint8_t* mask, float clip_eps,
+                                         float grad_scale, float* d_h, float* dW, uint32_t flags,
+                                         float* loss_tok, float* logp_tok, const grpo_loss_terms* terms,
+                                         grpo_step_acc* acc, void* workspace, size_t workspace_bytes,
+                                         void* stream);
 
 /* Allocation-free forward pass of the fused LM-head variant. The pages have no counterpart:
  * this entry point exists for callers that cannot allocate device memory when they need the

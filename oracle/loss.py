@@ -179,21 +179,29 @@ def finish_step(loss_tok, mask, clipped=None):
     return res
 
 
-def lmhead_fwd_bwd(h, W, target, old_logp, adv_tok, mask, eps, scale=1.0, rows=None, want_dw=True):
+def lmhead_fwd_bwd(h, W, target, old_logp, adv_tok, mask, eps, scale=1.0, rows=None, want_dw=True, terms=None):
     """Fused LM-head variant: the same objective with the logits produced by z = h W^T.
 
     ``h`` [T, H] and ``W`` [V, H] are bfloat16 bit patterns (uint16) or floats. Computes, in
     float64, z = h W^T, then the token objective above, then the two backward products
     d_h = dz W and dW = dz^T h. ``rows`` restricts the work to a subset of tokens (d_h rows
-    and per-token outputs only; dW needs every token and is then skipped).
+    and per-token outputs only; dW needs every token and is then skipped). ``scale`` and
+    ``terms`` are those of ``loss_fwd_bwd`` (a per-token scale array, the regularisers; the
+    reference log-probs ``terms["ref"]`` indexed like the tokens).
     """
     hf = as_f64(h)
     Wf = as_f64(W)
     T = hf.shape[0]
     idx = np.arange(T) if rows is None else np.asarray(rows)
     z = hf[idx] @ Wf.T
+    sc = np.asarray(scale)[idx] if np.ndim(scale) else scale
+    tt = None
+    if terms is not None:
+        tt = dict(terms)
+        if tt.get("ref") is not None:
+            tt["ref"] = np.asarray(tt["ref"])[idx]
     out = loss_fwd_bwd(z, np.asarray(target)[idx], None if old_logp is None else np.asarray(old_logp)[idx],
-                       np.asarray(adv_tok)[idx], np.asarray(mask)[idx], eps, scale, want_grad=True)
+                       np.asarray(adv_tok)[idx], np.asarray(mask)[idx], eps, sc, want_grad=True, terms=tt)
     dz = out.pop("dlogits")
     out["d_h"] = dz @ Wf
     if want_dw and rows is None:

@@ -137,6 +137,10 @@ def _lib() -> C.CDLL:
     lib.grpo_lmhead_loss_fwd_bwd.argtypes = [vp, vp, C.c_int64, C.c_int64, C.c_int64, vp, vp, vp, vp, C.c_float,
                                              C.c_float, vp, vp, C.c_uint32, vp, vp, vp, vp, C.c_size_t, vp]
     lib.grpo_lmhead_loss_fwd_bwd.restype = C.c_int
+    lib.grpo_lmhead_loss_fwd_bwd_ex.argtypes = [vp, vp, C.c_int64, C.c_int64, C.c_int64, vp, vp, vp, vp,
+                                                C.c_float, C.c_float, vp, vp, C.c_uint32, vp, vp,
+                                                C.POINTER(grpo_loss_terms), vp, vp, C.c_size_t, vp]
+    lib.grpo_lmhead_loss_fwd_bwd_ex.restype = C.c_int
     lib.grpo_lmhead_forward_noalloc.argtypes = [vp, vp, C.c_int64, C.c_int64, C.c_int64, vp, vp, vp, vp,
                                                 C.c_float, C.c_float, vp, vp, vp, vp]
     lib.grpo_lmhead_forward_noalloc.restype = C.c_int
@@ -449,14 +453,28 @@ LMHEAD_DW_ACCUMULATE = 1
 
 def grpo_lmhead_loss_fwd_bwd(h, W, target, old_logp, adv_tok, mask, clip_eps: float, grad_scale: float,
                              d_h, dW, loss_tok, logp_tok, acc, workspace, stream=None,
-                             dw_accumulate: bool = False) -> None:
+                             dw_accumulate: bool = False, terms: Optional[dict] = None) -> None:
     """h [T, H] and W [V, H] bf16 device tensors; d_h / dW float32 or None; dw_accumulate adds
-    this call's dW to the buffer instead of overwriting it; see grpo.h."""
+    this call's dW to the buffer instead of overwriting it; ``terms`` (as for
+    grpo_logprob_loss_fwd_bwd) selects grpo_lmhead_loss_fwd_bwd_ex; see grpo.h."""
     T, H = h.shape
     V = W.shape[0]
+    flags = LMHEAD_DW_ACCUMULATE if dw_accumulate else 0
+    if terms is not None:
+        tm = grpo_loss_terms(int(terms.get("kl_kind", 0)), float(terms.get("kl_coef", 0.0)),
+                             _ptr(terms.get("ref_logp")), float(terms.get("ent_coef", 0.0)),
+                             _ptr(terms.get("entropy_tok")), _ptr(terms.get("w_tok")))
+        rc = _lib().grpo_lmhead_loss_fwd_bwd_ex(_ptr(h), _ptr(W), T, V, H, _ptr(target), _ptr(old_logp),
+                                                _ptr(adv_tok), _ptr(mask), float(clip_eps), float(grad_scale),
+                                                _ptr(d_h), _ptr(dW), flags, _ptr(loss_tok), _ptr(logp_tok),
+                                                C.byref(tm), _ptr(acc), _ptr(workspace),
+                                                workspace.numel() * workspace.element_size(), _stream(stream))
+        if rc != OK:
+            raise GrpoError(rc, "grpo_lmhead_loss_fwd_bwd_ex")
+        return
     rc = _lib().grpo_lmhead_loss_fwd_bwd(_ptr(h), _ptr(W), T, V, H, _ptr(target), _ptr(old_logp),
                                          _ptr(adv_tok), _ptr(mask), float(clip_eps), float(grad_scale),
-                                         _ptr(d_h), _ptr(dW), LMHEAD_DW_ACCUMULATE if dw_accumulate else 0,
+                                         _ptr(d_h), _ptr(dW), flags,
                                          _ptr(loss_tok), _ptr(logp_tok), _ptr(acc),
                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
                                          _stream(stream))

@@ -31,60 +31,108 @@
 namespace grpo {
 namespace lmhead {
 
+// Inputs and outputs of the per-token reduce.
+struct ReduceArgs {
+  int64_t T, V;
+  int n_col_tiles;
+  const float *part_m, *part_s, *part_s2, *zy;  // part_s2: entropy instance only
+  const int32_t* target;
+  const float *old_logp, *adv;
+  const uint8_t* mask;
+  float eps, scale;
+  // terms (TERMS): KL to a reference policy, entropy bonus, per-token weight of the grad scale
+  int32_t kl_kind;
+  float kl_coef, ent_coef;
+  const float *ref_logp, *w_tok;
+  float* entropy_tok;
+  float *lse2_out, *coef_out, *ea_out, *eb_out;  // ea, eb: entropy instance only
+  float *loss_tok, *logp_tok;
+  grpo_step_acc* acc;
+};
+
 // Per token: combine the vocabulary-tile partials, then the token epilogue. A block takes 32
 // tokens (lane = token, so every partial load is one coalesced 128-byte line) and its 8 warps
 // split the tiles: warp w folds tiles w, w + 8, ... in order; warp 0 then folds the 8 warp
-// partials in warp order. The order depends only on the tile count.
+// partials in warp order. The order depends only on the tile count. ENT: the partials carry
+// sum e z, and the token's entropy LSE - E_p[z] is formed; TERMS: the regularisers and the
+// per-token weight are applied as in the row pass.
 constexpr int kReduceWarps = 8;
 
-__global__ void __launch_bounds__(kReduceWarps * 32)
-reduce_kernel(int64_t T, int n_col_tiles, const float* __restrict__ part_m, const float* __restrict__ part_s,
-              const float* __restrict__ zy, const int32_t* __restrict__ target, int64_t V, const float* old_logp,
-              const float* __restrict__ adv, const uint8_t* __restrict__ mask, float eps, float scale,
-              float* __restrict__ lse2_out, float* __restrict__ coef_out, float* loss_tok, float* logp_tok,
-              grpo_step_acc* acc) {
-  __shared__ float wm[kReduceWarps][32], ws[kReduceWarps][32];
+template <bool ENT, bool TERMS>
+__global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(ReduceArgs a) {
+  __shared__ float wm[kReduceWarps][32], ws[kReduceWarps][32], ws2[kReduceWarps][32];
   __shared__ unsigned long long sc[4];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   if (threadIdx.x < 4) sc[threadIdx.x] = 0;
-  const int64_t row = (int64_t)blockIdx.x * 32 + lane;
-  const bool live = row < T && mask[row] != 0;
-  MS t{-INFINITY, 0.f};
+  const int64_t T = a.T, row = (int64_t)blockIdx.x * 32 + lane;
+  const bool live = row < T && a.mask[row] != 0;
+  MS3 t{-INFINITY, 0.f, 0.f};
   if (live) {
 #pragma unroll 4
-    for (int c = w; c < n_col_tiles; c += kReduceWarps)
-      t = ms2_combine(t, MS{part_m[(int64_t)c * T + row], part_s[(int64_t)c * T + row]});
+    for (int c = w; c < a.n_col_tiles; c += kReduceWarps) {
+      const int64_t k = (int64_t)c * T + row;
+      if (ENT) {
+        t = ms3_combine2(t, MS3{a.part_m[k], a.part_s[k], a.part_s2[k]});
+      } else {
+        const MS u = ms2_combine(MS{t.m, t.s}, MS{a.part_m[k], a.part_s[k]});
+        t = MS3{u.m, u.s, 0.f};
+      }
+    }
   }
   wm[w][lane] = t.m;
   ws[w][lane] = t.s;
+  if (ENT) ws2[w][lane] = t.s2;
   __syncthreads();
   unsigned long long v_valid = 0, v_clip = 0, v_nf = 0, v_tok = 0;
   if (w == 0 && row < T) {
     v_tok = 1;
-    float coef = 0.f, l2 = 0.f;
+    float coef = 0.f, l2 = 0.f, ea = 0.f, eb = 0.f, H = 0.f;
     if (live) {
-      MS tot{wm[0][lane], ws[0][lane]};
+      MS3 tot{wm[0][lane], ws[0][lane], ENT ? ws2[0][lane] : 0.f};
 #pragma unroll
-      for (int k = 1; k < kReduceWarps; ++k) tot = ms2_combine(tot, MS{wm[k][lane], ws[k][lane]});
+      for (int k = 1; k < kReduceWarps; ++k) {
+        if (ENT) {
+          tot = ms3_combine2(tot, MS3{wm[k][lane], ws[k][lane], ws2[k][lane]});
+        } else {
+          const MS u = ms2_combine(MS{tot.m, tot.s}, MS{wm[k][lane], ws[k][lane]});
+          tot = MS3{u.m, u.s, 0.f};
+        }
+      }
       const float l2s = log2f(tot.s);
       l2 = tot.m + l2s;
-      const int32_t y = target[row];
-      const float z = (y >= 0 && (int64_t)y < V) ? zy[row] : __int_as_float(0x7fc00000);
+      const float ez = ENT ? tot.s2 / tot.s : 0.f;  // sum_v p_v z_v
+      const int32_t y = a.target[row];
+      const float z = (y >= 0 && (int64_t)y < a.V) ? a.zy[row] : __int_as_float(0x7fc00000);
+      const float scl = (TERMS && a.w_tok) ? a.scale * a.w_tok[row] : a.scale;
       // log2 p_y = (z_y log2e - m) - log2(sum), without cancellation
-      const TokenOut o = token_epilogue((fmaf(z, kLog2e, -tot.m) - l2s) * kLn2, fabsf(l2) <= kLseMax * kLog2e,
-                                        old_logp != nullptr, old_logp ? old_logp[row] : 0.f, adv[row], eps, scale);
-      loss_tok[row] = o.loss;
-      if (logp_tok) logp_tok[row] = o.logp;
+      TokenOut o = token_epilogue((fmaf(z, kLog2e, -tot.m) - l2s) * kLn2, fabsf(l2) <= kLseMax * kLog2e,
+                                  a.old_logp != nullptr, a.old_logp ? a.old_logp[row] : 0.f, a.adv[row], a.eps,
+                                  scl);
+      H = ENT ? l2 * kLn2 - ez : 0.f;
+      if (TERMS)
+        apply_terms(o, scl, a.kl_kind, a.kl_coef, a.kl_kind != GRPO_KL_NONE ? a.ref_logp[row] : 0.f, a.ent_coef,
+                    H);
+      a.loss_tok[row] = o.loss;
+      if (a.logp_tok) a.logp_tok[row] = o.logp;
       coef = o.coef;
+      if (ENT) {
+        eb = a.ent_coef * scl;
+        ea = coef - eb * ez;
+      }
       v_valid = 1;
       v_clip = o.clipped;
       v_nf = o.nonfinite;
     } else {
-      loss_tok[row] = 0.f;
-      if (logp_tok) logp_tok[row] = 0.f;
+      a.loss_tok[row] = 0.f;
+      if (a.logp_tok) a.logp_tok[row] = 0.f;
     }
-    lse2_out[row] = l2;
-    coef_out[row] = coef;
+    a.lse2_out[row] = l2;
+    a.coef_out[row] = coef;
+    if (ENT) {
+      a.ea_out[row] = ea;
+      a.eb_out[row] = eb;
+    }
+    if (TERMS && a.entropy_tok) a.entropy_tok[row] = H;
   }
   if (v_tok) atomicAdd(&sc[0], v_tok);
   if (v_valid) atomicAdd(&sc[1], v_valid);
@@ -92,10 +140,10 @@ reduce_kernel(int64_t T, int n_col_tiles, const float* __restrict__ part_m, cons
   if (v_nf) atomicAdd(&sc[3], v_nf);
   __syncthreads();
   if (threadIdx.x == 0) {
-    if (sc[0]) atomicAdd(reinterpret_cast<unsigned long long*>(&acc->n_tokens), sc[0]);
-    if (sc[1]) atomicAdd(reinterpret_cast<unsigned long long*>(&acc->n_valid), sc[1]);
-    if (sc[2]) atomicAdd(reinterpret_cast<unsigned long long*>(&acc->n_clipped), sc[2]);
-    if (sc[3]) atomicAdd(reinterpret_cast<unsigned long long*>(&acc->n_nonfinite), sc[3]);
+    if (sc[0]) atomicAdd(reinterpret_cast<unsigned long long*>(&a.acc->n_tokens), sc[0]);
+    if (sc[1]) atomicAdd(reinterpret_cast<unsigned long long*>(&a.acc->n_valid), sc[1]);
+    if (sc[2]) atomicAdd(reinterpret_cast<unsigned long long*>(&a.acc->n_clipped), sc[2]);
+    if (sc[3]) atomicAdd(reinterpret_cast<unsigned long long*>(&a.acc->n_nonfinite), sc[3]);
   }
 }
 
@@ -236,7 +284,9 @@ namespace {
 constexpr int kMaxChunkTiles = 66;
 
 struct WsLayout {
-  size_t part_m, part_s, zy, lse2, coef, dz, dz2, total;  // dz, dz2: the two dlogits chunk buffers
+  // dz, dz2: the two dlogits chunk buffers; part_s2, ea, eb (last, so that the forward pass's
+  // prefix is unchanged): the entropy bonus's third partial and its per-token coefficients
+  size_t part_m, part_s, zy, lse2, coef, dz, dz2, part_s2, ea, eb, total;
   int n_col_tiles, chunk_tiles;
   int64_t vchunk;  // columns of the dlogits chunk buffer
 };
@@ -256,6 +306,9 @@ WsLayout ws_layout(int64_t T, int64_t V) {
   w.coef = off; off += up((size_t)T * 4);
   w.dz = off; off += up((size_t)T * w.vchunk * 2);
   w.dz2 = off; off += up((size_t)T * w.vchunk * 2);
+  w.part_s2 = off; off += up((size_t)w.n_col_tiles * T * 4);
+  w.ea = off; off += up((size_t)T * 4);
+  w.eb = off; off += up((size_t)T * 4);
   w.total = off;
   return w;
 }
@@ -263,14 +316,29 @@ WsLayout ws_layout(int64_t T, int64_t V) {
 struct Scratch {
   float *part_m, *part_s, *zy, *lse2, *coef;
   __nv_bfloat16* dz[2];
+  float *part_s2, *ea, *eb;  // NULL when the region lies past the scratch (the no-alloc forward)
 };
 
-Scratch carve(void* base, const WsLayout& ws) {
+// The regions of a workspace: all of them (full), or only the forward pass's prefix.
+Scratch carve(void* base, const WsLayout& ws, bool full) {
   uint8_t* b = static_cast<uint8_t*>(base);
-  return {reinterpret_cast<float*>(b + ws.part_m), reinterpret_cast<float*>(b + ws.part_s),
-          reinterpret_cast<float*>(b + ws.zy),     reinterpret_cast<float*>(b + ws.lse2),
-          reinterpret_cast<float*>(b + ws.coef),
-          {reinterpret_cast<__nv_bfloat16*>(b + ws.dz), reinterpret_cast<__nv_bfloat16*>(b + ws.dz2)}};
+  Scratch s{reinterpret_cast<float*>(b + ws.part_m), reinterpret_cast<float*>(b + ws.part_s),
+            reinterpret_cast<float*>(b + ws.zy),     reinterpret_cast<float*>(b + ws.lse2),
+            reinterpret_cast<float*>(b + ws.coef),   {nullptr, nullptr},
+            nullptr, nullptr, nullptr};
+  if (full) {
+    s.dz[0] = reinterpret_cast<__nv_bfloat16*>(b + ws.dz);
+    s.dz[1] = reinterpret_cast<__nv_bfloat16*>(b + ws.dz2);
+    s.part_s2 = reinterpret_cast<float*>(b + ws.part_s2);
+    s.ea = reinterpret_cast<float*>(b + ws.ea);
+    s.eb = reinterpret_cast<float*>(b + ws.eb);
+  }
+  return s;
+}
+
+// Whether a call's terms need the entropy instances (the bonus, or the entropy as an output).
+bool wants_entropy(const grpo_loss_terms* terms) {
+  return terms && (terms->ent_coef != 0.f || terms->entropy_tok != nullptr);
 }
 
 int check_args(const void* h, const void* W, int64_t T, int64_t V, int64_t H, const int32_t* target,
@@ -287,21 +355,57 @@ int check_args(const void* h, const void* W, int64_t T, int64_t V, int64_t H, co
 // LSE and gradient coefficient in the scratch.
 int forward(int cg, const void* h, const void* W, int64_t T, int64_t V, int64_t H, const int32_t* target,
             const float* old_logp, const float* adv_tok, const uint8_t* mask, float clip_eps, float grad_scale,
-            float* loss_tok, float* logp_tok, grpo_step_acc* acc, const WsLayout& ws, const Scratch& sc,
-            cudaStream_t st) {
+            float* loss_tok, float* logp_tok, const grpo_loss_terms* terms, grpo_step_acc* acc,
+            const WsLayout& ws, const Scratch& sc, cudaStream_t st) {
+  const bool ent = wants_entropy(terms);
   GemmArgs g{};
   g.target = target;
   g.part_m = sc.part_m;
   g.part_s = sc.part_s;
+  g.part_s2 = sc.part_s2;
   g.zy = sc.zy;
   g.acc = acc;
   g.col_tile0 = 0;
   g.n_n = ws.n_col_tiles;
-  const int rc = logits_gemm<EPI_PARTIALS>(cg, h, W, T, V, H, g, st);
+  const int rc = ent ? logits_gemm<EPI_PARTIALS_ENT>(cg, h, W, T, V, H, g, st)
+                     : logits_gemm<EPI_PARTIALS>(cg, h, W, T, V, H, g, st);
   if (rc != GRPO_OK) return rc;
-  reduce_kernel<<<(unsigned)((T + 31) / 32), kReduceWarps * 32, 0, st>>>(
-      T, ws.n_col_tiles, sc.part_m, sc.part_s, sc.zy, target, V, old_logp, adv_tok, mask, clip_eps, grad_scale,
-      sc.lse2, sc.coef, loss_tok, logp_tok, acc);
+  ReduceArgs r{};
+  r.T = T;
+  r.V = V;
+  r.n_col_tiles = ws.n_col_tiles;
+  r.part_m = sc.part_m;
+  r.part_s = sc.part_s;
+  r.part_s2 = sc.part_s2;
+  r.zy = sc.zy;
+  r.target = target;
+  r.old_logp = old_logp;
+  r.adv = adv_tok;
+  r.mask = mask;
+  r.eps = clip_eps;
+  r.scale = grad_scale;
+  if (terms) {
+    r.kl_kind = terms->kl_kind;
+    r.kl_coef = terms->kl_coef;
+    r.ent_coef = terms->ent_coef;
+    r.ref_logp = terms->ref_logp;
+    r.w_tok = terms->w_tok;
+    r.entropy_tok = terms->entropy_tok;
+  }
+  r.lse2_out = sc.lse2;
+  r.coef_out = sc.coef;
+  r.ea_out = sc.ea;
+  r.eb_out = sc.eb;
+  r.loss_tok = loss_tok;
+  r.logp_tok = logp_tok;
+  r.acc = acc;
+  const dim3 grid((unsigned)((T + 31) / 32)), block(kReduceWarps * 32);
+  if (ent)
+    reduce_kernel<true, true><<<grid, block, 0, st>>>(r);
+  else if (terms)
+    reduce_kernel<false, true><<<grid, block, 0, st>>>(r);
+  else
+    reduce_kernel<false, false><<<grid, block, 0, st>>>(r);
   GRPO_CUDA_TRY(cudaGetLastError());
   return GRPO_OK;
 }
@@ -355,12 +459,19 @@ extern "C" GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int6
   return ws_layout(T, V).total;
 }
 
-extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, int64_t T, int64_t V, int64_t H,
-                                                 const int32_t* target, const float* old_logp,
-                                                 const float* adv_tok, const uint8_t* mask, float clip_eps,
-                                                 float grad_scale, float* d_h, float* dW, uint32_t flags,
-                                                 float* loss_tok, float* logp_tok, grpo_step_acc* acc,
-                                                 void* workspace, size_t workspace_bytes, void* stream) {
+extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd_ex(const void* h, const void* W, int64_t T, int64_t V,
+                                                    int64_t H, const int32_t* target, const float* old_logp,
+                                                    const float* adv_tok, const uint8_t* mask, float clip_eps,
+                                                    float grad_scale, float* d_h, float* dW, uint32_t flags,
+                                                    float* loss_tok, float* logp_tok,
+                                                    const grpo_loss_terms* terms, grpo_step_acc* acc,
+                                                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (terms) {
+    if (terms->kl_kind != GRPO_KL_NONE && terms->kl_kind != GRPO_KL_K1 && terms->kl_kind != GRPO_KL_K3)
+      return GRPO_ERR_INVALID;
+    if (terms->kl_kind != GRPO_KL_NONE && !terms->ref_logp) return GRPO_ERR_INVALID;
+    if (!isfinite(terms->kl_coef) || !isfinite(terms->ent_coef)) return GRPO_ERR_INVALID;
+  }
   const int arc = check_args(h, W, T, V, H, target, adv_tok, mask, loss_tok, acc);
   if (arc != GRPO_OK || T == 0) return arc;
   if (flags & ~(uint32_t)GRPO_LMHEAD_DW_ACCUMULATE) return GRPO_ERR_INVALID;
@@ -368,11 +479,13 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
   const WsLayout ws = ws_layout(T, V);
   if (workspace_bytes < ws.total) return GRPO_ERR_CAPACITY;
   const cudaStream_t st = as_stream(stream);
-  const Scratch sc = carve(workspace, ws);
+  const Scratch sc = carve(workspace, ws, true);
   const int cg = cta_group();
   int rc = forward(cg, h, W, T, V, H, target, old_logp, adv_tok, mask, clip_eps, grad_scale, loss_tok, logp_tok,
-                   acc, ws, sc, st);
+                   terms, acc, ws, sc, st);
   if (rc != GRPO_OK || (!d_h && !dW)) return rc;
+  // the dlogits take the entropy form p (ea + eb z) when the bonus has a coefficient
+  const bool ent_grad = terms && terms->ent_coef != 0.f;
 
   // Per vocabulary chunk c: the recompute writes the chunk's dlogits into buffer c % 2 on the
   // caller's stream; d_h and dW read it on the second stream, so the next chunk's recompute
@@ -395,6 +508,10 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
     g.target = target;
     g.lse2 = sc.lse2;
     g.coef = sc.coef;
+    if (ent_grad) {
+      g.ea = sc.ea;
+      g.eb = sc.eb;
+    }
     g.dz = dzb;
     g.ldz = ws.vchunk;
     g.v0 = v0;
@@ -455,6 +572,16 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, i
     }
   }
   return rc;
+}
+
+extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd(const void* h, const void* W, int64_t T, int64_t V, int64_t H,
+                                                 const int32_t* target, const float* old_logp,
+                                                 const float* adv_tok, const uint8_t* mask, float clip_eps,
+                                                 float grad_scale, float* d_h, float* dW, uint32_t flags,
+                                                 float* loss_tok, float* logp_tok, grpo_step_acc* acc,
+                                                 void* workspace, size_t workspace_bytes, void* stream) {
+  return grpo_lmhead_loss_fwd_bwd_ex(h, W, T, V, H, target, old_logp, adv_tok, mask, clip_eps, grad_scale, d_h, dW,
+                                     flags, loss_tok, logp_tok, nullptr, acc, workspace, workspace_bytes, stream);
 }
 
 // ---- allocation-free forward entry point -----------------------------------------------------
@@ -547,5 +674,5 @@ extern "C" GRPO_API int grpo_lmhead_forward_noalloc(const void* h, const void* W
   const int rc = noalloc_setup(&scratch);
   if (rc != GRPO_OK) return rc;
   return forward(cta_group(), h, W, T, V, H, target, old_logp, adv_tok, mask, clip_eps, grad_scale, loss_tok,
-                 logp_tok, acc, ws, carve(scratch, ws), as_stream(stream));
+                 logp_tok, nullptr, acc, ws, carve(scratch, ws, false), as_stream(stream));
 }

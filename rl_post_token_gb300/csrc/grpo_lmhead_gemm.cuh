@@ -36,7 +36,8 @@ constexpr int BK = 64;   // K per stage: one 128-byte swizzle row of bf16
 constexpr int NTHREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 
-enum Epi : int { EPI_PARTIALS = 0, EPI_DLOGITS = 1, EPI_STORE_F32 = 2 };
+// EPI_PARTIALS_ENT: the partials plus sum e z per tile (the entropy's third accumulator)
+enum Epi : int { EPI_PARTIALS = 0, EPI_DLOGITS = 1, EPI_STORE_F32 = 2, EPI_PARTIALS_ENT = 3 };
 
 // Dlogits epilogue staging: each epilogue warp writes its 32 rows x 32 columns of bf16 (2 KB,
 // 64-byte rows in the 64-byte swizzle a TMA store expects) into one of two buffers, and one lane
@@ -227,9 +228,13 @@ struct GemmArgs {
   const int32_t* target;
   float* part_m;  // [n_col_tiles_total][T] log2-domain shift of each token's tile
   float* part_s;  // [n_col_tiles_total][T] sum of 2^(z log2 e - shift) over the tile
+  float* part_s2; // [n_col_tiles_total][T] (EPI_PARTIALS_ENT) sum of 2^(z log2 e - shift) z
   float* zy;      // [T] target logit
   const float* lse2;  // [T] LSE * log2(e)
   const float* coef;  // [T] gradient coefficient (grad scale included)
+  // with the entropy bonus (eb != NULL): dz_v = p_v (ea + eb z_v) - coef [v == y]
+  const float* ea;    // [T] coef - eb E_p[z]
+  const float* eb;    // [T] entropy coefficient times the token's grad scale
   __nv_bfloat16* dz;  // chunk buffer [T][ldz], column 0 = vocabulary column v0
   int64_t ldz, v0;
   // EPI_STORE_F32: C[M][ldc] = (accumulate ? C : 0) + A B
@@ -282,6 +287,40 @@ __device__ __forceinline__ void epi_partials(const GemmArgs& g, uint32_t taddr, 
   }
 }
 
+// epi_partials with the entropy's third accumulator: (shift, sum e, sum e z) of the tile, the
+// target logit. Groups of 32 columns wholly past the vocabulary are skipped; a group holding
+// both takes the no-mass guard for its -inf columns.
+__device__ __forceinline__ void epi_partials_ent(const GemmArgs& g, uint32_t taddr, int64_t row, bool rok, int ct) {
+  const int64_t c0 = (int64_t)ct * BN;
+  const int32_t y = rok ? g.target[row] : -1;
+  const bool own = y >= c0 && y < c0 + BN;
+  MS3 acc{-INFINITY, 0.f, 0.f};
+  bool guarded = false;
+  float zy = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    float v[32];
+    tmem_ld32(taddr + c * 32, v);
+    const int64_t cb = c0 + c * 32;
+    if (cb >= g.V) continue;  // warp-uniform
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (cb + i >= g.V) v[i] = -INFINITY;
+    if (own && y >= cb && y < cb + 32) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (cb + i == y) zy = v[i];
+    }
+    lazy_online3<32>(acc, v, guarded);
+  }
+  if (rok) {
+    g.part_m[(int64_t)ct * g.M + row] = acc.m;
+    g.part_s[(int64_t)ct * g.M + row] = acc.s;
+    g.part_s2[(int64_t)ct * g.M + row] = acc.s2;
+    if (own) g.zy[row] = zy;
+  }
+}
+
 // dlogits of one tile: dz = coef * 2^(z log2 e - LSE2) - coef [v == y], rounded to bf16 (|coef|
 // is folded into the exponent, its sign applied to the packed pair). Masked and clipped tokens
 // (coef = 0) give zero rows. Each 32-column group of the warp's 32 rows is staged in shared
@@ -297,6 +336,10 @@ __device__ __forceinline__ void epi_dlogits(const GemmArgs& g, const CUtensorMap
   const float l2 = rok ? g.lse2[row] : 0.f;
   const float cexp = l2 - log2f(fabsf(cf));
   const uint32_t sgn = cf < 0.f ? 0x80008000u : 0u;
+  // with the entropy bonus: dz = p (ea + eb z); ea = eb = 0 for masked tokens
+  const bool ent = g.eb != nullptr;
+  const float ea = (ent && rok) ? g.ea[row] : 0.f, eb = (ent && rok) ? g.eb[row] : 0.f;
+  const bool live = ent ? (ea != 0.f || eb != 0.f) : cf != 0.f;
   const uint32_t sw = (uint32_t)((lane >> 1) & 3);
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
@@ -306,7 +349,7 @@ __device__ __forceinline__ void epi_dlogits(const GemmArgs& g, const CUtensorMap
     // warp-uniform: the rest of the tile lies past the vocabulary, or all 32 rows past T
     if (cb >= g.V || warp_row0 >= g.M) continue;
     uint32_t w[16];
-    if (cf != 0.f) {
+    if (live) {
       float zyv = 0.f;
       const bool hit = y >= cb && y < cb + 32;
       if (hit) {
@@ -314,13 +357,22 @@ __device__ __forceinline__ void epi_dlogits(const GemmArgs& g, const CUtensorMap
         for (int i = 0; i < 32; ++i)
           if (cb + i == y) zyv = v[i];
       }
+      if (ent) {
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const float2 p = ex2_pair(v[i], v[i + 1], cexp);
-        w[i / 2] = pack_bf16x2(p.x, p.y) ^ sgn;
+        for (int i = 0; i < 32; i += 2) {
+          const float2 p = ex2_pair(v[i], v[i + 1], l2);
+          w[i / 2] = pack_bf16x2(p.x * fmaf(eb, v[i], ea), p.y * fmaf(eb, v[i + 1], ea));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float2 p = ex2_pair(v[i], v[i + 1], cexp);
+          w[i / 2] = pack_bf16x2(p.x, p.y) ^ sgn;
+        }
       }
       if (hit) {
-        const float dzy = cf * ex2(fmaf(zyv, kLog2e, -l2)) - cf;
+        const float py = ex2(fmaf(zyv, kLog2e, -l2));
+        const float dzy = ent ? py * fmaf(eb, zyv, ea) - cf : cf * py - cf;
         const uint32_t hb = __bfloat16_as_ushort(__float2bfloat16_rn(dzy));
         const int k = (int)(y - cb);
 #pragma unroll
@@ -512,6 +564,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + ab * BN;
       if constexpr (EPI == EPI_PARTIALS)
         epi_partials(g, taddr, row, rok, g.col_tile0 + nu);
+      else if constexpr (EPI == EPI_PARTIALS_ENT)
+        epi_partials_ent(g, taddr, row, rok, g.col_tile0 + nu);
       else if constexpr (EPI == EPI_DLOGITS)
         epi_dlogits(g, &map_c, taddr, row, rok, g.col_tile0 + nu, row - lane,
                     epi_base + (uint32_t)quarter * 2u * EPI_BUF_BYTES, lane);

@@ -121,12 +121,13 @@ def test_lmhead_workspace_sizes():
                                  (16384, 151936, 2048, 66), (8, 256 * 66, 64, 66), (8, 256 * 67, 64, 34)]:
         plain = _lib.grpo_lmhead_workspace_size(T, V, H)
         nct = (V + 255) // 256
-        # partials (two float arrays per tile and token), three per-token floats, then two bf16
-        # dlogits chunk buffers: the tiles split into ceil(tiles / 66) chunks of equal width
+        # partials (two float arrays per tile and token), three per-token floats, two bf16
+        # dlogits chunk buffers (the tiles split into ceil(tiles / 66) chunks of equal width),
+        # then the entropy's third partial per tile and token and two per-token floats
         n_chunks = -(-nct // 66)
         assert -(-nct // n_chunks) == chunk_tiles
         base = 2 * up(4 * nct * T) + 3 * up(4 * T)
-        assert plain == base + 2 * up(2 * T * 256 * chunk_tiles)
+        assert plain == base + 2 * up(2 * T * 256 * chunk_tiles) + up(4 * nct * T) + 2 * up(4 * T)
     for bad in [(0, 8, 64), (8, 0, 64), (8, 8, 0), (-1, 8, 64)]:
         assert _lib.grpo_lmhead_workspace_size(*bad) == 0
     assert _lib.lib().grpo_lmhead_forward_noalloc_max_scratch() == 16 << 20

@@ -368,3 +368,117 @@ def test_lmhead_backward_overlap_gives_the_same_bits(monkeypatch):
         outs.append((d_h, dW, loss, logp))
     for a, b in zip(*outs):
         assert torch.equal(a, b)
+
+
+# ---- regularisers through the LM-head: KL to the reference policy, the entropy bonus, and
+# per-token gradient weights (grpo_lmhead_loss_fwd_bwd_ex) -------------------------------------
+
+@pytest.mark.parametrize("kl_kind, ent, weighted", [(1, 0.0, False), (2, 0.0, True), (0, 0.05, False),
+                                                     (2, 0.02, True)])
+def test_lmhead_kl_entropy_and_token_weights(cta_group, kl_kind, ent, weighted):
+    # 300 tokens (ragged tiles), V = 20000 (two vocabulary chunks, the second ragged), H = 192;
+    # the reference log-probs a normal perturbation of the policy's own, the weights those of
+    # sequence-mean aggregation (1 / row length, a few distinct values)
+    T, V, Hd = 300, 20000, 192
+    wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed=70 + kl_kind, valid_lo=0.1)
+    rng = np.random.default_rng(71)
+    ref = (old_logp + rng.normal(0, 0.3, T)).astype(np.float32)
+    w_tok = rng.choice([1.0, 0.5, 0.125, 1.0 / 3], T).astype(np.float32) if weighted else None
+    N = max(int(mask.sum()), 1)
+    gs = np.float32(1.0 / N)
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    d_h = torch.full((T, Hd), 7.0, device=DEV)
+    dW = torch.full((V, Hd), 7.0, device=DEV)
+    loss = torch.full((T,), -7.0, device=DEV)
+    logp = torch.full((T,), -7.0, device=DEV)
+    ent_t = torch.full((T,), -7.0, device=DEV)
+    acc = _lib.new_step_acc(DEV)
+    ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=DEV)
+    terms = dict(kl_kind=kl_kind, kl_coef=0.1, ref_logp=t(ref), ent_coef=ent, entropy_tok=ent_t, w_tok=t(w_tok))
+    _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, t(wl.target), t(old_logp), t(a_tok), t(mask), wl.eps, float(gs),
+                                  d_h, dW, loss, logp, acc, ws, terms=terms)
+    torch.cuda.synchronize()
+    # the oracle's per-token scale: the float32 product the kernels form, held in float64
+    scale = (gs * w_tok).astype(np.float64) if weighted else float(gs)
+    oterms = dict(kl_kind=kl_kind, kl_coef=float(np.float32(0.1)), ref=ref.astype(np.float64),
+                  ent_coef=float(np.float32(ent)))
+    out = OL.lmhead_fwd_bwd(hb, wb, wl.target, old_logp, a_tok, mask, wl.eps, scale=scale, terms=oterms)
+    m = mask.astype(bool)
+    gl, gp, ge = H.to_f64(loss), H.to_f64(logp), H.to_f64(ent_t)
+    assert np.all(np.abs(gp[m] - out["logp_tok"][m]) <= 1e-5 * np.maximum(1, np.abs(out["logp_tok"][m])))
+    assert np.all(np.abs(ge[m] - out["entropy"][m]) <= 1e-5 * np.maximum(1, out["entropy"][m]))
+    assert np.all(ge[~m] == 0) and np.all(gl[~m] == 0) and np.all(gp[~m] == 0)
+    assert np.all(np.abs(gl - out["loss_tok"]) <= 1e-5 * np.abs(out["loss_tok"]) + 1e-6)
+    res = _lib.grpo_finish_step(acc, loss, expected_N=int(mask.sum()))
+    assert res["status"] == 0 and res["kernel_flags"] == 0 and res["n_valid"] == int(mask.sum())
+    # d_h and dW: the module docstring's bar over the magnitudes of the regularised dlogits
+    hf, wf = OL.as_f64(hb), OL.as_f64(wb)
+    z = hf @ wf.T
+    dz_abs = np.zeros_like(z)
+    for k in range(T):
+        if mask[k]:
+            tt = dict(oterms, ref=float(ref[k]))
+            sk = scale[k] if weighted else scale
+            dz_abs[k] = np.abs(OL.token_objective(z[k], int(wl.target[k]), old_logp[k], a_tok[k], 1, wl.eps, sk,
+                                                  terms=tt)[4])
+    tol_h = 8e-3 * (dz_abs @ np.abs(wf)) + 1e-12
+    tol_w = 8e-3 * (dz_abs.T @ np.abs(hf)) + 1e-12
+    gh, gw = H.to_f64(d_h), H.to_f64(dW)
+    bad = np.abs(gh - out["d_h"]) > tol_h
+    assert not bad.any(), (np.argwhere(bad)[:3], gh[bad][:3], out["d_h"][bad][:3])
+    bad = np.abs(gw - out["dW"]) > tol_w
+    assert not bad.any(), (np.argwhere(bad)[:3], gw[bad][:3], out["dW"][bad][:3])
+
+
+def test_lmhead_terms_off_gives_the_plain_bits(cta_group):
+    # terms with every regulariser off and no per-token outputs take the plain path: the same
+    # bits as the call without terms; asking for the entropy as a metric only (ent_coef 0)
+    # leaves the loss, log-probs and gradients within the plain call's bars and the entropy at
+    # the oracle's
+    T, V, Hd = 300, 3000, 128
+    wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed=77, valid_lo=0.1)
+    N = max(int(mask.sum()), 1)
+    plain = _run(h, Wt, wl, mask, a_tok, old_logp, 1.0 / N)
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+    def run_terms(terms):
+        d_h = torch.full((T, Hd), 7.0, device=DEV)
+        dW = torch.full((V, Hd), 7.0, device=DEV)
+        loss = torch.full((T,), -7.0, device=DEV)
+        logp = torch.full((T,), -7.0, device=DEV)
+        acc = _lib.new_step_acc(DEV)
+        ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=DEV)
+        _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, t(wl.target), t(old_logp), t(a_tok), t(mask), wl.eps, 1.0 / N,
+                                      d_h, dW, loss, logp, acc, ws, terms=terms)
+        torch.cuda.synchronize()
+        return d_h, dW, loss, logp, acc
+
+    off = run_terms(dict(kl_kind=0, kl_coef=0.0, ent_coef=0.0))
+    for a, b in zip(plain[:4], off[:4]):
+        assert torch.equal(a, b)
+    ent_t = torch.full((T,), -7.0, device=DEV)
+    met = run_terms(dict(ent_coef=0.0, entropy_tok=ent_t))
+    ref = OL.lmhead_fwd_bwd(hb, wb, wl.target, old_logp, a_tok, mask, wl.eps, scale=1.0 / N,
+                            terms=dict(kl_kind=0, kl_coef=0.0, ref=None, ent_coef=0.0))
+    H.assert_tokens_close(H.to_f64(met[2]), H.to_f64(met[3]), ref, a_tok, mask)
+    m = mask.astype(bool)
+    ge = H.to_f64(ent_t)
+    assert np.all(np.abs(ge[m] - ref["entropy"][m]) <= 1e-5 * np.maximum(1, ref["entropy"][m]))
+    assert np.all(ge[~m] == 0)
+    _, tol_h, tol_w = _oracle_grad_tol(hb, wb, wl, mask, a_tok, old_logp, N)
+    assert not (np.abs(H.to_f64(met[0]) - ref["d_h"]) > tol_h).any()
+    assert not (np.abs(H.to_f64(met[1]) - ref["dW"]) > tol_w).any()
+
+
+def test_lmhead_terms_reject_bad_arguments():
+    T, V, Hd = 8, 64, 64
+    h = torch.zeros((T, Hd), dtype=torch.bfloat16, device=DEV)
+    Wt = torch.zeros((V, Hd), dtype=torch.bfloat16, device=DEV)
+    i = torch.zeros(T, dtype=torch.int32, device=DEV)
+    f = torch.zeros(T, device=DEV)
+    mk = torch.ones(T, dtype=torch.uint8, device=DEV)
+    acc = _lib.new_step_acc(DEV)
+    ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=DEV)
+    for bad in (dict(kl_kind=7), dict(kl_kind=1)):  # an unknown kind; KL without ref_logp
+        with pytest.raises(_lib.GrpoError):
+            _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, i, None, f, mk, 0.2, 1.0, None, None, f, None, acc, ws, terms=bad)

@@ -95,7 +95,7 @@ def test_lmhead_gemm_instances_do_not_spill(grpo_lib):
     # stack frame (a local array indexed at run time would live in local memory)
     k = _report("grpo_lmhead.cu")
     gemm = [n for n in k if "lmhead11gemm_kernel" in n]
-    assert len(gemm) == 8, sorted(gemm)
+    assert len(gemm) == 10, sorted(gemm)
     for name in gemm + [n for n in k if "lmhead13reduce_kernel" in n]:
         assert k[name]["spill"] == 0, (name, k[name])
         assert k[name]["regs"] <= 255, (name, k[name])

@@ -200,6 +200,50 @@ def test_lmhead_oracle_matches_chain_rule():
     assert np.all(out["d_h"][2] == 0)
 
 
+@pytest.mark.parametrize("kind, ent", [(2, 0.0), (0, 0.05), (1, 0.03)])
+def test_lmhead_oracle_with_terms_matches_chain_rule(kind, ent):
+    # the LM-head oracle with the regularisers (KL k1/k3 to a reference policy, the entropy
+    # bonus) and per-token gradient weights: d_h and dW are the central differences of the
+    # weighted step loss sum_t w_t l_t / N with respect to h and W
+    rng = np.random.default_rng(60 + kind)
+    T, H, V = 5, 6, 7
+    h = rng.normal(0, 1, (T, H))
+    W = rng.normal(0, 0.5, (V, H))
+    y = rng.integers(0, V, T)
+    A = rng.choice([-1.0, 0.5, 2.0], T)
+    m = np.array([1, 1, 0, 1, 1], np.uint8)
+    z = h @ W.T
+    lsm = np.array([sps.log_softmax(z[t])[y[t]] for t in range(T)])
+    old = lsm - np.log(rng.choice([0.9, 1.05, 1.1], T))
+    ref = lsm + rng.normal(0, 0.3, T)
+    w = rng.choice([1.0, 0.5, 0.25], T)
+    N = int(m.sum())
+    terms = dict(kl_kind=kind, kl_coef=0.1, ref=ref, ent_coef=ent)
+    out = L.lmhead_fwd_bwd(h, W, y, old, A, m, EPS, scale=w / N, terms=terms)
+
+    def f(hh, WW):
+        zz = hh @ WW.T
+        tot = 0.0
+        for t in range(T):
+            tt = dict(kl_kind=kind, kl_coef=0.1, ref=ref[t], ent_coef=ent)
+            tot += w[t] * L.token_objective(zz[t], int(y[t]), old[t], A[t], int(m[t]), EPS, want_grad=False,
+                                            terms=tt)[0]
+        return tot / N
+
+    eps_fd = 1e-6
+    for (i, j) in [(0, 0), (1, 3), (4, 5), (3, 2)]:
+        hp, hm = h.copy(), h.copy()
+        hp[i, j] += eps_fd
+        hm[i, j] -= eps_fd
+        assert out["d_h"][i, j] == pytest.approx((f(hp, W) - f(hm, W)) / (2 * eps_fd), rel=1e-5, abs=1e-9)
+    for (i, j) in [(0, 0), (6, 5), (3, 1), (2, 4)]:
+        Wp, Wm = W.copy(), W.copy()
+        Wp[i, j] += eps_fd
+        Wm[i, j] -= eps_fd
+        assert out["dW"][i, j] == pytest.approx((f(h, Wp) - f(h, Wm)) / (2 * eps_fd), rel=1e-5, abs=1e-9)
+    assert np.all(out["d_h"][2] == 0)
+
+
 @pytest.mark.parametrize("kind", [1, 2])
 @pytest.mark.parametrize("ent", [0.0, 0.03])
 def test_extra_terms_central_differences(kind, ent):
