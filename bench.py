@@ -179,9 +179,10 @@ def profiled_traffic():
 
 # ---- oracle timing (CPU baseline and reference arm) ----------------------------------------------
 
-def oracle_sample_rate(wl, n_tokens: int, budget_s: float):
+def oracle_sample_rate(wl, n_tokens: int, budget_s: float, lt=None):
     """Time the float64 oracle on the first valid tokens of a host-generated sample of the
-    workload. Returns (valid tokens/s, tokens timed, seconds)."""
+    workload, with the regularisers of ``lt`` (cli_terms' dict) when given. Returns (valid
+    tokens/s, tokens timed, seconds)."""
     from oracle import loss as OL
     from rl_post_token_gb300 import workloads as W
 
@@ -192,11 +193,14 @@ def oracle_sample_rate(wl, n_tokens: int, budget_s: float):
     tgt, msk, adv = wl.target[:rows], wl.mask[:rows], np.where(np.arange(rows) % 2, 1.0, -1.0)
     ref = np.array([OL.log_softmax_row(OL.as_f64(logits[t]))[tgt[t]] for t in range(rows)])
     old = ref + wl.old_noise[:rows]
+    kl_ref = ref + np.random.default_rng(wl.seed + 1).normal(0.0, 0.1, rows)
+    wt = oracle_token_weights(wl, lt)
     done, t0 = 0, time.perf_counter()
     while True:
         for t in range(rows):
+            tt = oracle_terms(lt, kl_ref[t])
             OL.token_objective(OL.as_f64(logits[t]), int(tgt[t]), float(old[t]), float(adv[t]),
-                               int(msk[t]), wl.eps, 1.0, True)
+                               int(msk[t]), wl.eps, float(wt[t]), True, tt)
             done += int(msk[t])
             if time.perf_counter() - t0 > budget_s:
                 break
@@ -206,10 +210,29 @@ def oracle_sample_rate(wl, n_tokens: int, budget_s: float):
     return done / dt, done, dt
 
 
-def oracle_lmhead_rate(wl, n_tokens: int, budget_s: float):
-    """Time the float64 LM-head oracle (z = h W^T, the objective, d_h and dW) on `n_tokens`
-    hidden states of a host-drawn sample at the workload's V and H, repeating the call until
-    `budget_s` has passed (at least once). Returns (valid tokens/s, tokens timed, seconds)."""
+def oracle_terms(lt, ref):
+    """The oracle's ``terms`` dict for one token (None without regularisers)."""
+    if lt is None or not (lt["kl_kind"] or lt["ent_coef"]):
+        return None
+    return {"kl_kind": lt["kl_kind"], "kl_coef": lt["kl_coef"], "ref": ref, "ent_coef": lt["ent_coef"]}
+
+
+def oracle_token_weights(wl, lt):
+    """Per-token gradient scales of the oracle's timed sample: 1, or 1/(valid tokens of the
+    token's row) under seq-mean-token-mean (the step's divisor is a constant factor)."""
+    from rl_post_token_gb300 import _lib
+    w = np.ones(wl.T)
+    if lt is not None and lt["agg"] == _lib.AGG_SEQ_MEAN_TOKEN_MEAN:
+        for r in range(len(wl.row_len)):
+            w[wl.tok_off[r]:wl.tok_off[r + 1]] = 1.0 / max(int(wl.row_valid[r]), 1)
+    return w
+
+
+def oracle_lmhead_rate(wl, n_tokens: int, budget_s: float, lt=None):
+    """Time the float64 LM-head oracle (z = h W^T, the objective, d_h and dW; the regularisers
+    of ``lt`` when given) on `n_tokens` hidden states of a host-drawn sample at the workload's
+    V and H, repeating the call until `budget_s` has passed (at least once). Returns (valid
+    tokens/s, tokens timed, seconds)."""
     from oracle import loss as OL
     from rl_post_token_gb300 import workloads as W
 
@@ -219,9 +242,11 @@ def oracle_lmhead_rate(wl, n_tokens: int, budget_s: float):
     h = W.bf16_round_bits(rng.standard_normal((n, H), dtype=np.float32) * np.float32(wl.extra["h_std"]))
     w = W.bf16_round_bits(rng.standard_normal((wl.V, H), dtype=np.float32) * np.float32(wl.extra["w_std"]))
     tgt, msk, adv = wl.target[:n], wl.mask[:n], np.where(np.arange(n) % 2, 1.0, -1.0)
+    terms = oracle_terms(lt, np.random.default_rng(wl.seed + 1).normal(-10.0, 0.1, n))
+    scale = oracle_token_weights(wl, lt)[:n]
     done, t0 = 0, time.perf_counter()
     while True:
-        OL.lmhead_fwd_bwd(h, w, tgt, None, adv, msk, wl.eps, 1.0)
+        OL.lmhead_fwd_bwd(h, w, tgt, None, adv, msk, wl.eps, scale, terms=terms)
         done += int(msk.sum())
         if time.perf_counter() - t0 > budget_s:
             break
@@ -258,21 +283,22 @@ def run_reference(args):
     if args.workload == "lmhead" and args.lm_tokens:
         ov = {"tokens": args.lm_tokens}
     wl = W.make_workload(args.workload, seed=0, **ov)
+    lt = cli_terms(args)
     if args.workload == "lmhead":
-        config = lmhead_config(wl)
+        config = dict(lmhead_config(wl), **({"terms": lt["text"]} if lt["text"] else {}))
     else:
         # the same config as the library arm's line; the exec rows from the oracle's planner
         pl = OP.plan(OP.PlanConfig(**wl.plan), wl.row_len, wl.row_valid, seg_counts=wl.seg_counts)
         exec_tokens = int(sum(int(wl.row_len[j]) for j in pl.row_src))
-        config = workload_config(args, wl, exec_tokens, world, args.workload)
+        config = workload_config(args, wl, exec_tokens, world, args.workload, lt["text"])
     per_step_s = 0.5
     if args.workload == "lmhead":
         # one call of the LM-head oracle on 4 tokens per step (its products use every BLAS thread)
-        rate = lambda budget: oracle_lmhead_rate(wl, 4, budget)
+        rate = lambda budget: oracle_lmhead_rate(wl, 4, budget, lt)
         cores = _blas_threads()
         sample = "float64 numpy LM-head oracle (z = h W^T, objective, d_h, dW), 4 host-drawn tokens per step"
     else:
-        rate = lambda budget: oracle_sample_rate(wl, 16, budget)
+        rate = lambda budget: oracle_sample_rate(wl, 16, budget, lt)
         cores = 1
         sample = (f"float64 numpy oracle, first 16 tokens of a host-drawn batch of the workload, "
                   f"{per_step_s}s per step")
@@ -413,6 +439,23 @@ class Batch:
         return valid * (2 * rowb + 4 + 4 + 4 + 1 + 4 + 4 + idx + extra) + masked * (rowb + 1 + idx)
 
 
+def cli_terms(args) -> dict:
+    """The regularisers and aggregation mode that the command line asks for (--kl, --kl-coef,
+    --ent-coef, --agg), with their text for the line's config."""
+    from rl_post_token_gb300 import _lib
+    kl = getattr(args, "kl", "none")
+    agg_name = getattr(args, "agg", "token-mean")
+    out = {"kl_kind": {"none": 0, "k1": _lib.KL_K1, "k3": _lib.KL_K3}[kl],
+           "kl_coef": float(getattr(args, "kl_coef", 0.0)), "ent_coef": float(getattr(args, "ent_coef", 0.0)),
+           "agg": {"token-mean": _lib.AGG_TOKEN_MEAN, "seq-mean-token-sum": _lib.AGG_SEQ_MEAN_TOKEN_SUM,
+                   "seq-mean-token-mean": _lib.AGG_SEQ_MEAN_TOKEN_MEAN}[agg_name]}
+    out["text"] = ", ".join(([f"KL {kl} coef {out['kl_coef']}"] if out["kl_kind"] else []) +
+                            ([f"entropy bonus coef {out['ent_coef']} (entropy written per token)"]
+                             if out["ent_coef"] else []) +
+                            ([f"aggregation {agg_name}"] if out["agg"] != _lib.AGG_TOKEN_MEAN else []))
+    return out
+
+
 def lmhead_chunks(V):
     """Vocabulary chunks of the LM-head backward: ceil(V/256) tiles in chunks of at most 66."""
     tiles = -(-V // 256)
@@ -465,20 +508,42 @@ def measure_lmhead(args, device, rank=0, local=0, with_e2e=True, with_cpu=True):
     stream = torch.cuda.current_stream(device)
     N = wl.n_valid
     call_evs = []
+    # the training step's regularisers and loss aggregation, as for the row-pass workloads (the
+    # pi_old pass takes neither); the aggregation's grad scale, weights and divisor come from
+    # grpo_plan_token_weights over the step's rows
+    lt = cli_terms(args)
+    gs, divisor, w_tok = 1.0 / max(N, 1), -1, None
+    if lt["agg"] != _lib.AGG_TOKEN_MEAN:
+        div, w, sc = _lib.grpo_plan_token_weights({"n_steps": 1, "step_in_row_off": [0, len(wl.row_len)]},
+                                                  wl.row_len, wl.row_valid, lt["agg"], want_scale=True)
+        gs, divisor = float(sc[0]), int(div[0])
+        w_tok = t(w) if lt["agg"] == _lib.AGG_SEQ_MEAN_TOKEN_MEAN else None
+    terms = None
 
     def step(grads=True, old=None, w=ws, evs=None):
         _lib.grpo_group_advantage(rewards, wl.group_size, 1e-6, True, adv_r, row_rollout, row_tok_off, adv)
         if evs is not None:
             evs.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
             evs[-1][0].record(stream)
-        _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, target, old, adv, mask, wl.eps, 1.0 / max(N, 1),
-                                      d_h if grads else None, dW if grads else None, loss, logp, acc, w)
+        tm = terms if grads else None
+        _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, target, old, adv, mask, wl.eps, gs if grads else 1.0 / max(N, 1),
+                                      d_h if grads else None, dW if grads else None, loss, logp, acc, w, terms=tm)
         if evs is not None:
             evs[-1][1].record(stream)
-        _lib.grpo_finish_step(acc, loss, expected_N=N, sync=False)
+        if grads and (w_tok is not None or divisor >= 0):
+            _lib.grpo_finish_step_ex(acc, loss, w_tok=w_tok, divisor=divisor, expected_N=N, sync=False)
+        else:
+            _lib.grpo_finish_step(acc, loss, expected_N=N, sync=False)
 
     step(grads=False)  # pi_old by the ahead pass, then seeded noise
     old = logp + t(wl.old_noise)
+    if lt["kl_kind"] or lt["ent_coef"] or w_tok is not None:
+        terms = {"kl_kind": lt["kl_kind"], "kl_coef": lt["kl_coef"], "ent_coef": lt["ent_coef"], "w_tok": w_tok}
+        if lt["kl_kind"]:  # a reference policy drawn like pi_old: the policy's log-probs plus noise
+            noise = np.random.default_rng(wl.seed + 1).normal(0.0, 0.1, T).astype(np.float32)
+            terms["ref_logp"] = logp + t(noise)
+        if lt["ent_coef"]:
+            terms["entropy_tok"] = torch.empty(T, dtype=torch.float32, device=device)
     torch.cuda.synchronize(device)
     # the clock sampler first, then the warm-up steps right before the timed ones (no idle gap
     # in which the power-capped GPU could recover before the timed region)
@@ -505,15 +570,31 @@ def measure_lmhead(args, device, rank=0, local=0, with_e2e=True, with_cpu=True):
     fwd_s = f0.elapsed_time(f1) / 1e3 / args.steps
     clk = clocks.stop()
 
-    e2e = measure_lmhead_e2e(args, wl, device, stream, h, Wt, target, mask, rewards, old, adv_r, adv, row_rollout,
-                             row_tok_off, d_h, dW, loss, logp, acc, ws, res) if with_e2e else None
+    # the e2e step: the same call on an input set that comes up from pinned host memory
+    dev_in = {"h": h, "Wt": Wt, "target": target, "mask": mask, "rewards": rewards, "old": old}
+    if terms is not None and terms.get("ref_logp") is not None:
+        dev_in["ref"] = terms["ref_logp"]
+    if w_tok is not None:
+        dev_in["w_tok"] = w_tok
+
+    def train_call(s):
+        _lib.grpo_group_advantage(s["rewards"], wl.group_size, 1e-6, True, adv_r, row_rollout, row_tok_off, adv)
+        tm = None if terms is None else dict(terms, ref_logp=s.get("ref"), w_tok=s.get("w_tok"))
+        _lib.grpo_lmhead_loss_fwd_bwd(s["h"], s["Wt"], s["target"], s["old"], adv, s["mask"], wl.eps, gs,
+                                      d_h, dW, loss, logp, acc, ws, terms=tm)
+        if w_tok is not None or divisor >= 0:
+            _lib.grpo_finish_step_ex(acc, loss, w_tok=s.get("w_tok"), divisor=divisor, expected_N=N, sync=False)
+        else:
+            _lib.grpo_finish_step(acc, loss, expected_N=N, sync=False)
+
+    e2e = measure_lmhead_e2e(args, wl, device, stream, dev_in, train_call, acc, res) if with_e2e else None
     flops = 6.0 * T * V * Hd
     peak, kind = bf16_peak(sustained=True)
     line = {
         "metric": LMHEAD_METRIC,
         "value": N / full_s, "unit": UNIT, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": 1e3 * full_s, "dtype": "bf16",
-        "config": lmhead_config(wl),
+        "config": dict(lmhead_config(wl), **({"terms": lt["text"]} if lt["text"] else {})),
         "workspace_gb": ws.numel() / 1e9,
         "roofline": {"bound": "tensor", "achieved": flops / call_s / 1e12, "peak": peak, "unit": "TFLOP/s",
                      "frac": flops / call_s / 1e12 / peak, "peak_source": f"{kind} bf16_tflops_sustained",
@@ -543,19 +624,17 @@ def measure_lmhead(args, device, rank=0, local=0, with_e2e=True, with_cpu=True):
     return line
 
 
-def measure_lmhead_e2e(args, wl, device, stream, h, Wt, target, mask, rewards, old, adv_r, adv, row_rollout,
-                       row_tok_off, d_h, dW, loss, logp, acc, ws, ref_res):
+def measure_lmhead_e2e(args, wl, device, stream, dev_in, train_call, acc, ref_res):
     """The LM-head step through the public API with every step's inputs (hidden states, weights,
-    side arrays) starting in pinned host memory: copied up on a copy stream into one of two
-    device input sets, the next step's copy overlapping this step's compute (the first step's
-    copy does not overlap); the step result is read back every step."""
+    side arrays, the regularisers' per-token inputs) starting in pinned host memory: copied up
+    on a copy stream into one of two device input sets, the next step's copy overlapping this
+    step's compute (the first step's copy does not overlap); ``train_call(set)`` runs the
+    step's calls on a set; the step result is read back every step."""
     import torch
     from rl_post_token_gb300 import _lib
 
     N = wl.n_valid
-    host = {"h": h.cpu().pin_memory(), "Wt": Wt.cpu().pin_memory(), "target": target.cpu().pin_memory(),
-            "mask": mask.cpu().pin_memory(), "rewards": rewards.cpu().pin_memory(), "old": old.cpu().pin_memory()}
-    dev_in = {"h": h, "Wt": Wt, "target": target, "mask": mask, "rewards": rewards, "old": old}
+    host = {k: v.cpu().pin_memory() for k, v in dev_in.items()}
     sets = [dev_in, {k: torch.empty_like(v) for k, v in dev_in.items()}]
     host_res = torch.empty(64, dtype=torch.uint8, pin_memory=True)
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
@@ -580,10 +659,7 @@ def measure_lmhead_e2e(args, wl, device, stream, h, Wt, target, mask, rewards, o
             upload(k + 1)
         s = sets[k % 2]
         stream.wait_event(copied[k % 2])
-        _lib.grpo_group_advantage(s["rewards"], wl.group_size, 1e-6, True, adv_r, row_rollout, row_tok_off, adv)
-        _lib.grpo_lmhead_loss_fwd_bwd(s["h"], s["Wt"], s["target"], s["old"], adv, s["mask"], wl.eps,
-                                      1.0 / max(N, 1), d_h, dW, loss, logp, acc, ws)
-        _lib.grpo_finish_step(acc, loss, expected_N=N, sync=False)
+        train_call(s)
         used[k % 2].record(stream)
         host_res.copy_(acc[64:128], non_blocking=True)
         stream.synchronize()
@@ -704,14 +780,9 @@ def run_gb300(args):
     if args.rows and args.workload == "qwen_step":
         ov.update(mini=args.rows, micro=args.rows)
     wl = W.make_workload(args.workload, seed=rank, **ov)
-    kl_kind = {"none": 0, "k1": _lib.KL_K1, "k3": _lib.KL_K3}[args.kl]
-    agg = {"token-mean": _lib.AGG_TOKEN_MEAN, "seq-mean-token-sum": _lib.AGG_SEQ_MEAN_TOKEN_SUM,
-           "seq-mean-token-mean": _lib.AGG_SEQ_MEAN_TOKEN_MEAN}[args.agg]
-    batch = Batch(wl, device, kl_kind=kl_kind, kl_coef=args.kl_coef, ent_coef=args.ent_coef, agg=agg)
-    terms_text = ", ".join(([f"KL {args.kl} coef {args.kl_coef}"] if kl_kind else []) +
-                           ([f"entropy bonus coef {args.ent_coef} (entropy written per token)"]
-                            if args.ent_coef else []) +
-                           ([f"aggregation {args.agg}"] if agg != _lib.AGG_TOKEN_MEAN else []))
+    lt = cli_terms(args)
+    batch = Batch(wl, device, kl_kind=lt["kl_kind"], kl_coef=lt["kl_coef"], ent_coef=lt["ent_coef"], agg=lt["agg"])
+    terms_text = lt["text"]
     stream = torch.cuda.current_stream(device)
     tm = time_rowpass(args, batch, device, stream, world, local, f"clocks_rank{rank}.csv")
     # the committed capture is of the default workload's instance without terms
