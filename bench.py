@@ -482,9 +482,10 @@ def run_lmhead(args):
 
 def measure_lmhead(args, device, rank=0, local=0, with_e2e=True, with_cpu=True):
     """Fused LM-head step: advantage, one grpo_lmhead_loss_fwd_bwd call (forward, dlogits, d_h
-    and dW, no [T, V] matrix stored: the backward recomputes each vocabulary chunk's logits),
-    the finish. Roofline: tensor, 6*T*V*H algorithmic flops (forward GEMM and the two backward
-    GEMMs; the recompute's extra 2*T*V*H is not credited) over the LM-head call's time, timed
+    and dW, no [T, V] matrix stored: the backward recomputes each vocabulary chunk's logits for
+    the tokens with a nonzero gradient), the finish. Roofline: tensor, 2*T*V*H + 4*T_live*V*H
+    algorithmic flops (the forward GEMM over every token, the two backward GEMMs over the live
+    ones; the recompute's 2*T_live*V*H is not credited) over the LM-head call's time, timed
     with CUDA events around each call on its stream."""
     import torch
     from rl_post_token_gb300 import _lib
@@ -588,7 +589,17 @@ def measure_lmhead(args, device, rank=0, local=0, with_e2e=True, with_cpu=True):
             _lib.grpo_finish_step(acc, loss, expected_N=N, sync=False)
 
     e2e = measure_lmhead_e2e(args, wl, device, stream, dev_in, train_call, acc, res) if with_e2e else None
-    flops = 6.0 * T * V * Hd
+    # the backward's live tokens (a nonzero dlogits row): with the KL term or the entropy bonus
+    # every valid token; otherwise the valid tokens with a nonzero advantage that the clip did
+    # not stop (a clipped token has a nonzero advantage by definition)
+    if terms is not None and (terms["kl_kind"] or terms["ent_coef"]):
+        t_live = N
+    else:
+        t_live = int(((adv != 0) & (mask != 0)).sum().item()) - int(res["n_clipped"])
+    # credited: the forward over every token and the two backward products over the live ones
+    # (a dead token's products are exact zeros); executed adds the live tokens' recompute
+    flops = (2.0 * T + 4.0 * t_live) * V * Hd
+    executed = (2.0 * T + 6.0 * t_live) * V * Hd
     peak, kind = bf16_peak(sustained=True)
     line = {
         "metric": LMHEAD_METRIC,
@@ -601,14 +612,18 @@ def measure_lmhead(args, device, rank=0, local=0, with_e2e=True, with_cpu=True):
                      "kernel": "grpo_lmhead_loss_fwd_bwd (its GEMM launches and the per-token reduce), CUDA events "
                                "around each call",
                      "ms_per_call": 1e3 * call_s, "flops_per_call": flops,
-                     "executed_flops_per_call": 8.0 * T * V * Hd,
-                     "executed_tflops": 8.0 * T * V * Hd / call_s / 1e12, "traffic": None},
+                     "flops_what": "2*T*V*H (forward, every token) + 4*T_live*V*H (d_h and dW over the "
+                                   "tokens with a nonzero dlogits row)",
+                     "live_tokens": t_live, "dense_flops_per_call": 6.0 * T * V * Hd,
+                     "executed_flops_per_call": executed,
+                     "executed_tflops": executed / call_s / 1e12, "traffic": None},
         "forward_only": {"ms": 1e3 * fwd_s, "tflops": 2.0 * T * V * Hd / fwd_s / 1e12,
                          "what": "softmax-partials GEMM pass + per-token reduce (2*T*V*H flops)"},
         "step_result": {k: res[k] for k in ("loss", "n_valid", "clipfrac", "status")},
-        # per step: the advantage (2), pass A and the per-token reduce (2), per vocabulary chunk
-        # the dlogits recompute, the d_h and the dW GEMM (3), the finish (1)
-        "gpu_launches": (5 + 3 * lmhead_chunks(V)) * args.steps,
+        # per step: the advantage (2), pass A and the per-token reduce (2), the live-token
+        # partition and gather (2), per vocabulary chunk the dlogits recompute, the d_h and the
+        # dW GEMM (3), the finish (1)
+        "gpu_launches": (7 + 3 * lmhead_chunks(V)) * args.steps,
     }
     if e2e is not None:
         line["e2e"] = e2e

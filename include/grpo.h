@@ -443,8 +443,9 @@ GRPO_API int grpo_window_rollup(const grpo_window* w, double* loss, int64_t* den
  * buffers [T, 256 * chunk_tiles], where the ceil(V/256) vocabulary tiles are split into
  * ceil(tiles/66) chunks of equal width (V = 151936: 9 chunks of 66 tiles, 16896 columns), and,
  * for the entropy bonus of grpo_lmhead_loss_fwd_bwd_ex, a third float32 partial per tile and
- * token and two float32 coefficients per token. Each part is rounded up to 256 bytes. 0 on bad
- * sizes. */
+ * token and two float32 coefficients per token, then the backward's token partition (an int32
+ * per token), its live count (one int32) and the live tokens' hidden states gathered into a
+ * bf16 [T, H] buffer. Each part is rounded up to 256 bytes. 0 on bad sizes. */
 GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H);
 
 /* The same loss with the logits produced on the tensor cores: z = h W^T, computed tile by tile
@@ -454,10 +455,15 @@ GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H);
  * paired MMAs, 256 x 256 tiles, bf16 operands, float32 accumulation).
  *  - Forward: LSE, log-prob, ratio, clipped surrogate, per-token loss (as
  *    grpo_logprob_loss_fwd_bwd, one token per row of h).
- *  - Backward (d_h or dW non-NULL): per vocabulary chunk, the chunk's logits are recomputed
- *    and its bf16 dlogits written to one of the two workspace chunk buffers; then d_h (+)=
- *    dlogits W_c, accumulated over the chunks in chunk order, and dW_c = dlogits^T h. The
- *    recompute makes the step 8 T V H flops (6 T V H without it). d_h and dW run on a second
+ *  - Backward (d_h or dW non-NULL): over the live tokens only, those whose dlogits row is not
+ *    all zero (a nonzero gradient coefficient, or with the entropy bonus a nonzero entropy
+ *    term; a masked, clipped or zero-advantage token without regularisers has a zero row and
+ *    its d_h row is written as zeros). Their hidden states are gathered in token order into the
+ *    workspace; the live count stays on the device (no host synchronisation). Per vocabulary
+ *    chunk, the chunk's logits of the live tokens are recomputed and their bf16 dlogits written
+ *    to one of the two workspace chunk buffers; then d_h (+)= dlogits W_c, accumulated over the
+ *    chunks in chunk order, and dW_c = dlogits^T h. The recompute makes the step
+ *    2 T V H + 6 T_live V H flops (T_live = T when every token has a gradient). d_h and dW run on a second
  *    stream of the library's (one per device, created by the first call that needs it, which
  *    should come before any stream capture), so the next chunk's recompute runs beside them;
  *    the call's work on both streams is done when `stream` reaches the call's end.
@@ -467,7 +473,8 @@ GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H);
  *  W          device bf16 [V, H] row-major, 16-byte aligned
  *  target, old_logp (or NULL), adv_tok, mask   device, indexed by token row
  *  grad_scale 1/max(N,1) (or 1 with a deferred finish on d_h / dW)
- *  d_h        device float [T, H] or NULL; dW device float [V, H] or NULL (both NULL: forward only)
+ *  d_h        device float [T, H] or NULL; dW device float [V, H] or NULL (both NULL: forward
+ *             only); each 16-byte aligned
  *  flags      0: dW = dlogits^T h of this call's tokens; GRPO_LMHEAD_DW_ACCUMULATE: dW += it, so
  *             the micro-batches of one optimizer step (one call each, grad_scale the step's
  *             1/max(N,1), or 1 with a deferred finish over d_h and dW) sum into one dW, each

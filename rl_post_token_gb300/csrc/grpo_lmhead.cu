@@ -147,6 +147,80 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(ReduceArgs a)
   }
 }
 
+// The backward's live tokens: those whose dlogits row is not all zero (a nonzero gradient
+// coefficient; with the entropy bonus, a nonzero ea or eb). A token with a zero coefficient
+// (masked, zero advantage, clipped, and no regulariser) contributes exact zeros to d_h and dW,
+// so the backward's three GEMMs run over the live tokens only. One block writes a stable
+// partition of the token indices, the live ones first, in token order, and the live count.
+constexpr int kPartThreads = 1024;
+
+__global__ void __launch_bounds__(kPartThreads) partition_kernel(int64_t T, const float* coef, const float* ea,
+                                                                 const float* eb, int32_t* idx, int32_t* live_n) {
+  __shared__ int32_t warp_sum[kPartThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int64_t per = (T + kPartThreads - 1) / kPartThreads;
+  const int64_t b = (int64_t)tid * per, e = b + per < T ? b + per : T;
+  auto live = [&](int64_t t) { return ea ? (ea[t] != 0.f || eb[t] != 0.f) : coef[t] != 0.f; };
+  int32_t c = 0;
+  for (int64_t t = b; t < e; ++t) c += live(t) ? 1 : 0;
+  // exclusive scan of the per-thread counts: within the warp, then over the warp totals
+  int32_t x = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sum[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int32_t v = warp_sum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    warp_sum[lane] = v;  // inclusive over warps
+  }
+  __syncthreads();
+  const int32_t total = warp_sum[kPartThreads / 32 - 1];
+  int32_t pos = (w > 0 ? warp_sum[w - 1] : 0) + x - c;  // live tokens before this thread's range
+  for (int64_t t = b; t < e; ++t) {
+    if (live(t))
+      idx[pos++] = (int32_t)t;
+    else
+      idx[total + (t - pos)] = (int32_t)t;  // t - pos = dead tokens before t
+  }
+  if (tid == 0) *live_n = total;
+}
+
+// Row i of the compact order, one warp per row: a live token's hidden state is copied into the
+// compact buffer; the rows from the live count to the padded count are zeroed (dW reduces over
+// them); a dead token's d_h row is zeroed (no GEMM writes it).
+__global__ void __launch_bounds__(256) gather_kernel(int64_t T, int H, const __nv_bfloat16* h, const int32_t* idx,
+                                                     const int32_t* live_n, __nv_bfloat16* h_live, float* d_h) {
+  const int64_t nl = *live_n;
+  const int64_t pad = live_pad(nl, T) < T ? live_pad(nl, T) : T;
+  const int lane = threadIdx.x & 31;
+  const int nvec = H >> 3;  // 16-byte vectors of a bf16 row (H is a multiple of 64)
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+  for (int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < T; i += warps) {
+    const int64_t tok = idx[i];
+    uint4* dst = reinterpret_cast<uint4*>(h_live) + i * nvec;
+    if (i < nl) {
+      const uint4* src = reinterpret_cast<const uint4*>(h) + tok * nvec;
+      for (int k = lane; k < nvec; k += 32) dst[k] = src[k];
+      continue;
+    }
+    if (i < pad)
+      for (int k = lane; k < nvec; k += 32) dst[k] = z4;
+    if (d_h) {  // a float row is two 16-byte vectors per bf16 vector
+      uint4* row = reinterpret_cast<uint4*>(d_h) + tok * (2 * nvec);
+      for (int k = lane; k < 2 * nvec; k += 32) row[k] = z4;
+    }
+  }
+}
+
 // ---- host -------------------------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -284,14 +358,15 @@ namespace {
 constexpr int kMaxChunkTiles = 66;
 
 struct WsLayout {
-  // dz, dz2: the two dlogits chunk buffers; part_s2, ea, eb (last, so that the forward pass's
-  // prefix is unchanged): the entropy bonus's third partial and its per-token coefficients
-  size_t part_m, part_s, zy, lse2, coef, dz, dz2, part_s2, ea, eb, total;
+  // dz, dz2: the two dlogits chunk buffers; then (after the forward pass's prefix) part_s2,
+  // ea, eb: the entropy bonus's third partial and its per-token coefficients; idx, live_n,
+  // h_live: the backward's token partition, live count and compact hidden states
+  size_t part_m, part_s, zy, lse2, coef, dz, dz2, part_s2, ea, eb, idx, live_n, h_live, total;
   int n_col_tiles, chunk_tiles;
   int64_t vchunk;  // columns of the dlogits chunk buffer
 };
 
-WsLayout ws_layout(int64_t T, int64_t V) {
+WsLayout ws_layout(int64_t T, int64_t V, int64_t H) {
   WsLayout w{};
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   w.n_col_tiles = (int)((V + BN - 1) / BN);
@@ -309,6 +384,9 @@ WsLayout ws_layout(int64_t T, int64_t V) {
   w.part_s2 = off; off += up((size_t)w.n_col_tiles * T * 4);
   w.ea = off; off += up((size_t)T * 4);
   w.eb = off; off += up((size_t)T * 4);
+  w.idx = off; off += up((size_t)T * 4);
+  w.live_n = off; off += up(4);
+  w.h_live = off; off += up((size_t)T * H * 2);
   w.total = off;
   return w;
 }
@@ -316,7 +394,10 @@ WsLayout ws_layout(int64_t T, int64_t V) {
 struct Scratch {
   float *part_m, *part_s, *zy, *lse2, *coef;
   __nv_bfloat16* dz[2];
-  float *part_s2, *ea, *eb;  // NULL when the region lies past the scratch (the no-alloc forward)
+  // NULL when the region lies past the scratch (the no-alloc forward)
+  float *part_s2, *ea, *eb;
+  int32_t *idx, *live_n;
+  __nv_bfloat16* h_live;
 };
 
 // The regions of a workspace: all of them (full), or only the forward pass's prefix.
@@ -325,13 +406,16 @@ Scratch carve(void* base, const WsLayout& ws, bool full) {
   Scratch s{reinterpret_cast<float*>(b + ws.part_m), reinterpret_cast<float*>(b + ws.part_s),
             reinterpret_cast<float*>(b + ws.zy),     reinterpret_cast<float*>(b + ws.lse2),
             reinterpret_cast<float*>(b + ws.coef),   {nullptr, nullptr},
-            nullptr, nullptr, nullptr};
+            nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   if (full) {
     s.dz[0] = reinterpret_cast<__nv_bfloat16*>(b + ws.dz);
     s.dz[1] = reinterpret_cast<__nv_bfloat16*>(b + ws.dz2);
     s.part_s2 = reinterpret_cast<float*>(b + ws.part_s2);
     s.ea = reinterpret_cast<float*>(b + ws.ea);
     s.eb = reinterpret_cast<float*>(b + ws.eb);
+    s.idx = reinterpret_cast<int32_t*>(b + ws.idx);
+    s.live_n = reinterpret_cast<int32_t*>(b + ws.live_n);
+    s.h_live = reinterpret_cast<__nv_bfloat16*>(b + ws.h_live);
   }
   return s;
 }
@@ -456,7 +540,7 @@ Overlap* overlap_state(std::unique_lock<std::mutex>& lock) {
 
 extern "C" GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H) {
   if (T <= 0 || V <= 0 || H <= 0) return 0;
-  return ws_layout(T, V).total;
+  return ws_layout(T, V, H).total;
 }
 
 extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd_ex(const void* h, const void* W, int64_t T, int64_t V,
@@ -476,7 +560,8 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd_ex(const void* h, const void* W
   if (arc != GRPO_OK || T == 0) return arc;
   if (flags & ~(uint32_t)GRPO_LMHEAD_DW_ACCUMULATE) return GRPO_ERR_INVALID;
   if (!workspace || ((uintptr_t)workspace & 255u)) return GRPO_ERR_INVALID;
-  const WsLayout ws = ws_layout(T, V);
+  if (((uintptr_t)d_h | (uintptr_t)dW) & 15u) return GRPO_ERR_INVALID;  // 16-byte row stores
+  const WsLayout ws = ws_layout(T, V, H);
   if (workspace_bytes < ws.total) return GRPO_ERR_CAPACITY;
   const cudaStream_t st = as_stream(stream);
   const Scratch sc = carve(workspace, ws, true);
@@ -496,6 +581,17 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd_ex(const void* h, const void* W
   Overlap* ov = (overlap_on() && n_chunks > 1) ? overlap_state(ov_lock) : nullptr;
   const cudaStream_t bst = ov ? ov->aux : st;  // the stream of d_h and dW
   const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
+  // the live tokens in a compact order, their hidden states gathered; the dead tokens' d_h rows
+  // zeroed
+  partition_kernel<<<1, kPartThreads, 0, st>>>(T, sc.coef, ent_grad ? sc.ea : nullptr, ent_grad ? sc.eb : nullptr,
+                                                sc.idx, sc.live_n);
+  GRPO_CUDA_TRY(cudaGetLastError());
+  {
+    const int64_t blocks = std::min<int64_t>((T + 7) / 8, (int64_t)sm_count() * 16);
+    gather_kernel<<<(unsigned)blocks, 256, 0, st>>>(T, (int)H, static_cast<const __nv_bfloat16*>(h), sc.idx, sc.live_n,
+                                                    sc.h_live, d_h);
+    GRPO_CUDA_TRY(cudaGetLastError());
+  }
   auto backward = [&]() -> int {
   for (int ct0 = 0, c = 0; ct0 < ws.n_col_tiles; ct0 += ws.chunk_tiles, ++c) {
     const int nct = std::min(ws.chunk_tiles, ws.n_col_tiles - ct0);
@@ -518,7 +614,10 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd_ex(const void* h, const void* W
     g.acc = acc;
     g.col_tile0 = ct0;
     g.n_n = nct;
-    rc = logits_gemm<EPI_DLOGITS>(cg, h, W, T, V, H, g, st, vc);
+    g.live_n = sc.live_n;  // compact rows; zero dlogits rows up to the padded live count
+    g.row_idx = sc.idx;
+    g.live_mode = LIVE_ROWS_PADDED;
+    rc = logits_gemm<EPI_DLOGITS>(cg, sc.h_live, W, T, V, H, g, st, vc);
     if (rc != GRPO_OK) return rc;
     if (ov) {
       GRPO_CUDA_TRY(cudaEventRecord(ov->dz_ready, st));
@@ -526,10 +625,13 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd_ex(const void* h, const void* W
     }
     CUtensorMap ma, mb;
     if (d_h) {
-      // d_h[T, H] (+)= dz_c[T, vc] W_c[vc, H]
+      // d_h[live rows, H] (+)= dz_c[live rows, vc] W_c[vc, H], each row stored to its token's row
       if (!map_k(&ma, dzb, T, vc, ws.vchunk, BM) || !map_mn(&mb, Wb + v0 * H, vc, H, H))
         return GRPO_ERR_UNSUPPORTED;
       GemmArgs b{};
+      b.live_n = sc.live_n;
+      b.row_idx = sc.idx;
+      b.live_mode = LIVE_ROWS;
       b.M = T;
       b.N = H;
       b.K = vc;
@@ -543,9 +645,11 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd_ex(const void* h, const void* W
       if (rc != GRPO_OK) return rc;
     }
     if (dW) {
-      // dW_c[vc, H] = dz_c^T[vc, T] h[T, H]
-      if (!map_mn(&ma, dzb, T, vc, ws.vchunk) || !map_mn(&mb, h, T, H, H)) return GRPO_ERR_UNSUPPORTED;
+      // dW_c[vc, H] = dz_c^T[vc, live] h_live[live, H], reduced over the padded live count
+      if (!map_mn(&ma, dzb, T, vc, ws.vchunk) || !map_mn(&mb, sc.h_live, T, H, H)) return GRPO_ERR_UNSUPPORTED;
       GemmArgs b{};
+      b.live_n = sc.live_n;
+      b.live_mode = LIVE_K;
       b.M = vc;
       b.N = H;
       b.K = T;
@@ -668,7 +772,7 @@ extern "C" GRPO_API int grpo_lmhead_forward_noalloc(const void* h, const void* W
   const int arc = check_args(h, W, T, V, H, target, adv_tok, mask, loss_tok, acc);
   if (arc != GRPO_OK || T == 0) return arc;
   // the forward pass uses the workspace layout up to (not including) the dlogits chunk
-  const WsLayout ws = ws_layout(T, V);
+  const WsLayout ws = ws_layout(T, V, H);
   if (ws.dz > kNoAllocScratchBytes) return GRPO_ERR_CAPACITY;
   void* scratch = nullptr;
   const int rc = noalloc_setup(&scratch);

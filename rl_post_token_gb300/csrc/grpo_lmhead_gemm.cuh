@@ -242,13 +242,35 @@ struct GemmArgs {
   int64_t ldc;
   int accumulate;
   grpo_step_acc* acc;
+  // The backward over the live tokens only (those whose dlogits row is not all zero), in a
+  // compact order that the partition kernel wrote earlier in stream order: *live_n of them,
+  // row i of the compact order being token row_idx[i]. live_mode says which extent follows
+  // from the device count (M and K above then give the allocated token rows, T):
+  //   LIVE_ROWS_PADDED  rows = live tokens, and the epilogue writes zero dlogits rows up to the
+  //                     padded count (live_pad below), so that dW's reduction over the padded
+  //                     count reads zeros past the live rows;
+  //   LIVE_ROWS         rows = live tokens (d_h: rows scattered to C[row_idx[i]]);
+  //   LIVE_K            reduction length = the padded count (dW over the compact tokens).
+  const int32_t* live_n;
+  const int32_t* row_idx;
+  int live_mode;
 };
 
+enum { LIVE_NONE = 0, LIVE_ROWS_PADDED = 1, LIVE_ROWS = 2, LIVE_K = 3 };
+
+// The padded live count: a multiple of the K block (at least one block, so that dW always
+// reduces over at least one block of zeros), at most the allocated rows rounded up.
+__device__ __forceinline__ int64_t live_pad(int64_t n, int64_t rows) {
+  const int64_t p = n < BK ? (int64_t)BK : (n + BK - 1) / BK * BK;
+  const int64_t cap = (rows + BK - 1) / BK * BK;
+  return p < cap ? p : cap;
+}
+
 // Work unit t -> (unit along M, tile along N).
-__device__ __forceinline__ void unit_coords(const GemmArgs& g, int t, int& mu, int& nu) {
+__device__ __forceinline__ void unit_coords(const GemmArgs& g, int n_m, int t, int& mu, int& nu) {
   if (g.m_fast) {
-    mu = t % g.n_m;
-    nu = t / g.n_m;
+    mu = t % n_m;
+    nu = t / n_m;
   } else {
     nu = t % g.n_n;
     mu = t / g.n_n;
@@ -328,17 +350,19 @@ __device__ __forceinline__ void epi_partials_ent(const GemmArgs& g, uint32_t tad
 // warp's 16-byte writes) and written by one TMA store through map_c, whose extents (the chunk's
 // vocabulary columns, T rows) clip the vocabulary tail and the rows past T.
 __device__ __forceinline__ void epi_dlogits(const GemmArgs& g, const CUtensorMap* map_c, uint32_t taddr,
-                                            int64_t row, bool rok, int ct, int64_t warp_row0, uint32_t stage_buf,
-                                            int lane) {
+                                            int64_t row, bool rok, int ct, int64_t warp_row0, int64_t rows_store,
+                                            uint32_t stage_buf, int lane) {
   const int64_t c0 = (int64_t)ct * BN;
-  const int32_t y = rok ? g.target[row] : -1;
-  const float cf = rok ? g.coef[row] : 0.f;
-  const float l2 = rok ? g.lse2[row] : 0.f;
+  // the token of this accumulator row (the compact order's, in the live-token backward)
+  const int64_t tok = (rok && g.row_idx) ? (int64_t)g.row_idx[row] : row;
+  const int32_t y = rok ? g.target[tok] : -1;
+  const float cf = rok ? g.coef[tok] : 0.f;
+  const float l2 = rok ? g.lse2[tok] : 0.f;
   const float cexp = l2 - log2f(fabsf(cf));
   const uint32_t sgn = cf < 0.f ? 0x80008000u : 0u;
   // with the entropy bonus: dz = p (ea + eb z); ea = eb = 0 for masked tokens
   const bool ent = g.eb != nullptr;
-  const float ea = (ent && rok) ? g.ea[row] : 0.f, eb = (ent && rok) ? g.eb[row] : 0.f;
+  const float ea = (ent && rok) ? g.ea[tok] : 0.f, eb = (ent && rok) ? g.eb[tok] : 0.f;
   const bool live = ent ? (ea != 0.f || eb != 0.f) : cf != 0.f;
   const uint32_t sw = (uint32_t)((lane >> 1) & 3);
 #pragma unroll 1
@@ -346,8 +370,9 @@ __device__ __forceinline__ void epi_dlogits(const GemmArgs& g, const CUtensorMap
     float v[32];
     tmem_ld32(taddr + c * 32, v);
     const int64_t cb = c0 + c * 32;
-    // warp-uniform: the rest of the tile lies past the vocabulary, or all 32 rows past T
-    if (cb >= g.V || warp_row0 >= g.M) continue;
+    // warp-uniform: the rest of the tile lies past the vocabulary, or all 32 rows past the
+    // rows to be written (T, or the padded live count; rows in between get zeros)
+    if (cb >= g.V || warp_row0 >= rows_store) continue;
     uint32_t w[16];
     if (live) {
       float zyv = 0.f;
@@ -406,7 +431,9 @@ __device__ __forceinline__ void epi_dlogits(const GemmArgs& g, const CUtensorMap
 // float32 output tile: C[row][n0 .. n0 + 256) = (accumulate ? C : 0) + D, columns past N skipped
 // (N is a multiple of 64, so a 32-column group is wholly inside or outside).
 __device__ __forceinline__ void epi_store_f32(const GemmArgs& g, uint32_t taddr, int64_t row, bool rok, int64_t n0) {
-  float* crow = g.C + row * g.ldc;
+  // d_h over the live tokens: compact row -> the token's row of C
+  const int64_t crow_i = (rok && g.row_idx) ? (int64_t)g.row_idx[row] : row;
+  float* crow = g.C + crow_i * g.ldc;
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     float v[32];
@@ -469,10 +496,25 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
   fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int n_units = g.n_m * g.n_n;
+  // extents: the launch's, or, in the live-token backward, from the device count (written by
+  // an earlier kernel in stream order; every thread reads the same value)
+  int64_t M = g.M, rows_store = g.M, K = g.K;
+  int n_m = g.n_m;
+  if (g.live_mode != LIVE_NONE) {
+    const int64_t nl = *g.live_n;
+    if (g.live_mode == LIVE_K) {
+      K = live_pad(nl, g.K);
+    } else {
+      M = nl;
+      rows_store = g.live_mode == LIVE_ROWS_PADDED ? live_pad(nl, g.M) : nl;
+      if (rows_store > g.M) rows_store = g.M;
+      n_m = (int)((rows_store + BM * CG - 1) / (BM * CG));
+    }
+  }
+  const int n_units = n_m * g.n_n;
   const int first = CG == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int stride = CG == 2 ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  const int KB = (int)((g.K + BK - 1) / BK);
+  const int KB = (int)((K + BK - 1) / BK);
 
   if (warp == 0) {
     // ---- TMA producer: this CTA's A rows and B rows of every stage ----
@@ -481,7 +523,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
       uint32_t stage = 0, phase = 0;
       for (int t = first; t < n_units; t += stride) {
         int mu, nu;
-        unit_coords(g, t, mu, nu);
+        unit_coords(g, n_m, t, mu, nu);
         const int a_row = mu * BM * CG + (int)rank * BM;
         const int b_row = (g.col_tile0 + nu) * BN + (int)rank * S::B_ROWS;
         for (int kb = 0; kb < KB; ++kb) {
@@ -556,18 +598,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
     uint32_t ab = 0, aphase = 0;
     for (int t = first; t < n_units; t += stride) {
       int mu, nu;
-      unit_coords(g, t, mu, nu);
+      unit_coords(g, n_m, t, mu, nu);
       mbar_wait_bounded(&tfull[ab], aphase, s_abort);
       fence_after();
       const int64_t row = (int64_t)mu * BM * CG + (int64_t)rank * BM + trow;
-      const bool rok = row < g.M;
+      const bool rok = row < M;
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + ab * BN;
       if constexpr (EPI == EPI_PARTIALS)
         epi_partials(g, taddr, row, rok, g.col_tile0 + nu);
       else if constexpr (EPI == EPI_PARTIALS_ENT)
         epi_partials_ent(g, taddr, row, rok, g.col_tile0 + nu);
       else if constexpr (EPI == EPI_DLOGITS)
-        epi_dlogits(g, &map_c, taddr, row, rok, g.col_tile0 + nu, row - lane,
+        epi_dlogits(g, &map_c, taddr, row, rok, g.col_tile0 + nu, row - lane, rows_store,
                     epi_base + (uint32_t)quarter * 2u * EPI_BUF_BYTES, lane);
       else
         epi_store_f32(g, taddr, row, rok, (int64_t)nu * BN);

@@ -85,9 +85,9 @@ def test_host_entry_argument_checks(kw, code):
     assert _host(**kw) == code
 
 
-def _lm(T=256, V=1024, H=128, h=P, W=P, ws=P, ws_bytes=1 << 30, acc=P, target=P, flags=0):
+def _lm(T=256, V=1024, H=128, h=P, W=P, ws=P, ws_bytes=1 << 30, acc=P, target=P, flags=0, d_h=P, dW=P):
     return _lib.lib().grpo_lmhead_loss_fwd_bwd(h, W, T, V, H, target, None, P, P, C.c_float(0.2),
-                                               C.c_float(1.0), P, P, flags, P, None, acc, ws, ws_bytes, None)
+                                               C.c_float(1.0), d_h, dW, flags, P, None, acc, ws, ws_bytes, None)
 
 
 @pytest.mark.parametrize("kw, code", [
@@ -101,6 +101,8 @@ def _lm(T=256, V=1024, H=128, h=P, W=P, ws=P, ws_bytes=1 << 30, acc=P, target=P,
     (dict(W=P + 8), _lib.ERR_INVALID),
     (dict(ws=P + 16), _lib.ERR_INVALID),  # the workspace (GEMM scratch included) 256-byte aligned
     (dict(ws=None), _lib.ERR_INVALID),
+    (dict(d_h=P + 4), _lib.ERR_INVALID),  # the float32 outputs' rows are written 16 bytes at a time
+    (dict(dW=P + 8), _lib.ERR_INVALID),
     (dict(target=None), _lib.ERR_INVALID),
     (dict(T=2 ** 30), _lib.ERR_INVALID),
     (dict(T=0), _lib.OK),
@@ -123,11 +125,14 @@ def test_lmhead_workspace_sizes():
         nct = (V + 255) // 256
         # partials (two float arrays per tile and token), three per-token floats, two bf16
         # dlogits chunk buffers (the tiles split into ceil(tiles / 66) chunks of equal width),
-        # then the entropy's third partial per tile and token and two per-token floats
+        # then the entropy's third partial per tile and token and two per-token floats, then
+        # the backward's token partition (an int32 per token), its live count and the compact
+        # bf16 hidden states [T, H]
         n_chunks = -(-nct // 66)
         assert -(-nct // n_chunks) == chunk_tiles
         base = 2 * up(4 * nct * T) + 3 * up(4 * T)
-        assert plain == base + 2 * up(2 * T * 256 * chunk_tiles) + up(4 * nct * T) + 2 * up(4 * T)
+        assert plain == (base + 2 * up(2 * T * 256 * chunk_tiles) + up(4 * nct * T) + 2 * up(4 * T)
+                         + up(4 * T) + 256 + up(2 * T * H))
     for bad in [(0, 8, 64), (8, 0, 64), (8, 8, 0), (-1, 8, 64)]:
         assert _lib.grpo_lmhead_workspace_size(*bad) == 0
     assert _lib.lib().grpo_lmhead_forward_noalloc_max_scratch() == 16 << 20

@@ -482,3 +482,84 @@ def test_lmhead_terms_reject_bad_arguments():
     for bad in (dict(kl_kind=7), dict(kl_kind=1)):  # an unknown kind; KL without ref_logp
         with pytest.raises(_lib.GrpoError):
             _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, i, None, f, mk, 0.2, 1.0, None, None, f, None, acc, ws, terms=bad)
+
+
+# ---- the backward over the live tokens only ---------------------------------------------------
+# A token with a zero gradient coefficient (masked, zero advantage, clipped) has an all-zero
+# dlogits row; the backward's GEMMs run over the others, in a compact order whose count stays on
+# the device. These cases put the count at 0, 1, and just past tile and K-block boundaries.
+
+def _adv_with_live(T, live_rows, seed):
+    adv = np.zeros(T, np.float32)
+    adv[live_rows] = np.random.default_rng(seed).choice([-1.5, -0.5, 0.5, 1.5], len(live_rows))
+    return adv
+
+
+@pytest.mark.parametrize("n_live", [0, 1, 63, 65, 257])
+def test_lmhead_live_token_counts(cta_group, n_live):
+    # 600 tokens (ragged), V = 3000, H = 128; the live tokens spread over the call, every other
+    # token with a zero advantage; d_h and dW start as 7.0, so a row or entry that no kernel
+    # writes fails the comparison
+    T, V, Hd = 600, 3000, 128
+    live = np.sort(np.random.default_rng(n_live).choice(T, n_live, replace=False))
+    adv = _adv_with_live(T, live, seed=80 + n_live)
+    ref = _check(T, V, Hd, seed=80, adv=adv)
+    assert np.all(ref["d_h"][np.setdiff1d(np.arange(T), live)] == 0)
+    if n_live == 0:
+        assert np.all(ref["dW"] == 0)
+
+
+def test_lmhead_dead_tokens_leave_exact_zeros_and_accumulated_dw():
+    # every token dead: d_h is written as exact zeros, dW as zeros, and with accumulation dW
+    # keeps its bits
+    T, V, Hd = 300, 2000, 64
+    wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed=90, adv=np.zeros(T))
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    d_h = torch.full((T, Hd), 7.0, device=DEV)
+    dW = torch.randn((V, Hd), device=DEV)
+    dW0 = dW.clone()
+    loss = torch.empty(T, device=DEV)
+    logp = torch.empty(T, device=DEV)
+    acc = _lib.new_step_acc(DEV)
+    ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=DEV)
+    args = (h, Wt, t(wl.target), t(old_logp), t(a_tok), t(mask), wl.eps, 1.0 / T, d_h, dW, loss, logp, acc, ws)
+    _lib.grpo_lmhead_loss_fwd_bwd(*args, dw_accumulate=True)
+    torch.cuda.synchronize()
+    assert torch.equal(d_h, torch.zeros_like(d_h))
+    assert torch.equal(dW, dW0)
+    res = _lib.grpo_finish_step(acc, loss)
+    assert res["status"] == 0 and res["n_valid"] == int(mask.sum())
+    acc2 = _lib.new_step_acc(DEV)
+    _lib.grpo_lmhead_loss_fwd_bwd(*args[:12], acc2, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(dW, torch.zeros_like(dW))
+
+
+def test_lmhead_live_tokens_reuse_a_dirty_workspace():
+    # the compact hidden-state buffer and the dlogits chunks hold another call's values (and
+    # NaN bytes) when a call with fewer live tokens runs: the padded rows it reduces over must
+    # be its own zeros
+    T, V, Hd = 400, 3000, 128
+    ws = torch.full((_lib.grpo_lmhead_workspace_size(T, V, Hd),), 0xFF, dtype=torch.uint8, device=DEV)
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    outs = []
+    for n_live, seed in ((400, 91), (37, 92)):
+        live = np.arange(0, T, T // n_live)[:n_live] if n_live < T else np.arange(T)
+        adv = _adv_with_live(T, live, seed=seed)
+        wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed=93, adv=adv)
+        d_h = torch.full((T, Hd), 7.0, device=DEV)
+        dW = torch.full((V, Hd), 7.0, device=DEV)
+        loss = torch.empty(T, device=DEV)
+        logp = torch.empty(T, device=DEV)
+        acc = _lib.new_step_acc(DEV)
+        N = int(mask.sum())
+        _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, t(wl.target), t(old_logp), t(a_tok), t(mask), wl.eps, 1.0 / N,
+                                      d_h, dW, loss, logp, acc, ws)
+        torch.cuda.synchronize()
+        ref, tol_h, tol_w = _oracle_grad_tol(hb, wb, wl, mask, a_tok, old_logp, N)
+        assert not (np.abs(H.to_f64(d_h) - ref["d_h"]) > tol_h).any()
+        assert not (np.abs(H.to_f64(dW) - ref["dW"]) > tol_w).any()
+        outs.append((d_h, dW))
+    # and the second call's results equal those of the same call on a fresh workspace
+    fresh = _run(h, Wt, wl, mask, a_tok, old_logp, 1.0 / N)
+    assert torch.equal(outs[1][0], fresh[0]) and torch.equal(outs[1][1], fresh[1])
