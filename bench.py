@@ -679,8 +679,8 @@ def measure_lmhead_e2e(args, wl, device, stream, dev_in, train_call, acc, ref_re
         host_res.copy_(acc[64:128], non_blocking=True)
         stream.synchronize()
 
-    for k in range(2):
-        e2e_step(k, 2)
+    for k in range(3):  # warm-up steps, as for the device-timed region
+        e2e_step(k, 3)
     torch.cuda.synchronize(device)
     t0 = time.perf_counter()
     for k in range(e2e_steps):
@@ -1045,7 +1045,8 @@ def run_e2e(batch, device, stream, steps: int, ref_results=None):
             host_res.copy_(batch.accs, non_blocking=True)
         stream.synchronize()
 
-    one_step()
+    for _ in range(3):  # warm-up steps, as for the device-timed region
+        one_step()
     link_before = _h2d_copy_gbs(host_logits, staging, copy)
     step_s = []
     t0 = time.perf_counter()
