@@ -563,3 +563,77 @@ def test_lmhead_live_tokens_reuse_a_dirty_workspace():
     # and the second call's results equal those of the same call on a fresh workspace
     fresh = _run(h, Wt, wl, mask, a_tok, old_logp, 1.0 / N)
     assert torch.equal(outs[1][0], fresh[0]) and torch.equal(outs[1][1], fresh[1])
+
+
+@pytest.mark.parametrize("with_terms", [False, True], ids=["plain", "kl_entropy_weights"])
+def test_lmhead_full_size_bench_configuration(with_terms):
+    # the bench's LM-head step at full size (16384 tokens, H = 2048, V = 151936): the group
+    # advantages of the workload's rewards (one of its two groups has equal rewards, so half
+    # the tokens have no gradient), plain or with KL k3, the entropy bonus and per-token
+    # weights. Sampled rows (dead and live ones, tile edges) against the oracle row by row;
+    # every d_h row of a token without a gradient exactly zero (plain); dW by the property that
+    # every dlogits row sums to zero, so the vocabulary sum of dW vanishes
+    wl = W.make_workload("lmhead", seed=0)
+    T, V, Hd = wl.T, wl.V, wl.extra["H"]
+    h, Wt = W.make_lmhead_inputs(wl, DEV)
+    adv = OA.broadcast_to_tokens(OA.group_advantage(wl.rewards, wl.group_size, np.float32(1e-6)),
+                                 wl.row_rollout, wl.row_len).astype(np.float32)
+    dead = np.flatnonzero(adv == 0)
+    assert 0 < len(dead) < T
+    N = int(wl.mask.sum())
+    gs = np.float32(1.0 / N)
+    rng = np.random.default_rng(14)
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    d_h = torch.full((T, Hd), 7.0, device=DEV)
+    dW = torch.full((V, Hd), 7.0, device=DEV)
+    loss = torch.full((T,), -7.0, device=DEV)
+    logp = torch.full((T,), -7.0, device=DEV)
+    acc = _lib.new_step_acc(DEV)
+    ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=DEV)
+    terms = oterms = None
+    w_tok = None
+    ref_lp = None
+    if with_terms:
+        ref_lp = (-12.0 + rng.normal(0, 0.3, T)).astype(np.float32)
+        w_tok = rng.choice([1.0, 0.5, 0.25], T).astype(np.float32)
+        ent_t = torch.full((T,), -7.0, device=DEV)
+        terms = dict(kl_kind=_lib.KL_K3, kl_coef=0.05, ref_logp=t(ref_lp), ent_coef=0.01, entropy_tok=ent_t,
+                     w_tok=t(w_tok))
+    _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, t(wl.target), None, t(adv), t(wl.mask), wl.eps, float(gs), d_h, dW,
+                                  loss, logp, acc, ws, terms=terms)
+    res = _lib.grpo_finish_step(acc, loss, expected_N=N)
+    assert res["status"] == 0 and res["n_valid"] == N and res["kernel_flags"] == 0
+    rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, 16383], rng.choice(dead, 3, replace=False),
+                                     rng.choice(np.setdiff1d(np.arange(T), dead), 3, replace=False)]))
+    hb = h[torch.from_numpy(rows).to(DEV)].view(torch.int16).cpu().numpy().view(np.uint16)
+    wb = Wt.view(torch.int16).cpu().numpy().view(np.uint16)
+    scale = (gs * w_tok[rows]).astype(np.float64) if with_terms else float(gs)
+    if with_terms:
+        oterms = dict(kl_kind=_lib.KL_K3, kl_coef=float(np.float32(0.05)), ref=ref_lp[rows].astype(np.float64),
+                      ent_coef=float(np.float32(0.01)))
+    ref = OL.lmhead_fwd_bwd(hb, wb, wl.target[rows], None, adv[rows], wl.mask[rows], wl.eps, scale=scale,
+                            want_dw=False, terms=oterms)
+    m = wl.mask[rows].astype(bool)
+    gl, gp = H.to_f64(loss)[rows], H.to_f64(logp)[rows]
+    assert np.all(np.abs(gp[m] - ref["logp_tok"][m]) <= 1e-5 * np.maximum(1, np.abs(ref["logp_tok"][m])))
+    assert np.all(np.abs(gl - ref["loss_tok"]) <= 1e-5 * np.abs(ref["loss_tok"]) + 1e-6)
+    if with_terms:
+        ge = H.to_f64(ent_t)[rows]
+        assert np.all(np.abs(ge[m] - ref["entropy"][m]) <= 1e-5 * np.maximum(1, ref["entropy"][m]))
+    wf = OL.as_f64(wb)
+    z = OL.as_f64(hb) @ wf.T
+    awf = np.abs(wf)
+    for k, tok in enumerate(rows):
+        tt = None if not with_terms else dict(oterms, ref=float(ref_lp[tok]))
+        sk = scale[k] if with_terms else scale
+        dz = np.abs(OL.token_objective(z[k], int(wl.target[tok]), None, adv[tok], int(wl.mask[tok]), wl.eps, sk,
+                                       terms=tt)[4])
+        tol = 8e-3 * (dz @ awf) + 1e-12
+        got = d_h[int(tok)].double().cpu().numpy()
+        assert np.all(np.abs(got - ref["d_h"][k]) <= tol), int(tok)
+    if not with_terms:
+        assert torch.equal(d_h[torch.from_numpy(dead).to(DEV)], torch.zeros((len(dead), Hd), device=DEV))
+    col = dW.double().sum(0)
+    mag = dW.double().abs().sum(0)
+    assert torch.all(col.abs() <= 2e-2 * mag + 1e-9)
+    assert torch.isfinite(dW).all() and torch.isfinite(d_h).all()
