@@ -637,3 +637,79 @@ def test_lmhead_full_size_bench_configuration(with_terms):
     mag = dW.double().abs().sum(0)
     assert torch.all(col.abs() <= 2e-2 * mag + 1e-9)
     assert torch.isfinite(dW).all() and torch.isfinite(d_h).all()
+
+
+def _random_case(k):
+    """A seeded random LM-head case: sizes, dead fraction, clip stress, regularisers."""
+    rng = np.random.default_rng(1000 + k)
+    T = int(rng.integers(1, 700))
+    V = int(rng.integers(1, 5000))
+    Hd = int(rng.choice([64, 128, 192, 256]))
+    dead_frac = float(rng.choice([0.0, 0.3, 0.7, 1.0]))
+    # by k: no regulariser (the dead tokens skip the backward), KL k1, KL k3 with the entropy
+    # bonus, no regulariser with weights
+    kl = (0, _lib.KL_K1, _lib.KL_K3, 0)[k % 4]
+    ent = 0.03 if k % 4 == 2 else 0.0
+    weighted = k % 4 == 3 or bool(rng.integers(0, 2))
+    return rng, T, V, Hd, dead_frac, kl, ent, weighted
+
+
+@pytest.mark.parametrize("k", range(12))
+def test_lmhead_random_cases(cta_group, k):
+    # seeded random sizes (ragged tokens, vocabulary and K), a random share of tokens without a
+    # gradient (zero advantage), masked tokens, random regularisers and weights, and half the
+    # cases accumulating into a dW that already holds values; every output against the oracle
+    rng, T, V, Hd, dead_frac, kl, ent, weighted = _random_case(k)
+    adv = rng.choice([-1.5, -0.4, 0.6, 2.0], T).astype(np.float32)
+    adv[rng.random(T) < dead_frac] = 0.0
+    wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed=2000 + k, valid_lo=0.15, adv=adv)
+    N = max(int(mask.sum()), 1)
+    gs = np.float32(1.0 / N)
+    ref_lp = (old_logp + rng.normal(0, 0.3, T)).astype(np.float32)
+    w_tok = rng.choice([1.0, 0.5, 0.125], T).astype(np.float32) if weighted else None
+    accumulate = bool(k % 2)
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    d_h = torch.full((T, Hd), 7.0, device=DEV)
+    dW0 = torch.randn((V, Hd), device=DEV) if accumulate else torch.full((V, Hd), 7.0, device=DEV)
+    dW = dW0.clone()
+    loss = torch.full((T,), -7.0, device=DEV)
+    logp = torch.full((T,), -7.0, device=DEV)
+    ent_t = torch.full((T,), -7.0, device=DEV)
+    acc = _lib.new_step_acc(DEV)
+    ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=DEV)
+    terms = dict(kl_kind=kl, kl_coef=0.1, ref_logp=t(ref_lp) if kl else None, ent_coef=ent, entropy_tok=ent_t,
+                 w_tok=t(w_tok))
+    _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, t(wl.target), t(old_logp), t(a_tok), t(mask), wl.eps, float(gs), d_h, dW,
+                                  loss, logp, acc, ws, dw_accumulate=accumulate, terms=terms)
+    torch.cuda.synchronize()
+    scale = (gs * w_tok).astype(np.float64) if weighted else float(gs)
+    oterms = dict(kl_kind=kl, kl_coef=float(np.float32(0.1)), ref=ref_lp.astype(np.float64),
+                  ent_coef=float(np.float32(ent)))
+    ref = OL.lmhead_fwd_bwd(hb, wb, wl.target, old_logp, a_tok, mask, wl.eps, scale=scale, terms=oterms)
+    m = mask.astype(bool)
+    gl, gp, ge = H.to_f64(loss), H.to_f64(logp), H.to_f64(ent_t)
+    assert np.all(np.abs(gp[m] - ref["logp_tok"][m]) <= 1e-5 * np.maximum(1, np.abs(ref["logp_tok"][m])))
+    assert np.all(np.abs(ge[m] - ref["entropy"][m]) <= 1e-5 * np.maximum(1, ref["entropy"][m]))
+    assert np.all(gl[~m] == 0) and np.all(gp[~m] == 0) and np.all(ge[~m] == 0)
+    assert np.all(np.abs(gl - ref["loss_tok"]) <= 1e-5 * np.abs(ref["loss_tok"]) + 1e-6)
+    res = _lib.grpo_finish_step(acc, loss, expected_N=int(mask.sum()))
+    assert res["status"] == 0 and res["kernel_flags"] == 0
+    hf, wf = OL.as_f64(hb), OL.as_f64(wb)
+    z = hf @ wf.T
+    dz_abs = np.zeros_like(z)
+    for i in range(T):
+        if mask[i]:
+            sk = scale[i] if weighted else scale
+            dz_abs[i] = np.abs(OL.token_objective(z[i], int(wl.target[i]), old_logp[i], a_tok[i], 1, wl.eps, sk,
+                                                  terms=dict(oterms, ref=float(ref_lp[i])))[4])
+    gh = H.to_f64(d_h)
+    bad = np.abs(gh - ref["d_h"]) > 8e-3 * (dz_abs @ np.abs(wf)) + 1e-12
+    assert not bad.any(), (np.argwhere(bad)[:3], gh[bad][:3], ref["d_h"][bad][:3])
+    want_w = ref["dW"] + (H.to_f64(dW0) if accumulate else 0.0)
+    gw = H.to_f64(dW)
+    tol_w = 8e-3 * (dz_abs.T @ np.abs(hf)) + 1e-12 + (2.0 ** -23) * np.abs(want_w)
+    bad = np.abs(gw - want_w) > tol_w
+    assert not bad.any(), (np.argwhere(bad)[:3], gw[bad][:3], want_w[bad][:3])
+    # tokens without a gradient: an exact zero d_h row
+    no_grad = ~np.any(dz_abs != 0, axis=1)
+    assert np.all(gh[no_grad] == 0)
