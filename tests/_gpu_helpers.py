@@ -18,6 +18,12 @@ rounding 2^-9):
   With the entropy bonus, element v also carries ent * scale * p_v (z_v - E_p z), whose float32
   difference is exact only to ~2^-23 |z|: a further 1e-5 * p_v * sum_u |dz_u| (relative to the
   element's own probability, so a wrong small element still fails).
+  The coefficient itself is a function of the float32 log-prob: c = A r g - kl_coef dk, with
+  dc/dlogp = A r g (the ratio) + kl_coef e^(ref - logp) (KL k3; 0 for k1). A log-prob within its
+  own bar (dlogp <= 1e-5 max(1, |logp|)) moves c by |dc/dlogp| dlogp, and every element of the
+  row with it: a further (that / |c|) * |ref| per row (coef_err). It matters where c is small
+  against its parts: a zero advantage with ref close to logp, or the KL term cancelling the
+  surrogate.
 Tokens whose float64 ratio lies within 1e-4 (relative) of a clip bound are ambiguous (float32
 and float64 may take the clip decision differently); their dlogits row must equal the
 oracle's row for one of the two decisions.
@@ -119,10 +125,11 @@ def row_probs(logits_host: np.ndarray) -> np.ndarray:
     return np.stack([np.exp(OL.log_softmax_row(OL.as_f64(r))) for r in logits_host])
 
 
-def dlogits_tol(ref, dtype, target=None, coef=None, probs=None, rel=None):
+def dlogits_tol(ref, dtype, target=None, coef=None, probs=None, rel=None, coef_err=None):
     """Elementwise dlogits bar (see the module docstring): `rel` (default by output dtype)
     times each element's own magnitude, the underflow floor, the target-element term when
-    `target` and `coef` are given, and the entropy term when `probs` (row softmax) is given."""
+    `target` and `coef` are given, the entropy term when `probs` (row softmax) is given, and
+    the coefficient's propagated error when `coef_err` (per row, absolute) and `coef` are."""
     r = DLOGIT_REL[dtype] if rel is None else rel
     tol = r * np.abs(ref) + UNDERFLOW_FLOOR
     if target is not None and coef is not None:
@@ -130,7 +137,21 @@ def dlogits_tol(ref, dtype, target=None, coef=None, probs=None, rel=None):
         tol[rows, target] += TARGET_COEF_TOL * np.abs(coef)
     if probs is not None:
         tol += ENTROPY_MASS_TOL * probs * np.sum(np.abs(ref), axis=1, keepdims=True)
+    if coef_err is not None and coef is not None:
+        c = np.abs(np.asarray(coef, dtype=np.float64))
+        rel_row = np.where(c > 0, np.asarray(coef_err, dtype=np.float64) / np.where(c > 0, c, 1.0), 0.0)
+        tol += rel_row[:, None] * np.abs(ref)
     return tol
+
+
+def coef_logp_err(adv, ratio, clipped, mask, logp, scale, kl_kind=0, kl_coef=0.0, ref_logp=None):
+    """Per token: |dc/dlogp| times the log-prob bar, times the grad scale (see the module
+    docstring): the coefficient error a float32 log-prob within its own bar explains."""
+    lp = np.asarray(logp, dtype=np.float64)
+    d = (np.abs(np.asarray(adv, dtype=np.float64) * ratio) * (~np.asarray(clipped, bool))).astype(np.float64)
+    if kl_kind == 2:
+        d = d + kl_coef * np.exp(np.asarray(ref_logp, dtype=np.float64) - lp)
+    return np.where(np.asarray(mask) != 0, d * 1e-5 * np.maximum(1.0, np.abs(lp)) * np.abs(scale), 0.0)
 
 
 def _bad(got, ref, dtype, target, coef):
