@@ -837,6 +837,11 @@ def run_gb300(args):
             del bx
         torch.cuda.empty_cache()
         extra["lmhead"] = measure_lmhead(args, device, rank, local, with_e2e=False, with_cpu=False)
+        # the same step with the KL term to a reference policy: every token has a gradient, so
+        # the backward runs over all of them (the dense case beside the plain step's live ones)
+        torch.cuda.empty_cache()
+        extra["lmhead_kl3"] = measure_lmhead(argparse.Namespace(**dict(vars(args), kl="k3", kl_coef=0.05)), device,
+                                             rank, local, with_e2e=False, with_cpu=False)
         line["workloads"] = extra
         line["gpu_launches"] += sum(e["gpu_launches"] for e in extra.values())
     if rank == 0:
