@@ -9,13 +9,16 @@
 //             target logit.
 //  reduce     per token: combine the partials in a fixed order -> LSE, log-prob, ratio,
 //             clipped surrogate, gradient coefficient (the row pass's token epilogue).
+//  partition  the live tokens (a dlogits row that is not all zero) first, in token order; their
+//             hidden states gathered into a compact buffer; the others' d_h rows zeroed. The
+//             live count stays on the device and sets the backward GEMMs' extents.
 //  backward   per vocabulary chunk c (at most 66 tiles, 16896 columns): the same GEMM recomputes
-//             the chunk's logits and its epilogue writes the chunk's bf16 dlogits dz_c into a
-//             bounded [T, chunk] buffer (two buffers, used in turn); then d_h (+)= dz_c W_c and
-//             dW_c = dz_c^T h, both on the same tcgen05 kernel with float32 outputs, on a second
-//             stream so that the next chunk's recompute runs beside them. d_h is accumulated
-//             over the chunks in chunk order (a fixed order: the result does not depend on how
-//             the tokens are split into calls).
+//             the chunk's logits of the live tokens and its epilogue writes their bf16 dlogits
+//             dz_c into a bounded [T, chunk] buffer (two buffers, used in turn); then d_h (+)=
+//             dz_c W_c and dW_c = dz_c^T h_live, both on the same tcgen05 kernel with float32
+//             outputs, on a second stream so that the next chunk's recompute runs beside them.
+//             d_h is accumulated over the chunks in chunk order (a fixed order: the result does
+//             not depend on how the tokens are split into calls).
 //
 // All four contractions run on grpo::lmhead::gemm_kernel (grpo_lmhead_gemm.cuh): 2-CTA
 // clusters with paired tcgen05.mma (cta_group::2, 256 x 256 tiles), plain TMA tile loads.
