@@ -41,7 +41,10 @@ class RowCase:
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
         lse = np.log(V) + 4.5  # about the LSE of N(0, 3) logits
         self.target, self.mask = t(wl.target), t(wl.mask)
-        self.adv = t(rng.normal(0.0, 1.0, T).astype(np.float32))
+        a = rng.normal(0.0, 1.0, T).astype(np.float32)
+        if k % 2:  # a third of the tokens without a gradient: the backward's live-token partition
+            a[: T // 3] = 0.0
+        self.adv = t(a)
         self.old = t((-lse + rng.normal(0.0, 1.0, T)).astype(np.float32))
         self.grad = grad
         self.terms = terms
@@ -107,7 +110,10 @@ class LmCase:
         rng = np.random.default_rng(950 + k)
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
         self.target, self.mask = t(wl.target), t(wl.mask)
-        self.adv = t(rng.normal(0.0, 1.0, T).astype(np.float32))
+        a = rng.normal(0.0, 1.0, T).astype(np.float32)
+        if k % 2:  # a third of the tokens without a gradient: the backward's live-token partition
+            a[: T // 3] = 0.0
+        self.adv = t(a)
         self.T, self.V, self.H = T, V, H
         self.ws_bytes = _lib.grpo_lmhead_workspace_size(T, V, H)
 
