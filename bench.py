@@ -835,6 +835,16 @@ def run_gb300(args):
             tmx = time_rowpass(args, bx, device, stream, world, local, f"clocks_{name}_rank{rank}.csv")
             extra[name] = rowpass_entry(args, wx, bx, tmx, world, device, name)
             del bx
+        # the headline step with the regularisers: KL k3 to a reference policy and the entropy
+        # bonus (the entropy written per token)
+        torch.cuda.empty_cache()
+        wx = W.make_workload("qwen_step", seed=rank)
+        bx = Batch(wx, device, kl_kind=_lib.KL_K3, kl_coef=0.05, ent_coef=0.01)
+        tmx = time_rowpass(args, bx, device, stream, world, local, f"clocks_terms_rank{rank}.csv")
+        extra["qwen_step_kl3_entropy"] = rowpass_entry(args, wx, bx, tmx, world, device, "qwen_step", None,
+                                                       "KL k3 coef 0.05, entropy bonus coef 0.01 (entropy "
+                                                       "written per token)")
+        del bx
         torch.cuda.empty_cache()
         extra["lmhead"] = measure_lmhead(args, device, rank, local, with_e2e=False, with_cpu=False)
         # the same step with the KL term to a reference policy: every token has a gradient, so
