@@ -449,17 +449,20 @@ def grpo_lmhead_workspace_size(T: int, V: int, H: int) -> int:
 
 
 LMHEAD_DW_ACCUMULATE = 1
+LMHEAD_SKIP_MASKED = 2
 
 
 def grpo_lmhead_loss_fwd_bwd(h, W, target, old_logp, adv_tok, mask, clip_eps: float, grad_scale: float,
                              d_h, dW, loss_tok, logp_tok, acc, workspace, stream=None,
-                             dw_accumulate: bool = False, terms: Optional[dict] = None) -> None:
+                             dw_accumulate: bool = False, terms: Optional[dict] = None,
+                             skip_masked: bool = False) -> None:
     """h [T, H] and W [V, H] bf16 device tensors; d_h / dW float32 or None; dw_accumulate adds
-    this call's dW to the buffer instead of overwriting it; ``terms`` (as for
-    grpo_logprob_loss_fwd_bwd) selects grpo_lmhead_loss_fwd_bwd_ex; see grpo.h."""
+    this call's dW to the buffer instead of overwriting it; skip_masked runs the forward GEMM
+    over the mask=1 tokens only; ``terms`` (as for grpo_logprob_loss_fwd_bwd) selects
+    grpo_lmhead_loss_fwd_bwd_ex; see grpo.h."""
     T, H = h.shape
     V = W.shape[0]
-    flags = LMHEAD_DW_ACCUMULATE if dw_accumulate else 0
+    flags = (LMHEAD_DW_ACCUMULATE if dw_accumulate else 0) | (LMHEAD_SKIP_MASKED if skip_masked else 0)
     if terms is not None:
         tm = grpo_loss_terms(int(terms.get("kl_kind", 0)), float(terms.get("kl_coef", 0.0)),
                              _ptr(terms.get("ref_logp")), float(terms.get("ent_coef", 0.0)),

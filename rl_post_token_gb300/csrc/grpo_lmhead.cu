@@ -51,6 +51,9 @@ struct ReduceArgs {
   float *lse2_out, *coef_out, *ea_out, *eb_out;  // ea, eb: entropy instance only
   float *loss_tok, *logp_tok;
   grpo_step_acc* acc;
+  // when pass A skipped the masked tokens: the compact order (valid tokens first) and the
+  // valid count; NULL otherwise
+  const int32_t *idx, *live_n;
 };
 
 // Per token: combine the vocabulary-tile partials, then the token epilogue. A block takes 32
@@ -67,13 +70,16 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(ReduceArgs a)
   __shared__ unsigned long long sc[4];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   if (threadIdx.x < 4) sc[threadIdx.x] = 0;
-  const int64_t T = a.T, row = (int64_t)blockIdx.x * 32 + lane;
-  const bool live = row < T && a.mask[row] != 0;
+  // i: this lane's row of the partials (a token, or a row of the compact order when pass A
+  // skipped the masked tokens); tok: the token whose inputs and outputs it holds
+  const int64_t T = a.T, i = (int64_t)blockIdx.x * 32 + lane;
+  const int64_t tok = (a.idx && i < T) ? (int64_t)a.idx[i] : i;
+  const bool live = i < T && (a.idx ? i < (int64_t)*a.live_n : a.mask[i] != 0);
   MS3 t{-INFINITY, 0.f, 0.f};
   if (live) {
 #pragma unroll 4
     for (int c = w; c < a.n_col_tiles; c += kReduceWarps) {
-      const int64_t k = (int64_t)c * T + row;
+      const int64_t k = (int64_t)c * T + i;
       if (ENT) {
         t = ms3_combine2(t, MS3{a.part_m[k], a.part_s[k], a.part_s2[k]});
       } else {
@@ -87,7 +93,7 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(ReduceArgs a)
   if (ENT) ws2[w][lane] = t.s2;
   __syncthreads();
   unsigned long long v_valid = 0, v_clip = 0, v_nf = 0, v_tok = 0;
-  if (w == 0 && row < T) {
+  if (w == 0 && i < T) {
     v_tok = 1;
     float coef = 0.f, l2 = 0.f, ea = 0.f, eb = 0.f, H = 0.f;
     if (live) {
@@ -104,19 +110,19 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(ReduceArgs a)
       const float l2s = log2f(tot.s);
       l2 = tot.m + l2s;
       const float ez = ENT ? tot.s2 / tot.s : 0.f;  // sum_v p_v z_v
-      const int32_t y = a.target[row];
-      const float z = (y >= 0 && (int64_t)y < a.V) ? a.zy[row] : __int_as_float(0x7fc00000);
-      const float scl = (TERMS && a.w_tok) ? a.scale * a.w_tok[row] : a.scale;
+      const int32_t y = a.target[tok];
+      const float z = (y >= 0 && (int64_t)y < a.V) ? a.zy[tok] : __int_as_float(0x7fc00000);
+      const float scl = (TERMS && a.w_tok) ? a.scale * a.w_tok[tok] : a.scale;
       // log2 p_y = (z_y log2e - m) - log2(sum), without cancellation
       TokenOut o = token_epilogue((fmaf(z, kLog2e, -tot.m) - l2s) * kLn2, fabsf(l2) <= kLseMax * kLog2e,
-                                  a.old_logp != nullptr, a.old_logp ? a.old_logp[row] : 0.f, a.adv[row], a.eps,
+                                  a.old_logp != nullptr, a.old_logp ? a.old_logp[tok] : 0.f, a.adv[tok], a.eps,
                                   scl);
       H = ENT ? l2 * kLn2 - ez : 0.f;
       if (TERMS)
-        apply_terms(o, scl, a.kl_kind, a.kl_coef, a.kl_kind != GRPO_KL_NONE ? a.ref_logp[row] : 0.f, a.ent_coef,
+        apply_terms(o, scl, a.kl_kind, a.kl_coef, a.kl_kind != GRPO_KL_NONE ? a.ref_logp[tok] : 0.f, a.ent_coef,
                     H);
-      a.loss_tok[row] = o.loss;
-      if (a.logp_tok) a.logp_tok[row] = o.logp;
+      a.loss_tok[tok] = o.loss;
+      if (a.logp_tok) a.logp_tok[tok] = o.logp;
       coef = o.coef;
       if (ENT) {
         eb = a.ent_coef * scl;
@@ -126,16 +132,16 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(ReduceArgs a)
       v_clip = o.clipped;
       v_nf = o.nonfinite;
     } else {
-      a.loss_tok[row] = 0.f;
-      if (a.logp_tok) a.logp_tok[row] = 0.f;
+      a.loss_tok[tok] = 0.f;
+      if (a.logp_tok) a.logp_tok[tok] = 0.f;
     }
-    a.lse2_out[row] = l2;
-    a.coef_out[row] = coef;
+    a.lse2_out[tok] = l2;
+    a.coef_out[tok] = coef;
     if (ENT) {
-      a.ea_out[row] = ea;
-      a.eb_out[row] = eb;
+      a.ea_out[tok] = ea;
+      a.eb_out[tok] = eb;
     }
-    if (TERMS && a.entropy_tok) a.entropy_tok[row] = H;
+    if (TERMS && a.entropy_tok) a.entropy_tok[tok] = H;
   }
   if (v_tok) atomicAdd(&sc[0], v_tok);
   if (v_valid) atomicAdd(&sc[1], v_valid);
@@ -155,15 +161,20 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(ReduceArgs a)
 // (masked, zero advantage, clipped, and no regulariser) contributes exact zeros to d_h and dW,
 // so the backward's three GEMMs run over the live tokens only. One block writes a stable
 // partition of the token indices, the live ones first, in token order, and the live count.
+// With `mask` non-NULL the partition is by the mask instead (the valid tokens first), for a
+// pass A that skips the masked tokens.
 constexpr int kPartThreads = 1024;
 
-__global__ void __launch_bounds__(kPartThreads) partition_kernel(int64_t T, const float* coef, const float* ea,
-                                                                 const float* eb, int32_t* idx, int32_t* live_n) {
+__global__ void __launch_bounds__(kPartThreads) partition_kernel(int64_t T, const uint8_t* mask, const float* coef,
+                                                                 const float* ea, const float* eb, int32_t* idx,
+                                                                 int32_t* live_n) {
   __shared__ int32_t warp_sum[kPartThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int64_t per = (T + kPartThreads - 1) / kPartThreads;
   const int64_t b = (int64_t)tid * per, e = b + per < T ? b + per : T;
-  auto live = [&](int64_t t) { return ea ? (ea[t] != 0.f || eb[t] != 0.f) : coef[t] != 0.f; };
+  auto live = [&](int64_t t) {
+    return mask ? mask[t] != 0 : (ea ? (ea[t] != 0.f || eb[t] != 0.f) : coef[t] != 0.f);
+  };
   int32_t c = 0;
   for (int64_t t = b; t < e; ++t) c += live(t) ? 1 : 0;
   // exclusive scan of the per-thread counts: within the warp, then over the warp totals
@@ -443,7 +454,7 @@ int check_args(const void* h, const void* W, int64_t T, int64_t V, int64_t H, co
 int forward(int cg, const void* h, const void* W, int64_t T, int64_t V, int64_t H, const int32_t* target,
             const float* old_logp, const float* adv_tok, const uint8_t* mask, float clip_eps, float grad_scale,
             float* loss_tok, float* logp_tok, const grpo_loss_terms* terms, grpo_step_acc* acc,
-            const WsLayout& ws, const Scratch& sc, cudaStream_t st) {
+            const WsLayout& ws, const Scratch& sc, cudaStream_t st, bool skip_masked = false) {
   const bool ent = wants_entropy(terms);
   GemmArgs g{};
   g.target = target;
@@ -454,8 +465,23 @@ int forward(int cg, const void* h, const void* W, int64_t T, int64_t V, int64_t 
   g.acc = acc;
   g.col_tile0 = 0;
   g.n_n = ws.n_col_tiles;
-  const int rc = ent ? logits_gemm<EPI_PARTIALS_ENT>(cg, h, W, T, V, H, g, st)
-                     : logits_gemm<EPI_PARTIALS>(cg, h, W, T, V, H, g, st);
+  const void* a_src = h;
+  if (skip_masked) {
+    // the valid tokens first (their count on the device) and their hidden states gathered:
+    // pass A and the reduce run over those rows only
+    partition_kernel<<<1, kPartThreads, 0, st>>>(T, mask, nullptr, nullptr, nullptr, sc.idx, sc.live_n);
+    GRPO_CUDA_TRY(cudaGetLastError());
+    const int64_t blocks = std::min<int64_t>((T + 7) / 8, (int64_t)sm_count() * 16);
+    gather_kernel<<<(unsigned)blocks, 256, 0, st>>>(T, (int)H, static_cast<const __nv_bfloat16*>(h), sc.idx,
+                                                    sc.live_n, sc.h_live, nullptr);
+    GRPO_CUDA_TRY(cudaGetLastError());
+    a_src = sc.h_live;
+    g.live_n = sc.live_n;
+    g.row_idx = sc.idx;
+    g.live_mode = LIVE_ROWS;
+  }
+  const int rc = ent ? logits_gemm<EPI_PARTIALS_ENT>(cg, a_src, W, T, V, H, g, st)
+                     : logits_gemm<EPI_PARTIALS>(cg, a_src, W, T, V, H, g, st);
   if (rc != GRPO_OK) return rc;
   ReduceArgs r{};
   r.T = T;
@@ -486,6 +512,10 @@ int forward(int cg, const void* h, const void* W, int64_t T, int64_t V, int64_t 
   r.loss_tok = loss_tok;
   r.logp_tok = logp_tok;
   r.acc = acc;
+  if (skip_masked) {
+    r.idx = sc.idx;
+    r.live_n = sc.live_n;
+  }
   const dim3 grid((unsigned)((T + 31) / 32)), block(kReduceWarps * 32);
   if (ent)
     reduce_kernel<true, true><<<grid, block, 0, st>>>(r);
@@ -561,7 +591,7 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd_ex(const void* h, const void* W
   }
   const int arc = check_args(h, W, T, V, H, target, adv_tok, mask, loss_tok, acc);
   if (arc != GRPO_OK || T == 0) return arc;
-  if (flags & ~(uint32_t)GRPO_LMHEAD_DW_ACCUMULATE) return GRPO_ERR_INVALID;
+  if (flags & ~(uint32_t)(GRPO_LMHEAD_DW_ACCUMULATE | GRPO_LMHEAD_SKIP_MASKED)) return GRPO_ERR_INVALID;
   if (!workspace || ((uintptr_t)workspace & 255u)) return GRPO_ERR_INVALID;
   if (((uintptr_t)d_h | (uintptr_t)dW) & 15u) return GRPO_ERR_INVALID;  // 16-byte row stores
   const WsLayout ws = ws_layout(T, V, H);
@@ -570,7 +600,7 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd_ex(const void* h, const void* W
   const Scratch sc = carve(workspace, ws, true);
   const int cg = cta_group();
   int rc = forward(cg, h, W, T, V, H, target, old_logp, adv_tok, mask, clip_eps, grad_scale, loss_tok, logp_tok,
-                   terms, acc, ws, sc, st);
+                   terms, acc, ws, sc, st, (flags & GRPO_LMHEAD_SKIP_MASKED) != 0);
   if (rc != GRPO_OK || (!d_h && !dW)) return rc;
   // the dlogits take the entropy form p (ea + eb z) when the bonus has a coefficient
   const bool ent_grad = terms && terms->ent_coef != 0.f;
@@ -586,8 +616,8 @@ extern "C" GRPO_API int grpo_lmhead_loss_fwd_bwd_ex(const void* h, const void* W
   const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
   // the live tokens in a compact order, their hidden states gathered; the dead tokens' d_h rows
   // zeroed
-  partition_kernel<<<1, kPartThreads, 0, st>>>(T, sc.coef, ent_grad ? sc.ea : nullptr, ent_grad ? sc.eb : nullptr,
-                                                sc.idx, sc.live_n);
+  partition_kernel<<<1, kPartThreads, 0, st>>>(T, nullptr, sc.coef, ent_grad ? sc.ea : nullptr,
+                                                ent_grad ? sc.eb : nullptr, sc.idx, sc.live_n);
   GRPO_CUDA_TRY(cudaGetLastError());
   {
     const int64_t blocks = std::min<int64_t>((T + 7) / 8, (int64_t)sm_count() * 16);

@@ -242,14 +242,16 @@ struct GemmArgs {
   int64_t ldc;
   int accumulate;
   grpo_step_acc* acc;
-  // The backward over the live tokens only (those whose dlogits row is not all zero), in a
-  // compact order that the partition kernel wrote earlier in stream order: *live_n of them,
-  // row i of the compact order being token row_idx[i]. live_mode says which extent follows
-  // from the device count (M and K above then give the allocated token rows, T):
+  // A compact order of the tokens that the partition kernel wrote earlier in stream order:
+  // *live_n of them, row i of the compact order being token row_idx[i]. The backward runs
+  // over the live tokens (a dlogits row that is not all zero); pass A, when asked to skip the
+  // masked tokens, over the valid ones. live_mode says which extent follows from the device
+  // count (M and K above then give the allocated token rows, T):
   //   LIVE_ROWS_PADDED  rows = live tokens, and the epilogue writes zero dlogits rows up to the
   //                     padded count (live_pad below), so that dW's reduction over the padded
   //                     count reads zeros past the live rows;
-  //   LIVE_ROWS         rows = live tokens (d_h: rows scattered to C[row_idx[i]]);
+  //   LIVE_ROWS         rows = live tokens (d_h: rows scattered to C[row_idx[i]]; pass A:
+  //                     partials at the compact row, the target logit at the token);
   //   LIVE_K            reduction length = the padded count (dW over the compact tokens).
   const int32_t* live_n;
   const int32_t* row_idx;
@@ -283,7 +285,10 @@ __device__ __forceinline__ void unit_coords(const GemmArgs& g, int n_m, int t, i
 // the target logit if the tile holds it. Zero-filled columns past the vocabulary count as -inf.
 __device__ __forceinline__ void epi_partials(const GemmArgs& g, uint32_t taddr, int64_t row, bool rok, int ct) {
   const int64_t c0 = (int64_t)ct * BN;
-  const int32_t y = rok ? g.target[row] : -1;
+  // the token of this row (the compact order's, when the masked tokens are skipped); the
+  // partials stay at the row, the target logit goes to the token
+  const int64_t tok = (rok && g.row_idx) ? (int64_t)g.row_idx[row] : row;
+  const int32_t y = rok ? g.target[tok] : -1;
   const bool own = y >= c0 && y < c0 + BN;
   MS acc{-INFINITY, 0.f};
   float zy = 0.f;
@@ -305,7 +310,7 @@ __device__ __forceinline__ void epi_partials(const GemmArgs& g, uint32_t taddr, 
   if (rok) {
     g.part_m[(int64_t)ct * g.M + row] = acc.m;
     g.part_s[(int64_t)ct * g.M + row] = acc.s;
-    if (own) g.zy[row] = zy;
+    if (own) g.zy[tok] = zy;
   }
 }
 
@@ -314,7 +319,8 @@ __device__ __forceinline__ void epi_partials(const GemmArgs& g, uint32_t taddr, 
 // both takes the no-mass guard for its -inf columns.
 __device__ __forceinline__ void epi_partials_ent(const GemmArgs& g, uint32_t taddr, int64_t row, bool rok, int ct) {
   const int64_t c0 = (int64_t)ct * BN;
-  const int32_t y = rok ? g.target[row] : -1;
+  const int64_t tok = (rok && g.row_idx) ? (int64_t)g.row_idx[row] : row;
+  const int32_t y = rok ? g.target[tok] : -1;
   const bool own = y >= c0 && y < c0 + BN;
   MS3 acc{-INFINITY, 0.f, 0.f};
   bool guarded = false;
@@ -339,7 +345,7 @@ __device__ __forceinline__ void epi_partials_ent(const GemmArgs& g, uint32_t tad
     g.part_m[(int64_t)ct * g.M + row] = acc.m;
     g.part_s[(int64_t)ct * g.M + row] = acc.s;
     g.part_s2[(int64_t)ct * g.M + row] = acc.s2;
-    if (own) g.zy[row] = zy;
+    if (own) g.zy[tok] = zy;
   }
 }
 

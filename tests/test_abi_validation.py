@@ -92,7 +92,7 @@ def _lm(T=256, V=1024, H=128, h=P, W=P, ws=P, ws_bytes=1 << 30, acc=P, target=P,
 
 @pytest.mark.parametrize("kw, code", [
     (dict(H=100), _lib.ERR_INVALID),  # H a multiple of 64
-    (dict(flags=2), _lib.ERR_INVALID),  # unknown flag bits
+    (dict(flags=4), _lib.ERR_INVALID),  # unknown flag bits
     (dict(H=32), _lib.ERR_INVALID),
     (dict(V=0), _lib.ERR_INVALID),
     (dict(T=-1), _lib.ERR_INVALID),

@@ -713,3 +713,53 @@ def test_lmhead_random_cases(cta_group, k):
     # tokens without a gradient: an exact zero d_h row
     no_grad = ~np.any(dz_abs != 0, axis=1)
     assert np.all(gh[no_grad] == 0)
+
+
+# ---- pass A over the valid tokens only (GRPO_LMHEAD_SKIP_MASKED) ------------------------------
+
+@pytest.mark.parametrize("T, V, Hd, masked, with_terms", [(300, 3000, 128, 0.6, False), (513, 20000, 192, 0.3, True),
+                                                          (256, 1024, 64, 0.0, False), (200, 2000, 64, 1.0, False),
+                                                          (1, 777, 64, 0.0, True)])
+def test_lmhead_skip_masked_gives_the_same_bits(cta_group, T, V, Hd, masked, with_terms):
+    # pass A over the mask=1 tokens only (compact order, count on the device) against the call
+    # that runs it over every token: every output the same bits, including with every token
+    # masked or none, the regularisers, and a forward-only call
+    rng = np.random.default_rng(int(T + V))
+    wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed=101 + T)
+    mask = (rng.random(T) >= masked).astype(np.uint8)
+    a_tok = a_tok.copy()
+    a_tok[: T // 4] = 0.0
+    N = max(int(mask.sum()), 1)
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    ref_lp = (old_logp + rng.normal(0, 0.3, T)).astype(np.float32)
+
+    def call(skip, grads=True):
+        o = dict(d_h=torch.full((T, Hd), 7.0, device=DEV) if grads else None,
+                 dW=torch.full((V, Hd), 7.0, device=DEV) if grads else None,
+                 loss=torch.full((T,), -7.0, device=DEV), logp=torch.full((T,), -7.0, device=DEV),
+                 ent=torch.full((T,), -7.0, device=DEV), acc=_lib.new_step_acc(DEV))
+        ws = torch.full((_lib.grpo_lmhead_workspace_size(T, V, Hd),), 0xFF, dtype=torch.uint8, device=DEV)
+        terms = dict(kl_kind=_lib.KL_K3, kl_coef=0.1, ref_logp=t(ref_lp), ent_coef=0.02, entropy_tok=o["ent"]) \
+            if with_terms else None
+        _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, t(wl.target), t(old_logp), t(a_tok), t(mask), wl.eps, 1.0 / N,
+                                      o["d_h"], o["dW"], o["loss"], o["logp"], o["acc"], ws, terms=terms,
+                                      skip_masked=skip)
+        o["res"] = _lib.grpo_finish_step(o["acc"], o["loss"], expected_N=int(mask.sum()))
+        return o
+
+    for grads in (True, False):
+        a, b = call(False, grads), call(True, grads)
+        for key in ("d_h", "dW", "loss", "logp", "ent"):
+            if a[key] is not None:
+                assert torch.equal(a[key], b[key]), key
+        assert a["res"] == b["res"]
+        assert b["res"]["status"] == 0 and b["res"]["kernel_flags"] == 0
+    # and against the oracle
+    ref = OL.lmhead_fwd_bwd(hb, wb, wl.target, old_logp, a_tok, mask, wl.eps, scale=1.0 / N,
+                            terms=dict(kl_kind=_lib.KL_K3, kl_coef=float(np.float32(0.1)),
+                                       ref=ref_lp.astype(np.float64), ent_coef=float(np.float32(0.02)))
+                            if with_terms else None)
+    m = mask.astype(bool)
+    gp = H.to_f64(b["logp"])
+    assert np.all(np.abs(gp[m] - ref["logp_tok"][m]) <= 1e-5 * np.maximum(1, np.abs(ref["logp_tok"][m])))
+    assert np.all(gp[~m] == 0) and np.all(H.to_f64(b["loss"])[~m] == 0)
