@@ -96,6 +96,7 @@ def test_plain_c_lmhead_client_matches_the_binding(grpo_lib, tmp_path):
     mask[rng.random(T) < 0.2] = 0
     adv = rng.normal(0, 1, T).astype(np.float32)
     old = rng.normal(-9, 1, T).astype(np.float32)
+    ref = (old + rng.normal(0, 0.3, T)).astype(np.float32)
     scale = np.float32(1.0 / max(int(mask.sum()), 1))
     inp, outp = os.path.join(str(tmp_path), "in.bin"), os.path.join(str(tmp_path), "out.bin")
     with open(inp, "wb") as f:
@@ -104,29 +105,39 @@ def test_plain_c_lmhead_client_matches_the_binding(grpo_lib, tmp_path):
         f.write(h.view(torch.int16).cpu().numpy().astype(np.uint16).tobytes())
         f.write(Wt.view(torch.int16).cpu().numpy().astype(np.uint16).tobytes())
         f.write(np.asarray(wl.target, np.int32).tobytes() + old.tobytes() + adv.tobytes() + mask.tobytes())
+        f.write(ref.tobytes())
     r = subprocess.run([exe, inp, outp], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
     raw = open(outp, "rb").read()
     o = 0
-    status = int(np.frombuffer(raw, np.int32, 1, o)[0]); o += 4
-    c_loss = np.frombuffer(raw, np.float32, T, o); o += 4 * T
-    c_logp = np.frombuffer(raw, np.float32, T, o); o += 4 * T
-    c_dh = np.frombuffer(raw, np.float32, T * Hd, o); o += 4 * T * Hd
-    c_dw = np.frombuffer(raw, np.float32, V * Hd, o); o += 4 * V * Hd
-    c_res_loss = float(np.frombuffer(raw, np.float64, 1, o)[0]); o += 8
-    c_n_valid, c_n_clipped = (int(x) for x in np.frombuffer(raw, np.int64, 2, o))
+    steps = []
+    for _ in range(2):  # the plain step, then the one with the regularisers and the flag
+        status = int(np.frombuffer(raw, np.int32, 1, o)[0]); o += 4
+        c_loss = np.frombuffer(raw, np.float32, T, o); o += 4 * T
+        c_logp = np.frombuffer(raw, np.float32, T, o); o += 4 * T
+        c_dh = np.frombuffer(raw, np.float32, T * Hd, o); o += 4 * T * Hd
+        c_dw = np.frombuffer(raw, np.float32, V * Hd, o); o += 4 * V * Hd
+        c_res_loss = float(np.frombuffer(raw, np.float64, 1, o)[0]); o += 8
+        c_n_valid, c_n_clipped = (int(x) for x in np.frombuffer(raw, np.int64, 2, o)); o += 16
+        steps.append((status, c_loss, c_logp, c_dh, c_dw, c_res_loss, c_n_valid, c_n_clipped))
+    c_ent = np.frombuffer(raw, np.float32, T, o)
 
     # the binding, same inputs
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
-    d_h = torch.empty((T, Hd), device=DEV)
-    dW = torch.empty((V, Hd), device=DEV)
-    loss, logp = torch.empty(T, device=DEV), torch.empty(T, device=DEV)
-    acc = _lib.new_step_acc(DEV)
-    ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=DEV)
-    _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, t(wl.target), t(old), t(adv), t(mask), wl.eps, float(scale), d_h, dW,
-                                  loss, logp, acc, ws)
-    res = _lib.grpo_finish_step(acc, loss)
-    assert status == res["status"] == 0
-    for got, want in ((c_loss, loss), (c_logp, logp), (c_dh, d_h), (c_dw, dW)):
-        assert np.array_equal(got.view(np.uint32), want.cpu().numpy().ravel().view(np.uint32))
-    assert c_res_loss == res["loss"] and c_n_valid == res["n_valid"] and c_n_clipped == res["n_clipped"]
+    ent = torch.empty(T, device=DEV)
+    for k, (status, c_loss, c_logp, c_dh, c_dw, c_res_loss, c_n_valid, c_n_clipped) in enumerate(steps):
+        d_h = torch.empty((T, Hd), device=DEV)
+        dW = torch.empty((V, Hd), device=DEV)
+        loss, logp = torch.empty(T, device=DEV), torch.empty(T, device=DEV)
+        acc = _lib.new_step_acc(DEV)
+        ws = torch.empty(_lib.grpo_lmhead_workspace_size(T, V, Hd), dtype=torch.uint8, device=DEV)
+        terms = None if k == 0 else dict(kl_kind=_lib.KL_K3, kl_coef=0.1, ref_logp=t(ref), ent_coef=0.02,
+                                         entropy_tok=ent)
+        _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, t(wl.target), t(old), t(adv), t(mask), wl.eps, float(scale), d_h, dW,
+                                      loss, logp, acc, ws, terms=terms, skip_masked=k == 1)
+        res = _lib.grpo_finish_step(acc, loss)
+        assert status == res["status"] == 0
+        for got, want in ((c_loss, loss), (c_logp, logp), (c_dh, d_h), (c_dw, dW)):
+            assert np.array_equal(got.view(np.uint32), want.cpu().numpy().ravel().view(np.uint32)), k
+        assert c_res_loss == res["loss"] and c_n_valid == res["n_valid"] and c_n_clipped == res["n_clipped"]
+    assert np.array_equal(c_ent.view(np.uint32), ent.cpu().numpy().view(np.uint32))
