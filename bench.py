@@ -218,14 +218,10 @@ def oracle_terms(lt, ref):
 
 
 def oracle_token_weights(wl, lt):
-    """Per-token gradient scales of the oracle's timed sample: 1, or 1/(valid tokens of the
-    token's row) under seq-mean-token-mean (the step's divisor is a constant factor)."""
-    from rl_post_token_gb300 import _lib
-    w = np.ones(wl.T)
-    if lt is not None and lt["agg"] == _lib.AGG_SEQ_MEAN_TOKEN_MEAN:
-        for r in range(len(wl.row_len)):
-            w[wl.tok_off[r]:wl.tok_off[r + 1]] = 1.0 / max(int(wl.row_valid[r]), 1)
-    return w
+    """Per-token gradient scales of the oracle's timed sample: the oracle's own dL/dl_t of the
+    aggregation mode (oracle.aggregate.token_scale), the workload's rows taken as one step."""
+    from oracle import aggregate as OG
+    return OG.token_scale(wl.tok_off, wl.mask, OG.TOKEN_MEAN if lt is None else lt["agg"])
 
 
 def oracle_lmhead_rate(wl, n_tokens: int, budget_s: float, lt=None):
