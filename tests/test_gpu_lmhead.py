@@ -763,3 +763,38 @@ def test_lmhead_skip_masked_gives_the_same_bits(cta_group, T, V, Hd, masked, wit
     gp = H.to_f64(b["logp"])
     assert np.all(np.abs(gp[m] - ref["logp_tok"][m]) <= 1e-5 * np.maximum(1, np.abs(ref["logp_tok"][m])))
     assert np.all(gp[~m] == 0) and np.all(H.to_f64(b["loss"])[~m] == 0)
+
+
+def test_lmhead_another_model_shape_sampled_rows():
+    # a Qwen2.5-7B-shaped head: H = 3584 (56 K blocks; d_h and dW over 14 column tiles) and
+    # V = 152064 (594 vocabulary tiles, the last one whole); 640 tokens, a quarter of them
+    # without a gradient. Sampled rows against the oracle row by row, dW by the vanishing
+    # vocabulary sum.
+    T, V, Hd = 640, 152064, 3584
+    wl = W.make_workload("lmhead", seed=12, rows=8, tokens=T, V=V, H=Hd)
+    h, Wt = W.make_lmhead_inputs(wl, DEV)
+    rng = np.random.default_rng(13)
+    adv = rng.choice([-1.0, 0.5, 1.5], T).astype(np.float32)
+    adv[rng.random(T) < 0.25] = 0.0
+    N = int(wl.mask.sum())
+    d_h, dW, loss, logp, acc = _run(h, Wt, wl, wl.mask, adv, None, 1.0 / N)
+    res = _lib.grpo_finish_step(acc, loss, expected_N=N)
+    assert res["status"] == 0 and res["kernel_flags"] == 0
+    rows = np.unique(np.concatenate([[0, 255, 256, 511, 639], rng.choice(T, 7, replace=False)]))
+    hb = h[torch.from_numpy(rows).to(DEV)].view(torch.int16).cpu().numpy().view(np.uint16)
+    wb = Wt.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = OL.lmhead_fwd_bwd(hb, wb, wl.target[rows], None, adv[rows], wl.mask[rows], wl.eps, scale=1.0 / N,
+                            want_dw=False)
+    H.assert_tokens_close(H.to_f64(loss)[rows], H.to_f64(logp)[rows], ref, adv[rows], wl.mask[rows])
+    wf = OL.as_f64(wb)
+    z = OL.as_f64(hb) @ wf.T
+    awf = np.abs(wf)
+    for k, tok in enumerate(rows):
+        dz = np.abs(OL.token_objective(z[k], int(wl.target[tok]), None, adv[tok], 1, wl.eps, 1.0 / N)[4])
+        got = d_h[int(tok)].double().cpu().numpy()
+        assert np.all(np.abs(got - ref["d_h"][k]) <= 8e-3 * (dz @ awf) + 1e-12), int(tok)
+        if adv[tok] == 0:
+            assert np.all(got == 0)
+    col = dW.double().sum(0)
+    assert torch.all(col.abs() <= 2e-2 * dW.double().abs().sum(0) + 1e-9)
+    assert torch.isfinite(dW).all() and torch.isfinite(d_h).all()
