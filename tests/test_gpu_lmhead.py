@@ -276,10 +276,12 @@ def test_lmhead_degenerate_sizes(cta_group, T, V, Hd):
     _check(T, V, Hd, seed=40 + T)
 
 
-def test_lmhead_step_captured_in_a_cuda_graph_replays_bitwise():
+@pytest.mark.parametrize("skip_masked", [False, True])
+def test_lmhead_step_captured_in_a_cuda_graph_replays_bitwise(skip_masked):
     # the LM-head step (one call with d_h and dW, then the finish) captured once into a CUDA
-    # graph: a replay gives the eager call's bits, and after new hidden states are written into
-    # the same buffer the replay gives what an eager call on them gives
+    # graph: a replay gives the eager call's bits, and after new hidden states and advantages
+    # are written into the same buffers (so the count of tokens with a gradient, read on the
+    # device, changes) the replay gives what an eager call on them gives
     T, V, Hd = 300, 5000, 128
     wl, h, Wt, hb, wb, mask, a_tok, old_logp = _case(T, V, Hd, seed=51)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
@@ -293,7 +295,7 @@ def test_lmhead_step_captured_in_a_cuda_graph_replays_bitwise():
 
     def step():
         _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, tgt, old, adv, msk, wl.eps, 1.0 / max(N, 1), d_h, dW, loss, logp,
-                                      acc, ws)
+                                      acc, ws, skip_masked=skip_masked)
         _lib.grpo_finish_step(acc, loss, expected_N=N, sync=False)
 
     def snapshot():
@@ -315,6 +317,7 @@ def test_lmhead_step_captured_in_a_cuda_graph_replays_bitwise():
         for a, b in zip(snapshot(), eager):
             assert torch.equal(a, b)
     h.copy_(torch.flip(h, dims=[0]))
+    adv.copy_(torch.where(torch.arange(T, device=DEV) % 5 < 2, torch.zeros_like(adv), adv))
     g.replay()
     replayed = snapshot()
     step()
