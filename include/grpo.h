@@ -463,10 +463,11 @@ GRPO_API size_t grpo_lmhead_workspace_size(int64_t T, int64_t V, int64_t H);
  *    chunk, the chunk's logits of the live tokens are recomputed and their bf16 dlogits written
  *    to one of the two workspace chunk buffers; then d_h (+)= dlogits W_c, accumulated over the
  *    chunks in chunk order, and dW_c = dlogits^T h. The recompute makes the step
- *    2 T V H + 6 T_live V H flops (T_live = T when every token has a gradient). d_h and dW run on a second
- *    stream of the library's (one per device, created by the first call that needs it, which
- *    should come before any stream capture), so the next chunk's recompute runs beside them;
- *    the call's work on both streams is done when `stream` reaches the call's end.
+ *    2 T V H + 6 T_live V H flops (T_live = T when every token has a gradient). d_h and dW
+ *    run on a second stream of the library's (one per device, created by the first call that
+ *    needs it, which should come before any stream capture), so the next chunk's recompute
+ *    runs beside them; the call's work on both streams is done when `stream` reaches the
+ *    call's end.
  *  - Determinism: d_h and the per-token outputs of a token do not depend on which other
  *    tokens share the call; dW sums over the call's tokens in a fixed order.
  *  h          device bf16 [T, H] row-major, 16-byte aligned; H a multiple of 64
