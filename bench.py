@@ -479,16 +479,21 @@ def run_lmhead(args):
 def measure_lmhead(args, device, rank=0, local=0, with_e2e=True, with_cpu=True):
     """Fused LM-head step: advantage, one grpo_lmhead_loss_fwd_bwd call (forward, dlogits, d_h
     and dW, no [T, V] matrix stored: the backward recomputes each vocabulary chunk's logits for
-    the tokens with a nonzero gradient), the finish. Roofline: tensor, 2*T*V*H + 4*T_live*V*H
-    algorithmic flops (the forward GEMM over every token, the two backward GEMMs over the live
-    ones; the recompute's 2*T_live*V*H is not credited) over the LM-head call's time, timed
-    with CUDA events around each call on its stream."""
+    the tokens with a nonzero gradient), the finish. Roofline: tensor, 2*N*V*H + 4*T_live*V*H
+    algorithmic flops (the forward GEMM over the N valid tokens, the two backward GEMMs over
+    the live ones; the recompute's 2*T_live*V*H is not credited) over the LM-head call's time,
+    timed with CUDA events around each call on its stream. --lm-mask-frac masks a share of the
+    tokens and --lm-skip-masked sets GRPO_LMHEAD_SKIP_MASKED."""
     import torch
     from rl_post_token_gb300 import _lib
     from rl_post_token_gb300 import workloads as W
 
     _lib.lib()
     wl = W.make_workload("lmhead", seed=rank, **({"tokens": args.lm_tokens} if args.lm_tokens else {}))
+    mask_frac = float(getattr(args, "lm_mask_frac", 0.0))
+    skip_masked = bool(getattr(args, "lm_skip_masked", False))
+    if mask_frac > 0:  # a seeded share of the tokens masked (padding), for the masked-token flag
+        wl.mask[np.random.default_rng(wl.seed + 5).random(wl.T) < mask_frac] = 0
     T, V, Hd = wl.T, wl.V, wl.extra["H"]
     h, Wt = W.make_lmhead_inputs(wl, device)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
@@ -524,7 +529,8 @@ def measure_lmhead(args, device, rank=0, local=0, with_e2e=True, with_cpu=True):
             evs[-1][0].record(stream)
         tm = terms if grads else None
         _lib.grpo_lmhead_loss_fwd_bwd(h, Wt, target, old, adv, mask, wl.eps, gs if grads else 1.0 / max(N, 1),
-                                      d_h if grads else None, dW if grads else None, loss, logp, acc, w, terms=tm)
+                                      d_h if grads else None, dW if grads else None, loss, logp, acc, w, terms=tm,
+                                      skip_masked=skip_masked)
         if evs is not None:
             evs[-1][1].record(stream)
         if grads and (w_tok is not None or divisor >= 0):
@@ -578,7 +584,7 @@ def measure_lmhead(args, device, rank=0, local=0, with_e2e=True, with_cpu=True):
         _lib.grpo_group_advantage(s["rewards"], wl.group_size, 1e-6, True, adv_r, row_rollout, row_tok_off, adv)
         tm = None if terms is None else dict(terms, ref_logp=s.get("ref"), w_tok=s.get("w_tok"))
         _lib.grpo_lmhead_loss_fwd_bwd(s["h"], s["Wt"], s["target"], s["old"], adv, s["mask"], wl.eps, gs,
-                                      d_h, dW, loss, logp, acc, ws, terms=tm)
+                                      d_h, dW, loss, logp, acc, ws, terms=tm, skip_masked=skip_masked)
         if w_tok is not None or divisor >= 0:
             _lib.grpo_finish_step_ex(acc, loss, w_tok=s.get("w_tok"), divisor=divisor, expected_N=N, sync=False)
         else:
@@ -592,23 +598,27 @@ def measure_lmhead(args, device, rank=0, local=0, with_e2e=True, with_cpu=True):
         t_live = N
     else:
         t_live = int(((adv != 0) & (mask != 0)).sum().item()) - int(res["n_clipped"])
-    # credited: the forward over every token and the two backward products over the live ones
-    # (a dead token's products are exact zeros); executed adds the live tokens' recompute
-    flops = (2.0 * T + 4.0 * t_live) * V * Hd
-    executed = (2.0 * T + 6.0 * t_live) * V * Hd
+    # credited: the forward over the valid tokens (every token in the bench's workload) and the
+    # two backward products over the live ones (a dead token's products are exact zeros);
+    # executed: the forward over every token (or the valid ones with the masked-token flag)
+    # plus the live tokens' recompute
+    flops = (2.0 * N + 4.0 * t_live) * V * Hd
+    executed = (2.0 * (N if skip_masked else T) + 6.0 * t_live) * V * Hd
     peak, kind = bf16_peak(sustained=True)
     line = {
         "metric": LMHEAD_METRIC,
         "value": N / full_s, "unit": UNIT, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": 1e3 * full_s, "dtype": "bf16",
-        "config": dict(lmhead_config(wl), **({"terms": lt["text"]} if lt["text"] else {})),
+        "config": dict(lmhead_config(wl), **({"terms": lt["text"]} if lt["text"] else {}),
+                       **({"masked_share": mask_frac} if mask_frac > 0 else {}),
+                       **({"skip_masked": True} if skip_masked else {})),
         "workspace_gb": ws.numel() / 1e9,
         "roofline": {"bound": "tensor", "achieved": flops / call_s / 1e12, "peak": peak, "unit": "TFLOP/s",
                      "frac": flops / call_s / 1e12 / peak, "peak_source": f"{kind} bf16_tflops_sustained",
                      "kernel": "grpo_lmhead_loss_fwd_bwd (its GEMM launches and the per-token reduce), CUDA events "
                                "around each call",
                      "ms_per_call": 1e3 * call_s, "flops_per_call": flops,
-                     "flops_what": "2*T*V*H (forward, every token) + 4*T_live*V*H (d_h and dW over the "
+                     "flops_what": "2*N*V*H (forward, the valid tokens) + 4*T_live*V*H (d_h and dW over the "
                                    "tokens with a nonzero dlogits row)",
                      "live_tokens": t_live, "dense_flops_per_call": 6.0 * T * V * Hd,
                      "executed_flops_per_call": executed,
@@ -1107,6 +1117,10 @@ def main(argv=None):
                          "and fused LM-head workloads)")
     ap.add_argument("--lm-tokens", type=int, default=0,
                     help="override the fused LM-head token count (smaller cases for profiling)")
+    ap.add_argument("--lm-mask-frac", type=float, default=0.0,
+                    help="mask a seeded share of the LM-head workload's tokens (padding)")
+    ap.add_argument("--lm-skip-masked", action="store_true",
+                    help="run the LM-head forward GEMM over the mask=1 tokens only (GRPO_LMHEAD_SKIP_MASKED)")
     ap.add_argument("--rows", type=int, default=0,
                     help="override the workload's row count (smaller cases for profiling)")
     ap.add_argument("--kl", default="none", choices=["none", "k1", "k3"],
